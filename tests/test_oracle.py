@@ -1,0 +1,423 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is trusted only after it is tied to things other than itself:
+hand-worked blocks (tests/golden/), library routines that decode the same
+encodings (numpy/struct binary16, torch bfloat16), an independent bit-level
+evaluator written here from the format text, closed forms (one-hot inputs,
+linearity, all-zero quants), and reductions of the expert layer to the dense
+case.  Each check is built so that a plausible slip in the oracle (a swapped
+nibble, a wrong packing shift, a dropped min term, a transposed operand)
+fails at least one of them.
+"""
+from __future__ import annotations
+
+import math
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_gguf_dequant_gb300 import synth
+from tests import _golden
+
+Q4_K, Q8_0 = oracle.Q4_K, oracle.Q8_0
+
+
+# ------------------------------------------------------------------ binary16
+
+def test_half_decode_exhaustive_vs_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_float64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # sign of zero
+    assert math.copysign(1.0, oracle.half_to_float64(0x8000)) == -1.0
+
+
+# ------------------------------------------------------------------ Q4_K scales
+
+def test_scale_min_hand_table():
+    for sc12, scs, ms in _golden.scale_min_table():
+        for j in range(8):
+            assert oracle.q4k_scale_min(sc12, j) == (scs[j], ms[j]), (sc12.hex(), j)
+
+
+def _pack_scale_min(sc, m):
+    """Independent packer: place each 6-bit field at the bit positions the
+    packing assigns it, viewing the 12 bytes as one little-endian integer."""
+    sc = [int(v) for v in sc]
+    m = [int(v) for v in m]
+    S = 0
+    for j in range(4):
+        S |= sc[j] << (8 * j)
+        S |= m[j] << (8 * (j + 4))
+    for j in range(4, 8):
+        S |= (sc[j] & 15) << (8 * (j + 4))
+        S |= (sc[j] >> 4) << (8 * (j - 4) + 6)
+        S |= (m[j] & 15) << (8 * (j + 4) + 4)
+        S |= (m[j] >> 4) << (8 * j + 6)
+    return S.to_bytes(12, "little")
+
+
+def test_scale_min_round_trip_all_values():
+    rng = np.random.default_rng(7)
+    # every (sc, m) pair in every slot, with random other fields
+    for j in range(8):
+        for v in range(64):
+            sc = list(rng.integers(0, 64, 8))
+            m = list(rng.integers(0, 64, 8))
+            sc[j] = v
+            m[j] = 63 - v
+            b = _pack_scale_min(sc, m)
+            for jj in range(8):
+                assert oracle.q4k_scale_min(b, jj) == (sc[jj], m[jj])
+
+
+def test_packing_is_a_bijection():
+    # the packer must use each of the 96 bits exactly once
+    used = 0
+    for j in range(8):
+        for field in ("sc", "m"):
+            for bit in range(6):
+                sc = [0] * 8
+                m = [0] * 8
+                (sc if field == "sc" else m)[j] = 1 << bit
+                S = int.from_bytes(_pack_scale_min(sc, m), "little")
+                assert bin(S).count("1") == 1
+                assert used & S == 0
+                used |= S
+    assert used == (1 << 96) - 1
+
+
+# ------------------------------------------------------------------ blocks
+
+def test_golden_blocks():
+    n = 0
+    for fmt, name, blk, expect in _golden.blocks():
+        w = oracle.dequant_block(fmt, blk)
+        for i, v in expect.items():
+            assert w[i] == v, (name, i, w[i], v)
+        n += 1
+    assert n >= 9
+
+
+def _naive_q4k_block(blk: bytes):
+    """Bit-level evaluator written from the format text, independent of the
+    C oracle: the fp16 fields via struct, the 6-bit fields and the nibbles
+    read from the bytes viewed as little-endian integers."""
+    d = struct.unpack("<e", blk[0:2])[0]
+    dmin = struct.unpack("<e", blk[2:4])[0]
+    S = int.from_bytes(blk[4:16], "little")
+    Q = int.from_bytes(blk[16:144], "little")
+
+    def bits(v, lo, n):
+        return (v >> lo) & ((1 << n) - 1)
+
+    out = []
+    for i in range(256):
+        c, l = divmod(i, 64)
+        j = 2 * c + (1 if l >= 32 else 0)
+        q = bits(Q, 8 * (32 * c + l % 32) + (4 if l >= 32 else 0), 4)
+        if j < 4:
+            sc = bits(S, 8 * j, 6)
+            m = bits(S, 8 * (j + 4), 6)
+        else:
+            sc = bits(S, 8 * (j + 4), 4) | (bits(S, 8 * (j - 4) + 6, 2) << 4)
+            m = bits(S, 8 * (j + 4) + 4, 4) | (bits(S, 8 * j + 6, 2) << 4)
+        out.append(float(d) * sc * q - float(dmin) * m)
+    return out
+
+
+def _naive_q8_0_block(blk: bytes):
+    d = struct.unpack("<e", blk[0:2])[0]
+    return [float(d) * q for q in struct.unpack("<32b", blk[2:34])]
+
+
+def test_random_blocks_vs_naive_evaluator():
+    w4 = synth.q4k_matrix(8, 512, seed=11)
+    for r in range(8):
+        row = w4[r].tobytes()
+        for b in range(2):
+            blk = row[b * 144:(b + 1) * 144]
+            assert list(oracle.dequant_block(Q4_K, blk)) == _naive_q4k_block(blk)
+    w8 = synth.q8_0_matrix(4, 256, seed=12)
+    for r in range(4):
+        row = w8[r].tobytes()
+        for b in range(8):
+            blk = row[b * 34:(b + 1) * 34]
+            assert list(oracle.dequant_block(Q8_0, blk)) == _naive_q8_0_block(blk)
+
+
+def test_all_zero_quants_is_minus_dmin_m():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        blk = bytearray(rng.bytes(144))
+        blk[16:] = bytes(128)
+        d, dmin = struct.unpack("<ee", bytes(blk[0:4]))
+        if not (math.isfinite(d) and math.isfinite(dmin)):
+            continue
+        w = oracle.dequant_block(Q4_K, bytes(blk))
+        for j in range(8):
+            _, m = oracle.q4k_scale_min(bytes(blk[4:16]), j)
+            assert np.all(w[32 * j:32 * j + 32] == -float(dmin) * m)
+
+
+def test_single_nibble_lands_on_its_weight():
+    # d=1, dmin=0, all sc=1, m=0: w = q exactly
+    base = bytearray(144)
+    base[0:2] = b"\x00\x3c"
+    base[4:16] = bytes.fromhex("010101010000000001010101")
+    for byte in range(128):
+        for hi in (0, 1):
+            blk = bytearray(base)
+            blk[16 + byte] = 0x70 if hi else 0x07
+            w = oracle.dequant_block(Q4_K, bytes(blk))
+            c, l = divmod(byte, 32)
+            idx = 64 * c + l + 32 * hi
+            expect = np.zeros(256)
+            expect[idx] = 7.0
+            assert np.array_equal(w, expect), (byte, hi)
+
+
+def test_q8_0_d_one_gives_integers():
+    blk = b"\x00\x3c" + bytes(range(256))[:32]
+    w = oracle.dequant_block(Q8_0, blk)
+    assert list(w) == list(range(32))
+    blk = b"\x00\x3c" + bytes(range(224, 256))
+    w = oracle.dequant_block(Q8_0, blk)
+    assert list(w) == list(range(-32, 0))
+
+
+def test_dequant_rows_matches_blocks():
+    N, K = 5, 768
+    w = synth.q4k_matrix(N, K, seed=5)
+    full = oracle.dequant_rows(Q4_K, w, N, K)
+    for r in range(N):
+        for b in range(3):
+            blk = w[r, b * 144:(b + 1) * 144].tobytes()
+            assert np.array_equal(full[r, b * 256:(b + 1) * 256],
+                                  oracle.dequant_block(Q4_K, blk))
+    part = oracle.dequant_rows(Q4_K, w, N, K, row0=2, nrows=2)
+    assert np.array_equal(part, full[2:4])
+
+
+# ------------------------------------------------------------------ GEMV
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
+def test_gemv_one_hot_extracts_columns(fmt):
+    N, K = 6, 512
+    w = synth.matrix(fmt, N, K, seed=21)
+    W = oracle.dequant_rows(fmt, w, N, K)
+    for k in (0, 1, 31, 32, 63, 64, 255, 256, 300, 511):
+        x = np.zeros(K, np.float32)
+        x[k] = 1.0
+        y, c = oracle.gemv(fmt, w, N, K, x)
+        assert np.array_equal(y, W[:, k])
+        assert np.array_equal(c, np.abs(W[:, k]))
+
+
+@pytest.mark.parametrize("fmt", [Q4_K, Q8_0])
+def test_gemv_brute_force_vs_naive(fmt):
+    for N, K in ((1, 256), (3, 256), (4, 512)):
+        w = synth.matrix(fmt, N, K, seed=N * 1000 + K)
+        x = synth.activations(1, K, seed=K)[0]
+        y, c = oracle.gemv(fmt, w, N, K, x)
+        nb = K // (256 if fmt == Q4_K else 32)
+        bb = 144 if fmt == Q4_K else 34
+        dec = _naive_q4k_block if fmt == Q4_K else _naive_q8_0_block
+        for r in range(N):
+            row = w[r].tobytes()
+            wr = []
+            for b in range(nb):
+                wr += dec(row[b * bb:(b + 1) * bb])
+            prods = [wv * float(xv) for wv, xv in zip(wr, x)]
+            assert math.isclose(y[r], math.fsum(prods), rel_tol=0, abs_tol=1e-12 * sum(map(abs, prods)))
+            assert math.isclose(c[r], math.fsum(map(abs, prods)), rel_tol=1e-14)
+
+
+def test_gemv_linearity_and_batch():
+    N, K = 7, 1024
+    w = synth.q4k_matrix(N, K, seed=31)
+    X = synth.activations(3, K, seed=32)
+    Y, C = oracle.gemv(Q4_K, w, N, K, X)
+    for m in range(3):
+        y, c = oracle.gemv(Q4_K, w, N, K, X[m])
+        assert np.array_equal(Y[m], y) and np.array_equal(C[m], c)
+    a, b = 0.75, -2.0
+    xs = (a * X[0].astype(np.float64) + b * X[1].astype(np.float64)).astype(np.float32)
+    ys, _ = oracle.gemv(Q4_K, w, N, K, xs)
+    # xs was rounded to fp32, so compare against the exact product of the rounded input
+    W = oracle.dequant_rows(Q4_K, w, N, K)
+    assert np.allclose(ys, W @ xs.astype(np.float64), rtol=0, atol=1e-12 * np.abs(W) @ np.abs(xs))
+    assert np.allclose(a * Y[0] + b * Y[1], W @ (a * X[0].astype(np.float64) + b * X[1]),
+                       rtol=0, atol=1e-11 * (np.abs(W) @ np.abs(X[0]) + np.abs(W) @ np.abs(X[1])))
+
+
+def test_gemv_rows_subset_and_threads():
+    N, K = 64, 512
+    w = synth.q8_0_matrix(N, K, seed=41)
+    x = synth.activations(2, K, seed=42)
+    Y, C = oracle.gemv(Q8_0, w, N, K, x, nthreads=1)
+    Y4, C4 = oracle.gemv(Q8_0, w, N, K, x, nthreads=4)
+    assert np.array_equal(Y, Y4) and np.array_equal(C, C4)
+    rows = [63, 0, 17, 17]
+    Ys, Cs = oracle.gemv(Q8_0, w, N, K, x, rows=rows)
+    assert np.array_equal(Ys, Y[:, rows]) and np.array_equal(Cs, C[:, rows])
+
+
+def test_gemv_zero_x_is_exactly_zero():
+    N, K = 3, 256
+    w = synth.q4k_matrix(N, K, seed=1)
+    y, c = oracle.gemv(Q4_K, w, N, K, np.zeros(K, np.float32))
+    assert np.all(y == 0) and np.all(c == 0)
+
+
+def test_bad_arguments_are_rejected():
+    w = synth.q4k_matrix(2, 256, seed=1)
+    with pytest.raises(ValueError):
+        oracle.row_bytes(Q4_K, 100)
+    with pytest.raises(ValueError):
+        oracle.gemv(Q4_K, w, 2, 256, np.zeros(256, np.float32), rows=[2])
+
+
+# ------------------------------------------------------------------ bf16
+
+def test_bf16_rounding_vs_torch():
+    import torch
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e30).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+        # exact ties: low 16 bits 0x8000, both parities of the kept part
+        (np.arange(1000, dtype=np.uint32) * 0x10000 + 0x3F808000).view(np.float32),
+        (np.arange(1000, dtype=np.uint32) * 0x10000 + 0xBF808000).view(np.float32),
+        np.array([0.0, -0.0, np.inf, -np.inf, 3.3895314e38, 1e-45], np.float32),
+    ])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_from_float(v) for v in vals], np.uint16)
+    assert np.array_equal(got, ref)
+    for b in (0x3F80, 0xC000, 0x0001, 0x7F7F):
+        assert oracle.bf16_to_float64(b) == float(
+            torch.from_numpy(np.array([b], np.uint16).view(np.int16)).view(torch.bfloat16).float().item())
+
+
+def test_gemm_bf16_identity_and_rounding():
+    import torch
+    N, K = 5, 512
+    w = synth.q4k_matrix(N, K, seed=51)
+    W = oracle.dequant_rows(Q4_K, w, N, K)
+    Wb = torch.from_numpy(W.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    # identity rows of X pick out the bf16 weights exactly
+    ks = [0, 7, 255, 256, 511]
+    X = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        X[i, k] = 0x3F80  # 1.0
+    Y, C = oracle.gemm_bf16(w, N, K, X)
+    for i, k in enumerate(ks):
+        assert np.array_equal(Y[i], Wb[:, k])
+        assert np.array_equal(C[i], np.abs(W[:, k]))
+    Xr = synth.activations_bf16(2, K, seed=52)
+    Y, _ = oracle.gemm_bf16(w, N, K, Xr)
+    xd = torch.from_numpy(Xr.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.allclose(Y, xd @ Wb.T, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ SwiGLU / experts
+
+def test_swiglu_closed_forms():
+    from scipy.special import expit
+    g = np.array([0.0, 1.0, -1.0, 30.0, -30.0, 2.5, -700.0, 700.0])
+    u = np.array([5.0, 2.0, 2.0, 1.0, 1.0, -3.0, 1.0, 1.0])
+    h = oracle.swiglu(g, u)
+    assert h[0] == 0.0
+    assert np.allclose(h, g * expit(g) * u, rtol=1e-15, atol=0)
+    assert math.isclose(h[3], 30.0, rel_tol=1e-12)
+    assert abs(h[4]) < 1e-11
+
+
+def _moe_fixture(seed=0, E=4, N_e=16, K=256, T=5, top_k=2, fmt=Q4_K):
+    w = synth.matrix(fmt, E * N_e, K, seed=seed)
+    ids, r = synth.router(T, E, top_k, seed=seed + 1)
+    X = synth.activations(T, K, seed=seed + 2)
+    return w, ids, r, X
+
+
+def test_moe_top1_unit_weight_is_dense():
+    E, N_e, K, T = 4, 16, 256, 6
+    w, ids, r, X = _moe_fixture(E=E, N_e=N_e, K=K, T=T, top_k=1)
+    Y, C = oracle.moe_gemv(Q4_K, w, E, N_e, K, ids, X, False, np.ones((T, 1)))
+    for t in range(T):
+        e = ids[t, 0]
+        y, c = oracle.gemv(Q4_K, w, E * N_e, K, X[t], rows=np.arange(e * N_e, (e + 1) * N_e))
+        assert np.array_equal(Y[t], y) and np.array_equal(C[t], c)
+
+
+def test_moe_identical_experts_ignore_ids():
+    E, N_e, K, T, top_k = 4, 16, 256, 5, 2
+    one = synth.q4k_matrix(N_e, K, seed=9)
+    w = np.concatenate([one] * E, axis=0)
+    _, _, r, X = _moe_fixture(E=E, N_e=N_e, K=K, T=T, top_k=top_k)
+    ids1 = np.array([[0, 1]] * T)
+    ids2 = np.array([[3, 2]] * T)
+    Y1, _ = oracle.moe_gemv(Q4_K, w, E, N_e, K, ids1, X, False, r)
+    Y2, _ = oracle.moe_gemv(Q4_K, w, E, N_e, K, ids2, X, False, r)
+    assert np.array_equal(Y1, Y2)
+    y, _ = oracle.gemv(Q4_K, one, N_e, K, X)
+    assert np.allclose(Y1, r.astype(np.float64).sum(axis=1, keepdims=True) * y, rtol=1e-13, atol=0)
+
+
+def test_moe_combined_equals_weighted_slots():
+    E, N_e, K, T, top_k = 8, 8, 512, 4, 3
+    w, ids, r, X = _moe_fixture(E=E, N_e=N_e, K=K, T=T, top_k=top_k, fmt=Q8_0)
+    S, SC = oracle.moe_gemv(Q8_0, w, E, N_e, K, ids, X, False)
+    Y, C = oracle.moe_gemv(Q8_0, w, E, N_e, K, ids, X, False, r)
+    ref = np.einsum("ts,tsn->tn", r.astype(np.float64), S.reshape(T, top_k, N_e))
+    assert np.allclose(Y, ref, rtol=1e-14, atol=0)
+    # per-slot inputs: X[t*top_k+s] replicated from X[t] gives the same result
+    Xs = np.repeat(X, top_k, axis=0)
+    S2, _ = oracle.moe_gemv(Q8_0, w, E, N_e, K, ids, Xs, True)
+    assert np.array_equal(S, S2)
+
+
+def test_moe_ffn_matches_composition():
+    E, D, F, T, top_k = 4, 256, 256, 3, 2
+    wg = synth.q4k_matrix(E * F, D, seed=61)
+    wu = synth.q4k_matrix(E * F, D, seed=62)
+    wd = synth.q4k_matrix(E * D, F, seed=63)
+    ids, r = synth.router(T, E, top_k, seed=64)
+    X = synth.activations(T, D, seed=65)
+    y = oracle.moe_ffn(Q4_K, wg, wu, wd, E, D, F, ids, X, r)
+    Wg = oracle.dequant_rows(Q4_K, wg, E * F, D)
+    Wu = oracle.dequant_rows(Q4_K, wu, E * F, D)
+    Wd = oracle.dequant_rows(Q4_K, wd, E * D, F)
+    ref = np.zeros((T, D))
+    for t in range(T):
+        for s in range(top_k):
+            e = ids[t, s]
+            g = Wg[e * F:(e + 1) * F] @ X[t].astype(np.float64)
+            u = Wu[e * F:(e + 1) * F] @ X[t].astype(np.float64)
+            h = g / (1 + np.exp(-g)) * u
+            ref[t] += r[t, s] * (Wd[e * D:(e + 1) * D] @ h)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+# ------------------------------------------------------------------ generator
+
+def test_generator_fields():
+    w = synth.q4k_matrix(64, 1024, seed=3)
+    blocks = w.reshape(-1, 144)
+    d = blocks[:, 0:2].copy().view("<f2").astype(np.float64)
+    dmin = blocks[:, 2:4].copy().view("<f2").astype(np.float64)
+    assert d.min() >= 9.99e-5 and d.max() <= 1.0001e-3
+    assert dmin.min() >= 9.99e-5 and dmin.max() <= 1.0001e-3
+    q8 = synth.q8_0_matrix(64, 1024, seed=3).reshape(-1, 34)
+    q = q8[:, 2:].view(np.int8)
+    assert q.min() == -127 and q.max() == 127
+    ids, r = synth.router(32, 64, 8, seed=1)
+    assert all(len(set(row)) == 8 for row in ids)
+    assert np.all(np.diff(r, axis=1) <= 0)
+    assert np.array_equal(synth.q4k_matrix(3, 256, 5), synth.q4k_matrix(3, 256, 5))
