@@ -1,0 +1,177 @@
+/*
+ * qmm.h -- fused-dequantisation GGUF quantized matmul on one NVIDIA GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no C++ or framework types.
+ *
+ * The operation (all entry points): multiply by a weight matrix held in its
+ * GGUF block encoding, decoding each block in registers at the moment its
+ * weights enter the dot product, never expanding the matrix into a
+ * full-precision buffer.  "Building a Rust Inference Engine That Matches
+ * Llama.cpp", section "What Ferrox actually is" (weights never fully
+ * decompressed; dequantisation fused into the dot product) and section
+ * "Where the wins came from" (the dequant math happens inline, paid once, in
+ * cache, instead of a separate memory-bound pass).  Activations are kept in
+ * f32 and are never quantized ("Frink Inference: the Rust alternative to
+ * llama.cpp", section "Where llama.cpp is still ahead").
+ *
+ * Weight layouts (GGUF; little-endian; the pages name these formats but do
+ * not print them):
+ *   QMM_Q4_K  super-block of 256 weights in 144 bytes:
+ *             [fp16 d][fp16 dmin][12 bytes: eight 6-bit scales + eight 6-bit
+ *             mins, llama.cpp get_scale_min_k4 packing][128 bytes of 4-bit
+ *             quants: weight 64c+l is the low nibble of qs[32c+l] (l<32, sub-
+ *             block 2c) or the high nibble of qs[32c+l-32] (sub-block 2c+1)].
+ *             w = d*sc_j*q - dmin*m_j.
+ *   QMM_Q8_0  block of 32 weights in 34 bytes: [fp16 d][32 x int8 q];
+ *             w = d*q.
+ *   A matrix of N rows and K columns is N rows back to back, each row K/256
+ *   (Q4_K) or K/32 (Q8_0) blocks.  An expert-stacked tensor is n_experts such
+ *   matrices back to back: row r of expert e is row e*N_e + r.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses on the current device; the
+ *     caller owns them and keeps them alive until the work that uses them has
+ *     finished.  Host pointers are named *_host.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous and stream-ordered; outputs are overwritten, never
+ *     accumulated into.
+ *   - One handle owns a small workspace (split-K partials and tickets) and a
+ *     device status word: calls that use the same handle must be ordered on
+ *     one stream.  Use one handle per concurrent stream.
+ *   - Arguments are checked on the host before anything is launched.  A call
+ *     that cannot do exactly what was asked does nothing and returns a
+ *     non-zero qmm_status; qmm_last_error() then holds a sentence naming what
+ *     is wrong.  The library never computes something other than what was
+ *     asked, never traps the GPU, and has no CPU fallback.
+ *   - Faults found on the device (an expert id out of range, a pipeline wait
+ *     that ran out of time) set the handle's status word; read it with
+ *     qmm_get_status() after synchronising.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* GGUF tensor-type ids of the supported encodings. */
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12 } qmm_format;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_NULL = -1,        /* a required pointer is NULL */
+    QMM_ERR_FORMAT = -2,      /* not Q4_K or Q8_0 */
+    QMM_ERR_SHAPE = -3,       /* a size is out of range or does not fill whole blocks */
+    QMM_ERR_ALIGN = -4,       /* a pointer or leading dimension is not aligned as required */
+    QMM_ERR_CUDA = -5,        /* the CUDA runtime reported an error (named in qmm_last_error) */
+    QMM_ERR_TIMEOUT = -6,     /* a device-side pipeline wait gave up (status word) */
+    QMM_ERR_UNSUPPORTED = -7, /* a valid request this version does not implement */
+    QMM_ERR_NOMEM = -8,       /* a workspace allocation failed */
+    QMM_ERR_EXPERT = -9       /* an expert id outside [0, n_experts) (status word) */
+} qmm_status;
+
+typedef struct qmm_matrix *qmm_t;
+typedef void *qmm_stream; /* cudaStream_t */
+
+/* Describe a quantized matrix of N rows x K columns at w_dev (borrowed, not
+ * copied).  Requires: fmt in {Q4_K, Q8_0}; N >= 1; K % 256 == 0 (Q4_K; for
+ * Q8_0 also K % 256 == 0 in this version, so every row starts 16-byte
+ * aligned); w_dev 16-byte aligned.  Allocates the handle's workspace and
+ * status word on the current device.  On success *out is a new handle. */
+QMM_API qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
+                      qmm_t *out);
+
+/* Free the handle and its workspace (synchronises the device first). */
+QMM_API qmm_status qmm_destroy(qmm_t h);
+
+/* Decode GEMV (one activation vector):  y[n] = sum_k w[n][k] * x[k].
+ * x: K fp32, y: N fp32, both device, 16-byte aligned.  Split-K over CTAs with
+ * a fixed-order reduction: results are bitwise repeatable. */
+QMM_API qmm_status qmm_gemv(qmm_t h, const float *x, float *y, qmm_stream stream);
+
+/* Several matrices that share one input vector in one launch (the q/k/v or
+ * gate/up projections of a layer).  All n handles have the same format and
+ * K; ys[i] receives matrix i's N_i outputs.  n <= 8.  hs and ys are host
+ * arrays of n entries; x and every ys[i] are device pointers as in qmm_gemv.
+ * The work and workspace of hs[0] are used. */
+QMM_API qmm_status qmm_gemv_group(const qmm_t *hs, int32_t n, const float *x,
+                          float *const *ys, qmm_stream stream);
+
+/* Batched decode (continuous batching): M activation rows share one read of
+ * the weights.  Y[m*ldy + n] = sum_k w[n][k] * X[m*ldx + k], 1 <= M <= 16,
+ * ldx >= K, ldy >= N, both multiples of 4. */
+QMM_API qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx,
+                            float *Y, int64_t ldy, qmm_stream stream);
+
+/* Grouped mixture-of-experts GEMV driven by router expert ids.  The handle
+ * holds n_experts stacked matrices of N_e = N / n_experts rows each.
+ * expert_ids: [T, top_k] int32 (device); the input of slot (t, s) is X[t]
+ * when x_per_slot == 0 (X is [T, K]) or X[t*top_k + s] when x_per_slot == 1
+ * (X is [T*top_k, K]).  route_w == NULL: Y is [T*top_k, N_e], Y[t*top_k+s] =
+ * W_{ids[t,s]} x.  route_w != NULL ([T, top_k] fp32): Y is [T, N_e],
+ * Y[t] = sum_s route_w[t,s] * W_{ids[t,s]} x (summed in slot order).  Each
+ * expert's rows are read once per call for all of its slots.  An id outside
+ * [0, n_experts) leaves that slot's contribution 0 and sets QMM_ERR_EXPERT in
+ * the status word.  1 <= T*top_k <= 4096, top_k <= 16. */
+QMM_API qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids,
+                        int32_t T, int32_t top_k, const float *X,
+                        int32_t x_per_slot, const float *route_w, float *Y,
+                        qmm_stream stream);
+
+/* h = silu(g) * u elementwise, silu(z) = z / (1 + exp(-z)); n fp32 values.
+ * The SwiGLU between an expert's gate/up and down projections. */
+QMM_API qmm_status qmm_swiglu(const float *g, const float *u, float *h, int64_t n,
+                      qmm_stream stream);
+
+/* A whole expert FFN: gate and up (both n_experts x d_ff x d_model), SwiGLU,
+ * down (n_experts x d_model x d_ff) and the routing-weighted sum over each
+ * token's top_k experts.  X [T, d_model] fp32, route_w [T, top_k] fp32,
+ * Y [T, d_model] fp32.  Uses hg's workspace for the [T*top_k, d_ff]
+ * intermediate.  Same limits and id checking as qmm_moe_gemv. */
+QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
+                       const int32_t *expert_ids, int32_t T, int32_t top_k,
+                       const float *X, const float *route_w, float *Y,
+                       qmm_stream stream);
+
+/* Prefill GEMM on the tensor cores (Q4_K only in this version):
+ * Y[m*N + n] = sum_k bf16(w[n][k]) * X[m*K + k], fp32 accumulation, where
+ * bf16(w) rounds the exact weight to fp32 and then to bf16 (nearest even).
+ * X: [M, K] bfloat16 bit patterns, 16-byte aligned; Y: [M, N] fp32.
+ * M >= 1. */
+QMM_API qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y,
+                    qmm_stream stream);
+
+/* Decode rows row0 .. row0+nrows-1 to fp32: out[i*K + k] = RN_fp32(w), which
+ * is the exact weight (Q8_0) or the exact weight rounded once (Q4_K; d*sc
+ * and dmin*m are exact in fp32).  For tests and inspection, not the hot
+ * path. */
+QMM_API qmm_status qmm_dequantize(qmm_t h, int64_t row0, int64_t nrows, float *out,
+                          qmm_stream stream);
+
+/* As qmm_dequantize, then rounded to bfloat16 (nearest even); out holds bit
+ * patterns.  These are exactly the weights qmm_gemm multiplies with. */
+QMM_API qmm_status qmm_dequantize_bf16(qmm_t h, int64_t row0, int64_t nrows,
+                               uint16_t *out, qmm_stream stream);
+
+/* Read and clear the handle's device status word (synchronises the handle's
+ * last stream first).  QMM_OK when no device-side fault was recorded. */
+QMM_API qmm_status qmm_get_status(qmm_t h);
+
+/* The calling thread's last refusal or error sentence ("" if none). */
+QMM_API const char *qmm_last_error(void);
+
+/* Library version as an integer (major*10000 + minor*100 + patch). */
+QMM_API int32_t qmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMM_H */

@@ -1,0 +1,86 @@
+// qmm_internal.h -- handle layout, launch plans and the internal launchers
+// that the C-ABI layer (qmm_api.cu) calls.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qmm.h"
+
+namespace qmm {
+
+constexpr int kMaxGroup = 8;
+
+// Device status-word bits (see qmm_get_status).
+constexpr unsigned kStatusTimeoutBit = 1u;
+constexpr unsigned kStatusBadExpertBit = 2u;
+
+struct Matrix {
+    int fmt = 0;
+    int64_t N = 0, K = 0, row_bytes = 0;
+    const uint8_t *w = nullptr;
+    int device = 0;
+    int sm_count = 0;
+    // workspace: split-K partials, per-row-slice tickets, status word
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+    unsigned *tickets = nullptr;
+    size_t n_tickets = 0;
+    unsigned *status = nullptr;
+    // expert-layer scratch (allocated on first qmm_moe_* call)
+    void *moe_ws = nullptr;
+    size_t moe_ws_bytes = 0;
+    cudaStream_t last_stream = nullptr;
+};
+
+// Bytes of one row for a supported format (K already validated).
+inline int64_t row_bytes_of(int fmt, int64_t K)
+{
+    return fmt == QMM_Q4_K ? (K / 256) * 144 : (K / 32) * 34;
+}
+
+// --------------------------------------------------------------- GEMV plan
+// A CTA owns a contiguous range of rows (balanced to within one row) and one
+// K-slice of `kchunks` 64-weight chunks.  Its threads form `rg` row teams of
+// `kchunks` threads; thread c of a team owns chunk c of the slice (its
+// activations stay in registers) and the team walks the rows.  Rows reach
+// shared memory in stages of `stage_rows` rows by bulk copies.
+struct GemvPlan {
+    int kchunks = 0;      // chunks (64 weights) per K-slice = team size
+    int ksplit = 1;       // number of K-slices
+    int rg = 0;           // row teams per CTA
+    int rpg = 0;          // rows per team per stage
+    int stage_rows = 0;   // rg * rpg
+    int stages = 0;       // ring depth
+    int threads = 0;      // rg * kchunks
+    int row_slices = 0;   // number of row ranges
+    int64_t slice_bytes = 0;  // bytes of one row within one K-slice
+    size_t smem = 0;
+};
+
+struct GemvArgs {
+    int fmt;
+    int nmat;                       // matrices sharing x (1 for plain GEMV)
+    const uint8_t *w[kMaxGroup];
+    float *y[kMaxGroup];
+    int64_t row_end[kMaxGroup];     // cumulative row counts
+    int64_t N;                      // total rows
+    int64_t K;
+    int64_t row_bytes;
+    const float *x;
+    float *ws;                      // [ksplit][N] partials (ksplit > 1)
+    unsigned *tickets;              // [row_slices] (ksplit > 1)
+    unsigned *status;
+};
+
+// Plan for N total rows of K columns; `force_ksplit` > 0 overrides split-K.
+GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit);
+size_t gemv_workspace_floats(const GemvPlan &p, int64_t N);
+cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
+
+// --------------------------------------------------------------- dequant
+cudaError_t launch_dequant(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,
+                           uint16_t *out_bf16, cudaStream_t s);
+
+} // namespace qmm

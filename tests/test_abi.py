@@ -1,0 +1,90 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every entry point include/qmm.h declares, and refuses bad arguments by name
+on the host before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import quantized_gguf_dequant_gb300 as q
+from quantized_gguf_dequant_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmm.h")
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qbuild.build()
+    return q.lib()
+
+
+def test_header_and_binding_agree():
+    assert sorted(q.ENTRY_POINTS) == declared_entry_points()
+
+
+def test_library_exports_every_entry_point(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", q.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (qmm_\w+)", out))
+    missing = [f for f in declared_entry_points() if f not in exported]
+    assert not missing, missing
+    for f in declared_entry_points():
+        assert hasattr(L, f)
+
+
+def test_library_is_built_for_sm_103a(L):
+    out = subprocess.run(["cuobjdump", "--list-elf", q.LIB_PATH], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+
+
+def test_version(L):
+    assert q.version() >= 100
+
+
+def _create(fmt, N, K, ptr):
+    h = ctypes.c_void_p()
+    rc = q.lib().qmm_create(fmt, N, K, ctypes.c_void_p(ptr), ctypes.byref(h))
+    return rc, q.last_error()
+
+
+def test_create_refuses_by_name(L):
+    rc, msg = _create(q.Q4_K, 16, 4096, 0)
+    assert rc == q.ERR_NULL and "weight pointer" in msg
+    rc, msg = _create(7, 16, 4096, 0x10000)
+    assert rc == q.ERR_FORMAT and "format 7" in msg
+    rc, msg = _create(q.Q4_K, 0, 4096, 0x10000)
+    assert rc == q.ERR_SHAPE and "N = 0" in msg
+    rc, msg = _create(q.Q4_K, 16, 1000, 0x10000)
+    assert rc == q.ERR_SHAPE and "K = 1000" in msg and "256" in msg
+    rc, msg = _create(q.Q8_0, 16, 96, 0x10000)
+    assert rc == q.ERR_SHAPE and "K = 96" in msg
+    rc, msg = _create(q.Q4_K, 16, 4096, 0x10008)
+    assert rc == q.ERR_ALIGN and "16-byte" in msg
+    rc = q.lib().qmm_create(q.Q4_K, 16, 4096, ctypes.c_void_p(0x10000), None)
+    assert rc == q.ERR_NULL
+
+
+def test_calls_on_null_handle_refuse(L):
+    vp = ctypes.c_void_p
+    assert L.qmm_gemv(None, vp(16), vp(16), None) == q.ERR_NULL
+    assert "handle is NULL" in q.last_error()
+    assert L.qmm_destroy(None) == q.ERR_NULL
+    assert L.qmm_dequantize(None, 0, 1, vp(16), None) == q.ERR_NULL
+    assert L.qmm_gemv_group(None, 1, vp(16), None, None) == q.ERR_NULL
+    arr = (vp * 1)(vp(0))
+    assert L.qmm_gemv_group(arr, 0, vp(16), arr, None) == q.ERR_SHAPE
+    assert L.qmm_gemv_group(arr, 9, vp(16), arr, None) == q.ERR_SHAPE

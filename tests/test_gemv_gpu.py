@@ -1,0 +1,193 @@
+"""GPU parity of the decoder and the decode GEMV against the CPU oracle,
+through the C ABI.
+
+Dequantised block values must be bit-exact (fp32 and bf16); GEMV outputs
+must satisfy |y - y_ref| <= 1e-4 * sum|w x|.  Sizes span several CTAs, ragged
+row tails, split-K, grouped launches and the full Llama-3.1-8B shapes (the
+big ones on sampled rows)."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_gguf_dequant_gb300 import synth
+from tests import _golden
+from tests._util import TOL_FP32, assert_close_to_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("quantized_gguf_dequant_gb300")
+
+FMTS = [q.Q4_K, q.Q8_0]
+
+
+def _matrix(fmt, N, K, seed):
+    w = synth.matrix(fmt, N, K, seed)
+    return w, q.Matrix(fmt, N, K, to_dev(w))
+
+
+# ------------------------------------------------------------------ dequant
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (33, 1024), (64, 4096)])
+def test_dequant_bit_exact(fmt, N, K):
+    w, m = _matrix(fmt, N, K, seed=N * 7 + K)
+    ref = oracle.dequant_rows(fmt, w, N, K)
+    got = m.dequantize().cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.astype(np.float32).view(np.uint32))
+    gb = m.dequantize_bf16().cpu().numpy().view(np.uint16)
+    refb = np.array([oracle.bf16_from_float(v) for v in ref.astype(np.float32).ravel()],
+                    np.uint16).reshape(ref.shape)
+    assert np.array_equal(gb, refb)
+    part = m.dequantize(row0=N // 2, nrows=N - N // 2).cpu().numpy()
+    assert np.array_equal(part, got[N // 2:])
+    m.close()
+
+
+def test_dequant_golden_blocks():
+    for fmt, name, blk, expect in _golden.blocks():
+        K = 256 if fmt == q.Q4_K else 256
+        reps = 1 if fmt == q.Q4_K else 8  # Q8_0 rows here hold 8 copies of the block
+        row = np.frombuffer(blk * reps, np.uint8)
+        m = q.Matrix(fmt, 1, K, to_dev(row))
+        got = m.dequantize().cpu().numpy()[0]
+        for i, v in expect.items():
+            assert got[i] == np.float32(v), (name, i, got[i], v)
+        m.close()
+
+
+# ------------------------------------------------------------------ GEMV
+
+def _check_gemv(fmt, N, K, seed, rows=None, x=None):
+    w, m = _matrix(fmt, N, K, seed)
+    if x is None:
+        x = synth.activations(1, K, seed + 1)[0]
+    y = m.gemv(to_dev(x)).cpu().numpy()
+    y_ref, c = oracle.gemv(fmt, w, N, K, x, rows=rows, nthreads=oracle.max_threads())
+    assert_close_to_oracle(y if rows is None else y[rows], y_ref, c, TOL_FP32,
+                           f"gemv fmt={fmt} N={N} K={K}")
+    assert m.status() == q.OK
+    return m, w, x, y
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 256), (33, 512), (1023, 1024), (1024, 1024),
+                                 (257, 2048), (100, 4096), (300, 3072), (5, 14336)])
+def test_gemv_small(fmt, N, K):
+    m, *_ = _check_gemv(fmt, N, K, seed=N + K)
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ksplit", [2, 4])
+def test_gemv_forced_split_k(fmt, ksplit, monkeypatch):
+    monkeypatch.setenv("QMM_SPLITK", str(ksplit))
+    for N, K in ((37, 2048), (300, 4096)):
+        m, *_ = _check_gemv(fmt, N, K, seed=ksplit * 100 + N)
+        # repeat: tickets must have been reset
+        m2, *_ = _check_gemv(fmt, N, K, seed=ksplit * 100 + N)
+        m.close()
+        m2.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("name,N,K", list(synth.LLAMA8B_SHAPES))
+def test_gemv_llama8b_shapes_sampled_rows(fmt, name, N, K):
+    rng = np.random.default_rng(N + K)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 254)]))
+    m, *_ = _check_gemv(fmt, N, K, seed=sum(map(ord, name)), rows=rows)
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_deterministic_and_power_of_two_scaling(fmt):
+    N, K = 2048, 4096
+    w, m = _matrix(fmt, N, K, seed=5)
+    x = to_dev(synth.activations(1, K, 6)[0])
+    y1 = m.gemv(x).cpu().numpy()
+    y2 = m.gemv(x).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    y4 = m.gemv(x * 4.0).cpu().numpy()
+    assert np.array_equal(y4, 4.0 * y1)
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_edge_activations(fmt):
+    N, K = 64, 1024
+    w, m = _matrix(fmt, N, K, seed=8)
+    x0 = np.zeros(K, np.float32)
+    y0 = m.gemv(to_dev(x0)).cpu().numpy()
+    assert np.all(y0 == 0)
+    rng = np.random.default_rng(9)
+    # wide dynamic range, tiny and huge magnitudes, one-hot
+    cases = [
+        (rng.standard_normal(K) * np.exp(rng.uniform(-40, 40, K))).astype(np.float32),
+        (rng.standard_normal(K) * 1e-30).astype(np.float32),
+        (rng.standard_normal(K) * 1e20).astype(np.float32),
+        np.eye(1, K, 777, dtype=np.float32)[0],
+    ]
+    for x in cases:
+        y = m.gemv(to_dev(x)).cpu().numpy()
+        y_ref, c = oracle.gemv(fmt, w, N, K, x)
+        assert_close_to_oracle(y, y_ref, c, TOL_FP32, f"edge fmt={fmt}")
+    # one-hot picks a column exactly (every product exact, one term)
+    W = oracle.dequant_rows(fmt, w, N, K)
+    y = m.gemv(to_dev(cases[-1])).cpu().numpy()
+    assert np.array_equal(y, W[:, 777].astype(np.float32))
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_leaves_neighbours_untouched(fmt):
+    N, K = 333, 1024
+    w, m = _matrix(fmt, N, K, seed=10)
+    x = synth.activations(1, K, 11)[0]
+    buf = torch.full((N + 64,), 12345.0, dtype=torch.float32, device="cuda")
+    q.gemv(m.h, to_dev(x), buf[32:32 + N])
+    out = buf.cpu().numpy()
+    assert np.all(out[:32] == 12345.0) and np.all(out[32 + N:] == 12345.0)
+    y_ref, c = oracle.gemv(fmt, w, N, K, x)
+    assert_close_to_oracle(out[32:32 + N], y_ref, c, TOL_FP32, "canary")
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_group_matches_separate(fmt):
+    K = 4096
+    shapes = [(4096, K), (1024, K), (1024, K)]
+    mats, ws = [], []
+    for i, (N, _) in enumerate(shapes):
+        w, m = _matrix(fmt, N, K, seed=40 + i)
+        mats.append(m)
+        ws.append(w)
+    x = synth.activations(1, K, 44)[0]
+    xd = to_dev(x)
+    ys = [torch.empty(N, dtype=torch.float32, device="cuda") for N, _ in shapes]
+    q.gemv_group([m.h for m in mats], xd, ys)
+    for m, w, y, (N, _) in zip(mats, ws, ys, shapes):
+        y_ref, c = oracle.gemv(fmt, w, N, K, x, nthreads=oracle.max_threads())
+        assert_close_to_oracle(y.cpu().numpy(), y_ref, c, TOL_FP32, "group")
+        ys_sep = m.gemv(xd).cpu().numpy()
+        assert np.all(np.isfinite(ys_sep))
+    for m in mats:
+        m.close()
+
+
+def test_gemv_refusals_on_device():
+    w, m = _matrix(q.Q4_K, 16, 256, seed=1)
+    x = torch.zeros(260, dtype=torch.float32, device="cuda")
+    y = torch.zeros(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(q.QmmError) as e:
+        q.gemv(m.h, x[1:], y)
+    assert e.value.status == q.ERR_ALIGN and "x is not 16-byte aligned" in e.value.message
+    w8, m8 = _matrix(q.Q8_0, 16, 512, seed=2)
+    with pytest.raises(q.QmmError) as e:
+        q.gemv_group([m.h, m8.h], x, [y, y])
+    assert e.value.status == q.ERR_SHAPE and "differs from matrix 0" in e.value.message
+    m.close()
+    m8.close()
