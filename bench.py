@@ -1,0 +1,507 @@
+"""Benchmark: fused-dequant Q4_K decode GEMV over the Llama-3.1-8B linear
+layers (32 layers x q,k,v,o,gate,up,down, batch 1), on GB300.
+
+One step = one pass over all 32 layers' seven matrices: every weight byte of
+the 3.93 GB Q4_K model is streamed once per step (the working set is 30x the
+L2, so no flush is needed between steps).  q/k/v and gate/up share an input
+and go out as grouped launches (128 launches per step, captured in a CUDA
+graph with programmatic dependent launch).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--no-extras]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from quantized_gguf_dequant_gb300 import synth  # noqa: E402
+
+METRIC = "Q4_K dequant-GEMV HBM GB/s (% of peak); Q4_K prefill GEMM TFLOP/s (% peak)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+SHAPES = synth.LLAMA8B_SHAPES
+LAYERS = synth.LLAMA8B_LAYERS
+SEED = 2026
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs")
+            bf = d.get("bf16_tflops")
+            bfs = d.get("bf16_tflops_sustained")
+            if hbm:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf or FALLBACK_BF16_TFLOPS),
+                        "bf16_tflops_sustained": float(bfs or bf or FALLBACK_BF16_TFLOPS),
+                        "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def layer_bytes(fmt):
+    """Algorithmic bytes of one layer: every weight byte once, each distinct
+    input vector once (q/k/v share one, gate/up share one), every output."""
+    w = sum(N * synth.row_bytes(fmt, K) for _, N, K in SHAPES)
+    x = 4 * (4096 + 4096 + 4096 + 14336)
+    y = 4 * sum(N for _, N, _ in SHAPES)
+    return w + x + y, w
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, pw = [], [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_median": statistics.median(pw), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def time_oracle(seconds=10.0):
+    """Oracle GEMV throughput over whole layers, generation excluded."""
+    import oracle
+    cores = os.cpu_count() or 1
+    total_t = 0.0
+    total_b = 0
+    layers = 0
+    while total_t < seconds and layers < LAYERS:
+        for j, (name, N, K) in enumerate(SHAPES):
+            w = synth.q4k_matrix(N, K, synth.layer_seed(SEED, layers, j))
+            x = synth.activations(1, K, synth.layer_seed(SEED + 1, layers, j))[0]
+            ts = time.perf_counter()
+            oracle.gemv(synth.Q4_K, w, N, K, x, nthreads=cores)
+            total_t += time.perf_counter() - ts
+            total_b += N * synth.row_bytes(synth.Q4_K, K)
+        layers += 1
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{layers} of 32 Llama-3.1-8B layers (all 7 matrices, all rows), Q4_K, "
+                      f"fp64 decode-then-dot, OpenMP over rows; {total_t:.1f} s of CPU time"}
+
+
+# ------------------------------------------------------------------ GPU model
+
+class Model:
+    """32 layers of Q4_K (or Q8_0) weights resident on the device, with inputs
+    and outputs laid out in two contiguous buffers."""
+
+    def __init__(self, fmt, layers=LAYERS, device="cuda"):
+        import torch
+        import quantized_gguf_dequant_gb300 as q
+        self.q = q
+        self.fmt = fmt
+        self.layers = []
+        x_sizes = [4096, 4096, 4096, 14336]  # inputs of qkv, o, gate/up, down
+        y_sizes = [N for _, N, _ in SHAPES]
+        self.x_per_layer = sum(x_sizes)
+        self.y_per_layer = sum(y_sizes)
+        self.x_all = torch.empty(layers * self.x_per_layer, dtype=torch.float32, device=device)
+        self.y_all = torch.empty(layers * self.y_per_layer, dtype=torch.float32, device=device)
+        xs = synth.activations(layers, self.x_per_layer, SEED + 7)
+        self.x_host = torch.from_numpy(xs.reshape(-1)).pin_memory()
+        self.x_all.copy_(self.x_host)
+        self.y_host = torch.empty(layers * self.y_per_layer, dtype=torch.float32).pin_memory()
+        for L in range(layers):
+            mats = []
+            for j, (name, N, K) in enumerate(SHAPES):
+                w = synth.matrix(fmt, N, K, synth.layer_seed(SEED, L, j))
+                mats.append(q.Matrix(fmt, N, K, torch.from_numpy(w).to(device)))
+            xo = L * self.x_per_layer
+            xv = []
+            for s in x_sizes:
+                xv.append(self.x_all[xo:xo + s])
+                xo += s
+            yo = L * self.y_per_layer
+            yv = []
+            for s in y_sizes:
+                yv.append(self.y_all[yo:yo + s])
+                yo += s
+            self.layers.append((mats, xv, yv))
+        torch.cuda.synchronize()
+
+    def step(self, grouped=True):
+        q = self.q
+        for mats, xv, yv in self.layers:
+            mq, mk, mv, mo, mg, mu, md = mats
+            if grouped:
+                q.gemv_group([mq.h, mk.h, mv.h], xv[0], yv[0:3])
+                q.gemv(mo.h, xv[1], yv[3])
+                q.gemv_group([mg.h, mu.h], xv[2], yv[4:6])
+            else:
+                q.gemv(mq.h, xv[0], yv[0])
+                q.gemv(mk.h, xv[0], yv[1])
+                q.gemv(mv.h, xv[0], yv[2])
+                q.gemv(mo.h, xv[1], yv[3])
+                q.gemv(mg.h, xv[2], yv[4])
+                q.gemv(mu.h, xv[2], yv[5])
+            q.gemv(md.h, xv[3], yv[6])
+
+    def launches(self, grouped=True):
+        return len(self.layers) * (4 if grouped else 7)
+
+    def close(self):
+        for mats, _, _ in self.layers:
+            for m in mats:
+                m.close()
+
+
+def time_graph(fn, steps, warmup, world, sampler_index=None):
+    """Capture fn into a CUDA graph, replay warmup + steps; returns (ms/step,
+    clocks summary)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the launch path outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    clocks = None
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    if sampler:
+        sampler.__enter__()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.__exit__(None, None, None)
+        clocks = sampler.summary()
+    ms = e0.elapsed_time(e1) / steps
+    ms = max_over_ranks(world, ms)
+    del g
+    return ms, clocks
+
+
+def time_eager(fn, steps, warmup, world):
+    """Direct launches (no graph); used for profiling runs."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return max_over_ranks(world, e0.elapsed_time(e1) / steps), None
+
+
+def time_e2e(model, steps, warmup, world):
+    """Same metric through the public API with host buffers: per step, copy
+    every input vector host->device (pinned), issue the layer calls, copy every
+    output back and wait for it."""
+    import torch
+    stream = torch.cuda.current_stream()
+
+    def one():
+        model.x_all.copy_(model.x_host, non_blocking=True)
+        model.step(grouped=True)
+        model.y_host.copy_(model.y_all, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(warmup):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    barrier(world)
+    ms = max_over_ranks(world, dt * 1e3 / steps)
+    return ms, model.x_host.numel() * 4, model.y_host.numel() * 4
+
+
+# ------------------------------------------------------------------ traffic
+
+def recorded_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
+    was taken on the kernel source as it is now (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel_key)
+        src = os.path.join(ROOT, rec["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != rec["source_sha"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ main arms
+
+def run_ours(args, world, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    pk = peaks()
+    nl = args.layers
+    q4 = Model(synth.Q4_K, layers=nl)
+    bytes_layer, wbytes_layer = layer_bytes(synth.Q4_K)
+    step_bytes = bytes_layer * nl
+    if args.graph:
+        ms, clocks = time_graph(lambda: q4.step(True), args.steps, args.warmup, world,
+                                sampler_index=local)
+    else:
+        ms, clocks = time_eager(lambda: q4.step(True), args.steps, args.warmup, world)
+    gbs = step_bytes / (ms * 1e-3) / 1e9 * world
+    per_gpu = step_bytes / (ms * 1e-3) / 1e9
+    launches_per_step = q4.launches(True)
+    launches = launches_per_step * args.steps
+    extras = {}
+    e2e = None
+    if args.e2e:
+        e2e_ms, h2d, d2h = time_e2e(q4, max(10, min(args.steps // 10, 300)), 3, world)
+        e2e = {"value": step_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms,
+               "how": "per step: pinned H2D of every input vector, the qmm_gemv / "
+                      "qmm_gemv_group calls through the binding (no graph), D2H of every "
+                      "output, stream sync"}
+    if args.extras:
+        ms_u, _ = time_graph(lambda: q4.step(False), max(3, args.steps // 4), args.warmup, world)
+        extras["q4k_decode_ungrouped"] = {
+            "value": step_bytes / (ms_u * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_u,
+            "launches_per_step": q4.launches(False),
+            "frac_of_peak": step_bytes / (ms_u * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    q4.close()
+    del q4
+    torch.cuda.empty_cache()
+    if args.extras:
+        q8 = Model(synth.Q8_0, layers=nl)
+        b8, _ = layer_bytes(synth.Q8_0)
+        ms8, _ = time_graph(lambda: q8.step(True), max(3, args.steps // 4), args.warmup, world)
+        extras["q8_0_decode"] = {
+            "value": b8 * nl / (ms8 * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms8,
+            "bytes_per_step": b8 * nl,
+            "frac_of_peak": b8 * nl / (ms8 * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        q8.close()
+        del q8
+        torch.cuda.empty_cache()
+
+    traffic = recorded_traffic("gemv_kernel<Q4_K>")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"Llama-3.1-8B decode GEMV, batch 1: {nl} layers x "
+                               "(q,k,v,o,gate,up,down), Q4_K weights, fp32 activations",
+                   "layers": nl,
+                   "weights_bytes_per_step": wbytes_layer * nl,
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "launches_per_step": launches_per_step,
+                   "l2": "working set 3.93 GB >> 129 MB L2: no flush between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": per_gpu / pk["hbm_gbs"], "traffic": traffic,
+                     "kernel": "gemv_kernel<Q4_K>", "peak_source": pk["source"],
+                     "note": "all launches in the timed region are this kernel; achieved = "
+                             "algorithmic bytes of the step / CUDA-event time of the step"},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "extras": extras,
+    }
+    return line
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step decodes-then-dots a
+    bounded sample (256 rows of each of the 7 matrices of one layer)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    rows = 256
+    cache = {}
+
+    def step(i):
+        L = i % 4
+        tot = 0
+        for j, (name, N, K) in enumerate(SHAPES):
+            key = (L, j)
+            if key not in cache:
+                w = synth.q4k_matrix(N, K, synth.layer_seed(SEED, L, j))
+                cache[key] = (np.ascontiguousarray(w[:rows]),
+                              synth.activations(1, K, synth.layer_seed(SEED + 1, L, j))[0])
+            w, x = cache[key]
+            oracle.gemv(synth.Q4_K, w, rows, K, x, nthreads=cores)
+            tot += rows * synth.row_bytes(synth.Q4_K, K)
+        return tot
+
+    for i in range(min(args.warmup, 4)):
+        step(i)
+    for i in range(4):
+        step(i)  # fill the input cache outside the timed region
+    t0 = time.perf_counter()
+    b = 0
+    for i in range(args.steps):
+        b += step(i)
+    dt = time.perf_counter() - t0
+    v = b / dt / 1e9
+    sample = (f"per step: 256 rows of each of the 7 matrices of one Llama-3.1-8B layer "
+              f"(Q4_K), fp64 decode-then-dot, OpenMP over rows on {cores} host threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "Llama-3.1-8B decode GEMV, batch 1, Q4_K (bounded row sample)"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers in the workload (32 = the full model; fewer only for profiling)")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="launch directly instead of replaying a CUDA graph (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        line["cpu_baseline"] = time_oracle(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -22,7 +22,8 @@ ERR_NULL, ERR_FORMAT, ERR_SHAPE, ERR_ALIGN, ERR_CUDA = -1, -2, -3, -4, -5
 ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_NOMEM, ERR_EXPERT = -6, -7, -8, -9
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libqmm.so")
+# QMM_LIBRARY may name another build of the library (e.g. an instrumented one).
+LIB_PATH = os.environ.get("QMM_LIBRARY") or os.path.join(_HERE, "libqmm.so")
 _lib = None
 
 # Every entry point of include/qmm.h.

@@ -7,17 +7,19 @@
 // full-precision buffer; the dequant math happens inline in the dot product.
 //
 // Work decomposition.  A CTA owns a contiguous range of rows (ranges are
-// balanced to within one row) and one K-slice.  Its threads form row teams;
-// thread c of a team owns the 64-weight chunk c of the slice for the whole
-// kernel: its 64 activations are loaded once, pre-scaled, and kept in
-// registers while the team walks the rows.  Rows arrive in shared memory in
-// stages (a ring of `stages` buffers, one bulk copy per contiguous run of
-// rows, completion tracked by an mbarrier transaction count).  Each thread
-// reads its chunk's bytes of a row from shared memory, decodes and
-// multiplies, and the team's partial sums meet in a shuffle tree and a
-// fixed-order sum over the team's warps.  With split-K the K-slices' partial
-// rows go to the workspace and the last CTA of a row range (atomic ticket)
-// adds them in slice order, so results are bitwise repeatable.
+// balanced to within one row) and one K-slice.  Its rows stream into a ring
+// of shared-memory stages by bulk copies (completion counted on a "full"
+// mbarrier).  Every warp consumes; warp 0 is also the producer and epilogue:
+// once every warp has released a stage (its "empty" mbarrier) it adds the
+// per-warp partial sums of the stage's rows in a fixed order, stores them and
+// refills the slot -- there is no CTA-wide barrier in the loop.  Warps form
+// row teams: thread c of a team owns the 64-weight chunk c of the K-slice for the
+// whole kernel -- its 64 activations are loaded once, pre-scaled, and kept
+// in registers -- and a team takes RPG rows of every stage.  The RPG partial
+// sums of a thread meet the team's other lanes in a shuffle reduce-scatter.
+// With split-K, K-slices write partial rows to the workspace and the last
+// CTA of a row range (atomic ticket) adds them in slice order, so results
+// are bitwise repeatable.
 //
 // Q4_K decode without integer-to-float conversions.  For a nibble q sitting
 // at bit p (p <= 20) of a 32-bit word, masking the word leaves the bit
@@ -41,9 +43,10 @@ namespace qmm {
 
 namespace {
 
-constexpr int kMaxThreads = 256;
-constexpr int kStageBytesTarget = 18432;
-constexpr int kStages = 4;
+constexpr int kMaxConsumers = 256;  // consumer threads per CTA
+constexpr int kStageBytesTarget = 36864;
+constexpr int kCtasPerSm = 1;  // leaves room for the next kernel's CTA (PDL prefetch)
+constexpr int kStages = 3;
 
 struct __align__(16) U4 {
     uint32_t a, b, c, d;
@@ -52,11 +55,6 @@ struct __align__(16) U4 {
 __device__ __forceinline__ U4 lds128(const uint8_t *p)
 {
     return *reinterpret_cast<const U4 *>(p);
-}
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
-{
-    return __ffma2_rn(a, b, c);
 }
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -77,53 +75,92 @@ __device__ __forceinline__ int64_t row_start(const GemvArgs &a, int m)
     return m == 0 ? 0 : a.row_end[m - 1];
 }
 
-// ----------------------------------------------------------------- per-thread
-// decode state (activations of the owned chunk, in registers).
+__device__ __forceinline__ void load_chunk_x(const float *xp, float (&lo)[32], float (&hi)[32])
+{
+    const float4 *xv = reinterpret_cast<const float4 *>(xp);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 a = __ldg(xv + i);
+        const float4 b = __ldg(xv + 8 + i);
+        lo[4 * i + 0] = a.x; lo[4 * i + 1] = a.y; lo[4 * i + 2] = a.z; lo[4 * i + 3] = a.w;
+        hi[4 * i + 0] = b.x; hi[4 * i + 1] = b.y; hi[4 * i + 2] = b.z; hi[4 * i + 3] = b.w;
+    }
+}
+
+// ----------------------------------------------------------------- Q4_K
+// Packed pairs of floats travel as 64-bit integers so that a pair is one
+// register pair from the load to the packed FMA (no re-pairing moves).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    return (uint64_t(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+
+__device__ __forceinline__ uint64_t ffma2_u64(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// Both nibbles of byte k of w in place, as the float pair
+// (q_lo * 2^(8k-149), q_hi * 2^(8k+4-149)): one 64-bit AND of {w, w}.
+template <int K>
+__device__ __forceinline__ uint64_t nibble_pair(uint64_t ww)
+{
+    constexpr uint64_t mask = (uint64_t(0xF0u << (8 * K)) << 32) | uint64_t(0x0Fu << (8 * K));
+    return ww & mask;
+}
 
 struct Q4State {
-    float xl[32], xh[32];  // pre-scaled activations for low / high nibbles
-    float Xl, Xh;          // plain sums of the two sub-block halves
-    float p1, p2;          // 2^E = p1 * p2
-    uint32_t selA, selB, mA, mB, mC, mD;
-    int hdr_off, qs_off;   // byte offsets of the chunk's header and quants in a row
+    uint64_t xp[32];  // (low-nibble, high-nibble) pre-scaled activations, l = 0..31
+    float2 X;         // plain sums of the two sub-block halves
+    float p1, p2;     // 2^E = p1 * p2
+    uint32_t selA, selB;
+    bool hi4;         // the chunk's sub-blocks are 4..7 (split 6-bit fields)
+    int hdr_off, qs_off;
 };
 
 __device__ __forceinline__ void q4_prologue(Q4State &st, const float *x, int64_t gchunk,
-                                            int local_chunk)
+                                            int local_chunk, bool idle)
 {
-    const int64_t blk = gchunk >> 2;
     const int c4 = int(gchunk & 3);
-    const float4 *xv = reinterpret_cast<const float4 *>(x + blk * 256 + c4 * 64);
-    float raw_l[32], raw_h[32];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float4 a = __ldg(xv + i);
-        float4 b = __ldg(xv + 8 + i);
-        raw_l[4 * i + 0] = a.x; raw_l[4 * i + 1] = a.y; raw_l[4 * i + 2] = a.z; raw_l[4 * i + 3] = a.w;
-        raw_h[4 * i + 0] = b.x; raw_h[4 * i + 1] = b.y; raw_h[4 * i + 2] = b.z; raw_h[4 * i + 3] = b.w;
-    }
+    const float4 *xv = reinterpret_cast<const float4 *>(x + (gchunk >> 2) * 256 + c4 * 64);
     uint32_t mbits = 0;
     float sl = 0.f, sh = 0.f;
 #pragma unroll
-    for (int l = 0; l < 32; ++l) {
-        mbits = max(mbits, __float_as_uint(raw_l[l]) & 0x7fffffffu);
-        mbits = max(mbits, __float_as_uint(raw_h[l]) & 0x7fffffffu);
-        sl += raw_l[l];
-        sh += raw_h[l];
+    for (int i = 0; i < 8; ++i) {
+        const float4 a = idle ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(xv + i);
+        const float4 b = idle ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(xv + 8 + i);
+        st.xp[4 * i + 0] = pack2(a.x, b.x);
+        st.xp[4 * i + 1] = pack2(a.y, b.y);
+        st.xp[4 * i + 2] = pack2(a.z, b.z);
+        st.xp[4 * i + 3] = pack2(a.w, b.w);
     }
-    // Largest |x| < 2^(eM+1); E = eM + 23 keeps every pre-scaled activation
-    // below 2^127 and puts the largest product near 2^-19.
-    const int eM = int(mbits >> 23) - 127;
-    const int E = eM + 23;
 #pragma unroll
     for (int l = 0; l < 32; ++l) {
-        const int i = l & 3;
-        const int p_lo = (i < 3) ? 8 * i : 0;  // byte 3 is shifted down by 24 first
-        st.xl[l] = scale_pow2(raw_l[l], 149 - p_lo - E);
-        st.xh[l] = scale_pow2(raw_h[l], 149 - (p_lo + 4) - E);
+        mbits = max(mbits, uint32_t(st.xp[l]) & 0x7fffffffu);
+        mbits = max(mbits, uint32_t(st.xp[l] >> 32) & 0x7fffffffu);
+        sl += lo_of(st.xp[l]);
+        sh += hi_of(st.xp[l]);
     }
-    st.Xl = sl;
-    st.Xh = sh;
+    // Largest |x| < 2^(eM+1).  E = eM + 23 keeps every pre-scaled activation
+    // below 2^127 and puts the largest product near 2^-19.  The pre-scale of a
+    // nibble at bit p is 2^(149-p-E) = 2^(126-p-eM).
+    const int eM = int(mbits >> 23) - 127;
+    const int E = eM + 23;
+    const bool one_step = (eM >= -1) && (eM <= 212);
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+        const int k = l & 3;
+        const int p = (k < 3) ? 8 * k : 0;  // byte 3 is shifted down by 24 first
+        const int s_lo = 126 - p - eM, s_hi = s_lo - 4;
+        const float xl = lo_of(st.xp[l]), xh = hi_of(st.xp[l]);
+        st.xp[l] = one_step ? pack2(xl * exp2i(s_lo), xh * exp2i(s_hi))
+                            : pack2(scale_pow2(xl, s_lo), scale_pow2(xh, s_hi));
+    }
+    st.X = make_float2(sl, sh);
     const int E1 = E / 2;
     st.p1 = exp2i(E1);
     st.p2 = exp2i(E - E1);
@@ -131,13 +168,11 @@ __device__ __forceinline__ void q4_prologue(Q4State &st, const float *x, int64_t
     const uint32_t u0 = 2u * uint32_t(c4 & 1);
     st.selA = u0 | ((u0 + 1) << 4) | ((4 + u0) << 8) | ((5 + u0) << 12);
     st.selB = u0 | ((u0 + 1) << 4) | (u0 << 8) | ((u0 + 1) << 12);
-    if (c4 < 2) {
-        st.mA = 0x3F3F3F3Fu; st.mB = 0; st.mC = 0; st.mD = 0;
-    } else {
-        st.mA = 0; st.mB = 0x30303030u; st.mC = 0x00000F0Fu; st.mD = 0x0F0F0000u;
-    }
-    st.hdr_off = (local_chunk >> 2) * 144;
-    st.qs_off = st.hdr_off + 16 + 32 * c4;
+    st.hi4 = c4 >= 2;
+    // Idle lanes (past the end of the K-slice) read the slice's first block,
+    // whose finite values times their zero activations contribute exactly 0.
+    st.hdr_off = idle ? 0 : (local_chunk >> 2) * 144;
+    st.qs_off = idle ? 16 : st.hdr_off + 16 + 32 * c4;
 }
 
 // Partial dot product of one row's chunk (64 weights) with the chunk's
@@ -148,54 +183,57 @@ __device__ __forceinline__ float q4_row(const Q4State &st, const uint8_t *row)
     const U4 q0 = lds128(row + st.qs_off);
     const U4 q1 = lds128(row + st.qs_off + 16);
     const uint32_t qw[8] = {q0.a, q0.b, q0.c, q0.d, q1.a, q1.b, q1.c, q1.d};
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    uint64_t acc0 = 0, acc1 = 0;  // (+0.0f, +0.0f)
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-        const uint32_t w = qw[t];
-        const uint32_t w3 = w >> 24;
-        float2 &acc = (t & 1) ? acc1 : acc0;
-        acc = ffma2(make_float2(as_float(w & 0x0000000Fu), as_float(w & 0x000000F0u)),
-                    make_float2(st.xl[4 * t + 0], st.xh[4 * t + 0]), acc);
-        acc = ffma2(make_float2(as_float(w & 0x00000F00u), as_float(w & 0x0000F000u)),
-                    make_float2(st.xl[4 * t + 1], st.xh[4 * t + 1]), acc);
-        acc = ffma2(make_float2(as_float(w & 0x000F0000u), as_float(w & 0x00F00000u)),
-                    make_float2(st.xl[4 * t + 2], st.xh[4 * t + 2]), acc);
-        acc = ffma2(make_float2(as_float(w3 & 0x0Fu), as_float(w3 & 0xF0u)),
-                    make_float2(st.xl[4 * t + 3], st.xh[4 * t + 3]), acc);
+        const uint64_t ww = (uint64_t(qw[t]) << 32) | qw[t];
+        const uint32_t w3 = qw[t] >> 24;
+        const uint64_t ww3 = (uint64_t(w3) << 32) | w3;
+        uint64_t &acc = (t & 1) ? acc1 : acc0;
+        acc = ffma2_u64(nibble_pair<0>(ww), st.xp[4 * t + 0], acc);
+        acc = ffma2_u64(nibble_pair<1>(ww), st.xp[4 * t + 1], acc);
+        acc = ffma2_u64(nibble_pair<2>(ww), st.xp[4 * t + 2], acc);
+        acc = ffma2_u64(nibble_pair<0>(ww3), st.xp[4 * t + 3], acc);
     }
-    const float2 S = __fadd2_rn(acc0, acc1);
+    const float2 S = __fadd2_rn(make_float2(lo_of(acc0), hi_of(acc0)),
+                                make_float2(lo_of(acc1), hi_of(acc1)));
     // (sc_lo, sc_hi, m_lo, m_hi) as bytes of R.
     const uint32_t A = __byte_perm(h.b, h.c, st.selA);
     const uint32_t B = __byte_perm(h.d, h.d, st.selB);
-    const uint32_t R = (A & st.mA) | ((A >> 2) & st.mB) | (B & st.mC) | ((B >> 4) & st.mD);
+    const uint32_t R = st.hi4 ? (((B & 0x00000F0Fu) | ((B >> 4) & 0x0F0F0000u)) |
+                                 ((A >> 2) & 0x30303030u))
+                              : (A & 0x3F3F3F3Fu);
     const float2 magic = make_float2(-8388608.f, -8388608.f);
     const float2 sc = __fadd2_rn(make_float2(byte_magic(R, 0), byte_magic(R, 1)), magic);
     const float2 mm = __fadd2_rn(make_float2(byte_magic(R, 2), byte_magic(R, 3)), magic);
     const float2 us = __fmul2_rn(sc, S);
-    const float u = us.x + us.y;
-    const float v = fmaf(mm.x, st.Xl, mm.y * st.Xh);
+    const float2 vs = __fmul2_rn(mm, st.X);
     const float2 dd = half2_bits_to_float2(h.a);  // (d, dmin)
-    const float t = (dd.x * u) * st.p1;
-    return fmaf(t, st.p2, -(dd.y * v));
+    const float t = (dd.x * (us.x + us.y)) * st.p1;
+    return fmaf(t, st.p2, -(dd.y * (vs.x + vs.y)));
 }
 
+// ----------------------------------------------------------------- Q8_0
 struct Q8State {
-    float xa[32], xb[32];  // activations of the chunk's two blocks
-    int off;               // byte offset of the chunk in a row
+    float2 xp[32];  // (block A activation j, block B activation j)
+    int off;        // byte offset of the chunk in a row
 };
 
 __device__ __forceinline__ void q8_prologue(Q8State &st, const float *x, int64_t gchunk,
-                                            int local_chunk)
+                                            int local_chunk, bool idle)
 {
-    const float4 *xv = reinterpret_cast<const float4 *>(x + gchunk * 64);
+    float a[32], b[32];
+    if (idle) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float4 a = __ldg(xv + i);
-        float4 b = __ldg(xv + 8 + i);
-        st.xa[4 * i + 0] = a.x; st.xa[4 * i + 1] = a.y; st.xa[4 * i + 2] = a.z; st.xa[4 * i + 3] = a.w;
-        st.xb[4 * i + 0] = b.x; st.xb[4 * i + 1] = b.y; st.xb[4 * i + 2] = b.z; st.xb[4 * i + 3] = b.w;
+        for (int l = 0; l < 32; ++l)
+            a[l] = b[l] = 0.f;
+    } else {
+        load_chunk_x(x + gchunk * 64, a, b);
     }
-    st.off = local_chunk * 68;
+#pragma unroll
+    for (int l = 0; l < 32; ++l)
+        st.xp[l] = make_float2(a[l], b[l]);
+    st.off = idle ? 0 : local_chunk * 68;
 }
 
 // Two Q8_0 blocks (68 bytes, 4-byte aligned): block A = bytes 0..33, block B
@@ -220,182 +258,253 @@ __device__ __forceinline__ float q8_row(const Q8State &st, const uint8_t *row)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float2 q = __fadd2_rn(make_float2(byte_magic(qa, i), byte_magic(qb, i)), off);
-            acc = ffma2(q, make_float2(st.xa[4 * k + i], st.xb[4 * k + i]), acc);
+            acc = __ffma2_rn(q, st.xp[4 * k + i], acc);
         }
     }
     const float2 S = __fadd2_rn(acc0, acc1);
     return fmaf(d.x, S.x, d.y * S.y);
 }
 
+// ----------------------------------------------------------------- reduction
+// Sum RPG values over groups of W lanes (W a power of two <= 32, RPG <= W)
+// with a reduce-scatter: afterwards every lane holds the full sum of one of
+// the RPG rows (its index is returned in j), and the lanes whose low
+// log2(W/RPG) bits are zero are the designated writers.
+template <int W, int RPG>
+__device__ __forceinline__ float reduce_rows(const float (&v)[RPG], int lane, int &j)
+{
+    float cur[RPG];
+#pragma unroll
+    for (int k = 0; k < RPG; ++k)
+        cur[k] = v[k];
+    int idx = 0;
+    int off = W / 2;
+#pragma unroll
+    for (int n = RPG; n > 1; n /= 2) {
+        const int half = n / 2;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+            const float send = upper ? cur[k] : cur[k + half];
+            const float keep = upper ? cur[k + half] : cur[k];
+            cur[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        if (upper)
+            idx += half;
+        off /= 2;
+    }
+#pragma unroll
+    for (; off >= 1; off /= 2)
+        cur[0] += __shfl_xor_sync(0xffffffffu, cur[0], off);
+    j = idx;
+    return cur[0];
+}
+
 // ----------------------------------------------------------------- kernel
 struct KParams {
     GemvArgs a;
-    int kchunks, team, rg, rpg, stage_rows, stages, ksplit, row_slices;
+    int kchunks, team, rg, stage_rows, stages, ksplit, row_slices;
     int64_t slice_bytes;
 };
 
-template <int FMT>
-__global__ void __launch_bounds__(kMaxThreads, 2) gemv_kernel(const __grid_constant__ KParams P)
+template <int FMT, int W, int RPG, int MINB>
+__global__ void __launch_bounds__(kMaxConsumers, MINB) gemv_kernel(const __grid_constant__ KParams P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const GemvArgs &a = P.a;
     const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int NS = P.stages;
+    const int SR = P.stage_rows;
+    const int64_t SB = P.slice_bytes;
     const int rs = blockIdx.x / P.ksplit;  // row slice
     const int ks = blockIdx.x % P.ksplit;  // K-slice
-    // Balanced contiguous row range of this slice.
     const int64_t base = a.N / P.row_slices, extra = a.N % P.row_slices;
     const int64_t r0 = rs * base + min64(rs, extra);
     const int64_t r1 = r0 + base + (rs < extra ? 1 : 0);
-    const int64_t nrows = r1 - r0;
-    const int nst = int((nrows + P.stage_rows - 1) / P.stage_rows);
-
-    const size_t stage_bytes = size_t(P.stage_rows) * size_t(P.slice_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(P.stages) * stage_bytes);
+    const int nst = int((r1 - r0 + SR - 1) / SR);
     const int nwt = (P.team + 31) / 32;  // warps per team
-    float *red = reinterpret_cast<float *>(full + P.stages);  // [2][stage_rows][nwt]
-    int *flag = reinterpret_cast<int *>(red + 2 * P.stage_rows * nwt);
+    const int nwarps = int(blockDim.x) / 32;
 
-    uint64_t policy = 0;
+    const size_t stage_bytes = size_t(SR) * size_t(SB);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + size_t(NS) * stage_bytes);
+    uint64_t *empty = full + NS;
+    float *red = reinterpret_cast<float *>(empty + NS);  // [NS][SR][nwt]
+
     if (tid == 0) {
-        for (int s = 0; s < P.stages; ++s)
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&empty[s], unsigned(nwarps));
+        }
         fence_barrier_init();
-        *flag = 0;
-        policy = policy_evict_first();
     }
     __syncthreads();
     pdl_launch_dependents();
 
-    // Producer: stage s -> buffer s % stages.  The weights are constant, so
-    // the first stages are requested before waiting for the previous kernel.
+    // Producer (lane 0 of warp 0): stage s goes to ring slot s % NS.
+    const bool producer = tid < 32;
+    uint64_t policy = 0;
     auto issue = [&](int s) {
-        const int64_t ra = r0 + int64_t(s) * P.stage_rows;
-        const int64_t rb = min64(ra + P.stage_rows, r1);
-        uint8_t *dst = smem + size_t(s % P.stages) * stage_bytes;
-        uint64_t *bar = &full[s % P.stages];
-        mbar_arrive_expect_tx(bar, unsigned((rb - ra) * P.slice_bytes));
+        const int64_t ra = r0 + int64_t(s) * SR;
+        const int64_t rb = min64(ra + SR, r1);
+        uint8_t *dst = smem + size_t(s % NS) * stage_bytes;
+        uint64_t *bar = &full[s % NS];
+        mbar_arrive_expect_tx(bar, unsigned((rb - ra) * SB));
         if (P.ksplit == 1) {
             int64_t r = ra;
             while (r < rb) {
                 const int m = matrix_of(a, r);
                 const int64_t seg_end = min64(rb, a.row_end[m]);
                 const uint8_t *src = a.w[m] + (r - row_start(a, m)) * a.row_bytes;
-                bulk_g2s(dst + (r - ra) * P.slice_bytes, src, unsigned((seg_end - r) * a.row_bytes),
-                         bar, policy);
+                bulk_g2s(dst + (r - ra) * SB, src, unsigned((seg_end - r) * a.row_bytes), bar,
+                         policy);
                 r = seg_end;
             }
         } else {
             for (int64_t r = ra; r < rb; ++r) {
                 const int m = matrix_of(a, r);
-                const uint8_t *src =
-                    a.w[m] + (r - row_start(a, m)) * a.row_bytes + int64_t(ks) * P.slice_bytes;
-                bulk_g2s(dst + (r - ra) * P.slice_bytes, src, unsigned(P.slice_bytes), bar, policy);
+                const uint8_t *src = a.w[m] + (r - row_start(a, m)) * a.row_bytes + int64_t(ks) * SB;
+                bulk_g2s(dst + (r - ra) * SB, src, unsigned(SB), bar, policy);
             }
         }
     };
-    int issued = 0;
+    // The weights are constant: the first stages are requested before waiting
+    // for the previous kernel in the stream.
+    int issued = min(NS, nst);
     if (tid == 0) {
-        for (; issued < min(P.stages, nst); ++issued)
-            issue(issued);
+        policy = policy_evict_first();
+        for (int s = 0; s < issued; ++s)
+            issue(s);
     }
 
-    pdl_wait();  // x (and y / workspace) belong to the previous kernel until here
-
-    const int g = tid / P.team;         // row team
-    const int c = tid % P.team;         // chunk lane within the team
-    const bool active = (g < P.rg) && (c < P.kchunks);
+    const int g = tid / P.team;  // row team
+    const int c = tid % P.team;  // chunk lane within the team
+    const bool idle = c >= P.kchunks;
     const int64_t gchunk = int64_t(ks) * P.kchunks + c;
+    const int warp_in_team = c >> 5;
+    const int rg = P.rg;
 
+    pdl_wait();  // x, y and the workspace belong to the previous kernel until here
     Q4State s4;
     Q8State s8;
-    if (active) {
-        if (FMT == QMM_Q4_K)
-            q4_prologue(s4, a.x, gchunk, c);
-        else
-            q8_prologue(s8, a.x, gchunk, c);
-    }
-    const int lane = tid & 31;
-    const int width = P.team < 32 ? P.team : 32;
-    const int warp_in_team = c >> 5;
+    if (FMT == QMM_Q4_K)
+        q4_prologue(s4, a.x, gchunk, c, idle);
+    else
+        q8_prologue(s8, a.x, gchunk, c, idle);
 
     bool failed = false;
     for (int s = 0; s < nst; ++s) {
-        const int buf = s % P.stages;
-        if (!mbar_wait_bounded(&full[buf], unsigned(s / P.stages) & 1u)) {
-            atomicOr(a.status, kStatusTimeoutBit);
-            *flag = 1;
-        }
-        const uint8_t *stage = smem + size_t(buf) * stage_bytes;
-        const int64_t ra = r0 + int64_t(s) * P.stage_rows;
-        const int nr = int(min64(P.stage_rows, r1 - ra));
-        float *rd = red + (s & 1) * P.stage_rows * nwt;
-#pragma unroll 1
-        for (int j = 0; j < P.rpg; ++j) {
-            const int i = g + P.rg * j;  // row within the stage
-            float part = 0.f;
-            if (active && i < nr && !*flag) {
-                const uint8_t *row = stage + size_t(i) * P.slice_bytes;
-                part = (FMT == QMM_Q4_K) ? q4_row(s4, row) : q8_row(s8, row);
-            }
-            part = warp_sum(part, width);
-            if ((c & 31) == 0 && g < P.rg && i < nr)
-                rd[i * nwt + warp_in_team] = part;
-        }
-        __syncthreads();  // stage buffer free; partial sums visible
-        if (*flag) {
+        const int b = s % NS;
+        const unsigned parity = unsigned(s / NS) & 1u;
+        if (!mbar_wait_bounded(&full[b], parity)) {
             failed = true;
             break;
         }
-        if (tid < nr) {
-            float v = 0.f;
-            for (int wv = 0; wv < nwt; ++wv)
-                v += rd[tid * nwt + wv];
-            const int64_t row = ra + tid;
-            if (P.ksplit == 1) {
-                const int m = matrix_of(a, row);
-                a.y[m][row - row_start(a, m)] = v;
-            } else {
-                a.ws[int64_t(ks) * a.N + row] = v;
+        const uint8_t *stage = smem + size_t(b) * stage_bytes;
+        float part[RPG];
+#pragma unroll
+        for (int j = 0; j < RPG; ++j) {
+            // Rows past the end of the range hold stale bytes; their sums are
+            // computed and never stored.
+            const uint8_t *row = stage + size_t(g + rg * j) * SB;
+            part[j] = (FMT == QMM_Q4_K) ? q4_row(s4, row) : q8_row(s8, row);
+        }
+        int j;
+        const float v = reduce_rows<W, RPG>(part, lane, j);
+        if ((lane & (W / RPG - 1)) == 0)
+            red[(size_t(b) * SR + g + rg * j) * nwt + warp_in_team] = v;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[b]);
+        if (producer) {
+            // Epilogue of stage s once every warp has released it, then refill.
+            if (!mbar_wait_bounded(&empty[b], parity)) {
+                failed = true;
+                break;
+            }
+            const int64_t ra = r0 + int64_t(s) * SR;
+            const int nr = int(min64(SR, r1 - ra));
+            const float *rd = red + size_t(b) * SR * nwt;
+            for (int i = lane; i < nr; i += 32) {
+                float acc = 0.f;
+                for (int wv = 0; wv < nwt; ++wv)
+                    acc += rd[i * nwt + wv];
+                const int64_t row = ra + i;
+                if (P.ksplit == 1) {
+                    const int m = matrix_of(a, row);
+                    a.y[m][row - row_start(a, m)] = acc;
+                } else {
+                    a.ws[int64_t(ks) * a.N + row] = acc;
+                }
+            }
+            __syncwarp();
+            if (issued < nst) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue(issued);
+                }
+                ++issued;
             }
         }
-        if (tid == 0 && issued < nst) {
-            fence_proxy_async_smem();
-            issue(issued++);
-        }
     }
-
     if (failed) {
-        // Let the copies still in flight land before the CTA's shared memory
-        // is released (bounded as well).
-        if (tid == 0) {
+        if (lane == 0)
+            atomicOr(a.status, kStatusTimeoutBit);
+        // Let the copies still in flight land before shared memory goes away.
+        if (tid == 0)
             for (int s = 0; s < issued; ++s)
-                mbar_wait_bounded(&full[s % P.stages], unsigned(s / P.stages) & 1u, 100000000ll);
-        }
+                mbar_wait_bounded(&full[s % NS], unsigned(s / NS) & 1u, 100000000ll);
         return;
     }
-
-    if (P.ksplit > 1) {
-        __shared__ int last;
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            const unsigned old = atomicAdd(&a.tickets[rs], 1u);
-            last = (old == unsigned(P.ksplit - 1));
-        }
-        __syncthreads();
+    if (producer && P.ksplit > 1) {
+        __threadfence();
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0)
+            last = atomicAdd(&a.tickets[rs], 1u) == unsigned(P.ksplit - 1);
+        last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence();
-            for (int64_t r = r0 + tid; r < r1; r += blockDim.x) {
-                float v = 0.f;
+            for (int64_t r = r0 + lane; r < r1; r += 32) {
+                float acc = 0.f;
                 for (int k = 0; k < P.ksplit; ++k)
-                    v += __ldcg(a.ws + int64_t(k) * a.N + r);
+                    acc += __ldcg(a.ws + int64_t(k) * a.N + r);
                 const int m = matrix_of(a, r);
-                a.y[m][r - row_start(a, m)] = v;
+                a.y[m][r - row_start(a, m)] = acc;
             }
-            if (tid == 0)
+            if (lane == 0)
                 a.tickets[rs] = 0u;
         }
     }
+}
+
+using KernelFn = void (*)(KParams);
+
+template <int FMT, int W, int MINB>
+KernelFn pick_rpg(int rpg)
+{
+    switch (rpg) {
+    case 1: return gemv_kernel<FMT, W, 1, MINB>;
+    case 2: return gemv_kernel<FMT, W, 2, MINB>;
+    default: return gemv_kernel<FMT, W, 4, MINB>;
+    }
+}
+
+template <int FMT, int MINB>
+KernelFn pick_w(int w, int rpg)
+{
+    switch (w) {
+    case 4: return pick_rpg<FMT, 4, MINB>(rpg);
+    case 8: return pick_rpg<FMT, 8, MINB>(rpg);
+    case 16: return pick_rpg<FMT, 16, MINB>(rpg);
+    default: return pick_rpg<FMT, 32, MINB>(rpg);
+    }
+}
+
+template <int FMT>
+KernelFn pick(int w, int rpg, int minb)
+{
+    return minb >= 2 ? pick_w<FMT, 2>(w, rpg) : pick_w<FMT, 1>(w, rpg);
 }
 
 } // namespace
@@ -404,39 +513,53 @@ GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit
 {
     GemvPlan p;
     const int64_t chunks = K / 64;  // K % 256 == 0 for both formats here
-    // K-slices: at most 256 chunks each (one thread per chunk), whole Q4_K
-    // blocks (a multiple of 4 chunks), and enough CTAs to cover the GPU when
-    // there are few rows.
-    // A valid split cuts the row into equal slices of whole 256-weight blocks.
+    // A valid split cuts the row into equal slices of whole 256-weight blocks,
+    // each at most kMaxConsumers chunks (one consumer thread per chunk).
     const int64_t nblocks = chunks / 4;
-    auto valid = [&](int64_t ks) { return ks >= 1 && ks <= nblocks && nblocks % ks == 0; };
-    int ksplit = int((chunks + kMaxThreads - 1) / kMaxThreads);
+    auto valid = [&](int64_t ks) {
+        return ks >= 1 && ks <= nblocks && nblocks % ks == 0 && chunks / ks <= kMaxConsumers;
+    };
+    int ksplit = int((chunks + kMaxConsumers - 1) / kMaxConsumers);
     while (!valid(ksplit))
         ++ksplit;
-    const int64_t target_ctas = int64_t(sm_count) * 2;
+    // Tuning knobs (environment): CTAs per SM, stage size target in bytes,
+    // ring depth.
+    const char *e_cp = getenv("QMM_GEMV_CTAS_PER_SM");
+    const char *e_sb = getenv("QMM_GEMV_STAGE_BYTES");
+    const char *e_ns = getenv("QMM_GEMV_STAGES");
+    const int ctas_per_sm = (e_cp && atoi(e_cp) > 0) ? atoi(e_cp) : kCtasPerSm;
+    const int64_t target_ctas = int64_t(sm_count) * ctas_per_sm;
     while (force_ksplit <= 0 && N * ksplit < target_ctas && valid(int64_t(ksplit) * 2))
         ksplit *= 2;
-    if (force_ksplit > 0 && valid(force_ksplit) && chunks / force_ksplit <= kMaxThreads)
+    if (force_ksplit > 0 && valid(force_ksplit))
         ksplit = force_ksplit;
     p.ksplit = ksplit;
     p.kchunks = int(chunks / ksplit);
-    int team = 1;
+    int team = 4;
     if (p.kchunks <= 32) {
         while (team < p.kchunks)
             team *= 2;
     } else {
         team = (p.kchunks + 31) / 32 * 32;
     }
-    p.rg = kMaxThreads / team;
+    p.rg = kMaxConsumers / team;
     if (p.rg < 1)
         p.rg = 1;
     p.threads = p.rg * team;
     p.slice_bytes = (fmt == QMM_Q4_K) ? int64_t(p.kchunks / 4) * 144 : int64_t(p.kchunks) * 68;
-    int rpg = int(kStageBytesTarget / (int64_t(p.rg) * p.slice_bytes));
-    rpg = rpg < 1 ? 1 : (rpg > 4 ? 4 : rpg);
+    const int64_t stage_target = e_sb ? atoll(e_sb) : kStageBytesTarget;
+    int rpg = int(stage_target / (int64_t(p.rg) * p.slice_bytes));
+    const int wred = team < 32 ? team : 32;
+    rpg = rpg >= 4 ? 4 : (rpg >= 2 ? 2 : 1);
+    while (rpg > wred)
+        rpg /= 2;
     p.rpg = rpg;
     p.stage_rows = p.rg * rpg;
-    p.stages = kStages;
+    p.stages = e_ns ? atoi(e_ns) : kStages;
+    if (p.stages < 2)
+        p.stages = 2;
+    if (p.stages > 16)
+        p.stages = 16;
     int64_t slices = target_ctas / ksplit;
     if (slices > N)
         slices = N;
@@ -445,7 +568,7 @@ GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit
     p.row_slices = int(slices);
     const int nwt = (team + 31) / 32;
     p.smem = size_t(p.stages) * size_t(p.stage_rows) * size_t(p.slice_bytes) +
-             size_t(p.stages) * 8 + size_t(2 * p.stage_rows * nwt) * 4 + 16;
+             size_t(p.stages) * 16 + size_t(p.stages) * size_t(p.stage_rows) * nwt * 4;
     return p;
 }
 
@@ -454,23 +577,23 @@ size_t gemv_workspace_floats(const GemvPlan &p, int64_t N)
     return p.ksplit > 1 ? size_t(p.ksplit) * size_t(N) : 0;
 }
 
-static int team_of(const GemvPlan &p) { return p.threads / p.rg; }
-
 cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
 {
     KParams P;
     P.a = a;
     P.kchunks = p.kchunks;
-    P.team = team_of(p);
+    P.team = p.threads / p.rg;
     P.rg = p.rg;
-    P.rpg = p.rpg;
     P.stage_rows = p.stage_rows;
     P.stages = p.stages;
     P.ksplit = p.ksplit;
     P.row_slices = p.row_slices;
     P.slice_bytes = p.slice_bytes;
-
-    void (*kern)(KParams) = (a.fmt == QMM_Q4_K) ? gemv_kernel<QMM_Q4_K> : gemv_kernel<QMM_Q8_0>;
+    const int w = P.team < 32 ? P.team : 32;
+    const char *e_lb = getenv("QMM_GEMV_MINB");
+    const int minb = e_lb ? atoi(e_lb) : 1;
+    KernelFn kern = (a.fmt == QMM_Q4_K) ? pick<QMM_Q4_K>(w, p.rpg, minb)
+                                        : pick<QMM_Q8_0>(w, p.rpg, minb);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(p.smem));
     if (e != cudaSuccess)
@@ -484,7 +607,7 @@ cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, P);
 }
 

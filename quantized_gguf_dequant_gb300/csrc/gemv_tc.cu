@@ -1,0 +1,632 @@
+// gemv_tc.cu -- Q4_K decode GEMV (M = 1..4 activation rows) on the tensor
+// cores, with the dequantisation fused into the operand construction.
+//
+// The operation: "Building a Rust Inference Engine That Matches Llama.cpp",
+// "Where the wins came from" -- the dequant math happens inline in the dot
+// product; the weights never become a full-precision buffer.
+//
+// Why tensor cores for a GEMV.  Decoding Q4_K in plain fp32 costs one
+// integer-pipe instruction per weight (isolate the nibble) plus an FMA, and
+// the integer pipe (16 lanes per scheduler) then caps the kernel below the
+// HBM rate.  Here two nibbles are isolated per instruction straight into an
+// fp16 pair: (w & 0x000F000F) | 0x64006400 is the half2 (1024+q0, 1024+q1);
+// one exact fp16 FMA, (1024+q)*sc - 1024*sc = q*sc (<= 945, exact in fp16),
+// applies the sub-block scale, and mma.sync multiplies these q*sc values by
+// the activations.  The activations enter as two fp16 terms (hi + lo, about
+// 22 significant bits) after an exact power-of-two scale per super-block, so
+// the products are exact and only the fp32 accumulation rounds.  The mins
+// are a second small MMA per super-block (m_s against the sub-block sums of
+// x, scaled by a further 2^-5 to stay inside fp16).  Per super-block and row:
+// y += (d*Dq - dmin*32*Dmin) * 2^-s.
+//
+// Work decomposition.  The matrix is cut into units of 16 rows x one
+// 256-weight super-block column (2304 bytes), ordered (matrix, row tile,
+// super-block).  Every CTA owns whole row tiles (an even split, so CTAs
+// differ by at most one tile) and splits their units evenly over its warps.
+// A warp streams its units through its own ring of shared-memory slots with
+// 2-D TMA copies (no CTA-wide synchronisation in the loop), keeps its rows'
+// partial sums in registers, and writes a row tile directly when it covered
+// the whole tile.  Tiles split between warps are added in shared memory at the
+// end, in warp order: no global synchronisation, and results are bitwise
+// repeatable.
+//
+// Fragment layout (mma.sync m16n8k16, A row-major, B col-major): lane = 4g+c.
+// For a 16-row tile, lane (g, c) holds rows g and g+8 and owns chunk c of the
+// super-block (qs bytes 32c..32c+31: sub-blocks 2c and 2c+1).  Word t of the
+// chunk feeds k-steps 2t and 2t+1: step 2t takes nibbles (0,4) [sub-block 2c]
+// in k-slots (2c, 2c+1) and nibbles (1,5) [sub-block 2c+1] in (2c+8, 2c+9);
+// step 2t+1 takes nibbles (2,6) and (3,7).  The B fragment for the same
+// (step, c) holds the matching activations; column n of B is (x row n/2,
+// term n%2), so lane c's accumulator columns (2c, 2c+1) are both terms of
+// activation row c.
+#include <cstdlib>
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kTileRows = 16;
+constexpr int kTileBytes = kTileRows * 144;  // 2304
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// (a & b) | c in one LOP3 (lookup table 0xEA); written out because the
+// compiler otherwise splits a mask-and-merge with two constants in two.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// D = A B (+ C) with fp16 operands and fp32 accumulation.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    const float z = 0.f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+struct TcParams {
+    CUtensorMap tmap[kMaxGroup];  // rows of each matrix as a 2-D uint64 tensor
+    int64_t tile_end[kMaxGroup];  // cumulative 16-row tile counts
+    int64_t rows[kMaxGroup];
+    float *y[kMaxGroup];
+    const float *x;
+    float *ws;          // [CTAs][2][4][16] partial sums of tiles split between CTAs
+    unsigned *tickets;  // [tiles]
+    unsigned *status;
+    int64_t U;          // units
+    int64_t ldx, ldy;   // activation / output row strides (elements)
+    int nmat, M, NB, W, nslot;  // W: CTAs
+    int late_trigger;           // let the next kernel launch only after the main loop
+};
+
+// Per-row decode of the super-block header for chunk c: the fp16 pairs the
+// operand construction needs, and (d, dmin).
+struct RowScales {
+    uint32_t SL, CL, SH, CH;  // (sc_lo, sc_lo), -1024*SL, (sc_hi/16, ..), -1024*SH
+    uint32_t Am;              // (m_lo, m_hi)
+    float d, dmin;
+};
+
+__device__ __forceinline__ RowScales row_scales(uint4 h, uint32_t selA, uint32_t selB, bool hi4)
+{
+    const uint32_t A = __byte_perm(h.y, h.z, selA);
+    const uint32_t B = __byte_perm(h.w, h.w, selB);
+    const uint32_t R = hi4 ? (((B & 0x00000F0Fu) | ((B >> 4) & 0x0F0F0000u)) |
+                              ((A >> 2) & 0x30303030u))
+                           : (A & 0x3F3F3F3Fu);  // bytes: sc_lo, sc_hi, m_lo, m_hi
+    RowScales s;
+    // 0x64vv is the fp16 1024 + v; subtracting 1024 (0xE400) leaves v exactly.
+    s.SL = hadd2(__byte_perm(R, 0x64u, 0x4040u), 0xE400E400u);
+    s.SH = hfma2(__byte_perm(R, 0x64u, 0x4141u), 0x2C002C00u, 0xD400D400u);  // (1024+v)/16 - 64
+    s.CL = hmul2(s.SL, 0xE400E400u);
+    s.CH = hmul2(s.SH, 0xE400E400u);
+    s.Am = hadd2(__byte_perm(R, 0x64u, 0x4342u), 0xE400E400u);
+    const float2 dd = half2_bits_to_float2(h.x);
+    s.d = dd.x;
+    s.dmin = dd.y;
+    return s;
+}
+
+__device__ __forceinline__ int matrix_of_tile(const TcParams &P, int64_t tile)
+{
+    int m = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxGroup - 1; ++i)
+        if (i < P.nmat - 1 && tile >= P.tile_end[i])
+            m = i + 1;
+    return m;
+}
+
+// A position in the unit sequence, advanced without divisions.
+struct Cursor {
+    int tile;     // global 16-row tile
+    int sb;       // super-block column
+    int mat;      // matrix of the tile
+    int tend;     // first global tile of the next matrix
+    int tbase;    // first global tile of this matrix
+};
+
+__device__ __forceinline__ Cursor cursor_at(const TcParams &P, int64_t u)
+{
+    Cursor q;
+    q.tile = int(u / P.NB);
+    q.sb = int(u % P.NB);
+    q.mat = matrix_of_tile(P, q.tile);
+    q.tbase = q.mat == 0 ? 0 : int(P.tile_end[q.mat - 1]);
+    q.tend = int(P.tile_end[q.mat]);
+    return q;
+}
+
+__device__ __forceinline__ void advance(const TcParams &P, Cursor &q)
+{
+    if (++q.sb == P.NB) {
+        q.sb = 0;
+        if (++q.tile == q.tend && q.mat + 1 < P.nmat) {
+            ++q.mat;
+            q.tbase = q.tend;
+            q.tend = int(P.tile_end[q.mat]);
+        }
+    }
+}
+
+// Activations of super-block sb, x row m, as this lane's share of the B
+// fragments (see the fragment layout above), the sub-block sums for the min
+// MMA, and the inverse scale.  Lane (cc, tt) = (lane >> 3, lane & 7) holds
+// x[64cc + 4tt .. +3] (v) and x[64cc + 32 + 4tt .. +3] (w).
+template <int NCOL>
+__device__ __forceinline__ void prep_super_block(int sb, int m, int M, float4 v, float4 w,
+                                                 int lane, uint2 *Bs, uint32_t *Bm, float *inv)
+{
+    const int cc = lane >> 3, tt = lane & 7;
+    uint32_t mb = 0;
+    mb = max(mb, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    mb = max(mb, max(max(__float_as_uint(w.x) & 0x7fffffffu, __float_as_uint(w.y) & 0x7fffffffu),
+                     max(__float_as_uint(w.z) & 0x7fffffffu, __float_as_uint(w.w) & 0x7fffffffu)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    // max|x| < 2^(eM+1): scaling by 2^(14-eM) keeps every term below 2^15.
+    const int s = mb ? 14 - (int(mb >> 23) - 127) : 0;
+    float xs[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
+    if (s >= -126 && s <= 127) {
+        const float f = exp2i(s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] *= f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] = scale_pow2(xs[i], s);
+    }
+    __half hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = __float2half_rn(xs[i]);
+        lo[i] = __float2half_rn(xs[i] - __half2float(hi[i]));
+    }
+    auto pack = [](__half a, __half b) {
+        return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
+    };
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const size_t base = (size_t(sb) * 16 + 2 * tt + e) * NCOL;
+        Bs[(base + 2 * m) * 4 + cc] = make_uint2(pack(hi[e], hi[e + 2]), pack(hi[4 + e], hi[6 + e]));
+        Bs[(base + 2 * m + 1) * 4 + cc] =
+            make_uint2(pack(lo[e], lo[e + 2]), pack(lo[4 + e], lo[6 + e]));
+    }
+    // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
+    float sl = (v.x + v.y) + (v.z + v.w);
+    float sh = (w.x + w.y) + (w.z + w.w);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+    }
+    if (tt == 0) {
+        // A sub-block sum of 32 terms below 2^15 stays below 2^20: a further
+        // 2^-5 keeps it inside fp16 (undone exactly in the epilogue).
+        const float a = scale_pow2(sl, s - 5), b = scale_pow2(sh, s - 5);
+        const __half ah = __float2half_rn(a), bh = __float2half_rn(b);
+        const __half al = __float2half_rn(a - __half2float(ah));
+        const __half bl = __float2half_rn(b - __half2float(bh));
+        Bm[(size_t(sb) * NCOL + 2 * m) * 4 + cc] = pack(ah, bh);
+        Bm[(size_t(sb) * NCOL + 2 * m + 1) * 4 + cc] = pack(al, bl);
+    }
+    if (lane == 0)
+        inv[sb * M + m] = scale_pow2(1.f, -s);
+}
+
+template <int NCOL>
+__global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__ TcParams P)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nw = int(blockDim.x) >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int NB = P.NB, M = P.M, NS = P.nslot;
+
+    uint8_t *ring = smem + size_t(warp) * NS * kTileBytes;
+    uint2 *Bs = reinterpret_cast<uint2 *>(smem + size_t(nw) * NS * kTileBytes);  // [NB][16][NCOL][4]
+    uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(NB) * 16 * NCOL * 4);  // [NB][NCOL][4]
+    float *inv = reinterpret_cast<float *>(Bm + size_t(NB) * NCOL * 4);           // [NB][M]
+    float *part = inv + size_t(NB) * M;                                           // [nw][2][4][16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(
+        (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * 4 * kTileRows) + 7) & ~uintptr_t(7));
+    uint64_t *bar = bars + warp * NS;
+
+    // Each CTA owns whole row tiles (split evenly, G <= tiles) and splits
+    // their units evenly over its warps.
+    const int64_t G = gridDim.x;
+    const int64_t T = P.U / NB;
+    const int64_t cU0 = (blockIdx.x * T / G) * NB, cU1 = ((blockIdx.x + 1) * T / G) * NB;
+    const int64_t cn = cU1 - cU0;
+    auto warp_begin = [&](int w) { return cU0 + int64_t(w) * cn / nw; };
+    const int64_t u0 = warp_begin(warp), u1 = warp_begin(warp + 1);
+    const int nu = int(u1 - u0);
+    __shared__ int wbeg[17];  // warp boundaries relative to cU0 (wbeg[nw] = cn)
+    if (lane == 0) {
+        wbeg[warp] = int(u0 - cU0);
+        if (warp == nw - 1)
+            wbeg[nw] = int(cn);
+    }
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s)
+            mbar_init(&bar[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (!P.late_trigger)
+        pdl_launch_dependents();
+
+    uint64_t policy = 0;
+    Cursor qi = cursor_at(P, u0);  // next unit to request
+    int slot_i = 0;
+    auto issue = [&]() {
+        mbar_arrive_expect_tx(&bar[slot_i], kTileBytes);
+        tma_load_2d(ring + size_t(slot_i) * kTileBytes, &P.tmap[qi.mat], qi.sb * 18,
+                    (qi.tile - qi.tbase) * kTileRows, &bar[slot_i], policy);
+        advance(P, qi);
+        if (++slot_i == NS)
+            slot_i = 0;
+    };
+    // Weights are constant: start streaming before waiting for the previous
+    // kernel in the stream.
+    int issued = nu < NS ? nu : NS;
+    if (lane == 0) {
+        policy = policy_evict_first();
+        for (int j = 0; j < issued; ++j)
+            issue();
+    }
+
+    pdl_wait();  // x, y and the workspace belong to the previous kernel until here
+
+    // ---- activations -> B fragments.  Warp w takes super-blocks w, w+nw, ...;
+    // the loads of up to 8 of them are in flight together.
+    {
+        const int cc = lane >> 3, tt = lane & 7;
+        for (int m = 0; m < M; ++m) {
+            for (int sb0 = warp; sb0 < NB; sb0 += 8 * nw) {
+                float4 v[8], w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int sb = sb0 + i * nw;
+                    if (sb < NB) {
+                        const float *xr =
+                            P.x + int64_t(m) * P.ldx + int64_t(sb) * 256 + 64 * cc + 4 * tt;
+                        v[i] = __ldg(reinterpret_cast<const float4 *>(xr));
+                        w[i] = __ldg(reinterpret_cast<const float4 *>(xr + 32));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int sb = sb0 + i * nw;
+                    if (sb < NB)
+                        prep_super_block<NCOL>(sb, m, M, v[i], w[i], lane, Bs, Bm, inv);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- main loop
+    const uint32_t u0b = 2u * uint32_t(c & 1);
+    const uint32_t selA = u0b * 0x1111u + 0x5410u;  // bytes (u0, u0+1) of sc12[0..3] and [4..7]
+    const uint32_t selB = u0b * 0x1111u + 0x1010u;  // bytes (u0, u0+1) of sc12[8..11], twice
+    const bool hi4 = c >= 2;
+    const int col = g % NCOL;  // columns beyond 2M repeat real ones (finite, never stored)
+    const int mrow = c;        // activation row whose two terms sit in this lane's columns
+    const int minv = mrow < M ? mrow : 0;
+    const uint8_t *rowA = ring + g * 144;
+    float *mypart = part + size_t(warp) * 2 * 4 * kTileRows;
+    float tot0 = 0.f, tot1 = 0.f;
+    Cursor q = cursor_at(P, u0);
+    int slot = 0;
+    unsigned parity = 0;
+    int jfail = -1;
+
+    for (int j = 0; j < nu; ++j) {
+        if (!mbar_wait_bounded(&bar[slot], parity)) {
+            jfail = j;
+            break;
+        }
+        const uint8_t *tp = rowA + slot * kTileBytes;
+        const uint4 h0 = *reinterpret_cast<const uint4 *>(tp);
+        const uint4 h1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144);
+        const uint4 qa0 = *reinterpret_cast<const uint4 *>(tp + 16 + 32 * c);
+        const uint4 qa1 = *reinterpret_cast<const uint4 *>(tp + 32 + 32 * c);
+        const uint4 qb0 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 16 + 32 * c);
+        const uint4 qb1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 32 + 32 * c);
+        const RowScales r0 = row_scales(h0, selA, selB, hi4);
+        const RowScales r1 = row_scales(h1, selA, selB, hi4);
+        const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+        const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+        const uint2 *bsb = Bs + (size_t(q.sb) * 16 * NCOL + col) * 4 + c;
+        const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+        float dq0[4], dq1[4];  // two independent accumulation chains (even / odd k-steps)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t xa = e ? (wa[t] >> 8) : wa[t];
+                const uint32_t xb = e ? (wb[t] >> 8) : wb[t];
+                const uint32_t a0 = hfma2(and_or(xa, mlo, magic), r0.SL, r0.CL);
+                const uint32_t a1 = hfma2(and_or(xb, mlo, magic), r1.SL, r1.CL);
+                const uint32_t a2 = hfma2(and_or(xa, mhi, magic), r0.SH, r0.CH);
+                const uint32_t a3 = hfma2(and_or(xb, mhi, magic), r1.SH, r1.CH);
+                const uint2 b = bsb[(2 * t + e) * NCOL * 4];
+                float(&dq)[4] = e ? dq1 : dq0;
+                if (t == 0)
+                    mma16816_zero(dq, a0, a1, a2, a3, b.x, b.y);
+                else
+                    mma16816(dq, a0, a1, a2, a3, b.x, b.y);
+            }
+        }
+        const uint32_t bm = Bm[(size_t(q.sb) * NCOL + col) * 4 + c];
+        float dm[4];
+        mma16816_zero(dm, r0.Am, r1.Am, 0u, 0u, bm, bm);
+        const float sc = inv[q.sb * M + minv];
+        tot0 = fmaf(fmaf(r0.d, (dq0[0] + dq1[0]) + (dq0[1] + dq1[1]),
+                         -(r0.dmin * ((dm[0] + dm[1]) * 32.f))), sc, tot0);
+        tot1 = fmaf(fmaf(r1.d, (dq0[2] + dq1[2]) + (dq0[3] + dq1[3]),
+                         -(r1.dmin * ((dm[2] + dm[3]) * 32.f))), sc, tot1);
+
+        // Refill this slot with the unit NS ahead: every lane has consumed its
+        // loads of the slot (the values fed the MMAs above), so the copy may
+        // overwrite it.
+        __syncwarp();
+        if (issued < nu) {
+            if (lane == 0)
+                issue();
+            ++issued;
+        }
+        if (++slot == NS) {
+            slot = 0;
+            parity ^= 1u;
+        }
+
+        // ---- the tile ends here (or this warp's share does)
+        if (q.sb == NB - 1 || j == nu - 1) {
+            const int64_t first = int64_t(q.tile) * NB, last = first + NB - 1;
+            if (u0 <= first && u1 - 1 >= last) {
+                if (mrow < M) {
+                    const int64_t rA = int64_t(q.tile - q.tbase) * kTileRows + g;
+                    float *yr = P.y[q.mat] + int64_t(mrow) * P.ldy;
+                    if (rA < P.rows[q.mat])
+                        yr[rA] = tot0;
+                    if (rA + 8 < P.rows[q.mat])
+                        yr[rA + 8] = tot1;
+                }
+            } else {
+                // Shared with other warps: park this warp's share in shared memory.
+                const int k = (u0 >= int64_t(q.tile) * NB) ? 0 : 1;  // first or last tile of this warp
+                mypart[(k * 4 + mrow) * kTileRows + g] = tot0;
+                mypart[(k * 4 + mrow) * kTileRows + g + 8] = tot1;
+            }
+            tot0 = tot1 = 0.f;
+        }
+        advance(P, q);
+    }
+    if (jfail >= 0) {
+        if (lane == 0)
+            atomicOr(P.status, kStatusTimeoutBit);
+        // Let this warp's copies in flight (units jfail .. issued-1) land
+        // before shared memory is released.
+        if (lane == 0)
+            for (int j = jfail; j < issued; ++j)
+                mbar_wait_bounded(&bar[j % NS], unsigned(j / NS) & 1u, 100000000ll);
+    }
+    if (P.late_trigger)
+        pdl_launch_dependents();
+    __syncthreads();
+
+    // ---- tiles no single warp covered: add the warps' shares in warp order.
+    // Units are counted from the CTA's first one here (32-bit, no divisions
+    // inside the loops); warp w owns [wb[w], wb[w+1]).
+    const int cm = lane >> 3, cr = lane & 7;  // this lane: x row cm, rows cr and cr+8
+    const int ntile = int(cn / NB);
+    for (int tr = warp; tr < ntile; tr += nw) {
+        const int first = tr * NB, last = first + NB - 1;
+        int wf = 0, wl = 0;
+        for (int w = 0; w < nw; ++w) {
+            const int b0 = wbeg[w];
+            if (b0 <= first)
+                wf = w;
+            if (b0 <= last)
+                wl = w;
+        }
+        if (wf == wl)
+            continue;  // written by its warp
+        float s0 = 0.f, s1 = 0.f;
+        for (int w = wf; w <= wl; ++w) {
+            const int b0 = wbeg[w], b1 = wbeg[w + 1];
+            if (b1 == b0)
+                continue;  // a warp without units
+            const int kw = (b0 >= first) ? 0 : 1;  // this tile is w's first (0) or last (1)
+            const float *pw = part + (size_t(w) * 2 + kw) * 4 * kTileRows + cm * kTileRows;
+            s0 += pw[cr];
+            s1 += pw[cr + 8];
+        }
+        if (cm < M) {
+            const int64_t t = cU0 / NB + tr;
+            const int mi = matrix_of_tile(P, t);
+            const int64_t rA = (t - (mi == 0 ? 0 : P.tile_end[mi - 1])) * kTileRows + cr;
+            float *yr = P.y[mi] + int64_t(cm) * P.ldy;
+            if (rA < P.rows[mi])
+                yr[rA] = s0;
+            if (rA + 8 < P.rows[mi])
+                yr[rA + 8] = s1;
+        }
+    }
+}
+
+using TcKernel = void (*)(TcParams);
+
+TcKernel pick_tc(int ncol)
+{
+    switch (ncol) {
+    case 2: return gemv_tc_kernel<2>;
+    case 4: return gemv_tc_kernel<4>;
+    case 6: return gemv_tc_kernel<6>;
+    default: return gemv_tc_kernel<8>;
+    }
+}
+
+} // namespace
+
+// Warps per CTA and ring depth: 16 warps x 3 slots when every CTA has at
+// least 64 units (long launches want latency hiding), else 8 x 4 (the
+// smaller footprint leaves room for the next kernel's CTA to start early).
+// QMM_TC_WARPS / QMM_TC_NSLOT override.
+void gemv_tc_shape(int64_t units_per_cta, int &warps, int &nslot)
+{
+    const bool big = units_per_cta >= 64;
+    warps = big ? 16 : 8;
+    nslot = big ? 3 : 4;
+    const char *e = getenv("QMM_TC_WARPS");
+    if (e && atoi(e) >= 4 && atoi(e) <= 16)
+        warps = atoi(e);
+    const char *n = getenv("QMM_TC_NSLOT");
+    if (n && atoi(n) >= 2 && atoi(n) <= 16)
+        nslot = atoi(n);
+}
+
+size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw)
+{
+    const int64_t NB = K / 256;
+    const int ncol = 2 * M;
+    return size_t(nw) * nslot * kTileBytes + size_t(NB) * 16 * ncol * 4 * 8 +
+           size_t(NB) * ncol * 4 * 4 + size_t(NB) * M * 4 + size_t(nw) * 2 * 4 * kTileRows * 4 + 8 +
+           size_t(nw) * nslot * 8;
+}
+
+size_t gemv_tc_ws_floats(int sm_count) { return size_t(sm_count) * 2 * 4 * kTileRows; }
+
+cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
+{
+    TcParams P;
+    memset(&P, 0, sizeof(P));
+    int64_t tiles = 0;
+    for (int i = 0; i < a.nmat; ++i) {
+        P.tmap[i] = *reinterpret_cast<const CUtensorMap *>(a.tmap[i]);
+        tiles += (a.rows[i] + kTileRows - 1) / kTileRows;
+        P.tile_end[i] = tiles;
+        P.rows[i] = a.rows[i];
+        P.y[i] = a.y[i];
+    }
+    for (int i = a.nmat; i < kMaxGroup; ++i)
+        P.tile_end[i] = tiles;
+    P.x = a.x;
+    P.ws = a.ws;
+    P.tickets = a.tickets;
+    P.status = a.status;
+    P.NB = int(a.K / 256);
+    P.U = tiles * P.NB;
+    P.ldx = a.ldx;
+    P.ldy = a.ldy;
+    P.nmat = a.nmat;
+    P.M = a.M;
+    const char *lt = getenv("QMM_PDL_TRIGGER");
+    P.late_trigger = (lt && strcmp(lt, "late") == 0) ? 1 : 0;
+    int64_t ctas = sm_count;
+    if (ctas > tiles)
+        ctas = tiles;  // every CTA owns at least one row tile
+    P.W = int(ctas);
+    int nw, nslot;
+    gemv_tc_shape(P.U / ctas, nw, nslot);
+    P.nslot = nslot;
+    const size_t smem = gemv_tc_smem(a.K, a.M, nslot, nw);
+    TcKernel kern = pick_tc(2 * a.M);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(ctas));
+    cfg.blockDim = dim3(unsigned(nw * 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// Describe the rows of a Q4_K matrix as a 2-D tensor of 8-byte elements
+// (row_bytes/8 x N) whose boxes are one super-block column of 16 rows.
+int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return -1;
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const cuuint64_t dims[2] = {cuuint64_t(row_bytes / 8), cuuint64_t(N)};
+    const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+    const cuuint32_t box[2] = {18u, cuuint32_t(kTileRows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = encode(reinterpret_cast<CUtensorMap *>(out128), CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+                        const_cast<void *>(w), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+} // namespace qmm

@@ -59,10 +59,64 @@ int env_int(const char *name)
     return v ? atoi(v) : 0;
 }
 
+constexpr size_t kMaxSmem = 227 * 1024;
+
+// Q4_K on the tensor cores for M activation rows (1..4) when the activations
+// of this K fit in shared memory (with the largest CTA shape).  For a single
+// activation row and a very long K the fp32 kernel is faster (the tensor-core
+// kernel re-lays all of x out in every CTA first).  QMM_Q4K_PATH = "simt" or
+// "tc" forces a path.
+bool tc_fits(const Matrix &m0, int M)
+{
+    const char *path = getenv("QMM_Q4K_PATH");
+    if (path && strcmp(path, "simt") == 0)
+        return false;
+    if (!m0.has_tmap || M < 1 || M > 4 || qmm::gemv_tc_smem(m0.K, M, 3, 16) > kMaxSmem)
+        return false;
+    if (path && strcmp(path, "tc") == 0)
+        return true;
+    return !(M == 1 && m0.K > 8192);
+}
+
+qmm_status do_gemv_tc(const qmm_t *hs, int n, const float *x, int64_t ldx, int M, float *const *ys,
+                      int64_t ldy, cudaStream_t s, const char *fn)
+{
+    const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    qmm::TcArgs a;
+    memset(&a, 0, sizeof(a));
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
+        a.tmap[i] = mi.tmap;
+        a.rows[i] = mi.N;
+        a.y[i] = ys[i];
+        tiles += (mi.N + 15) / 16;
+    }
+    if (size_t(tiles) > m0.tc_tickets_n)
+        return fail(QMM_ERR_NOMEM, "%s: %lld row tiles exceed handle 0's ticket array (%zu)", fn,
+                    (long long)tiles, m0.tc_tickets_n);
+    a.nmat = n;
+    a.K = m0.K;
+    a.M = M;
+    a.ldx = ldx;
+    a.ldy = ldy;
+    a.x = x;
+    a.ws = m0.tc_ws;
+    a.tickets = m0.tc_tickets;
+    a.status = m0.status;
+    cudaError_t e = qmm::launch_gemv_tc(a, m0.sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+    return QMM_OK;
+}
+
 qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    if (m0.fmt == QMM_Q4_K && tc_fits(m0, 1))
+        return do_gemv_tc(hs, n, x, m0.K, 1, ys, 0, s, fn);
     qmm::GemvArgs a;
     memset(&a, 0, sizeof(a));
     a.fmt = m0.fmt;
@@ -151,8 +205,19 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
     }
     m->ws_floats = size_t(8) * size_t(N) + 1024;
     m->n_tickets = size_t(m->sm_count) * 4;
+    if (fmt == QMM_Q4_K) {
+        if (qmm::make_q4k_tensor_map(m->tmap, w_dev, N, m->row_bytes) != 0) {
+            delete m;
+            return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor map for the weight rows could "
+                                      "not be encoded (driver entry point or arguments refused)");
+        }
+        m->has_tmap = true;
+        m->tc_ws_floats = qmm::gemv_tc_ws_floats(m->sm_count);
+        m->tc_tickets_n = size_t(N > 32768 ? N : 32768) / 16 + 64;
+    }
     void *p = nullptr;
-    const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256;
+    const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256 + m->tc_ws_floats * 4 +
+                         m->tc_tickets_n * 4;
     e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess) {
         delete m;
@@ -168,6 +233,8 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
     m->ws = static_cast<float *>(p);
     m->tickets = reinterpret_cast<unsigned *>(m->ws + m->ws_floats);
     m->status = m->tickets + m->n_tickets;
+    m->tc_ws = reinterpret_cast<float *>(m->status + 64);
+    m->tc_tickets = reinterpret_cast<unsigned *>(m->tc_ws + m->tc_ws_floats);
     *out = reinterpret_cast<qmm_t>(m);
     return QMM_OK;
 }
@@ -244,8 +311,42 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
                             int64_t ldy, qmm_stream stream)
 {
     g_err.clear();
-    (void)h; (void)X; (void)M; (void)ldx; (void)Y; (void)ldy; (void)stream;
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_gemv_batched: not implemented in this build");
+    qmm_status st = check_handle(h, "qmm_gemv_batched");
+    if (st != QMM_OK)
+        return st;
+    const Matrix &m = *reinterpret_cast<const Matrix *>(h);
+    if (!X || !Y)
+        return fail(QMM_ERR_NULL, "qmm_gemv_batched: %s is NULL", !X ? "X" : "Y");
+    if (M < 1 || M > 16)
+        return fail(QMM_ERR_SHAPE, "qmm_gemv_batched: M = %lld; 1 <= M <= 16 is supported",
+                    (long long)M);
+    if (ldx < m.K || ldy < m.N)
+        return fail(QMM_ERR_SHAPE, "qmm_gemv_batched: ldx = %lld < K = %lld or ldy = %lld < N = %lld",
+                    (long long)ldx, (long long)m.K, (long long)ldy, (long long)m.N);
+    if (ldx % 4 || !aligned(X, 16))
+        return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: X rows must start 16-byte aligned "
+                                   "(X aligned and ldx a multiple of 4)");
+    if (!aligned(Y, 4))
+        return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Up to four activation rows share one pass over the weights; larger
+    // batches take ceil(M/4) passes.
+    for (int64_t m0 = 0; m0 < M;) {
+        int mc = int(M - m0 < 4 ? M - m0 : 4);
+        while (mc > 1 && !tc_fits(m, mc))
+            --mc;
+        float *yrow = Y + m0 * ldy;
+        if (m.fmt == QMM_Q4_K && tc_fits(m, mc)) {
+            st = do_gemv_tc(&h, 1, X + m0 * ldx, ldx, mc, &yrow, ldy, s, "qmm_gemv_batched");
+        } else {
+            mc = 1;
+            st = do_gemv(&h, 1, X + m0 * ldx, &yrow, s, "qmm_gemv_batched");
+        }
+        if (st != QMM_OK)
+            return st;
+        m0 += mc;
+    }
+    return QMM_OK;
 }
 
 qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, int32_t T,

@@ -45,6 +45,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
 {
     uint32_t ok;
@@ -58,6 +63,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep (up to the hint,
+// in ns) until the phase completes instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier, giving up after `budget` cycles.
 // Returns false on timeout (the caller records it and winds down).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity,
@@ -66,11 +86,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity
     if (mbar_try_wait(bar, parity))
         return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_sleep(bar, parity))
+                return true;
         if (clock64() - t0 > budget)
             return false;
     }
-    return true;
 }
 
 // ----------------------------------------------------------------- bulk copy

@@ -4,9 +4,10 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
-#include "../../include/qmm.h"
+#include "qmm.h"
 
 namespace qmm {
 
@@ -28,6 +29,14 @@ struct Matrix {
     unsigned *tickets = nullptr;
     size_t n_tickets = 0;
     unsigned *status = nullptr;
+    // Q4_K tensor-core path: 2-D tensor map over the rows (a CUtensorMap),
+    // stream-K partial sums and per-tile tickets
+    alignas(64) unsigned char tmap[128];
+    bool has_tmap = false;
+    float *tc_ws = nullptr;
+    size_t tc_ws_floats = 0;
+    unsigned *tc_tickets = nullptr;
+    size_t tc_tickets_n = 0;
     // expert-layer scratch (allocated on first qmm_moe_* call)
     void *moe_ws = nullptr;
     size_t moe_ws_bytes = 0;
@@ -40,6 +49,13 @@ inline int64_t row_bytes_of(int fmt, int64_t K)
     return fmt == QMM_Q4_K ? (K / 256) * 144 : (K / 32) * 34;
 }
 
+// Programmatic dependent launch on every kernel unless QMM_PDL=0.
+inline bool pdl_enabled()
+{
+    const char *e = getenv("QMM_PDL");
+    return !(e && e[0] == '0');
+}
+
 // --------------------------------------------------------------- GEMV plan
 // A CTA owns a contiguous range of rows (balanced to within one row) and one
 // K-slice of `kchunks` 64-weight chunks.  Its threads form `rg` row teams of
@@ -50,7 +66,7 @@ struct GemvPlan {
     int kchunks = 0;      // chunks (64 weights) per K-slice = team size
     int ksplit = 1;       // number of K-slices
     int rg = 0;           // row teams per CTA
-    int rpg = 0;          // rows per team per stage
+    int rpg = 0;          // rows per team per stage (1, 2 or 4)
     int stage_rows = 0;   // rg * rpg
     int stages = 0;       // ring depth
     int threads = 0;      // rg * kchunks
@@ -78,6 +94,25 @@ struct GemvArgs {
 GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit);
 size_t gemv_workspace_floats(const GemvPlan &p, int64_t N);
 cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
+
+// --------------------------------------------------------------- tensor-core Q4_K GEMV
+struct TcArgs {
+    const void *tmap[kMaxGroup];  // 128-byte CUtensorMap of each matrix
+    int64_t rows[kMaxGroup];
+    float *y[kMaxGroup];
+    int nmat;
+    int64_t K;
+    int M;                // activation rows, 1..4
+    int64_t ldx, ldy;     // row strides of X and Y (elements)
+    const float *x;
+    float *ws;
+    unsigned *tickets;
+    unsigned *status;
+};
+size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw);
+size_t gemv_tc_ws_floats(int sm_count);
+cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
+int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
 // --------------------------------------------------------------- dequant
 cudaError_t launch_dequant(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,

@@ -85,6 +85,8 @@ def test_gemv_small(fmt, N, K):
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ksplit", [2, 4])
 def test_gemv_forced_split_k(fmt, ksplit, monkeypatch):
+    # split-K lives in the fp32 kernel (Q8_0, and Q4_K when asked for it)
+    monkeypatch.setenv("QMM_Q4K_PATH", "simt")
     monkeypatch.setenv("QMM_SPLITK", str(ksplit))
     for N, K in ((37, 2048), (300, 4096)):
         m, *_ = _check_gemv(fmt, N, K, seed=ksplit * 100 + N)
@@ -191,3 +193,55 @@ def test_gemv_refusals_on_device():
     assert e.value.status == q.ERR_SHAPE and "differs from matrix 0" in e.value.message
     m.close()
     m8.close()
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (17, 512), (1000, 4096), (4096, 1024), (300, 14336)])
+def test_gemv_q4k_fp32_kernel(N, K, monkeypatch):
+    """The fp32 (SIMT) Q4_K kernel, kept for K whose activations exceed the
+    tensor-core kernel's shared memory."""
+    monkeypatch.setenv("QMM_Q4K_PATH", "simt")
+    m, *_ = _check_gemv(q.Q4_K, N, K, seed=N * 3 + K)
+    m.close()
+
+
+@pytest.mark.parametrize("nslot,warps", [("2", "8"), ("3", "16"), ("6", "8"), ("4", "12")])
+def test_gemv_q4k_tensor_core_shapes(nslot, warps, monkeypatch):
+    """The tensor-core kernel with other ring depths / CTA sizes, and on a
+    long K where the fp32 kernel would normally be chosen."""
+    monkeypatch.setenv("QMM_Q4K_PATH", "tc")
+    monkeypatch.setenv("QMM_TC_NSLOT", nslot)
+    monkeypatch.setenv("QMM_TC_WARPS", warps)
+    for N, K in ((2048, 4096), (77, 14336), (1, 256), (40, 768)):
+        m, *_ = _check_gemv(q.Q4_K, N, K, seed=int(nslot) * 10 + N)
+        m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 16])
+def test_gemv_batched(fmt, M):
+    N, K = 1000, 4096
+    w, m = _matrix(fmt, N, K, seed=70 + M)
+    X = synth.activations(M, K, seed=71 + M)
+    Y = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Yr, C = oracle.gemv(fmt, w, N, K, X, nthreads=oracle.max_threads())
+    assert_close_to_oracle(Y, Yr, C, TOL_FP32, f"batched fmt={fmt} M={M}")
+    # row m of the batch equals the single-vector GEMV of row m
+    for r in (0, M - 1):
+        y1 = m.gemv(to_dev(X[r])).cpu().numpy()
+        assert_close_to_oracle(y1, Yr[r], C[r], TOL_FP32, "batched row")
+    m.close()
+
+
+def test_gemv_batched_strided_and_big_k():
+    N, K, M = 333, 14336, 4
+    w, m = _matrix(q.Q4_K, N, K, seed=90)
+    X = synth.activations(M, K + 64, seed=91)  # ldx = K + 64
+    Xd = to_dev(X)
+    Yd = torch.full((M, N + 8), 7.0, dtype=torch.float32, device="cuda")
+    q.gemv_batched(m.h, Xd, M, K + 64, Yd, N + 8)
+    Y = Yd.cpu().numpy()
+    assert np.all(Y[:, N:] == 7.0)
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, np.ascontiguousarray(X[:, :K]),
+                        nthreads=oracle.max_threads())
+    assert_close_to_oracle(Y[:, :N], Yr, C, TOL_FP32, "batched strided")
+    m.close()
