@@ -161,6 +161,27 @@ QMM_API qmm_status qmm_dequantize(qmm_t h, int64_t row0, int64_t nrows, float *o
 QMM_API qmm_status qmm_dequantize_bf16(qmm_t h, int64_t row0, int64_t nrows,
                                uint16_t *out, qmm_stream stream);
 
+/* Decode GEMV that allocates nothing, for callers that cannot call
+ * cudaMalloc (code running inside a fixed memory pool, a driver-managed
+ * allocator or a plug-in that must not grow the process's device footprint).
+ * The pages have no counterpart: it is this library's addition.
+ *
+ * Computes y[n] = sum_k w[n][k] * x[k] like qmm_gemv, but takes the matrix
+ * description directly (fmt, N, K, w_dev as in qmm_create) instead of a
+ * handle, and keeps its split-K scratch -- partial sums, tickets and a status
+ * word -- in one 1 MiB device array inside the library image (held by every
+ * GPU that loads the library until the process exits).  No cudaMalloc,
+ * cudaFree or other allocating call is made.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress); make it
+ * before any stream capture.  Each call clears the tickets and status word on
+ * `stream` before launching.  All calls share the one array: calls whose
+ * work can overlap on the GPU (different streams, or concurrent host threads)
+ * race and must be serialised by the caller.  Shapes whose split-K scratch
+ * exceeds the array are refused (QMM_ERR_SHAPE) with the sizes named.
+ * Device-side faults are not reported (there is no handle status word). */
+QMM_API qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
+                                    const float *x, float *y, qmm_stream stream);
+
 /* Read and clear the handle's device status word (synchronises the handle's
  * last stream first).  QMM_OK when no device-side fault was recorded. */
 QMM_API qmm_status qmm_get_status(qmm_t h);

@@ -31,6 +31,7 @@ ENTRY_POINTS = (
     "qmm_create", "qmm_destroy", "qmm_gemv", "qmm_gemv_group", "qmm_gemv_batched",
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
+    "qmm_gemv_noalloc",
 )
 
 
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "qmm_get_status": [vp],
             "qmm_last_error": [],
             "qmm_version": [],
+            "qmm_gemv_noalloc": [i32, i64, i64, vp, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -163,6 +165,12 @@ def dequantize(h: int, row0: int, nrows: int, out, stream=None):
 def dequantize_bf16(h: int, row0: int, nrows: int, out, stream=None):
     _check(lib().qmm_dequantize_bf16(ctypes.c_void_p(h), row0, nrows, _ptr(out),
                                      _stream(stream)))
+
+
+def gemv_noalloc(fmt: int, N: int, K: int, w, x, y, stream=None):
+    """qmm_gemv_noalloc: the decode GEMV without a handle or any device
+    allocation (scratch lives in a fixed array inside the library)."""
+    _check(lib().qmm_gemv_noalloc(fmt, N, K, _ptr(w), _ptr(x), _ptr(y), _stream(stream)))
 
 
 def get_status(h: int) -> int:

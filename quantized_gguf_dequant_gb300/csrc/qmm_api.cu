@@ -157,6 +157,45 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
 
 } // namespace
 
+namespace qmm {
+
+qmm_status noalloc_fail(qmm_status code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+qmm_status noalloc_check(int fmt, int64_t N, int64_t K, const void *w, const float *x,
+                         const float *y)
+{
+    g_err.clear();
+    if (!w || !x || !y)
+        return fail(QMM_ERR_NULL, "qmm_gemv_noalloc: %s is NULL", !w ? "the weight pointer"
+                                                                 : (!x ? "x" : "y"));
+    if (fmt != QMM_Q4_K && fmt != QMM_Q8_0)
+        return fail(QMM_ERR_FORMAT,
+                    "qmm_gemv_noalloc: format %d is not supported (Q4_K = 12 and Q8_0 = 8 are)",
+                    fmt);
+    if (N < 1)
+        return fail(QMM_ERR_SHAPE, "qmm_gemv_noalloc: N = %lld rows; at least one row is needed",
+                    (long long)N);
+    if (K < 256 || K % 256 != 0 || K > (int64_t(1) << 20))
+        return fail(QMM_ERR_SHAPE,
+                    "qmm_gemv_noalloc: K = %lld is not a multiple of 256 in [256, 1048576]",
+                    (long long)K);
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4))
+        return fail(QMM_ERR_ALIGN, "qmm_gemv_noalloc: the weights and x must be 16-byte aligned "
+                                   "and y 4-byte aligned");
+    return QMM_OK;
+}
+
+} // namespace qmm
+
 extern "C" {
 
 const char *qmm_last_error(void) { return g_err.c_str(); }

@@ -114,6 +114,13 @@ size_t gemv_tc_ws_floats(int sm_count);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
+// --------------------------------------------------------------- no-allocation entry
+// Argument checks of qmm_gemv_noalloc, and recording its refusal sentence for
+// qmm_last_error().
+qmm_status noalloc_check(int fmt, int64_t N, int64_t K, const void *w, const float *x,
+                         const float *y);
+qmm_status noalloc_fail(qmm_status code, const char *fmt, ...);
+
 // --------------------------------------------------------------- dequant
 cudaError_t launch_dequant(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,
                            uint16_t *out_bf16, cudaStream_t s);
