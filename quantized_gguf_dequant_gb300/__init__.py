@@ -137,10 +137,10 @@ def gemv_batched(h: int, X, M: int, ldx: int, Y, ldy: int, stream=None):
                                   _stream(stream)))
 
 
-def moe_gemv(h: int, n_experts: int, ids, T: int, top_k: int, X, x_per_slot: bool,
+def moe_gemv(h: int, n_experts: int, ids, T: int, top_k: int, X, x_per_slot: int,
              route_w, Y, stream=None):
     _check(lib().qmm_moe_gemv(ctypes.c_void_p(h), n_experts, _ptr(ids), T, top_k, _ptr(X),
-                              1 if x_per_slot else 0, _ptr(route_w), _ptr(Y), _stream(stream)))
+                              int(x_per_slot), _ptr(route_w), _ptr(Y), _stream(stream)))
 
 
 def swiglu(g, u, hout, n: int, stream=None):

@@ -155,6 +155,92 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
     return QMM_OK;
 }
 
+// ------------------------------------------------------------------ experts
+
+// Checks shared by the expert entry points, for one stacked handle.
+qmm_status moe_check(const Matrix &m, int n_experts, const int32_t *ids, int T, int top_k,
+                     const char *fn)
+{
+    if (m.fmt != QMM_Q4_K)
+        return fail(QMM_ERR_UNSUPPORTED,
+                    "%s: the expert GEMV is implemented for Q4_K weights only (this handle is "
+                    "format %d)", fn, m.fmt);
+    if (!ids)
+        return fail(QMM_ERR_NULL, "%s: expert_ids is NULL", fn);
+    if (n_experts < 1 || n_experts > qmm::kMoeMaxExperts)
+        return fail(QMM_ERR_SHAPE, "%s: n_experts = %d; 1 <= n_experts <= %d is supported", fn,
+                    n_experts, qmm::kMoeMaxExperts);
+    if (m.N % n_experts != 0)
+        return fail(QMM_ERR_SHAPE, "%s: the handle's %lld rows do not split into %d equal experts",
+                    fn, (long long)m.N, n_experts);
+    if (top_k < 1 || top_k > qmm::kMoeMaxTopK)
+        return fail(QMM_ERR_SHAPE, "%s: top_k = %d; 1 <= top_k <= %d is supported", fn, top_k,
+                    qmm::kMoeMaxTopK);
+    if (T < 1 || int64_t(T) * top_k > qmm::kMoeMaxSlots)
+        return fail(QMM_ERR_SHAPE, "%s: T = %d tokens x top_k = %d; 1 <= T*top_k <= %d is "
+                    "supported", fn, T, top_k, qmm::kMoeMaxSlots);
+    if (!aligned(ids, 4))
+        return fail(QMM_ERR_ALIGN, "%s: expert_ids is not 4-byte aligned", fn);
+    int nw, nslot;
+    qmm::moe_expert_shape(m.K, nw, nslot);
+    if (qmm::moe_expert_smem(m.K, nw, nslot) > kMaxSmem)
+        return fail(QMM_ERR_SHAPE, "%s: K = %lld is too long for the expert kernel's shared "
+                    "memory (%zu bytes needed)", fn, (long long)m.K,
+                    qmm::moe_expert_smem(m.K, nw, nslot));
+    return QMM_OK;
+}
+
+struct MoeScratch {
+    qmm::MoeIndex ix;
+    float *ys, *g, *u, *h;
+};
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// The handle's expert scratch: the bucketing tables, ys_floats per-slot
+// outputs and, for the FFN, three [S][d_ff] intermediates (ff_floats each).
+// It grows when a call needs more; growing waits for the device first.
+qmm_status moe_scratch(Matrix &m, int S, int E, size_t ys_floats, size_t ff_floats,
+                       const char *fn, MoeScratch &out)
+{
+    const size_t o_groups = 0;
+    const size_t o_slots = o_groups + round256(qmm::moe_max_groups(S, E) * sizeof(int4));
+    const size_t o_ng = o_slots + round256(size_t(S) * sizeof(int));
+    const size_t o_ys = o_ng + 256;
+    const size_t o_g = o_ys + round256(ys_floats * 4);
+    const size_t o_u = o_g + round256(ff_floats * 4);
+    const size_t o_h = o_u + round256(ff_floats * 4);
+    const size_t total = o_h + round256(ff_floats * 4);
+    if (total > m.moe_ws_bytes) {
+        cudaError_t e = cudaSuccess;
+        if (m.moe_ws) {
+            e = cudaDeviceSynchronize();
+            if (e == cudaSuccess)
+                e = cudaFree(m.moe_ws);
+            m.moe_ws = nullptr;
+            m.moe_ws_bytes = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e, fn);
+        }
+        void *p = nullptr;
+        e = cudaMalloc(&p, total);
+        if (e != cudaSuccess)
+            return fail(QMM_ERR_NOMEM, "%s: could not allocate %zu bytes of expert scratch (%s)",
+                        fn, total, cudaGetErrorString(e));
+        m.moe_ws = p;
+        m.moe_ws_bytes = total;
+    }
+    unsigned char *b = static_cast<unsigned char *>(m.moe_ws);
+    out.ix.groups = reinterpret_cast<int4 *>(b + o_groups);
+    out.ix.slots = reinterpret_cast<int *>(b + o_slots);
+    out.ix.n_groups = reinterpret_cast<int *>(b + o_ng);
+    out.ys = reinterpret_cast<float *>(b + o_ys);
+    out.g = reinterpret_cast<float *>(b + o_g);
+    out.u = reinterpret_cast<float *>(b + o_u);
+    out.h = reinterpret_cast<float *>(b + o_h);
+    return QMM_OK;
+}
+
 } // namespace
 
 namespace qmm {
@@ -393,16 +479,77 @@ qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, i
                         const float *route_w, float *Y, qmm_stream stream)
 {
     g_err.clear();
-    (void)h; (void)n_experts; (void)expert_ids; (void)T; (void)top_k; (void)X;
-    (void)x_per_slot; (void)route_w; (void)Y; (void)stream;
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_moe_gemv: not implemented in this build");
+    const char *fn = "qmm_moe_gemv";
+    qmm_status st = check_handle(h, fn);
+    if (st != QMM_OK)
+        return st;
+    Matrix *m = reinterpret_cast<Matrix *>(h);
+    st = moe_check(*m, n_experts, expert_ids, T, top_k, fn);
+    if (st != QMM_OK)
+        return st;
+    if (!X || !Y)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X ? "X" : "Y");
+    if (x_per_slot != 0 && x_per_slot != 1)
+        return fail(QMM_ERR_SHAPE, "%s: x_per_slot = %d; it must be 0 or 1", fn, x_per_slot);
+    if (!aligned(X, 16))
+        return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
+    if (!aligned(Y, 4) || (route_w && !aligned(route_w, 4)))
+        return fail(QMM_ERR_ALIGN, "%s: %s is not 4-byte aligned", fn, !aligned(Y, 4) ? "Y" : "route_w");
+    const int S = T * top_k;
+    const int64_t Ne = m->N / n_experts;
+    MoeScratch ms;
+    st = moe_scratch(*m, S, n_experts, route_w ? size_t(S) * Ne : 0, 0, fn, ms);
+    if (st != QMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = qmm::launch_moe_bucket(expert_ids, S, n_experts, ms.ix, route_w ? nullptr : Y,
+                                           Ne, Ne, m->status, s);
+    if (e == cudaSuccess) {
+        qmm::MoeExpertArgs a;
+        memset(&a, 0, sizeof(a));
+        a.tmap[0] = m->tmap;
+        a.y[0] = route_w ? ms.ys : Y;
+        a.nmat = 1;
+        a.Ne = Ne;
+        a.K = m->K;
+        a.x = X;
+        a.ldx = m->K;
+        a.top_k = top_k;
+        a.x_per_slot = x_per_slot;
+        a.ix = ms.ix;
+        a.status = m->status;
+        e = qmm::launch_moe_expert(a, m->sm_count, s);
+    }
+    if (e == cudaSuccess && route_w)
+        e = qmm::launch_moe_combine(ms.ys, route_w, expert_ids, n_experts, T, top_k, Ne, Y,
+                                    m->sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    m->last_stream = s;
+    return QMM_OK;
 }
 
 qmm_status qmm_swiglu(const float *g, const float *u, float *hh, int64_t n, qmm_stream stream)
 {
     g_err.clear();
-    (void)g; (void)u; (void)hh; (void)n; (void)stream;
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_swiglu: not implemented in this build");
+    const char *fn = "qmm_swiglu";
+    if (!g || !u || !hh)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !g ? "g" : (!u ? "u" : "h"));
+    if (n < 0)
+        return fail(QMM_ERR_SHAPE, "%s: n = %lld is negative", fn, (long long)n);
+    if (!aligned(g, 4) || !aligned(u, 4) || !aligned(hh, 4))
+        return fail(QMM_ERR_ALIGN, "%s: g, u and h must be 4-byte aligned", fn);
+    if (n == 0)
+        return QMM_OK;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = qmm::launch_swiglu(g, u, hh, n, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    return QMM_OK;
 }
 
 qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
@@ -410,9 +557,87 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
                        const float *route_w, float *Y, qmm_stream stream)
 {
     g_err.clear();
-    (void)hg; (void)hu; (void)hd; (void)n_experts; (void)expert_ids; (void)T; (void)top_k;
-    (void)X; (void)route_w; (void)Y; (void)stream;
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_moe_ffn: not implemented in this build");
+    const char *fn = "qmm_moe_ffn";
+    qmm_status st = check_handle(hg, fn);
+    if (st == QMM_OK)
+        st = check_handle(hu, fn);
+    if (st == QMM_OK)
+        st = check_handle(hd, fn);
+    if (st != QMM_OK)
+        return st;
+    Matrix *mg = reinterpret_cast<Matrix *>(hg);
+    const Matrix *mu = reinterpret_cast<const Matrix *>(hu);
+    const Matrix *md = reinterpret_cast<const Matrix *>(hd);
+    st = moe_check(*mg, n_experts, expert_ids, T, top_k, fn);
+    if (st == QMM_OK)
+        st = moe_check(*mu, n_experts, expert_ids, T, top_k, fn);
+    if (st == QMM_OK)
+        st = moe_check(*md, n_experts, expert_ids, T, top_k, fn);
+    if (st != QMM_OK)
+        return st;
+    const int64_t d_ff = mg->N / n_experts, d_model = mg->K;
+    if (mu->N != mg->N || mu->K != mg->K || md->K != d_ff || md->N != int64_t(n_experts) * d_model)
+        return fail(QMM_ERR_SHAPE,
+                    "%s: shapes disagree: gate %lld x %lld, up %lld x %lld, down %lld x %lld; "
+                    "with %d experts gate and up must be (E*d_ff) x d_model and down "
+                    "(E*d_model) x d_ff",
+                    fn, (long long)mg->N, (long long)mg->K, (long long)mu->N, (long long)mu->K,
+                    (long long)md->N, (long long)md->K, n_experts);
+    if (!X || !Y || !route_w)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X ? "X" : (!Y ? "Y" : "route_w"));
+    if (!aligned(X, 16))
+        return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
+    if (!aligned(Y, 4) || !aligned(route_w, 4))
+        return fail(QMM_ERR_ALIGN, "%s: %s is not 4-byte aligned", fn, !aligned(Y, 4) ? "Y" : "route_w");
+    const int S = T * top_k;
+    MoeScratch ms;
+    st = moe_scratch(*mg, S, n_experts, size_t(S) * d_model, size_t(S) * d_ff, fn, ms);
+    if (st != QMM_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = mg->sm_count;
+    cudaError_t e = qmm::launch_moe_bucket(expert_ids, S, n_experts, ms.ix, nullptr, 0, 0,
+                                           mg->status, s);
+    qmm::MoeExpertArgs a;
+    memset(&a, 0, sizeof(a));
+    a.top_k = top_k;
+    a.ix = ms.ix;
+    a.status = mg->status;
+    if (e == cudaSuccess) {  // gate and up, one launch
+        a.tmap[0] = mg->tmap;
+        a.tmap[1] = mu->tmap;
+        a.y[0] = ms.g;
+        a.y[1] = ms.u;
+        a.nmat = 2;
+        a.Ne = d_ff;
+        a.K = d_model;
+        a.x = X;
+        a.ldx = d_model;
+        a.x_per_slot = 0;
+        e = qmm::launch_moe_expert(a, sms, s);
+    }
+    if (e == cudaSuccess)
+        e = qmm::launch_swiglu(ms.g, ms.u, ms.h, int64_t(S) * d_ff, sms, s);
+    if (e == cudaSuccess) {  // down, one input row per slot
+        a.tmap[0] = md->tmap;
+        a.tmap[1] = nullptr;
+        a.y[0] = ms.ys;
+        a.y[1] = nullptr;
+        a.nmat = 1;
+        a.Ne = d_model;
+        a.K = d_ff;
+        a.x = ms.h;
+        a.ldx = d_ff;
+        a.x_per_slot = 1;
+        e = qmm::launch_moe_expert(a, sms, s);
+    }
+    if (e == cudaSuccess)
+        e = qmm::launch_moe_combine(ms.ys, route_w, expert_ids, n_experts, T, top_k, d_model, Y,
+                                    sms, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    mg->last_stream = s;
+    return QMM_OK;
 }
 
 qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_stream stream)

@@ -114,6 +114,46 @@ size_t gemv_tc_ws_floats(int sm_count);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
+// --------------------------------------------------------------- mixture of experts
+// Slots of one expert are processed in groups of at most kGroupTokens tokens
+// (the activation rows of one tensor-core pass).
+constexpr int kGroupTokens = 4;
+constexpr int kMoeMaxSlots = 4096;   // T * top_k
+constexpr int kMoeMaxExperts = 512;
+constexpr int kMoeMaxTopK = 16;
+
+// The bucketing result on the device.
+struct MoeIndex {
+    int4 *groups;   // [<= S / kGroupTokens + E] {expert, first, count, 0}
+    int *slots;     // [S] slots sorted by (expert, slot)
+    int *n_groups;  // [1]
+};
+inline size_t moe_max_groups(int S, int E) { return size_t(S / kGroupTokens + E); }
+
+struct MoeExpertArgs {
+    const void *tmap[2];  // stacked expert matrices (n_experts * Ne rows each)
+    float *y[2];          // per-slot outputs, [S][Ne]
+    int nmat;             // 1, or 2 for gate and up together
+    int64_t Ne, K;
+    const float *x;
+    int64_t ldx;
+    int top_k;
+    int x_per_slot;
+    MoeIndex ix;
+    unsigned *status;
+};
+
+size_t moe_bucket_smem(int S, int E);
+cudaError_t launch_moe_bucket(const int32_t *ids, int S, int E, const MoeIndex &ix, float *y0,
+                              int64_t n0, int64_t ld0, unsigned *status, cudaStream_t s);
+void moe_expert_shape(int64_t K, int &nw, int &nslot);
+size_t moe_expert_smem(int64_t K, int nw, int nslot);
+cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t s);
+cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, int sm_count,
+                          cudaStream_t s);
+cudaError_t launch_moe_combine(const float *ys, const float *r, const int32_t *ids, int E, int T,
+                               int top_k, int64_t Ne, float *y, int sm_count, cudaStream_t s);
+
 // --------------------------------------------------------------- no-allocation entry
 // Argument checks of qmm_gemv_noalloc, and recording its refusal sentence for
 // qmm_last_error().
