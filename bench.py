@@ -263,6 +263,81 @@ class Model:
                 m.close()
 
 
+class BatchedModel:
+    """Continuous-batching decode: the Llama-3.1-8B Q4_K matrices of a Model
+    applied to M activation rows per call (one read of the weights for all M)."""
+
+    def __init__(self, model, M_max=16, device="cuda"):
+        import torch
+        self.model = model
+        self.M_max = M_max
+        x_sizes = [4096, 4096, 4096, 14336]
+        nl = len(model.layers)
+        xs = synth.activations(nl * M_max, sum(x_sizes), SEED + 11)
+        self.X = torch.from_numpy(xs).to(device).view(nl, M_max, sum(x_sizes))
+        self.xoff = [0, 4096, 8192, 12288]
+        self.kin = [0, 0, 0, 1, 2, 2, 3]  # which input each matrix reads
+        self.Y = [torch.empty((M_max, N), dtype=torch.float32, device=device)
+                  for _, N, _ in SHAPES]
+
+    def step(self, M):
+        q = self.model.q
+        for L, (mats, _, _) in enumerate(self.model.layers):
+            XL = self.X[L]
+            for j, m in enumerate(mats):
+                i = self.kin[j]
+                x = XL[:, self.xoff[i]:]
+                q.gemv_batched(m.h, x.data_ptr(), M, XL.stride(0), self.Y[j], self.Y[j].stride(0))
+
+    def bytes_per_step(self, M):
+        w = sum(N * synth.row_bytes(synth.Q4_K, K) for _, N, K in SHAPES)
+        x = 4 * M * (4096 + 4096 + 4096 + 14336)
+        y = 4 * M * sum(N for _, N, _ in SHAPES)
+        return (w + x + y) * len(self.model.layers)
+
+
+class MoeModel:
+    """OLMoE-1B-7B expert layers: 64 experts, d_model 2048, d_ff 1024, Q4_K,
+    32 tokens routed top-8 by a seeded softmax; one step runs every layer's
+    whole expert FFN (bucket, gate+up, SwiGLU, down, combine)."""
+
+    def __init__(self, layers=16, T=32, device="cuda"):
+        import torch
+        import quantized_gguf_dequant_gb300 as q
+        self.q = q
+        E, dm, dff, k = synth.OLMOE_EXPERTS, synth.OLMOE_D_MODEL, synth.OLMOE_D_FF, synth.OLMOE_TOP_K
+        self.E, self.T, self.k, self.dm, self.dff = E, T, k, dm, dff
+        self.layers = []
+        self.active_bytes = 0
+        per_expert = 3 * dff * synth.row_bytes(synth.Q4_K, dm)  # gate, up, down (same size)
+        for L in range(layers):
+            hs = []
+            for j, (N, K) in enumerate(((E * dff, dm), (E * dff, dm), (E * dm, dff))):
+                w = synth.q4k_matrix(N, K, synth.layer_seed(SEED + 100, L, j))
+                hs.append(q.Matrix(synth.Q4_K, N, K, torch.from_numpy(w).to(device)))
+            ids, r = synth.router(T, E, k, synth.layer_seed(SEED + 200, L, 0))
+            X = synth.activations(T, dm, synth.layer_seed(SEED + 300, L, 0))
+            self.active_bytes += len(np.unique(ids)) * per_expert
+            self.layers.append((hs, torch.from_numpy(ids).to(device), torch.from_numpy(r).to(device),
+                                torch.from_numpy(X).to(device),
+                                torch.empty((T, dm), dtype=torch.float32, device=device)))
+        torch.cuda.synchronize()
+
+    def step(self):
+        q = self.q
+        for hs, ids, r, X, Y in self.layers:
+            q.moe_ffn(hs[0].h, hs[1].h, hs[2].h, self.E, ids, self.T, self.k, X, r, Y)
+
+    def bytes_per_step(self):
+        xy = 2 * 4 * self.T * self.dm + 2 * 4 * self.T * self.k  # X, Y, ids, r
+        return self.active_bytes + xy * len(self.layers)
+
+    def close(self):
+        for hs, *_ in self.layers:
+            for h in hs:
+                h.close()
+
+
 def time_graph(fn, steps, warmup, world, sampler_index=None):
     """Capture fn into a CUDA graph, replay warmup + steps; returns (ms/step,
     clocks summary)."""
@@ -416,9 +491,38 @@ def run_ours(args, world, rank, local):
             "value": step_bytes / (ms_u * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_u,
             "launches_per_step": q4.launches(False),
             "frac_of_peak": step_bytes / (ms_u * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    if args.extras:
+        bm = BatchedModel(q4)
+        sweep = {}
+        for M in (1, 2, 4, 8, 16):
+            ms_b, _ = time_graph(lambda: bm.step(M), max(3, args.steps // 8), args.warmup, world)
+            b = bm.bytes_per_step(M)
+            sweep[str(M)] = {"ms_per_step": ms_b, "gbs": b / (ms_b * 1e-3) / 1e9,
+                             "frac_of_peak": b / (ms_b * 1e-3) / 1e9 / pk["hbm_gbs"],
+                             "tokens_per_s": M / (ms_b * 1e-3)}
+        extras["q4k_batched_decode"] = {
+            "unit": "GB/s", "by_M": sweep, "launches_per_step": 7 * nl,
+            "note": "qmm_gemv_batched on every matrix of every layer, M activation rows per "
+                    "call; bytes = weights once + M input rows + M output rows"}
+        del bm
     q4.close()
     del q4
     torch.cuda.empty_cache()
+    if args.extras:
+        mo = MoeModel()
+        ms_m, _ = time_graph(mo.step, max(3, args.steps // 4), args.warmup, world)
+        bm_ = mo.bytes_per_step()
+        extras["olmoe_moe_ffn"] = {
+            "value": bm_ / (ms_m * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_m,
+            "bytes_per_step": bm_, "layers": len(mo.layers), "tokens": mo.T,
+            "frac_of_peak": bm_ / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "us_per_layer": ms_m * 1e3 / len(mo.layers), "launches_per_step": 5 * len(mo.layers),
+            "note": "qmm_moe_ffn per layer (bucket, gate+up, SwiGLU, down, combine); bytes = "
+                    "the Q4_K gate/up/down bytes of every expert some token picked, plus X, Y, "
+                    "ids and routing weights; 16 layers = 3.6 GB of experts > L2"}
+        mo.close()
+        del mo
+        torch.cuda.empty_cache()
     if args.extras:
         q8 = Model(synth.Q8_0, layers=nl)
         b8, _ = layer_bytes(synth.Q8_0)
