@@ -1,0 +1,461 @@
+// gemm_tc.cu -- Q4_K prefill GEMM on the 5th-generation tensor cores
+// (tcgen05.mma with the accumulators in tensor memory), dequantising the
+// weights into shared memory on the way.
+//
+// The operation: "Frink Inference: the Rust alternative to llama.cpp",
+// section "Where llama.cpp is still ahead" -- prompt processing (prefill),
+// where many tokens go through every weight matrix at once, so the matmul is
+// compute-bound rather than bandwidth-bound; and "Building a Rust Inference
+// Engine That Matches Llama.cpp", "Where the wins came from" -- dequantise
+// once per weight, in fast memory, not as a separate pass over a
+// full-precision copy.
+//
+//   Y[m][n] = sum_k bf16(w[n][k]) * X[m][k]     (fp32 accumulation)
+//
+// bf16(w) is the exact Q4_K weight d*sc*q - dmin*m rounded to fp32 and then
+// to bfloat16 (nearest even), the same values qmm_dequantize_bf16 returns.
+//
+// Tiling.  One CTA tile is 128 tokens x 256 weight rows: the tokens are the
+// MMA's M side (A operand, TMEM lanes) and the weight rows its N side
+// (B operand, TMEM columns), so each dequantised weight feeds 128 tokens and
+// each thread of the epilogue owns one token's row of Y.  K advances in
+// stages of 64 (one 128-byte swizzle row of bf16):
+//   A  128 x 64 bf16 of X, by TMA with the 128-byte swizzle   (16 KB)
+//   raw  the 256 rows' Q4_K header (16 B) and the 32 nibble bytes of this
+//        64-weight chunk, by two TMA boxes                     (12 KB)
+//   B  256 x 64 bf16 weights, written by the dequant warps in the same
+//      swizzled K-major layout                                 (32 KB)
+// Four m128 n256 k16 MMAs per stage accumulate into one of two 256-column
+// TMEM accumulators; the second lets the epilogue of one tile overlap the
+// main loop of the next.  Tiles are spread over a persistent grid.
+//
+// Warp roles (448 threads):
+//   warp 0        TMA producer (one lane)
+//   warp 1        TMEM allocation and MMA issue (one lane)
+//   warps 2..5    epilogue: TMEM -> registers -> Y (warp w reads lanes
+//                 32*(w%4) .. +31, the quarter it may access)
+//   warps 6..13   dequantisation, one weight row per thread
+//
+// Every pipeline wait is bounded.  A wait that runs out records the timeout
+// in the status word and raises a CTA-wide abort flag; every role then leaves
+// its loop, the copies and MMAs already issued are waited for (again with a
+// limit), and the tensor memory is released before the CTA exits.
+#include <cstring>
+
+#include <cuda.h>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+namespace {
+
+constexpr int kTok = 128;            // tokens per tile (MMA M)
+constexpr int kRows = 256;           // weight rows per tile (MMA N)
+constexpr int kStages = 3;
+constexpr int kABytes = kTok * 128;  // 16384
+constexpr int kBBytes = kRows * 128; // 32768
+constexpr int kHdrBytes = kRows * 16;
+constexpr int kNibBytes = kRows * 32;
+constexpr int kRawBytes = kHdrBytes + kNibBytes;  // 12288
+constexpr int kThreads = 448;
+constexpr int kDequantWarp0 = 6;
+constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
+// bf16, both K-major, N = 256 (bits 17-22 hold N/8), M = 128 (bits 24-28
+// hold M/16).
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kRows >> 3) << 17) |
+                            (uint32_t(kTok >> 4) << 24);
+
+constexpr size_t kSmemBytes =
+    1024 /* alignment slack */ + size_t(kStages) * (kABytes + kBBytes + kRawBytes) + 256;
+
+struct GemmParams {
+    CUtensorMap tm_x;    // X [M][K] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_hdr;  // weight bytes [N][row_bytes] u8, box 16 x 256
+    CUtensorMap tm_nib;  // weight bytes, box 32 x 256
+    float *y;
+    int M, N, K;
+    int tok_tiles, tiles;
+    int vec_store;       // Y rows 16-byte aligned: store float4
+    unsigned *status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                       uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core
+// groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t(1) << 16;            // leading byte offset (unused for this layout)
+    d |= uint64_t(1024 >> 4) << 32;    // stride byte offset
+    d |= uint64_t(1) << 46;            // version
+    d |= uint64_t(2) << 61;            // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier completes one arrival when every tcgen05 operation this
+// thread issued so far has finished.
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Bounded wait that also gives up when another role raised the abort flag.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, unsigned parity, volatile int *abort,
+                                           unsigned *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_sleep(bar, parity))
+                return true;
+        if (*abort)
+            return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            atomicOr(status, kStatusTimeoutBit);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// The (sc, m) pair of sub-block j (0..7) from the 12 packed scale bytes
+// q[0..11] held in words s0 = q[0..3], s1 = q[4..7], s2 = q[8..11].
+__device__ __forceinline__ void scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j,
+                                          uint32_t &sc, uint32_t &m)
+{
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63u;
+        m = (s1 >> (8 * j)) & 63u;
+    } else {
+        const int i = j - 4;
+        const uint32_t b = (s2 >> (8 * i)) & 0xFFu;
+        sc = (b & 0x0Fu) | (((s0 >> (8 * i + 6)) & 3u) << 4);
+        m = (b >> 4) | (((s1 >> (8 * i + 6)) & 3u) << 4);
+    }
+}
+
+// Four weights of one nibble lane of word v (mask 0x0F0F0F0F: the low
+// nibbles, values q; mask 0xF0F0F0F0: the high nibbles, values 16q) as two
+// bf16 pairs of RN_fp32(a*q - b); `as` is a (or a/16 for the high nibbles).
+__device__ __forceinline__ void dequant4(uint32_t v, float as, float b, uint32_t &p0, uint32_t &p1)
+{
+    const float2 magic = make_float2(-8388608.f, -8388608.f);
+    const float2 A = make_float2(as, as), B = make_float2(-b, -b);
+    float2 f0 = make_float2(byte_magic(v, 0), byte_magic(v, 1));
+    float2 f1 = make_float2(byte_magic(v, 2), byte_magic(v, 3));
+    f0 = __fadd2_rn(f0, magic);  // q (or 16q), exact
+    f1 = __fadd2_rn(f1, magic);
+    f0 = __ffma2_rn(f0, A, B);   // RN(a*q - b)
+    f1 = __ffma2_rn(f1, A, B);
+    p0 = cvt_bf16x2(f0.x, f0.y);
+    p1 = cvt_bf16x2(f1.x, f1.y);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_constant__ GemmParams P)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
+    uint8_t *sA = base;                                   // [kStages][16 KB]
+    uint8_t *sB = sA + kStages * kABytes;                 // [kStages][32 KB]
+    uint8_t *sRaw = sB + kStages * kBBytes;               // [kStages][12 KB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + kStages * kRawBytes);
+    uint64_t *full = bars;                 // A + raw landed          (tx)
+    uint64_t *bready = full + kStages;     // B written               (8 dequant warps)
+    uint64_t *empty = bready + kStages;    // MMAs of the slot done   (commit)
+    uint64_t *accfull = empty + kStages;   // accumulator complete    (commit)
+    uint64_t *accempty = accfull + 2;      // accumulator drained     (4 epilogue warps)
+    uint64_t *drain = accempty + 2;        // final MMA drain         (commit)
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ks_n = P.K / 64;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&bready[s], 8);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&accfull[a], 1);
+            mbar_init(&accempty[a], 4);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base_sh)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    pdl_wait();  // X belongs to earlier kernels until here, Y too
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x) {
+                const int tok0 = (t % P.tok_tiles) * kTok, row0 = (t / P.tok_tiles) * kRows;
+                for (int ks = 0; ks < ks_n; ++ks, ++it) {
+                    const int s = it % kStages, u = it / kStages;
+                    if (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
+                        break;
+                    mbar_arrive_expect_tx(&full[s], kABytes + kRawBytes);
+                    tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
+                    const int sb = ks >> 2, c = ks & 3;
+                    uint8_t *raw = sRaw + s * kRawBytes;
+                    tma_2d(raw, &P.tm_hdr, sb * 144, row0, &full[s]);
+                    tma_2d(raw + kHdrBytes, &P.tm_nib, sb * 144 + 16 + 32 * c, row0, &full[s]);
+                }
+                if (abort_flag)
+                    break;
+            }
+            // Copies still in flight must land before the CTA exits: wait for
+            // the last phase of every slot that was used (bounded).
+            for (int s = 0; s < kStages; ++s) {
+                if (s >= it)
+                    break;
+                const int last_u = (it - 1 - s) / kStages;
+                mbar_wait_bounded(&full[s], unsigned(last_u) & 1u, 200000000ll);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            int it = 0, lt = 0;
+            for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x, ++lt) {
+                const int acc = lt & 1, v = lt >> 1;
+                if (v >= 1 && !wait_phase(&accempty[acc], unsigned(v - 1) & 1u, &abort_flag, P.status))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + uint32_t(acc * kRows);
+                bool ok = true;
+                for (int ks = 0; ks < ks_n; ++ks, ++it) {
+                    const int s = it % kStages, u = it / kStages;
+                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
+                        !wait_phase(&bready[s], unsigned(u) & 1u, &abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(d, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk),
+                                 (ks | kk) != 0 ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                }
+                if (!ok)
+                    break;
+                mma_commit(&accfull[acc]);
+            }
+            // Every MMA issued has finished once this commit arrives.
+            mma_commit(drain);
+            mbar_wait_bounded(drain, 0u, 200000000ll);
+        }
+    } else if (warp < kDequantWarp0) {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int tok_in_tile = quarter * 32 + lane;
+        int lt = 0;
+        for (int t = blockIdx.x; t < P.tiles; t += gridDim.x, ++lt) {
+            const int acc = lt & 1, v = lt >> 1;
+            if (!wait_phase(&accfull[acc], unsigned(v) & 1u, &abort_flag, P.status))
+                break;
+            tc_fence_after();
+            const int tok = (t % P.tok_tiles) * kTok + tok_in_tile;
+            const int row0 = (t / P.tok_tiles) * kRows;
+            float *yrow = P.y + int64_t(tok) * P.N;
+            const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kRows);
+#pragma unroll 1
+            for (int ch = 0; ch < kRows / 16; ++ch) {
+                uint32_t r[16];
+                tmem_ld16(taddr + uint32_t(ch * 16), r);
+                tmem_ld_wait();
+                const int n0 = row0 + ch * 16;
+                if (tok < P.M) {
+                    if (P.vec_store && n0 + 16 <= P.N) {
+                        float4 *dst = reinterpret_cast<float4 *>(yrow + n0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                 __uint_as_float(r[4 * i + 2]),
+                                                 __uint_as_float(r[4 * i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (n0 + i < P.N)
+                                yrow[n0 + i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&accempty[acc]);
+        }
+    } else {
+        // ---------------------------------------------------------- dequantisation
+        const int r = (warp - kDequantWarp0) * 32 + lane;  // weight row within the tile
+        const uint32_t swz = uint32_t(r & 7);
+        int it = 0;
+        for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
+            bool ok = true;
+            for (int ks = 0; ks < ks_n; ++ks, ++it) {
+                const int s = it % kStages, u = it / kStages;
+                if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
+                    (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *raw = sRaw + s * kRawBytes;
+                const uint4 h = *reinterpret_cast<const uint4 *>(raw + r * 16);
+                const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + kHdrBytes + r * 32);
+                const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + kHdrBytes + r * 32 + 16);
+                const int c = ks & 3;
+                const float2 dd = half2_bits_to_float2(h.x);
+                uint32_t sc_lo, m_lo, sc_hi, m_hi;
+                scale_min(h.y, h.z, h.w, 2 * c, sc_lo, m_lo);
+                scale_min(h.y, h.z, h.w, 2 * c + 1, sc_hi, m_hi);
+                const float a_lo = dd.x * float(sc_lo), b_lo = dd.y * float(m_lo);
+                const float a_hi16 = dd.x * float(sc_hi) * 0.0625f, b_hi = dd.y * float(m_hi);
+                const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+                uint8_t *brow = sB + s * kBBytes + r * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // chunks j (low nibbles) and j + 4 (high)
+                    uint32_t p[4], q[4];
+                    dequant4(w[2 * j] & 0x0F0F0F0Fu, a_lo, b_lo, p[0], p[1]);
+                    dequant4(w[2 * j + 1] & 0x0F0F0F0Fu, a_lo, b_lo, p[2], p[3]);
+                    dequant4(w[2 * j] & 0xF0F0F0F0u, a_hi16, b_hi, q[0], q[1]);
+                    dequant4(w[2 * j + 1] & 0xF0F0F0F0u, a_hi16, b_hi, q[2], q[3]);
+                    *reinterpret_cast<uint4 *>(brow + ((uint32_t(j) ^ swz) << 4)) =
+                        make_uint4(p[0], p[1], p[2], p[3]);
+                    *reinterpret_cast<uint4 *>(brow + ((uint32_t(j + 4) ^ swz) << 4)) =
+                        make_uint4(q[0], q[1], q[2], q[3]);
+                }
+                fence_proxy_async_smem();  // the MMA reads B through the async proxy
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&bready[s]);
+            }
+            if (!ok)
+                break;
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+} // namespace
+
+size_t gemm_q4k_smem() { return kSmemBytes; }
+
+cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
+{
+    GemmParams P;
+    memset(&P, 0, sizeof(P));
+    memcpy(&P.tm_x, a.tmap_x, sizeof(CUtensorMap));
+    memcpy(&P.tm_hdr, a.tmap_hdr, sizeof(CUtensorMap));
+    memcpy(&P.tm_nib, a.tmap_nib, sizeof(CUtensorMap));
+    P.y = a.y;
+    P.M = int(a.M);
+    P.N = int(a.N);
+    P.K = int(a.K);
+    P.tok_tiles = int((a.M + kTok - 1) / kTok);
+    P.tiles = P.tok_tiles * int((a.N + kRows - 1) / kRows);
+    P.vec_store = (a.N % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
+    P.status = a.status;
+    cudaError_t e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess)
+        return e;
+    int grid = sm_count < P.tiles ? sm_count : P.tiles;
+    if (const char *g = getenv("QMM_GEMM_CTAS"))
+        if (atoi(g) > 0 && atoi(g) < grid)
+            grid = atoi(g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P);
+}
+
+} // namespace qmm

@@ -43,7 +43,6 @@
 #include <cstring>
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
@@ -55,7 +54,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kWarps = 8;
 struct TcParams {
     CUtensorMap tmap[kMaxGroup];  // rows of each matrix as a 2-D uint64 tensor
     int64_t tile_end[kMaxGroup];  // cumulative 16-row tile counts
@@ -417,25 +415,9 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
 // (row_bytes/8 x N) whose boxes are one super-block column of 16 rows.
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes)
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !fn)
-            return -1;
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    const cuuint64_t dims[2] = {cuuint64_t(row_bytes / 8), cuuint64_t(N)};
-    const cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
-    const cuuint32_t box[2] = {18u, cuuint32_t(kTileRows)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = encode(reinterpret_cast<CUtensorMap *>(out128), CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
-                        const_cast<void *>(w), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? 0 : -2;
+    return encode_tmap_2d(out128, CU_TENSOR_MAP_DATA_TYPE_UINT64, w, uint64_t(row_bytes / 8),
+                          uint64_t(N), uint64_t(row_bytes), 18u, uint32_t(kTileRows),
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 } // namespace qmm

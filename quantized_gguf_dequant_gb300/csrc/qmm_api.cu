@@ -11,6 +11,8 @@
 #include <cstring>
 #include <string>
 
+#include <cuda.h>
+
 #include "qmm_internal.h"
 
 using qmm::Matrix;
@@ -337,6 +339,16 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
                                       "not be encoded (driver entry point or arguments refused)");
         }
         m->has_tmap = true;
+        if (qmm::encode_tmap_2d(m->tmap_hdr, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_dev,
+                                uint64_t(m->row_bytes), uint64_t(N), uint64_t(m->row_bytes), 16u,
+                                256u, CU_TENSOR_MAP_SWIZZLE_NONE) != 0 ||
+            qmm::encode_tmap_2d(m->tmap_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_dev,
+                                uint64_t(m->row_bytes), uint64_t(N), uint64_t(m->row_bytes), 32u,
+                                256u, CU_TENSOR_MAP_SWIZZLE_NONE) != 0) {
+            delete m;
+            return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor maps for the prefill GEMM "
+                                      "could not be encoded");
+        }
         m->tc_ws_floats = qmm::gemv_tc_ws_floats(m->sm_count);
         m->tc_tickets_n = size_t(N > 32768 ? N : 32768) / 16 + 64;
     }
@@ -643,8 +655,47 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
 qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_stream stream)
 {
     g_err.clear();
-    (void)h; (void)X_bf16; (void)M; (void)Y; (void)stream;
-    return fail(QMM_ERR_UNSUPPORTED, "qmm_gemm: not implemented in this build");
+    const char *fn = "qmm_gemm";
+    qmm_status st = check_handle(h, fn);
+    if (st != QMM_OK)
+        return st;
+    Matrix *m = reinterpret_cast<Matrix *>(h);
+    if (m->fmt != QMM_Q4_K)
+        return fail(QMM_ERR_UNSUPPORTED,
+                    "%s: the prefill GEMM is implemented for Q4_K weights only (this handle is "
+                    "format %d)", fn, m->fmt);
+    if (!X_bf16 || !Y)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X_bf16 ? "X" : "Y");
+    if (M < 1 || M > (int64_t(1) << 24))
+        return fail(QMM_ERR_SHAPE, "%s: M = %lld; 1 <= M <= 16777216 is supported", fn,
+                    (long long)M);
+    if (m->N > (int64_t(1) << 30))
+        return fail(QMM_ERR_SHAPE, "%s: N = %lld rows exceed the GEMM's limit of 2^30", fn,
+                    (long long)m->N);
+    if (!aligned(X_bf16, 16))
+        return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
+    if (!aligned(Y, 4))
+        return fail(QMM_ERR_ALIGN, "%s: Y is not 4-byte aligned", fn);
+    alignas(64) unsigned char tmx[128];
+    if (qmm::encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X_bf16, uint64_t(m->K),
+                            uint64_t(M), uint64_t(m->K) * 2, 64u, 128u,
+                            CU_TENSOR_MAP_SWIZZLE_128B) != 0)
+        return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
+    qmm::GemmArgs a;
+    a.tmap_x = tmx;
+    a.tmap_hdr = m->tmap_hdr;
+    a.tmap_nib = m->tmap_nib;
+    a.y = Y;
+    a.M = M;
+    a.N = m->N;
+    a.K = m->K;
+    a.status = m->status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = qmm::launch_gemm_q4k(a, m->sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    m->last_stream = s;
+    return QMM_OK;
 }
 
 static qmm_status dequant_common(qmm_t h, int64_t row0, int64_t nrows, float *of, uint16_t *ob,

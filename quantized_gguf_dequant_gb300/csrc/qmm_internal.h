@@ -37,6 +37,10 @@ struct Matrix {
     size_t tc_ws_floats = 0;
     unsigned *tc_tickets = nullptr;
     size_t tc_tickets_n = 0;
+    // prefill GEMM: tensor maps over the weight bytes (u8) with boxes of the
+    // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
+    alignas(64) unsigned char tmap_hdr[128];
+    alignas(64) unsigned char tmap_nib[128];
     // expert-layer scratch (allocated on first qmm_moe_* call)
     void *moe_ws = nullptr;
     size_t moe_ws_bytes = 0;
@@ -113,6 +117,24 @@ size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw);
 size_t gemv_tc_ws_floats(int sm_count);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
+
+// --------------------------------------------------------------- TMA tensor maps
+// Encode a 2-D tiled tensor map (dtype: a CUtensorMapDataType, swizzle: a
+// CUtensorMapSwizzle); 0 on success.
+int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uint64_t dim1,
+                   uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle);
+
+// --------------------------------------------------------------- prefill GEMM
+struct GemmArgs {
+    const void *tmap_x;    // X [M][K] bf16: box 64 x 128, 128-byte swizzle
+    const void *tmap_hdr;  // Matrix::tmap_hdr
+    const void *tmap_nib;  // Matrix::tmap_nib
+    float *y;              // [M][N]
+    int64_t M, N, K;
+    unsigned *status;
+};
+size_t gemm_q4k_smem();
+cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s);
 
 // --------------------------------------------------------------- mixture of experts
 // Slots of one expert are processed in groups of at most kGroupTokens tokens

@@ -1,0 +1,143 @@
+"""GPU parity of the tensor-core prefill GEMM (qmm_gemm) against the CPU
+oracle, through the C ABI.
+
+The GEMM multiplies bf16 X by the weights rounded to bf16 (bf16(RN_fp32(w)))
+with fp32 accumulation.  The contract bound is |y - y_ref| <= 1e-2 * sum|w x|
+(exact weights); since the oracle's y_ref uses the same bf16 weights, the
+tests also hold the kernel to 1e-3 of that sum, which only accumulation order
+can use up.  An identity X makes Y the transposed bf16 weight matrix, which
+must match the oracle's decode bit for bit."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_gguf_dequant_gb300 import synth
+from tests._util import TOL_BF16, assert_close_to_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("quantized_gguf_dequant_gb300")
+
+NTHREADS = max(1, oracle.max_threads())
+TIGHT = 1e-3
+
+
+def _bf16_bits_of(ref32: np.ndarray) -> np.ndarray:
+    """bf16 (nearest even) bit patterns of fp32 values, via torch's CPU cast."""
+    t = torch.from_numpy(np.ascontiguousarray(ref32, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _run(m, Xb, M):
+    Y = torch.full((M, m.N), float("nan"), dtype=torch.float32, device="cuda")
+    m.gemm(to_dev(Xb.view(np.int16)), Y)
+    torch.cuda.synchronize()
+    return Y.cpu().numpy()
+
+
+def _check(M, N, K, seed, rows=None):
+    w = synth.q4k_matrix(N, K, seed)
+    Xb = synth.activations_bf16(M, K, seed + 1)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    y = _run(m, Xb, M)
+    y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS)
+    got = y if rows is None else y[:, rows]
+    assert_close_to_oracle(got, y_ref, c, TOL_BF16, f"gemm M={M} N={N} K={K}")
+    assert_close_to_oracle(got, y_ref, c, TIGHT, f"gemm (tight) M={M} N={N} K={K}")
+    assert m.status() == 0
+    m.close()
+    return y
+
+
+def test_gemm_identity_is_bf16_weights():
+    """X = I (K x K): Y[m][n] = bf16(w[n][m]) exactly (one nonzero product per
+    output), for every position of every super-block, chunk and nibble."""
+    N, K = 300, 512
+    w = synth.q4k_matrix(N, K, 7)
+    eye = np.eye(K, dtype=np.float32)
+    Xb = _bf16_bits_of(eye)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    y = _run(m, Xb, K)
+    ref = oracle.dequant_rows(q.Q4_K, w, N, K).astype(np.float32)
+    want = _bf16_bits_of(ref).T  # [K, N]
+    got = _bf16_bits_of(y)       # y holds bf16 values exactly; compare as bits
+    assert np.array_equal(y, y.astype(np.float32))
+    assert np.array_equal(got, want)
+    # and y itself is exactly the bf16 value widened to fp32
+    widened = (want.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(y.view(np.uint32), widened.view(np.uint32))
+    m.close()
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 256), (5, 300, 512), (128, 256, 1024), (130, 513, 768), (257, 1024, 2048),
+    (300, 64, 256), (129, 257, 4096),
+])
+def test_gemm_small(M, N, K):
+    _check(M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)])
+def test_gemm_llama_shapes_m512(N, K):
+    """The Llama-3.1-8B shapes at M = 512 tokens, on sampled rows (every
+    token, the first/last row tiles and random rows)."""
+    rng = np.random.default_rng(N + K)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(N - 8, N), rng.choice(N, 48, False)]))
+    _check(512, N, K, seed=N * 3 + K, rows=rows)
+
+
+def test_gemm_m2048_sampled():
+    rng = np.random.default_rng(5)
+    N, K = 4096, 4096
+    rows = np.unique(np.concatenate([np.arange(4), np.arange(N - 4, N), rng.choice(N, 24, False)]))
+    _check(2048, N, K, seed=99, rows=rows)
+
+
+def test_gemm_deterministic_and_graph():
+    M, N, K = 384, 1024, 1024
+    w = synth.q4k_matrix(N, K, 3)
+    Xb = to_dev(synth.activations_bf16(M, K, 4).view(np.int16))
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    Y1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    Y2 = torch.empty_like(Y1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        m.gemm(Xb, Y1, stream=s)
+        m.gemm(Xb, Y2, stream=s)
+    s.synchronize()
+    assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
+    g = torch.cuda.CUDAGraph()
+    Y3 = torch.zeros_like(Y1)
+    with torch.cuda.graph(g, stream=s):
+        m.gemm(Xb, Y3, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Y1.view(torch.int32), Y3.view(torch.int32))
+    m.close()
+
+
+def test_gemm_refusals():
+    N, K = 64, 256
+    w8 = synth.q8_0_matrix(N, K, 1)
+    m8 = q.Matrix(q.Q8_0, N, K, to_dev(w8))
+    X = torch.zeros((4, K), dtype=torch.int16, device="cuda")
+    Y = torch.zeros((4, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(q.QmmError) as ei:
+        m8.gemm(X, Y)
+    assert ei.value.status == q.ERR_UNSUPPORTED and "Q4_K" in ei.value.message
+    m8.close()
+    w = synth.q4k_matrix(N, K, 2)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    with pytest.raises(q.QmmError) as ei:
+        q.gemm(m.h, X, 0, Y)
+    assert ei.value.status == q.ERR_SHAPE
+    with pytest.raises(q.QmmError) as ei:
+        q.gemm(m.h, X.data_ptr() + 2, 2, Y)
+    assert ei.value.status == q.ERR_ALIGN
+    with pytest.raises(q.QmmError) as ei:
+        q.gemm(m.h, None, 2, Y)
+    assert ei.value.status == q.ERR_NULL
+    m.close()
