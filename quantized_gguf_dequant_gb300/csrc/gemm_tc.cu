@@ -15,26 +15,27 @@
 // bf16(w) is the exact Q4_K weight d*sc*q - dmin*m rounded to fp32 and then
 // to bfloat16 (nearest even), the same values qmm_dequantize_bf16 returns.
 //
-// Tiling.  One CTA tile is 128 tokens x 256 weight rows: the tokens are the
-// MMA's M side (A operand, TMEM lanes) and the weight rows its N side
-// (B operand, TMEM columns), so each dequantised weight feeds 128 tokens and
-// each thread of the epilogue owns one token's row of Y.  K advances in
+// Tiling.  One CTA tile is 256 tokens x 256 weight rows: the tokens are the
+// MMA's M side (A operand, TMEM lanes; two halves of 128) and the weight rows
+// its N side (B operand, TMEM columns), so each dequantised weight feeds 256
+// tokens and each epilogue thread owns one token's row of Y.  K advances in
 // stages of 64 (one 128-byte swizzle row of bf16):
-//   A  128 x 64 bf16 of X, by TMA with the 128-byte swizzle   (16 KB)
-//   raw  the 256 rows' Q4_K header (16 B) and the 32 nibble bytes of this
-//        64-weight chunk, by two TMA boxes                     (12 KB)
-//   B  256 x 64 bf16 weights, written by the dequant warps in the same
-//      swizzled K-major layout                                 (32 KB)
-// Four m128 n256 k16 MMAs per stage accumulate into one of two 256-column
-// TMEM accumulators; the second lets the epilogue of one tile overlap the
-// main loop of the next.  Tiles are spread over a persistent grid.
+//   A    256 x 64 bf16 of X, one TMA box, 128-byte swizzle         (32 KB)
+//   nib  the 32 nibble bytes of this 64-weight chunk, 256 rows      (8 KB)
+//   B    256 x 64 bf16 weights, written by the dequant warps in the
+//        same swizzled K-major layout                               (32 KB)
+// and once per super-block the rows' 16-byte headers (4 KB, two slots).
+// Eight m128 n256 k16 MMAs per stage (four K steps x two token halves)
+// accumulate into two 256-column TMEM accumulators (all 512 columns).
+// Tiles are spread over a persistent grid.
 //
-// Warp roles (448 threads):
+// Warp roles (576 threads):
 //   warp 0        TMA producer (one lane)
 //   warp 1        TMEM allocation and MMA issue (one lane)
-//   warps 2..5    epilogue: TMEM -> registers -> Y (warp w reads lanes
-//                 32*(w%4) .. +31, the quarter it may access)
-//   warps 6..13   dequantisation, one weight row per thread
+//   warps 2..9    epilogue: TMEM -> registers -> Y.  Warp w reads TMEM lanes
+//                 32*(w%4) .. +31 (the quarter it may access) of token half
+//                 (w-2)/4.
+//   warps 10..17  dequantisation, one weight row per thread
 //
 // Every pipeline wait is bounded.  A wait that runs out records the timeout
 // in the status word and raises a CTA-wide abort flag; every role then leaves
@@ -51,29 +52,32 @@ namespace qmm {
 
 namespace {
 
-constexpr int kTok = 128;            // tokens per tile (MMA M)
-constexpr int kRows = 256;           // weight rows per tile (MMA N)
+constexpr int kTok = 256;             // tokens per tile (two MMAs of M = 128)
+constexpr int kRows = 256;            // weight rows per tile (MMA N)
 constexpr int kStages = 3;
-constexpr int kABytes = kTok * 128;  // 16384
-constexpr int kBBytes = kRows * 128; // 32768
-constexpr int kHdrBytes = kRows * 16;
-constexpr int kNibBytes = kRows * 32;
-constexpr int kRawBytes = kHdrBytes + kNibBytes;  // 12288
-constexpr int kThreads = 448;
-constexpr int kDequantWarp0 = 6;
-constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr int kABytes = kTok * 128;   // 32768
+constexpr int kBBytes = kRows * 128;  // 32768
+constexpr int kNibBytes = kRows * 32; // 8192
+constexpr int kHdrBytes = kRows * 16; // 4096
+constexpr int kHdrSlots = 2;
+constexpr int kThreads = 576;
+constexpr int kEpiWarp0 = 2;
+constexpr int kDequantWarp0 = 10;
+constexpr uint32_t kTmemCols = 512;   // two 256-column fp32 accumulators
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
 // bf16, both K-major, N = 256 (bits 17-22 hold N/8), M = 128 (bits 24-28
 // hold M/16).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kRows >> 3) << 17) |
-                            (uint32_t(kTok >> 4) << 24);
+                            (uint32_t(128 >> 4) << 24);
 
+constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kNibBytes;
 constexpr size_t kSmemBytes =
-    1024 /* alignment slack */ + size_t(kStages) * (kABytes + kBBytes + kRawBytes) + 256;
+    1024 /* alignment slack */ + size_t(kStages) * kStageBytes + size_t(kHdrSlots) * kHdrBytes + 256;
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 struct GemmParams {
-    CUtensorMap tm_x;    // X [M][K] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_x;    // X [M][K] bf16, box 64 x 256, 128-byte swizzle
     CUtensorMap tm_hdr;  // weight bytes [N][row_bytes] u8, box 16 x 256
     CUtensorMap tm_nib;  // weight bytes, box 32 x 256
     float *y;
@@ -210,21 +214,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
-    uint8_t *sA = base;                                   // [kStages][16 KB]
-    uint8_t *sB = sA + kStages * kABytes;                 // [kStages][32 KB]
-    uint8_t *sRaw = sB + kStages * kBBytes;               // [kStages][12 KB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + kStages * kRawBytes);
-    uint64_t *full = bars;                 // A + raw landed          (tx)
-    uint64_t *bready = full + kStages;     // B written               (8 dequant warps)
-    uint64_t *empty = bready + kStages;    // MMAs of the slot done   (commit)
-    uint64_t *accfull = empty + kStages;   // accumulator complete    (commit)
-    uint64_t *accempty = accfull + 2;      // accumulator drained     (4 epilogue warps)
-    uint64_t *drain = accempty + 2;        // final MMA drain         (commit)
+    uint8_t *sA = base;                                  // [kStages][32 KB]
+    uint8_t *sB = sA + kStages * kABytes;                // [kStages][32 KB]
+    uint8_t *sNib = sB + kStages * kBBytes;              // [kStages][8 KB]
+    uint8_t *sHdr = sNib + kStages * kNibBytes;          // [kHdrSlots][4 KB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sHdr + kHdrSlots * kHdrBytes);
+    uint64_t *full = bars;                  // A + nibbles landed      (tx)
+    uint64_t *bready = full + kStages;      // B written               (8 dequant warps)
+    uint64_t *empty = bready + kStages;     // MMAs of the slot done   (commit)
+    uint64_t *hfull = empty + kStages;      // headers landed          (tx)
+    uint64_t *hempty = hfull + kHdrSlots;   // headers consumed        (8 dequant warps)
+    uint64_t *accfull = hempty + kHdrSlots; // accumulators complete   (commit)
+    uint64_t *accempty = accfull + 1;       // accumulators drained    (8 epilogue warps)
+    uint64_t *drain = accempty + 1;         // final MMA drain         (commit)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ks_n = P.K / 64;
+    const int sb_n = P.K / 256;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -232,10 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             mbar_init(&bready[s], 8);
             mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&accfull[a], 1);
-            mbar_init(&accempty[a], 4);
+        for (int h = 0; h < kHdrSlots; ++h) {
+            mbar_init(&hfull[h], 1);
+            mbar_init(&hempty[h], 8);
         }
+        mbar_init(accfull, 1);
+        mbar_init(accempty, 8);
         mbar_init(drain, 1);
         abort_flag = 0;
         fence_barrier_init();
@@ -257,42 +267,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int it = 0;
+            int it = 0, hit = 0;  // stages and super-blocks issued
             for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x) {
                 const int tok0 = (t % P.tok_tiles) * kTok, row0 = (t / P.tok_tiles) * kRows;
                 for (int ks = 0; ks < ks_n; ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
+                    const int sb = ks >> 2, c = ks & 3;
+                    if (c == 0) {
+                        const int h = hit % kHdrSlots, hu = hit / kHdrSlots;
+                        if (hu >= 1 &&
+                            !wait_phase(&hempty[h], unsigned(hu - 1) & 1u, &abort_flag, P.status))
+                            break;
+                        mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
+                        tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr, sb * 144, row0, &hfull[h]);
+                        ++hit;
+                    }
                     if (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
                         break;
-                    mbar_arrive_expect_tx(&full[s], kABytes + kRawBytes);
+                    mbar_arrive_expect_tx(&full[s], kABytes + kNibBytes);
                     tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
-                    const int sb = ks >> 2, c = ks & 3;
-                    uint8_t *raw = sRaw + s * kRawBytes;
-                    tma_2d(raw, &P.tm_hdr, sb * 144, row0, &full[s]);
-                    tma_2d(raw + kHdrBytes, &P.tm_nib, sb * 144 + 16 + 32 * c, row0, &full[s]);
+                    tma_2d(sNib + s * kNibBytes, &P.tm_nib, sb * 144 + 16 + 32 * c, row0, &full[s]);
                 }
                 if (abort_flag)
                     break;
             }
             // Copies still in flight must land before the CTA exits: wait for
             // the last phase of every slot that was used (bounded).
-            for (int s = 0; s < kStages; ++s) {
-                if (s >= it)
-                    break;
-                const int last_u = (it - 1 - s) / kStages;
-                mbar_wait_bounded(&full[s], unsigned(last_u) & 1u, 200000000ll);
-            }
+            for (int s = 0; s < kStages && s < it; ++s)
+                mbar_wait_bounded(&full[s], unsigned((it - 1 - s) / kStages) & 1u, 200000000ll);
+            for (int h = 0; h < kHdrSlots && h < hit; ++h)
+                mbar_wait_bounded(&hfull[h], unsigned((hit - 1 - h) / kHdrSlots) & 1u, 200000000ll);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             int it = 0, lt = 0;
             for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x, ++lt) {
-                const int acc = lt & 1, v = lt >> 1;
-                if (v >= 1 && !wait_phase(&accempty[acc], unsigned(v - 1) & 1u, &abort_flag, P.status))
+                if (lt >= 1 && !wait_phase(accempty, unsigned(lt - 1) & 1u, &abort_flag, P.status))
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem + uint32_t(acc * kRows);
                 bool ok = true;
                 for (int ks = 0; ks < ks_n; ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
@@ -304,14 +317,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(d, sw128_desc(a0 + 32 * kk), sw128_desc(b0 + 32 * kk),
-                                 (ks | kk) != 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t bd = sw128_desc(b0 + 32 * kk);
+                        const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
+                        mma_bf16(tmem, sw128_desc(a0 + 32 * kk), bd, acc);
+                        mma_bf16(tmem + uint32_t(kRows), sw128_desc(a0 + kABytes / 2 + 32 * kk), bd,
+                                 acc);
+                    }
                     mma_commit(&empty[s]);
                 }
                 if (!ok)
                     break;
-                mma_commit(&accfull[acc]);
+                mma_commit(accfull);
             }
             // Every MMA issued has finished once this commit arrives.
             mma_commit(drain);
@@ -320,34 +337,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     } else if (warp < kDequantWarp0) {
         // ---------------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        const int tok_in_tile = quarter * 32 + lane;
+        const int half = (warp - kEpiWarp0) >> 2;
+        const int tok_in_tile = half * 128 + quarter * 32 + lane;
         int lt = 0;
         for (int t = blockIdx.x; t < P.tiles; t += gridDim.x, ++lt) {
-            const int acc = lt & 1, v = lt >> 1;
-            if (!wait_phase(&accfull[acc], unsigned(v) & 1u, &abort_flag, P.status))
+            if (!wait_phase(accfull, unsigned(lt) & 1u, &abort_flag, P.status))
                 break;
             tc_fence_after();
             const int tok = (t % P.tok_tiles) * kTok + tok_in_tile;
             const int row0 = (t / P.tok_tiles) * kRows;
             float *yrow = P.y + int64_t(tok) * P.N;
-            const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(acc * kRows);
+            const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * kRows);
 #pragma unroll 1
-            for (int ch = 0; ch < kRows / 16; ++ch) {
-                uint32_t r[16];
-                tmem_ld16(taddr + uint32_t(ch * 16), r);
+            for (int ch = 0; ch < kRows / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld16(taddr + uint32_t(ch * 32), *reinterpret_cast<uint32_t(*)[16]>(r));
+                tmem_ld16(taddr + uint32_t(ch * 32 + 16), *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                 tmem_ld_wait();
-                const int n0 = row0 + ch * 16;
+                const int n0 = row0 + ch * 32;
                 if (tok < P.M) {
-                    if (P.vec_store && n0 + 16 <= P.N) {
+                    if (P.vec_store && n0 + 32 <= P.N) {
                         float4 *dst = reinterpret_cast<float4 *>(yrow + n0);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
+                        for (int i = 0; i < 8; ++i)
                             dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                                  __uint_as_float(r[4 * i + 2]),
                                                  __uint_as_float(r[4 * i + 3]));
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
+                        for (int i = 0; i < 32; ++i)
                             if (n0 + i < P.N)
                                 yrow[n0 + i] = __uint_as_float(r[i]);
                     }
@@ -356,54 +374,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&accempty[acc]);
+                mbar_arrive(accempty);
         }
     } else {
         // ---------------------------------------------------------- dequantisation
         const int r = (warp - kDequantWarp0) * 32 + lane;  // weight row within the tile
         const uint32_t swz = uint32_t(r & 7);
-        int it = 0;
-        for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
-            bool ok = true;
-            for (int ks = 0; ks < ks_n; ++ks, ++it) {
-                const int s = it % kStages, u = it / kStages;
-                if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
-                    (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+        int it = 0, hit = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.tiles && ok; t += gridDim.x) {
+            for (int sb = 0; sb < sb_n && ok; ++sb, ++hit) {
+                const int h = hit % kHdrSlots;
+                if (!wait_phase(&hfull[h], unsigned(hit / kHdrSlots) & 1u, &abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *raw = sRaw + s * kRawBytes;
-                const uint4 h = *reinterpret_cast<const uint4 *>(raw + r * 16);
-                const uint4 n0 = *reinterpret_cast<const uint4 *>(raw + kHdrBytes + r * 32);
-                const uint4 n1 = *reinterpret_cast<const uint4 *>(raw + kHdrBytes + r * 32 + 16);
-                const int c = ks & 3;
-                const float2 dd = half2_bits_to_float2(h.x);
-                uint32_t sc_lo, m_lo, sc_hi, m_hi;
-                scale_min(h.y, h.z, h.w, 2 * c, sc_lo, m_lo);
-                scale_min(h.y, h.z, h.w, 2 * c + 1, sc_hi, m_hi);
-                const float a_lo = dd.x * float(sc_lo), b_lo = dd.y * float(m_lo);
-                const float a_hi16 = dd.x * float(sc_hi) * 0.0625f, b_hi = dd.y * float(m_hi);
-                const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-                uint8_t *brow = sB + s * kBBytes + r * 128;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {  // chunks j (low nibbles) and j + 4 (high)
-                    uint32_t p[4], q[4];
-                    dequant4(w[2 * j] & 0x0F0F0F0Fu, a_lo, b_lo, p[0], p[1]);
-                    dequant4(w[2 * j + 1] & 0x0F0F0F0Fu, a_lo, b_lo, p[2], p[3]);
-                    dequant4(w[2 * j] & 0xF0F0F0F0u, a_hi16, b_hi, q[0], q[1]);
-                    dequant4(w[2 * j + 1] & 0xF0F0F0F0u, a_hi16, b_hi, q[2], q[3]);
-                    *reinterpret_cast<uint4 *>(brow + ((uint32_t(j) ^ swz) << 4)) =
-                        make_uint4(p[0], p[1], p[2], p[3]);
-                    *reinterpret_cast<uint4 *>(brow + ((uint32_t(j + 4) ^ swz) << 4)) =
-                        make_uint4(q[0], q[1], q[2], q[3]);
-                }
-                fence_proxy_async_smem();  // the MMA reads B through the async proxy
+                const uint4 hd = *reinterpret_cast<const uint4 *>(sHdr + h * kHdrBytes + r * 16);
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&bready[s]);
+                    mbar_arrive(&hempty[h]);  // the header now lives in registers
+                const float2 dd = half2_bits_to_float2(hd.x);
+                for (int c = 0; c < 4; ++c, ++it) {
+                    const int s = it % kStages, u = it / kStages;
+                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
+                        (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *nib = sNib + s * kNibBytes + r * 32;
+                    const uint4 n0 = *reinterpret_cast<const uint4 *>(nib);
+                    const uint4 n1 = *reinterpret_cast<const uint4 *>(nib + 16);
+                    uint32_t sc_lo, m_lo, sc_hi, m_hi;
+                    scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
+                    scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
+                    const float a_lo = dd.x * float(sc_lo), b_lo = dd.y * float(m_lo);
+                    const float a_hi16 = dd.x * float(sc_hi) * 0.0625f, b_hi = dd.y * float(m_hi);
+                    const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+                    uint8_t *brow = sB + s * kBBytes + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {  // chunks j (low nibbles) and j + 4 (high)
+                        uint32_t p[4], q[4];
+                        dequant4(w[2 * j] & 0x0F0F0F0Fu, a_lo, b_lo, p[0], p[1]);
+                        dequant4(w[2 * j + 1] & 0x0F0F0F0Fu, a_lo, b_lo, p[2], p[3]);
+                        dequant4(w[2 * j] & 0xF0F0F0F0u, a_hi16, b_hi, q[0], q[1]);
+                        dequant4(w[2 * j + 1] & 0xF0F0F0F0u, a_hi16, b_hi, q[2], q[3]);
+                        *reinterpret_cast<uint4 *>(brow + ((uint32_t(j) ^ swz) << 4)) =
+                            make_uint4(p[0], p[1], p[2], p[3]);
+                        *reinterpret_cast<uint4 *>(brow + ((uint32_t(j + 4) ^ swz) << 4)) =
+                            make_uint4(q[0], q[1], q[2], q[3]);
+                    }
+                    fence_proxy_async_smem();  // the MMA reads B through the async proxy
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bready[s]);
+                }
             }
-            if (!ok)
-                break;
         }
     }
 

@@ -678,7 +678,7 @@ qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_st
         return fail(QMM_ERR_ALIGN, "%s: Y is not 4-byte aligned", fn);
     alignas(64) unsigned char tmx[128];
     if (qmm::encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X_bf16, uint64_t(m->K),
-                            uint64_t(M), uint64_t(m->K) * 2, 64u, 128u,
+                            uint64_t(M), uint64_t(m->K) * 2, 64u, 256u,
                             CU_TENSOR_MAP_SWIZZLE_128B) != 0)
         return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
     qmm::GemmArgs a;

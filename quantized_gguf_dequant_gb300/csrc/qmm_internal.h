@@ -126,7 +126,7 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
 
 // --------------------------------------------------------------- prefill GEMM
 struct GemmArgs {
-    const void *tmap_x;    // X [M][K] bf16: box 64 x 128, 128-byte swizzle
+    const void *tmap_x;    // X [M][K] bf16: box 64 x 256, 128-byte swizzle
     const void *tmap_hdr;  // Matrix::tmap_hdr
     const void *tmap_nib;  // Matrix::tmap_nib
     float *y;              // [M][N]
