@@ -338,6 +338,40 @@ class MoeModel:
                 h.close()
 
 
+class PrefillModel:
+    """Prefill: the seven Llama-3.1-8B Q4_K matrices of `layers` layers applied
+    to M bf16 tokens each (qmm_gemm per matrix; Y fp32)."""
+
+    def __init__(self, M, layers=4, device="cuda"):
+        import torch
+        import quantized_gguf_dequant_gb300 as q
+        self.q, self.M = q, M
+        self.mats = []
+        for L in range(layers):
+            row = []
+            for j, (name, N, K) in enumerate(SHAPES):
+                w = synth.q4k_matrix(N, K, synth.layer_seed(SEED + 400, L, j))
+                row.append(q.Matrix(synth.Q4_K, N, K, torch.from_numpy(w).to(device)))
+            self.mats.append(row)
+        self.X = {K: torch.from_numpy(synth.activations_bf16(M, K, SEED + K).view(np.int16)).to(device)
+                  for K in sorted({K for _, _, K in SHAPES})}
+        self.Y = [torch.empty((M, N), dtype=torch.float32, device=device) for _, N, _ in SHAPES]
+        torch.cuda.synchronize()
+
+    def step(self):
+        for row in self.mats:
+            for j, m in enumerate(row):
+                m.gemm(self.X[m.K], self.Y[j])
+
+    def flops_per_step(self):
+        return 2.0 * self.M * sum(N * K for _, N, K in SHAPES) * len(self.mats)
+
+    def close(self):
+        for row in self.mats:
+            for m in row:
+                m.close()
+
+
 def time_graph(fn, steps, warmup, world, sampler_index=None):
     """Capture fn into a CUDA graph, replay warmup + steps; returns (ms/step,
     clocks summary)."""
@@ -523,6 +557,29 @@ def run_ours(args, world, rank, local):
         mo.close()
         del mo
         torch.cuda.empty_cache()
+    if args.extras:
+        pre = {}
+        for M in (512, 2048):
+            pm = PrefillModel(M)
+            ms_p, _ = time_graph(pm.step, max(3, args.steps // 40), args.warmup, world)
+            fl = pm.flops_per_step()
+            tf = fl / (ms_p * 1e-3) / 1e12
+            pre[str(M)] = {"ms_per_step": ms_p, "tflops": tf,
+                           "frac_of_peak": tf / pk["bf16_tflops"],
+                           "launches_per_step": 7 * len(pm.mats)}
+            pm.close()
+            del pm
+            torch.cuda.empty_cache()
+        extras["q4k_prefill_gemm"] = {
+            "unit": "TFLOP/s", "by_M": pre,
+            "roofline": {"bound": "tensor", "kernel": "gemm_q4k_kernel",
+                         "achieved": pre["2048"]["tflops"], "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": pre["2048"]["tflops"] / pk["bf16_tflops"],
+                         "peak_source": pk["source"], "traffic": recorded_traffic("gemm_q4k_kernel")},
+            "note": "qmm_gemm on the 7 Llama-3.1-8B matrices of 4 layers (491 MB of Q4_K "
+                    "weights > L2), bf16 X of M tokens, fp32 Y; flops = 2*M*N*K; peak = bf16 "
+                    "dense (burst figure: each GEMM is a separate launch of tens to hundreds "
+                    "of microseconds)"}
     if args.extras:
         q8 = Model(synth.Q8_0, layers=nl)
         b8, _ = layer_bytes(synth.Q8_0)

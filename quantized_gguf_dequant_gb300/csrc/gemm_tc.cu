@@ -64,6 +64,7 @@ constexpr int kThreads = 576;
 constexpr int kEpiWarp0 = 2;
 constexpr int kDequantWarp0 = 10;
 constexpr uint32_t kTmemCols = 512;   // two 256-column fp32 accumulators
+constexpr int kMaxKSplit = 16;
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
 // bf16, both K-major, N = 256 (bits 17-22 hold N/8), M = 128 (bits 24-28
@@ -81,8 +82,11 @@ struct GemmParams {
     CUtensorMap tm_hdr;  // weight bytes [N][row_bytes] u8, box 16 x 256
     CUtensorMap tm_nib;  // weight bytes, box 32 x 256
     float *y;
+    float *ws;           // split-K partials [ksplit][M][N] (ksplit > 1)
     int M, N, K;
     int tok_tiles, tiles;
+    int ksplit;          // K slices per tile (divides K / 256)
+    int units;           // tiles * ksplit
     int vec_store;       // Y rows 16-byte aligned: store float4
     unsigned *status;
 };
@@ -231,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ks_n = P.K / 64;
-    const int sb_n = P.K / 256;
+    const int sb_u = P.K / 256 / P.ksplit;  // super-blocks per unit
+    const int ks_u = 4 * sb_u;               // stages per unit
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -268,9 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             int it = 0, hit = 0;  // stages and super-blocks issued
-            for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x) {
+            for (int un = blockIdx.x; un < P.units && !abort_flag; un += gridDim.x) {
+                const int t = un / P.ksplit, kslice = un - t * P.ksplit;
                 const int tok0 = (t % P.tok_tiles) * kTok, row0 = (t / P.tok_tiles) * kRows;
-                for (int ks = 0; ks < ks_n; ++ks, ++it) {
+                for (int ks = kslice * ks_u; ks < (kslice + 1) * ks_u; ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
                     const int sb = ks >> 2, c = ks & 3;
                     if (c == 0) {
@@ -302,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             int it = 0, lt = 0;
-            for (int t = blockIdx.x; t < P.tiles && !abort_flag; t += gridDim.x, ++lt) {
+            for (int un = blockIdx.x; un < P.units && !abort_flag; un += gridDim.x, ++lt) {
                 if (lt >= 1 && !wait_phase(accempty, unsigned(lt - 1) & 1u, &abort_flag, P.status))
                     break;
                 tc_fence_after();
                 bool ok = true;
-                for (int ks = 0; ks < ks_n; ++ks, ++it) {
+                for (int ks = 0; ks < ks_u; ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
                     if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
                         !wait_phase(&bready[s], unsigned(u) & 1u, &abort_flag, P.status)) {
@@ -340,13 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         const int half = (warp - kEpiWarp0) >> 2;
         const int tok_in_tile = half * 128 + quarter * 32 + lane;
         int lt = 0;
-        for (int t = blockIdx.x; t < P.tiles; t += gridDim.x, ++lt) {
+        for (int un = blockIdx.x; un < P.units; un += gridDim.x, ++lt) {
             if (!wait_phase(accfull, unsigned(lt) & 1u, &abort_flag, P.status))
                 break;
             tc_fence_after();
+            const int t = un / P.ksplit, kslice = un - t * P.ksplit;
             const int tok = (t % P.tok_tiles) * kTok + tok_in_tile;
             const int row0 = (t / P.tok_tiles) * kRows;
-            float *yrow = P.y + int64_t(tok) * P.N;
+            // With K split, slice k writes its partial product to ws[k] (laid
+            // out like Y); a reduction kernel adds the slices in order.
+            float *yrow = (P.ksplit > 1 ? P.ws + size_t(kslice) * size_t(P.M) * P.N : P.y) +
+                          int64_t(tok) * P.N;
             const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * kRows);
 #pragma unroll 1
             for (int ch = 0; ch < kRows / 32; ++ch) {
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(accempty);
+                mbar_arrive(accempty);  // the accumulators are free for the next unit
         }
     } else {
         // ---------------------------------------------------------- dequantisation
@@ -382,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         const uint32_t swz = uint32_t(r & 7);
         int it = 0, hit = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < P.tiles && ok; t += gridDim.x) {
-            for (int sb = 0; sb < sb_n && ok; ++sb, ++hit) {
+        for (int un = blockIdx.x; un < P.units && ok; un += gridDim.x) {
+            const int kslice = un % P.ksplit;
+            for (int sb = kslice * sb_u; sb < (kslice + 1) * sb_u && ok; ++sb, ++hit) {
                 const int h = hit % kHdrSlots;
                 if (!wait_phase(&hfull[h], unsigned(hit / kHdrSlots) & 1u, &abort_flag, P.status)) {
                     ok = false;
@@ -443,9 +453,80 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     }
 }
 
+// y[i] = ws[0][i] + ws[1][i] + ... + ws[ks-1][i], in slice order.
+__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int ks, int64_t n,
+                                     float *__restrict__ y, int vec)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    if (vec) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+            float4 acc = __ldcs(reinterpret_cast<const float4 *>(ws) + i);
+            for (int k = 1; k < ks; ++k) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(ws + size_t(k) * n) + i);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            reinterpret_cast<float4 *>(y)[i] = acc;
+        }
+    } else {
+        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+            float acc = ws[i];
+            for (int k = 1; k < ks; ++k)
+                acc += ws[size_t(k) * n + i];
+            y[i] = acc;
+        }
+    }
+}
+
 } // namespace
 
 size_t gemm_q4k_smem() { return kSmemBytes; }
+
+int gemm_q4k_tiles(int64_t M, int64_t N)
+{
+    return int((M + kTok - 1) / kTok) * int((N + kRows - 1) / kRows);
+}
+
+// K slices per tile.  Splitting costs a write and a re-read of every partial
+// product (the reduction kernel), so it is used only when the tiles fill less
+// than half of the SMs; then the count (dividing K/256, at most 16) minimises
+// waves x super-blocks per slice plus a quarter super-block per slice.
+// QMM_GEMM_KSPLIT forces a value (if it divides K/256).
+int gemm_q4k_ksplit(int64_t M, int64_t N, int64_t K, int sm_count)
+{
+    const int sb = int(K / 256);
+    const int tiles = gemm_q4k_tiles(M, N);
+    if (const char *e = getenv("QMM_GEMM_KSPLIT")) {
+        const int f = atoi(e);
+        if (f >= 1 && f <= kMaxKSplit && sb % f == 0)
+            return f;
+    }
+    if (2 * tiles >= sm_count)
+        return 1;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int ks = 1; ks <= kMaxKSplit && ks <= sb; ++ks) {
+        if (sb % ks != 0)
+            continue;
+        const double waves = double((int64_t(tiles) * ks + sm_count - 1) / sm_count);
+        const double cost = waves * (sb / ks) + (ks > 1 ? 0.25 * ks : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = ks;
+        }
+    }
+    return best;
+}
+
+size_t gemm_q4k_ws_floats(int64_t M, int64_t N, int ksplit)
+{
+    return ksplit > 1 ? size_t(ksplit) * size_t(M) * size_t(N) : 0;
+}
 
 cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
 {
@@ -455,18 +536,21 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     memcpy(&P.tm_hdr, a.tmap_hdr, sizeof(CUtensorMap));
     memcpy(&P.tm_nib, a.tmap_nib, sizeof(CUtensorMap));
     P.y = a.y;
+    P.ws = a.ws;
     P.M = int(a.M);
     P.N = int(a.N);
     P.K = int(a.K);
     P.tok_tiles = int((a.M + kTok - 1) / kTok);
-    P.tiles = P.tok_tiles * int((a.N + kRows - 1) / kRows);
+    P.tiles = gemm_q4k_tiles(a.M, a.N);
+    P.ksplit = a.ksplit;
+    P.units = P.tiles * P.ksplit;
     P.vec_store = (a.N % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
     P.status = a.status;
     cudaError_t e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess)
         return e;
-    int grid = sm_count < P.tiles ? sm_count : P.tiles;
+    int grid = sm_count < P.units ? sm_count : P.units;
     if (const char *g = getenv("QMM_GEMM_CTAS"))
         if (atoi(g) > 0 && atoi(g) < grid)
             grid = atoi(g);
@@ -480,7 +564,21 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P);
+    e = cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P);
+    if (e != cudaSuccess || P.ksplit == 1)
+        return e;
+    const int64_t n = a.M * a.N;
+    const int vec = (n % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
+    const int64_t work = vec ? n / 4 : n;
+    int64_t blocks = (work + 255) / 256;
+    if (blocks > int64_t(sm_count) * 16)
+        blocks = int64_t(sm_count) * 16;
+    cudaLaunchConfig_t rc = cfg;
+    rc.gridDim = dim3(unsigned(blocks));
+    rc.blockDim = dim3(256);
+    rc.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, static_cast<const float *>(a.ws), P.ksplit, n,
+                              a.y, vec);
 }
 
 } // namespace qmm

@@ -390,6 +390,8 @@ qmm_status qmm_destroy(qmm_t h)
         cudaFree(m->ws);
     if (m->moe_ws)
         cudaFree(m->moe_ws);
+    if (m->gemm_ws)
+        cudaFree(m->gemm_ws);
     if (prev >= 0)
         cudaSetDevice(prev);
     delete m;
@@ -682,6 +684,33 @@ qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_st
                             CU_TENSOR_MAP_SWIZZLE_128B) != 0)
         return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
     qmm::GemmArgs a;
+    memset(&a, 0, sizeof(a));
+    a.ksplit = qmm::gemm_q4k_ksplit(M, m->N, m->K, m->sm_count);
+    if (a.ksplit > 1) {
+        // Split K: the partial products; the scratch grows on demand (waiting
+        // for the device first).
+        const size_t need = qmm::gemm_q4k_ws_floats(M, m->N, a.ksplit) * 4;
+        if (need > m->gemm_ws_bytes) {
+            cudaError_t e = cudaSuccess;
+            if (m->gemm_ws) {
+                e = cudaDeviceSynchronize();
+                if (e == cudaSuccess)
+                    e = cudaFree(m->gemm_ws);
+                m->gemm_ws = nullptr;
+                m->gemm_ws_bytes = 0;
+                if (e != cudaSuccess)
+                    return cuda_fail(e, fn);
+            }
+            void *p = nullptr;
+            e = cudaMalloc(&p, need);
+            if (e != cudaSuccess)
+                return fail(QMM_ERR_NOMEM, "%s: could not allocate %zu bytes of split-K scratch (%s)",
+                            fn, need, cudaGetErrorString(e));
+            m->gemm_ws = p;
+            m->gemm_ws_bytes = need;
+        }
+        a.ws = static_cast<float *>(m->gemm_ws);
+    }
     a.tmap_x = tmx;
     a.tmap_hdr = m->tmap_hdr;
     a.tmap_nib = m->tmap_nib;

@@ -41,6 +41,9 @@ struct Matrix {
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
     alignas(64) unsigned char tmap_nib[128];
+    // prefill split-K scratch: the partial products (grown on demand)
+    void *gemm_ws = nullptr;
+    size_t gemm_ws_bytes = 0;
     // expert-layer scratch (allocated on first qmm_moe_* call)
     void *moe_ws = nullptr;
     size_t moe_ws_bytes = 0;
@@ -130,10 +133,15 @@ struct GemmArgs {
     const void *tmap_hdr;  // Matrix::tmap_hdr
     const void *tmap_nib;  // Matrix::tmap_nib
     float *y;              // [M][N]
+    float *ws;             // split-K partials (gemm_q4k_ws_floats floats) when ksplit > 1
+    int ksplit;
     int64_t M, N, K;
     unsigned *status;
 };
 size_t gemm_q4k_smem();
+int gemm_q4k_tiles(int64_t M, int64_t N);
+int gemm_q4k_ksplit(int64_t M, int64_t N, int64_t K, int sm_count);
+size_t gemm_q4k_ws_floats(int64_t M, int64_t N, int ksplit);
 cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s);
 
 // --------------------------------------------------------------- mixture of experts

@@ -141,3 +141,20 @@ def test_gemm_refusals():
         q.gemm(m.h, None, 2, Y)
     assert ei.value.status == q.ERR_NULL
     m.close()
+
+
+@pytest.mark.parametrize("ksplit", [2, 4, 8])
+def test_gemm_split_k_forced(monkeypatch, ksplit):
+    """K split over several CTAs, the partial products added in slice order by
+    a reduction kernel: within bounds, and repeatable bit for bit."""
+    monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
+    M, N, K = 300, 513, 2048
+    y = _check(M, N, K, seed=ksplit)
+    w = synth.q4k_matrix(N, K, ksplit)
+    Xb = synth.activations_bf16(M, K, ksplit + 1)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    y2 = _run(m, Xb, M)
+    y3 = _run(m, Xb, M)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    assert np.array_equal(y2.view(np.uint32), y3.view(np.uint32))
+    m.close()
