@@ -459,16 +459,17 @@ def time_e2e(model, steps, warmup, world):
 
 def recorded_traffic(kernel_key):
     """Per-launch DRAM bytes of a kernel from the committed ncu summary, if it
-    was taken on the kernel source as it is now (else None)."""
+    was taken on the kernel sources as they are now (else None)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         rec = json.load(open(path)).get(kernel_key)
-        src = os.path.join(ROOT, rec["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != rec["source_sha"]:
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest()[:16] != rec["sources_sha"]:
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
@@ -624,6 +625,25 @@ def run_ours(args, world, rank, local):
     return line
 
 
+def run_only(args, world, local):
+    """One secondary workload alone (for profiling runs)."""
+    import torch
+    torch.cuda.set_device(local)
+    timer = time_graph if args.graph else time_eager
+    if args.only == "prefill":
+        pm = PrefillModel(args.prefill_m, layers=args.layers)
+        ms, _ = timer(pm.step, args.steps, args.warmup, world)
+        tf = pm.flops_per_step() / (ms * 1e-3) / 1e12
+        pm.close()
+        return {"workload": f"prefill GEMM M={args.prefill_m}, {args.layers} layers", "ms_per_step": ms,
+                "tflops": tf}
+    mo = MoeModel(layers=args.layers)
+    ms, _ = timer(mo.step, args.steps, args.warmup, world)
+    gbs = mo.bytes_per_step() / (ms * 1e-3) / 1e9
+    mo.close()
+    return {"workload": f"OLMoE expert FFN, {args.layers} layers", "ms_per_step": ms, "gbs": gbs}
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: each step decodes-then-dots a
     bounded sample (256 rows of each of the 7 matrices of one layer)."""
@@ -683,6 +703,10 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch directly instead of replaying a CUDA graph (profiling)")
+    ap.add_argument("--only", choices=["prefill", "moe"], default=None,
+                    help="time just one secondary workload (profiling): the prefill GEMMs at "
+                         "--prefill-m tokens, or the OLMoE expert FFN")
+    ap.add_argument("--prefill-m", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -690,6 +714,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    if args.only:
+        line = run_only(args, world, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         return
     line = run_ours(args, world, rank, local)
     if rank == 0:
