@@ -637,6 +637,15 @@ def run_only(args, world, local):
         pm.close()
         return {"workload": f"prefill GEMM M={args.prefill_m}, {args.layers} layers", "ms_per_step": ms,
                 "tflops": tf}
+    if args.only == "batched":
+        q4 = Model(synth.Q4_K, layers=args.layers)
+        bm = BatchedModel(q4)
+        out = {"workload": f"batched Q4_K decode, {args.layers} layers"}
+        for M in (1, 2, 4, 8, 16):
+            ms, _ = timer(lambda: bm.step(M), args.steps, args.warmup, world)
+            out[str(M)] = {"ms_per_step": ms, "gbs": bm.bytes_per_step(M) / (ms * 1e-3) / 1e9}
+        q4.close()
+        return out
     mo = MoeModel(layers=args.layers)
     ms, _ = timer(mo.step, args.steps, args.warmup, world)
     gbs = mo.bytes_per_step() / (ms * 1e-3) / 1e9
@@ -703,7 +712,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch directly instead of replaying a CUDA graph (profiling)")
-    ap.add_argument("--only", choices=["prefill", "moe"], default=None,
+    ap.add_argument("--only", choices=["prefill", "moe", "batched"], default=None,
                     help="time just one secondary workload (profiling): the prefill GEMMs at "
                          "--prefill-m tokens, or the OLMoE expert FFN")
     ap.add_argument("--prefill-m", type=int, default=2048)

@@ -1,0 +1,356 @@
+// gemv_batched.cu -- Q4_K decode GEMV for a batch of activation rows
+// (continuous batching: every row of X shares one read of the weights), on
+// the tensor cores with the operand construction of gemv_tc.cu.
+//
+// The operation: "Frink Inference: the Rust alternative to llama.cpp",
+// section "A serving stack with the full sampling surface" -- continuous
+// batching runs the requests of one step through the weights together; with
+// the dequantisation fused into the dot product ("Building a Rust Inference
+// Engine That Matches Llama.cpp", "Where the wins came from").
+//
+//   Y[m][n] = sum_k w[n][k] * X[m][k],   m < M <= 16
+//
+// Up to 4*NT rows go through one pass: the A fragments of each k-step (the
+// expensive part, built from the nibbles) feed NT mma.sync instructions, one
+// per group of four rows.  The activations of all rows are re-laid out as B
+// fragments in shared memory; since 16 rows of a long K do not fit, the grid
+// is two-dimensional: CTA (r, s) owns row tiles [r*T/R, (r+1)*T/R) and
+// super-blocks [s*NB/S, (s+1)*NB/S), so it prepares only its slice of X.
+// With S > 1 the CTAs write partial sums per slice; the last CTA of a row
+// range to finish (an atomic ticket) adds the S slices in slice order, so
+// results are bitwise repeatable.
+#include <cstring>
+
+#include <cuda.h>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+#include "tc_common.cuh"
+
+namespace qmm {
+
+namespace {
+
+using namespace tc;
+
+struct TcbParams {
+    CUtensorMap tmap;   // rows as 2-D uint64, box 18 x 16 (one unit)
+    const float *x;     // [M][ldx]
+    float *y;           // [M][ldy]
+    float *ws;          // [S][M][N] partial sums (S > 1)
+    unsigned *tickets;  // [R], zero between launches (S > 1)
+    unsigned *status;
+    int64_t ldx, ldy;
+    int N, M, NB;
+    int T;              // row tiles
+    int R, S;           // row groups x K slices = grid
+    int nslot;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant__ TcbParams P)
+{
+    constexpr int NCOL = 8 * NT, MP = 4 * NT;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nw = int(blockDim.x) >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int NS = P.nslot;
+    const int r = blockIdx.x / P.S, s = blockIdx.x - r * P.S;
+    const int t0 = int(int64_t(r) * P.T / P.R), t1 = int(int64_t(r + 1) * P.T / P.R);
+    const int sb0 = int(int64_t(s) * P.NB / P.S), sb1 = int(int64_t(s + 1) * P.NB / P.S);
+    const int KC = sb1 - sb0;
+
+    uint8_t *ring = smem + size_t(warp) * NS * kTileBytes;
+    uint2 *Bs = reinterpret_cast<uint2 *>(smem + size_t(nw) * NS * kTileBytes);  // [KC][16][NCOL][4]
+    uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(KC) * 16 * NCOL * 4);   // [KC][NCOL][4]
+    float *inv = reinterpret_cast<float *>(Bm + size_t(KC) * NCOL * 4);            // [KC][MP]
+    float *part = inv + size_t(KC) * MP;                                          // [nw][2][MP][16]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(
+        (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * MP * kTileRows) + 7) & ~uintptr_t(7));
+    uint64_t *bar = bars + warp * NS;
+    __shared__ int wbeg[9];
+    __shared__ int s_last;
+
+    const int cn = (t1 - t0) * KC;  // units of this CTA, ordered (tile, super-block)
+    const int u0 = int(int64_t(warp) * cn / nw), u1 = int(int64_t(warp + 1) * cn / nw);
+    const int nu = u1 - u0;
+    if (lane == 0) {
+        wbeg[warp] = u0;
+        if (warp == nw - 1)
+            wbeg[nw] = cn;
+        for (int i = 0; i < NS; ++i)
+            mbar_init(&bar[i], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    int i_tile = t0 + u0 / KC, i_sb = u0 % KC, slot_i = 0;
+    auto issue = [&]() {
+        mbar_arrive_expect_tx(&bar[slot_i], kTileBytes);
+        tma_load_2d(ring + size_t(slot_i) * kTileBytes, &P.tmap, (sb0 + i_sb) * 18, i_tile * kTileRows,
+                    &bar[slot_i], 0ull);
+        if (++i_sb == KC) {
+            i_sb = 0;
+            ++i_tile;
+        }
+        if (++slot_i == NS)
+            slot_i = 0;
+    };
+    int issued = nu < NS ? nu : NS;
+    if (lane == 0)
+        for (int j = 0; j < issued; ++j)
+            issue();  // weights are constant: stream them before waiting on earlier kernels
+
+    pdl_wait();
+
+    // ---- this CTA's slice of every activation row -> B fragments (rows
+    // beyond M are zeros, so every column is finite)
+    {
+        const int cc = lane >> 3, tt = lane & 7;
+        for (int item = warp; item < KC * MP; item += nw) {
+            const int sbl = item % KC, m = item / KC;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f), w = v;
+            if (m < P.M) {
+                const float *xr = P.x + int64_t(m) * P.ldx + int64_t(sb0 + sbl) * 256 + 64 * cc + 4 * tt;
+                v = __ldg(reinterpret_cast<const float4 *>(xr));
+                w = __ldg(reinterpret_cast<const float4 *>(xr + 32));
+            }
+            prep_super_block<NCOL>(sbl, m, MP, v, w, lane, Bs, Bm, inv);
+        }
+    }
+    __syncthreads();
+
+    uint32_t selA, selB;
+    bool hi4;
+    chunk_selectors(c, selA, selB, hi4);
+    const uint8_t *rowA = ring + g * 144;
+    float *mypart = part + size_t(warp) * 2 * MP * kTileRows;
+    // One output (row tile t, rows rr and rr+8, activation row m): to Y, or to
+    // this slice's partial sums.
+    auto emit = [&](int t, int rr, int m, float v0, float v1) {
+        if (m >= P.M)
+            return;
+        const int row = t * kTileRows + rr;
+        float *dst = P.S > 1 ? P.ws + (int64_t(s) * P.M + m) * P.N : P.y + int64_t(m) * P.ldy;
+        if (row < P.N)
+            dst[row] = v0;
+        if (row + 8 < P.N)
+            dst[row + 8] = v1;
+    };
+
+    float tot0[NT], tot1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+        tot0[nt] = tot1[nt] = 0.f;
+    int q_tile = t0 + u0 / KC, q_sb = u0 % KC;
+    int slot = 0;
+    unsigned parity = 0;
+    int jfail = -1;
+    for (int j = 0; j < nu; ++j) {
+        if (!mbar_wait_bounded(&bar[slot], parity)) {
+            jfail = j;
+            break;
+        }
+        unit_dot_nt<NT>(rowA + slot * kTileBytes, c, selA, selB, hi4,
+                        Bs + (size_t(q_sb) * 16 * NCOL + g) * 4 + c, Bm + (size_t(q_sb) * NCOL + g) * 4 + c,
+                        inv + q_sb * MP + c, tot0, tot1);
+        __syncwarp();
+        if (issued < nu) {
+            if (lane == 0)
+                issue();
+            ++issued;
+        }
+        if (++slot == NS) {
+            slot = 0;
+            parity ^= 1u;
+        }
+        const int ju = u0 + j;
+        if (q_sb == KC - 1 || j == nu - 1) {
+            const int first = (ju / KC) * KC, last = first + KC - 1;
+            if (u0 <= first && u1 - 1 >= last) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    emit(q_tile, g, 4 * nt + c, tot0[nt], tot1[nt]);
+            } else {
+                const int k = (u0 >= first) ? 0 : 1;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mypart[(k * MP + 4 * nt + c) * kTileRows + g] = tot0[nt];
+                    mypart[(k * MP + 4 * nt + c) * kTileRows + g + 8] = tot1[nt];
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                tot0[nt] = tot1[nt] = 0.f;
+        }
+        if (++q_sb == KC) {
+            q_sb = 0;
+            ++q_tile;
+        }
+    }
+    if (jfail >= 0 && lane == 0) {
+        atomicOr(P.status, kStatusTimeoutBit);
+        for (int j = jfail; j < issued; ++j)
+            mbar_wait_bounded(&bar[j % NS], unsigned(j / NS) & 1u, 100000000ll);
+    }
+    pdl_launch_dependents();
+    __syncthreads();
+
+    // ---- tiles split between warps: add the shares in warp order
+    {
+        const int cm = lane >> 3, cr = lane & 7;
+        for (int tr = warp; tr < t1 - t0; tr += nw) {
+            const int first = tr * KC, last = first + KC - 1;
+            int wf = 0, wl = 0;
+            for (int w = 0; w < nw; ++w) {
+                if (wbeg[w] <= first)
+                    wf = w;
+                if (wbeg[w] <= last)
+                    wl = w;
+            }
+            if (wf == wl)
+                continue;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float s0 = 0.f, s1 = 0.f;
+                for (int w = wf; w <= wl; ++w) {
+                    const int b0 = wbeg[w], b1 = wbeg[w + 1];
+                    if (b1 == b0)
+                        continue;
+                    const int kw = (b0 >= first) ? 0 : 1;
+                    const float *pw = part + (size_t(w) * 2 + kw) * MP * kTileRows +
+                                      (4 * nt + cm) * kTileRows;
+                    s0 += pw[cr];
+                    s1 += pw[cr + 8];
+                }
+                emit(t0 + tr, cr, 4 * nt + cm, s0, s1);
+            }
+        }
+    }
+    if (P.S == 1)
+        return;
+
+    // ---- K slices: the last CTA of this row range adds them in slice order
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(&P.tickets[r], 1u) == unsigned(P.S - 1);
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    const int row0 = t0 * kTileRows, row1 = min(t1 * kTileRows, P.N);
+    const int nrow = row1 - row0;
+    for (int i = threadIdx.x; i < nrow * P.M; i += blockDim.x) {
+        const int m = i / nrow, row = row0 + (i - m * nrow);
+        float acc = 0.f;
+        for (int k = 0; k < P.S; ++k)
+            acc += __ldcg(P.ws + (int64_t(k) * P.M + m) * P.N + row);
+        P.y[int64_t(m) * P.ldy + row] = acc;
+    }
+    if (threadIdx.x == 0)
+        P.tickets[r] = 0u;  // ready for the next launch
+}
+
+using TcbKernel = void (*)(TcbParams);
+
+TcbKernel pick_tcb(int nt)
+{
+    switch (nt) {
+    case 1: return gemv_tcb_kernel<1>;
+    case 2: return gemv_tcb_kernel<2>;
+    case 3: return gemv_tcb_kernel<3>;
+    default: return gemv_tcb_kernel<4>;
+    }
+}
+
+constexpr int kTcbWarps = 8;
+constexpr int kTcbSlots = 4;
+
+size_t tcb_smem(int nt, int kc)
+{
+    const size_t ncol = 8 * nt, mp = 4 * nt;
+    return size_t(kTcbWarps) * kTcbSlots * kTileBytes + size_t(kc) * 16 * ncol * 4 * 8 +
+           size_t(kc) * ncol * 4 * 4 + size_t(kc) * mp * 4 + size_t(kTcbWarps) * 2 * mp * kTileRows * 4 +
+           8 + size_t(kTcbWarps) * kTcbSlots * 8;
+}
+
+} // namespace
+
+// Grid plan: rows per pass up to 16 (NT = ceil(M/4) groups of four), K split
+// into S slices small enough that one slice of every activation row fits in
+// shared memory (more slices when there are too few row tiles to cover the
+// SMs), and about one CTA per SM: R = SMs / S row groups (at most one per row
+// tile).  QMM_TCB_S forces S (at least the number that fits).
+TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
+{
+    TcbPlan p;
+    p.nt = (M + 3) / 4;
+    const int NB = int(K / 256);
+    const int T = int((N + kTileRows - 1) / kTileRows);
+    int kcmax = 0;
+    while (kcmax < NB && tcb_smem(p.nt, kcmax + 1) <= size_t(227 * 1024))
+        ++kcmax;
+    p.S = kcmax > 0 ? (NB + kcmax - 1) / kcmax : 0;
+    if (const char *e = getenv("QMM_TCB_S")) {
+        const int f = atoi(e);
+        if (f >= p.S && f <= NB)
+            p.S = f;
+    }
+    if (p.S == 0)
+        return p;
+    // Few row tiles: slice K further so that the grid still covers the SMs.
+    if (!getenv("QMM_TCB_S") && p.S * T < sm_count) {
+        const int want = sm_count / T;
+        p.S = want < NB ? want : NB;
+    }
+    p.R = sm_count / p.S;
+    if (p.R < 1)
+        p.R = 1;
+    if (p.R > T)
+        p.R = T;
+    p.kc = (NB + p.S - 1) / p.S;
+    p.smem = tcb_smem(p.nt, p.kc);
+    p.ws_floats = p.S > 1 ? size_t(p.S) * size_t(M) * size_t(N) : 0;
+    p.tickets = p.S > 1 ? size_t(p.R) : 0;
+    return p;
+}
+
+cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
+{
+    TcbParams P;
+    memset(&P, 0, sizeof(P));
+    P.tmap = *reinterpret_cast<const CUtensorMap *>(a.tmap);
+    P.x = a.x;
+    P.y = a.y;
+    P.ws = a.ws;
+    P.tickets = a.tickets;
+    P.status = a.status;
+    P.ldx = a.ldx;
+    P.ldy = a.ldy;
+    P.N = int(a.N);
+    P.M = a.M;
+    P.NB = int(a.K / 256);
+    P.T = int((a.N + kTileRows - 1) / kTileRows);
+    P.R = p.R;
+    P.S = p.S;
+    P.nslot = kTcbSlots;
+    TcbKernel kern = pick_tcb(p.nt);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.R * p.S));
+    cfg.blockDim = dim3(unsigned(kTcbWarps * 32));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+} // namespace qmm

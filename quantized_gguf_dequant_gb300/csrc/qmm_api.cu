@@ -392,6 +392,8 @@ qmm_status qmm_destroy(qmm_t h)
         cudaFree(m->moe_ws);
     if (m->gemm_ws)
         cudaFree(m->gemm_ws);
+    if (m->tcb_ws)
+        cudaFree(m->tcb_ws);
     if (prev >= 0)
         cudaSetDevice(prev);
     delete m;
@@ -468,6 +470,64 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     if (!aligned(Y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char *bpath = getenv("QMM_BATCHED_PATH");
+    const bool force_one = bpath && strcmp(bpath, "one") == 0;
+    const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
+    if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes && (force_one || M > 4 || !tc_fits(m, int(M)))) {
+        // All rows in one pass over the weights (tensor cores, K sliced when
+        // the activations do not fit in shared memory at once).  Up to four
+        // rows whose activations fit take the decode kernel below instead.
+        const qmm::TcbPlan p = qmm::plan_tcb(m.N, m.K, int(M), m.sm_count);
+        if (p.S > 0) {
+            Matrix &mm = *reinterpret_cast<Matrix *>(h);
+            const size_t tick_bytes = (p.tickets * 4 + 255) & ~size_t(255);
+            const size_t need = p.S > 1 ? tick_bytes + p.ws_floats * 4 : 0;
+            if (need > mm.tcb_ws_bytes) {
+                cudaError_t e = cudaSuccess;
+                if (mm.tcb_ws) {
+                    e = cudaDeviceSynchronize();
+                    if (e == cudaSuccess)
+                        e = cudaFree(mm.tcb_ws);
+                    mm.tcb_ws = nullptr;
+                    mm.tcb_ws_bytes = 0;
+                    if (e != cudaSuccess)
+                        return cuda_fail(e, "qmm_gemv_batched");
+                }
+                void *ptr = nullptr;
+                e = cudaMalloc(&ptr, need);
+                if (e != cudaSuccess)
+                    return fail(QMM_ERR_NOMEM, "qmm_gemv_batched: could not allocate %zu bytes of "
+                                               "K-slice scratch (%s)", need, cudaGetErrorString(e));
+                e = cudaMemset(ptr, 0, need);
+                if (e != cudaSuccess) {
+                    cudaFree(ptr);
+                    return cuda_fail(e, "qmm_gemv_batched");
+                }
+                mm.tcb_ws = ptr;
+                mm.tcb_ws_bytes = need;
+            }
+            qmm::TcbArgs a;
+            memset(&a, 0, sizeof(a));
+            a.tmap = m.tmap;
+            a.x = X;
+            a.y = Y;
+            if (p.S > 1) {
+                a.tickets = static_cast<unsigned *>(mm.tcb_ws);
+                a.ws = reinterpret_cast<float *>(static_cast<unsigned char *>(mm.tcb_ws) + tick_bytes);
+            }
+            a.status = m.status;
+            a.ldx = ldx;
+            a.ldy = ldy;
+            a.N = m.N;
+            a.K = m.K;
+            a.M = int(M);
+            cudaError_t e = qmm::launch_gemv_tcb(a, p, s);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "qmm_gemv_batched");
+            mm.last_stream = s;
+            return QMM_OK;
+        }
+    }
     // Up to four activation rows share one pass over the weights; larger
     // batches take ceil(M/4) passes.
     for (int64_t m0 = 0; m0 < M;) {

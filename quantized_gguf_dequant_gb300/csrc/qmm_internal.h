@@ -41,6 +41,9 @@ struct Matrix {
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
     alignas(64) unsigned char tmap_nib[128];
+    // batched GEMV scratch: tickets, then the K-slice partial sums (grown on demand)
+    void *tcb_ws = nullptr;
+    size_t tcb_ws_bytes = 0;
     // prefill split-K scratch: the partial products (grown on demand)
     void *gemm_ws = nullptr;
     size_t gemm_ws_bytes = 0;
@@ -120,6 +123,30 @@ size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw);
 size_t gemv_tc_ws_floats(int sm_count);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
+
+// --------------------------------------------------------------- batched tensor-core Q4_K GEMV
+// Up to 16 activation rows in one pass; CTA (r, s) of an R x S grid owns a
+// range of row tiles and a slice of K (see gemv_batched.cu).
+struct TcbPlan {
+    int nt = 0;            // groups of four activation rows
+    int S = 0, R = 0;      // K slices, row groups (S == 0: does not fit)
+    int kc = 0;            // super-blocks per slice (at most)
+    size_t smem = 0;
+    size_t ws_floats = 0;  // partial sums, S * M * N when S > 1
+    size_t tickets = 0;    // R when S > 1
+};
+struct TcbArgs {
+    const void *tmap;      // Matrix::tmap
+    const float *x;
+    float *y;
+    float *ws;
+    unsigned *tickets;     // zeroed, left zero by every launch
+    unsigned *status;
+    int64_t ldx, ldy, N, K;
+    int M;
+};
+TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count);
+cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s);
 
 // --------------------------------------------------------------- TMA tensor maps
 // Encode a 2-D tiled tensor map (dtype: a CUtensorMapDataType, swizzle: a

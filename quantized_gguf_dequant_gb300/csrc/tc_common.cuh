@@ -226,5 +226,61 @@ __device__ __forceinline__ void chunk_selectors(int c, uint32_t &selA, uint32_t 
     hi4 = c >= 2;
 }
 
+// unit_dot for NT groups of four activation rows (B has NCOL = 8*NT columns):
+// the A fragments of each k-step are built once and feed NT MMAs.  bsb =
+// Bs + ((sb*16)*NCOL + g)*4 + c, bmp = Bm + (sb*NCOL + g)*4 + c, scp = inv +
+// sb*4*NT + c (row 4*nt + c at scp[4*nt]).  tot0[nt] / tot1[nt] gain rows g
+// and g+8 of activation row 4*nt + c.
+template <int NT>
+__device__ __forceinline__ void unit_dot_nt(const uint8_t *tp, int c, uint32_t selA, uint32_t selB,
+                                            bool hi4, const uint2 *bsb, const uint32_t *bmp,
+                                            const float *scp, float (&tot0)[NT], float (&tot1)[NT])
+{
+    constexpr int NCOL = 8 * NT;
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(tp);
+    const uint4 h1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144);
+    const uint4 qa0 = *reinterpret_cast<const uint4 *>(tp + 16 + 32 * c);
+    const uint4 qa1 = *reinterpret_cast<const uint4 *>(tp + 32 + 32 * c);
+    const uint4 qb0 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 16 + 32 * c);
+    const uint4 qb1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 32 + 32 * c);
+    const RowScales r0 = row_scales(h0, selA, selB, hi4);
+    const RowScales r1 = row_scales(h1, selA, selB, hi4);
+    const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+    const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+    float dq[NT][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t xa = e ? (wa[t] >> 8) : wa[t];
+            const uint32_t xb = e ? (wb[t] >> 8) : wb[t];
+            const uint32_t a0 = hfma2(and_or(xa, mlo, magic), r0.SL, r0.CL);
+            const uint32_t a1 = hfma2(and_or(xb, mlo, magic), r1.SL, r1.CL);
+            const uint32_t a2 = hfma2(and_or(xa, mhi, magic), r0.SH, r0.CH);
+            const uint32_t a3 = hfma2(and_or(xb, mhi, magic), r1.SH, r1.CH);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint2 b = bsb[(2 * t + e) * NCOL * 4 + nt * 32];
+                if (t == 0 && e == 0)
+                    mma16816_zero(dq[nt], a0, a1, a2, a3, b.x, b.y);
+                else
+                    mma16816(dq[nt], a0, a1, a2, a3, b.x, b.y);
+            }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t bm = bmp[nt * 32];
+        float dm[4];
+        mma16816_zero(dm, r0.Am, r1.Am, 0u, 0u, bm, bm);
+        const float sc = scp[4 * nt];
+        tot0[nt] = fmaf(fmaf(r0.d, dq[nt][0] + dq[nt][1], -(r0.dmin * ((dm[0] + dm[1]) * 32.f))), sc,
+                        tot0[nt]);
+        tot1[nt] = fmaf(fmaf(r1.d, dq[nt][2] + dq[nt][3], -(r1.dmin * ((dm[2] + dm[3]) * 32.f))), sc,
+                        tot1[nt]);
+    }
+}
+
 } // namespace tc
 } // namespace qmm

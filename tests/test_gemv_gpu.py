@@ -245,3 +245,38 @@ def test_gemv_batched_strided_and_big_k():
                         nthreads=oracle.max_threads())
     assert_close_to_oracle(Y[:, :N], Yr, C, TOL_FP32, "batched strided")
     m.close()
+
+
+@pytest.mark.parametrize("M", [2, 5, 8, 12, 16])
+@pytest.mark.parametrize("N,K", [(4096, 14336), (1024, 4096), (300, 768)])
+def test_gemv_batched_one_pass(monkeypatch, M, N, K):
+    """All M rows in one pass (K sliced across CTAs where needed), against
+    the oracle on sampled rows of the large shapes."""
+    monkeypatch.setenv("QMM_BATCHED_PATH", "one")
+    w, m = _matrix(q.Q4_K, N, K, seed=M * 11 + K)
+    X = synth.activations(M, K, seed=M + N)
+    Y = m.gemv_batched(to_dev(X)).cpu().numpy()
+    rng = np.random.default_rng(M)
+    rows = None if N <= 1024 else np.unique(np.concatenate(
+        [np.arange(16), np.arange(N - 16, N), rng.choice(N, 64, False)]))
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, rows=rows, nthreads=oracle.max_threads())
+    got = Y if rows is None else Y[:, rows]
+    assert_close_to_oracle(got, Yr, C, TOL_FP32, f"batched one pass M={M} N={N} K={K}")
+    assert m.status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("S", [2, 3, 7])
+def test_gemv_batched_forced_k_slices(monkeypatch, S):
+    """K split into S slices whose partial sums the last CTA adds in slice
+    order: within bounds and bitwise repeatable."""
+    monkeypatch.setenv("QMM_TCB_S", str(S))
+    N, K, M = 515, 256 * 14, 9
+    w, m = _matrix(q.Q4_K, N, K, seed=S)
+    X = synth.activations(M, K, seed=S + 1)
+    Y1 = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Y2 = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, nthreads=oracle.max_threads())
+    assert_close_to_oracle(Y1, Yr, C, TOL_FP32, f"batched S={S}")
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    m.close()
