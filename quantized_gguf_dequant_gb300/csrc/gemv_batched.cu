@@ -16,9 +16,8 @@
 // fragments in shared memory; since 16 rows of a long K do not fit, the grid
 // is two-dimensional: CTA (r, s) owns row tiles [r*T/R, (r+1)*T/R) and
 // super-blocks [s*NB/S, (s+1)*NB/S), so it prepares only its slice of X.
-// With S > 1 the CTAs write partial sums per slice; the last CTA of a row
-// range to finish (an atomic ticket) adds the S slices in slice order, so
-// results are bitwise repeatable.
+// With S > 1 the CTAs write partial sums per slice and a reduction kernel
+// adds the S slices in slice order, so results are bitwise repeatable.
 #include <cstring>
 
 #include <cuda.h>
@@ -38,7 +37,6 @@ struct TcbParams {
     const float *x;     // [M][ldx]
     float *y;           // [M][ldy]
     float *ws;          // [S][M][N] partial sums (S > 1)
-    unsigned *tickets;  // [R], zero between launches (S > 1)
     unsigned *status;
     int64_t ldx, ldy;
     int N, M, NB;
@@ -70,7 +68,6 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
         (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * MP * kTileRows) + 7) & ~uintptr_t(7));
     uint64_t *bar = bars + warp * NS;
     __shared__ int wbeg[9];
-    __shared__ int s_last;
 
     const int cn = (t1 - t0) * KC;  // units of this CTA, ordered (tile, super-block)
     const int u0 = int(int64_t(warp) * cn / nw), u1 = int(int64_t(warp + 1) * cn / nw);
@@ -107,16 +104,30 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
     // ---- this CTA's slice of every activation row -> B fragments (rows
     // beyond M are zeros, so every column is finite)
     {
+        // Items (super-block, row) in rounds of eight per warp, their loads
+        // in flight together.
         const int cc = lane >> 3, tt = lane & 7;
-        for (int item = warp; item < KC * MP; item += nw) {
-            const int sbl = item % KC, m = item / KC;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f), w = v;
-            if (m < P.M) {
-                const float *xr = P.x + int64_t(m) * P.ldx + int64_t(sb0 + sbl) * 256 + 64 * cc + 4 * tt;
-                v = __ldg(reinterpret_cast<const float4 *>(xr));
-                w = __ldg(reinterpret_cast<const float4 *>(xr + 32));
+        const int items = KC * MP;
+        for (int base = warp; base < items; base += 8 * nw) {
+            float4 v[8], w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int item = base + i * nw;
+                v[i] = w[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const int sbl = item % KC, m = item / KC;
+                if (item < items && m < P.M) {
+                    const float *xr =
+                        P.x + int64_t(m) * P.ldx + int64_t(sb0 + sbl) * 256 + 64 * cc + 4 * tt;
+                    v[i] = __ldg(reinterpret_cast<const float4 *>(xr));
+                    w[i] = __ldg(reinterpret_cast<const float4 *>(xr + 32));
+                }
             }
-            prep_super_block<NCOL>(sbl, m, MP, v, w, lane, Bs, Bm, inv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int item = base + i * nw;
+                if (item < items)
+                    prep_super_block<NCOL>(item % KC, item / KC, MP, v[i], w[i], lane, Bs, Bm, inv);
+            }
         }
     }
     __syncthreads();
@@ -228,29 +239,22 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
             }
         }
     }
-    if (P.S == 1)
-        return;
+}
 
-    // ---- K slices: the last CTA of this row range adds them in slice order
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0)
-        s_last = atomicAdd(&P.tickets[r], 1u) == unsigned(P.S - 1);
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    const int row0 = t0 * kTileRows, row1 = min(t1 * kTileRows, P.N);
-    const int nrow = row1 - row0;
-    for (int i = threadIdx.x; i < nrow * P.M; i += blockDim.x) {
-        const int m = i / nrow, row = row0 + (i - m * nrow);
-        float acc = 0.f;
-        for (int k = 0; k < P.S; ++k)
-            acc += __ldcg(P.ws + (int64_t(k) * P.M + m) * P.N + row);
-        P.y[int64_t(m) * P.ldy + row] = acc;
+// y[m][n] = ws[0][m][n] + ... + ws[S-1][m][n], in slice order.
+__global__ void tcb_reduce_kernel(const float *__restrict__ ws, int S, int M, int N,
+                                  float *__restrict__ y, int64_t ldy)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t n_all = int64_t(M) * N, stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_all; i += stride) {
+        float acc = __ldcs(ws + i);
+        for (int k = 1; k < S; ++k)
+            acc += __ldcs(ws + int64_t(k) * n_all + i);
+        const int64_t m = i / N;
+        y[m * ldy + (i - m * N)] = acc;
     }
-    if (threadIdx.x == 0)
-        P.tickets[r] = 0u;  // ready for the next launch
 }
 
 using TcbKernel = void (*)(TcbParams);
@@ -278,11 +282,13 @@ size_t tcb_smem(int nt, int kc)
 
 } // namespace
 
-// Grid plan: rows per pass up to 16 (NT = ceil(M/4) groups of four), K split
-// into S slices small enough that one slice of every activation row fits in
-// shared memory (more slices when there are too few row tiles to cover the
-// SMs), and about one CTA per SM: R = SMs / S row groups (at most one per row
-// tile).  QMM_TCB_S forces S (at least the number that fits).
+// Grid plan: rows per pass up to 16 (NT = ceil(M/4) groups of four); K split
+// into S slices of at most 16/NT super-blocks, so a CTA lays out at most 64
+// (super-block, row) activation items -- one round of eight per warp -- and
+// into more slices when there are too few row tiles to cover the SMs; about
+// one CTA per SM: R = SMs / S row groups (at most one per row tile).  The
+// work per CTA does not depend on S; the partial sums (S x M x N floats) do.
+// QMM_TCB_S forces S (at least the number that fits).
 TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
 {
     TcbPlan p;
@@ -292,18 +298,25 @@ TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
     int kcmax = 0;
     while (kcmax < NB && tcb_smem(p.nt, kcmax + 1) <= size_t(227 * 1024))
         ++kcmax;
-    p.S = kcmax > 0 ? (NB + kcmax - 1) / kcmax : 0;
+    if (kcmax == 0)
+        return p;
+    // One round of eight activation items per warp: KC * 4 * NT <= 64.
+    int kc = 16 / p.nt;
+    if (kc > kcmax)
+        kc = kcmax;
+    if (kc > NB)
+        kc = NB;
+    p.S = (NB + kc - 1) / kc;
     if (const char *e = getenv("QMM_TCB_S")) {
         const int f = atoi(e);
-        if (f >= p.S && f <= NB)
+        if (f >= (NB + kcmax - 1) / kcmax && f <= NB)
             p.S = f;
     }
-    if (p.S == 0)
-        return p;
     // Few row tiles: slice K further so that the grid still covers the SMs.
     if (!getenv("QMM_TCB_S") && p.S * T < sm_count) {
         const int want = sm_count / T;
-        p.S = want < NB ? want : NB;
+        if (want > p.S)
+            p.S = want < NB ? want : NB;
     }
     p.R = sm_count / p.S;
     if (p.R < 1)
@@ -313,7 +326,7 @@ TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
     p.kc = (NB + p.S - 1) / p.S;
     p.smem = tcb_smem(p.nt, p.kc);
     p.ws_floats = p.S > 1 ? size_t(p.S) * size_t(M) * size_t(N) : 0;
-    p.tickets = p.S > 1 ? size_t(p.R) : 0;
+    p.tickets = 0;
     return p;
 }
 
@@ -325,7 +338,6 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     P.x = a.x;
     P.y = a.y;
     P.ws = a.ws;
-    P.tickets = a.tickets;
     P.status = a.status;
     P.ldx = a.ldx;
     P.ldy = a.ldy;
@@ -350,7 +362,20 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    e = cudaLaunchKernelEx(&cfg, kern, P);
+    if (e != cudaSuccess || p.S == 1)
+        return e;
+    const int64_t n = int64_t(a.M) * a.N;
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = int64_t(p.R) * p.S * 8;
+    if (blocks > cap)
+        blocks = cap;
+    cudaLaunchConfig_t rc = cfg;
+    rc.gridDim = dim3(unsigned(blocks));
+    rc.blockDim = dim3(256);
+    rc.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&rc, tcb_reduce_kernel, static_cast<const float *>(a.ws), p.S, a.M,
+                              int(a.N), a.y, a.ldy);
 }
 
 } // namespace qmm

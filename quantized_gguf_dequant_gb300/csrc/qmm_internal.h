@@ -41,7 +41,7 @@ struct Matrix {
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
     alignas(64) unsigned char tmap_nib[128];
-    // batched GEMV scratch: tickets, then the K-slice partial sums (grown on demand)
+    // batched GEMV scratch: the K-slice partial sums (grown on demand)
     void *tcb_ws = nullptr;
     size_t tcb_ws_bytes = 0;
     // prefill split-K scratch: the partial products (grown on demand)
@@ -133,14 +133,14 @@ struct TcbPlan {
     int kc = 0;            // super-blocks per slice (at most)
     size_t smem = 0;
     size_t ws_floats = 0;  // partial sums, S * M * N when S > 1
-    size_t tickets = 0;    // R when S > 1
+    size_t tickets = 0;    // unused (0)
 };
 struct TcbArgs {
     const void *tmap;      // Matrix::tmap
     const float *x;
     float *y;
-    float *ws;
-    unsigned *tickets;     // zeroed, left zero by every launch
+    float *ws;             // plan.ws_floats floats when S > 1
+    unsigned *tickets;     // unused
     unsigned *status;
     int64_t ldx, ldy, N, K;
     int M;

@@ -268,8 +268,8 @@ def test_gemv_batched_one_pass(monkeypatch, M, N, K):
 
 @pytest.mark.parametrize("S", [2, 3, 7])
 def test_gemv_batched_forced_k_slices(monkeypatch, S):
-    """K split into S slices whose partial sums the last CTA adds in slice
-    order: within bounds and bitwise repeatable."""
+    """K split into S slices whose partial sums a reduction kernel adds in
+    slice order: within bounds and bitwise repeatable."""
     monkeypatch.setenv("QMM_TCB_S", str(S))
     N, K, M = 515, 256 * 14, 9
     w, m = _matrix(q.Q4_K, N, K, seed=S)
