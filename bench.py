@@ -496,15 +496,15 @@ def run_ours(args, world, rank, local):
     launches_per_step = q4.launches(True)
     launches = launches_per_step * args.steps
     # Each kernel family timed on its own (same graph + PDL set-up): the
-    # K=4096 projections run on the tensor-core kernel, down (K=14336) on the
-    # fp32 kernel.
+    # K=4096 projections run on the decode tensor-core kernel, down (K=14336)
+    # on the K-sliced one-pass tensor-core kernel.
     fam = {}
     wb = {s_: 0 for s_ in ("short", "long")}
     for name, N, K in SHAPES:
         wb["long" if K > 8192 else "short"] += N * synth.row_bytes(synth.Q4_K, K)
     xy = {"short": 4 * (3 * 4096 + 4096 + 1024 * 2 + 4096 + 14336 * 2),
           "long": 4 * (14336 + 4096)}
-    for which, kname, lpl in (("short", "gemv_tc_kernel", 3), ("long", "gemv_kernel<Q4_K>", 1)):
+    for which, kname, lpl in (("short", "gemv_tc_kernel", 3), ("long", "gemv_tcb_kernel<1>", 1)):
         ms_f, _ = time_graph(lambda: q4.step_subset(which), max(3, args.steps // 4), args.warmup,
                              world)
         b = (wb[which] + xy[which]) * nl

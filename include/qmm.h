@@ -107,7 +107,9 @@ QMM_API qmm_status qmm_gemv_group(const qmm_t *hs, int32_t n, const float *x,
 
 /* Batched decode (continuous batching): M activation rows share one read of
  * the weights.  Y[m*ldy + n] = sum_k w[n][k] * X[m*ldx + k], 1 <= M <= 16,
- * ldx >= K, ldy >= N, both multiples of 4. */
+ * ldx >= K, ldy >= N, both multiples of 4.  Q4_K from two rows on: all rows
+ * in one pass; the first call with a larger M may grow the handle's scratch
+ * (a synchronising allocation: make it before capturing a CUDA graph). */
 QMM_API qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx,
                             float *Y, int64_t ldy, qmm_stream stream);
 

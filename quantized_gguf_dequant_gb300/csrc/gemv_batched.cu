@@ -125,7 +125,9 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int item = base + i * nw;
-                if (item < items)
+                // One group of four: rows beyond M are not laid out (their
+                // columns repeat real ones below); more groups: zeros.
+                if (item < items && (NT > 1 || item / KC < P.M))
                     prep_super_block<NCOL>(item % KC, item / KC, MP, v[i], w[i], lane, Bs, Bm, inv);
             }
         }
@@ -137,6 +139,10 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
     chunk_selectors(c, selA, selB, hi4);
     const uint8_t *rowA = ring + g * 144;
     float *mypart = part + size_t(warp) * 2 * MP * kTileRows;
+    // B column of this lane: with one group of four and M < 4, columns
+    // beyond 2M repeat real ones (finite; their outputs are never stored).
+    const int col = NT == 1 ? g % (2 * P.M) : g;
+    const int cinv = NT == 1 && c >= P.M ? 0 : c;
     // One output (row tile t, rows rr and rr+8, activation row m): to Y, or to
     // this slice's partial sums.
     auto emit = [&](int t, int rr, int m, float v0, float v1) {
@@ -164,8 +170,8 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
             break;
         }
         unit_dot_nt<NT>(rowA + slot * kTileBytes, c, selA, selB, hi4,
-                        Bs + (size_t(q_sb) * 16 * NCOL + g) * 4 + c, Bm + (size_t(q_sb) * NCOL + g) * 4 + c,
-                        inv + q_sb * MP + c, tot0, tot1);
+                        Bs + (size_t(q_sb) * 16 * NCOL + col) * 4 + c,
+                        Bm + (size_t(q_sb) * NCOL + col) * 4 + c, inv + q_sb * MP + cinv, tot0, tot1);
         __syncwarp();
         if (issued < nu) {
             if (lane == 0)

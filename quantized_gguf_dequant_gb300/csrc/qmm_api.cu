@@ -113,12 +113,69 @@ qmm_status do_gemv_tc(const qmm_t *hs, int n, const float *x, int64_t ldx, int M
     return QMM_OK;
 }
 
+// The one-pass batched tensor-core kernel (gemv_batched.cu) for M rows of one
+// Q4_K matrix.  QMM_ERR_UNSUPPORTED (nothing launched) if the shape does not
+// fit its shared memory.
+qmm_status do_gemv_tcb(qmm_t h, const float *X, int64_t ldx, int M, float *Y, int64_t ldy,
+                       cudaStream_t s, const char *fn)
+{
+    Matrix &mm = *reinterpret_cast<Matrix *>(h);
+    const qmm::TcbPlan p = qmm::plan_tcb(mm.N, mm.K, M, mm.sm_count);
+    if (p.S == 0)
+        return QMM_ERR_UNSUPPORTED;
+    const size_t need = p.ws_floats * 4;
+    if (need > mm.tcb_ws_bytes) {
+        cudaError_t e = cudaSuccess;
+        if (mm.tcb_ws) {
+            e = cudaDeviceSynchronize();
+            if (e == cudaSuccess)
+                e = cudaFree(mm.tcb_ws);
+            mm.tcb_ws = nullptr;
+            mm.tcb_ws_bytes = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e, fn);
+        }
+        void *ptr = nullptr;
+        e = cudaMalloc(&ptr, need);
+        if (e != cudaSuccess)
+            return fail(QMM_ERR_NOMEM, "%s: could not allocate %zu bytes of K-slice scratch (%s)", fn,
+                        need, cudaGetErrorString(e));
+        mm.tcb_ws = ptr;
+        mm.tcb_ws_bytes = need;
+    }
+    qmm::TcbArgs a;
+    memset(&a, 0, sizeof(a));
+    a.tmap = mm.tmap;
+    a.x = X;
+    a.y = Y;
+    a.ws = p.S > 1 ? static_cast<float *>(mm.tcb_ws) : nullptr;
+    a.status = mm.status;
+    a.ldx = ldx;
+    a.ldy = ldy;
+    a.N = mm.N;
+    a.K = mm.K;
+    a.M = M;
+    cudaError_t e = qmm::launch_gemv_tcb(a, p, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    mm.last_stream = s;
+    return QMM_OK;
+}
+
 qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
     if (m0.fmt == QMM_Q4_K && tc_fits(m0, 1))
         return do_gemv_tc(hs, n, x, m0.K, 1, ys, 0, s, fn);
+    // One Q4_K matrix whose x does not fit the decode kernel (K > 8192): the
+    // K-sliced tensor-core kernel (measured faster than the fp32 kernel).
+    if (m0.fmt == QMM_Q4_K && n == 1 && !(getenv("QMM_Q4K_PATH") &&
+                                          strcmp(getenv("QMM_Q4K_PATH"), "simt") == 0)) {
+        qmm_status st = do_gemv_tcb(hs[0], x, m0.K, 1, ys[0], m0.N, s, fn);
+        if (st != QMM_ERR_UNSUPPORTED)
+            return st;
+    }
     qmm::GemvArgs a;
     memset(&a, 0, sizeof(a));
     a.fmt = m0.fmt;
@@ -368,6 +425,22 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
         return cuda_fail(e, "qmm_create");
     }
     m->ws = static_cast<float *>(p);
+    if (fmt == QMM_Q4_K) {
+        // K-slice scratch of the one-pass tensor-core kernel for one
+        // activation row (the M = 1 path when K is too long for the decode
+        // kernel), so that qmm_gemv never allocates.
+        const size_t need = qmm::plan_tcb(N, K, 1, m->sm_count).ws_floats * 4;
+        if (need > 0) {
+            e = cudaMalloc(&m->tcb_ws, need);
+            if (e != cudaSuccess) {
+                cudaFree(p);
+                delete m;
+                return fail(QMM_ERR_NOMEM, "qmm_create: could not allocate %zu bytes of K-slice "
+                                           "scratch (%s)", need, cudaGetErrorString(e));
+            }
+            m->tcb_ws_bytes = need;
+        }
+    }
     m->tickets = reinterpret_cast<unsigned *>(m->ws + m->ws_floats);
     m->status = m->tickets + m->n_tickets;
     m->tc_ws = reinterpret_cast<float *>(m->status + 64);
@@ -471,62 +544,13 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const char *bpath = getenv("QMM_BATCHED_PATH");
-    const bool force_one = bpath && strcmp(bpath, "one") == 0;
     const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
-    if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes && (force_one || M > 4 || !tc_fits(m, int(M)))) {
-        // All rows in one pass over the weights (tensor cores, K sliced when
-        // the activations do not fit in shared memory at once).  Up to four
-        // rows whose activations fit take the decode kernel below instead.
-        const qmm::TcbPlan p = qmm::plan_tcb(m.N, m.K, int(M), m.sm_count);
-        if (p.S > 0) {
-            Matrix &mm = *reinterpret_cast<Matrix *>(h);
-            const size_t tick_bytes = (p.tickets * 4 + 255) & ~size_t(255);
-            const size_t need = p.S > 1 ? tick_bytes + p.ws_floats * 4 : 0;
-            if (need > mm.tcb_ws_bytes) {
-                cudaError_t e = cudaSuccess;
-                if (mm.tcb_ws) {
-                    e = cudaDeviceSynchronize();
-                    if (e == cudaSuccess)
-                        e = cudaFree(mm.tcb_ws);
-                    mm.tcb_ws = nullptr;
-                    mm.tcb_ws_bytes = 0;
-                    if (e != cudaSuccess)
-                        return cuda_fail(e, "qmm_gemv_batched");
-                }
-                void *ptr = nullptr;
-                e = cudaMalloc(&ptr, need);
-                if (e != cudaSuccess)
-                    return fail(QMM_ERR_NOMEM, "qmm_gemv_batched: could not allocate %zu bytes of "
-                                               "K-slice scratch (%s)", need, cudaGetErrorString(e));
-                e = cudaMemset(ptr, 0, need);
-                if (e != cudaSuccess) {
-                    cudaFree(ptr);
-                    return cuda_fail(e, "qmm_gemv_batched");
-                }
-                mm.tcb_ws = ptr;
-                mm.tcb_ws_bytes = need;
-            }
-            qmm::TcbArgs a;
-            memset(&a, 0, sizeof(a));
-            a.tmap = m.tmap;
-            a.x = X;
-            a.y = Y;
-            if (p.S > 1) {
-                a.tickets = static_cast<unsigned *>(mm.tcb_ws);
-                a.ws = reinterpret_cast<float *>(static_cast<unsigned char *>(mm.tcb_ws) + tick_bytes);
-            }
-            a.status = m.status;
-            a.ldx = ldx;
-            a.ldy = ldy;
-            a.N = m.N;
-            a.K = m.K;
-            a.M = int(M);
-            cudaError_t e = qmm::launch_gemv_tcb(a, p, s);
-            if (e != cudaSuccess)
-                return cuda_fail(e, "qmm_gemv_batched");
-            mm.last_stream = s;
-            return QMM_OK;
-        }
+    if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes) {
+        // All rows in one pass over the weights (measured faster than passes
+        // of the decode kernel for every Llama shape from two rows on).
+        st = do_gemv_tcb(h, X, ldx, int(M), Y, ldy, s, "qmm_gemv_batched");
+        if (st != QMM_ERR_UNSUPPORTED)
+            return st;
     }
     // Up to four activation rows share one pass over the weights; larger
     // batches take ceil(M/4) passes.

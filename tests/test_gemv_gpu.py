@@ -249,10 +249,9 @@ def test_gemv_batched_strided_and_big_k():
 
 @pytest.mark.parametrize("M", [2, 5, 8, 12, 16])
 @pytest.mark.parametrize("N,K", [(4096, 14336), (1024, 4096), (300, 768)])
-def test_gemv_batched_one_pass(monkeypatch, M, N, K):
+def test_gemv_batched_one_pass(M, N, K):
     """All M rows in one pass (K sliced across CTAs where needed), against
     the oracle on sampled rows of the large shapes."""
-    monkeypatch.setenv("QMM_BATCHED_PATH", "one")
     w, m = _matrix(q.Q4_K, N, K, seed=M * 11 + K)
     X = synth.activations(M, K, seed=M + N)
     Y = m.gemv_batched(to_dev(X)).cpu().numpy()
