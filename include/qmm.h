@@ -151,6 +151,13 @@ QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
 QMM_API qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y,
                     qmm_stream stream);
 
+/* qmm_gemm for n matrices that share X (the q/k/v or gate/up projections of
+ * a layer's prefill) in one launch: Ys[i] is [M, N_i].  All n handles are
+ * Q4_K with the same K, n <= 4; hs and Ys are host arrays of n entries.  The
+ * split-K scratch of hs[0] is used. */
+QMM_API qmm_status qmm_gemm_group(const qmm_t *hs, int32_t n, const uint16_t *X_bf16, int64_t M,
+                                  float *const *Ys, qmm_stream stream);
+
 /* Decode rows row0 .. row0+nrows-1 to fp32: out[i*K + k] = RN_fp32(w), which
  * is the exact weight (Q8_0) or the exact weight rounded once (Q4_K; d*sc
  * and dmin*m are exact in fp32).  For tests and inspection, not the hot

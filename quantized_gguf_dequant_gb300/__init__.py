@@ -31,7 +31,7 @@ ENTRY_POINTS = (
     "qmm_create", "qmm_destroy", "qmm_gemv", "qmm_gemv_group", "qmm_gemv_batched",
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
-    "qmm_gemv_noalloc",
+    "qmm_gemv_noalloc", "qmm_gemm_group",
 )
 
 
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "qmm_last_error": [],
             "qmm_version": [],
             "qmm_gemv_noalloc": [i32, i64, i64, vp, vp, vp, vp],
+            "qmm_gemm_group": [ctypes.POINTER(vp), i32, vp, i64, ctypes.POINTER(vp), vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -156,6 +157,13 @@ def moe_ffn(hg: int, hu: int, hd: int, n_experts: int, ids, T: int, top_k: int, 
 
 def gemm(h: int, X_bf16, M: int, Y, stream=None):
     _check(lib().qmm_gemm(ctypes.c_void_p(h), _ptr(X_bf16), M, _ptr(Y), _stream(stream)))
+
+
+def gemm_group(hs, X_bf16, M: int, Ys, stream=None):
+    n = len(hs)
+    harr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(h) for h in hs])
+    yarr = (ctypes.c_void_p * n)(*[_ptr(y) for y in Ys])
+    _check(lib().qmm_gemm_group(harr, n, _ptr(X_bf16), M, yarr, _stream(stream)))
 
 
 def dequantize(h: int, row0: int, nrows: int, out, stream=None):

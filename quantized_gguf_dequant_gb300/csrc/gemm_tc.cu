@@ -78,18 +78,35 @@ constexpr size_t kSmemBytes =
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 struct GemmParams {
-    CUtensorMap tm_x;    // X [M][K] bf16, box 64 x 256, 128-byte swizzle
-    CUtensorMap tm_hdr;  // weight bytes [N][row_bytes] u8, box 16 x 256
-    CUtensorMap tm_nib;  // weight bytes, box 32 x 256
-    float *y;
-    float *ws;           // split-K partials [ksplit][M][N] (ksplit > 1)
-    int M, N, K;
+    CUtensorMap tm_x;                   // X [M][K] bf16, box 64 x 256, 128-byte swizzle
+    CUtensorMap tm_hdr[kGemmMaxGroup];  // weight bytes [N_i][row_bytes] u8, box 16 x 256
+    CUtensorMap tm_nib[kGemmMaxGroup];  // weight bytes, box 32 x 256
+    float *y[kGemmMaxGroup];            // [M][N_i]
+    int n_rows[kGemmMaxGroup];          // N_i
+    int rt_end[kGemmMaxGroup];          // cumulative 256-row tiles
+    int col_off[kGemmMaxGroup];         // first column of matrix i in the partials
+    int nmat;
+    int Ntot;                           // sum of N_i
+    float *ws;           // split-K partials [ksplit][M][Ntot] (ksplit > 1)
+    int M, K;
     int tok_tiles, tiles;
-    int ksplit;          // K slices per tile (divides K / 256)
-    int units;           // tiles * ksplit
+    int ksplit;          // K slices of each tail tile (divides K / 256)
+    int full_units;      // tiles [0, full_units) run whole, one unit each
+    int units;           // full_units + (tiles - full_units) * ksplit
     int vec_store;       // Y rows 16-byte aligned: store float4
     unsigned *status;
 };
+
+// Global 256-row tile -> (matrix of the group, first row within it).
+__device__ __forceinline__ void matrix_row_tile(const GemmParams &P, int grt, int &mi, int &row0)
+{
+    mi = 0;
+#pragma unroll
+    for (int i = 0; i < kGemmMaxGroup - 1; ++i)
+        if (i < P.nmat - 1 && grt >= P.rt_end[i])
+            mi = i + 1;
+    row0 = (grt - (mi == 0 ? 0 : P.rt_end[mi - 1])) * kRows;
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -235,8 +252,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sb_u = P.K / 256 / P.ksplit;  // super-blocks per unit
-    const int ks_u = 4 * sb_u;               // stages per unit
+    const int sb_n = P.K / 256;
+    // Unit un: a whole tile (un < full_units) or K slice `kslice` of one of
+    // the tail tiles; sb_u super-blocks from sb0 each.
+    auto unit_of = [&](int un, int &t, int &kslice, int &sb0, int &sb_u) {
+        if (un < P.full_units) {
+            t = un;
+            kslice = 0;
+            sb0 = 0;
+            sb_u = sb_n;
+        } else {
+            const int v = un - P.full_units;
+            t = P.full_units + v / P.ksplit;
+            kslice = v - (v / P.ksplit) * P.ksplit;
+            sb_u = sb_n / P.ksplit;
+            sb0 = kslice * sb_u;
+        }
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -273,9 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         if (lane == 0) {
             int it = 0, hit = 0;  // stages and super-blocks issued
             for (int un = blockIdx.x; un < P.units && !abort_flag; un += gridDim.x) {
-                const int t = un / P.ksplit, kslice = un - t * P.ksplit;
-                const int tok0 = (t % P.tok_tiles) * kTok, row0 = (t / P.tok_tiles) * kRows;
-                for (int ks = kslice * ks_u; ks < (kslice + 1) * ks_u; ++ks, ++it) {
+                int t, kslice, sb0, sb_u;
+                unit_of(un, t, kslice, sb0, sb_u);
+                int mi, row0;
+                matrix_row_tile(P, t / P.tok_tiles, mi, row0);
+                const int tok0 = (t % P.tok_tiles) * kTok;
+                for (int ks = 4 * sb0; ks < 4 * (sb0 + sb_u); ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
                     const int sb = ks >> 2, c = ks & 3;
                     if (c == 0) {
@@ -284,14 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                             !wait_phase(&hempty[h], unsigned(hu - 1) & 1u, &abort_flag, P.status))
                             break;
                         mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
-                        tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr, sb * 144, row0, &hfull[h]);
+                        tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr[mi], sb * 144, row0, &hfull[h]);
                         ++hit;
                     }
                     if (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
                         break;
                     mbar_arrive_expect_tx(&full[s], kABytes + kNibBytes);
                     tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
-                    tma_2d(sNib + s * kNibBytes, &P.tm_nib, sb * 144 + 16 + 32 * c, row0, &full[s]);
+                    tma_2d(sNib + s * kNibBytes, &P.tm_nib[mi], sb * 144 + 16 + 32 * c, row0, &full[s]);
                 }
                 if (abort_flag)
                     break;
@@ -312,7 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     break;
                 tc_fence_after();
                 bool ok = true;
-                for (int ks = 0; ks < ks_u; ++ks, ++it) {
+                int t_, ksl_, sb0_, sb_u;
+                unit_of(un, t_, ksl_, sb0_, sb_u);
+                for (int ks = 0; ks < 4 * sb_u; ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
                     if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
                         !wait_phase(&bready[s], unsigned(u) & 1u, &abort_flag, P.status)) {
@@ -349,13 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             if (!wait_phase(accfull, unsigned(lt) & 1u, &abort_flag, P.status))
                 break;
             tc_fence_after();
-            const int t = un / P.ksplit, kslice = un - t * P.ksplit;
+            int t, kslice, sb0_, sb_u_;
+            unit_of(un, t, kslice, sb0_, sb_u_);
+            const bool split = un >= P.full_units && P.ksplit > 1;
             const int tok = (t % P.tok_tiles) * kTok + tok_in_tile;
-            const int row0 = (t / P.tok_tiles) * kRows;
-            // With K split, slice k writes its partial product to ws[k] (laid
-            // out like Y); a reduction kernel adds the slices in order.
-            float *yrow = (P.ksplit > 1 ? P.ws + size_t(kslice) * size_t(P.M) * P.N : P.y) +
-                          int64_t(tok) * P.N;
+            int mi, row0;
+            matrix_row_tile(P, t / P.tok_tiles, mi, row0);
+            const int Nm = P.n_rows[mi];
+            // With K split, slice k writes its partial product to ws[k] (the
+            // group's matrices side by side, Ntot columns); a reduction
+            // kernel adds the slices in order.
+            float *yrow = split ? P.ws + (size_t(kslice) * size_t(P.M) + tok) * P.Ntot + P.col_off[mi]
+                                : P.y[mi] + int64_t(tok) * Nm;
             const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * kRows);
 #pragma unroll 1
             for (int ch = 0; ch < kRows / 32; ++ch) {
@@ -365,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 tmem_ld_wait();
                 const int n0 = row0 + ch * 32;
                 if (tok < P.M) {
-                    if (P.vec_store && n0 + 32 <= P.N) {
+                    if (P.vec_store && n0 + 32 <= Nm) {
                         float4 *dst = reinterpret_cast<float4 *>(yrow + n0);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -375,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (n0 + i < P.N)
+                            if (n0 + i < Nm)
                                 yrow[n0 + i] = __uint_as_float(r[i]);
                     }
                 }
@@ -392,8 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         int it = 0, hit = 0;
         bool ok = true;
         for (int un = blockIdx.x; un < P.units && ok; un += gridDim.x) {
-            const int kslice = un % P.ksplit;
-            for (int sb = kslice * sb_u; sb < (kslice + 1) * sb_u && ok; ++sb, ++hit) {
+            int t_, ksl_, sb0, sb_u;
+            unit_of(un, t_, ksl_, sb0, sb_u);
+            for (int sb = sb0; sb < sb0 + sb_u && ok; ++sb, ++hit) {
                 const int h = hit % kHdrSlots;
                 if (!wait_phase(&hfull[h], unsigned(hit / kHdrSlots) & 1u, &abort_flag, P.status)) {
                     ok = false;
@@ -453,32 +496,68 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     }
 }
 
-// y[i] = ws[0][i] + ws[1][i] + ... + ws[ks-1][i], in slice order.
-__global__ void splitk_reduce_kernel(const float *__restrict__ ws, int ks, int64_t n,
-                                     float *__restrict__ y, int vec)
+struct ReduceParams {
+    float *y[kGemmMaxGroup];
+    int n_rows[kGemmMaxGroup];
+    int col_off[kGemmMaxGroup];
+    int rt_end[kGemmMaxGroup];
+    int nmat, Ntot, M, ks;
+    int tok_tiles, first_tail, n_tail;  // tail tiles [first_tail, first_tail + n_tail)
+    int vec;                            // every N_i % 4 == 0 and every Y 16-byte aligned
+    const float *ws;
+};
+
+// For every tail tile (split in K): y_i[m][c] = ws[0][m][off_i + c] + ... +
+// ws[ks-1][m][off_i + c], in slice order.  Four columns per thread (a tile
+// is 256 wide and 16-byte aligned in the partials when every N_i % 4 == 0;
+// otherwise the columns are handled one by one).
+__global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
 {
     pdl_wait();
     pdl_launch_dependents();
+    const int64_t plane = int64_t(R.M) * R.Ntot;
+    const int64_t per_tile = int64_t(kTok) * (kRows / 4);
+    const int64_t n = int64_t(R.n_tail) * per_tile;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    if (vec) {
-        const int64_t n4 = n / 4;
-        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-            float4 acc = __ldcs(reinterpret_cast<const float4 *>(ws) + i);
-            for (int k = 1; k < ks; ++k) {
-                const float4 v = __ldcs(reinterpret_cast<const float4 *>(ws + size_t(k) * n) + i);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int tt = int(i / per_tile);
+        const int rem = int(i - int64_t(tt) * per_tile);
+        const int t = R.first_tail + tt;
+        const int tok = (t % R.tok_tiles) * kTok + rem / (kRows / 4);
+        const int grt = t / R.tok_tiles;
+        int mi = 0;
+#pragma unroll
+        for (int j = 0; j < kGemmMaxGroup - 1; ++j)
+            if (j < R.nmat - 1 && grt >= R.rt_end[j])
+                mi = j + 1;
+        const int row = (grt - (mi == 0 ? 0 : R.rt_end[mi - 1])) * kRows + (rem % (kRows / 4)) * 4;
+        if (tok >= R.M)
+            continue;
+        const int64_t e = int64_t(tok) * R.Ntot + R.col_off[mi] + row;
+        float *dst = R.y[mi] + int64_t(tok) * R.n_rows[mi] + row;
+        if (R.vec && row + 4 <= R.n_rows[mi]) {
+            float4 v[kMaxKSplit];
+#pragma unroll
+            for (int k = 0; k < kMaxKSplit; ++k)
+                if (k < R.ks)
+                    v[k] = __ldcs(reinterpret_cast<const float4 *>(R.ws + k * plane + e));
+            float4 acc = v[0];
+#pragma unroll
+            for (int k = 1; k < kMaxKSplit; ++k)
+                if (k < R.ks) {
+                    acc.x += v[k].x;
+                    acc.y += v[k].y;
+                    acc.z += v[k].z;
+                    acc.w += v[k].w;
+                }
+            *reinterpret_cast<float4 *>(dst) = acc;
+        } else {
+            for (int c = 0; c < 4 && row + c < R.n_rows[mi]; ++c) {
+                float acc = __ldcs(R.ws + e + c);
+                for (int k = 1; k < R.ks; ++k)
+                    acc += __ldcs(R.ws + k * plane + e + c);
+                dst[c] = acc;
             }
-            reinterpret_cast<float4 *>(y)[i] = acc;
-        }
-    } else {
-        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-            float acc = ws[i];
-            for (int k = 1; k < ks; ++k)
-                acc += ws[size_t(k) * n + i];
-            y[i] = acc;
         }
     }
 }
@@ -492,40 +571,55 @@ int gemm_q4k_tiles(int64_t M, int64_t N)
     return int((M + kTok - 1) / kTok) * int((N + kRows - 1) / kRows);
 }
 
-// K slices per tile.  Splitting costs a write and a re-read of every partial
-// product (the reduction kernel), so it is used only when the tiles fill less
-// than half of the SMs; then the count (dividing K/256, at most 16) minimises
-// waves x super-blocks per slice plus a quarter super-block per slice.
-// QMM_GEMM_KSPLIT forces a value (if it divides K/256).
-int gemm_q4k_ksplit(int64_t M, int64_t N, int64_t K, int sm_count)
+// How to cut the work into units, from a time model: a CTA spends about
+// 3.7 us per super-block of a 256 x 256 tile and runs its units one after the
+// other (one CTA per SM).  Whole tiles fill full waves; the tiles of the last,
+// partial wave (all tiles when there are fewer than the SMs) are split in K
+// into `ksplit` slices (a divisor of K/256, at most 16), which costs writing
+// and re-reading their fp32 partials at about 5 TB/s.  The count with the
+// least estimated time wins (1 = no split).  QMM_GEMM_KSPLIT forces a value
+// (if it divides K/256); then every tile is split.
+GemmSplit gemm_q4k_split(int tiles, int64_t K, int sm_count)
 {
     const int sb = int(K / 256);
-    const int tiles = gemm_q4k_tiles(M, N);
+    GemmSplit g;
+    g.full = tiles;
+    g.ksplit = 1;
     if (const char *e = getenv("QMM_GEMM_KSPLIT")) {
         const int f = atoi(e);
-        if (f >= 1 && f <= kMaxKSplit && sb % f == 0)
-            return f;
+        if (f >= 1 && f <= kMaxKSplit && sb % f == 0) {
+            g.ksplit = f;
+            g.full = f > 1 ? 0 : tiles;
+            return g;
+        }
     }
-    if (2 * tiles >= sm_count)
-        return 1;
-    int best = 1;
-    double best_cost = 1e30;
+    const int tail = tiles % sm_count;
+    if (tail == 0)
+        return g;
+    const int full = tiles - tail;
+    const double us_per_sb = 3.7, partial_bytes_per_us = 5.0e6, tile_bytes = double(kTok) * kRows * 4;
+    double best_t = 1e30;
     for (int ks = 1; ks <= kMaxKSplit && ks <= sb; ++ks) {
         if (sb % ks != 0)
             continue;
-        const double waves = double((int64_t(tiles) * ks + sm_count - 1) / sm_count);
-        const double cost = waves * (sb / ks) + (ks > 1 ? 0.25 * ks : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = ks;
+        const double waves = double((int64_t(tail) * ks + sm_count - 1) / sm_count);
+        double t = waves * (sb / ks) * us_per_sb;
+        if (ks > 1)
+            t += double(ks) * tail * tile_bytes * 2.0 / partial_bytes_per_us;
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            g.ksplit = ks;
         }
     }
-    return best;
+    g.full = g.ksplit > 1 ? full : tiles;
+    return g;
 }
 
-size_t gemm_q4k_ws_floats(int64_t M, int64_t N, int ksplit)
+size_t gemm_q4k_ws_floats(int64_t M, int64_t Ntot, int ksplit)
 {
-    return ksplit > 1 ? size_t(ksplit) * size_t(M) * size_t(N) : 0;
+    // Partials keep Y's layout (the group's matrices side by side); only the
+    // tail tiles' regions are written.
+    return ksplit > 1 ? size_t(ksplit) * size_t(M) * size_t(Ntot) : 0;
 }
 
 cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
@@ -533,18 +627,32 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     GemmParams P;
     memset(&P, 0, sizeof(P));
     memcpy(&P.tm_x, a.tmap_x, sizeof(CUtensorMap));
-    memcpy(&P.tm_hdr, a.tmap_hdr, sizeof(CUtensorMap));
-    memcpy(&P.tm_nib, a.tmap_nib, sizeof(CUtensorMap));
-    P.y = a.y;
+    P.nmat = a.nmat;
+    int rt = 0, off = 0;
+    bool vec = true;
+    for (int i = 0; i < a.nmat; ++i) {
+        memcpy(&P.tm_hdr[i], a.tmap_hdr[i], sizeof(CUtensorMap));
+        memcpy(&P.tm_nib[i], a.tmap_nib[i], sizeof(CUtensorMap));
+        P.y[i] = a.y[i];
+        P.n_rows[i] = int(a.N[i]);
+        rt += int((a.N[i] + kRows - 1) / kRows);
+        P.rt_end[i] = rt;
+        P.col_off[i] = off;
+        off += int(a.N[i]);
+        vec = vec && a.N[i] % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y[i]) & 15) == 0;
+    }
+    for (int i = a.nmat; i < kGemmMaxGroup; ++i)
+        P.rt_end[i] = rt;
+    P.Ntot = off;
     P.ws = a.ws;
     P.M = int(a.M);
-    P.N = int(a.N);
     P.K = int(a.K);
     P.tok_tiles = int((a.M + kTok - 1) / kTok);
-    P.tiles = gemm_q4k_tiles(a.M, a.N);
+    P.tiles = P.tok_tiles * rt;
     P.ksplit = a.ksplit;
-    P.units = P.tiles * P.ksplit;
-    P.vec_store = (a.N % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
+    P.full_units = a.ksplit > 1 ? a.full_tiles : P.tiles;
+    P.units = P.full_units + (P.tiles - P.full_units) * P.ksplit;
+    P.vec_store = vec ? 1 : 0;
     P.status = a.status;
     cudaError_t e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
@@ -567,9 +675,24 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     e = cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P);
     if (e != cudaSuccess || P.ksplit == 1)
         return e;
-    const int64_t n = a.M * a.N;
-    const int vec = (n % 4 == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0) ? 1 : 0;
-    const int64_t work = vec ? n / 4 : n;
+    ReduceParams R;
+    memset(&R, 0, sizeof(R));
+    for (int i = 0; i < kGemmMaxGroup; ++i) {
+        R.y[i] = P.y[i];
+        R.n_rows[i] = P.n_rows[i];
+        R.col_off[i] = P.col_off[i];
+        R.rt_end[i] = P.rt_end[i];
+    }
+    R.nmat = a.nmat;
+    R.Ntot = P.Ntot;
+    R.M = P.M;
+    R.ks = P.ksplit;
+    R.tok_tiles = P.tok_tiles;
+    R.first_tail = P.full_units;
+    R.n_tail = P.tiles - P.full_units;
+    R.ws = a.ws;
+    R.vec = vec ? 1 : 0;
+    const int64_t work = int64_t(R.n_tail) * kTok * (kRows / 4);
     int64_t blocks = (work + 255) / 256;
     if (blocks > int64_t(sm_count) * 16)
         blocks = int64_t(sm_count) * 16;
@@ -577,8 +700,7 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     rc.gridDim = dim3(unsigned(blocks));
     rc.blockDim = dim3(256);
     rc.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, static_cast<const float *>(a.ws), P.ksplit, n,
-                              a.y, vec);
+    return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, R);
 }
 
 } // namespace qmm

@@ -738,30 +738,38 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     return QMM_OK;
 }
 
-qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_stream stream)
+// The prefill GEMM for n Q4_K matrices sharing X (n <= 4).
+static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, int64_t M,
+                              float *const *Ys, qmm_stream stream, const char *fn)
 {
-    g_err.clear();
-    const char *fn = "qmm_gemm";
-    qmm_status st = check_handle(h, fn);
-    if (st != QMM_OK)
-        return st;
-    Matrix *m = reinterpret_cast<Matrix *>(h);
-    if (m->fmt != QMM_Q4_K)
-        return fail(QMM_ERR_UNSUPPORTED,
-                    "%s: the prefill GEMM is implemented for Q4_K weights only (this handle is "
-                    "format %d)", fn, m->fmt);
-    if (!X_bf16 || !Y)
-        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X_bf16 ? "X" : "Y");
+    for (int i = 0; i < n; ++i) {
+        qmm_status st = check_handle(hs[i], fn);
+        if (st != QMM_OK)
+            return st;
+        const Matrix *mi = reinterpret_cast<const Matrix *>(hs[i]);
+        if (mi->fmt != QMM_Q4_K)
+            return fail(QMM_ERR_UNSUPPORTED,
+                        "%s: the prefill GEMM is implemented for Q4_K weights only (matrix %d is "
+                        "format %d)", fn, i, mi->fmt);
+        if (mi->K != reinterpret_cast<const Matrix *>(hs[0])->K)
+            return fail(QMM_ERR_SHAPE, "%s: matrix %d has K = %lld, matrix 0 K = %lld", fn, i,
+                        (long long)mi->K, (long long)reinterpret_cast<const Matrix *>(hs[0])->K);
+        if (mi->N > (int64_t(1) << 30))
+            return fail(QMM_ERR_SHAPE, "%s: N = %lld rows exceed the GEMM's limit of 2^30", fn,
+                        (long long)mi->N);
+        if (!Ys[i])
+            return fail(QMM_ERR_NULL, "%s: output %d is NULL", fn, i);
+        if (!aligned(Ys[i], 4))
+            return fail(QMM_ERR_ALIGN, "%s: output %d is not 4-byte aligned", fn, i);
+    }
+    Matrix *m = reinterpret_cast<Matrix *>(hs[0]);
+    if (!X_bf16)
+        return fail(QMM_ERR_NULL, "%s: X is NULL", fn);
     if (M < 1 || M > (int64_t(1) << 24))
         return fail(QMM_ERR_SHAPE, "%s: M = %lld; 1 <= M <= 16777216 is supported", fn,
                     (long long)M);
-    if (m->N > (int64_t(1) << 30))
-        return fail(QMM_ERR_SHAPE, "%s: N = %lld rows exceed the GEMM's limit of 2^30", fn,
-                    (long long)m->N);
     if (!aligned(X_bf16, 16))
         return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
-    if (!aligned(Y, 4))
-        return fail(QMM_ERR_ALIGN, "%s: Y is not 4-byte aligned", fn);
     alignas(64) unsigned char tmx[128];
     if (qmm::encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X_bf16, uint64_t(m->K),
                             uint64_t(M), uint64_t(m->K) * 2, 64u, 256u,
@@ -769,11 +777,25 @@ qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_st
         return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
     qmm::GemmArgs a;
     memset(&a, 0, sizeof(a));
-    a.ksplit = qmm::gemm_q4k_ksplit(M, m->N, m->K, m->sm_count);
+    int64_t Ntot = 0;
+    int tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const Matrix *mi = reinterpret_cast<const Matrix *>(hs[i]);
+        a.tmap_hdr[i] = mi->tmap_hdr;
+        a.tmap_nib[i] = mi->tmap_nib;
+        a.y[i] = Ys[i];
+        a.N[i] = mi->N;
+        Ntot += mi->N;
+        tiles += qmm::gemm_q4k_tiles(M, mi->N);
+    }
+    a.nmat = n;
+    const qmm::GemmSplit split = qmm::gemm_q4k_split(tiles, m->K, m->sm_count);
+    a.ksplit = split.ksplit;
+    a.full_tiles = split.full;
     if (a.ksplit > 1) {
-        // Split K: the partial products; the scratch grows on demand (waiting
-        // for the device first).
-        const size_t need = qmm::gemm_q4k_ws_floats(M, m->N, a.ksplit) * 4;
+        // Split K: the partial products; the scratch of matrix 0 grows on
+        // demand (waiting for the device first).
+        const size_t need = qmm::gemm_q4k_ws_floats(M, Ntot, a.ksplit) * 4;
         if (need > m->gemm_ws_bytes) {
             cudaError_t e = cudaSuccess;
             if (m->gemm_ws) {
@@ -796,11 +818,7 @@ qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_st
         a.ws = static_cast<float *>(m->gemm_ws);
     }
     a.tmap_x = tmx;
-    a.tmap_hdr = m->tmap_hdr;
-    a.tmap_nib = m->tmap_nib;
-    a.y = Y;
     a.M = M;
-    a.N = m->N;
     a.K = m->K;
     a.status = m->status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -809,6 +827,24 @@ qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_st
         return cuda_fail(e, fn);
     m->last_stream = s;
     return QMM_OK;
+}
+
+qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y, qmm_stream stream)
+{
+    g_err.clear();
+    return gemm_common(&h, 1, X_bf16, M, &Y, stream, "qmm_gemm");
+}
+
+qmm_status qmm_gemm_group(const qmm_t *hs, int32_t n, const uint16_t *X_bf16, int64_t M,
+                          float *const *Ys, qmm_stream stream)
+{
+    g_err.clear();
+    if (!hs || !Ys)
+        return fail(QMM_ERR_NULL, "qmm_gemm_group: the %s array is NULL", !hs ? "handle" : "output");
+    if (n < 1 || n > qmm::kGemmMaxGroup)
+        return fail(QMM_ERR_SHAPE, "qmm_gemm_group: n = %d; between 1 and %d matrices are supported",
+                    n, qmm::kGemmMaxGroup);
+    return gemm_common(hs, n, X_bf16, M, Ys, stream, "qmm_gemm_group");
 }
 
 static qmm_status dequant_common(qmm_t h, int64_t row0, int64_t nrows, float *of, uint16_t *ob,

@@ -155,20 +155,28 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle);
 
 // --------------------------------------------------------------- prefill GEMM
+constexpr int kGemmMaxGroup = 4;
 struct GemmArgs {
-    const void *tmap_x;    // X [M][K] bf16: box 64 x 256, 128-byte swizzle
-    const void *tmap_hdr;  // Matrix::tmap_hdr
-    const void *tmap_nib;  // Matrix::tmap_nib
-    float *y;              // [M][N]
+    const void *tmap_x;                  // X [M][K] bf16: box 64 x 256, 128-byte swizzle
+    const void *tmap_hdr[kGemmMaxGroup]; // Matrix::tmap_hdr of each matrix
+    const void *tmap_nib[kGemmMaxGroup]; // Matrix::tmap_nib
+    float *y[kGemmMaxGroup];             // [M][N_i]
+    int64_t N[kGemmMaxGroup];
+    int nmat;
     float *ws;             // split-K partials (gemm_q4k_ws_floats floats) when ksplit > 1
-    int ksplit;
-    int64_t M, N, K;
+    int ksplit;            // K slices of each tail tile
+    int full_tiles;        // tiles that run whole (the rest are split) when ksplit > 1
+    int64_t M, K;
     unsigned *status;
 };
 size_t gemm_q4k_smem();
 int gemm_q4k_tiles(int64_t M, int64_t N);
-int gemm_q4k_ksplit(int64_t M, int64_t N, int64_t K, int sm_count);
-size_t gemm_q4k_ws_floats(int64_t M, int64_t N, int ksplit);
+struct GemmSplit {
+    int full;    // whole tiles (the first ones)
+    int ksplit;  // K slices of each remaining tile (1: none split)
+};
+GemmSplit gemm_q4k_split(int tiles, int64_t K, int sm_count);
+size_t gemm_q4k_ws_floats(int64_t M, int64_t Ntot, int ksplit);
 cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s);
 
 // --------------------------------------------------------------- mixture of experts

@@ -158,3 +158,62 @@ def test_gemm_split_k_forced(monkeypatch, ksplit):
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
     assert np.array_equal(y2.view(np.uint32), y3.view(np.uint32))
     m.close()
+
+
+@pytest.mark.parametrize("ksplit", [None, 2])
+@pytest.mark.parametrize("Ns,K,M", [((300, 64, 513), 1024, 300), ((4096, 1024, 1024), 4096, 512)])
+def test_gemm_group(monkeypatch, ksplit, Ns, K, M):
+    """qmm_gemm_group: matrices sharing X in one launch (ragged row counts, so
+    row tiles of different matrices meet mid-launch), each against the oracle."""
+    if ksplit:
+        monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
+    ws = [synth.q4k_matrix(N, K, 40 + i) for i, N in enumerate(Ns)]
+    ms = [q.Matrix(q.Q4_K, N, K, to_dev(w)) for N, w in zip(Ns, ws)]
+    Xb = synth.activations_bf16(M, K, 41)
+    Ys = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") for N in Ns]
+    q.gemm_group([m.h for m in ms], to_dev(Xb.view(np.int16)), M, Ys)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(K)
+    for N, w, Y in zip(Ns, ws, Ys):
+        rows = None if N <= 600 else np.unique(np.concatenate(
+            [np.arange(4), np.arange(N - 4, N), rng.choice(N, 24, False)]))
+        y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS)
+        got = Y.cpu().numpy() if rows is None else Y.cpu().numpy()[:, rows]
+        assert_close_to_oracle(got, y_ref, c, TIGHT, f"group N={N}")
+    assert ms[0].status() == 0
+    for m in ms:
+        m.close()
+
+
+def test_gemm_group_refusals():
+    K = 256
+    a = q.Matrix(q.Q4_K, 64, K, to_dev(synth.q4k_matrix(64, K, 1)))
+    b = q.Matrix(q.Q4_K, 64, 512, to_dev(synth.q4k_matrix(64, 512, 2)))
+    X = torch.zeros((4, K), dtype=torch.int16, device="cuda")
+    Y = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(q.QmmError) as ei:
+        q.gemm_group([a.h, b.h], X, 4, [Y, Y])
+    assert ei.value.status == q.ERR_SHAPE
+    with pytest.raises(q.QmmError) as ei:
+        q.gemm_group([a.h] * 5, X, 4, [Y] * 5)
+    assert ei.value.status == q.ERR_SHAPE
+    a.close()
+    b.close()
+
+
+def test_gemm_tail_wave_split():
+    """More tiles than SMs: full waves run whole tiles, the tail wave's tiles
+    are split in K (reduced in slice order) -- rows from both kinds."""
+    M, N, K = 300, 20480, 1024
+    w = synth.q4k_matrix(N, K, 77)
+    Xb = synth.activations_bf16(M, K, 78)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    Y1 = _run(m, Xb, M)
+    Y2 = _run(m, Xb, M)
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(N - 8, N), rng.choice(N, 56, False),
+                                     np.arange(19456, 19456 + 8)]))
+    y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS)
+    assert_close_to_oracle(Y1[:, rows], y_ref, c, TIGHT, "tail split")
+    m.close()
