@@ -162,7 +162,14 @@ struct MoeParams {
     int top_k;
     int x_per_slot;
     int nslot;
+    // fuse = 1 (nmat = 2, gate and up): tiles are taken in (gate, up) pairs
+    // of the same rows, staged in shared memory (room for maxpairs pairs per
+    // CTA) and y[0] receives h = silu(gate) * up instead of either product.
+    int fuse;
+    int maxpairs;
 };
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 // One CTA: an even share of the (group, tile) sequence; within it, one
 // segment per group, each computed like the decode GEMV (warps split the
@@ -181,8 +188,10 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
     uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(NB) * 16 * kNcol * 4);  // [NB][8][4]
     float *inv = reinterpret_cast<float *>(Bm + size_t(NB) * kNcol * 4);            // [NB][4]
     float *part = inv + size_t(NB) * kGroupTokens;                                 // [nw][2][4][16]
+    float *res = part + size_t(nw) * 2 * 4 * kTileRows;  // fused: [2*maxpairs][4][16] tile results
     uint64_t *bars = reinterpret_cast<uint64_t *>(
-        (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * 4 * kTileRows) + 7) & ~uintptr_t(7));
+        (reinterpret_cast<uintptr_t>(res + size_t(P.fuse ? 2 * P.maxpairs : 0) * 4 * kTileRows) + 7) &
+        ~uintptr_t(7));
     uint64_t *bar = bars + warp * NS;
     __shared__ int wbeg[17];
     __shared__ int gslot[kGroupTokens];
@@ -200,7 +209,21 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
     const int tilesG = P.nmat * P.tpm;             // tiles per group
     const int64_t Ttot = int64_t(*P.n_groups) * tilesG;
     const int64_t G = gridDim.x;
-    const int64_t t0 = blockIdx.x * Ttot / G, t1 = (blockIdx.x + 1) * Ttot / G;
+    // Fused: CTAs take whole (gate, up) pairs, so the split is over pairs.
+    const int64_t unit_tiles = P.fuse ? 2 : 1;
+    const int64_t Tsplit = Ttot / unit_tiles;
+    const int64_t t0 = (blockIdx.x * Tsplit / G) * unit_tiles,
+                  t1 = ((blockIdx.x + 1) * Tsplit / G) * unit_tiles;
+    // Local tile of a group -> (matrix, 16-row tile of the expert).
+    auto tile_mat = [&](int lt, int &mat, int &rt) {
+        if (P.fuse) {
+            mat = lt & 1;
+            rt = lt >> 1;
+        } else {
+            mat = lt >= P.tpm ? 1 : 0;
+            rt = lt - mat * P.tpm;
+        }
+    };
 
     uint32_t selA, selB;
     bool hi4;
@@ -238,8 +261,8 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
         int i_tile = lt0 + u0 / NB, i_sb = u0 % NB;
         int slot_i = gbase % NS;
         auto issue = [&]() {
-            const int mat = i_tile >= P.tpm ? 1 : 0;
-            const int lt = i_tile - mat * P.tpm;
+            int mat, lt;
+            tile_mat(i_tile, mat, lt);
             mbar_arrive_expect_tx(&bar[slot_i], kTileBytes);
             tma_load_2d(ring + size_t(slot_i) * kTileBytes, &P.tmap[mat], i_sb * 18,
                         grp.x * P.Ne + lt * kTileRows, &bar[slot_i], 0ull);
@@ -306,9 +329,14 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
                 const int first = (ju / NB) * NB, last = first + NB - 1;
                 if (u0 <= first && u1 - 1 >= last) {
                     const int s = gslot[mrow];
-                    if (s >= 0) {
-                        const int mat = q_tile >= P.tpm ? 1 : 0;
-                        const int r = (q_tile - mat * P.tpm) * kTileRows + g;
+                    if (P.fuse) {
+                        float *rr = res + (size_t(q_tile - lt0) * 4 + mrow) * kTileRows;
+                        rr[g] = tot0;
+                        rr[g + 8] = tot1;
+                    } else if (s >= 0) {
+                        int mat, rt;
+                        tile_mat(q_tile, mat, rt);
+                        const int r = rt * kTileRows + g;
                         float *yr = P.y[mat] + int64_t(s) * P.Ne;
                         if (r < P.Ne)
                             yr[r] = tot0;
@@ -364,15 +392,34 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
                 s1 += pw[cr + 8];
             }
             const int s = gslot[cm];
-            if (s >= 0) {
-                const int lt = lt0 + tr;
-                const int mat = lt >= P.tpm ? 1 : 0;
-                const int r = (lt - mat * P.tpm) * kTileRows + cr;
+            if (P.fuse) {
+                float *rr = res + (size_t(tr) * 4 + cm) * kTileRows;
+                rr[cr] = s0;
+                rr[cr + 8] = s1;
+            } else if (s >= 0) {
+                int mat, rt;
+                tile_mat(lt0 + tr, mat, rt);
+                const int r = rt * kTileRows + cr;
                 float *yr = P.y[mat] + int64_t(s) * P.Ne;
                 if (r < P.Ne)
                     yr[r] = s0;
                 if (r + 8 < P.Ne)
                     yr[r + 8] = s1;
+            }
+        }
+        if (P.fuse && !failed) {
+            // ---- h = silu(gate) * up for every (pair, token, row) of the segment
+            __syncthreads();
+            const int npair = ntile / 2;
+            for (int i = threadIdx.x; i < npair * 4 * kTileRows; i += blockDim.x) {
+                const int pl = i / (4 * kTileRows), m = (i / kTileRows) & 3, rr = i % kTileRows;
+                const int s = gslot[m];
+                const int r = ((lt0 >> 1) + pl) * kTileRows + rr;
+                if (s < 0 || r >= P.Ne)
+                    continue;
+                const float gv = res[(size_t(2 * pl) * 4 + m) * kTileRows + rr];
+                const float uv = res[(size_t(2 * pl + 1) * 4 + m) * kTileRows + rr];
+                P.y[0][int64_t(s) * P.Ne + r] = silu(gv) * uv;
             }
         }
         gbase += nu;
@@ -382,8 +429,6 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
 }
 
 // ------------------------------------------------------------------ elementwise
-
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 __global__ void swiglu_kernel(const float *__restrict__ g, const float *__restrict__ u,
                               float *__restrict__ h, int64_t n)
@@ -459,13 +504,13 @@ void moe_expert_shape(int64_t K, int &nw, int &nslot)
         nw = atoi(ew);
     if (es && atoi(es) > 0)
         nslot = atoi(es);
-    if (!(ew || es) && moe_expert_smem(K, nw, nslot) > size_t(227 * 1024)) {
+    if (!(ew || es) && moe_expert_smem(K, nw, nslot, 0) > size_t(227 * 1024)) {
         nw = 8;
         nslot = 4;
     }
 }
 
-size_t moe_expert_smem(int64_t K, int nw, int nslot)
+size_t moe_expert_smem(int64_t K, int nw, int nslot, int maxpairs)
 {
     const size_t NB = size_t(K / 256);
     size_t b = size_t(nw) * nslot * kTileBytes;
@@ -473,6 +518,7 @@ size_t moe_expert_smem(int64_t K, int nw, int nslot)
     b += NB * kNcol * 4 * sizeof(uint32_t);
     b += NB * kGroupTokens * sizeof(float);
     b += size_t(nw) * 2 * 4 * kTileRows * sizeof(float);
+    b += size_t(2 * maxpairs) * 4 * kTileRows * sizeof(float);
     b = (b + 7) & ~size_t(7);
     b += size_t(nw) * nslot * sizeof(uint64_t);
     return b;
@@ -498,10 +544,12 @@ cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t
     P.NB = int(a.K / 256);
     P.top_k = a.top_k;
     P.x_per_slot = a.x_per_slot;
+    P.fuse = a.fuse_swiglu;
+    P.maxpairs = a.fuse_swiglu ? a.maxpairs : 0;
     int nw, nslot;
     moe_expert_shape(a.K, nw, nslot);
     P.nslot = nslot;
-    const size_t smem = moe_expert_smem(a.K, nw, nslot);
+    const size_t smem = moe_expert_smem(a.K, nw, nslot, P.maxpairs);
     cudaError_t e = cudaFuncSetAttribute(moe_expert_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess)

@@ -242,10 +242,10 @@ qmm_status moe_check(const Matrix &m, int n_experts, const int32_t *ids, int T, 
         return fail(QMM_ERR_ALIGN, "%s: expert_ids is not 4-byte aligned", fn);
     int nw, nslot;
     qmm::moe_expert_shape(m.K, nw, nslot);
-    if (qmm::moe_expert_smem(m.K, nw, nslot) > kMaxSmem)
+    if (qmm::moe_expert_smem(m.K, nw, nslot, 0) > kMaxSmem)
         return fail(QMM_ERR_SHAPE, "%s: K = %lld is too long for the expert kernel's shared "
                     "memory (%zu bytes needed)", fn, (long long)m.K,
-                    qmm::moe_expert_smem(m.K, nw, nslot));
+                    qmm::moe_expert_smem(m.K, nw, nslot, 0));
     return QMM_OK;
 }
 
@@ -701,21 +701,34 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     a.top_k = top_k;
     a.ix = ms.ix;
     a.status = mg->status;
-    if (e == cudaSuccess) {  // gate and up, one launch
+    // Gate and up in one launch.  With room in shared memory for every CTA's
+    // (gate, up) tile pairs, SwiGLU is applied in the same launch; otherwise
+    // a separate kernel combines the two products.
+    int nw = 0, nslot = 0;
+    qmm::moe_expert_shape(d_model, nw, nslot);
+    const int64_t tpm = (d_ff + 15) / 16;
+    const int maxpairs =
+        int((int64_t(qmm::moe_max_groups(S, n_experts)) * tpm + sms - 1) / sms) + 1;
+    const bool fuse = !getenv("QMM_MOE_NOFUSE") &&
+                      qmm::moe_expert_smem(d_model, nw, nslot, maxpairs) <= kMaxSmem;
+    if (e == cudaSuccess) {
         a.tmap[0] = mg->tmap;
         a.tmap[1] = mu->tmap;
-        a.y[0] = ms.g;
-        a.y[1] = ms.u;
+        a.y[0] = fuse ? ms.h : ms.g;
+        a.y[1] = fuse ? nullptr : ms.u;
         a.nmat = 2;
         a.Ne = d_ff;
         a.K = d_model;
         a.x = X;
         a.ldx = d_model;
         a.x_per_slot = 0;
+        a.fuse_swiglu = fuse ? 1 : 0;
+        a.maxpairs = maxpairs;
         e = qmm::launch_moe_expert(a, sms, s);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !fuse)
         e = qmm::launch_swiglu(ms.g, ms.u, ms.h, int64_t(S) * d_ff, sms, s);
+    a.fuse_swiglu = 0;
     if (e == cudaSuccess) {  // down, one input row per slot
         a.tmap[0] = md->tmap;
         a.tmap[1] = nullptr;

@@ -204,6 +204,8 @@ struct MoeExpertArgs {
     int64_t ldx;
     int top_k;
     int x_per_slot;
+    int fuse_swiglu;      // nmat == 2: y[0] = silu(gate) * up, y[1] unused
+    int maxpairs;         // (fused) shared-memory room: (gate, up) tile pairs per CTA
     MoeIndex ix;
     unsigned *status;
 };
@@ -212,7 +214,7 @@ size_t moe_bucket_smem(int S, int E);
 cudaError_t launch_moe_bucket(const int32_t *ids, int S, int E, const MoeIndex &ix, float *y0,
                               int64_t n0, int64_t ld0, unsigned *status, cudaStream_t s);
 void moe_expert_shape(int64_t K, int &nw, int &nslot);
-size_t moe_expert_smem(int64_t K, int nw, int nslot);
+size_t moe_expert_smem(int64_t K, int nw, int nslot, int maxpairs);
 cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t s);
 cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, int sm_count,
                           cudaStream_t s);

@@ -236,11 +236,17 @@ def _run_ffn(hs, E, ids, r, X, d_model, stream=None):
     return Y
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("E,d_model,d_ff,T,top_k", [
     (4, 512, 256, 3, 2),
+    (6, 768, 512, 9, 3),
     (synth.OLMOE_EXPERTS, synth.OLMOE_D_MODEL, synth.OLMOE_D_FF, 32, synth.OLMOE_TOP_K),
 ])
-def test_moe_ffn(E, d_model, d_ff, T, top_k):
+def test_moe_ffn(monkeypatch, fused, E, d_model, d_ff, T, top_k):
+    """The whole expert FFN, with SwiGLU fused into the gate/up launch or as
+    its own kernel."""
+    if not fused:
+        monkeypatch.setenv("QMM_MOE_NOFUSE", "1")
     wg, wu, wd, ids, r, X = _ffn_case(E, d_model, d_ff, T, top_k, seed=E + T)
     y_ref, c = _ffn_bound(wg, wu, wd, E, d_model, d_ff, ids, r, X)
     hs = [q.Matrix(q.Q4_K, E * d_ff, d_model, to_dev(wg)),
