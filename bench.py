@@ -376,6 +376,17 @@ class PrefillModel:
                 m.close()
 
 
+def launches_of(fn):
+    """Kernels the library launches for one call of fn (counted by the
+    library itself; run eagerly, outside any capture)."""
+    import torch
+    import quantized_gguf_dequant_gb300 as q
+    c0 = q.launch_count()
+    fn()
+    torch.cuda.synchronize()
+    return q.launch_count() - c0
+
+
 def time_graph(fn, steps, warmup, world, sampler_index=None):
     """Capture fn into a CUDA graph, replay warmup + steps; returns (ms/step,
     clocks summary)."""
@@ -497,7 +508,7 @@ def run_ours(args, world, rank, local):
         ms, clocks = time_eager(lambda: q4.step(True), args.steps, args.warmup, world)
     gbs = step_bytes / (ms * 1e-3) / 1e9 * world
     per_gpu = step_bytes / (ms * 1e-3) / 1e9
-    launches_per_step = q4.launches(True)
+    launches_per_step = launches_of(lambda: q4.step(True))
     launches = launches_per_step * args.steps
     # Each kernel family timed on its own (same graph + PDL set-up): the
     # K=4096 projections run on the decode tensor-core kernel, down (K=14336)
@@ -513,7 +524,8 @@ def run_ours(args, world, rank, local):
                              world)
         b = (wb[which] + xy[which]) * nl
         fam[which] = {"kernel": kname, "ms_per_step": ms_f, "bytes_per_step": b,
-                      "launches_per_step": lpl * nl, "gbs": b / (ms_f * 1e-3) / 1e9}
+                      "launches_per_step": launches_of(lambda: q4.step_subset(which)),
+                      "gbs": b / (ms_f * 1e-3) / 1e9}
     extras = {}
     e2e = None
     if args.e2e:
@@ -528,7 +540,7 @@ def run_ours(args, world, rank, local):
         ms_u, _ = time_graph(lambda: q4.step(False), max(3, args.steps // 4), args.warmup, world)
         extras["q4k_decode_ungrouped"] = {
             "value": step_bytes / (ms_u * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_u,
-            "launches_per_step": q4.launches(False),
+            "launches_per_step": launches_of(lambda: q4.step(False)),
             "frac_of_peak": step_bytes / (ms_u * 1e-3) / 1e9 / pk["hbm_gbs"]}
     if args.extras:
         bm = BatchedModel(q4)
@@ -538,9 +550,10 @@ def run_ours(args, world, rank, local):
             b = bm.bytes_per_step(M)
             sweep[str(M)] = {"ms_per_step": ms_b, "gbs": b / (ms_b * 1e-3) / 1e9,
                              "frac_of_peak": b / (ms_b * 1e-3) / 1e9 / pk["hbm_gbs"],
-                             "tokens_per_s": M / (ms_b * 1e-3)}
+                             "tokens_per_s": M / (ms_b * 1e-3),
+                             "launches_per_step": launches_of(lambda: bm.step(M))}
         extras["q4k_batched_decode"] = {
-            "unit": "GB/s", "by_M": sweep, "launches_per_step": 7 * nl,
+            "unit": "GB/s", "by_M": sweep,
             "note": "qmm_gemv_batched on every matrix of every layer, M activation rows per "
                     "call; bytes = weights once + M input rows + M output rows"}
         del bm
@@ -555,7 +568,7 @@ def run_ours(args, world, rank, local):
             "value": bm_ / (ms_m * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_m,
             "bytes_per_step": bm_, "layers": len(mo.layers), "tokens": mo.T,
             "frac_of_peak": bm_ / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"],
-            "us_per_layer": ms_m * 1e3 / len(mo.layers), "launches_per_step": 5 * len(mo.layers),
+            "us_per_layer": ms_m * 1e3 / len(mo.layers), "launches_per_step": launches_of(mo.step),
             "note": "qmm_moe_ffn per layer (bucket, gate+up, SwiGLU, down, combine); bytes = "
                     "the Q4_K gate/up/down bytes of every expert some token picked, plus X, Y, "
                     "ids and routing weights; 16 layers = 3.6 GB of experts > L2"}
@@ -571,7 +584,7 @@ def run_ours(args, world, rank, local):
             tf = fl / (ms_p * 1e-3) / 1e12
             pre[str(M)] = {"ms_per_step": ms_p, "tflops": tf,
                            "frac_of_peak": tf / pk["bf16_tflops"],
-                           "launches_per_step": 4 * len(pm.mats)}
+                           "launches_per_step": launches_of(pm.step)}
             pm.close()
             del pm
             torch.cuda.empty_cache()

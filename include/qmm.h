@@ -201,6 +201,11 @@ QMM_API const char *qmm_last_error(void);
 /* Library version as an integer (major*10000 + minor*100 + patch). */
 QMM_API int32_t qmm_version(void);
 
+/* Kernel launches this library has issued in this process so far (all entry
+ * points, all devices), for instrumentation: the difference across a region
+ * counts the library's kernels in it.  Never fails. */
+QMM_API int64_t qmm_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ ENTRY_POINTS = (
     "qmm_create", "qmm_destroy", "qmm_gemv", "qmm_gemv_group", "qmm_gemv_batched",
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
-    "qmm_gemv_noalloc", "qmm_gemm_group",
+    "qmm_gemv_noalloc", "qmm_gemm_group", "qmm_launch_count",
 )
 
 
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             f.argtypes = args
             f.restype = i32
         L.qmm_last_error.restype = ctypes.c_char_p
+        L.qmm_launch_count.argtypes = []
+        L.qmm_launch_count.restype = ctypes.c_int64
         _lib = L
     return _lib
 
@@ -85,6 +87,11 @@ def last_error() -> str:
 
 def version() -> int:
     return int(lib().qmm_version())
+
+
+def launch_count() -> int:
+    """Kernel launches the library has issued in this process so far."""
+    return int(lib().qmm_launch_count())
 
 
 def _check(rc: int):

@@ -93,7 +93,7 @@ cudaError_t launch_dequant(const Matrix &m, int64_t row0, int64_t nrows, float *
             dequant_kernel<QMM_Q8_0, false><<<blocks, threads, 0, s>>>(m.w, m.K, m.row_bytes, row0,
                                                                        nrows, out_f32, nullptr);
     }
-    return cudaGetLastError();
+    return counted(cudaGetLastError());
 }
 
 } // namespace qmm

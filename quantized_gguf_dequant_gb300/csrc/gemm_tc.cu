@@ -672,7 +672,7 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P);
+    e = counted(cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P));
     if (e != cudaSuccess || P.ksplit == 1)
         return e;
     ReduceParams R;
@@ -700,7 +700,7 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     rc.gridDim = dim3(unsigned(blocks));
     rc.blockDim = dim3(256);
     rc.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&rc, splitk_reduce_kernel, R);
+    return counted(cudaLaunchKernelEx(&rc, splitk_reduce_kernel, R));
 }
 
 } // namespace qmm

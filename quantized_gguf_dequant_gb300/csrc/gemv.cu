@@ -608,7 +608,7 @@ cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    return counted(cudaLaunchKernelEx(&cfg, kern, P));
 }
 
 } // namespace qmm

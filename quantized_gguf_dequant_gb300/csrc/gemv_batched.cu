@@ -368,7 +368,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, kern, P);
+    e = counted(cudaLaunchKernelEx(&cfg, kern, P));
     if (e != cudaSuccess || p.S == 1)
         return e;
     const int64_t n = int64_t(a.M) * a.N;
@@ -380,8 +380,8 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     rc.gridDim = dim3(unsigned(blocks));
     rc.blockDim = dim3(256);
     rc.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&rc, tcb_reduce_kernel, static_cast<const float *>(a.ws), p.S, a.M,
-                              int(a.N), a.y, a.ldy);
+    return counted(cudaLaunchKernelEx(&rc, tcb_reduce_kernel, static_cast<const float *>(a.ws), p.S, a.M,
+                              int(a.N), a.y, a.ldy));
 }
 
 } // namespace qmm

@@ -408,7 +408,7 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, P);
+    return counted(cudaLaunchKernelEx(&cfg, kern, P));
 }
 
 // Describe the rows of a Q4_K matrix as a 2-D tensor of 8-byte elements

@@ -476,7 +476,7 @@ cudaError_t launch_ex(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k, args...);
+    return counted(cudaLaunchKernelEx(&cfg, k, args...));
 }
 
 } // namespace

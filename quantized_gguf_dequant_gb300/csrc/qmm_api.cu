@@ -5,6 +5,7 @@
 // Refusal convention: "Frink Inference: the Rust alternative to llama.cpp",
 // section "The goal, stated once" -- load, or refuse with a sentence naming
 // exactly what is missing; never compute something else.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -304,6 +305,12 @@ qmm_status moe_scratch(Matrix &m, int S, int E, size_t ys_floats, size_t ff_floa
 
 namespace qmm {
 
+namespace {
+std::atomic<int64_t> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 qmm_status noalloc_fail(qmm_status code, const char *fmt, ...)
 {
     char buf[512];
@@ -346,6 +353,8 @@ extern "C" {
 const char *qmm_last_error(void) { return g_err.c_str(); }
 
 int32_t qmm_version(void) { return 100; }
+
+int64_t qmm_launch_count(void) { return qmm::g_launches.load(std::memory_order_relaxed); }
 
 qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, qmm_t *out)
 {

@@ -59,6 +59,16 @@ inline int64_t row_bytes_of(int fmt, int64_t K)
     return fmt == QMM_Q4_K ? (K / 256) * 144 : (K / 32) * 34;
 }
 
+// Kernel launches issued by the library (qmm_launch_count): every launcher
+// passes its launch status through counted().
+void count_launch();
+inline cudaError_t counted(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        count_launch();
+    return e;
+}
+
 // Programmatic dependent launch on every kernel unless QMM_PDL=0.
 inline bool pdl_enabled()
 {

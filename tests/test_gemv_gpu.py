@@ -279,3 +279,14 @@ def test_gemv_batched_forced_k_slices(monkeypatch, S):
     assert_close_to_oracle(Y1, Yr, C, TOL_FP32, f"batched S={S}")
     assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
     m.close()
+
+
+def test_launch_count_counts_kernels():
+    """qmm_launch_count advances by the kernels each call launches."""
+    w, m = _matrix(q.Q4_K, 512, 1024, seed=5)
+    x = to_dev(synth.activations(1, 1024, 6)[0])
+    c0 = q.launch_count()
+    m.gemv(x)
+    torch.cuda.synchronize()
+    assert q.launch_count() - c0 == 1
+    m.close()
