@@ -52,10 +52,7 @@ namespace qmm {
 
 namespace {
 
-constexpr int kTok = 256;             // tokens per tile (two MMAs of M = 128)
 constexpr int kRows = 256;            // weight rows per tile (MMA N)
-constexpr int kStages = 3;
-constexpr int kABytes = kTok * 128;   // 32768
 constexpr int kBBytes = kRows * 128;  // 32768
 constexpr int kNibBytes = kRows * 32; // 8192
 constexpr int kHdrBytes = kRows * 16; // 4096
@@ -63,19 +60,29 @@ constexpr int kHdrSlots = 2;
 constexpr int kThreads = 576;
 constexpr int kEpiWarp0 = 2;
 constexpr int kDequantWarp0 = 10;
-constexpr uint32_t kTmemCols = 512;   // two 256-column fp32 accumulators
 constexpr int kMaxKSplit = 16;
+
+// Token tiles of 256 (two MMAs of M = 128 per K step into both 256-column
+// TMEM accumulators) or of 128 (one MMA, one accumulator) for problems whose
+// 256-token tiles would not fill the SMs.  Three stages either way.
+template <int TOK>
+struct TileCfg {
+    static constexpr int kTok = TOK;
+    static constexpr int kHalves = TOK / 128;           // MMAs of M = 128 per K step
+    static constexpr int kStages = 3;
+    static constexpr int kABytes = TOK * 128;
+    static constexpr uint32_t kTmemCols = uint32_t(kHalves) * 256;
+    static constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kNibBytes;
+    static constexpr size_t kSmemBytes =
+        1024 /* alignment slack */ + size_t(kStages) * kStageBytes + size_t(kHdrSlots) * kHdrBytes + 256;
+    static_assert(kSmemBytes <= 232448, "shared memory per block");
+};
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
 // bf16, both K-major, N = 256 (bits 17-22 hold N/8), M = 128 (bits 24-28
 // hold M/16).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kRows >> 3) << 17) |
                             (uint32_t(128 >> 4) << 24);
-
-constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kNibBytes;
-constexpr size_t kSmemBytes =
-    1024 /* alignment slack */ + size_t(kStages) * kStageBytes + size_t(kHdrSlots) * kHdrBytes + 256;
-static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 struct GemmParams {
     CUtensorMap tm_x;                   // X [M][K] bf16, box 64 x 256, 128-byte swizzle
@@ -230,12 +237,16 @@ __device__ __forceinline__ void dequant4(uint32_t v, float as, float b, uint32_t
     p1 = cvt_bf16x2(f1.x, f1.y);
 }
 
+template <int TOK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_constant__ GemmParams P)
 {
+    using C = TileCfg<TOK>;
+    constexpr int kTok = C::kTok, kStages = C::kStages, kABytes = C::kABytes;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
-    uint8_t *sA = base;                                  // [kStages][32 KB]
+    uint8_t *sA = base;                                  // [kStages][TOK x 128 B]
     uint8_t *sB = sA + kStages * kABytes;                // [kStages][32 KB]
     uint8_t *sNib = sB + kStages * kBBytes;              // [kStages][8 KB]
     uint8_t *sHdr = sNib + kStages * kNibBytes;          // [kHdrSlots][4 KB]
@@ -362,9 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = sw128_desc(b0 + 32 * kk);
                         const uint32_t acc = (ks | kk) != 0 ? 1u : 0u;
-                        mma_bf16(tmem, sw128_desc(a0 + 32 * kk), bd, acc);
-                        mma_bf16(tmem + uint32_t(kRows), sw128_desc(a0 + kABytes / 2 + 32 * kk), bd,
-                                 acc);
+#pragma unroll
+                        for (int h = 0; h < C::kHalves; ++h)
+                            mma_bf16(tmem + uint32_t(h * kRows), sw128_desc(a0 + h * 16384 + 32 * kk),
+                                     bd, acc);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -379,8 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     } else if (warp < kDequantWarp0) {
         // ---------------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        const int half = (warp - kEpiWarp0) >> 2;
-        const int tok_in_tile = half * 128 + quarter * 32 + lane;
+        const int eh = (warp - kEpiWarp0) >> 2;  // 256-token tiles: token half; 128: column half
+        const int tok_in_tile = (C::kHalves == 2 ? eh * 128 : 0) + quarter * 32 + lane;
+        constexpr int kCols = C::kHalves == 2 ? kRows : kRows / 2;  // columns this warp drains
+        const int col0 = C::kHalves == 2 ? 0 : eh * (kRows / 2);
         int lt = 0;
         for (int un = blockIdx.x; un < P.units; un += gridDim.x, ++lt) {
             if (!wait_phase(accfull, unsigned(lt) & 1u, &abort_flag, P.status))
@@ -398,14 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             // kernel adds the slices in order.
             float *yrow = split ? P.ws + (size_t(kslice) * size_t(P.M) + tok) * P.Ntot + P.col_off[mi]
                                 : P.y[mi] + int64_t(tok) * Nm;
-            const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * kRows);
+            const uint32_t taddr = tmem + (uint32_t(quarter * 32) << 16) +
+                                   uint32_t(C::kHalves == 2 ? eh * kRows : col0);
 #pragma unroll 1
-            for (int ch = 0; ch < kRows / 32; ++ch) {
+            for (int ch = 0; ch < kCols / 32; ++ch) {
                 uint32_t r[32];
                 tmem_ld16(taddr + uint32_t(ch * 32), *reinterpret_cast<uint32_t(*)[16]>(r));
                 tmem_ld16(taddr + uint32_t(ch * 32 + 16), *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                 tmem_ld_wait();
-                const int n0 = row0 + ch * 32;
+                const int n0 = row0 + col0 + ch * 32;
                 if (tok < P.M) {
                     if (P.vec_store && n0 + 32 <= Nm) {
                         float4 *dst = reinterpret_cast<float4 *>(yrow + n0);
@@ -502,7 +517,7 @@ struct ReduceParams {
     int col_off[kGemmMaxGroup];
     int rt_end[kGemmMaxGroup];
     int nmat, Ntot, M, ks;
-    int tok_tiles, first_tail, n_tail;  // tail tiles [first_tail, first_tail + n_tail)
+    int tok, tok_tiles, first_tail, n_tail;  // token tile height; tail tiles [first_tail, +n_tail)
     int vec;                            // every N_i % 4 == 0 and every Y 16-byte aligned
     const float *ws;
 };
@@ -516,14 +531,14 @@ __global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
     pdl_wait();
     pdl_launch_dependents();
     const int64_t plane = int64_t(R.M) * R.Ntot;
-    const int64_t per_tile = int64_t(kTok) * (kRows / 4);
+    const int64_t per_tile = int64_t(R.tok) * (kRows / 4);
     const int64_t n = int64_t(R.n_tail) * per_tile;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int tt = int(i / per_tile);
         const int rem = int(i - int64_t(tt) * per_tile);
         const int t = R.first_tail + tt;
-        const int tok = (t % R.tok_tiles) * kTok + rem / (kRows / 4);
+        const int tok = (t % R.tok_tiles) * R.tok + rem / (kRows / 4);
         const int grt = t / R.tok_tiles;
         int mi = 0;
 #pragma unroll
@@ -564,11 +579,14 @@ __global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
 
 } // namespace
 
-size_t gemm_q4k_smem() { return kSmemBytes; }
-
-int gemm_q4k_tiles(int64_t M, int64_t N)
+size_t gemm_q4k_smem(int tok)
 {
-    return int((M + kTok - 1) / kTok) * int((N + kRows - 1) / kRows);
+    return tok == 128 ? TileCfg<128>::kSmemBytes : TileCfg<256>::kSmemBytes;
+}
+
+int gemm_q4k_tiles(int64_t M, int64_t N, int tok)
+{
+    return int((M + tok - 1) / tok) * int((N + kRows - 1) / kRows);
 }
 
 // How to cut the work into units, from a time model: a CTA spends about
@@ -579,7 +597,7 @@ int gemm_q4k_tiles(int64_t M, int64_t N)
 // and re-reading their fp32 partials at about 5 TB/s.  The count with the
 // least estimated time wins (1 = no split).  QMM_GEMM_KSPLIT forces a value
 // (if it divides K/256); then every tile is split.
-GemmSplit gemm_q4k_split(int tiles, int64_t K, int sm_count)
+GemmSplit gemm_q4k_split(int tiles, int tok, int64_t K, int sm_count)
 {
     const int sb = int(K / 256);
     GemmSplit g;
@@ -597,7 +615,7 @@ GemmSplit gemm_q4k_split(int tiles, int64_t K, int sm_count)
     if (tail == 0)
         return g;
     const int full = tiles - tail;
-    const double us_per_sb = 3.7, partial_bytes_per_us = 5.0e6, tile_bytes = double(kTok) * kRows * 4;
+    const double us_per_sb = 3.7, partial_bytes_per_us = 5.0e6, tile_bytes = double(tok) * kRows * 4;
     double best_t = 1e30;
     for (int ks = 1; ks <= kMaxKSplit && ks <= sb; ++ks) {
         if (sb % ks != 0)
@@ -647,15 +665,16 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     P.ws = a.ws;
     P.M = int(a.M);
     P.K = int(a.K);
-    P.tok_tiles = int((a.M + kTok - 1) / kTok);
+    P.tok_tiles = int((a.M + a.tok - 1) / a.tok);
     P.tiles = P.tok_tiles * rt;
     P.ksplit = a.ksplit;
     P.full_units = a.ksplit > 1 ? a.full_tiles : P.tiles;
     P.units = P.full_units + (P.tiles - P.full_units) * P.ksplit;
     P.vec_store = vec ? 1 : 0;
     P.status = a.status;
-    cudaError_t e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
+    auto kern = a.tok == 128 ? gemm_q4k_kernel<128> : gemm_q4k_kernel<256>;
+    const size_t smem = gemm_q4k_smem(a.tok);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess)
         return e;
     int grid = sm_count < P.units ? sm_count : P.units;
@@ -665,14 +684,14 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    e = counted(cudaLaunchKernelEx(&cfg, gemm_q4k_kernel, P));
+    e = counted(cudaLaunchKernelEx(&cfg, kern, P));
     if (e != cudaSuccess || P.ksplit == 1)
         return e;
     ReduceParams R;
@@ -687,12 +706,13 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     R.Ntot = P.Ntot;
     R.M = P.M;
     R.ks = P.ksplit;
+    R.tok = a.tok;
     R.tok_tiles = P.tok_tiles;
     R.first_tail = P.full_units;
     R.n_tail = P.tiles - P.full_units;
     R.ws = a.ws;
     R.vec = vec ? 1 : 0;
-    const int64_t work = int64_t(R.n_tail) * kTok * (kRows / 4);
+    const int64_t work = int64_t(R.n_tail) * a.tok * (kRows / 4);
     int64_t blocks = (work + 255) / 256;
     if (blocks > int64_t(sm_count) * 16)
         blocks = int64_t(sm_count) * 16;

@@ -792,15 +792,10 @@ static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, in
                     (long long)M);
     if (!aligned(X_bf16, 16))
         return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
-    alignas(64) unsigned char tmx[128];
-    if (qmm::encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X_bf16, uint64_t(m->K),
-                            uint64_t(M), uint64_t(m->K) * 2, 64u, 256u,
-                            CU_TENSOR_MAP_SWIZZLE_128B) != 0)
-        return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
     qmm::GemmArgs a;
     memset(&a, 0, sizeof(a));
     int64_t Ntot = 0;
-    int tiles = 0;
+    int tiles256 = 0, tiles128 = 0;
     for (int i = 0; i < n; ++i) {
         const Matrix *mi = reinterpret_cast<const Matrix *>(hs[i]);
         a.tmap_hdr[i] = mi->tmap_hdr;
@@ -808,10 +803,26 @@ static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, in
         a.y[i] = Ys[i];
         a.N[i] = mi->N;
         Ntot += mi->N;
-        tiles += qmm::gemm_q4k_tiles(M, mi->N);
+        tiles256 += qmm::gemm_q4k_tiles(M, mi->N, 256);
+        tiles128 += qmm::gemm_q4k_tiles(M, mi->N, 128);
     }
     a.nmat = n;
-    const qmm::GemmSplit split = qmm::gemm_q4k_split(tiles, m->K, m->sm_count);
+    // 256-token tiles reuse each dequantised weight twice as often as 128-token
+    // tiles; measured on the Llama shapes, they are as fast or faster except
+    // for the q/k/v group at 512 tokens, so they are the default (the K-split
+    // of the tail wave recovers the parallelism).  QMM_GEMM_TOK=128 selects
+    // the smaller tile.
+    a.tok = 256;
+    if (const char *e = getenv("QMM_GEMM_TOK"))
+        if (atoi(e) == 128 || atoi(e) == 256)
+            a.tok = atoi(e);
+    const int tiles = a.tok == 128 ? tiles128 : tiles256;
+    alignas(64) unsigned char tmx[128];
+    if (qmm::encode_tmap_2d(tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X_bf16, uint64_t(m->K),
+                            uint64_t(M), uint64_t(m->K) * 2, 64u, uint32_t(a.tok),
+                            CU_TENSOR_MAP_SWIZZLE_128B) != 0)
+        return fail(QMM_ERR_CUDA, "%s: the TMA tensor map for X could not be encoded", fn);
+    const qmm::GemmSplit split = qmm::gemm_q4k_split(tiles, a.tok, m->K, m->sm_count);
     a.ksplit = split.ksplit;
     a.full_tiles = split.full;
     if (a.ksplit > 1) {

@@ -167,7 +167,7 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
 // --------------------------------------------------------------- prefill GEMM
 constexpr int kGemmMaxGroup = 4;
 struct GemmArgs {
-    const void *tmap_x;                  // X [M][K] bf16: box 64 x 256, 128-byte swizzle
+    const void *tmap_x;                  // X [M][K] bf16: box 64 x tok, 128-byte swizzle
     const void *tmap_hdr[kGemmMaxGroup]; // Matrix::tmap_hdr of each matrix
     const void *tmap_nib[kGemmMaxGroup]; // Matrix::tmap_nib
     float *y[kGemmMaxGroup];             // [M][N_i]
@@ -176,16 +176,17 @@ struct GemmArgs {
     float *ws;             // split-K partials (gemm_q4k_ws_floats floats) when ksplit > 1
     int ksplit;            // K slices of each tail tile
     int full_tiles;        // tiles that run whole (the rest are split) when ksplit > 1
+    int tok;               // token tile height: 256, or 128 when 256-token tiles are too few
     int64_t M, K;
     unsigned *status;
 };
-size_t gemm_q4k_smem();
-int gemm_q4k_tiles(int64_t M, int64_t N);
+size_t gemm_q4k_smem(int tok);
+int gemm_q4k_tiles(int64_t M, int64_t N, int tok);
 struct GemmSplit {
     int full;    // whole tiles (the first ones)
     int ksplit;  // K slices of each remaining tile (1: none split)
 };
-GemmSplit gemm_q4k_split(int tiles, int64_t K, int sm_count);
+GemmSplit gemm_q4k_split(int tiles, int tok, int64_t K, int sm_count);
 size_t gemm_q4k_ws_floats(int64_t M, int64_t Ntot, int ksplit);
 cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s);
 

@@ -72,12 +72,23 @@ def test_gemm_identity_is_bf16_weights():
     m.close()
 
 
+@pytest.mark.parametrize("tok", [None, 128, 256])
 @pytest.mark.parametrize("M,N,K", [
     (1, 256, 256), (5, 300, 512), (128, 256, 1024), (130, 513, 768), (257, 1024, 2048),
     (300, 64, 256), (129, 257, 4096),
 ])
-def test_gemm_small(M, N, K):
+def test_gemm_small(monkeypatch, tok, M, N, K):
+    """Small and ragged shapes, with the token tile chosen by the library or
+    forced to 128 or 256."""
+    if tok:
+        monkeypatch.setenv("QMM_GEMM_TOK", str(tok))
     _check(M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("tok", [128, 256])
+def test_gemm_identity_both_tiles(monkeypatch, tok):
+    monkeypatch.setenv("QMM_GEMM_TOK", str(tok))
+    test_gemm_identity_is_bf16_weights()
 
 
 @pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)])
