@@ -617,14 +617,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"Llama-3.1-8B decode GEMV, batch 1: {nl} layers x "
-                               "(q,k,v,o,gate,up,down), Q4_K weights, fp32 activations",
-                   "layers": nl,
-                   "weights_bytes_per_step": wbytes_layer * nl,
-                   "algorithmic_bytes_per_step": step_bytes,
-                   "launches_per_step": launches_per_step,
-                   "l2": "working set 3.93 GB >> 129 MB L2: no flush between steps",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(decode_config(nl, world), launches_per_step=launches_per_step),
         "roofline": {"bound": "hbm", "achieved": dom["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": dom["gbs"] / pk["hbm_gbs"], "traffic": traffic,
                      "kernel": dom["kernel"], "peak_source": pk["source"],
@@ -671,6 +664,18 @@ def run_only(args, world, local):
     return {"workload": f"OLMoE expert FFN, {args.layers} layers", "ms_per_step": ms, "gbs": gbs}
 
 
+def decode_config(nl, world):
+    """The decode workload's description (both arms report the same one)."""
+    bytes_layer, wbytes_layer = layer_bytes(synth.Q4_K)
+    return {"workload": f"Llama-3.1-8B decode GEMV, batch 1: {nl} layers x "
+                        "(q,k,v,o,gate,up,down), Q4_K weights, fp32 activations",
+            "layers": nl,
+            "weights_bytes_per_step": wbytes_layer * nl,
+            "algorithmic_bytes_per_step": bytes_layer * nl,
+            "l2": "working set 3.93 GB >> 129 MB L2: no flush between steps",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: each step decodes-then-dots a
     bounded sample (256 rows of each of the 7 matrices of one layer)."""
@@ -710,7 +715,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "Llama-3.1-8B decode GEMV, batch 1, Q4_K (bounded row sample)"},
+        "config": decode_config(args.layers, world),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
