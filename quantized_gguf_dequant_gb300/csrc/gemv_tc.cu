@@ -39,6 +39,7 @@
 // (step, c) holds the matching activations; column n of B is (x row n/2,
 // term n%2), so lane c's accumulator columns (2c, 2c+1) are both terms of
 // activation row c.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -332,15 +333,24 @@ TcKernel pick_tc(int ncol)
 
 } // namespace
 
-// Warps per CTA and ring depth: 16 warps x 3 slots when every CTA has at
-// least 64 units (long launches want latency hiding), else 8 x 4 (the
-// smaller footprint leaves room for the next kernel's CTA to start early).
-// QMM_TC_WARPS / QMM_TC_NSLOT override.
+// Warps per CTA and ring depth: 16 warps x 2 slots, the fastest setting of
+// a sweep over the Llama-3.1-8B decode step (warps 8-16 x slots 2-6, for
+// launches with at least 64 units per CTA -- "big" -- and the rest separately:
+// every CTA wants all 16 warps, and deeper rings only add queueing).
+// QMM_TC_BIG / QMM_TC_SMALL ("warps,slots") override one class,
+// QMM_TC_WARPS / QMM_TC_NSLOT both.
 void gemv_tc_shape(int64_t units_per_cta, int &warps, int &nslot)
 {
     const bool big = units_per_cta >= 64;
-    warps = big ? 16 : 8;
-    nslot = big ? 3 : 4;
+    warps = 16;
+    nslot = 2;
+    if (const char *c = getenv(big ? "QMM_TC_BIG" : "QMM_TC_SMALL")) {
+        int w = 0, n = 0;
+        if (sscanf(c, "%d,%d", &w, &n) == 2 && w >= 4 && w <= 16 && n >= 2 && n <= 16) {
+            warps = w;
+            nslot = n;
+        }
+    }
     const char *e = getenv("QMM_TC_WARPS");
     if (e && atoi(e) >= 4 && atoi(e) <= 16)
         warps = atoi(e);
