@@ -276,14 +276,25 @@ TcbKernel pick_tcb(int nt)
 }
 
 constexpr int kTcbWarps = 8;
-constexpr int kTcbSlots = 4;
+constexpr int kTcbMaxSlots = 8;
+
+// Ring slots per warp: 2 (a sweep of 2, 3, 4 and 6 on the decode step and
+// the batched sweep put 2-3 first); QMM_TCB_NSLOT overrides, 2..8.
+int tcb_slots()
+{
+    const char *e = getenv("QMM_TCB_NSLOT");
+    if (e && atoi(e) >= 2 && atoi(e) <= kTcbMaxSlots)
+        return atoi(e);
+    return 2;
+}
 
 size_t tcb_smem(int nt, int kc)
 {
     const size_t ncol = 8 * nt, mp = 4 * nt;
-    return size_t(kTcbWarps) * kTcbSlots * kTileBytes + size_t(kc) * 16 * ncol * 4 * 8 +
+    const int ns = tcb_slots();
+    return size_t(kTcbWarps) * ns * kTileBytes + size_t(kc) * 16 * ncol * 4 * 8 +
            size_t(kc) * ncol * 4 * 4 + size_t(kc) * mp * 4 + size_t(kTcbWarps) * 2 * mp * kTileRows * 4 +
-           8 + size_t(kTcbWarps) * kTcbSlots * 8;
+           8 + size_t(kTcbWarps) * ns * 8;
 }
 
 } // namespace
@@ -353,7 +364,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     P.T = int((a.N + kTileRows - 1) / kTileRows);
     P.R = p.R;
     P.S = p.S;
-    P.nslot = kTcbSlots;
+    P.nslot = tcb_slots();
     TcbKernel kern = pick_tcb(p.nt);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
     if (e != cudaSuccess)
