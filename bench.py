@@ -648,6 +648,13 @@ def run_only(args, world, local):
         pm.close()
         return {"workload": f"prefill GEMM M={args.prefill_m}, {args.layers} layers", "ms_per_step": ms,
                 "tflops": tf}
+    if args.only == "q8":
+        q8 = Model(synth.Q8_0, layers=args.layers)
+        b8, _ = layer_bytes(synth.Q8_0)
+        ms, _ = timer(lambda: q8.step(True), args.steps, args.warmup, world)
+        q8.close()
+        return {"workload": f"Llama-3.1-8B Q8_0 decode, {args.layers} layers", "ms_per_step": ms,
+                "gbs": b8 * args.layers / (ms * 1e-3) / 1e9}
     if args.only == "batched":
         q4 = Model(synth.Q4_K, layers=args.layers)
         bm = BatchedModel(q4)
@@ -735,7 +742,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch directly instead of replaying a CUDA graph (profiling)")
-    ap.add_argument("--only", choices=["prefill", "moe", "batched"], default=None,
+    ap.add_argument("--only", choices=["prefill", "moe", "batched", "q8"], default=None,
                     help="time just one secondary workload (profiling): the prefill GEMMs at "
                          "--prefill-m tokens, or the OLMoE expert FFN")
     ap.add_argument("--prefill-m", type=int, default=2048)
