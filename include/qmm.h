@@ -93,8 +93,9 @@ QMM_API qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *
 QMM_API qmm_status qmm_destroy(qmm_t h);
 
 /* Decode GEMV (one activation vector):  y[n] = sum_k w[n][k] * x[k].
- * x: K fp32, y: N fp32, both device, 16-byte aligned.  Split-K over CTAs with
- * a fixed-order reduction: results are bitwise repeatable. */
+ * x: K fp32 (device, 16-byte aligned), y: N fp32 (device, 4-byte aligned).
+ * Any split of K over CTAs is reduced in a fixed order: results are bitwise
+ * repeatable.  Never allocates (the handle's scratch covers it). */
 QMM_API qmm_status qmm_gemv(qmm_t h, const float *x, float *y, qmm_stream stream);
 
 /* Several matrices that share one input vector in one launch (the q/k/v or
