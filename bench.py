@@ -376,6 +376,43 @@ class PrefillModel:
                 m.close()
 
 
+def small_matrix_extra(pk):
+    """The 1024 x 1024 Q4_K matrix alone: (i) single-call latency with L2
+    flushed before every call (a 256 MB write between calls), median of 21;
+    (ii) throughput over 512 distinct copies (302 MB > L2) in one graph."""
+    import torch
+    import quantized_gguf_dequant_gb300 as q
+    N = K = 1024
+    copies = 512
+    mats = [q.Matrix(synth.Q4_K, N, K, torch.from_numpy(synth.q4k_matrix(N, K, 7000 + i)).cuda())
+            for i in range(copies)]
+    x = torch.from_numpy(synth.activations(1, K, 7)[0]).cuda()
+    ys = torch.empty((copies, N), dtype=torch.float32, device="cuda")
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+    wbytes = N * synth.row_bytes(synth.Q4_K, K)
+    lat = []
+    for i in range(24):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        q.gemv(mats[i].h, x, ys[i])
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            lat.append(e0.elapsed_time(e1) * 1e3)
+    ms, _ = time_graph(lambda: [q.gemv(m.h, x, ys[i]) for i, m in enumerate(mats)], 5, 3, 1)
+    tput = copies * (wbytes + 4 * K + 4 * N) / (ms * 1e-3) / 1e9
+    for m in mats:
+        m.close()
+    del flush
+    return {"latency_us_median": statistics.median(lat), "latency_us_min": min(lat),
+            "rotating_gbs": tput, "rotating_frac_of_peak": tput / pk["hbm_gbs"],
+            "note": "qmm_gemv on a 1024 x 1024 Q4_K matrix (589,824 B): latency of one call with "
+                    "L2 flushed (CUDA events around the call), and 512 distinct copies in one CUDA "
+                    "graph (weights > L2)"}
+
+
 def launches_of(fn):
     """Kernels the library launches for one call of fn (counted by the
     library itself; run eagerly, outside any capture)."""
@@ -560,6 +597,9 @@ def run_ours(args, world, rank, local):
     q4.close()
     del q4
     torch.cuda.empty_cache()
+    if args.extras:
+        extras["q4k_1024x1024"] = small_matrix_extra(pk)
+        torch.cuda.empty_cache()
     if args.extras:
         mo = MoeModel()
         ms_m, _ = time_graph(mo.step, max(3, args.steps // 4), args.warmup, world)
