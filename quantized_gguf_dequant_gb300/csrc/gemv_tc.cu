@@ -61,12 +61,10 @@ struct TcParams {
     int64_t rows[kMaxGroup];
     float *y[kMaxGroup];
     const float *x;
-    float *ws;          // [CTAs][2][4][16] partial sums of tiles split between CTAs
-    unsigned *tickets;  // [tiles]
     unsigned *status;
     int64_t U;          // units
     int64_t ldx, ldy;   // activation / output row strides (elements)
-    int nmat, M, NB, W, nslot;  // W: CTAs
+    int nmat, M, NB, nslot;
     int late_trigger;           // let the next kernel launch only after the main loop
 };
 
@@ -368,7 +366,6 @@ size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw)
            size_t(nw) * nslot * 8;
 }
 
-size_t gemv_tc_ws_floats(int sm_count) { return size_t(sm_count) * 2 * 4 * kTileRows; }
 
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
 {
@@ -385,8 +382,6 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
     for (int i = a.nmat; i < kMaxGroup; ++i)
         P.tile_end[i] = tiles;
     P.x = a.x;
-    P.ws = a.ws;
-    P.tickets = a.tickets;
     P.status = a.status;
     P.NB = int(a.K / 256);
     P.U = tiles * P.NB;
@@ -399,7 +394,6 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
     int64_t ctas = sm_count;
     if (ctas > tiles)
         ctas = tiles;  // every CTA owns at least one row tile
-    P.W = int(ctas);
     int nw, nslot;
     gemv_tc_shape(P.U / ctas, nw, nslot);
     P.nslot = nslot;

@@ -87,25 +87,18 @@ qmm_status do_gemv_tc(const qmm_t *hs, int n, const float *x, int64_t ldx, int M
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
     qmm::TcArgs a;
     memset(&a, 0, sizeof(a));
-    int64_t tiles = 0;
     for (int i = 0; i < n; ++i) {
         const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
         a.tmap[i] = mi.tmap;
         a.rows[i] = mi.N;
         a.y[i] = ys[i];
-        tiles += (mi.N + 15) / 16;
     }
-    if (size_t(tiles) > m0.tc_tickets_n)
-        return fail(QMM_ERR_NOMEM, "%s: %lld row tiles exceed handle 0's ticket array (%zu)", fn,
-                    (long long)tiles, m0.tc_tickets_n);
     a.nmat = n;
     a.K = m0.K;
     a.M = M;
     a.ldx = ldx;
     a.ldy = ldy;
     a.x = x;
-    a.ws = m0.tc_ws;
-    a.tickets = m0.tc_tickets;
     a.status = m0.status;
     cudaError_t e = qmm::launch_gemv_tc(a, m0.sm_count, s);
     if (e != cudaSuccess)
@@ -415,12 +408,9 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
             return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor maps for the prefill GEMM "
                                       "could not be encoded");
         }
-        m->tc_ws_floats = qmm::gemv_tc_ws_floats(m->sm_count);
-        m->tc_tickets_n = size_t(N > 32768 ? N : 32768) / 16 + 64;
     }
     void *p = nullptr;
-    const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256 + m->tc_ws_floats * 4 +
-                         m->tc_tickets_n * 4;
+    const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256;
     e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess) {
         delete m;
@@ -452,8 +442,6 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
     }
     m->tickets = reinterpret_cast<unsigned *>(m->ws + m->ws_floats);
     m->status = m->tickets + m->n_tickets;
-    m->tc_ws = reinterpret_cast<float *>(m->status + 64);
-    m->tc_tickets = reinterpret_cast<unsigned *>(m->tc_ws + m->tc_ws_floats);
     *out = reinterpret_cast<qmm_t>(m);
     return QMM_OK;
 }

@@ -29,14 +29,9 @@ struct Matrix {
     unsigned *tickets = nullptr;
     size_t n_tickets = 0;
     unsigned *status = nullptr;
-    // Q4_K tensor-core path: 2-D tensor map over the rows (a CUtensorMap),
-    // stream-K partial sums and per-tile tickets
+    // Q4_K tensor-core paths: 2-D tensor map over the rows (a CUtensorMap)
     alignas(64) unsigned char tmap[128];
     bool has_tmap = false;
-    float *tc_ws = nullptr;
-    size_t tc_ws_floats = 0;
-    unsigned *tc_tickets = nullptr;
-    size_t tc_tickets_n = 0;
     // prefill GEMM: tensor maps over the weight bytes (u8) with boxes of the
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
@@ -125,12 +120,9 @@ struct TcArgs {
     int M;                // activation rows, 1..4
     int64_t ldx, ldy;     // row strides of X and Y (elements)
     const float *x;
-    float *ws;
-    unsigned *tickets;
     unsigned *status;
 };
 size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw);
-size_t gemv_tc_ws_floats(int sm_count);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
