@@ -79,7 +79,7 @@ def _failing_pins(tmp_path, monkeypatch, src):
             fn(**kw)
         except Exception:  # an assertion (or a refusal) in the pin
             failed.append(pname)
-    monkeypatch.setattr(oracle, "_lib", None)  # drop this build before the real one returns
+    monkeypatch.setattr(oracle, "_lib", None)  # drop the copied library before the real one returns
     return failed
 
 
