@@ -290,3 +290,43 @@ def test_launch_count_counts_kernels():
     torch.cuda.synchronize()
     assert q.launch_count() - c0 == 1
     m.close()
+
+
+def test_gemv_chain_in_cuda_graph_matches_eager():
+    """Launch chaining: a grouped q/k/v call, a single call and the long-K
+    call captured in one CUDA graph (programmatic dependent launch between
+    them) replay to the same bits as eager launches."""
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096), (512, 4096), (1024, 14336)]
+    mats, ws = [], []
+    for i, (N, K) in enumerate(shapes):
+        w, m = _matrix(q.Q4_K, N, K, seed=300 + i)
+        mats.append(m)
+        ws.append(w)
+    x1 = to_dev(synth.activations(1, 4096, 301)[0])
+    x2 = to_dev(synth.activations(1, 14336, 302)[0])
+    ys = [torch.zeros(N, dtype=torch.float32, device="cuda") for N, _ in shapes]
+
+    def step(stream):
+        q.gemv_group([mats[0].h, mats[1].h, mats[2].h], x1, ys[0:3], stream)
+        q.gemv(mats[3].h, x1, ys[3], stream)
+        q.gemv(mats[4].h, x2, ys[4], stream)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s)
+    s.synchronize()
+    eager = [y.clone() for y in ys]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s)
+    for y in ys:
+        y.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ys, eager):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    y_ref, c = oracle.gemv(q.Q4_K, ws[4], 1024, 14336, x2.cpu().numpy(), nthreads=oracle.max_threads())
+    assert_close_to_oracle(ys[4].cpu().numpy(), np.ravel(y_ref), np.ravel(c), TOL_FP32, "chain long K")
+    for m in mats:
+        m.close()
