@@ -1,0 +1,89 @@
+"""Seeded random shapes through every compute entry point, against the oracle.
+
+Each case draws N, K (any multiple of 256), batch sizes, expert counts and
+top-k from a fixed seed, so odd row counts (not multiples of 16 or 256), odd
+super-block counts and odd batch sizes all occur; each result must meet the
+path's bound (1e-4 of sum|w x| for the fp32 paths, 1e-3 for the bf16 prefill
+against the oracle's bf16 product)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_gguf_dequant_gb300 import synth
+from tests._util import TOL_FP32, assert_close_to_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+q = pytest.importorskip("quantized_gguf_dequant_gb300")
+
+NT = max(1, oracle.max_threads())
+CASES = 12
+
+
+def _rng(case, salt):
+    return np.random.default_rng(1000 * salt + case)
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_gemv_and_batched(case):
+    r = _rng(case, 1)
+    fmt = q.Q4_K if case % 3 else q.Q8_0
+    N = int(r.integers(1, 700))
+    K = 256 * int(r.integers(1, 24))
+    M = int(r.integers(1, 17))
+    w = synth.matrix(fmt, N, K, 50 + case)
+    m = q.Matrix(fmt, N, K, to_dev(w))
+    X = synth.activations(M, K, 60 + case)
+    Y = m.gemv_batched(to_dev(X)).cpu().numpy()
+    y1 = m.gemv(to_dev(X[0])).cpu().numpy()
+    Yr, C = oracle.gemv(fmt, w, N, K, X, nthreads=NT)
+    assert_close_to_oracle(Y, Yr, C, TOL_FP32, f"batched fmt={fmt} N={N} K={K} M={M}")
+    assert_close_to_oracle(y1, Yr[0], C[0], TOL_FP32, f"gemv fmt={fmt} N={N} K={K}")
+    assert m.status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_gemm(case):
+    r = _rng(case, 2)
+    N = int(r.integers(1, 900))
+    K = 256 * int(r.integers(1, 12))
+    M = int(r.integers(1, 600))
+    w = synth.q4k_matrix(N, K, 70 + case)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    Xb = synth.activations_bf16(M, K, 80 + case)
+    Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    m.gemm(to_dev(Xb.view(np.int16)), Y)
+    torch.cuda.synchronize()
+    Yr, C = oracle.gemm_bf16(w, N, K, Xb, nthreads=NT)
+    assert_close_to_oracle(Y.cpu().numpy(), Yr, C, 1e-3, f"gemm N={N} K={K} M={M}")
+    assert m.status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_moe(case):
+    r = _rng(case, 3)
+    E = int(r.integers(1, 24))
+    Ne = int(r.integers(1, 200))
+    K = 256 * int(r.integers(1, 6))
+    T = int(r.integers(1, 40))
+    top_k = int(r.integers(1, min(E, 8) + 1))
+    xps = bool(case % 2)
+    routed = case % 3 != 0
+    w = synth.q4k_matrix(E * Ne, K, 90 + case)
+    m = q.Matrix(q.Q4_K, E * Ne, K, to_dev(w))
+    ids, rw = synth.router(T, E, top_k, 91 + case)
+    X = synth.activations(T * top_k if xps else T, K, 92 + case)
+    rows = T if routed else T * top_k
+    Y = torch.full((rows, Ne), float("nan"), dtype=torch.float32, device="cuda")
+    q.moe_gemv(m.h, E, to_dev(ids), T, top_k, to_dev(X), xps, to_dev(rw) if routed else None, Y)
+    torch.cuda.synchronize()
+    Yr, C = oracle.moe_gemv(q.Q4_K, w, E, Ne, K, ids, X, xps, rw if routed else None, nthreads=NT)
+    assert_close_to_oracle(Y.cpu().numpy(), Yr, C, TOL_FP32,
+                           f"moe E={E} Ne={Ne} K={K} T={T} k={top_k} xps={xps} routed={routed}")
+    assert m.status() == 0
+    m.close()
