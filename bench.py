@@ -254,6 +254,27 @@ class Model:
             else:
                 q.gemv(md.h, xv[3], yv[6])
 
+    def ffn_step(self, fused=True):
+        """The dense SwiGLU FFN of every layer (gate, up, down): qmm_ffn_decode,
+        or the grouped gate/up GEMV, qmm_swiglu and the down GEMV as separate
+        calls.  h lands in the gate's output slot."""
+        q = self.q
+        for mats, xv, yv in self.layers:
+            mg, mu, md = mats[4], mats[5], mats[6]
+            if fused:
+                q.ffn_decode(mg.h, mu.h, md.h, xv[2], yv[4], yv[6])
+            else:
+                q.gemv_group([mg.h, mu.h], xv[2], yv[4:6])
+                q.swiglu(yv[4], yv[5], yv[4], yv[4].numel())
+                q.gemv(md.h, yv[4], yv[6])
+
+    def ffn_bytes(self):
+        """Algorithmic bytes of ffn_step: gate/up/down weights once, x, h
+        written and read once, y."""
+        w = sum(N * synth.row_bytes(self.fmt, K) for name, N, K in SHAPES
+                if name in ("gate", "up", "down"))
+        return (w + 4 * (4096 + 2 * 14336 + 4096)) * len(self.layers)
+
     def launches(self, grouped=True):
         return len(self.layers) * (4 if grouped else 7)
 
@@ -594,6 +615,21 @@ def run_ours(args, world, rank, local):
             "note": "qmm_gemv_batched on every matrix of every layer, M activation rows per "
                     "call; bytes = weights once + M input rows + M output rows"}
         del bm
+    if args.extras:
+        fb = q4.ffn_bytes()
+        ffn = {}
+        for fused in (True, False):
+            ms_f, _ = time_graph(lambda: q4.ffn_step(fused), max(3, args.steps // 4), args.warmup,
+                                 world)
+            ffn["fused" if fused else "separate"] = {
+                "ms_per_step": ms_f, "gbs": fb / (ms_f * 1e-3) / 1e9,
+                "frac_of_peak": fb / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "launches_per_step": launches_of(lambda: q4.ffn_step(fused))}
+        extras["q4k_dense_ffn_decode"] = {
+            "unit": "GB/s", "bytes_per_step": fb, **ffn,
+            "note": "the Llama-3.1-8B SwiGLU FFN of every layer for one token: qmm_ffn_decode "
+                    "(gate and up in one launch with SwiGLU in its epilogue, then down) against "
+                    "the grouped gate/up GEMV, qmm_swiglu and the down GEMV as separate calls"}
     q4.close()
     del q4
     torch.cuda.empty_cache()
@@ -695,6 +731,15 @@ def run_only(args, world, local):
         q8.close()
         return {"workload": f"Llama-3.1-8B Q8_0 decode, {args.layers} layers", "ms_per_step": ms,
                 "gbs": b8 * args.layers / (ms * 1e-3) / 1e9}
+    if args.only == "ffn":
+        q4 = Model(synth.Q4_K, layers=args.layers)
+        out = {"workload": f"Llama-3.1-8B dense FFN decode, {args.layers} layers"}
+        for fused in (True, False):
+            ms, _ = timer(lambda: q4.ffn_step(fused), args.steps, args.warmup, world)
+            out["fused" if fused else "separate"] = {
+                "ms_per_step": ms, "gbs": q4.ffn_bytes() / (ms * 1e-3) / 1e9}
+        q4.close()
+        return out
     if args.only == "batched":
         q4 = Model(synth.Q4_K, layers=args.layers)
         bm = BatchedModel(q4)
@@ -782,7 +827,7 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch directly instead of replaying a CUDA graph (profiling)")
-    ap.add_argument("--only", choices=["prefill", "moe", "batched", "q8"], default=None,
+    ap.add_argument("--only", choices=["prefill", "moe", "batched", "q8", "ffn"], default=None,
                     help="time just one secondary workload (profiling): the prefill GEMMs at "
                          "--prefill-m tokens, or the OLMoE expert FFN")
     ap.add_argument("--prefill-m", type=int, default=2048)

@@ -31,7 +31,7 @@ ENTRY_POINTS = (
     "qmm_create", "qmm_destroy", "qmm_gemv", "qmm_gemv_group", "qmm_gemv_batched",
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
-    "qmm_gemv_noalloc", "qmm_gemm_group", "qmm_launch_count",
+    "qmm_gemv_noalloc", "qmm_gemm_group", "qmm_launch_count", "qmm_ffn_decode",
 )
 
 
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "qmm_version": [],
             "qmm_gemv_noalloc": [i32, i64, i64, vp, vp, vp, vp],
             "qmm_gemm_group": [ctypes.POINTER(vp), i32, vp, i64, ctypes.POINTER(vp), vp],
+            "qmm_ffn_decode": [vp, vp, vp, vp, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -149,6 +150,12 @@ def moe_gemv(h: int, n_experts: int, ids, T: int, top_k: int, X, x_per_slot: int
              route_w, Y, stream=None):
     _check(lib().qmm_moe_gemv(ctypes.c_void_p(h), n_experts, _ptr(ids), T, top_k, _ptr(X),
                               int(x_per_slot), _ptr(route_w), _ptr(Y), _stream(stream)))
+
+
+def ffn_decode(hg: int, hu: int, hd: int, x, h, y, stream=None):
+    """qmm_ffn_decode: h = silu(Wg x) * (Wu x), y = Wd h (one token)."""
+    _check(lib().qmm_ffn_decode(ctypes.c_void_p(hg), ctypes.c_void_p(hu), ctypes.c_void_p(hd),
+                                _ptr(x), _ptr(h), _ptr(y), _stream(stream)))
 
 
 def swiglu(g, u, hout, n: int, stream=None):

@@ -66,7 +66,14 @@ struct TcParams {
     int64_t ldx, ldy;   // activation / output row strides (elements)
     int nmat, M, NB, nslot;
     int late_trigger;           // let the next kernel launch only after the main loop
+    // fuse = 1 (two matrices of the same shape, M = 1): tiles are taken as
+    // (gate, up) pairs of the same rows, staged in shared memory (room for
+    // res_tiles tiles per CTA), and y[0] receives h = silu(gate x) * (up x).
+    int fuse;
+    int res_tiles;
 };
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 __device__ __forceinline__ int matrix_of_tile(const TcParams &P, int64_t tile)
 {
@@ -92,6 +99,12 @@ __device__ __forceinline__ Cursor cursor_at(const TcParams &P, int64_t u)
     Cursor q;
     q.tile = int(u / P.NB);
     q.sb = int(u % P.NB);
+    if (P.fuse) {
+        q.mat = q.tile & 1;
+        q.tbase = q.tile - (q.tile >> 1);  // so that tile - tbase = the row tile
+        q.tend = 0;
+        return q;
+    }
     q.mat = matrix_of_tile(P, q.tile);
     q.tbase = q.mat == 0 ? 0 : int(P.tile_end[q.mat - 1]);
     q.tend = int(P.tile_end[q.mat]);
@@ -102,7 +115,11 @@ __device__ __forceinline__ void advance(const TcParams &P, Cursor &q)
 {
     if (++q.sb == P.NB) {
         q.sb = 0;
-        if (++q.tile == q.tend && q.mat + 1 < P.nmat) {
+        ++q.tile;
+        if (P.fuse) {
+            q.mat = q.tile & 1;
+            q.tbase = q.tile - (q.tile >> 1);
+        } else if (q.tile == q.tend && q.mat + 1 < P.nmat) {
             ++q.mat;
             q.tbase = q.tend;
             q.tend = int(P.tile_end[q.mat]);
@@ -125,15 +142,20 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
     uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(NB) * 16 * NCOL * 4);  // [NB][NCOL][4]
     float *inv = reinterpret_cast<float *>(Bm + size_t(NB) * NCOL * 4);           // [NB][M]
     float *part = inv + size_t(NB) * M;                                           // [nw][2][4][16]
+    float *res = part + size_t(nw) * 2 * 4 * kTileRows;  // fused: [res_tiles][16] tile results
     uint64_t *bars = reinterpret_cast<uint64_t *>(
-        (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * 4 * kTileRows) + 7) & ~uintptr_t(7));
+        (reinterpret_cast<uintptr_t>(res + size_t(P.fuse ? P.res_tiles : 0) * kTileRows) + 7) &
+        ~uintptr_t(7));
     uint64_t *bar = bars + warp * NS;
 
     // Each CTA owns whole row tiles (split evenly, G <= tiles) and splits
     // their units evenly over its warps.
     const int64_t G = gridDim.x;
     const int64_t T = P.U / NB;
-    const int64_t cU0 = (blockIdx.x * T / G) * NB, cU1 = ((blockIdx.x + 1) * T / G) * NB;
+    // Fused: whole (gate, up) pairs per CTA.
+    const int64_t tu = P.fuse ? 2 : 1;
+    const int64_t cU0 = (blockIdx.x * (T / tu) / G) * tu * NB,
+                  cU1 = ((blockIdx.x + 1) * (T / tu) / G) * tu * NB;
     const int64_t cn = cU1 - cU0;
     auto warp_begin = [&](int w) { return cU0 + int64_t(w) * cn / nw; };
     const int64_t u0 = warp_begin(warp), u1 = warp_begin(warp + 1);
@@ -246,7 +268,13 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
         if (q.sb == NB - 1 || j == nu - 1) {
             const int64_t first = int64_t(q.tile) * NB, last = first + NB - 1;
             if (u0 <= first && u1 - 1 >= last) {
-                if (mrow < M) {
+                if (P.fuse) {
+                    if (mrow == 0) {
+                        float *rr = res + (int64_t(q.tile) - cU0 / NB) * kTileRows;
+                        rr[g] = tot0;
+                        rr[g + 8] = tot1;
+                    }
+                } else if (mrow < M) {
                     const int64_t rA = int64_t(q.tile - q.tbase) * kTileRows + g;
                     float *yr = P.y[q.mat] + int64_t(mrow) * P.ldy;
                     if (rA < P.rows[q.mat])
@@ -304,7 +332,12 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
             s0 += pw[cr];
             s1 += pw[cr + 8];
         }
-        if (cm < M) {
+        if (P.fuse) {
+            if (cm == 0) {
+                res[tr * kTileRows + cr] = s0;
+                res[tr * kTileRows + cr + 8] = s1;
+            }
+        } else if (cm < M) {
             const int64_t t = cU0 / NB + tr;
             const int mi = matrix_of_tile(P, t);
             const int64_t rA = (t - (mi == 0 ? 0 : P.tile_end[mi - 1])) * kTileRows + cr;
@@ -314,6 +347,18 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
             if (rA + 8 < P.rows[mi])
                 yr[rA + 8] = s1;
         }
+    }
+    if (!P.fuse)
+        return;
+    // ---- h = silu(gate) * up for the CTA's (gate, up) tile pairs
+    __syncthreads();
+    const int npair = ntile / 2;
+    const int64_t rt0 = cU0 / NB / 2;  // first row tile of the CTA
+    for (int i = threadIdx.x; i < npair * kTileRows; i += blockDim.x) {
+        const int pl = i / kTileRows, r = i % kTileRows;
+        const int64_t row = (rt0 + pl) * kTileRows + r;
+        if (row < P.rows[0])
+            P.y[0][row] = silu(res[(2 * pl) * kTileRows + r]) * res[(2 * pl + 1) * kTileRows + r];
     }
 }
 
@@ -357,13 +402,13 @@ void gemv_tc_shape(int64_t units_per_cta, int &warps, int &nslot)
         nslot = atoi(n);
 }
 
-size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw)
+size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw, int res_tiles)
 {
     const int64_t NB = K / 256;
     const int ncol = 2 * M;
     return size_t(nw) * nslot * kTileBytes + size_t(NB) * 16 * ncol * 4 * 8 +
-           size_t(NB) * ncol * 4 * 4 + size_t(NB) * M * 4 + size_t(nw) * 2 * 4 * kTileRows * 4 + 8 +
-           size_t(nw) * nslot * 8;
+           size_t(NB) * ncol * 4 * 4 + size_t(NB) * M * 4 + size_t(nw) * 2 * 4 * kTileRows * 4 +
+           size_t(res_tiles) * kTileRows * 4 + 8 + size_t(nw) * nslot * 8;
 }
 
 
@@ -391,13 +436,17 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
     P.M = a.M;
     const char *lt = getenv("QMM_PDL_TRIGGER");
     P.late_trigger = (lt && strcmp(lt, "late") == 0) ? 1 : 0;
+    P.fuse = a.fuse_swiglu;
     int64_t ctas = sm_count;
-    if (ctas > tiles)
-        ctas = tiles;  // every CTA owns at least one row tile
+    const int64_t owned = P.fuse ? tiles / 2 : tiles;  // row tiles, or (gate, up) pairs
+    if (ctas > owned)
+        ctas = owned;  // every CTA owns at least one
     int nw, nslot;
     gemv_tc_shape(P.U / ctas, nw, nslot);
     P.nslot = nslot;
-    const size_t smem = gemv_tc_smem(a.K, a.M, nslot, nw);
+    if (P.fuse)
+        P.res_tiles = int(2 * ((tiles / 2 + ctas - 1) / ctas));
+    const size_t smem = gemv_tc_smem(a.K, a.M, nslot, nw, P.res_tiles);
     TcKernel kern = pick_tc(2 * a.M);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess)

@@ -748,6 +748,74 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     return QMM_OK;
 }
 
+qmm_status qmm_ffn_decode(qmm_t hg, qmm_t hu, qmm_t hd, const float *x, float *h, float *y,
+                          qmm_stream stream)
+{
+    g_err.clear();
+    const char *fn = "qmm_ffn_decode";
+    qmm_status st = check_handle(hg, fn);
+    if (st == QMM_OK)
+        st = check_handle(hu, fn);
+    if (st == QMM_OK)
+        st = check_handle(hd, fn);
+    if (st != QMM_OK)
+        return st;
+    const Matrix &mg = *reinterpret_cast<const Matrix *>(hg);
+    const Matrix &mu = *reinterpret_cast<const Matrix *>(hu);
+    const Matrix &md = *reinterpret_cast<const Matrix *>(hd);
+    if (mg.fmt != mu.fmt || mg.N != mu.N || mg.K != mu.K || md.K != mg.N)
+        return fail(QMM_ERR_SHAPE,
+                    "%s: gate %lld x %lld and up %lld x %lld must match (same format too) and down's "
+                    "K = %lld must equal their N", fn, (long long)mg.N, (long long)mg.K,
+                    (long long)mu.N, (long long)mu.K, (long long)md.K);
+    if (!x || !h || !y)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !x ? "x" : (!h ? "h" : "y"));
+    if (!aligned(x, 16) || !aligned(h, 16))
+        return fail(QMM_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, !aligned(x, 16) ? "x" : "h");
+    if (!aligned(y, 4))
+        return fail(QMM_ERR_ALIGN, "%s: y is not 4-byte aligned", fn);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const qmm_t gu[2] = {hg, hu};
+    if (mg.fmt == QMM_Q4_K && tc_fits(mg, 1) &&
+        !(getenv("QMM_FFN_NOFUSE") && getenv("QMM_FFN_NOFUSE")[0] == '1')) {
+        // Gate and up in one tensor-core launch, SwiGLU in its epilogue.
+        qmm::TcArgs a;
+        memset(&a, 0, sizeof(a));
+        a.tmap[0] = mg.tmap;
+        a.tmap[1] = mu.tmap;
+        a.rows[0] = a.rows[1] = mg.N;
+        a.y[0] = h;
+        a.nmat = 2;
+        a.K = mg.K;
+        a.M = 1;
+        a.ldx = mg.K;
+        a.x = x;
+        a.status = mg.status;
+        a.fuse_swiglu = 1;
+        cudaError_t e = qmm::launch_gemv_tc(a, mg.sm_count, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, fn);
+        reinterpret_cast<Matrix *>(hg)->last_stream = s;
+    } else {
+        // Gate into h and up into the up handle's scratch (one grouped launch
+        // when both fit a kernel together), then SwiGLU as its own kernel.
+        MoeScratch ms;
+        st = moe_scratch(*reinterpret_cast<Matrix *>(hu), 1, 1, 0, size_t(mg.N), fn, ms);
+        if (st != QMM_OK)
+            return st;
+        float *ys[2] = {h, ms.u};
+        st = do_gemv(gu, 2, x, ys, s, fn);
+        if (st != QMM_OK)
+            return st;
+        cudaError_t e = qmm::launch_swiglu(h, ms.u, h, mg.N, mg.sm_count, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, fn);
+    }
+    // down: y = Wd h
+    float *yd[1] = {y};
+    return do_gemv(&hd, 1, h, yd, s, fn);
+}
+
 // The prefill GEMM for n Q4_K matrices sharing X (n <= 4).
 static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, int64_t M,
                               float *const *Ys, qmm_stream stream, const char *fn)

@@ -121,8 +121,9 @@ struct TcArgs {
     int64_t ldx, ldy;     // row strides of X and Y (elements)
     const float *x;
     unsigned *status;
+    int fuse_swiglu;      // nmat == 2, M == 1, equal shapes: y[0] = silu(m0 x) * (m1 x)
 };
-size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw);
+size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw, int res_tiles = 0);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
