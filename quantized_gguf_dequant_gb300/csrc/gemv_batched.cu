@@ -16,8 +16,10 @@
 // fragments in shared memory; since 16 rows of a long K do not fit, the grid
 // is two-dimensional: CTA (r, s) owns row tiles [r*T/R, (r+1)*T/R) and
 // super-blocks [s*NB/S, (s+1)*NB/S), so it prepares only its slice of X.
-// With S > 1 the CTAs write partial sums per slice and a reduction kernel
-// adds the S slices in slice order, so results are bitwise repeatable.
+// With S > 1 the CTAs write partial sums per slice, added in slice order (so
+// results are bitwise repeatable): for few partials per output (M*S <= 16)
+// by the last CTA of each row group to finish (a ticket per row group), in
+// the same launch; otherwise by a reduction kernel spread over the GPU.
 #include <cstring>
 
 #include <cuda.h>
@@ -37,6 +39,7 @@ struct TcbParams {
     const float *x;     // [M][ldx]
     float *y;           // [M][ldy]
     float *ws;          // [S][M][N] partial sums (S > 1)
+    unsigned *tickets;  // [R] arrivals per row group (in-kernel reduction; zero between launches)
     unsigned *status;
     int64_t ldx, ldy;
     int N, M, NB;
@@ -68,6 +71,7 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
         (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * MP * kTileRows) + 7) & ~uintptr_t(7));
     uint64_t *bar = bars + warp * NS;
     __shared__ int wbeg[9];
+    __shared__ unsigned s_last;
 
     const int cn = (t1 - t0) * KC;  // units of this CTA, ordered (tile, super-block)
     const int u0 = int(int64_t(warp) * cn / nw), u1 = int(int64_t(warp + 1) * cn / nw);
@@ -245,6 +249,31 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
             }
         }
     }
+    if (P.S == 1 || !P.tickets)
+        return;
+
+    // ---- K slices: the row group's last CTA to arrive adds the S partial
+    // sums of its rows in slice order and resets the ticket.
+    __threadfence();  // this thread's partial sums, device-wide, before the ticket
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(&P.tickets[r], 1u) == unsigned(P.S - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    const int row0 = t0 * kTileRows, row1 = min(t1 * kTileRows, P.N), nr = row1 - row0;
+    const int64_t slice = int64_t(P.M) * P.N;
+    for (int i = threadIdx.x; i < P.M * nr; i += blockDim.x) {
+        const int m = i / nr, row = row0 + (i - m * nr);
+        const float *src = P.ws + int64_t(m) * P.N + row;
+        float acc = __ldcg(src);
+        for (int k = 1; k < P.S; ++k)
+            acc += __ldcg(src + k * slice);
+        P.y[int64_t(m) * P.ldy + row] = acc;
+    }
+    if (threadIdx.x == 0)
+        P.tickets[r] = 0u;
 }
 
 // y[m][n] = ws[0][m][n] + ... + ws[S-1][m][n], in slice order.
@@ -276,6 +305,10 @@ TcbKernel pick_tcb(int nt)
 }
 
 constexpr int kTcbWarps = 8;
+// Largest M*S whose slices one CTA per row group adds at the end of the main
+// launch (measured: M = 1 with four slices gains; M = 8 and 16 with 4-14
+// slices lose against the separate reduction).
+constexpr int kTcbInKernelPartials = 16;
 constexpr int kTcbMaxSlots = 8;
 
 // Ring slots per warp: 2 (a sweep of 2, 3, 4 and 6 on the decode step and
@@ -343,7 +376,7 @@ TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
     p.kc = (NB + p.S - 1) / p.S;
     p.smem = tcb_smem(p.nt, p.kc);
     p.ws_floats = p.S > 1 ? size_t(p.S) * size_t(M) * size_t(N) : 0;
-    p.tickets = 0;
+    p.tickets = (p.S > 1 && M * p.S <= kTcbInKernelPartials) ? size_t(p.R) : 0;
     return p;
 }
 
@@ -355,6 +388,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     P.x = a.x;
     P.y = a.y;
     P.ws = a.ws;
+    P.tickets = p.tickets ? a.tickets : nullptr;
     P.status = a.status;
     P.ldx = a.ldx;
     P.ldy = a.ldy;
@@ -380,7 +414,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
     e = counted(cudaLaunchKernelEx(&cfg, kern, P));
-    if (e != cudaSuccess || p.S == 1)
+    if (e != cudaSuccess || p.S == 1 || p.tickets)
         return e;
     const int64_t n = int64_t(a.M) * a.N;
     int64_t blocks = (n + 255) / 256;
@@ -391,8 +425,8 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     rc.gridDim = dim3(unsigned(blocks));
     rc.blockDim = dim3(256);
     rc.dynamicSmemBytes = 0;
-    return counted(cudaLaunchKernelEx(&rc, tcb_reduce_kernel, static_cast<const float *>(a.ws), p.S, a.M,
-                              int(a.N), a.y, a.ldy));
+    return counted(cudaLaunchKernelEx(&rc, tcb_reduce_kernel, static_cast<const float *>(a.ws), p.S,
+                                      a.M, int(a.N), a.y, a.ldy));
 }
 
 } // namespace qmm

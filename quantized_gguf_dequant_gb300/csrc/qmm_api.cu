@@ -143,6 +143,10 @@ qmm_status do_gemv_tcb(qmm_t h, const float *X, int64_t ldx, int M, float *Y, in
     a.x = X;
     a.y = Y;
     a.ws = p.S > 1 ? static_cast<float *>(mm.tcb_ws) : nullptr;
+    if (p.tickets > mm.n_tickets)
+        return fail(QMM_ERR_UNSUPPORTED, "%s: the K-sliced plan needs %zu row-group tickets, the "
+                    "handle holds %zu", fn, p.tickets, mm.n_tickets);
+    a.tickets = mm.tickets;
     a.status = mm.status;
     a.ldx = ldx;
     a.ldy = ldy;

@@ -136,14 +136,14 @@ struct TcbPlan {
     int kc = 0;            // super-blocks per slice (at most)
     size_t smem = 0;
     size_t ws_floats = 0;  // partial sums, S * M * N when S > 1
-    size_t tickets = 0;    // unused (0)
+    size_t tickets = 0;    // row-group tickets: R when the slices are added in-kernel, else 0
 };
 struct TcbArgs {
     const void *tmap;      // Matrix::tmap
     const float *x;
     float *y;
     float *ws;             // plan.ws_floats floats when S > 1
-    unsigned *tickets;     // unused
+    unsigned *tickets;     // plan.tickets zeroed counters (reset by the kernel)
     unsigned *status;
     int64_t ldx, ldy, N, K;
     int M;

@@ -290,6 +290,20 @@ def test_launch_count_counts_kernels():
     torch.cuda.synchronize()
     assert q.launch_count() - c0 == 1
     m.close()
+    # K in slices: for one or four rows the slices are added inside the same
+    # launch (last CTA of each row group); for sixteen rows by a second kernel.
+    w, m = _matrix(q.Q4_K, 512, 14336, seed=7)
+    x = to_dev(synth.activations(16, 14336, 8))
+    c0 = q.launch_count()
+    m.gemv(x[0])
+    m.gemv_batched(x[:4])
+    torch.cuda.synchronize()
+    assert q.launch_count() - c0 == 2
+    c0 = q.launch_count()
+    m.gemv_batched(x)
+    torch.cuda.synchronize()
+    assert q.launch_count() - c0 == 2
+    m.close()
 
 
 def test_gemv_chain_in_cuda_graph_matches_eager():
