@@ -9,15 +9,21 @@
 // integer-pipe instruction per weight (isolate the nibble) plus an FMA, and
 // the integer pipe (16 lanes per scheduler) then caps the kernel below the
 // HBM rate.  Here two nibbles are isolated per instruction straight into an
-// fp16 pair: (w & 0x000F000F) | 0x64006400 is the half2 (1024+q0, 1024+q1);
-// one exact fp16 FMA, (1024+q)*sc - 1024*sc = q*sc (<= 945, exact in fp16),
-// applies the sub-block scale, and mma.sync multiplies these q*sc values by
-// the activations.  The activations enter as two fp16 terms (hi + lo, about
-// 22 significant bits) after an exact power-of-two scale per super-block, so
-// the products are exact and only the fp32 accumulation rounds.  The mins
-// are a second small MMA per super-block (m_s against the sub-block sums of
-// x, scaled by a further 2^-5 to stay inside fp16).  Per super-block and row:
-// y += (d*Dq - dmin*32*Dmin) * 2^-s.
+// fp16 pair, and mma.sync multiplies them by the activations.  The
+// activations enter as two fp16 terms (hi + lo, about 22 significant bits)
+// after an exact power-of-two scale per super-block, so the products are
+// exact and only the fp32 accumulation rounds.
+//
+// One activation row (the decode case): the nibbles enter unscaled, as fp16
+// subnormals (w & 0x000F000F is the half2 (q0, q1) * 2^-24), and each pair of
+// MMA columns collects one sub-block (hi and lo activation terms), so the
+// scales and mins apply once per sub-block in fp32 (tc_common.cuh,
+// unit_dot_sb).  Two to four rows: one
+// exact fp16 FMA, (1024+q)*sc - 1024*sc = q*sc (<= 945, exact in fp16), on
+// (w & 0x000F000F) | 0x64006400 applies the sub-block scale to the operand,
+// and the mins are a second small MMA per super-block (m_s against the
+// sub-block sums of x, scaled by a further 2^-5 to stay inside fp16).  Per
+// super-block and row: y += (d*Dq - dmin*32*Dmin) * 2^-s.
 //
 // Work decomposition.  The matrix is cut into units of 16 rows x one
 // 256-weight super-block column (2304 bytes), ordered (matrix, row tile,
@@ -31,6 +37,8 @@
 // repeatable.
 //
 // Fragment layout (mma.sync m16n8k16, A row-major, B col-major): lane = 4g+c.
+// (Two to four activation rows; the one-row layout is described with
+// unit_dot_sb.)
 // For a 16-row tile, lane (g, c) holds rows g and g+8 and owns chunk c of the
 // super-block (qs bytes 32c..32c+31: sub-blocks 2c and 2c+1).  Word t of the
 // chunk feeds k-steps 2t and 2t+1: step 2t takes nibbles (0,4) [sub-block 2c]
@@ -138,10 +146,19 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
     const int NB = P.NB, M = P.M, NS = P.nslot;
 
     uint8_t *ring = smem + size_t(warp) * NS * kTileBytes;
-    uint2 *Bs = reinterpret_cast<uint2 *>(smem + size_t(nw) * NS * kTileBytes);  // [NB][16][NCOL][4]
-    uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(NB) * 16 * NCOL * 4);  // [NB][NCOL][4]
-    float *inv = reinterpret_cast<float *>(Bm + size_t(NB) * NCOL * 4);           // [NB][M]
-    float *part = inv + size_t(NB) * M;                                           // [nw][2][4][16]
+    uint8_t *acts = smem + size_t(nw) * NS * kTileBytes;
+    // One activation row (NCOL == 2): the per-sub-block B layout of
+    // tc_common.cuh, Bx [NB][16][4][2] uint2, its zero block Zx [16][8] and
+    // the sub-block sums Xs [NB][8].  Several rows: Bs [NB][16][NCOL][4] and
+    // the min-MMA fragments Bm [NB][NCOL][4].
+    uint2 *Bx = reinterpret_cast<uint2 *>(acts);
+    uint2 *Zx = Bx + size_t(NB) * 128;
+    float *Xs = reinterpret_cast<float *>(Zx + 128);
+    uint2 *Bs = reinterpret_cast<uint2 *>(acts);
+    uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(NB) * 16 * NCOL * 4);
+    float *inv = NCOL == 2 ? Xs + size_t(NB) * 8
+                           : reinterpret_cast<float *>(Bm + size_t(NB) * NCOL * 4);  // [NB][M]
+    float *part = inv + size_t(NB) * M;                                              // [nw][2][4][16]
     float *res = part + size_t(nw) * 2 * 4 * kTileRows;  // fused: [res_tiles][16] tile results
     uint64_t *bars = reinterpret_cast<uint64_t *>(
         (reinterpret_cast<uintptr_t>(res + size_t(P.fuse ? P.res_tiles : 0) * kTileRows) + 7) &
@@ -218,11 +235,18 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int sb = sb0 + i * nw;
-                    if (sb < NB)
-                        prep_super_block<NCOL>(sb, m, M, v[i], w[i], lane, Bs, Bm, inv);
+                    if (sb < NB) {
+                        if constexpr (NCOL == 2)
+                            prep_super_block_sb(sb, v[i], w[i], lane, Bx, Xs, inv);
+                        else
+                            prep_super_block<NCOL>(sb, m, M, v[i], w[i], lane, Bs, Bm, inv);
+                    }
                 }
             }
         }
+        if constexpr (NCOL == 2)
+            for (int i = threadIdx.x; i < 128; i += blockDim.x)
+                Zx[i] = make_uint2(0u, 0u);
     }
     __syncthreads();
 
@@ -234,6 +258,10 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
     const int mrow = c;        // activation row whose two terms sit in this lane's columns
     const int minv = mrow < M ? mrow : 0;
     const uint8_t *rowA = ring + g * 144;
+    // NCOL == 2: lanes g = 2c and 2c+1 read their half of the chunk's B entry,
+    // the others the zero block.
+    const bool bact = (g >> 1) == c;
+    const int boff = 2 * c + (g & 1);
     float *mypart = part + size_t(warp) * 2 * 4 * kTileRows;
     float tot0 = 0.f, tot1 = 0.f;
     Cursor q = cursor_at(P, u0);
@@ -246,9 +274,17 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
             jfail = j;
             break;
         }
-        unit_dot<NCOL>(rowA + slot * kTileBytes, c, selA, selB, hi4,
-                       Bs + (size_t(q.sb) * 16 * NCOL + col) * 4 + c,
-                       Bm[(size_t(q.sb) * NCOL + col) * 4 + c], inv[q.sb * M + minv], tot0, tot1);
+        if constexpr (NCOL == 2) {
+            const uint2 *bx = bact ? Bx + (size_t(q.sb) * 128 + boff) : Zx;
+            const float2 xab = *reinterpret_cast<const float2 *>(Xs + q.sb * 8 + 2 * c);
+            unit_dot_sb(rowA + slot * kTileBytes, c, selA, selB, hi4, bx, xab, inv[q.sb], tot0,
+                        tot1);
+        } else {
+            unit_dot<NCOL>(rowA + slot * kTileBytes, c, selA, selB, hi4,
+                           Bs + (size_t(q.sb) * 16 * NCOL + col) * 4 + c,
+                           Bm[(size_t(q.sb) * NCOL + col) * 4 + c], inv[q.sb * M + minv], tot0,
+                           tot1);
+        }
 
         // Refill this slot with the unit NS ahead: every lane has consumed its
         // loads of the slot (the values fed the MMAs above), so the copy may
@@ -266,6 +302,13 @@ __global__ void __launch_bounds__(512, 1) gemv_tc_kernel(const __grid_constant__
 
         // ---- the tile ends here (or this warp's share does)
         if (q.sb == NB - 1 || j == nu - 1) {
+            if constexpr (NCOL == 2) {
+                // The four lanes of a row pair hold two sub-blocks each.
+                tot0 += __shfl_xor_sync(0xffffffffu, tot0, 1);
+                tot1 += __shfl_xor_sync(0xffffffffu, tot1, 1);
+                tot0 += __shfl_xor_sync(0xffffffffu, tot0, 2);
+                tot1 += __shfl_xor_sync(0xffffffffu, tot1, 2);
+            }
             const int64_t first = int64_t(q.tile) * NB, last = first + NB - 1;
             if (u0 <= first && u1 - 1 >= last) {
                 if (P.fuse) {
@@ -404,10 +447,11 @@ void gemv_tc_shape(int64_t units_per_cta, int &warps, int &nslot)
 
 size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw, int res_tiles)
 {
-    const int64_t NB = K / 256;
-    const int ncol = 2 * M;
-    return size_t(nw) * nslot * kTileBytes + size_t(NB) * 16 * ncol * 4 * 8 +
-           size_t(NB) * ncol * 4 * 4 + size_t(NB) * M * 4 + size_t(nw) * 2 * 4 * kTileRows * 4 +
+    const size_t NB = size_t(K / 256);
+    const size_t ncol = 2 * size_t(M);
+    const size_t acts = M == 1 ? NB * 128 * 8 + 128 * 8 + NB * 8 * 4 + NB * 4
+                               : NB * 16 * ncol * 4 * 8 + NB * ncol * 4 * 4 + NB * M * 4;
+    return size_t(nw) * nslot * kTileBytes + acts + size_t(nw) * 2 * 4 * kTileRows * 4 +
            size_t(res_tiles) * kTileRows * 4 + 8 + size_t(nw) * nslot * 8;
 }
 

@@ -216,6 +216,156 @@ __device__ __forceinline__ void unit_dot(const uint8_t *tp, int c, uint32_t selA
                      -(r1.dmin * ((dm[2] + dm[3]) * 32.f))), sc, tot1);
 }
 
+// ---------------------------------------------------------------------------
+// One activation row: the nibbles enter the MMA as fp16 subnormals with no
+// scale applied -- w & 0x000F000F is the half2 (q0, q1) * 2^-24 and
+// w & 0x00F000F0 is (q0, q1) * 2^-20, both exact -- and each MMA gathers four
+// sub-blocks, one per lane column c, so that the sub-block scales apply once
+// per sub-block in fp32 instead of once per weight.
+//
+// MMA m = 2t + h of a unit (t = 0..7, h = 0 low / 1 high nibbles): lane c
+// supplies word t of its chunk c, i.e. sub-block 2c+h, elements (4t, 4t+2)
+// in k-slots (2c, 2c+1) and (4t+1, 4t+3) in k-slots (2c+8, 2c+9).  B column
+// 2j holds the hi fp16 terms and column 2j+1 the lo terms of the activations
+// of lane j's sub-block in lane j's k-slots, zeros elsewhere.  So lane c's
+// accumulator columns (2c, 2c+1) are the hi and lo parts of the dot product
+// of its rows with sub-block 2c+h; the 8 MMAs of each h accumulate a whole
+// sub-block:
+//   y_r += d * 2^-s * (sc_2c * 2^24 * D_lo[r] + sc_2c+1 * 2^20 * D_hi[r])
+//          - dmin * (m_2c * X_2c + m_2c+1 * X_2c+1)
+// with X_j the fp32 sum of sub-block j's activations and 2^s the exact
+// power-of-two scale that puts the super-block's activations in fp16 range.
+//
+// B layout in shared memory: uint2 [super-block][m][c][part], part 0 = hi,
+// 1 = lo; lane (g, c) with g >> 1 == c reads entry (c, g & 1), the other
+// lanes a zero block laid out with the same stride.
+
+struct SbScales {
+    float sa, sb;    // sc_2c * 2^24, sc_2c+1 * 2^20
+    float ma, mb;    // m_2c, m_2c+1
+    float d, dmin;
+};
+
+__device__ __forceinline__ SbScales sb_scales(uint4 h, uint32_t selA, uint32_t selB, bool hi4)
+{
+    const uint32_t A = __byte_perm(h.y, h.z, selA);
+    const uint32_t B = __byte_perm(h.w, h.w, selB);
+    const uint32_t R = hi4 ? (((B & 0x00000F0Fu) | ((B >> 4) & 0x0F0F0000u)) |
+                              ((A >> 2) & 0x30303030u))
+                           : (A & 0x3F3F3F3Fu);  // bytes: sc_lo, sc_hi, m_lo, m_hi
+    SbScales s;
+    // (2^23 + v) * 2^k - 2^(23+k) = v * 2^k exactly.
+    s.sa = fmaf(byte_magic(R, 0), 16777216.f, -140737488355328.f);  // 2^24, 2^47
+    s.sb = fmaf(byte_magic(R, 1), 1048576.f, -8796093022208.f);     // 2^20, 2^43
+    s.ma = byte_magic(R, 2) - 8388608.f;
+    s.mb = byte_magic(R, 3) - 8388608.f;
+    const float2 dd = half2_bits_to_float2(h.x);
+    s.d = dd.x;
+    s.dmin = dd.y;
+    return s;
+}
+
+// Super-block sb of the activation row into the layout above.  Lane (cc, tt)
+// = (lane >> 3, lane & 7) holds x[64cc + 4tt .. +3] (v, sub-block 2cc) and
+// x[64cc + 32 + 4tt .. +3] (w, sub-block 2cc+1).  Bx: [NB][16][4][2] uint2,
+// Xs: [NB][8] sub-block sums, inv: [NB] the inverse power-of-two scale.
+__device__ __forceinline__ void prep_super_block_sb(int sb, float4 v, float4 w, int lane, uint2 *Bx,
+                                                    float *Xs, float *inv)
+{
+    const int cc = lane >> 3, tt = lane & 7;
+    uint32_t mb = 0;
+    mb = max(mb, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    mb = max(mb, max(max(__float_as_uint(w.x) & 0x7fffffffu, __float_as_uint(w.y) & 0x7fffffffu),
+                     max(__float_as_uint(w.z) & 0x7fffffffu, __float_as_uint(w.w) & 0x7fffffffu)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    // max|x| < 2^(eM+1): scaling by 2^(14-eM) keeps every term below 2^15.
+    const int s = mb ? 14 - (int(mb >> 23) - 127) : 0;
+    float xs[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
+    if (s >= -126 && s <= 127) {
+        const float f = exp2i(s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] *= f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] = scale_pow2(xs[i], s);
+    }
+    __half hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = __float2half_rn(xs[i]);
+        lo[i] = __float2half_rn(xs[i] - __half2float(hi[i]));
+    }
+    auto pack = [](__half a, __half b) {
+        return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
+    };
+    // MMA 2tt + h takes elements (4tt, 4tt+2 | 4tt+1, 4tt+3) of sub-block 2cc+h.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int o = 4 * h;
+        *reinterpret_cast<uint4 *>(Bx + ((size_t(sb) * 16 + 2 * tt + h) * 4 + cc) * 2) =
+            make_uint4(pack(hi[o], hi[o + 2]), pack(hi[o + 1], hi[o + 3]), pack(lo[o], lo[o + 2]),
+                       pack(lo[o + 1], lo[o + 3]));
+    }
+    // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
+    float sl = (v.x + v.y) + (v.z + v.w);
+    float sh = (w.x + w.y) + (w.z + w.w);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+    }
+    if (tt == 0) {
+        Xs[sb * 8 + 2 * cc] = sl;
+        Xs[sb * 8 + 2 * cc + 1] = sh;
+    }
+    if (lane == 0)
+        inv[sb] = scale_pow2(1.f, -s);
+}
+
+// One unit (16 rows x one super-block) for one activation row.  tp: the tile
+// plus row g; bx: this lane's B entry of MMA 0 (consecutive MMAs 8 uint2
+// apart); xab: (X_2c, X_2c+1); inv: 2^-s.  Adds the unit's share of rows g and
+// g+8 over sub-blocks 2c and 2c+1 to tot0 / tot1 (the four lanes of a row
+// pair are summed at the end of the row tile).
+__device__ __forceinline__ void unit_dot_sb(const uint8_t *tp, int c, uint32_t selA, uint32_t selB,
+                                            bool hi4, const uint2 *bx, float2 xab, float inv,
+                                            float &tot0, float &tot1)
+{
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(tp);
+    const uint4 h1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144);
+    const uint4 qa0 = *reinterpret_cast<const uint4 *>(tp + 16 + 32 * c);
+    const uint4 qa1 = *reinterpret_cast<const uint4 *>(tp + 32 + 32 * c);
+    const uint4 qb0 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 16 + 32 * c);
+    const uint4 qb1 = *reinterpret_cast<const uint4 *>(tp + 8 * 144 + 32 + 32 * c);
+    const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+    const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
+    float dlo[4], dhi[4];  // sub-blocks 2c (low nibbles) and 2c+1 (high nibbles)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
+        const uint2 bl = bx[(2 * t) * 8], bh = bx[(2 * t + 1) * 8];
+        if (t == 0) {
+            mma16816_zero(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, bl.x, bl.y);
+            mma16816_zero(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, bh.x, bh.y);
+        } else {
+            mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, bl.x, bl.y);
+            mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, bh.x, bh.y);
+        }
+    }
+    const SbScales r0 = sb_scales(h0, selA, selB, hi4);
+    const SbScales r1 = sb_scales(h1, selA, selB, hi4);
+    const float q0 = fmaf(r0.sa, dlo[0] + dlo[1], r0.sb * (dhi[0] + dhi[1]));
+    const float q1 = fmaf(r1.sa, dlo[2] + dlo[3], r1.sb * (dhi[2] + dhi[3]));
+    tot0 = fmaf(r0.d * inv, q0, fmaf(-r0.dmin, fmaf(r0.ma, xab.x, r0.mb * xab.y), tot0));
+    tot1 = fmaf(r1.d * inv, q1, fmaf(-r1.dmin, fmaf(r1.ma, xab.x, r1.mb * xab.y), tot1));
+}
+
 // Lane-constant selectors of the (sc, m) bytes of chunk c (see the Q4_K
 // packing): bytes (u0, u0+1) of sc12[0..3] and [4..7], and of sc12[8..11].
 __device__ __forceinline__ void chunk_selectors(int c, uint32_t &selA, uint32_t &selB, bool &hi4)
