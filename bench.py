@@ -577,7 +577,7 @@ def run_ours(args, world, rank, local):
         wb["long" if K > 8192 else "short"] += N * synth.row_bytes(synth.Q4_K, K)
     xy = {"short": 4 * (3 * 4096 + 4096 + 1024 * 2 + 4096 + 14336 * 2),
           "long": 4 * (14336 + 4096)}
-    for which, kname, lpl in (("short", "gemv_tc_kernel", 3), ("long", "gemv_tcb_kernel<1>", 1)):
+    for which, kname, lpl in (("short", "gemv_tc_kernel", 3), ("long", "gemv_tcb_kernel<1, true>", 1)):
         ms_f, _ = time_graph(lambda: q4.step_subset(which), max(3, args.steps // 4), args.warmup,
                              world)
         b = (wb[which] + xy[which]) * nl

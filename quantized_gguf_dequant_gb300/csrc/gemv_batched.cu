@@ -48,7 +48,10 @@ struct TcbParams {
     int nslot;
 };
 
-template <int NT>
+// SB: one activation row (NT == 1, M == 1) with the per-sub-block operand
+// form of tc_common.cuh (unit_dot_sb): unscaled subnormal nibbles, the
+// sub-block scales applied once per sub-block.
+template <int NT, bool SB>
 __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant__ TcbParams P)
 {
     constexpr int NCOL = 8 * NT, MP = 4 * NT;
@@ -63,9 +66,14 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
     const int KC = sb1 - sb0;
 
     uint8_t *ring = smem + size_t(warp) * NS * kTileBytes;
-    uint2 *Bs = reinterpret_cast<uint2 *>(smem + size_t(nw) * NS * kTileBytes);  // [KC][16][NCOL][4]
+    uint8_t *acts = smem + size_t(nw) * NS * kTileBytes;
+    uint2 *Bs = reinterpret_cast<uint2 *>(acts);                                   // [KC][16][NCOL][4]
     uint32_t *Bm = reinterpret_cast<uint32_t *>(Bs + size_t(KC) * 16 * NCOL * 4);   // [KC][NCOL][4]
-    float *inv = reinterpret_cast<float *>(Bm + size_t(KC) * NCOL * 4);            // [KC][MP]
+    // SB: Bx [KC][16][4][2], the zero block Zx [16][8] and Xs [KC][8]
+    uint2 *Bx = reinterpret_cast<uint2 *>(acts);
+    uint2 *Zx = Bx + size_t(KC) * 128;
+    float *Xs = reinterpret_cast<float *>(Zx + 128);
+    float *inv = SB ? Xs + size_t(KC) * 8 : reinterpret_cast<float *>(Bm + size_t(KC) * NCOL * 4);  // [KC][MP]
     float *part = inv + size_t(KC) * MP;                                          // [nw][2][MP][16]
     uint64_t *bars = reinterpret_cast<uint64_t *>(
         (reinterpret_cast<uintptr_t>(part + size_t(nw) * 2 * MP * kTileRows) + 7) & ~uintptr_t(7));
@@ -131,10 +139,17 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
                 const int item = base + i * nw;
                 // One group of four: rows beyond M are not laid out (their
                 // columns repeat real ones below); more groups: zeros.
-                if (item < items && (NT > 1 || item / KC < P.M))
+                if constexpr (SB) {
+                    if (item < KC)
+                        prep_super_block_sb(item, v[i], w[i], lane, Bx, Xs, inv);
+                } else if (item < items && (NT > 1 || item / KC < P.M)) {
                     prep_super_block<NCOL>(item % KC, item / KC, MP, v[i], w[i], lane, Bs, Bm, inv);
+                }
             }
         }
+        if constexpr (SB)
+            for (int i = threadIdx.x; i < 128; i += blockDim.x)
+                Zx[i] = make_uint2(0u, 0u);
     }
     __syncthreads();
 
@@ -145,6 +160,8 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
     float *mypart = part + size_t(warp) * 2 * MP * kTileRows;
     // B column of this lane: with one group of four and M < 4, columns
     // beyond 2M repeat real ones (finite; their outputs are never stored).
+    const bool bact = (g >> 1) == c;  // SB: this lane reads a B entry (else the zero block)
+    const int boff = 2 * c + (g & 1);
     const int col = NT == 1 ? g % (2 * P.M) : g;
     const int cinv = NT == 1 && c >= P.M ? 0 : c;
     // One output (row tile t, rows rr and rr+8, activation row m): to Y, or to
@@ -173,9 +190,17 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
             jfail = j;
             break;
         }
-        unit_dot_nt<NT>(rowA + slot * kTileBytes, c, selA, selB, hi4,
-                        Bs + (size_t(q_sb) * 16 * NCOL + col) * 4 + c,
-                        Bm + (size_t(q_sb) * NCOL + col) * 4 + c, inv + q_sb * MP + cinv, tot0, tot1);
+        if constexpr (SB) {
+            const uint2 *bx = bact ? Bx + (size_t(q_sb) * 128 + boff) : Zx;
+            const float2 xab = *reinterpret_cast<const float2 *>(Xs + q_sb * 8 + 2 * c);
+            unit_dot_sb(rowA + slot * kTileBytes, c, selA, selB, hi4, bx, xab, inv[q_sb], tot0[0],
+                        tot1[0]);
+        } else {
+            unit_dot_nt<NT>(rowA + slot * kTileBytes, c, selA, selB, hi4,
+                            Bs + (size_t(q_sb) * 16 * NCOL + col) * 4 + c,
+                            Bm + (size_t(q_sb) * NCOL + col) * 4 + c, inv + q_sb * MP + cinv, tot0,
+                            tot1);
+        }
         __syncwarp();
         if (issued < nu) {
             if (lane == 0)
@@ -188,6 +213,13 @@ __global__ void __launch_bounds__(256, 1) gemv_tcb_kernel(const __grid_constant_
         }
         const int ju = u0 + j;
         if (q_sb == KC - 1 || j == nu - 1) {
+            if constexpr (SB) {
+                // The four lanes of a row pair hold two sub-blocks each.
+                tot0[0] += __shfl_xor_sync(0xffffffffu, tot0[0], 1);
+                tot1[0] += __shfl_xor_sync(0xffffffffu, tot1[0], 1);
+                tot0[0] += __shfl_xor_sync(0xffffffffu, tot0[0], 2);
+                tot1[0] += __shfl_xor_sync(0xffffffffu, tot1[0], 2);
+            }
             const int first = (ju / KC) * KC, last = first + KC - 1;
             if (u0 <= first && u1 - 1 >= last) {
 #pragma unroll
@@ -294,13 +326,13 @@ __global__ void tcb_reduce_kernel(const float *__restrict__ ws, int S, int M, in
 
 using TcbKernel = void (*)(TcbParams);
 
-TcbKernel pick_tcb(int nt)
+TcbKernel pick_tcb(int nt, bool sb)
 {
     switch (nt) {
-    case 1: return gemv_tcb_kernel<1>;
-    case 2: return gemv_tcb_kernel<2>;
-    case 3: return gemv_tcb_kernel<3>;
-    default: return gemv_tcb_kernel<4>;
+    case 1: return sb ? gemv_tcb_kernel<1, true> : gemv_tcb_kernel<1, false>;
+    case 2: return gemv_tcb_kernel<2, false>;
+    case 3: return gemv_tcb_kernel<3, false>;
+    default: return gemv_tcb_kernel<4, false>;
     }
 }
 
@@ -321,13 +353,14 @@ int tcb_slots()
     return 2;
 }
 
-size_t tcb_smem(int nt, int kc)
+size_t tcb_smem(int nt, int kc, bool sb)
 {
     const size_t ncol = 8 * nt, mp = 4 * nt;
     const int ns = tcb_slots();
-    return size_t(kTcbWarps) * ns * kTileBytes + size_t(kc) * 16 * ncol * 4 * 8 +
-           size_t(kc) * ncol * 4 * 4 + size_t(kc) * mp * 4 + size_t(kTcbWarps) * 2 * mp * kTileRows * 4 +
-           8 + size_t(kTcbWarps) * ns * 8;
+    const size_t acts = sb ? size_t(kc) * 128 * 8 + 128 * 8 + size_t(kc) * 8 * 4
+                           : size_t(kc) * 16 * ncol * 4 * 8 + size_t(kc) * ncol * 4 * 4;
+    return size_t(kTcbWarps) * ns * kTileBytes + acts + size_t(kc) * mp * 4 +
+           size_t(kTcbWarps) * 2 * mp * kTileRows * 4 + 8 + size_t(kTcbWarps) * ns * 8;
 }
 
 } // namespace
@@ -346,7 +379,8 @@ TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
     const int NB = int(K / 256);
     const int T = int((N + kTileRows - 1) / kTileRows);
     int kcmax = 0;
-    while (kcmax < NB && tcb_smem(p.nt, kcmax + 1) <= size_t(227 * 1024))
+    const bool sb = M == 1;
+    while (kcmax < NB && tcb_smem(p.nt, kcmax + 1, sb) <= size_t(227 * 1024))
         ++kcmax;
     if (kcmax == 0)
         return p;
@@ -374,7 +408,7 @@ TcbPlan plan_tcb(int64_t N, int64_t K, int M, int sm_count)
     if (p.R > T)
         p.R = T;
     p.kc = (NB + p.S - 1) / p.S;
-    p.smem = tcb_smem(p.nt, p.kc);
+    p.smem = tcb_smem(p.nt, p.kc, sb);
     p.ws_floats = p.S > 1 ? size_t(p.S) * size_t(M) * size_t(N) : 0;
     p.tickets = (p.S > 1 && M * p.S <= kTcbInKernelPartials) ? size_t(p.R) : 0;
     return p;
@@ -399,7 +433,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     P.R = p.R;
     P.S = p.S;
     P.nslot = tcb_slots();
-    TcbKernel kern = pick_tcb(p.nt);
+    TcbKernel kern = pick_tcb(p.nt, a.M == 1);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
     if (e != cudaSuccess)
         return e;
