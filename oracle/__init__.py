@@ -27,6 +27,13 @@ import numpy as np
 
 Q8_0 = 8
 Q4_K = 12
+Q5_K = 13
+Q6_K = 14
+IQ4_NL = 20
+
+# (bytes, weights) of one block of each format
+BLOCK = {Q8_0: (34, 32), Q4_K: (144, 256), Q5_K: (176, 256), Q6_K: (210, 256),
+         IQ4_NL: (18, 32)}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
@@ -58,6 +65,9 @@ def lib():
         L.or_q4k_scale_min.argtypes = [vp, i32, vp, vp]
         L.or_dequant_block_q4k.argtypes = [vp, vp]
         L.or_dequant_block_q8_0.argtypes = [vp, vp]
+        L.or_dequant_block_q5k.argtypes = [vp, vp]
+        L.or_dequant_block_q6k.argtypes = [vp, vp]
+        L.or_dequant_block_iq4nl.argtypes = [vp, vp]
         L.or_row_bytes.argtypes = [i32, i64]
         L.or_row_bytes.restype = i64
         L.or_dequant_rows.argtypes = [i32, vp, i64, i64, i64, i64, vp]
@@ -123,15 +133,15 @@ def row_bytes(fmt: int, K: int) -> int:
 
 
 def dequant_block(fmt: int, block: bytes) -> np.ndarray:
+    """The exact values of one block of any supported format."""
     b = np.frombuffer(bytes(block), dtype=np.uint8).copy()
-    if fmt == Q4_K:
-        assert b.size == 144
-        out = np.empty(256, np.float64)
-        _check(lib().or_dequant_block_q4k(_p(b), _p(out)), "dequant_block_q4k")
-    else:
-        assert b.size == 34
-        out = np.empty(32, np.float64)
-        _check(lib().or_dequant_block_q8_0(_p(b), _p(out)), "dequant_block_q8_0")
+    nbytes, nw = BLOCK[fmt]
+    assert b.size == nbytes
+    out = np.empty(nw, np.float64)
+    fn = {Q4_K: lib().or_dequant_block_q4k, Q8_0: lib().or_dequant_block_q8_0,
+          Q5_K: lib().or_dequant_block_q5k, Q6_K: lib().or_dequant_block_q6k,
+          IQ4_NL: lib().or_dequant_block_iq4nl}[fmt]
+    _check(fn(_p(b), _p(out)), f"dequant_block({fmt})")
     return out
 
 

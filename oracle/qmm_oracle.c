@@ -28,6 +28,24 @@
  *       2c+1.  w = d*sc_j*q - dmin*m_j.
  *     Q8_0 block, 34 bytes, 32 weights: [0..1] d (binary16), then 32 int8;
  *       w = d*q.
+ *   The further formats of the next step ("Frink Inference: the Rust
+ *   alternative to llama.cpp", sections "Where llama.cpp is still ahead" --
+ *   IQ4_NL -- and "What is supported" -- the other K-quants), also GGUF
+ *   block formats:
+ *     Q5_K super-block, 176 bytes, 256 weights: d, dmin (binary16), the
+ *       twelve scale/min bytes of Q4_K, qh[32] (fifth bits), qs[128] (low
+ *       four bits, in the Q4_K nibble order).  Weight i: chunk c = i/64,
+ *       l = i%64; the fifth bit is bit (2c + (l >= 32)) of qh[l % 32].
+ *       w = d*sc_j*q - dmin*m_j with q in 0..31.
+ *     Q6_K super-block, 210 bytes, 256 weights: ql[128] (low four bits),
+ *       qh[64] (high two bits), sixteen int8 scales, d (binary16).  Weight
+ *       i: half n = i/128, r = i%128, quarter t = r/32, l = r%32; the low
+ *       bits are nibble (t >= 2) of ql[64n + 32*(t & 1) + l], the high bits
+ *       are bits 2t..2t+1 of qh[32n + l]; q = low | high << 4 (0..63);
+ *       w = d * scale[i/16] * (q - 32).
+ *     IQ4_NL block, 18 bytes, 32 weights: d (binary16), qs[16]; weight j
+ *       (j < 16) is the low nibble of qs[j], weight 16+j the high nibble;
+ *       w = d * T[q] with the non-uniform 16-entry table T below.
  *   Every value is little-endian.
  *
  * Every function returns 0 on success and a negative number on a bad
@@ -46,6 +64,15 @@
 
 #define OR_Q8_0 8
 #define OR_Q4_K 12
+#define OR_Q5_K 13
+#define OR_Q6_K 14
+#define OR_IQ4_NL 20
+
+/* The IQ4_NL code book: the value of each 4-bit code before the block
+ * scale (GGUF IQ4_NL format definition).  Parity unpinned: no source here
+ * prints these sixteen values; the tests pin their structure only. */
+static const int iq4nl_table[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
+                                    1,    13,   25,  38,  53,  69,  89,  113};
 
 /* ---------------------------------------------------------------------- */
 /* Scalar decoders                                                         */
@@ -136,6 +163,66 @@ int or_dequant_block_q8_0(const uint8_t *blk, double *w)
     return 0;
 }
 
+/* Decode one 176-byte Q5_K super-block into 256 exact values. */
+int or_dequant_block_q5k(const uint8_t *blk, double *w)
+{
+    if (!blk || !w)
+        return -1;
+    double d = or_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    double dmin = or_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+    const uint8_t *sc12 = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    for (int i = 0; i < 256; ++i) {
+        int j, sc, m;
+        int lo = q4k_quant(qs, i, &j); /* same nibble order as Q4_K */
+        int c = i / 64, l = i % 64;
+        int hi = (qh[l % 32] >> (2 * c + (l >= 32))) & 1;
+        int q5 = lo | (hi << 4);
+        or_q4k_scale_min(sc12, j, &sc, &m);
+        /* d*sc*q5: at most 11+6+5 significant bits; exact in fp64. */
+        w[i] = d * sc * q5 - dmin * m;
+    }
+    return 0;
+}
+
+/* Decode one 210-byte Q6_K super-block into 256 exact values. */
+int or_dequant_block_q6k(const uint8_t *blk, double *w)
+{
+    if (!blk || !w)
+        return -1;
+    const uint8_t *ql = blk;
+    const uint8_t *qh = blk + 128;
+    const uint8_t *scales = blk + 192;
+    double d = or_half_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+    for (int i = 0; i < 256; ++i) {
+        int n = i / 128, r = i % 128, t = r / 32, l = r % 32;
+        int byte = ql[64 * n + 32 * (t & 1) + l];
+        int lo = (t >= 2) ? (byte >> 4) : (byte & 15);
+        int hi = (qh[32 * n + l] >> (2 * t)) & 3;
+        int q = (lo | (hi << 4)) - 32;
+        int sc = (int)scales[i / 16];
+        if (sc > 127)
+            sc -= 256; /* int8 scale */
+        w[i] = d * sc * q;
+    }
+    return 0;
+}
+
+/* Decode one 18-byte IQ4_NL block into 32 exact values. */
+int or_dequant_block_iq4nl(const uint8_t *blk, double *w)
+{
+    if (!blk || !w)
+        return -1;
+    double d = or_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    const uint8_t *qs = blk + 2;
+    for (int j = 0; j < 16; ++j) {
+        w[j] = d * iq4nl_table[qs[j] & 15];
+        w[16 + j] = d * iq4nl_table[qs[j] >> 4];
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Matrix geometry                                                         */
 /* ---------------------------------------------------------------------- */
@@ -149,6 +236,12 @@ int64_t or_row_bytes(int fmt, int64_t K)
         return (K % 256) ? -1 : (K / 256) * 144;
     if (fmt == OR_Q8_0)
         return (K % 32) ? -1 : (K / 32) * 34;
+    if (fmt == OR_Q5_K)
+        return (K % 256) ? -1 : (K / 256) * 176;
+    if (fmt == OR_Q6_K)
+        return (K % 256) ? -1 : (K / 256) * 210;
+    if (fmt == OR_IQ4_NL)
+        return (K % 32) ? -1 : (K / 32) * 18;
     return -1;
 }
 
@@ -160,6 +253,15 @@ static void dequant_row(int fmt, const uint8_t *w, int64_t K, int64_t rb,
     if (fmt == OR_Q4_K) {
         for (int64_t b = 0; b < K / 256; ++b)
             or_dequant_block_q4k(row + b * 144, out + b * 256);
+    } else if (fmt == OR_Q5_K) {
+        for (int64_t b = 0; b < K / 256; ++b)
+            or_dequant_block_q5k(row + b * 176, out + b * 256);
+    } else if (fmt == OR_Q6_K) {
+        for (int64_t b = 0; b < K / 256; ++b)
+            or_dequant_block_q6k(row + b * 210, out + b * 256);
+    } else if (fmt == OR_IQ4_NL) {
+        for (int64_t b = 0; b < K / 32; ++b)
+            or_dequant_block_iq4nl(row + b * 18, out + b * 32);
     } else {
         for (int64_t b = 0; b < K / 32; ++b)
             or_dequant_block_q8_0(row + b * 34, out + b * 32);

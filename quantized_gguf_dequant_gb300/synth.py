@@ -15,6 +15,11 @@ print no real weights):
   0..63 and quants uniform on 0..15, all independent.
 * Q8_0 (34-byte blocks of 32 weights): d as above, quants uniform int8 on
   -127..127.
+* Q5_K (176 bytes / 256): as Q4_K, with the 32 fifth-bit bytes uniform too.
+* Q6_K (210 bytes / 256): the 128 low-bit and 64 high-bit bytes uniform
+  (quants uniform on 0..63), sixteen int8 scales uniform on -128..127, d
+  as above.
+* IQ4_NL (18 bytes / 32): d as above, the 16 code bytes uniform.
 * Activations: fp32 N(0, 1).  Prefill activations: N(0, 1) rounded to bf16.
 * Router: logits N(0, 1) per (token, expert); p = softmax; the top_k largest
   p give the expert ids (distinct) and their p (not renormalised) the fp32
@@ -28,6 +33,9 @@ import numpy as np
 
 Q8_0 = 8
 Q4_K = 12
+Q5_K = 13
+Q6_K = 14
+IQ4_NL = 20
 
 Q4K_BLOCK_BYTES = 144
 Q4K_BLOCK_WEIGHTS = 256
@@ -54,7 +62,16 @@ OLMOE_D_FF = 1024
 OLMOE_TOP_K = 8
 
 
+# (block bytes, block weights) of the formats beyond Q4_K and Q8_0
+_BLOCKS = {Q5_K: (176, 256), Q6_K: (210, 256), IQ4_NL: (18, 32)}
+
+
 def row_bytes(fmt: int, K: int) -> int:
+    if fmt in _BLOCKS:
+        nbytes, nw = _BLOCKS[fmt]
+        if K % nw:
+            raise ValueError(f"format {fmt} needs K % {nw} == 0")
+        return K // nw * nbytes
     if fmt == Q4_K:
         if K % Q4K_BLOCK_WEIGHTS:
             raise ValueError("Q4_K needs K % 256 == 0")
@@ -92,8 +109,44 @@ def q8_0_matrix(N: int, K: int, seed: int) -> np.ndarray:
     return out.reshape(N, -1)
 
 
+def _raw_blocks(fmt: int, N: int, K: int, rng: np.random.Generator) -> np.ndarray:
+    nbytes, nw = _BLOCKS[fmt]
+    nb = N * (K // nw)
+    row_bytes(fmt, K)
+    return np.frombuffer(rng.bytes(nb * nbytes), dtype=np.uint8).reshape(nb, nbytes).copy()
+
+
+def q5k_matrix(N: int, K: int, seed: int) -> np.ndarray:
+    """N x K weights as Q5_K bytes, shape [N, K/256*176] uint8."""
+    rng = np.random.default_rng(seed)
+    raw = _raw_blocks(Q5_K, N, K, rng)
+    raw[:, 0:4] = _fp16_scales(rng, (raw.shape[0], 2)).view(np.uint8).reshape(-1, 4)
+    return raw.reshape(N, -1)
+
+
+def q6k_matrix(N: int, K: int, seed: int) -> np.ndarray:
+    """N x K weights as Q6_K bytes, shape [N, K/256*210] uint8 (the int8
+    scales are uniform bytes)."""
+    rng = np.random.default_rng(seed)
+    raw = _raw_blocks(Q6_K, N, K, rng)
+    raw[:, 208:210] = _fp16_scales(rng, raw.shape[0]).view(np.uint8).reshape(-1, 2)
+    return raw.reshape(N, -1)
+
+
+def iq4nl_matrix(N: int, K: int, seed: int) -> np.ndarray:
+    """N x K weights as IQ4_NL bytes, shape [N, K/32*18] uint8."""
+    rng = np.random.default_rng(seed)
+    raw = _raw_blocks(IQ4_NL, N, K, rng)
+    raw[:, 0:2] = _fp16_scales(rng, raw.shape[0]).view(np.uint8).reshape(-1, 2)
+    return raw.reshape(N, -1)
+
+
 def matrix(fmt: int, N: int, K: int, seed: int) -> np.ndarray:
-    return q4k_matrix(N, K, seed) if fmt == Q4_K else q8_0_matrix(N, K, seed)
+    if fmt == Q4_K:
+        return q4k_matrix(N, K, seed)
+    if fmt == Q8_0:
+        return q8_0_matrix(N, K, seed)
+    return {Q5_K: q5k_matrix, Q6_K: q6k_matrix, IQ4_NL: iq4nl_matrix}[fmt](N, K, seed)
 
 
 def activations(M: int, K: int, seed: int) -> np.ndarray:

@@ -3,7 +3,8 @@
 Each case rebuilds the oracle from a copy of its C source with one mistake
 planted (a swapped nibble, a wrong sign, a wrong index, a dropped term, a
 wrong rounding...), points the oracle module at that build, and runs the
-pins of tests/test_oracle.py against it: at least one pin must fail.  A
+pins of tests/test_oracle.py and tests/test_oracle_formats.py against it:
+at least one pin must fail.  A
 control build of the unchanged source must pass every pin, so a failure
 means the planted mistake was seen.  The planted mistake lives only in the
 temporary copy; the real oracle is untouched and is restored afterwards."""
@@ -17,6 +18,7 @@ import pytest
 
 import oracle
 from tests import test_oracle as pins
+from tests import test_oracle_formats as format_pins
 
 SRC = os.path.join(os.path.dirname(os.path.abspath(oracle.__file__)), "qmm_oracle.c")
 
@@ -42,24 +44,40 @@ MUTANTS = [
     ("bf16 ties away", [("(rest == 0x8000u && (lower & 1u))", "(rest == 0x8000u)")]),
     ("prefill uses exact weights", [("s += wb[k] * xv;", "s += wr[k] * xv;")]),
     ("silu sign", [("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];")]),
+    ("q5_k fifth bit from the wrong sub-block", [("(2 * c + (l >= 32))", "(2 * c)")]),
+    ("q5_k fifth bit weight", [("int q5 = lo | (hi << 4);", "int q5 = lo | (hi << 3);")]),
+    ("q5_k min term dropped", [("w[i] = d * sc * q5 - dmin * m;", "w[i] = d * sc * q5;")]),
+    ("q5_k fifth bit byte", [("(qh[l % 32] >>", "(qh[l / 2] >>")]),
+    ("q6_k offset", [("int q = (lo | (hi << 4)) - 32;", "int q = (lo | (hi << 4)) - 31;")]),
+    ("q6_k scale group of 32", [("scales[i / 16]", "scales[i / 32]")]),
+    ("q6_k scale read unsigned", [("        if (sc > 127)\n            sc -= 256; /* int8 scale */\n", "")]),
+    ("q6_k high-bit shift", [("(qh[32 * n + l] >> (2 * t)) & 3", "(qh[32 * n + l] >> t) & 3")]),
+    ("q6_k low-bit byte", [("ql[64 * n + 32 * (t & 1) + l]", "ql[64 * n + 32 * (t >> 1) + l]")]),
+    ("q6_k nibble choice", [("(t >= 2) ? (byte >> 4) : (byte & 15)", "(t & 1) ? (byte >> 4) : (byte & 15)")]),
+    ("q6_k d from the front", [("blk[208] | (blk[209] << 8)", "blk[0] | (blk[1] << 8)")]),
+    ("iq4_nl nibble halves swapped", [("w[j] = d * iq4nl_table[qs[j] & 15];", "w[j] = d * iq4nl_table[qs[j] >> 4];"),
+                                      ("w[16 + j] = d * iq4nl_table[qs[j] >> 4];", "w[16 + j] = d * iq4nl_table[qs[j] & 15];")]),
+    ("iq4_nl interleaved order", [("w[16 + j] = d * iq4nl_table[qs[j] >> 4];", "w[16 + j] = d * iq4nl_table[qs[15 - j] >> 4];")]),
 ]
 
 
 def _pin_calls():
-    """Every pin of tests/test_oracle.py with its parameter sets."""
+    """Every pin of the two oracle pin modules with its parameter sets."""
     calls = []
-    for name in dir(pins):
-        if not name.startswith("test_"):
-            continue
-        fn = getattr(pins, name)
-        marks = getattr(fn, "pytestmark", [])
-        params = [m for m in marks if m.name == "parametrize"]
-        if not params:
-            calls.append((name, fn, {}))
-            continue
-        argname, values = params[0].args[0], params[0].args[1]
-        for v in values:
-            calls.append((f"{name}[{v}]", fn, {argname: v}))
+    for mod in (pins, format_pins):
+        for name in dir(mod):
+            if not name.startswith("test_"):
+                continue
+            fn = getattr(mod, name)
+            marks = getattr(fn, "pytestmark", [])
+            params = [m for m in marks if m.name == "parametrize"]
+            label = f"{mod.__name__.rsplit('.', 1)[-1]}::{name}"
+            if not params:
+                calls.append((label, fn, {}))
+                continue
+            argname, values = params[0].args[0], params[0].args[1]
+            for v in values:
+                calls.append((f"{label}[{v}]", fn, {argname: v}))
     return calls
 
 
