@@ -676,6 +676,28 @@ def run_ours(args, world, rank, local):
                     "dense (burst figure: each GEMM is a separate launch of tens to hundreds "
                     "of microseconds)"}
     if args.extras:
+        # The further block formats on the same decode step (4 layers, > L2),
+        # through the plain one-warp-per-row decode GEMV.
+        fx = {}
+        for fname, fcode in (("Q5_K", synth.Q5_K), ("Q6_K", synth.Q6_K), ("IQ4_NL", synth.IQ4_NL)):
+            try:
+                mf = Model(fcode, layers=4)
+                bf, _ = layer_bytes(fcode)
+                ms_x, _ = time_graph(lambda: mf.step(True), max(3, args.steps // 8), args.warmup,
+                                     world)
+                fx[fname] = {"ms_per_step": ms_x, "layers": 4, "bytes_per_step": bf * 4,
+                             "gbs": bf * 4 / (ms_x * 1e-3) / 1e9,
+                             "frac_of_peak": bf * 4 / (ms_x * 1e-3) / 1e9 / pk["hbm_gbs"]}
+                mf.close()
+                del mf
+            except Exception as e:  # a secondary line: report, do not lose the run
+                fx[fname] = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.empty_cache()
+        extras["extra_formats_decode"] = dict(
+            fx, unit="GB/s",
+            note="Llama-3.1-8B decode step, 4 layers, the weights in each further format; the "
+                 "first, plain GEMV of these formats (one warp per row)")
+    if args.extras:
         q8 = Model(synth.Q8_0, layers=nl)
         b8, _ = layer_bytes(synth.Q8_0)
         ms8, _ = time_graph(lambda: q8.step(True), max(3, args.steps // 4), args.warmup, world)

@@ -23,8 +23,26 @@
  *             w = d*sc_j*q - dmin*m_j.
  *   QMM_Q8_0  block of 32 weights in 34 bytes: [fp16 d][32 x int8 q];
  *             w = d*q.
+ *   Further formats ("Frink Inference: the Rust alternative to llama.cpp",
+ *   "What is supported": the K-quants; "Where llama.cpp is still ahead":
+ *   IQ4_NL), for qmm_create, qmm_gemv, qmm_gemv_group, qmm_gemv_batched,
+ *   qmm_ffn_decode and qmm_dequantize[_bf16]; the expert and prefill calls
+ *   refuse them (QMM_ERR_UNSUPPORTED):
+ *   QMM_Q5_K  176 bytes / 256 weights: [fp16 d][fp16 dmin][the 12 scale/min
+ *             bytes of Q4_K][32 bytes of fifth bits: bit j of byte l belongs
+ *             to weight l of sub-block j][128 bytes of low nibbles, the Q4_K
+ *             order]; w = d*sc_j*q - dmin*m_j, q in 0..31.
+ *   QMM_Q6_K  210 bytes / 256 weights: [128 bytes of low nibbles][64 bytes of
+ *             2-bit high parts][16 int8 scales, one per 16 weights][fp16 d];
+ *             weight i: half n = i/128, t = (i%128)/32, l = i%32; low bits =
+ *             nibble (t >= 2) of byte 64n + 32*(t&1) + l, high bits = bits
+ *             2t..2t+1 of high-part byte 32n + l; w = d*scale[i/16]*(q - 32).
+ *   QMM_IQ4_NL 18 bytes / 32 weights: [fp16 d][16 bytes: weight l < 16 is the
+ *             low nibble of byte l, weight 16+l its high nibble]; w = d*T[q]
+ *             with GGUF's 16-entry IQ4_NL code book T.
+ *   Every format needs K % 256 == 0 here.
  *   A matrix of N rows and K columns is N rows back to back, each row K/256
- *   (Q4_K) or K/32 (Q8_0) blocks.  An expert-stacked tensor is n_experts such
+ *   (K-quants) or K/32 (Q8_0, IQ4_NL) blocks.  An expert-stacked tensor is n_experts such
  *   matrices back to back: row r of expert e is row e*N_e + r.
  *
  * Conventions for every call:
@@ -63,7 +81,7 @@ extern "C" {
 #endif
 
 /* GGUF tensor-type ids of the supported encodings. */
-typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12 } qmm_format;
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q5_K = 13, QMM_Q6_K = 14, QMM_IQ4_NL = 20 } qmm_format;
 
 typedef enum {
     QMM_OK = 0,

@@ -16,6 +16,9 @@ import os
 
 Q8_0 = 8
 Q4_K = 12
+Q5_K = 13
+Q6_K = 14
+IQ4_NL = 20
 
 OK = 0
 ERR_NULL, ERR_FORMAT, ERR_SHAPE, ERR_ALIGN, ERR_CUDA = -1, -2, -3, -4, -5

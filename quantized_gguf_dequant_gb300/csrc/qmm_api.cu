@@ -164,6 +164,16 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    if (qmm::is_extra_format(m0.fmt)) {
+        for (int i = 0; i < n; ++i) {
+            const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
+            cudaError_t e = qmm::launch_gemv_fmt(mi, x, 1, mi.K, ys[i], mi.N, s);
+            if (e != cudaSuccess)
+                return cuda_fail(e, fn);
+        }
+        reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+        return QMM_OK;
+    }
     if (m0.fmt == QMM_Q4_K && tc_fits(m0, 1))
         return do_gemv_tc(hs, n, x, m0.K, 1, ys, 0, s, fn);
     // One Q4_K matrix whose x does not fit the decode kernel (K > 8192): the
@@ -361,19 +371,20 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
     *out = nullptr;
     if (!w_dev)
         return fail(QMM_ERR_NULL, "qmm_create: the weight pointer is NULL");
-    if (fmt != QMM_Q4_K && fmt != QMM_Q8_0)
+    if (fmt != QMM_Q4_K && fmt != QMM_Q8_0 && !qmm::is_extra_format(fmt))
         return fail(QMM_ERR_FORMAT,
-                    "qmm_create: format %d is not supported (Q4_K = 12 and Q8_0 = 8 are)", int(fmt));
+                    "qmm_create: format %d is not supported (Q4_K = 12, Q8_0 = 8, Q5_K = 13, "
+                    "Q6_K = 14 and IQ4_NL = 20 are)", int(fmt));
     if (N < 1)
         return fail(QMM_ERR_SHAPE, "qmm_create: N = %lld rows; at least one row is needed",
                     (long long)N);
     if (K < 256 || K % 256 != 0)
         return fail(QMM_ERR_SHAPE,
-                    fmt == QMM_Q4_K
-                        ? "qmm_create: K = %lld is not a positive multiple of 256 (a Q4_K "
-                          "super-block holds 256 weights)"
-                        : "qmm_create: K = %lld is not a positive multiple of 256 (Q8_0 rows must "
-                          "be 16-byte multiples here, which needs K %% 256 == 0)",
+                    (fmt == QMM_Q8_0 || fmt == QMM_IQ4_NL)
+                        ? "qmm_create: K = %lld is not a positive multiple of 256 (rows of "
+                          "32-weight blocks are taken in whole 256-weight groups here)"
+                        : "qmm_create: K = %lld is not a positive multiple of 256 (a K-quant "
+                          "super-block holds 256 weights)",
                     (long long)K);
     if (K > (int64_t(1) << 20))
         return fail(QMM_ERR_SHAPE, "qmm_create: K = %lld exceeds the supported maximum 1048576",
@@ -544,6 +555,13 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     if (!aligned(Y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (qmm::is_extra_format(m.fmt)) {
+        cudaError_t e = qmm::launch_gemv_fmt(m, X, int(M), ldx, Y, ldy, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "qmm_gemv_batched");
+        reinterpret_cast<Matrix *>(h)->last_stream = s;
+        return QMM_OK;
+    }
     const char *bpath = getenv("QMM_BATCHED_PATH");
     const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
     if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes) {

@@ -51,8 +51,23 @@ struct Matrix {
 // Bytes of one row for a supported format (K already validated).
 inline int64_t row_bytes_of(int fmt, int64_t K)
 {
-    return fmt == QMM_Q4_K ? (K / 256) * 144 : (K / 32) * 34;
+    switch (fmt) {
+    case QMM_Q4_K: return (K / 256) * 144;
+    case QMM_Q5_K: return (K / 256) * 176;
+    case QMM_Q6_K: return (K / 256) * 210;
+    case QMM_IQ4_NL: return (K / 32) * 18;
+    default: return (K / 32) * 34;
+    }
 }
+
+// The further block formats (formats.cu): Q5_K, Q6_K, IQ4_NL.  Decode GEMV
+// for 1..16 activation rows (X rows ldx apart, Y rows ldy apart) and block
+// decode to fp32 or bf16 (exactly one of out_f32 / out_bf16).
+bool is_extra_format(int fmt);
+cudaError_t launch_gemv_fmt(const Matrix &m, const float *X, int M, int64_t ldx, float *Y,
+                            int64_t ldy, cudaStream_t s);
+cudaError_t launch_dequant_fmt(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,
+                               uint16_t *out_bf16, cudaStream_t s);
 
 // Kernel launches issued by the library (qmm_launch_count): every launcher
 // passes its launch status through counted().
