@@ -79,10 +79,31 @@ def test_create_refuses_by_name(L):
     assert rc == q.ERR_NULL
 
 
+def test_format_ids_agree_with_the_header():
+    text = open(HEADER).read()
+    enum = re.search(r"typedef enum \{([^}]*)\} qmm_format;", text).group(1)
+    ids = {k: int(v) for k, v in re.findall(r"QMM_(\w+)\s*=\s*(\d+)", enum)}
+    assert ids == {"Q8_0": q.Q8_0, "Q4_K": q.Q4_K, "Q5_K": q.Q5_K, "Q6_K": q.Q6_K,
+                   "IQ4_NL": q.IQ4_NL}
+    # GGUF tensor-type ids
+    assert (q.Q8_0, q.Q4_K, q.Q5_K, q.Q6_K, q.IQ4_NL) == (8, 12, 13, 14, 20)
+
+
+def test_create_refuses_further_formats_by_name(L):
+    for fmt in (q.Q5_K, q.Q6_K, q.IQ4_NL):
+        rc, msg = _create(fmt, 16, 1000, 0x10000)
+        assert rc == q.ERR_SHAPE and "K = 1000" in msg and "256" in msg
+        rc, msg = _create(fmt, 16, 4096, 0x10008)
+        assert rc == q.ERR_ALIGN and "16-byte" in msg
+    rc, msg = _create(15, 16, 4096, 0x10000)
+    assert rc == q.ERR_FORMAT and "format 15" in msg and "IQ4_NL = 20" in msg
+
+
 def test_calls_on_null_handle_refuse(L):
     vp = ctypes.c_void_p
     assert L.qmm_gemv(None, vp(16), vp(16), None) == q.ERR_NULL
     assert "handle is NULL" in q.last_error()
+    assert L.qmm_ffn_decode(None, None, None, vp(16), vp(16), vp(16), None) == q.ERR_NULL
     assert L.qmm_destroy(None) == q.ERR_NULL
     assert L.qmm_dequantize(None, 0, 1, vp(16), None) == q.ERR_NULL
     assert L.qmm_gemv_group(None, 1, vp(16), None, None) == q.ERR_NULL
