@@ -676,6 +676,57 @@ def run_ours(args, world, rank, local):
                     "dense (burst figure: each GEMM is a separate launch of tens to hundreds "
                     "of microseconds)"}
     if args.extras:
+        q8 = Model(synth.Q8_0, layers=nl)
+        b8, _ = layer_bytes(synth.Q8_0)
+        ms8, _ = time_graph(lambda: q8.step(True), max(3, args.steps // 4), args.warmup, world)
+        extras["q8_0_decode"] = {
+            "value": b8 * nl / (ms8 * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms8,
+            "bytes_per_step": b8 * nl,
+            "frac_of_peak": b8 * nl / (ms8 * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        q8.close()
+        del q8
+        torch.cuda.empty_cache()
+    if args.extras:
+        # Context for the fusion itself: the same 4-layer Q4_K decode step done
+        # the unfused way -- each matrix decoded to a bf16 buffer in HBM
+        # (qmm_dequantize_bf16), then a cuBLAS bf16 GEMV through torch.matmul
+        # (x given in bf16 already).  Not a product path; a reported baseline.
+        try:
+            mu = Model(synth.Q4_K, layers=4)
+            kin = [0, 0, 0, 1, 2, 2, 3]
+            xbs = [[x.to(torch.bfloat16) for x in xv] for _, xv, _ in mu.layers]
+            ybs = [[torch.empty(N, dtype=torch.bfloat16, device="cuda") for _, N, _ in SHAPES]
+                   for _ in mu.layers]
+            wbuf = torch.empty(max(N * K for _, N, K in SHAPES), dtype=torch.int16, device="cuda")
+            q = mu.q
+
+            def unfused_step():
+                for L, (mats, _, _) in enumerate(mu.layers):
+                    for j, m in enumerate(mats):
+                        q.dequantize_bf16(m.h, 0, m.N, wbuf)
+                        W = wbuf[:m.N * m.K].view(torch.bfloat16).view(m.N, m.K)
+                        torch.matmul(W, xbs[L][kin[j]], out=ybs[L][j])
+
+            nsteps = max(3, args.steps // 20)
+            ms_un, _ = time_graph(unfused_step, nsteps, args.warmup, world)
+            ms_fu, _ = time_graph(lambda: mu.step(True), nsteps, args.warmup, world)
+            b4, _ = layer_bytes(synth.Q4_K)
+            extras["unfused_torch_baseline"] = {
+                "layers": 4, "ms_per_step_unfused": ms_un, "ms_per_step_fused": ms_fu,
+                "unfused_over_fused": ms_un / ms_fu,
+                "gbs_unfused": b4 * 4 / (ms_un * 1e-3) / 1e9, "gbs_fused": b4 * 4 / (ms_fu * 1e-3) / 1e9,
+                "unit": "GB/s of quantized algorithmic bytes",
+                "note": "decode to a bf16 buffer (qmm_dequantize_bf16) then torch.matmul (cuBLAS) per "
+                        "matrix, against the fused path on the same 4 layers"}
+            mu.close()
+            del mu, wbuf, xbs, ybs
+        except Exception as e:  # a secondary line: report, do not lose the run
+            extras["unfused_torch_baseline"] = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            torch.cuda.empty_cache()
+        except Exception:
+            pass
+    if args.extras:
         # The further block formats on the same decode step (4 layers, > L2),
         # through the plain one-warp-per-row decode GEMV.
         fx = {}
@@ -692,22 +743,14 @@ def run_ours(args, world, rank, local):
                 del mf
             except Exception as e:  # a secondary line: report, do not lose the run
                 fx[fname] = {"error": f"{type(e).__name__}: {e}"}
-            torch.cuda.empty_cache()
+            try:
+                torch.cuda.empty_cache()
+            except Exception:
+                pass
         extras["extra_formats_decode"] = dict(
             fx, unit="GB/s",
             note="Llama-3.1-8B decode step, 4 layers, the weights in each further format; the "
                  "first, plain GEMV of these formats (one warp per row)")
-    if args.extras:
-        q8 = Model(synth.Q8_0, layers=nl)
-        b8, _ = layer_bytes(synth.Q8_0)
-        ms8, _ = time_graph(lambda: q8.step(True), max(3, args.steps // 4), args.warmup, world)
-        extras["q8_0_decode"] = {
-            "value": b8 * nl / (ms8 * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms8,
-            "bytes_per_step": b8 * nl,
-            "frac_of_peak": b8 * nl / (ms8 * 1e-3) / 1e9 / pk["hbm_gbs"]}
-        q8.close()
-        del q8
-        torch.cuda.empty_cache()
 
     dom = max(fam.values(), key=lambda f: f["ms_per_step"])
     traffic = recorded_traffic(dom["kernel"])
