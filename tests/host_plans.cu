@@ -1,0 +1,57 @@
+// Host-only driver of the library's launch planners (no GPU needed): prints
+// one JSON object per line for the shapes tests/test_host_plans.py asks
+// about.  Linked against the library's object files; it calls only host
+// functions that make no CUDA runtime call.
+//
+// Usage: host_plans <sm_count>
+#include <cstdio>
+#include <cstdlib>
+
+#include "../quantized_gguf_dequant_gb300/csrc/qmm_internal.h"
+
+int main(int argc, char **argv)
+{
+    const int sms = argc > 1 ? atoi(argv[1]) : 152;
+    const long long Ns[] = {1, 16, 300, 512, 1024, 4096, 14336, 28672};
+    const long long Ks[] = {256, 1024, 2048, 4096, 8192, 14336};
+    for (long long N : Ns)
+        for (long long K : Ks)
+            for (int M = 1; M <= 16; ++M) {
+                const qmm::TcbPlan p = qmm::plan_tcb(N, K, M, sms);
+                printf("{\"kind\": \"tcb\", \"N\": %lld, \"K\": %lld, \"M\": %d, \"nt\": %d, "
+                       "\"S\": %d, \"R\": %d, \"kc\": %d, \"smem\": %zu, \"ws_floats\": %zu, "
+                       "\"tickets\": %zu}\n",
+                       N, K, M, p.nt, p.S, p.R, p.kc, p.smem, p.ws_floats, p.tickets);
+            }
+    for (int tok : {128, 256})
+        for (long long K : {1024LL, 4096LL, 14336LL})
+            for (int tiles = 1; tiles <= 4 * sms + 7; ++tiles) {
+                const qmm::GemmSplit g = qmm::gemm_q4k_split(tiles, tok, K, sms);
+                printf("{\"kind\": \"gemm_split\", \"tiles\": %d, \"tok\": %d, \"K\": %lld, "
+                       "\"full\": %d, \"ksplit\": %d}\n",
+                       tiles, tok, K, g.full, g.ksplit);
+            }
+    for (long long M : {1LL, 100LL, 512LL, 2048LL})
+        for (long long N : {1LL, 1024LL, 4096LL, 14336LL})
+            for (int tok : {128, 256})
+                printf("{\"kind\": \"gemm_tiles\", \"M\": %lld, \"N\": %lld, \"tok\": %d, "
+                       "\"tiles\": %d, \"smem\": %zu}\n",
+                       M, N, tok, qmm::gemm_q4k_tiles(M, N, tok), qmm::gemm_q4k_smem(tok));
+    for (long long K : Ks)
+        for (int M = 1; M <= 4; ++M)
+            printf("{\"kind\": \"tc_smem\", \"K\": %lld, \"M\": %d, \"smem_16x2\": %zu, "
+                   "\"smem_16x3\": %zu}\n",
+                   K, M, qmm::gemv_tc_smem(K, M, 2, 16), qmm::gemv_tc_smem(K, M, 3, 16));
+    for (int fmt : {int(QMM_Q4_K), int(QMM_Q8_0)})
+        for (long long N : Ns)
+            for (long long K : Ks) {
+                const qmm::GemvPlan p = qmm::plan_gemv(fmt, N, K, sms, 0);
+                printf("{\"kind\": \"gemv\", \"fmt\": %d, \"N\": %lld, \"K\": %lld, "
+                       "\"kchunks\": %d, \"ksplit\": %d, \"rg\": %d, \"rpg\": %d, "
+                       "\"stage_rows\": %d, \"stages\": %d, \"threads\": %d, "
+                       "\"row_slices\": %d, \"slice_bytes\": %lld, \"smem\": %zu}\n",
+                       fmt, N, K, p.kchunks, p.ksplit, p.rg, p.rpg, p.stage_rows, p.stages,
+                       p.threads, p.row_slices, (long long)p.slice_bytes, p.smem);
+            }
+    return 0;
+}

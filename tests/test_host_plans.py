@@ -1,0 +1,137 @@
+"""The library's launch planners on the host (no GPU): how the decode, batched,
+prefill and fp32 GEMV launches cut their work, checked for every shape of a
+grid against the invariants the kernels rely on (every weight covered once,
+shared memory within the 227 KB a CTA may have, the grid within one CTA per
+SM, scratch sized to what is written, in-kernel slice sums only where they
+were measured to pay).
+
+tests/host_plans.cu drives the planners through the library's own object
+files; it makes no CUDA runtime call, so it runs here.
+"""
+from __future__ import annotations
+
+import json
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from quantized_gguf_dequant_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152
+SMEM_MAX = 227 * 1024
+
+needs_nvcc = pytest.mark.skipif(not os.path.exists(qbuild.nvcc()) and shutil.which("nvcc") is None,
+                                reason="nvcc is needed to link the planner driver")
+
+
+@pytest.fixture(scope="module")
+def plans(tmp_path_factory):
+    qbuild.build()
+
+    def objects():
+        if not os.path.isdir(qbuild.BUILD):
+            return []
+        return sorted(os.path.join(qbuild.BUILD, f) for f in os.listdir(qbuild.BUILD)
+                      if f.endswith(".o"))
+
+    objs = objects()
+    if len(objs) < len(qbuild.SOURCES):  # the library exists but its objects were removed
+        qbuild.build(force=True)
+        objs = objects()
+    exe = str(tmp_path_factory.mktemp("plans") / "host_plans")
+    subprocess.run([qbuild.nvcc(), "-std=c++17", "-O1", "-I" + os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "host_plans.cu"), *objs, "-o", exe, *qbuild.ARCH],
+                   check=True, capture_output=True)
+    env = {k: v for k, v in os.environ.items() if not k.startswith("QMM_")}  # defaults only
+    out = subprocess.run([exe, str(SMS)], check=True, capture_output=True, text=True, env=env).stdout
+    recs = [json.loads(line) for line in out.splitlines()]
+    by = {}
+    for r in recs:
+        by.setdefault(r["kind"], []).append(r)
+    return by
+
+
+@needs_nvcc
+def test_batched_plans(plans):
+    rows = plans["tcb"]
+    assert len(rows) == 8 * 6 * 16
+    for p in rows:
+        N, K, M = p["N"], p["K"], p["M"]
+        NB, T = K // 256, (N + 15) // 16
+        assert p["nt"] == (M + 3) // 4
+        assert p["S"] >= 1, p  # every shape of the grid fits
+        S, kc, R = p["S"], p["kc"], p["R"]
+        assert kc * S >= NB and (S - 1) * kc < NB, p  # K covered, no empty slice
+        assert kc <= max(1, 16 // p["nt"]), p  # one round of activation items per warp
+        assert 1 <= R <= T and R * S <= max(SMS, S), p
+        assert p["smem"] <= SMEM_MAX, p
+        assert p["ws_floats"] == (S * M * N if S > 1 else 0), p
+        in_kernel = S > 1 and M * S <= 16
+        assert p["tickets"] == (R if in_kernel else 0), p
+
+
+@needs_nvcc
+def test_batched_plan_of_the_down_projection(plans):
+    down = {p["M"]: p for p in plans["tcb"] if p["N"] == 4096 and p["K"] == 14336}
+    one = down[1]
+    assert (one["S"], one["R"], one["kc"], one["tickets"]) == (4, 38, 14, 38)
+    sixteen = down[16]
+    assert (sixteen["nt"], sixteen["S"], sixteen["tickets"]) == (4, 14, 0)
+
+
+@needs_nvcc
+def test_prefill_split(plans):
+    for g in plans["gemm_split"]:
+        tiles, K, full, ks = g["tiles"], g["K"], g["full"], g["ksplit"]
+        assert 1 <= ks <= 16 and (K // 256) % ks == 0, g
+        if tiles % SMS == 0:
+            assert ks == 1 and full == tiles, g  # whole waves: nothing to split
+        if ks > 1:
+            assert full == tiles - tiles % SMS and full % SMS == 0, g  # only the tail wave splits
+        else:
+            assert full == tiles, g
+    # a short tail of a long K is split; a nearly full wave is not
+    d = {(g["tiles"], g["tok"], g["K"]): g for g in plans["gemm_split"]}
+    assert d[(SMS + 8, 256, 14336)]["ksplit"] > 1
+    assert d[(2 * SMS - 1, 256, 14336)]["ksplit"] == 1
+
+
+@needs_nvcc
+def test_prefill_tiles(plans):
+    for g in plans["gemm_tiles"]:
+        M, N, tok = g["M"], g["N"], g["tok"]
+        assert g["tiles"] == -(-M // tok) * -(-N // 256), g
+        assert g["smem"] <= SMEM_MAX, g
+
+
+@needs_nvcc
+def test_decode_kernel_shared_memory(plans):
+    rows = {(r["K"], r["M"]): r for r in plans["tc_smem"]}
+    for (K, M), r in rows.items():
+        assert r["smem_16x2"] < r["smem_16x3"]
+        if M > 1:
+            assert rows[(K, M - 1)]["smem_16x2"] <= r["smem_16x2"]
+    Ks = sorted({K for K, _ in rows})
+    for M in range(1, 5):
+        s = [rows[(K, M)]["smem_16x2"] for K in Ks]
+        assert s == sorted(s)  # grows with K
+    # the decode route takes every K <= 8192 for one row (checked with 3 slots)
+    assert rows[(8192, 1)]["smem_16x3"] <= SMEM_MAX
+
+
+@needs_nvcc
+def test_fp32_gemv_plans(plans):
+    for p in plans["gemv"]:
+        fmt, N, K = p["fmt"], p["N"], p["K"]
+        assert p["kchunks"] * p["ksplit"] == K // 64, p  # the row is cut into whole slices
+        assert (K // 256) % p["ksplit"] == 0, p  # of whole 256-weight blocks
+        assert p["kchunks"] <= 256 and p["threads"] <= 1024, p
+        assert p["stage_rows"] == p["rg"] * p["rpg"] and p["rpg"] in (1, 2, 4), p
+        assert 2 <= p["stages"] <= 16, p
+        assert 1 <= p["row_slices"] <= N, p
+        per_chunk = 36 if fmt == 12 else 68  # bytes of 64 weights: Q4_K, Q8_0
+        assert p["slice_bytes"] == p["kchunks"] * per_chunk, p
+        assert p["smem"] <= SMEM_MAX, p
