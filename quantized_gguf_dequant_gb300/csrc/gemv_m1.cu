@@ -1,0 +1,714 @@
+// gemv_m1.cu -- Q4_K decode GEMV for one activation row (y = W x), the
+// kernel that streams the weights of a batch-1 decode step.
+//
+// The operation: "Building a Rust Inference Engine That Matches Llama.cpp",
+// "Where the wins came from" -- the dequantisation is paid once, inside the
+// dot product, never as a separate memory-bound pass over a decoded buffer.
+//
+// Arithmetic (the one-row operand form of tc_common.cuh, unit_dot_sb): the
+// nibbles enter mma.sync.m16n8k16 unscaled, as fp16 subnormals (w & 0x000F000F
+// is the half pair (q0, q1) * 2^-24, w & 0x00F000F0 is (q0, q1) * 2^-20), and
+// the activations as two fp16 terms (hi + lo) after an exact power-of-two
+// scale per super-block, so every product is exact and only the fp32
+// accumulation rounds.  Lane column c of an MMA carries sub-block 2c (low
+// nibbles) or 2c+1 (high nibbles); B column pair (2c, 2c+1) holds the hi and
+// lo terms of that sub-block's activations, zeros elsewhere.  Each lane then
+// applies d*sc and dmin*m once per (row, sub-block) in fp32, for its two rows
+// g and g+8 together in packed fp32 (FFMA2):
+//   y_r += d * 2^-s * (sc_2c * 2^24 * D_lo + sc_2c+1 * 2^20 * D_hi)
+//          - dmin * (m_2c * X_2c + m_2c+1 * X_2c+1)
+// with X_j the fp32 sum of sub-block j's activations.
+//
+// Work decomposition.  The 16-row tiles of all matrices of a group (they
+// share x) are concatenated (T tiles); K is cut into S slices of KS <= 16
+// super-blocks.  A work item is TS consecutive tiles x one slice: KS*TS
+// units of 16 rows x 256 weights (2304 bytes each), exactly one ring slot.
+// CTA b works on slice b % S.  Items are handed out in two phases: each CTA's
+// first F items are fixed (so that its producer can fetch them before the
+// previous kernel in the stream has finished), the rest come from a counter
+// per slice, so CTAs on faster SMs take more.  Each item is computed whole by
+// one CTA, in a fixed order: results do not depend on the schedule.
+//
+// Inside a CTA one producer warp and W = KS*TS consumer warps:
+//  - the producer fills a ring of slots with one TMA box per tile, through
+//    a 3-D view of the matrix (144-byte super-block, row, super-block index)
+//    that lands the tile as KS units of 16 rows x 144 bytes -- rows 144 bytes
+//    apart, so the lanes reading the same column of neighbouring rows hit
+//    different banks -- completing on the slot's mbarrier.  It writes the
+//    slot's item index first, and a negative index once the work has run out;
+//  - consumer warp w always takes unit w = (tile w / KS, super-block w % KS)
+//    of a slot, so its B fragments stay in registers for the whole launch.  It
+//    copies its unit to registers, releases the slot, runs 16 MMAs and the
+//    scaling, and stores the two rows it covers into the column of partial
+//    sums of its super-block;
+//  - at the end the columns are added in column order and, with S > 1, the
+//    slices in slice order by the CTA that finished an item's last slice (a
+//    ticket per item): no float atomics, bitwise repeatable.
+// The last CTA of a slice to stop fetching resets its counters, and counters
+// are touched only after the previous kernel has completed, so back-to-back
+// launches and CUDA-graph replays each start from zero.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include <cuda.h>
+
+#include "qmm_device.cuh"
+#include "qmm_internal.h"
+#include "tc_common.cuh"
+
+namespace qmm {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kM1MaxSlots = 16;
+constexpr int kM1MaxShare = 16;  // average items per CTA at most
+
+struct M1Params {
+    CUtensorMap tmap[kMaxGroup];  // 3-D column view of each matrix, box (18, 16, KS)
+    int tile_end[kMaxGroup];      // cumulative 16-row tile counts
+    int rows[kMaxGroup];
+    float *y[kMaxGroup];
+    const float *x;
+    float *ws;                    // [S][T*16] K-slice partial sums (S > 1)
+    unsigned *ctr;                // [S] next item, [S] CTAs done, [n_items] item tickets (S > 1)
+    unsigned *status;
+    int T, nmat;
+    int S, KS;                    // K slices, super-blocks per slice
+    int TS, W;                    // tiles per item, consumer warps (KS * TS)
+    int G1;                       // CTAs per slice
+    int n_items;                  // items per slice (ceil(T / TS))
+    int F;                        // fixed items per CTA
+    int cap;                      // items a CTA may take
+    int nslot, slot_bytes;
+};
+
+__device__ __forceinline__ void named_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
+{
+    int m = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxGroup - 1; ++i)
+        if (i < P.nmat - 1 && t >= P.tile_end[i])
+            m = i + 1;
+    return m;
+}
+
+// Global row (tile*16 + r) -> (matrix, row of the matrix); false if the tile
+// is the ragged end of a matrix and the row does not exist.
+__device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, int &m, int &row)
+{
+    m = mat_of_tile(P, tile);
+    row = (tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
+    return row < P.rows[m];
+}
+
+// One box of the 3-D column view (tmap.cu, make_q4k_column_map): rows
+// [row, row+16) x super-blocks [sb, sb+KS) -> KS units of 16 x 144 bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int row, int sb,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(sb), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+
+// Shared-memory float store executed only where pred holds.
+__device__ __forceinline__ void sts_f32_if(uint32_t a, float v, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%0], %1;\n\t}" ::"r"(a),
+                 "f"(v), "r"(uint32_t(pred))
+                 : "memory");
+}
+
+// Poll an mbarrier phase without spinning hard: between polls the thread
+// sleeps, so a waiting producer leaves the issue slots to the consumers.
+// Gives up (false) after `budget` cycles.
+__device__ __forceinline__ bool mbar_wait_polled(uint64_t *bar, unsigned parity,
+                                                 long long budget = kWaitBudgetCycles)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(128);
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (clock64() - t0 > budget)
+            return false;
+    }
+}
+
+// Lane-constant part of the (sc, m) byte extraction for chunk c (see the
+// Q4_K packing): sel picks bytes (u, u+1, 4+u, 5+u), u = 2*(c & 1).  For
+// chunks 0 and 1 the fields are the low six bits of sc12[u..] and sc12[4+u..];
+// for chunks 2 and 3 the low four bits come from sc12[8+u..] (low or high
+// nibble) and the top two from bits 6-7 of sc12[u..] / sc12[4+u..].
+struct ScaleSel {
+    uint32_t sel, m1, m2, sh;
+};
+
+__device__ __forceinline__ ScaleSel scale_sel(int c)
+{
+    ScaleSel s;
+    const uint32_t u = 2u * uint32_t(c & 1);
+    s.sel = u * 0x1111u + 0x5410u;
+    const bool hi = c >= 2;
+    s.m1 = hi ? 0x0F0F0F0Fu : 0u;
+    s.m2 = hi ? 0x30303030u : 0x3F3F3F3Fu;
+    s.sh = hi ? 2u : 0u;
+    return s;
+}
+
+// Bytes (sc_2c, sc_2c+1, m_2c, m_2c+1) of a row header.
+__device__ __forceinline__ uint32_t scale_bytes(uint4 h, const ScaleSel &L)
+{
+    const uint32_t A = __byte_perm(h.y, h.z, L.sel);
+    const uint32_t Q = __byte_perm(h.w, h.w >> 4, L.sel);
+    return (Q & L.m1) | ((A >> L.sh) & L.m2);
+}
+
+// The contributions of rows g (header h0) and g+8 (h1) over this lane's two
+// sub-blocks, in packed fp32: Dlo / Dhi hold (row g, row g+8) sums of the hi
+// and lo MMA columns of sub-blocks 2c / 2c+1.
+__device__ __forceinline__ float2 pair_total(uint4 h0, uint4 h1, const ScaleSel &L, float2 Dlo,
+                                             float2 Dhi, float2 X0, float2 X1, float2 iv)
+{
+    const uint32_t R0 = scale_bytes(h0, L), R1 = scale_bytes(h1, L);
+    // (2^23 + v) * 2^k - 2^(23+k) = v * 2^k exactly.
+    const float2 sa = __ffma2_rn(make_float2(byte_magic(R0, 0), byte_magic(R1, 0)),
+                                 make_float2(16777216.f, 16777216.f),
+                                 make_float2(-140737488355328.f, -140737488355328.f));
+    const float2 sb = __ffma2_rn(make_float2(byte_magic(R0, 1), byte_magic(R1, 1)),
+                                 make_float2(1048576.f, 1048576.f),
+                                 make_float2(-8796093022208.f, -8796093022208.f));
+    const float2 ma = __fadd2_rn(make_float2(byte_magic(R0, 2), byte_magic(R1, 2)),
+                                 make_float2(-8388608.f, -8388608.f));
+    const float2 mb = __fadd2_rn(make_float2(byte_magic(R0, 3), byte_magic(R1, 3)),
+                                 make_float2(-8388608.f, -8388608.f));
+    const float2 d0 = half2_bits_to_float2(h0.x), d1 = half2_bits_to_float2(h1.x);
+    const float2 q = __ffma2_rn(sa, Dlo, __fmul2_rn(sb, Dhi));
+    const float2 mn = __ffma2_rn(ma, X0, __fmul2_rn(mb, X1));
+    const float2 dd = __fmul2_rn(make_float2(d0.x, d1.x), iv);
+    return __ffma2_rn(dd, q, __fmul2_rn(make_float2(-d0.y, -d1.y), mn));
+}
+
+// Activations of one super-block into its B entries bx[t][c][term] (uint4:
+// the fragments of the low- and high-nibble MMAs of k-step t), its eight
+// sub-block sums and 2^-s.  Lane (cc, tt) = (lane >> 3, lane & 7) holds
+// x[64cc + 4tt .. +3] (v, sub-block 2cc) and x[64cc + 32 + 4tt .. +3] (w,
+// sub-block 2cc+1).
+__device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx, float *xsum,
+                                        float *inv)
+{
+    const int cc = lane >> 3, tt = lane & 7;
+    uint32_t mb = 0;
+    mb = max(mb, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
+                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
+    mb = max(mb, max(max(__float_as_uint(w.x) & 0x7fffffffu, __float_as_uint(w.y) & 0x7fffffffu),
+                     max(__float_as_uint(w.z) & 0x7fffffffu, __float_as_uint(w.w) & 0x7fffffffu)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    // max|x| < 2^(eM+1): scaling by 2^(14-eM) keeps every term below 2^15.
+    const int s = mb ? 14 - (int(mb >> 23) - 127) : 0;
+    float xs[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
+    if (s >= -126 && s <= 127) {
+        const float f = exp2i(s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] *= f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xs[i] = scale_pow2(xs[i], s);
+    }
+    __half hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        hi[i] = __float2half_rn(xs[i]);
+        lo[i] = __float2half_rn(xs[i] - __half2float(hi[i]));
+    }
+    auto pack = [](__half a, __half b) {
+        return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
+    };
+    // k-step tt: elements (4tt, 4tt+2) in k-slots (2c, 2c+1), (4tt+1, 4tt+3) in (2c+8, 2c+9).
+    bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[2]), pack(hi[1], hi[3]),
+                                           pack(hi[4], hi[6]), pack(hi[5], hi[7]));
+    bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[2]), pack(lo[1], lo[3]),
+                                           pack(lo[4], lo[6]), pack(lo[5], lo[7]));
+    // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
+    float sl = (v.x + v.y) + (v.z + v.w);
+    float sh = (w.x + w.y) + (w.z + w.w);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+    }
+    if (tt == 0) {
+        xsum[2 * cc] = sl;
+        xsum[2 * cc + 1] = sh;
+    }
+    if (lane == 0)
+        *inv = scale_pow2(1.f, -s);
+}
+
+__global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const __grid_constant__ M1Params P)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
+    const int lane = threadIdx.x & 31;
+    const int W = P.W, NS = P.nslot, KS = P.KS, TS = P.TS;
+    const int b1 = int(blockIdx.x) / P.S, sl = int(blockIdx.x) - b1 * P.S;
+    const int sb0 = sl * KS;
+    const int itile = TS * kTileRows;  // rows of one item
+
+    // Shared memory: ring [NS][slot_bytes] | Bx [KS][8][4][2] uint4 | Xs [KS][8]
+    // | inv [KS] | part [KS][cap*TS*16] | items [cap] | flags [cap] | full[NS],
+    // empty[NS]
+    uint8_t *ring = smem;
+    uint4 *Bx = reinterpret_cast<uint4 *>(smem + size_t(NS) * P.slot_bytes);
+    float *Xs = reinterpret_cast<float *>(Bx + size_t(KS) * 64);
+    float *inv = Xs + size_t(KS) * 8;
+    float *part = inv + ((KS + 3) & ~3);
+    const int pcol = P.cap * itile;  // floats per column of partial sums
+    int *items = reinterpret_cast<int *>(part + size_t(KS) * pcol);
+    int *flags = items + P.cap;
+    uint64_t *full = reinterpret_cast<uint64_t *>(
+        (reinterpret_cast<uintptr_t>(flags + P.cap) + 7) & ~uintptr_t(7));
+    uint64_t *empty = full + NS;
+    __shared__ int s_item[kM1MaxSlots];
+    __shared__ int s_abort;
+    __shared__ int s_issued;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], unsigned(32 * W));  // every consumer lane arrives
+        }
+        fence_barrier_init();
+        s_abort = 0;
+        s_issued = 0;
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == W) {
+        // ---------------------------------------------------------- producer
+        const uint64_t pol = policy_evict_first();
+        int k = 0, slot = 0;
+        unsigned par = 0;
+        bool ok = true;
+        // One slot: item `it` (negative: no more work).
+        auto issue = [&](int it) {
+            if (k >= NS && !mbar_wait_polled(&empty[slot], par ^ 1u)) {
+                if (lane == 0) {
+                    atomicOr(P.status, kStatusTimeoutBit);
+                    *(volatile int *)&s_abort = 1;
+                }
+                ok = false;
+                return;
+            }
+            if (lane == 0)
+                s_item[slot] = it;
+            if (it >= 0) {
+                // Lane u < TS copies tile it*TS + u: one box of 16 rows x the
+                // slice's KS super-blocks, landing as units u*KS .. u*KS+KS-1
+                // (rows past a matrix end read as zeros and count in full
+                // towards the transaction bytes).
+                const int tile = it * TS + lane;
+                const bool mine = lane < TS && tile < P.T;
+                const int nvalid = __popc(__ballot_sync(0xffffffffu, mine));
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * KS) * kTileBytes);
+                __syncwarp();
+                if (mine) {
+                    const int m = mat_of_tile(P, tile);
+                    const int lt = tile - (m == 0 ? 0 : P.tile_end[m - 1]);
+                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * KS * kTileBytes,
+                                &P.tmap[m], lt * kTileRows, sb0, &full[slot], pol);
+                }
+            } else if (lane == 0) {
+                mbar_arrive(&full[slot]);  // completes the phase with no bytes
+            }
+            __syncwarp();
+            ++k;
+            if (++slot == NS) {
+                slot = 0;
+                par ^= 1u;
+            }
+        };
+        unsigned *next = P.ctr + sl, *done = P.ctr + P.S + sl;
+        // Fixed items b1*F .. b1*F + nfix-1; then dynamic items from the
+        // counter.  `reserved` (lane 0) counts the items this CTA will compute
+        // -- its fixed ones plus every index fetched -- and never exceeds cap,
+        // so no fetched index is left uncomputed.  Two fetches are kept in
+        // flight so that the atomics' round trips overlap the copies
+        // (INT_MAX: nothing fetched).
+        const int nfix = max(0, min(P.F, P.n_items - b1 * P.F));
+        const int dyn0 = P.G1 * P.F;
+        int reserved = nfix;
+        int n0 = 0x7fffffff, n1 = 0x7fffffff;
+        auto fetch = [&]() {
+            if (reserved >= P.cap)
+                return 0x7fffffff;
+            ++reserved;
+            return dyn0 + int(atomicAdd(next, 1u));
+        };
+        bool waited = false;
+        auto start_dynamic = [&]() {
+            // Counters are shared with earlier launches: touch them only
+            // after those have completed.
+            pdl_wait();
+            waited = true;
+            if (lane == 0) {
+                n0 = fetch();
+                n1 = fetch();
+            }
+        };
+        // The first NS fixed items are fetched before the previous kernel has
+        // finished.
+        for (int f = 0; f < nfix && ok; ++f) {
+            if (f == NS)
+                start_dynamic();
+            issue(b1 * P.F + f);
+        }
+        if (!waited)
+            start_dynamic();
+        while (ok && !*(volatile int *)&s_abort) {
+            const int it = __shfl_sync(0xffffffffu, n0, 0);
+            if (it >= P.n_items)
+                break;  // later fetches of this CTA return larger indices
+            if (lane == 0) {
+                n0 = n1;
+                n1 = fetch();
+            }
+            issue(it);
+        }
+        if (lane == 0 && atomicAdd(done, 1u) == unsigned(P.G1 - 1)) {
+            *next = 0u;  // every CTA of this slice has stopped fetching
+            *done = 0u;
+        }
+        if (ok)
+            issue(-1);
+        if (lane == 0)
+            s_issued = k;
+    } else {
+        // ---------------------------------------------------------- consumers
+        pdl_wait();  // x, y and the workspace belong to earlier kernels until here
+        {
+            // This slice of x -> B entries; super-blocks j = warp, warp + W, ...,
+            // the loads of up to four in flight together.
+            const int cc = lane >> 3, tt = lane & 7;
+            const float *xb = P.x + int64_t(sb0) * 256 + 64 * cc + 4 * tt;
+            for (int j0 = warp; j0 < KS; j0 += 4 * W) {
+                float4 v[4], w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = j0 + i * W;
+                    if (j < KS) {
+                        v[i] = __ldg(reinterpret_cast<const float4 *>(xb + int64_t(j) * 256));
+                        w[i] = __ldg(reinterpret_cast<const float4 *>(xb + int64_t(j) * 256 + 32));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int j = j0 + i * W;
+                    if (j < KS)
+                        prep_sb(v[i], w[i], lane, Bx + size_t(j) * 64, Xs + j * 8, inv + j);
+                }
+            }
+        }
+        named_sync(1, W * 32);
+
+        const int g = lane >> 2, c = lane & 3;
+        const int wsb = warp % KS, wt = warp / KS;
+        const bool act = (g >> 1) == c;
+        const int term = g & 1;
+        const ScaleSel L = scale_sel(c);
+        const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
+        uint4 B[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+            B[t] = act ? Bx[size_t(wsb) * 64 + (t * 4 + c) * 2 + term] : make_uint4(0u, 0u, 0u, 0u);
+        const float2 X0 = make_float2(Xs[wsb * 8 + 2 * c], Xs[wsb * 8 + 2 * c]);
+        const float2 X1 = make_float2(Xs[wsb * 8 + 2 * c + 1], Xs[wsb * 8 + 2 * c + 1]);
+        const float2 iv = make_float2(inv[wsb], inv[wsb]);
+        const int slot_bytes = P.slot_bytes;
+        // This lane's bytes of its unit in slot 0: header of row g (and of
+        // row g+8 at +8*144), its 32-byte nibble chunk at +16+32c.
+        const uint32_t ubase = smem_u32(ring) + uint32_t(warp * kTileBytes + g * 144);
+        // Column wsb of the partial sums; lanes c = 0 and 1 store rows g and
+        // g+8 of tile wt of the item.
+        const uint32_t pbase =
+            smem_u32(part + size_t(wsb) * pcol + wt * kTileRows + g + 8 * (c & 1));
+        const bool writer = c < 2;
+        uint32_t soff = 0;  // byte offset of the current slot
+        unsigned par = 0;
+        int slot = 0, k = 0;
+        for (;; ++k) {
+            if (!mbar_wait_bounded(&full[slot], par)) {
+                if (lane == 0) {
+                    atomicOr(P.status, kStatusTimeoutBit);
+                    *(volatile int *)&s_abort = 1;
+                }
+                break;
+            }
+            const int it = *(volatile int *)&s_item[slot];
+            if (it < 0)
+                break;
+            const uint32_t a0 = ubase + soff;
+            const uint4 h0 = lds128(a0);
+            const uint4 h1 = lds128(a0 + 8 * 144);
+            const uint4 qa0 = lds128(a0 + 16 + 32 * c);
+            const uint4 qa1 = lds128(a0 + 32 + 32 * c);
+            const uint4 qb0 = lds128(a0 + 8 * 144 + 16 + 32 * c);
+            const uint4 qb1 = lds128(a0 + 8 * 144 + 32 + 32 * c);
+            mbar_arrive(&empty[slot]);  // the unit is in registers: release the slot
+            soff += uint32_t(slot_bytes);
+            if (++slot == NS) {
+                slot = 0;
+                soff = 0;
+                par ^= 1u;
+            }
+            if (warp == 0 && lane == 0)
+                items[k] = it;
+            if (it * TS + wt >= P.T)
+                continue;  // past the last tile (a ragged final item)
+            const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+            const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+            float dlo[4], dhi[4];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
+                if (t == 0) {
+                    mma16816_zero(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
+                    mma16816_zero(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
+                } else {
+                    mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
+                    mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
+                }
+            }
+            const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
+                                                                  make_float2(dlo[1], dlo[3])),
+                                          __fadd2_rn(make_float2(dhi[0], dhi[2]),
+                                                     make_float2(dhi[1], dhi[3])),
+                                          X0, X1, iv);
+            // Sum the four lanes of the row pair: lanes c = 0 / 1 end with rows
+            // g / g+8 (the same fixed order for every unit).
+            const bool odd = c & 1;
+            float keep = odd ? tot.y : tot.x;
+            keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
+            keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+            sts_f32_if(pbase + uint32_t(k * itile * 4), keep, writer);
+        }
+        named_sync(1, W * 32);
+
+        // ---- output: add the columns in column order, then (S > 1) the slices
+        const int nrow = k * itile;
+        if (P.S == 1) {
+            for (int i = threadIdx.x; i < nrow; i += W * 32) {
+                const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
+                if (tile >= P.T)
+                    continue;
+                float s = 0.f;
+                for (int w = 0; w < KS; ++w)
+                    s += part[size_t(w) * pcol + i];
+                int m, row;
+                if (locate_row(P, tile, i % kTileRows, m, row))
+                    P.y[m][row] = s;
+            }
+        } else {
+            const size_t sst = size_t(P.T) * kTileRows;
+            unsigned *tick = P.ctr + 2 * P.S;
+            for (int i = threadIdx.x; i < nrow; i += W * 32) {
+                const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
+                if (tile >= P.T)
+                    continue;
+                float s = 0.f;
+                for (int w = 0; w < KS; ++w)
+                    s += part[size_t(w) * pcol + i];
+                __stcg(P.ws + size_t(sl) * sst + size_t(tile) * kTileRows + i % kTileRows, s);
+            }
+            __threadfence();
+            named_sync(1, W * 32);
+            for (int i = threadIdx.x; i < k; i += W * 32)
+                flags[i] = atomicAdd(&tick[items[i]], 1u) == unsigned(P.S - 1) ? 1 : 0;
+            named_sync(1, W * 32);
+            __threadfence();
+            for (int i = threadIdx.x; i < nrow; i += W * 32) {
+                if (!flags[i / itile])
+                    continue;
+                const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
+                if (tile >= P.T)
+                    continue;
+                float s = 0.f;
+                for (int q = 0; q < P.S; ++q)
+                    s += __ldcg(P.ws + size_t(q) * sst + size_t(tile) * kTileRows + i % kTileRows);
+                int m, row;
+                if (locate_row(P, tile, i % kTileRows, m, row))
+                    P.y[m][row] = s;
+            }
+            named_sync(1, W * 32);
+            for (int i = threadIdx.x; i < k; i += W * 32)
+                if (flags[i])
+                    tick[items[i]] = 0u;  // every slice of the item has been added
+        }
+    }
+
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0) {
+        // Let copies still in flight land before shared memory is released:
+        // only the last NS issued slots can be outstanding.
+        for (int i = s_issued - NS < 0 ? 0 : s_issued - NS; i < s_issued; ++i)
+            mbar_wait_bounded(&full[i % NS], unsigned(i / NS) & 1u, 100000000ll);
+    }
+}
+
+int env_m1_slices()
+{
+    const char *e = getenv("QMM_M1_S");
+    return e ? atoi(e) : 0;
+}
+
+} // namespace
+
+size_t m1_smem(int KS, int TS, int cap, int nslot)
+{
+    const int W = KS * TS;
+    return size_t(nslot) * (size_t(W) * kTileBytes + 16) + size_t(KS) * 1024 + size_t(KS) * 32 +
+           size_t((KS + 3) & ~3) * 4 + size_t(KS) * cap * TS * kTileRows * 4 + size_t(cap) * 8 + 8;
+}
+
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S)
+{
+    M1Plan p;
+    const int forced = force_S > 0 ? force_S : env_m1_slices();
+    // K slices: a divisor of NB with at most 16 super-blocks per slice (one
+    // consumer warp per super-block); the fewest that leave each CTA about
+    // six tiles, so that laying out x is paid over enough weights.
+    int S = 0;
+    if (forced > 0 && NB % forced == 0 && NB / forced <= kM1MaxWarps && forced <= sm_count)
+        S = forced;
+    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand) {
+        if (NB % cand || NB / cand > kM1MaxWarps)
+            continue;
+        if (T * cand >= 6 * int64_t(sm_count) || NB / cand <= 4)
+            S = int(cand);
+    }
+    if (S == 0) {  // otherwise the smallest slice count that fits
+        for (int64_t cand = 1; cand <= NB && cand <= sm_count; ++cand)
+            if (NB % cand == 0 && NB / cand <= kM1MaxWarps) {
+                S = int(cand);
+                break;
+            }
+    }
+    if (S == 0)
+        return p;  // nslot == 0: not supported
+    p.S = S;
+    p.KS = int(NB / S);
+    p.TS = 1;
+    while (p.KS * p.TS * 2 <= kM1MaxWarps && p.TS < 8)
+        p.TS *= 2;
+    p.W = p.KS * p.TS;
+    p.n_items = int((T + p.TS - 1) / p.TS);
+    // One CTA per SM and slice; for very tall matrices more (several waves),
+    // so that a CTA's share stays within kM1MaxShare items.
+    p.G1 = sm_count / S;
+    if ((p.n_items + p.G1 - 1) / p.G1 > kM1MaxShare)
+        p.G1 = (p.n_items + kM1MaxShare - 1) / kM1MaxShare;
+    if (p.G1 > p.n_items)
+        p.G1 = p.n_items;
+    const int avg = (p.n_items + p.G1 - 1) / p.G1;
+    // Ring slots: as many as shared memory holds (at most 16) next to room
+    // for twice a CTA's average share of items; if fewer than three slots
+    // fit, the item room shrinks (never below one item over the average).
+    p.cap = 2 * avg + 2;
+    auto slots = [&](int cap) {
+        int ns = 0;
+        while (ns < 16 && m1_smem(p.KS, p.TS, cap, ns + 1) <= kM1SmemBudgetWhole)
+            ++ns;
+        return ns;
+    };
+    int ns = slots(p.cap);
+    while (ns < 3 && p.cap > avg + 1)
+        ns = slots(--p.cap);
+    p.nslot = ns;
+    // Fixed items per CTA: three quarters of the average share (all of it
+    // when the share fits the ring), the rest from the counter.
+    p.F = avg <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
+    if (p.F < 1)
+        p.F = 1;
+    p.slot_bytes = p.W * kTileBytes;
+    p.smem = m1_smem(p.KS, p.TS, p.cap, ns);
+    p.ws_floats = S > 1 ? size_t(S) * size_t(T) * kTileRows : 0;
+    p.tickets = size_t(2 * S) + (S > 1 ? size_t(p.n_items) : 0);
+    return p;
+}
+
+cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
+{
+    M1Params P;
+    memset(&P, 0, sizeof(P));
+    int tiles = 0;
+    for (int i = 0; i < a.nmat; ++i) {
+        P.tmap[i] = *reinterpret_cast<const CUtensorMap *>(a.tmap[i]);
+        tiles += int((a.rows[i] + kTileRows - 1) / kTileRows);
+        P.tile_end[i] = tiles;
+        P.rows[i] = int(a.rows[i]);
+        P.y[i] = a.y[i];
+    }
+    for (int i = a.nmat; i < kMaxGroup; ++i)
+        P.tile_end[i] = tiles;
+    P.x = a.x;
+    P.ws = a.ws;
+    P.ctr = a.tickets;
+    P.status = a.status;
+    P.T = tiles;
+    P.nmat = a.nmat;
+    P.S = p.S;
+    P.KS = p.KS;
+    P.TS = p.TS;
+    P.W = p.W;
+    P.G1 = p.G1;
+    P.n_items = p.n_items;
+    P.F = p.F;
+    P.cap = p.cap;
+    P.nslot = p.nslot;
+    P.slot_bytes = p.slot_bytes;
+    cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(p.smem));
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.G1 * p.S));
+    cfg.blockDim = dim3(unsigned((p.W + 1) * 32));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return counted(cudaLaunchKernelEx(&cfg, gemv_m1_kernel, P));
+}
+
+} // namespace qmm

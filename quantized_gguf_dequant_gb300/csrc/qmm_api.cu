@@ -160,6 +160,57 @@ qmm_status do_gemv_tcb(qmm_t h, const float *X, int64_t ldx, int M, float *Y, in
     return QMM_OK;
 }
 
+// The one-row Q4_K decode kernel (gemv_m1.cu) for n matrices sharing x.
+// QMM_ERR_UNSUPPORTED (nothing launched) when no plan fits its shared memory
+// or the handle's workspace.  QMM_M1_S fixes the number of K slices.
+qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
+                      const char *fn)
+{
+    const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    qmm::M1Args a;
+    memset(&a, 0, sizeof(a));
+    int64_t T = 0;
+    for (int i = 0; i < n; ++i) {
+        const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
+        if (!mi.has_tmap)
+            return QMM_ERR_UNSUPPORTED;
+        a.rows[i] = mi.N;
+        a.y[i] = ys[i];
+        T += (mi.N + 15) / 16;
+    }
+    if (T * 16 > (int64_t(1) << 30))
+        return QMM_ERR_UNSUPPORTED;
+    const int64_t NB = m0.K / 256;
+    qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0);
+    // Fewer K slices when the handle's workspace or tickets are too small.
+    for (int S = p.S; S >= 1 && (p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets); --S)
+        if (NB % S == 0)
+            p = qmm::plan_m1(T, NB, m0.sm_count, S);
+    if (p.nslot < 2 || p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets)
+        return QMM_ERR_UNSUPPORTED;
+    // Each matrix's column view with boxes of this plan's slice width (kept
+    // in the handle; re-encoded when a plan asks for another width).
+    for (int i = 0; i < n; ++i) {
+        Matrix &mi = *reinterpret_cast<Matrix *>(hs[i]);
+        if (mi.tmap3_ks != p.KS) {
+            if (qmm::make_q4k_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.KS) != 0)
+                return QMM_ERR_UNSUPPORTED;
+            mi.tmap3_ks = p.KS;
+        }
+        a.tmap[i] = mi.tmap3;
+    }
+    a.nmat = n;
+    a.x = x;
+    a.ws = m0.ws;
+    a.tickets = m0.tickets;
+    a.status = m0.status;
+    cudaError_t e = qmm::launch_gemv_m1(a, p, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+    return QMM_OK;
+}
+
 qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
                    const char *fn)
 {
@@ -173,6 +224,12 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
         }
         reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
         return QMM_OK;
+    }
+    const char *qpath = getenv("QMM_Q4K_PATH");
+    if (m0.fmt == QMM_Q4_K && !(qpath && (strcmp(qpath, "simt") == 0 || strcmp(qpath, "tc") == 0))) {
+        qmm_status st = do_gemv_m1(hs, n, x, ys, s, fn);
+        if (st != QMM_ERR_UNSUPPORTED)
+            return st;
     }
     if (m0.fmt == QMM_Q4_K && tc_fits(m0, 1))
         return do_gemv_tc(hs, n, x, m0.K, 1, ys, 0, s, fn);
@@ -405,7 +462,9 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
         return cuda_fail(e, "qmm_create");
     }
     m->ws_floats = size_t(8) * size_t(N) + 1024;
-    m->n_tickets = size_t(m->sm_count) * 4;
+    // Row-group tickets of the split-K paths, and the item counters and
+    // tickets of the one-row decode kernel (one per 16-row tile at most).
+    m->n_tickets = size_t(m->sm_count) * 4 + size_t((N + 15) / 16) + 64;
     if (fmt == QMM_Q4_K) {
         if (qmm::make_q4k_tensor_map(m->tmap, w_dev, N, m->row_bytes) != 0) {
             delete m;

@@ -155,8 +155,8 @@ __device__ __forceinline__ float byte_magic(uint32_t v, int k)
 
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t h)
 {
-    __half2 v = *reinterpret_cast<const __half2 *>(&h);
-    return __half22float2(v);
+    return make_float2(__half2float(__ushort_as_half((unsigned short)(h & 0xffffu))),
+                       __half2float(__ushort_as_half((unsigned short)(h >> 16))));
 }
 
 __device__ __forceinline__ float warp_sum(float v, int width)

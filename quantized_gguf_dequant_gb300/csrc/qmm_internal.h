@@ -32,6 +32,10 @@ struct Matrix {
     // Q4_K tensor-core paths: 2-D tensor map over the rows (a CUtensorMap)
     alignas(64) unsigned char tmap[128];
     bool has_tmap = false;
+    // one-row decode kernel: the 3-D column view with boxes of tmap3_ks
+    // super-blocks (0: not encoded yet)
+    alignas(64) unsigned char tmap3[128];
+    int tmap3_ks = 0;
     // prefill GEMM: tensor maps over the weight bytes (u8) with boxes of the
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
@@ -142,6 +146,42 @@ size_t gemv_tc_smem(int64_t K, int M, int nslot, int nw, int res_tiles = 0);
 cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s);
 int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 
+// --------------------------------------------------------------- one-row Q4_K decode GEMV
+// gemv_m1.cu: a producer warp streams 16-row units into a shared-memory ring,
+// one consumer warp per super-block of a K slice runs the tensor-core unit;
+// work items (tile groups) are handed out first statically, then from a
+// counter per slice.
+constexpr int kM1MaxWarps = 16;
+constexpr size_t kM1SmemBudgetWhole = 226 * 1024;
+struct M1Plan {
+    int S = 0, KS = 0;           // K slices, super-blocks per slice
+    int TS = 0, W = 0;           // tiles per item, consumer warps (KS * TS)
+    int G1 = 0;                  // CTAs per slice (grid = G1 * S)
+    int n_items = 0;             // items per slice
+    int F = 0;                   // fixed items per CTA (fetched before the PDL wait)
+    int cap = 0;                 // items a CTA may take
+    int nslot = 0, slot_bytes = 0;
+    size_t smem = 0;
+    size_t ws_floats = 0;        // K-slice partial sums (S > 1)
+    size_t tickets = 0;          // counters: 2 per slice, plus one per item when S > 1
+};
+struct M1Args {
+    const void *tmap[kMaxGroup];  // Matrix::tmap3 of each matrix (boxes of KS super-blocks)
+    int64_t rows[kMaxGroup];
+    float *y[kMaxGroup];
+    int nmat;
+    const float *x;
+    float *ws;
+    unsigned *tickets;
+    unsigned *status;
+};
+// T: 16-row tiles over all matrices; NB: super-blocks per row; force_S > 0
+// fixes the number of K slices (it must divide NB, with NB / S <= 16).
+// nslot == 0: no plan fits.
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S);
+size_t m1_smem(int KS, int TS, int cap, int nslot);
+cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s);
+
 // --------------------------------------------------------------- batched tensor-core Q4_K GEMV
 // Up to 16 activation rows in one pass; CTA (r, s) of an R x S grid owns a
 // range of row tiles and a slice of K (see gemv_batched.cu).
@@ -171,6 +211,9 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s);
 // CUtensorMapSwizzle); 0 on success.
 int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uint64_t dim1,
                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle);
+// The 3-D column view of a Q4_K matrix (tmap.cu) with boxes of one 16-row
+// tile x ks super-blocks; 0 on success.
+int make_q4k_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks);
 
 // --------------------------------------------------------------- prefill GEMM
 constexpr int kGemmMaxGroup = 4;

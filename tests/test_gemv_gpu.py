@@ -204,6 +204,45 @@ def test_gemv_q4k_fp32_kernel(N, K, monkeypatch):
     m.close()
 
 
+@pytest.mark.parametrize("S", ["1", "2", "4", "7", "8", "16"])
+def test_gemv_m1_forced_k_slices(S, monkeypatch):
+    """The one-row decode kernel with every K-slice count that divides the
+    shape's super-blocks (others fall back to the default plan): ragged row
+    tiles, slot groups of one to eight tiles, row segments of one to eight
+    super-blocks, slices added by the last CTA; twice, so the row-group
+    tickets must have been reset."""
+    monkeypatch.setenv("QMM_M1_S", S)
+    for N, K in ((37, 2048), (300, 4096), (1000, 1024), (77, 14336), (1, 256), (40, 768),
+                 (4096, 3584)):
+        for rep in range(2):
+            m, *_ = _check_gemv(q.Q4_K, N, K, seed=int(S) * 1000 + N + rep)
+            m.close()
+
+
+@pytest.mark.parametrize("S", ["1", "4"])
+def test_gemv_m1_ragged_group(S, monkeypatch):
+    """A group of matrices with ragged row counts sharing x: slots that
+    straddle two matrices, rows past a matrix end never written."""
+    monkeypatch.setenv("QMM_M1_S", S)
+    K = 2048
+    shapes = [17, 1, 250, 33]
+    mats, ws = [], []
+    for i, N in enumerate(shapes):
+        w, m = _matrix(q.Q4_K, N, K, seed=70 + i)
+        mats.append(m)
+        ws.append(w)
+    x = synth.activations(1, K, 74)[0]
+    bufs = [torch.full((N + 8,), 777.0, dtype=torch.float32, device="cuda") for N in shapes]
+    q.gemv_group([m.h for m in mats], to_dev(x), [b[4:4 + N] for b, N in zip(bufs, shapes)])
+    for w, b, N in zip(ws, bufs, shapes):
+        out = b.cpu().numpy()
+        assert np.all(out[:4] == 777.0) and np.all(out[4 + N:] == 777.0)
+        y_ref, c = oracle.gemv(q.Q4_K, w, N, K, x)
+        assert_close_to_oracle(out[4:4 + N], y_ref, c, TOL_FP32, f"ragged group N={N}")
+    for m in mats:
+        m.close()
+
+
 @pytest.mark.parametrize("nslot,warps", [("2", "8"), ("3", "16"), ("6", "8"), ("4", "12")])
 def test_gemv_q4k_tensor_core_shapes(nslot, warps, monkeypatch):
     """The tensor-core kernel with other ring depths / CTA sizes, and on a
