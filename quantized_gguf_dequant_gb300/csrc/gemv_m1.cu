@@ -20,27 +20,31 @@
 // with X_j the fp32 sum of sub-block j's activations.
 //
 // Work decomposition.  The 16-row tiles of all matrices of a group (they
-// share x) are concatenated (T tiles); K is cut into S slices of KS <= 16
-// super-blocks.  A work item is TS consecutive tiles x one slice: KS*TS
-// units of 16 rows x 256 weights (2304 bytes each), exactly one ring slot.
-// CTA b works on slice b % S.  Items are handed out in two phases: each CTA's
+// share x) are concatenated (T tiles); K may be cut into S slices of KS
+// super-blocks (only when x's layout for the whole K would crowd the ring
+// out of shared memory).  A work item is TS consecutive tiles x one slice,
+// taken in NP passes of WS super-blocks; one pass is WS*TS units of 16 rows x
+// 256 weights (2304 bytes each), exactly one ring slot.  CTA b works on slice
+// b % S.  Items are handed out in two phases: each CTA's
 // first F items are fixed (so that its producer can fetch them before the
 // previous kernel in the stream has finished), the rest come from a counter
 // per slice, so CTAs on faster SMs take more.  Each item is computed whole by
 // one CTA, in a fixed order: results do not depend on the schedule.
 //
-// Inside a CTA one producer warp and W = KS*TS consumer warps:
+// Inside a CTA one producer warp and W = WS*TS consumer warps:
 //  - the producer fills a ring of slots with one TMA box per tile, through
 //    a 3-D view of the matrix (144-byte super-block, row, super-block index)
-//    that lands the tile as KS units of 16 rows x 144 bytes -- rows 144 bytes
+//    that lands the tile as WS units of 16 rows x 144 bytes -- rows 144 bytes
 //    apart, so the lanes reading the same column of neighbouring rows hit
 //    different banks -- completing on the slot's mbarrier.  It writes the
-//    slot's item index first, and a negative index once the work has run out;
-//  - consumer warp w always takes unit w = (tile w / KS, super-block w % KS)
-//    of a slot, so its B fragments stay in registers for the whole launch.  It
-//    copies its unit to registers, releases the slot, runs 16 MMAs and the
-//    scaling, and stores the two rows it covers into the column of partial
-//    sums of its super-block;
+//    slot's item index and pass first, and a negative index once the work has
+//    run out;
+//  - consumer warp w always takes unit w = (tile w / WS, super-block w % WS
+//    of the pass) of a slot; with one pass its B fragments stay in registers
+//    for the whole launch, with several it reloads them from shared memory
+//    for each pass.  It copies its unit to registers, releases the slot, runs
+//    16 MMAs and the scaling, and adds the two rows it covers into the column
+//    of partial sums of its super-block position (passes in order);
 //  - at the end the columns are added in column order and, with S > 1, the
 //    slices in slice order by the CTA that finished an item's last slice (a
 //    ticket per item): no float atomics, bitwise repeatable.
@@ -67,7 +71,7 @@ constexpr int kM1MaxSlots = 16;
 constexpr int kM1MaxShare = 16;  // average items per CTA at most
 
 struct M1Params {
-    CUtensorMap tmap[kMaxGroup];  // 3-D column view of each matrix, box (18, 16, KS)
+    CUtensorMap tmap[kMaxGroup];  // 3-D column view of each matrix, box (18, 16, WS)
     int tile_end[kMaxGroup];      // cumulative 16-row tile counts
     int rows[kMaxGroup];
     float *y[kMaxGroup];
@@ -77,7 +81,8 @@ struct M1Params {
     unsigned *status;
     int T, nmat;
     int S, KS;                    // K slices, super-blocks per slice
-    int TS, W;                    // tiles per item, consumer warps (KS * TS)
+    int WS, NP;                   // super-blocks per pass, passes (KS = WS * NP)
+    int TS, W;                    // tiles per item, consumer warps (WS * TS)
     int G1;                       // CTAs per slice
     int n_items;                  // items per slice (ceil(T / TS))
     int F;                        // fixed items per CTA
@@ -110,7 +115,7 @@ __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, i
 }
 
 // One box of the 3-D column view (tmap.cu, make_q4k_column_map): rows
-// [row, row+16) x super-blocks [sb, sb+KS) -> KS units of 16 x 144 bytes.
+// [row, row+16) x super-blocks [sb, sb+WS) -> WS units of 16 x 144 bytes.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int row, int sb,
                                             uint64_t *bar, uint64_t policy)
 {
@@ -131,7 +136,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t a)
     return v;
 }
 
-// Shared-memory float store executed only where pred holds.
+// Shared-memory float load / store executed only where pred holds (the
+// load gives 0 elsewhere).
+__device__ __forceinline__ float lds_f32_if(uint32_t a, bool pred)
+{
+    float v = 0.f;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p ld.shared.f32 %0, [%1];\n\t}"
+                 : "+f"(v)
+                 : "r"(a), "r"(uint32_t(pred))
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void sts_f32_if(uint32_t a, float v, bool pred)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%0], %1;\n\t}" ::"r"(a),
@@ -276,13 +292,13 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
     const int lane = threadIdx.x & 31;
-    const int W = P.W, NS = P.nslot, KS = P.KS, TS = P.TS;
+    const int W = P.W, NS = P.nslot, KS = P.KS, TS = P.TS, WS = P.WS, NP = P.NP;
     const int b1 = int(blockIdx.x) / P.S, sl = int(blockIdx.x) - b1 * P.S;
     const int sb0 = sl * KS;
     const int itile = TS * kTileRows;  // rows of one item
 
     // Shared memory: ring [NS][slot_bytes] | Bx [KS][8][4][2] uint4 | Xs [KS][8]
-    // | inv [KS] | part [KS][cap*TS*16] | items [cap] | flags [cap] | full[NS],
+    // | inv [KS] | part [WS][cap*TS*16] | items [cap] | flags [cap] | full[NS],
     // empty[NS]
     uint8_t *ring = smem;
     uint4 *Bx = reinterpret_cast<uint4 *>(smem + size_t(NS) * P.slot_bytes);
@@ -290,12 +306,13 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     float *inv = Xs + size_t(KS) * 8;
     float *part = inv + ((KS + 3) & ~3);
     const int pcol = P.cap * itile;  // floats per column of partial sums
-    int *items = reinterpret_cast<int *>(part + size_t(KS) * pcol);
+    int *items = reinterpret_cast<int *>(part + size_t(WS) * pcol);
     int *flags = items + P.cap;
     uint64_t *full = reinterpret_cast<uint64_t *>(
         (reinterpret_cast<uintptr_t>(flags + P.cap) + 7) & ~uintptr_t(7));
     uint64_t *empty = full + NS;
     __shared__ int s_item[kM1MaxSlots];
+    __shared__ int s_pass[kM1MaxSlots];
     __shared__ int s_abort;
     __shared__ int s_issued;
 
@@ -317,8 +334,8 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         int k = 0, slot = 0;
         unsigned par = 0;
         bool ok = true;
-        // One slot: item `it` (negative: no more work).
-        auto issue = [&](int it) {
+        // One slot: pass p of item `it` (negative: no more work).
+        auto issue = [&](int it, int p) {
             if (k >= NS && !mbar_wait_polled(&empty[slot], par ^ 1u)) {
                 if (lane == 0) {
                     atomicOr(P.status, kStatusTimeoutBit);
@@ -327,24 +344,26 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 ok = false;
                 return;
             }
-            if (lane == 0)
+            if (lane == 0) {
                 s_item[slot] = it;
+                s_pass[slot] = p;
+            }
             if (it >= 0) {
                 // Lane u < TS copies tile it*TS + u: one box of 16 rows x the
-                // slice's KS super-blocks, landing as units u*KS .. u*KS+KS-1
+                // pass's WS super-blocks, landing as units u*WS .. u*WS+WS-1
                 // (rows past a matrix end read as zeros and count in full
                 // towards the transaction bytes).
                 const int tile = it * TS + lane;
                 const bool mine = lane < TS && tile < P.T;
                 const int nvalid = __popc(__ballot_sync(0xffffffffu, mine));
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * KS) * kTileBytes);
+                    mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * WS) * kTileBytes);
                 __syncwarp();
                 if (mine) {
                     const int m = mat_of_tile(P, tile);
                     const int lt = tile - (m == 0 ? 0 : P.tile_end[m - 1]);
-                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * KS * kTileBytes,
-                                &P.tmap[m], lt * kTileRows, sb0, &full[slot], pol);
+                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * kTileBytes,
+                                &P.tmap[m], lt * kTileRows, sb0 + p * WS, &full[slot], pol);
                 }
             } else if (lane == 0) {
                 mbar_arrive(&full[slot]);  // completes the phase with no bytes
@@ -384,13 +403,14 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 n1 = fetch();
             }
         };
-        // The first NS fixed items are fetched before the previous kernel has
-        // finished.
-        for (int f = 0; f < nfix && ok; ++f) {
-            if (f == NS)
-                start_dynamic();
-            issue(b1 * P.F + f);
-        }
+        // The fixed items' first NS slots are fetched before the previous
+        // kernel has finished.
+        for (int f = 0; f < nfix && ok; ++f)
+            for (int p = 0; p < NP && ok; ++p) {
+                if (k == NS && !waited)
+                    start_dynamic();
+                issue(b1 * P.F + f, p);
+            }
         if (!waited)
             start_dynamic();
         while (ok && !*(volatile int *)&s_abort) {
@@ -401,14 +421,15 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 n0 = n1;
                 n1 = fetch();
             }
-            issue(it);
+            for (int p = 0; p < NP && ok; ++p)
+                issue(it, p);
         }
         if (lane == 0 && atomicAdd(done, 1u) == unsigned(P.G1 - 1)) {
             *next = 0u;  // every CTA of this slice has stopped fetching
             *done = 0u;
         }
         if (ok)
-            issue(-1);
+            issue(-1, 0);
         if (lane == 0)
             s_issued = k;
     } else {
@@ -440,31 +461,38 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         named_sync(1, W * 32);
 
         const int g = lane >> 2, c = lane & 3;
-        const int wsb = warp % KS, wt = warp / KS;
+        const int wsb = warp % WS, wt = warp / WS;
         const bool act = (g >> 1) == c;
         const int term = g & 1;
         const ScaleSel L = scale_sel(c);
         const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
+        // B fragments, sub-block sums and inverse scale of this warp's
+        // super-block of pass p (reloaded per pass when there are several).
         uint4 B[8];
+        float2 X0, X1, iv;
+        auto load_b = [&](int p) {
+            const int j = p * WS + wsb;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-            B[t] = act ? Bx[size_t(wsb) * 64 + (t * 4 + c) * 2 + term] : make_uint4(0u, 0u, 0u, 0u);
-        const float2 X0 = make_float2(Xs[wsb * 8 + 2 * c], Xs[wsb * 8 + 2 * c]);
-        const float2 X1 = make_float2(Xs[wsb * 8 + 2 * c + 1], Xs[wsb * 8 + 2 * c + 1]);
-        const float2 iv = make_float2(inv[wsb], inv[wsb]);
+            for (int t = 0; t < 8; ++t)
+                B[t] = act ? Bx[size_t(j) * 64 + (t * 4 + c) * 2 + term] : make_uint4(0u, 0u, 0u, 0u);
+            X0 = make_float2(Xs[j * 8 + 2 * c], Xs[j * 8 + 2 * c]);
+            X1 = make_float2(Xs[j * 8 + 2 * c + 1], Xs[j * 8 + 2 * c + 1]);
+            iv = make_float2(inv[j], inv[j]);
+        };
+        load_b(0);
         const int slot_bytes = P.slot_bytes;
         // This lane's bytes of its unit in slot 0: header of row g (and of
         // row g+8 at +8*144), its 32-byte nibble chunk at +16+32c.
         const uint32_t ubase = smem_u32(ring) + uint32_t(warp * kTileBytes + g * 144);
-        // Column wsb of the partial sums; lanes c = 0 and 1 store rows g and
+        // Column wsb of the partial sums; lanes c = 0 and 1 own rows g and
         // g+8 of tile wt of the item.
         const uint32_t pbase =
             smem_u32(part + size_t(wsb) * pcol + wt * kTileRows + g + 8 * (c & 1));
         const bool writer = c < 2;
         uint32_t soff = 0;  // byte offset of the current slot
         unsigned par = 0;
-        int slot = 0, k = 0;
-        for (;; ++k) {
+        int slot = 0, k = 0;  // k: items completed by this CTA
+        for (;;) {
             if (!mbar_wait_bounded(&full[slot], par)) {
                 if (lane == 0) {
                     atomicOr(P.status, kStatusTimeoutBit);
@@ -475,6 +503,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             const int it = *(volatile int *)&s_item[slot];
             if (it < 0)
                 break;
+            const int p = *(volatile int *)&s_pass[slot];
             const uint32_t a0 = ubase + soff;
             const uint4 h0 = lds128(a0);
             const uint4 h1 = lds128(a0 + 8 * 144);
@@ -489,8 +518,13 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 soff = 0;
                 par ^= 1u;
             }
-            if (warp == 0 && lane == 0)
-                items[k] = it;
+            if (NP > 1)
+                load_b(p);
+            const int kc = k;
+            if (p == NP - 1)
+                ++k;
+            if (p == 0 && warp == 0 && lane == 0)
+                items[kc] = it;
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
             const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
@@ -518,7 +552,10 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             float keep = odd ? tot.y : tot.x;
             keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
             keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-            sts_f32_if(pbase + uint32_t(k * itile * 4), keep, writer);
+            const uint32_t pa = pbase + uint32_t(kc * itile * 4);
+            if (p > 0)
+                keep = lds_f32_if(pa, writer) + keep;  // passes added in order
+            sts_f32_if(pa, keep, writer);
         }
         named_sync(1, W * 32);
 
@@ -530,7 +567,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 if (tile >= P.T)
                     continue;
                 float s = 0.f;
-                for (int w = 0; w < KS; ++w)
+                for (int w = 0; w < WS; ++w)
                     s += part[size_t(w) * pcol + i];
                 int m, row;
                 if (locate_row(P, tile, i % kTileRows, m, row))
@@ -544,7 +581,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 if (tile >= P.T)
                     continue;
                 float s = 0.f;
-                for (int w = 0; w < KS; ++w)
+                for (int w = 0; w < WS; ++w)
                     s += part[size_t(w) * pcol + i];
                 __stcg(P.ws + size_t(sl) * sst + size_t(tile) * kTileRows + i % kTileRows, s);
             }
@@ -591,48 +628,73 @@ int env_m1_slices()
 
 } // namespace
 
-size_t m1_smem(int KS, int TS, int cap, int nslot)
+size_t m1_smem(int KS, int WS, int TS, int cap, int nslot)
 {
-    const int W = KS * TS;
+    const int W = WS * TS;
     return size_t(nslot) * (size_t(W) * kTileBytes + 16) + size_t(KS) * 1024 + size_t(KS) * 32 +
-           size_t((KS + 3) & ~3) * 4 + size_t(KS) * cap * TS * kTileRows * 4 + size_t(cap) * 8 + 8;
+           size_t((KS + 3) & ~3) * 4 + size_t(WS) * cap * TS * kTileRows * 4 + size_t(cap) * 8 + 8;
 }
 
-M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S)
+int env_m1_warps()
+{
+    const char *e = getenv("QMM_M1_WARPS");
+    return (e && atoi(e) == 8) ? 8 : kM1MaxWarps;
+}
+
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
 {
     M1Plan p;
+    if (maxw <= 0)
+        maxw = env_m1_warps();
+    maxw = maxw <= 8 ? 8 : kM1MaxWarps;
+    // 8 consumer warps: half an SM, so that the next launch in the stream
+    // can be resident beside this one; 16: the whole SM.
+    const size_t budget = maxw <= 8 ? kM1SmemBudgetHalf : kM1SmemBudgetWhole;
+    // K slices: the fewest (dividing NB) with at most 16 super-blocks each --
+    // one pass, x laid out per CTA for 16 super-blocks at most: laying out a
+    // long x in every CTA costs more than adding slices -- else the fewest
+    // whose layout of x leaves two thirds of shared memory to the ring.
+    // QMM_M1_S (or force_S) fixes S.
     const int forced = force_S > 0 ? force_S : env_m1_slices();
-    // K slices: a divisor of NB with at most 16 super-blocks per slice (one
-    // consumer warp per super-block); the fewest that leave each CTA about
-    // six tiles, so that laying out x is paid over enough weights.
     int S = 0;
-    if (forced > 0 && NB % forced == 0 && NB / forced <= kM1MaxWarps && forced <= sm_count)
+    if (forced > 0 && NB % forced == 0 && forced <= sm_count)
         S = forced;
-    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand) {
-        if (NB % cand || NB / cand > kM1MaxWarps)
-            continue;
-        if (T * cand >= 6 * int64_t(sm_count) || NB / cand <= 4)
+    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand)
+        if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3 && NB / cand <= 16)
             S = int(cand);
-    }
-    if (S == 0) {  // otherwise the smallest slice count that fits
-        for (int64_t cand = 1; cand <= NB && cand <= sm_count; ++cand)
-            if (NB % cand == 0 && NB / cand <= kM1MaxWarps) {
-                S = int(cand);
-                break;
-            }
-    }
+    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand)
+        if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3)
+            S = int(cand);
     if (S == 0)
         return p;  // nslot == 0: not supported
+    p.maxw = maxw;
     p.S = S;
     p.KS = int(NB / S);
-    p.TS = 1;
-    while (p.KS * p.TS * 2 <= kM1MaxWarps && p.TS < 8)
-        p.TS *= 2;
-    p.W = p.KS * p.TS;
+    // Pass width WS (a divisor of KS, at most maxw) and tiles per item TS: the
+    // most consumer warps that still leave every SM an item, then the widest
+    // pass (fewest passes).
+    double best = -1.0;
+    const int per_slice = sm_count / S >= 1 ? sm_count / S : 1;
+    for (int ws = (p.KS < maxw ? p.KS : maxw); ws >= 1; --ws) {
+        if (p.KS % ws)
+            continue;
+        for (int ts = 1; ts <= 8 && ws * ts <= maxw; ts *= 2) {
+            const int64_t items = (T + ts - 1) / ts;
+            const double use = items >= per_slice ? 1.0 : double(items) / per_slice;
+            const double score = ws * ts * use;
+            if (score > best + 1e-9) {
+                best = score;
+                p.WS = ws;
+                p.TS = ts;
+            }
+        }
+    }
+    p.NP = p.KS / p.WS;
+    p.W = p.WS * p.TS;
     p.n_items = int((T + p.TS - 1) / p.TS);
     // One CTA per SM and slice; for very tall matrices more (several waves),
     // so that a CTA's share stays within kM1MaxShare items.
-    p.G1 = sm_count / S;
+    p.G1 = per_slice;
     if ((p.n_items + p.G1 - 1) / p.G1 > kM1MaxShare)
         p.G1 = (p.n_items + kM1MaxShare - 1) / kM1MaxShare;
     if (p.G1 > p.n_items)
@@ -644,21 +706,23 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S)
     p.cap = 2 * avg + 2;
     auto slots = [&](int cap) {
         int ns = 0;
-        while (ns < 16 && m1_smem(p.KS, p.TS, cap, ns + 1) <= kM1SmemBudgetWhole)
+        while (ns < 16 && m1_smem(p.KS, p.WS, p.TS, cap, ns + 1) <= budget)
             ++ns;
         return ns;
     };
     int ns = slots(p.cap);
     while (ns < 3 && p.cap > avg + 1)
         ns = slots(--p.cap);
+    if (ns < 2)
+        return M1Plan();  // x's layout leaves no room for a ring: not supported
     p.nslot = ns;
     // Fixed items per CTA: three quarters of the average share (all of it
     // when the share fits the ring), the rest from the counter.
-    p.F = avg <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
+    p.F = avg * p.NP <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
     if (p.F < 1)
         p.F = 1;
     p.slot_bytes = p.W * kTileBytes;
-    p.smem = m1_smem(p.KS, p.TS, p.cap, ns);
+    p.smem = m1_smem(p.KS, p.WS, p.TS, p.cap, ns);
     p.ws_floats = S > 1 ? size_t(S) * size_t(T) * kTileRows : 0;
     p.tickets = size_t(2 * S) + (S > 1 ? size_t(p.n_items) : 0);
     return p;
@@ -686,6 +750,8 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.nmat = a.nmat;
     P.S = p.S;
     P.KS = p.KS;
+    P.WS = p.WS;
+    P.NP = p.NP;
     P.TS = p.TS;
     P.W = p.W;
     P.G1 = p.G1;
@@ -696,6 +762,12 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.slot_bytes = p.slot_bytes;
     cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(p.smem));
+    if (e != cudaSuccess)
+        return e;
+    // All shared memory, so that two half-SM CTAs (this launch and the next)
+    // fit side by side.
+    e = cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             int(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -188,14 +188,14 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
             p = qmm::plan_m1(T, NB, m0.sm_count, S);
     if (p.nslot < 2 || p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets)
         return QMM_ERR_UNSUPPORTED;
-    // Each matrix's column view with boxes of this plan's slice width (kept
+    // Each matrix's column view with boxes of this plan's pass width (kept
     // in the handle; re-encoded when a plan asks for another width).
     for (int i = 0; i < n; ++i) {
         Matrix &mi = *reinterpret_cast<Matrix *>(hs[i]);
-        if (mi.tmap3_ks != p.KS) {
-            if (qmm::make_q4k_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.KS) != 0)
+        if (mi.tmap3_ks != p.WS) {
+            if (qmm::make_q4k_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.WS) != 0)
                 return QMM_ERR_UNSUPPORTED;
-            mi.tmap3_ks = p.KS;
+            mi.tmap3_ks = p.WS;
         }
         a.tmap[i] = mi.tmap3;
     }

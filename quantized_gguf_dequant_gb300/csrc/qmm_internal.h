@@ -152,10 +152,13 @@ int make_q4k_tensor_map(void *out128, const void *w, int64_t N, int64_t row_byte
 // work items (tile groups) are handed out first statically, then from a
 // counter per slice.
 constexpr int kM1MaxWarps = 16;
-constexpr size_t kM1SmemBudgetWhole = 226 * 1024;
+constexpr size_t kM1SmemBudgetWhole = 226 * 1024;  // one CTA per SM
+constexpr size_t kM1SmemBudgetHalf = 110 * 1024;   // two CTAs per SM
 struct M1Plan {
+    int maxw = 0;                // consumer warps at most: 8 (half an SM) or 16
     int S = 0, KS = 0;           // K slices, super-blocks per slice
-    int TS = 0, W = 0;           // tiles per item, consumer warps (KS * TS)
+    int WS = 0, NP = 0;          // super-blocks per pass, passes per item (KS = WS * NP)
+    int TS = 0, W = 0;           // tiles per item, consumer warps (WS * TS)
     int G1 = 0;                  // CTAs per slice (grid = G1 * S)
     int n_items = 0;             // items per slice
     int F = 0;                   // fixed items per CTA (fetched before the PDL wait)
@@ -166,7 +169,7 @@ struct M1Plan {
     size_t tickets = 0;          // counters: 2 per slice, plus one per item when S > 1
 };
 struct M1Args {
-    const void *tmap[kMaxGroup];  // Matrix::tmap3 of each matrix (boxes of KS super-blocks)
+    const void *tmap[kMaxGroup];  // Matrix::tmap3 of each matrix (boxes of WS super-blocks)
     int64_t rows[kMaxGroup];
     float *y[kMaxGroup];
     int nmat;
@@ -176,10 +179,11 @@ struct M1Args {
     unsigned *status;
 };
 // T: 16-row tiles over all matrices; NB: super-blocks per row; force_S > 0
-// fixes the number of K slices (it must divide NB, with NB / S <= 16).
+// fixes the number of K slices (it must divide NB).
+// maxw: 8 or 16 consumer warps at most (0: QMM_M1_WARPS, default 16).
 // nslot == 0: no plan fits.
-M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S);
-size_t m1_smem(int KS, int TS, int cap, int nslot);
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw = 0);
+size_t m1_smem(int KS, int WS, int TS, int cap, int nslot);
 cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s);
 
 // --------------------------------------------------------------- batched tensor-core Q4_K GEMV

@@ -59,17 +59,18 @@ int main(int argc, char **argv)
     const long long NBs[] = {1, 2, 3, 4, 6, 7, 8, 12, 14, 16, 17, 28, 32, 56, 64};
     for (long long T : Ts)
         for (long long NB : NBs)
-            for (int S : {0, 1, 2, 4, 7, 8, 16}) {
+            for (int S : {0, 1, 2, 4, 7, 8, 16})
+                for (int maxw : {8, 16}) {
                 if (S > 0 && NB % S != 0)
                     continue;
-                const qmm::M1Plan p = qmm::plan_m1(T, NB, sms, S);
-                printf("{\"kind\": \"m1\", \"T\": %lld, \"NB\": %lld, \"force\": %d, "
-                       "\"S\": %d, \"KS\": %d, \"TS\": %d, \"W\": %d, \"G1\": %d, "
+                const qmm::M1Plan p = qmm::plan_m1(T, NB, sms, S, maxw);
+                printf("{\"kind\": \"m1\", \"maxw\": %d, \"T\": %lld, \"NB\": %lld, \"force\": %d, "
+                       "\"S\": %d, \"KS\": %d, \"WS\": %d, \"NP\": %d, \"TS\": %d, \"W\": %d, \"G1\": %d, "
                        "\"n_items\": %d, \"F\": %d, \"cap\": %d, \"nslot\": %d, "
                        "\"slot_bytes\": %d, \"smem\": %zu, \"smem_check\": %zu, "
                        "\"ws_floats\": %zu, \"tickets\": %zu}\n",
-                       T, NB, S, p.S, p.KS, p.TS, p.W, p.G1, p.n_items, p.F, p.cap, p.nslot,
-                       p.slot_bytes, p.smem, p.nslot ? qmm::m1_smem(p.KS, p.TS, p.cap, p.nslot) : 0,
+                       maxw, T, NB, S, p.S, p.KS, p.WS, p.NP, p.TS, p.W, p.G1, p.n_items, p.F, p.cap, p.nslot,
+                       p.slot_bytes, p.smem, p.nslot ? qmm::m1_smem(p.KS, p.WS, p.TS, p.cap, p.nslot) : 0,
                        p.ws_floats, p.tickets);
             }
     return 0;

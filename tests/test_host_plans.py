@@ -141,55 +141,55 @@ def test_fp32_gemv_plans(plans):
 def test_m1_plans_cover_and_stay_in_bounds(plans):
     """The one-row decode kernel (gemv_m1.cu): for every plan, the index
     arithmetic of the kernel restated here -- slice s = b % S of KS
-    super-blocks; item i = tiles [i*TS, (i+1)*TS) x the slice, one ring slot of
-    W = KS*TS units of 2304 bytes; consumer warp w reads unit (w // KS, w % KS);
-    CTA b1 of a slice takes items b1*F .. b1*F+F-1, then items G1*F + n from the
-    counter, at most cap in all -- covers every (tile, super-block) exactly
-    once, keeps every shared-memory index inside its array, sizes the counters
-    and scratch to what is touched, and fits the shared memory of one CTA."""
+    super-blocks; item i = tiles [i*TS, (i+1)*TS) x the slice in NP passes of
+    WS super-blocks, each pass one ring slot of W = WS*TS units of 2304 bytes;
+    consumer warp w reads unit (w // WS, w % WS); CTA b1 of a slice takes items
+    b1*F .. b1*F+F-1, then items G1*F + n from the counter, at most cap in all
+    -- covers every (tile, super-block) exactly once, keeps every
+    shared-memory index inside its array, sizes the counters and scratch to
+    what is touched, and fits the shared memory of one CTA (two CTAs per SM
+    with 8 consumer warps)."""
     rows = plans["m1"]
     assert rows
-    budget = 226 * 1024
     for p in rows:
-        T, NB, S, KS, TS, W = (p[k] for k in ("T", "NB", "S", "KS", "TS", "W"))
-        tag = f"T={T} NB={NB} force={p['force']}"
+        T, NB, S, KS, WS, NP, TS, W = (p[k] for k in ("T", "NB", "S", "KS", "WS", "NP", "TS", "W"))
+        maxw = p["maxw"]
+        budget = 110 * 1024 if maxw == 8 else 226 * 1024
+        tag = f"T={T} NB={NB} force={p['force']} maxw={maxw}"
         if p["nslot"] == 0:
-            # refused (the caller falls back): no slice of at most 16 super-blocks
-            assert not any(NB % s == 0 and NB // s <= 16 for s in range(1, min(NB, SMS) + 1)), tag
-            continue
-        if p["force"] and NB // p["force"] <= 16:
+            continue  # refused: the caller falls back to another kernel
+        if p["force"]:
             assert S == p["force"], tag
-        assert S * KS == NB and 1 <= KS <= 16, tag
-        assert W == KS * TS and W <= 16 and TS in (1, 2, 4, 8), tag
+        assert S * KS == NB and KS == WS * NP and 1 <= WS <= maxw, tag
+        assert W == WS * TS and W <= maxw and TS in (1, 2, 4, 8), tag
         n_items, G1, F, cap = p["n_items"], p["G1"], p["F"], p["cap"]
         assert n_items == -(-T // TS), tag
         assert 1 <= G1 <= n_items and (G1 * S <= SMS or -(-n_items // G1) <= 16), tag
-        assert p["nslot"] >= 2 and p["nslot"] <= 16, tag
+        assert 2 <= p["nslot"] <= 16, tag
         assert 1 <= F <= cap, tag
         # every item has a taker: the fixed shares plus cap per CTA cover them
-        assert G1 * cap >= n_items and G1 * F <= max(n_items, G1 * p["nslot"]), tag
+        assert G1 * cap >= n_items, tag
         assert p["slot_bytes"] == W * 2304, tag
         assert p["smem"] == p["smem_check"] <= budget, tag
         assert p["ws_floats"] == (S * T * 16 if S > 1 else 0), tag
         assert p["tickets"] == 2 * S + (n_items if S > 1 else 0), tag
         # the largest byte a consumer lane reads in a slot: unit W-1, row 15,
-        # bytes up to 144 of the row
+        # bytes up to 144 of the row; a producer box u lands at u*WS*2304
         assert (W - 1) * 2304 + 15 * 144 + 144 <= p["slot_bytes"], tag
+        assert (TS - 1) * WS * 2304 + WS * 2304 <= p["slot_bytes"], tag
         # fixed shares: items b1*F + f below n_items are distinct over CTAs
         fixed = {b * F + f for b in range(G1) for f in range(F) if b * F + f < n_items}
         assert len(fixed) == min(n_items, G1 * F), tag
-        # units: every (tile, super-block) of the slice appears in exactly one item
         assert n_items * TS >= T > (n_items - 1) * TS, tag
 
 
 @needs_nvcc
 def test_m1_default_plans_for_llama_shapes(plans):
     """The default plans of the Llama-3.1-8B decode launches: gate/up (1792
-    tiles) whole K per CTA with 16 consumer warps, q/k/v (384) and o (256) in
-    four K slices of 4 super-blocks x 4 tiles, down (256 tiles of 56
-    super-blocks) in four slices of 14."""
-    by = {(p["T"], p["NB"]): p for p in plans["m1"] if p["force"] == 0}
-    assert by[(1792, 16)]["S"] == 1 and by[(1792, 16)]["W"] == 16
-    assert by[(384, 16)]["S"] == 4 and by[(384, 16)]["TS"] == 4
-    assert by[(256, 16)]["S"] == 4
-    assert by[(256, 56)]["S"] == 4 and by[(256, 56)]["KS"] == 14
+    tiles), q/k/v (384) and o (256) whole K, one consumer warp per
+    super-block (16), one pass; down (256 tiles of 56 super-blocks) in four K
+    slices of 14, one pass."""
+    by = {(p["T"], p["NB"]): p for p in plans["m1"] if p["force"] == 0 and p["maxw"] == 16}
+    for T in (1792, 384, 256):
+        assert by[(T, 16)]["S"] == 1 and by[(T, 16)]["W"] == 16 and by[(T, 16)]["NP"] == 1
+    assert by[(256, 56)]["S"] == 4 and by[(256, 56)]["WS"] == 14 and by[(256, 56)]["NP"] == 1
