@@ -59,6 +59,7 @@
 
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
+#include "m1_device.cuh"
 #include "tc_common.cuh"
 
 namespace qmm {
@@ -66,8 +67,9 @@ namespace qmm {
 namespace {
 
 using namespace tc;
+using namespace m1;
 
-constexpr int kM1MaxSlots = 16;
+constexpr int kM1MaxSlots = kMaxSlots;
 constexpr int kM1MaxShare = 16;  // average items per CTA at most
 
 struct M1Params {
@@ -90,11 +92,6 @@ struct M1Params {
     int nslot, slot_bytes;
 };
 
-__device__ __forceinline__ void named_sync(int id, int n)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 __device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
 {
     int m = 0;
@@ -112,179 +109,6 @@ __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, i
     m = mat_of_tile(P, tile);
     row = (tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
     return row < P.rows[m];
-}
-
-// One box of the 3-D column view (tmap.cu, make_q4k_column_map): rows
-// [row, row+16) x super-blocks [sb, sb+WS) -> WS units of 16 x 144 bytes.
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int row, int sb,
-                                            uint64_t *bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(sb), "r"(smem_u32(bar)),
-        "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(a));
-    return v;
-}
-
-// Shared-memory float load / store executed only where pred holds (the
-// load gives 0 elsewhere).
-__device__ __forceinline__ float lds_f32_if(uint32_t a, bool pred)
-{
-    float v = 0.f;
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p ld.shared.f32 %0, [%1];\n\t}"
-                 : "+f"(v)
-                 : "r"(a), "r"(uint32_t(pred))
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void sts_f32_if(uint32_t a, float v, bool pred)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.f32 [%0], %1;\n\t}" ::"r"(a),
-                 "f"(v), "r"(uint32_t(pred))
-                 : "memory");
-}
-
-// Poll an mbarrier phase without spinning hard: between polls the thread
-// sleeps, so a waiting producer leaves the issue slots to the consumers.
-// Gives up (false) after `budget` cycles.
-__device__ __forceinline__ bool mbar_wait_polled(uint64_t *bar, unsigned parity,
-                                                 long long budget = kWaitBudgetCycles)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const long long t0 = clock64();
-    for (;;) {
-        __nanosleep(128);
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (clock64() - t0 > budget)
-            return false;
-    }
-}
-
-// Lane-constant part of the (sc, m) byte extraction for chunk c (see the
-// Q4_K packing): sel picks bytes (u, u+1, 4+u, 5+u), u = 2*(c & 1).  For
-// chunks 0 and 1 the fields are the low six bits of sc12[u..] and sc12[4+u..];
-// for chunks 2 and 3 the low four bits come from sc12[8+u..] (low or high
-// nibble) and the top two from bits 6-7 of sc12[u..] / sc12[4+u..].
-struct ScaleSel {
-    uint32_t sel, m1, m2, sh;
-};
-
-__device__ __forceinline__ ScaleSel scale_sel(int c)
-{
-    ScaleSel s;
-    const uint32_t u = 2u * uint32_t(c & 1);
-    s.sel = u * 0x1111u + 0x5410u;
-    const bool hi = c >= 2;
-    s.m1 = hi ? 0x0F0F0F0Fu : 0u;
-    s.m2 = hi ? 0x30303030u : 0x3F3F3F3Fu;
-    s.sh = hi ? 2u : 0u;
-    return s;
-}
-
-// Bytes (sc_2c, sc_2c+1, m_2c, m_2c+1) of a row header.
-__device__ __forceinline__ uint32_t scale_bytes(uint4 h, const ScaleSel &L)
-{
-    const uint32_t A = __byte_perm(h.y, h.z, L.sel);
-    const uint32_t Q = __byte_perm(h.w, h.w >> 4, L.sel);
-    return (Q & L.m1) | ((A >> L.sh) & L.m2);
-}
-
-// The contributions of rows g (header h0) and g+8 (h1) over this lane's two
-// sub-blocks, in packed fp32: Dlo / Dhi hold (row g, row g+8) sums of the hi
-// and lo MMA columns of sub-blocks 2c / 2c+1.
-__device__ __forceinline__ float2 pair_total(uint4 h0, uint4 h1, const ScaleSel &L, float2 Dlo,
-                                             float2 Dhi, float2 X0, float2 X1, float2 iv)
-{
-    const uint32_t R0 = scale_bytes(h0, L), R1 = scale_bytes(h1, L);
-    // (2^23 + v) * 2^k - 2^(23+k) = v * 2^k exactly.
-    const float2 sa = __ffma2_rn(make_float2(byte_magic(R0, 0), byte_magic(R1, 0)),
-                                 make_float2(16777216.f, 16777216.f),
-                                 make_float2(-140737488355328.f, -140737488355328.f));
-    const float2 sb = __ffma2_rn(make_float2(byte_magic(R0, 1), byte_magic(R1, 1)),
-                                 make_float2(1048576.f, 1048576.f),
-                                 make_float2(-8796093022208.f, -8796093022208.f));
-    const float2 ma = __fadd2_rn(make_float2(byte_magic(R0, 2), byte_magic(R1, 2)),
-                                 make_float2(-8388608.f, -8388608.f));
-    const float2 mb = __fadd2_rn(make_float2(byte_magic(R0, 3), byte_magic(R1, 3)),
-                                 make_float2(-8388608.f, -8388608.f));
-    const float2 d0 = half2_bits_to_float2(h0.x), d1 = half2_bits_to_float2(h1.x);
-    const float2 q = __ffma2_rn(sa, Dlo, __fmul2_rn(sb, Dhi));
-    const float2 mn = __ffma2_rn(ma, X0, __fmul2_rn(mb, X1));
-    const float2 dd = __fmul2_rn(make_float2(d0.x, d1.x), iv);
-    return __ffma2_rn(dd, q, __fmul2_rn(make_float2(-d0.y, -d1.y), mn));
-}
-
-// Activations of one super-block into its B entries bx[t][c][term] (uint4:
-// the fragments of the low- and high-nibble MMAs of k-step t), its eight
-// sub-block sums and 2^-s.  Lane (cc, tt) = (lane >> 3, lane & 7) holds
-// x[64cc + 4tt .. +3] (v, sub-block 2cc) and x[64cc + 32 + 4tt .. +3] (w,
-// sub-block 2cc+1).
-__device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx, float *xsum,
-                                        float *inv)
-{
-    const int cc = lane >> 3, tt = lane & 7;
-    uint32_t mb = 0;
-    mb = max(mb, max(max(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu),
-                     max(__float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu)));
-    mb = max(mb, max(max(__float_as_uint(w.x) & 0x7fffffffu, __float_as_uint(w.y) & 0x7fffffffu),
-                     max(__float_as_uint(w.z) & 0x7fffffffu, __float_as_uint(w.w) & 0x7fffffffu)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-    // max|x| < 2^(eM+1): scaling by 2^(14-eM) keeps every term below 2^15.
-    const int s = mb ? 14 - (int(mb >> 23) - 127) : 0;
-    float xs[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
-    if (s >= -126 && s <= 127) {
-        const float f = exp2i(s);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            xs[i] *= f;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            xs[i] = scale_pow2(xs[i], s);
-    }
-    __half hi[8], lo[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        hi[i] = __float2half_rn(xs[i]);
-        lo[i] = __float2half_rn(xs[i] - __half2float(hi[i]));
-    }
-    auto pack = [](__half a, __half b) {
-        return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
-    };
-    // k-step tt: elements (4tt, 4tt+2) in k-slots (2c, 2c+1), (4tt+1, 4tt+3) in (2c+8, 2c+9).
-    bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[2]), pack(hi[1], hi[3]),
-                                           pack(hi[4], hi[6]), pack(hi[5], hi[7]));
-    bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[2]), pack(lo[1], lo[3]),
-                                           pack(lo[4], lo[6]), pack(lo[5], lo[7]));
-    // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
-    float sl = (v.x + v.y) + (v.z + v.w);
-    float sh = (w.x + w.y) + (w.z + w.w);
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        sl += __shfl_xor_sync(0xffffffffu, sl, o);
-        sh += __shfl_xor_sync(0xffffffffu, sh, o);
-    }
-    if (tt == 0) {
-        xsum[2 * cc] = sl;
-        xsum[2 * cc + 1] = sh;
-    }
-    if (lane == 0)
-        *inv = scale_pow2(1.f, -s);
 }
 
 __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const __grid_constant__ M1Params P)
@@ -376,13 +200,15 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             }
         };
         unsigned *next = P.ctr + sl, *done = P.ctr + P.S + sl;
-        // Fixed items b1*F .. b1*F + nfix-1; then dynamic items from the
+        // Fixed items f*G1 + b1 (f < nfix); then dynamic items from the
         // counter.  `reserved` (lane 0) counts the items this CTA will compute
         // -- its fixed ones plus every index fetched -- and never exceeds cap,
         // so no fetched index is left uncomputed.  Two fetches are kept in
         // flight so that the atomics' round trips overlap the copies
         // (INT_MAX: nothing fetched).
-        const int nfix = max(0, min(P.F, P.n_items - b1 * P.F));
+        // fixed item f of this CTA: f*G1 + b1 (interleaved, so that every CTA
+        // has its share even when F*G1 overshoots the items)
+        const int nfix = b1 < P.n_items ? min(P.F, (P.n_items - b1 + P.G1 - 1) / P.G1) : 0;
         const int dyn0 = P.G1 * P.F;
         int reserved = nfix;
         int n0 = 0x7fffffff, n1 = 0x7fffffff;
@@ -409,7 +235,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             for (int p = 0; p < NP && ok; ++p) {
                 if (k == NS && !waited)
                     start_dynamic();
-                issue(b1 * P.F + f, p);
+                issue(f * P.G1 + b1, p);
             }
         if (!waited)
             start_dynamic();
@@ -465,7 +291,6 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         const bool act = (g >> 1) == c;
         const int term = g & 1;
         const ScaleSel L = scale_sel(c);
-        const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
         // B fragments, sub-block sums and inverse scale of this warp's
         // super-block of pass p (reloaded per pass when there are several).
         uint4 B[8];
@@ -527,31 +352,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 items[kc] = it;
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
-            const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
-            const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
-            float dlo[4], dhi[4];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
-                if (t == 0) {
-                    mma16816_zero(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
-                    mma16816_zero(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
-                } else {
-                    mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
-                    mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
-                }
-            }
-            const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
-                                                                  make_float2(dlo[1], dlo[3])),
-                                          __fadd2_rn(make_float2(dhi[0], dhi[2]),
-                                                     make_float2(dhi[1], dhi[3])),
-                                          X0, X1, iv);
-            // Sum the four lanes of the row pair: lanes c = 0 / 1 end with rows
-            // g / g+8 (the same fixed order for every unit).
-            const bool odd = c & 1;
-            float keep = odd ? tot.y : tot.x;
-            keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
-            keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+            float keep = unit_rows(h0, h1, qa0, qa1, qb0, qb1, B, L, c, X0, X1, iv);
             const uint32_t pa = pbase + uint32_t(kc * itile * 4);
             if (p > 0)
                 keep = lds_f32_if(pa, writer) + keep;  // passes added in order
@@ -656,12 +457,50 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
     // whose layout of x leaves two thirds of shared memory to the ring.
     // QMM_M1_S (or force_S) fixes S.
     const int forced = force_S > 0 ? force_S : env_m1_slices();
+    // (WS, TS) for a slice of ks super-blocks: the most consumer warps that
+    // still leave every SM an item, then the widest pass.
+    auto shape = [&](int ks, int s_, int &ws_best, int &ts_best) {
+        double best = -1.0;
+        const int per = sm_count / s_ >= 1 ? sm_count / s_ : 1;
+        for (int ws = (ks < maxw ? ks : maxw); ws >= 1; --ws) {
+            if (ks % ws)
+                continue;
+            for (int ts = 1; ts <= 8 && ws * ts <= maxw; ts *= 2) {
+                const int64_t items = (T + ts - 1) / ts;
+                const double use = items >= per ? 1.0 : double(items) / per;
+                const double score = ws * ts * use;
+                if (score > best + 1e-9) {
+                    best = score;
+                    ws_best = ws;
+                    ts_best = ts;
+                }
+            }
+        }
+        return best;
+    };
     int S = 0;
     if (forced > 0 && NB % forced == 0 && forced <= sm_count)
         S = forced;
-    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand)
-        if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3 && NB / cand <= 16)
+    // K slices: among those with one pass (at most 16 super-blocks, laid out
+    // per CTA -- laying out a long x in every CTA costs more than slices),
+    // the most consumer warps, then the fewest slices; else the fewest whose
+    // layout of x leaves two thirds of shared memory to the ring.
+    double best = -1.0;
+    for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand) {
+        if (NB % cand || NB / cand > maxw || size_t(NB / cand) * 1056 > budget / 3)
+            continue;
+        int ws = 0, ts = 0;
+        const double sc = shape(int(NB / cand), int(cand), ws, ts);
+        if (sc > best + 1e-9)
+            best = sc;
+    }
+    for (int64_t cand = 1; S == 0 && best > 0 && cand <= NB && cand <= sm_count; ++cand) {
+        if (NB % cand || NB / cand > maxw || size_t(NB / cand) * 1056 > budget / 3)
+            continue;
+        int ws = 0, ts = 0;
+        if (shape(int(NB / cand), int(cand), ws, ts) >= best - 1e-9)
             S = int(cand);
+    }
     for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand)
         if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3)
             S = int(cand);
@@ -670,25 +509,9 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
     p.maxw = maxw;
     p.S = S;
     p.KS = int(NB / S);
-    // Pass width WS (a divisor of KS, at most maxw) and tiles per item TS: the
-    // most consumer warps that still leave every SM an item, then the widest
-    // pass (fewest passes).
-    double best = -1.0;
+    // Pass width WS (a divisor of KS, at most maxw) and tiles per item TS.
+    shape(p.KS, S, p.WS, p.TS);
     const int per_slice = sm_count / S >= 1 ? sm_count / S : 1;
-    for (int ws = (p.KS < maxw ? p.KS : maxw); ws >= 1; --ws) {
-        if (p.KS % ws)
-            continue;
-        for (int ts = 1; ts <= 8 && ws * ts <= maxw; ts *= 2) {
-            const int64_t items = (T + ts - 1) / ts;
-            const double use = items >= per_slice ? 1.0 : double(items) / per_slice;
-            const double score = ws * ts * use;
-            if (score > best + 1e-9) {
-                best = score;
-                p.WS = ws;
-                p.TS = ts;
-            }
-        }
-    }
     p.NP = p.KS / p.WS;
     p.W = p.WS * p.TS;
     p.n_items = int((T + p.TS - 1) / p.TS);
@@ -716,8 +539,9 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
     if (ns < 2)
         return M1Plan();  // x's layout leaves no room for a ring: not supported
     p.nslot = ns;
-    // Fixed items per CTA: three quarters of the average share (all of it
-    // when the share fits the ring), the rest from the counter.
+    // Fixed items per CTA: the whole share (rounded up) when it fits the
+    // ring, so that all of it is fetched before the previous kernel ends;
+    // else three quarters of it.  The rest comes from the counter.
     p.F = avg * p.NP <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
     if (p.F < 1)
         p.F = 1;

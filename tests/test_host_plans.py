@@ -177,9 +177,12 @@ def test_m1_plans_cover_and_stay_in_bounds(plans):
         # bytes up to 144 of the row; a producer box u lands at u*WS*2304
         assert (W - 1) * 2304 + 15 * 144 + 144 <= p["slot_bytes"], tag
         assert (TS - 1) * WS * 2304 + WS * 2304 <= p["slot_bytes"], tag
-        # fixed shares: items b1*F + f below n_items are distinct over CTAs
-        fixed = {b * F + f for b in range(G1) for f in range(F) if b * F + f < n_items}
-        assert len(fixed) == min(n_items, G1 * F), tag
+        # fixed shares: items f*G1 + b1 below n_items, distinct over CTAs and
+        # at most one apart in count (every CTA starts with its share)
+        share = [sum(1 for f in range(F) if f * G1 + b < n_items) for b in range(G1)]
+        fixed = {f * G1 + b for b in range(G1) for f in range(F) if f * G1 + b < n_items}
+        assert len(fixed) == sum(share) == min(n_items, G1 * F), tag
+        assert max(share) - min(share) <= 1, tag
         assert n_items * TS >= T > (n_items - 1) * TS, tag
 
 
@@ -187,9 +190,9 @@ def test_m1_plans_cover_and_stay_in_bounds(plans):
 def test_m1_default_plans_for_llama_shapes(plans):
     """The default plans of the Llama-3.1-8B decode launches: gate/up (1792
     tiles), q/k/v (384) and o (256) whole K, one consumer warp per
-    super-block (16), one pass; down (256 tiles of 56 super-blocks) in four K
-    slices of 14, one pass."""
+    super-block (16), one pass; down (256 tiles of 56 super-blocks) in seven
+    K slices of 8 super-blocks x 2 tiles (16 consumer warps), one pass."""
     by = {(p["T"], p["NB"]): p for p in plans["m1"] if p["force"] == 0 and p["maxw"] == 16}
     for T in (1792, 384, 256):
         assert by[(T, 16)]["S"] == 1 and by[(T, 16)]["W"] == 16 and by[(T, 16)]["NP"] == 1
-    assert by[(256, 56)]["S"] == 4 and by[(256, 56)]["WS"] == 14 and by[(256, 56)]["NP"] == 1
+    assert by[(256, 56)]["S"] == 7 and by[(256, 56)]["W"] == 16 and by[(256, 56)]["NP"] == 1
