@@ -484,6 +484,38 @@ def time_graph(fn, steps, warmup, world, sampler_index=None):
     return ms, clocks
 
 
+def time_graph_stats(fn, reps, warmup, world):
+    """Capture fn into a CUDA graph, replay warmup times, then reps times with
+    an event pair around each replay; returns {median_ms, min_ms, mean_ms,
+    reps} over the replays (max over ranks)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for i in range(reps):
+        g.replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+    del g
+    return {"median_ms": max_over_ranks(world, statistics.median(t)),
+            "min_ms": max_over_ranks(world, min(t)),
+            "mean_ms": max_over_ranks(world, sum(t) / reps), "reps": reps}
+
+
 def time_eager(fn, steps, warmup, world):
     """Direct launches (no graph); used for profiling runs."""
     import torch
@@ -568,20 +600,22 @@ def run_ours(args, world, rank, local):
     per_gpu = step_bytes / (ms * 1e-3) / 1e9
     launches_per_step = launches_of(lambda: q4.step(True))
     launches = launches_per_step * args.steps
-    # Each kernel family timed on its own (same graph + PDL set-up): the
-    # K=4096 projections run on the decode tensor-core kernel, down (K=14336)
-    # on the K-sliced one-pass tensor-core kernel.
+    # Each family of launches timed on its own (same graph + PDL set-up): the
+    # K=4096 projections (q/k/v group, o, gate/up group) and down (K=14336,
+    # seven K slices), all on the one-row decode kernel.
     fam = {}
     wb = {s_: 0 for s_ in ("short", "long")}
     for name, N, K in SHAPES:
         wb["long" if K > 8192 else "short"] += N * synth.row_bytes(synth.Q4_K, K)
     xy = {"short": 4 * (3 * 4096 + 4096 + 1024 * 2 + 4096 + 14336 * 2),
           "long": 4 * (14336 + 4096)}
-    for which, kname, lpl in (("short", "gemv_tc_kernel", 3), ("long", "gemv_tcb_kernel<1, true>", 1)):
-        ms_f, _ = time_graph(lambda: q4.step_subset(which), max(3, args.steps // 4), args.warmup,
-                             world)
+    for which, kname in (("short", "gemv_m1_kernel"), ("long", "gemv_m1_kernel")):
+        st = time_graph_stats(lambda: q4.step_subset(which), max(20, args.steps // 4), args.warmup,
+                              world)
+        ms_f = st["median_ms"]
         b = (wb[which] + xy[which]) * nl
-        fam[which] = {"kernel": kname, "ms_per_step": ms_f, "bytes_per_step": b,
+        fam[which] = {"kernel": kname, "ms_per_step": ms_f, "min_ms": st["min_ms"],
+                      "reps": st["reps"], "bytes_per_step": b,
                       "launches_per_step": launches_of(lambda: q4.step_subset(which)),
                       "gbs": b / (ms_f * 1e-3) / 1e9}
     extras = {}
@@ -595,18 +629,22 @@ def run_ours(args, world, rank, local):
                       "qmm_gemv_group calls through the binding (no graph), D2H of every "
                       "output, stream sync"}
     if args.extras:
-        ms_u, _ = time_graph(lambda: q4.step(False), max(3, args.steps // 4), args.warmup, world)
+        st_u = time_graph_stats(lambda: q4.step(False), max(20, args.steps // 4), args.warmup, world)
+        ms_u = st_u["median_ms"]
         extras["q4k_decode_ungrouped"] = {
             "value": step_bytes / (ms_u * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_u,
+            "min_ms": st_u["min_ms"], "reps": st_u["reps"],
             "launches_per_step": launches_of(lambda: q4.step(False)),
             "frac_of_peak": step_bytes / (ms_u * 1e-3) / 1e9 / pk["hbm_gbs"]}
     if args.extras:
         bm = BatchedModel(q4)
         sweep = {}
         for M in (1, 2, 4, 8, 16):
-            ms_b, _ = time_graph(lambda: bm.step(M), max(3, args.steps // 8), args.warmup, world)
+            st_b = time_graph_stats(lambda: bm.step(M), max(20, args.steps // 8), args.warmup, world)
+            ms_b = st_b["median_ms"]
             b = bm.bytes_per_step(M)
-            sweep[str(M)] = {"ms_per_step": ms_b, "gbs": b / (ms_b * 1e-3) / 1e9,
+            sweep[str(M)] = {"ms_per_step": ms_b, "min_ms": st_b["min_ms"], "reps": st_b["reps"],
+                             "gbs": b / (ms_b * 1e-3) / 1e9,
                              "frac_of_peak": b / (ms_b * 1e-3) / 1e9 / pk["hbm_gbs"],
                              "tokens_per_s": M / (ms_b * 1e-3),
                              "launches_per_step": launches_of(lambda: bm.step(M))}
@@ -619,10 +657,12 @@ def run_ours(args, world, rank, local):
         fb = q4.ffn_bytes()
         ffn = {}
         for fused in (True, False):
-            ms_f, _ = time_graph(lambda: q4.ffn_step(fused), max(3, args.steps // 4), args.warmup,
-                                 world)
+            st_f = time_graph_stats(lambda: q4.ffn_step(fused), max(20, args.steps // 4), args.warmup,
+                                   world)
+            ms_f = st_f["median_ms"]
             ffn["fused" if fused else "separate"] = {
-                "ms_per_step": ms_f, "gbs": fb / (ms_f * 1e-3) / 1e9,
+                "ms_per_step": ms_f, "min_ms": st_f["min_ms"], "reps": st_f["reps"],
+                "gbs": fb / (ms_f * 1e-3) / 1e9,
                 "frac_of_peak": fb / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"],
                 "launches_per_step": launches_of(lambda: q4.ffn_step(fused))}
         extras["q4k_dense_ffn_decode"] = {
@@ -638,10 +678,12 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
     if args.extras:
         mo = MoeModel()
-        ms_m, _ = time_graph(mo.step, max(3, args.steps // 4), args.warmup, world)
+        st_m = time_graph_stats(mo.step, max(20, args.steps // 4), args.warmup, world)
+        ms_m = st_m["median_ms"]
         bm_ = mo.bytes_per_step()
         extras["olmoe_moe_ffn"] = {
             "value": bm_ / (ms_m * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_m,
+            "min_ms": st_m["min_ms"], "reps": st_m["reps"],
             "bytes_per_step": bm_, "layers": len(mo.layers), "tokens": mo.T,
             "frac_of_peak": bm_ / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"],
             "us_per_layer": ms_m * 1e3 / len(mo.layers), "launches_per_step": launches_of(mo.step),
@@ -655,10 +697,12 @@ def run_ours(args, world, rank, local):
         pre = {}
         for M in (512, 2048):
             pm = PrefillModel(M)
-            ms_p, _ = time_graph(pm.step, max(3, args.steps // 40), args.warmup, world)
+            st_p = time_graph_stats(pm.step, max(20, args.steps // 40), args.warmup, world)
+            ms_p = st_p["median_ms"]
             fl = pm.flops_per_step()
             tf = fl / (ms_p * 1e-3) / 1e12
-            pre[str(M)] = {"ms_per_step": ms_p, "tflops": tf,
+            pre[str(M)] = {"ms_per_step": ms_p, "min_ms": st_p["min_ms"], "reps": st_p["reps"],
+                           "tflops": tf, "tflops_at_min": fl / (st_p["min_ms"] * 1e-3) / 1e12,
                            "frac_of_peak": tf / pk["bf16_tflops"],
                            "launches_per_step": launches_of(pm.step)}
             pm.close()
@@ -678,9 +722,11 @@ def run_ours(args, world, rank, local):
     if args.extras:
         q8 = Model(synth.Q8_0, layers=nl)
         b8, _ = layer_bytes(synth.Q8_0)
-        ms8, _ = time_graph(lambda: q8.step(True), max(3, args.steps // 4), args.warmup, world)
+        st8 = time_graph_stats(lambda: q8.step(True), max(20, args.steps // 4), args.warmup, world)
+        ms8 = st8["median_ms"]
         extras["q8_0_decode"] = {
             "value": b8 * nl / (ms8 * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms8,
+            "min_ms": st8["min_ms"], "reps": st8["reps"],
             "bytes_per_step": b8 * nl,
             "frac_of_peak": b8 * nl / (ms8 * 1e-3) / 1e9 / pk["hbm_gbs"]}
         q8.close()
@@ -708,11 +754,14 @@ def run_ours(args, world, rank, local):
                         torch.matmul(W, xbs[L][kin[j]], out=ybs[L][j])
 
             nsteps = max(3, args.steps // 20)
-            ms_un, _ = time_graph(unfused_step, nsteps, args.warmup, world)
-            ms_fu, _ = time_graph(lambda: mu.step(True), nsteps, args.warmup, world)
+            st_un = time_graph_stats(unfused_step, max(20, nsteps), args.warmup, world)
+            st_fu = time_graph_stats(lambda: mu.step(True), max(20, nsteps), args.warmup, world)
+            ms_un, ms_fu = st_un["median_ms"], st_fu["median_ms"]
             b4, _ = layer_bytes(synth.Q4_K)
             extras["unfused_torch_baseline"] = {
                 "layers": 4, "ms_per_step_unfused": ms_un, "ms_per_step_fused": ms_fu,
+                "min_ms_unfused": st_un["min_ms"], "min_ms_fused": st_fu["min_ms"],
+                "reps": st_un["reps"],
                 "unfused_over_fused": ms_un / ms_fu,
                 "gbs_unfused": b4 * 4 / (ms_un * 1e-3) / 1e9, "gbs_fused": b4 * 4 / (ms_fu * 1e-3) / 1e9,
                 "unit": "GB/s of quantized algorithmic bytes",
@@ -734,9 +783,11 @@ def run_ours(args, world, rank, local):
             try:
                 mf = Model(fcode, layers=4)
                 bf, _ = layer_bytes(fcode)
-                ms_x, _ = time_graph(lambda: mf.step(True), max(3, args.steps // 8), args.warmup,
-                                     world)
-                fx[fname] = {"ms_per_step": ms_x, "layers": 4, "bytes_per_step": bf * 4,
+                st_x = time_graph_stats(lambda: mf.step(True), max(20, args.steps // 8),
+                                        args.warmup, world)
+                ms_x = st_x["median_ms"]
+                fx[fname] = {"ms_per_step": ms_x, "min_ms": st_x["min_ms"], "reps": st_x["reps"],
+                             "layers": 4, "bytes_per_step": bf * 4,
                              "gbs": bf * 4 / (ms_x * 1e-3) / 1e9,
                              "frac_of_peak": bf * 4 / (ms_x * 1e-3) / 1e9 / pk["hbm_gbs"]}
                 mf.close()
@@ -752,21 +803,28 @@ def run_ours(args, world, rank, local):
             note="Llama-3.1-8B decode step, 4 layers, the weights in each further format; the "
                  "first, plain GEMV of these formats (one warp per row)")
 
-    dom = max(fam.values(), key=lambda f: f["ms_per_step"])
-    traffic = recorded_traffic(dom["kernel"])
+    # Every launch of the step is the one-row decode kernel, so its average
+    # launch is the step's: algorithmic bytes per launch = step bytes / launches,
+    # launch duration = the step's device time / launches.
+    kname = "gemv_m1_kernel"
+    assert all(f["kernel"] == kname for f in fam.values())
+    traffic = recorded_traffic(kname)
     line = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(decode_config(nl, world), launches_per_step=launches_per_step),
-        "roofline": {"bound": "hbm", "achieved": dom["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": dom["gbs"] / pk["hbm_gbs"], "traffic": traffic,
-                     "kernel": dom["kernel"], "peak_source": pk["source"],
-                     "step_frac": per_gpu / pk["hbm_gbs"],
-                     "note": "dominant kernel (largest share of the step); achieved = its "
-                             "algorithmic bytes per step (weights once, inputs once, outputs) / "
-                             "CUDA-event time of a graph of only its launches (PDL on), "
-                             "averaged over its launches; traffic = ncu DRAM bytes per launch "
+        "roofline": {"bound": "hbm", "achieved": per_gpu, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": per_gpu / pk["hbm_gbs"], "traffic": traffic,
+                     "kernel": kname, "peak_source": pk["source"],
+                     "launches_per_step": launches_per_step,
+                     "algorithmic_bytes_per_launch": step_bytes / launches_per_step,
+                     "launch_ms": ms / launches_per_step,
+                     "note": "the step is launches of this one kernel only (100% of the step's "
+                             "device time); achieved = algorithmic bytes per launch (weights "
+                             "once, inputs once, outputs; mean over the step's launch mix) / "
+                             "mean launch duration (CUDA events over the timed region / "
+                             "launches); traffic = ncu DRAM bytes per launch over the same mix, "
                              "from profiles/traffic.json when taken on the current source"},
         "kernels": fam,
         "e2e": e2e,
@@ -872,7 +930,10 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": decode_config(args.layers, world),
+        "config": dict(decode_config(args.layers, world),
+                       timed_sample=f"{rows} rows x 7 matrices x 1 layer per step "
+                                    "(layers cycled over 4 seeds); value = sampled "
+                                    "algorithmic bytes / wall time"),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
