@@ -214,17 +214,20 @@ QMM_API qmm_status qmm_dequantize_bf16(qmm_t h, int64_t row0, int64_t nrows,
  *
  * Computes y[n] = sum_k w[n][k] * x[k] like qmm_gemv, but takes the matrix
  * description directly (fmt, N, K, w_dev as in qmm_create) instead of a
- * handle, and keeps its split-K scratch -- partial sums, tickets and a status
- * word -- in one 1 MiB device array inside the library image (held by every
- * GPU that loads the library until the process exits).  No cudaMalloc,
- * cudaFree or other allocating call is made.  The first call on a device
- * looks up that array's device address (cudaGetSymbolAddress); make it
- * before any stream capture.  Each call clears the tickets and status word on
- * `stream` before launching.  All calls share the one array: calls whose
- * work can overlap on the GPU (different streams, or concurrent host threads)
- * race and must be serialised by the caller.  Shapes whose split-K scratch
- * exceeds the array are refused (QMM_ERR_SHAPE) with the sizes named.
- * Device-side faults are not reported (there is no handle status word). */
+ * handle, and keeps its split-K scratch -- partial sums and tickets -- in one
+ * 1 MiB device array inside the library image (held by every GPU that loads
+ * the library until the process exits).  No cudaMalloc, cudaFree or other
+ * allocating call is made.  Every call looks up that array's device address
+ * in the current context (cudaGetSymbolAddress; the first lookup in a context
+ * may load the library's module, so make the first call before any stream
+ * capture); a context reset therefore needs nothing from the caller.  Each
+ * call clears the tickets on `stream` before launching.  All calls share the
+ * one array: calls whose work can overlap on the GPU (different streams, or
+ * concurrent host threads) race and must be serialised by the caller.  Shapes
+ * whose split-K scratch exceeds the array are refused (QMM_ERR_SHAPE) with
+ * the sizes named.  Unlike qmm_gemv, a device-side timeout is not reported:
+ * the kernel records it in a word of the same array that no call reads back,
+ * so a wedged pipeline shows only as a wrong y. */
 QMM_API qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
                                     const float *x, float *y, qmm_stream stream);
 

@@ -288,6 +288,21 @@ cudaError_t launch_moe_combine(const float *ys, const float *r, const int32_t *i
                                int top_k, int64_t Ne, float *y, int sm_count, cudaStream_t s);
 
 // --------------------------------------------------------------- no-allocation entry
+// Layout of qmm_gemv_noalloc's static scratch: [status word, padded to 256 B]
+// [tickets][split-K partial sums], 1 MiB in total.
+constexpr size_t kNoallocScratchBytes = size_t(1) << 20;
+constexpr size_t kNoallocStatusBytes = 256;
+constexpr size_t kNoallocTickets = 4096;
+constexpr size_t kNoallocPartialFloats =
+    (kNoallocScratchBytes - kNoallocStatusBytes - kNoallocTickets * 4) / 4;
+
+// Whether a decode GEMV plan's split-K scratch fits the static array.
+inline bool noalloc_fits(const GemvPlan &p, int64_t N)
+{
+    return gemv_workspace_floats(p, N) <= kNoallocPartialFloats &&
+           size_t(p.row_slices) <= kNoallocTickets;
+}
+
 // Argument checks of qmm_gemv_noalloc, and recording its refusal sentence for
 // qmm_last_error().
 qmm_status noalloc_check(int fmt, int64_t N, int64_t K, const void *w, const float *x,

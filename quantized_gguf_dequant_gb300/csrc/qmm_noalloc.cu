@@ -8,40 +8,24 @@
 // memory pool is fixed up front, or in a plug-in that must not change the
 // host program's device-memory footprint after start-up.
 #include <cstring>
-#include <mutex>
 
 #include "qmm_internal.h"
 
 namespace {
 
-// Layout of the static scratch: [status word, padded to 256 B][tickets]
-// [split-K partial sums].  1 MiB in total; every GPU that loads the library
-// keeps it until the process exits.
-constexpr size_t kScratchBytes = size_t(1) << 20;
-constexpr size_t kStatusBytes = 256;
-constexpr size_t kTickets = 4096;
-constexpr size_t kPartialFloats = (kScratchBytes - kStatusBytes - kTickets * 4) / 4;
+using qmm::kNoallocPartialFloats;
+using qmm::kNoallocScratchBytes;
+using qmm::kNoallocStatusBytes;
+using qmm::kNoallocTickets;
 
-static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+static __device__ __align__(256) unsigned char g_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_addr[kMaxDevices] = {};
-
-// The device address of g_scratch on the current device, looked up once per
-// device (the host-side name is only a stand-in for it).
-cudaError_t scratch_address(int dev, void **out)
+// The device address of g_scratch in the current context, looked up on every
+// call: a context torn down and made again (cudaDeviceReset) may place the
+// image elsewhere, so no address is kept between calls.
+cudaError_t scratch_address(void **out)
 {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
-    return cudaSuccess;
+    return cudaGetSymbolAddress(out, g_scratch);
 }
 
 } // namespace
@@ -59,23 +43,20 @@ qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: cudaGetDevice failed: %s",
                                  cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: device %d is beyond the %d "
-                                               "devices this entry point tracks", dev, kMaxDevices);
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: %s", cudaGetErrorString(e));
     const qmm::GemvPlan p = qmm::plan_gemv(fmt, N, K, sms, 0);
     const size_t need = qmm::gemv_workspace_floats(p, N);
-    if (need > kPartialFloats || size_t(p.row_slices) > kTickets)
+    if (!qmm::noalloc_fits(p, N))
         return qmm::noalloc_fail(
             QMM_ERR_SHAPE,
             "qmm_gemv_noalloc: this shape needs %zu floats of split-K scratch and %d tickets; the "
             "static scratch holds %zu floats and %zu tickets (use qmm_create/qmm_gemv)",
-            need, p.row_slices, kPartialFloats, kTickets);
+            need, p.row_slices, kNoallocPartialFloats, kNoallocTickets);
     void *base = nullptr;
-    e = scratch_address(dev, &base);
+    e = scratch_address(&base);
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA,
                                  "qmm_gemv_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
@@ -85,7 +66,7 @@ qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_
     // The tickets must start at zero.  A completed call leaves them zero, but
     // a call that timed out may not, so clear them (and the status word) on
     // the stream first -- a memset, not an allocation.
-    e = cudaMemsetAsync(b, 0, kStatusBytes + size_t(p.row_slices) * 4, s);
+    e = cudaMemsetAsync(b, 0, kNoallocStatusBytes + size_t(p.row_slices) * 4, s);
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: clearing the scratch failed: %s",
                                  cudaGetErrorString(e));
@@ -102,8 +83,8 @@ qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_
     a.row_bytes = qmm::row_bytes_of(fmt, K);
     a.x = x;
     a.status = reinterpret_cast<unsigned *>(b);
-    a.tickets = reinterpret_cast<unsigned *>(b + kStatusBytes);
-    a.ws = reinterpret_cast<float *>(b + kStatusBytes + kTickets * 4);
+    a.tickets = reinterpret_cast<unsigned *>(b + kNoallocStatusBytes);
+    a.ws = reinterpret_cast<float *>(b + kNoallocStatusBytes + kNoallocTickets * 4);
     e = qmm::launch_gemv(p, a, s);
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: launch failed: %s",

@@ -53,6 +53,19 @@ int main(int argc, char **argv)
                        fmt, N, K, p.kchunks, p.ksplit, p.rg, p.rpg, p.stage_rows, p.stages,
                        p.threads, p.row_slices, (long long)p.slice_bytes, p.smem);
             }
+    // the no-allocation entry point's shapes: split-K scratch against the
+    // static array
+    const long long na[][2] = {{37, 2048}, {3000, 4096}, {5, 14336}, {16384, 1LL << 20}};
+    for (int fmt : {int(QMM_Q4_K), int(QMM_Q8_0)})
+        for (const auto &nk : na) {
+            const qmm::GemvPlan p = qmm::plan_gemv(fmt, nk[0], nk[1], sms, 0);
+            printf("{\"kind\": \"noalloc\", \"fmt\": %d, \"N\": %lld, \"K\": %lld, "
+                   "\"ksplit\": %d, \"row_slices\": %d, \"need_floats\": %zu, "
+                   "\"have_floats\": %zu, \"have_tickets\": %zu, \"fits\": %d}\n",
+                   fmt, nk[0], nk[1], p.ksplit, p.row_slices,
+                   qmm::gemv_workspace_floats(p, nk[0]), qmm::kNoallocPartialFloats,
+                   qmm::kNoallocTickets, int(qmm::noalloc_fits(p, nk[0])));
+        }
     // one-row decode kernel: tile counts of single matrices and groups,
     // every K-slice count (0 = the default choice)
     const long long Ts[] = {1, 2, 3, 16, 19, 64, 250, 256, 384, 1792, 8192, 20000};

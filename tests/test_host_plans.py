@@ -196,3 +196,18 @@ def test_m1_default_plans_for_llama_shapes(plans):
     for T in (1792, 384, 256):
         assert by[(T, 16)]["S"] == 1 and by[(T, 16)]["W"] == 16 and by[(T, 16)]["NP"] == 1
     assert by[(256, 56)]["S"] == 7 and by[(256, 56)]["W"] == 16 and by[(256, 56)]["NP"] == 1
+
+
+@needs_nvcc
+def test_noalloc_shapes_split_k_and_refuse(plans):
+    """The shapes tests/test_zz_no_alloc.py runs: at least one per format
+    splits K (so the static scratch is written and read), every one of them
+    fits, and the refused shape needs the scratch many times over (so the
+    refusal does not hang on a planner detail)."""
+    recs = {(r["fmt"], r["N"], r["K"]): r for r in plans["noalloc"]}
+    for fmt in (12, 8):  # Q4_K, Q8_0
+        run = [recs[(fmt, N, K)] for N, K in ((37, 2048), (3000, 4096), (5, 14336))]
+        assert all(r["fits"] for r in run), run
+        assert any(r["ksplit"] > 1 and r["need_floats"] > 0 for r in run), run
+    big = recs[(12, 16384, 1 << 20)]
+    assert not big["fits"] and big["need_floats"] >= 4 * big["have_floats"], big
