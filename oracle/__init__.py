@@ -227,7 +227,8 @@ def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
 
 def moe_gemv(fmt: int, w: np.ndarray, n_experts: int, N_e: int, K: int,
              ids: np.ndarray, X: np.ndarray, x_per_slot: bool,
-             route_w: np.ndarray | None = None, nthreads: int = 1):
+             route_w: np.ndarray | None = None, nthreads: int = 1,
+             route_on_input: bool = False):
     """Grouped expert GEMV driven by router expert ids.
 
     w holds n_experts matrices of N_e x K stacked back to back (row r of
@@ -236,6 +237,11 @@ def moe_gemv(fmt: int, w: np.ndarray, n_experts: int, N_e: int, K: int,
     Without route_w: returns (Y, C) with Y[t*top_k + s] = W_e x   ([T*top_k, N_e]).
     With route_w [T, top_k]: Y[t] = sum_s r[t,s] * W_{ids[t,s]} x_(t,s),
     C[t] = sum_s |r[t,s]| * sum_k |w x|  ([T, N_e]).
+    With route_w and route_on_input (the Llama 4 form: the routing weight
+    multiplies the expert's input, "Frink Inference: the Rust alternative to
+    llama.cpp", "Architecture coverage: 100 models with evidence"): per slot,
+    no sum, Y[t*top_k + s] = W_e (r[t,s] x_(t,s)) with the scaled input
+    formed in fp64, C = sum_k |w| |r x|  ([T*top_k, N_e]).
     """
     ids = np.asarray(ids, dtype=np.int64)
     T, top_k = ids.shape
@@ -243,6 +249,20 @@ def moe_gemv(fmt: int, w: np.ndarray, n_experts: int, N_e: int, K: int,
     assert X.shape[0] == (T * top_k if x_per_slot else T) and X.shape[1] == K
     if ids.min() < 0 or ids.max() >= n_experts:
         raise ValueError("expert id out of range")
+    if route_on_input:
+        if route_w is None:
+            raise ValueError("route_on_input needs route_w")
+        r = np.asarray(route_w, dtype=np.float64).reshape(-1)
+        Y = np.zeros((T * top_k, N_e), np.float64)
+        C = np.zeros((T * top_k, N_e), np.float64)
+        for e in np.unique(ids):
+            slots = np.nonzero(ids.reshape(-1) == e)[0]
+            xin = (X[slots] if x_per_slot else X[slots // top_k]).astype(np.float64)
+            xin = r[slots][:, None] * xin
+            W = dequant_rows(fmt, w, n_experts * N_e, K, row0=e * N_e, nrows=N_e)
+            Y[slots] = xin @ W.T
+            C[slots] = np.abs(xin) @ np.abs(W).T
+        return Y, C
     slot_y = np.zeros((T * top_k, N_e), np.float64)
     slot_c = np.zeros((T * top_k, N_e), np.float64)
     rows_of = np.arange(N_e, dtype=np.int64)
@@ -266,19 +286,34 @@ def moe_gemv(fmt: int, w: np.ndarray, n_experts: int, N_e: int, K: int,
 
 def moe_ffn(fmt: int, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray,
             n_experts: int, d_model: int, d_ff: int, ids: np.ndarray,
-            X: np.ndarray, route_w: np.ndarray, nthreads: int = 1):
+            X: np.ndarray, route_w: np.ndarray, nthreads: int = 1,
+            route_on_input: bool = False):
     """The whole expert FFN in fp64: for each token t and slot s with
     e = ids[t,s]:  g = Wg_e x_t, u = Wu_e x_t, h = silu(g) u,
     y_t += r[t,s] * Wd_e h.  Gate/up are d_ff x d_model per expert and down is
-    d_model x d_ff.  Returns y [T, d_model] (fp64)."""
+    d_model x d_ff.  Returns y [T, d_model] (fp64).
+
+    route_on_input (Llama 4, "Frink Inference: the Rust alternative to
+    llama.cpp", "Architecture coverage: 100 models with evidence": the expert
+    weight applied to the input of the expert): g = Wg_e (r x_t),
+    u = Wu_e (r x_t), h = silu(g) u, y_t += Wd_e h -- r scales the input and
+    is not applied again.  SwiGLU is not homogeneous, so the two forms
+    differ unless r = 1."""
     ids = np.asarray(ids, dtype=np.int64)
     T, top_k = ids.shape
-    g, _ = moe_gemv(fmt, w_gate, n_experts, d_ff, d_model, ids, X, False,
-                    nthreads=nthreads)
-    u, _ = moe_gemv(fmt, w_up, n_experts, d_ff, d_model, ids, X, False,
-                    nthreads=nthreads)
+    if route_on_input:
+        g, _ = moe_gemv(fmt, w_gate, n_experts, d_ff, d_model, ids, X, False, route_w,
+                        nthreads=nthreads, route_on_input=True)
+        u, _ = moe_gemv(fmt, w_up, n_experts, d_ff, d_model, ids, X, False, route_w,
+                        nthreads=nthreads, route_on_input=True)
+        r = np.ones((T, top_k), np.float64)
+    else:
+        g, _ = moe_gemv(fmt, w_gate, n_experts, d_ff, d_model, ids, X, False,
+                        nthreads=nthreads)
+        u, _ = moe_gemv(fmt, w_up, n_experts, d_ff, d_model, ids, X, False,
+                        nthreads=nthreads)
+        r = np.asarray(route_w, dtype=np.float64).reshape(T, top_k)
     h = swiglu(g, u)
-    r = np.asarray(route_w, dtype=np.float64).reshape(T, top_k)
     y = np.zeros((T, d_model), np.float64)
     for e in np.unique(ids):
         slots = np.nonzero(ids.reshape(-1) == e)[0]

@@ -421,3 +421,77 @@ def test_generator_fields():
     assert all(len(set(row)) == 8 for row in ids)
     assert np.all(np.diff(r, axis=1) <= 0)
     assert np.array_equal(synth.q4k_matrix(3, 256, 5), synth.q4k_matrix(3, 256, 5))
+
+
+# ------------------------------------------------------------- routing on input
+
+def _q8_0_diagonal(n: int, q_of_row) -> np.ndarray:
+    """n x n Q8_0 matrix (one 32-weight block per row when n = 32), d = 1,
+    weight (i, i) = q_of_row(i) and 0 elsewhere: its exact value is the
+    diagonal matrix diag(q_of_row(i))."""
+    assert n == 32
+    rows = []
+    for i in range(n):
+        q = np.zeros(32, np.int8)
+        q[i] = q_of_row(i)
+        rows.append(struct.pack("<e", 1.0) + q.tobytes())
+    return np.frombuffer(b"".join(rows), np.uint8).copy()
+
+
+def test_moe_ffn_route_on_input_closed_form():
+    """Llama 4 applies the routing weight to the expert's input ("Frink
+    Inference: the Rust alternative to llama.cpp", "Architecture coverage:
+    100 models with evidence").  With diagonal experts every output is a
+    scalar closed form: expert 0 has Wg = I, Wu = 2I, Wd = I; expert 1 has
+    Wg = 3I, Wu = I, Wd = -I.  Input form:  y = sum_s Wd (silu(r Wg x) * (r Wu x));
+    output form: y = sum_s r Wd (silu(Wg x) * (Wu x))."""
+    D = F = 32
+    E = 2
+    wg = np.concatenate([_q8_0_diagonal(32, lambda i: 1), _q8_0_diagonal(32, lambda i: 3)])
+    wu = np.concatenate([_q8_0_diagonal(32, lambda i: 2), _q8_0_diagonal(32, lambda i: 1)])
+    wd = np.concatenate([_q8_0_diagonal(32, lambda i: 1), _q8_0_diagonal(32, lambda i: -1)])
+    ids = np.array([[0, 1], [1, 0], [0, 0]])
+    r = np.array([[0.25, 1.5], [2.0, -0.5], [0.75, 0.125]], np.float32)
+    X = np.linspace(-3.0, 3.0, 3 * D, dtype=np.float32).reshape(3, D)
+
+    def silu(z):
+        return z / (1.0 + math.exp(-z))
+
+    gscale, uscale, dscale = {0: 1, 1: 3}, {0: 2, 1: 1}, {0: 1, 1: -1}
+    ref_in = np.zeros((3, D))
+    ref_out = np.zeros((3, D))
+    for t in range(3):
+        for s in range(2):
+            e, rw = int(ids[t, s]), float(r[t, s])
+            for i in range(D):
+                x = float(X[t, i])
+                ref_in[t, i] += dscale[e] * silu(gscale[e] * rw * x) * (uscale[e] * rw * x)
+                ref_out[t, i] += rw * dscale[e] * silu(gscale[e] * x) * (uscale[e] * x)
+    y_in = oracle.moe_ffn(Q8_0, wg, wu, wd, E, D, F, ids, X, r, route_on_input=True)
+    y_out = oracle.moe_ffn(Q8_0, wg, wu, wd, E, D, F, ids, X, r)
+    assert np.allclose(y_in, ref_in, rtol=1e-13, atol=1e-13)
+    assert np.allclose(y_out, ref_out, rtol=1e-13, atol=1e-13)
+    assert np.abs(y_in - y_out).max() > 0.1  # SwiGLU tells the two orders apart
+
+
+def test_moe_route_on_input_unit_weights_and_linearity():
+    """r = 1: the input form equals the output form exactly in the FFN; the
+    expert GEMV is linear, so the scaled-input slot outputs equal r times the
+    plain slot outputs to fp64 rounding."""
+    E, D, F, T, top_k = 4, 256, 256, 3, 2
+    wg = synth.q4k_matrix(E * F, D, seed=71)
+    wu = synth.q4k_matrix(E * F, D, seed=72)
+    wd = synth.q4k_matrix(E * D, F, seed=73)
+    ids, r = synth.router(T, E, top_k, seed=74)
+    X = synth.activations(T, D, seed=75)
+    one = np.ones_like(r)
+    y1 = oracle.moe_ffn(Q4_K, wg, wu, wd, E, D, F, ids, X, one, route_on_input=True)
+    y2 = oracle.moe_ffn(Q4_K, wg, wu, wd, E, D, F, ids, X, one)
+    assert np.allclose(y1, y2, rtol=1e-12, atol=1e-12 * np.abs(y2).max())
+    S, _ = oracle.moe_gemv(Q4_K, wg, E, F, D, ids, X, False)
+    Si, Ci = oracle.moe_gemv(Q4_K, wg, E, F, D, ids, X, False, r, route_on_input=True)
+    ref = r.astype(np.float64).reshape(-1, 1) * S
+    assert np.allclose(Si, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(Ci >= np.abs(Si) * (1 - 1e-12))
+    with pytest.raises(ValueError):
+        oracle.moe_gemv(Q4_K, wg, E, F, D, ids, X, False, None, route_on_input=True)
