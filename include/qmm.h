@@ -24,8 +24,9 @@
  *   QMM_Q8_0  block of 32 weights in 34 bytes: [fp16 d][32 x int8 q];
  *             w = d*q.
  *   Further formats ("Frink Inference: the Rust alternative to llama.cpp",
- *   "What is supported": the K-quants; "Where llama.cpp is still ahead":
- *   IQ4_NL), for qmm_create, qmm_gemv, qmm_gemv_group, qmm_gemv_batched,
+ *   "Where Frink is already better than llama.cpp": Q8_0 and the K-quants
+ *   written byte-identically to llama-quantize; "Where llama.cpp is still
+ *   ahead": IQ4_NL logits that match), for qmm_create, qmm_gemv, qmm_gemv_group, qmm_gemv_batched,
  *   qmm_ffn_decode and qmm_dequantize[_bf16]; the expert and prefill calls
  *   refuse them (QMM_ERR_UNSUPPORTED):
  *   QMM_Q5_K  176 bytes / 256 weights: [fp16 d][fp16 dmin][the 12 scale/min
@@ -86,7 +87,7 @@ typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q5_K = 13, QMM_Q6_K = 14, QMM_IQ
 typedef enum {
     QMM_OK = 0,
     QMM_ERR_NULL = -1,        /* a required pointer is NULL */
-    QMM_ERR_FORMAT = -2,      /* not Q4_K or Q8_0 */
+    QMM_ERR_FORMAT = -2,      /* not one of Q4_K, Q8_0, Q5_K, Q6_K, IQ4_NL */
     QMM_ERR_SHAPE = -3,       /* a size is out of range or does not fill whole blocks */
     QMM_ERR_ALIGN = -4,       /* a pointer or leading dimension is not aligned as required */
     QMM_ERR_CUDA = -5,        /* the CUDA runtime reported an error (named in qmm_last_error) */
@@ -100,8 +101,8 @@ typedef struct qmm_matrix *qmm_t;
 typedef void *qmm_stream; /* cudaStream_t */
 
 /* Describe a quantized matrix of N rows x K columns at w_dev (borrowed, not
- * copied).  Requires: fmt in {Q4_K, Q8_0}; N >= 1; K % 256 == 0 (Q4_K; for
- * Q8_0 also K % 256 == 0 in this version, so every row starts 16-byte
+ * copied).  Requires: fmt one of Q4_K, Q8_0, Q5_K, Q6_K, IQ4_NL; N >= 1;
+ * K % 256 == 0 (every format in this version, so every row starts 16-byte
  * aligned); w_dev 16-byte aligned.  Allocates the handle's workspace and
  * status word on the current device.  On success *out is a new handle. */
 QMM_API qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
@@ -124,28 +125,39 @@ QMM_API qmm_status qmm_gemv(qmm_t h, const float *x, float *y, qmm_stream stream
 QMM_API qmm_status qmm_gemv_group(const qmm_t *hs, int32_t n, const float *x,
                           float *const *ys, qmm_stream stream);
 
-/* Batched decode (continuous batching): M activation rows share one read of
- * the weights.  Y[m*ldy + n] = sum_k w[n][k] * X[m*ldx + k], 1 <= M <= 16,
+/* Batched decode: M activation rows share one read of the weights -- the
+ * decode step of a server that batches requests continuously ("Frink
+ * Inference: the Rust alternative to llama.cpp", "The goal, stated once":
+ * the server bullet, continuous batching over paged KV).  Y[m*ldy + n] = sum_k w[n][k] * X[m*ldx + k], 1 <= M <= 16,
  * ldx >= K, ldy >= N, both multiples of 4.  Q4_K from two rows on: all rows
  * in one pass; the first call with a larger M may grow the handle's scratch
  * (a synchronising allocation: make it before capturing a CUDA graph). */
 QMM_API qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx,
                             float *Y, int64_t ldy, qmm_stream stream);
 
-/* Grouped mixture-of-experts GEMV driven by router expert ids.  The handle
+/* Grouped mixture-of-experts GEMV driven by router expert ids, the expert
+ * layers of the mixture-of-experts models the pages run ("Frink Inference:
+ * the Rust alternative to llama.cpp", "Where Frink is already better than
+ * llama.cpp": OLMoE decode on Metal; "Architecture coverage: 100 models with
+ * evidence": dense and mixture-of-experts alike).  The handle
  * holds n_experts stacked matrices of N_e = N / n_experts rows each.
  * expert_ids: [T, top_k] int32 (device); the input of slot (t, s) is X[t]
  * when x_per_slot == 0 (X is [T, K]) or X[t*top_k + s] when x_per_slot == 1
  * (X is [T*top_k, K]).  route_w == NULL: Y is [T*top_k, N_e], Y[t*top_k+s] =
- * W_{ids[t,s]} x.  route_w != NULL ([T, top_k] fp32): Y is [T, N_e],
- * Y[t] = sum_s route_w[t,s] * W_{ids[t,s]} x (summed in slot order).  Each
+ * W_{ids[t,s]} x.  route_w != NULL ([T, top_k] fp32) and route_on_input == 0:
+ * Y is [T, N_e], Y[t] = sum_s route_w[t,s] * W_{ids[t,s]} x (summed in slot
+ * order).  route_on_input == 1 (route_w required; the Llama 4 form, where
+ * the routing weight multiplies the expert's input -- "Architecture
+ * coverage: 100 models with evidence"): Y is [T*top_k, N_e],
+ * Y[t*top_k+s] = W_{ids[t,s]} (route_w[t,s] * x), the product r*x rounded to
+ * fp32 as the activations are loaded, no sum over slots.  Each
  * expert's rows are read once per call for all of its slots.  An id outside
  * [0, n_experts) leaves that slot's contribution 0 and sets QMM_ERR_EXPERT in
  * the status word.  1 <= T*top_k <= 4096, top_k <= 16. */
 QMM_API qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids,
                         int32_t T, int32_t top_k, const float *X,
-                        int32_t x_per_slot, const float *route_w, float *Y,
-                        qmm_stream stream);
+                        int32_t x_per_slot, const float *route_w, int32_t route_on_input,
+                        float *Y, qmm_stream stream);
 
 /* h = silu(g) * u elementwise, silu(z) = z / (1 + exp(-z)); n fp32 values.
  * The SwiGLU between an expert's gate/up and down projections. */
@@ -155,12 +167,18 @@ QMM_API qmm_status qmm_swiglu(const float *g, const float *u, float *h, int64_t 
 /* A whole expert FFN: gate and up (both n_experts x d_ff x d_model), SwiGLU,
  * down (n_experts x d_model x d_ff) and the routing-weighted sum over each
  * token's top_k experts.  X [T, d_model] fp32, route_w [T, top_k] fp32,
- * Y [T, d_model] fp32.  Uses hg's workspace for the [T*top_k, d_ff]
- * intermediate.  Same limits and id checking as qmm_moe_gemv. */
+ * Y [T, d_model] fp32.  route_on_input == 0: y_t = sum_s r * Wd h with
+ * h = silu(Wg x) * (Wu x) (OLMoE, Mixtral, Qwen-MoE).  route_on_input == 1:
+ * the Llama 4 form ("Frink Inference: the Rust alternative to llama.cpp",
+ * "Architecture coverage: 100 models with evidence": the expert weight
+ * applied to the input of the expert), h = silu(Wg (r x)) * (Wu (r x)),
+ * y_t = sum_s Wd h; SwiGLU makes the two differ.  Uses hg's workspace for
+ * the [T*top_k, d_ff] intermediate.  Same limits and id checking as
+ * qmm_moe_gemv. */
 QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
                        const int32_t *expert_ids, int32_t T, int32_t top_k,
-                       const float *X, const float *route_w, float *Y,
-                       qmm_stream stream);
+                       const float *X, const float *route_w, int32_t route_on_input,
+                       float *Y, qmm_stream stream);
 
 /* A dense SwiGLU FFN for one token (decode):  h = silu(Wg x) * (Wu x),
  * y = Wd h.  hg, hu: d_ff x d_model (same format), hd: d_model x d_ff.
@@ -180,7 +198,11 @@ QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
 QMM_API qmm_status qmm_ffn_decode(qmm_t hg, qmm_t hu, qmm_t hd, const float *x, float *h, float *y,
                                   qmm_stream stream);
 
-/* Prefill GEMM on the tensor cores (Q4_K only in this version):
+/* Prefill GEMM on the tensor cores -- prompt processing, the one phase
+ * where the pages' CUDA engine trails most ("Frink Inference: the Rust
+ * alternative to llama.cpp", "Where llama.cpp is still ahead": prefill 25x
+ * to 43x slower on CUDA; a tensor-core GEMM as the newer work).  Q4_K only
+ * in this version:
  * Y[m*N + n] = sum_k bf16(w[n][k]) * X[m*K + k], fp32 accumulation, where
  * bf16(w) rounds the exact weight to fp32 and then to bf16 (nearest even).
  * X: [M, K] bfloat16 bit patterns, 16-byte aligned; Y: [M, N] fp32.

@@ -61,9 +61,9 @@ def lib() -> ctypes.CDLL:
             "qmm_gemv": [vp, vp, vp, vp],
             "qmm_gemv_group": [ctypes.POINTER(vp), i32, vp, ctypes.POINTER(vp), vp],
             "qmm_gemv_batched": [vp, vp, i64, i64, vp, i64, vp],
-            "qmm_moe_gemv": [vp, i32, vp, i32, i32, vp, i32, vp, vp, vp],
+            "qmm_moe_gemv": [vp, i32, vp, i32, i32, vp, i32, vp, i32, vp, vp],
             "qmm_swiglu": [vp, vp, vp, i64, vp],
-            "qmm_moe_ffn": [vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, vp],
+            "qmm_moe_ffn": [vp, vp, vp, i32, vp, i32, i32, vp, vp, i32, vp, vp],
             "qmm_gemm": [vp, vp, i64, vp, vp],
             "qmm_dequantize": [vp, i64, i64, vp, vp],
             "qmm_dequantize_bf16": [vp, i64, i64, vp, vp],
@@ -150,9 +150,10 @@ def gemv_batched(h: int, X, M: int, ldx: int, Y, ldy: int, stream=None):
 
 
 def moe_gemv(h: int, n_experts: int, ids, T: int, top_k: int, X, x_per_slot: int,
-             route_w, Y, stream=None):
+             route_w, Y, stream=None, route_on_input: bool = False):
     _check(lib().qmm_moe_gemv(ctypes.c_void_p(h), n_experts, _ptr(ids), T, top_k, _ptr(X),
-                              int(x_per_slot), _ptr(route_w), _ptr(Y), _stream(stream)))
+                              int(x_per_slot), _ptr(route_w), int(route_on_input), _ptr(Y),
+                              _stream(stream)))
 
 
 def ffn_decode(hg: int, hu: int, hd: int, x, h, y, stream=None):
@@ -166,10 +167,10 @@ def swiglu(g, u, hout, n: int, stream=None):
 
 
 def moe_ffn(hg: int, hu: int, hd: int, n_experts: int, ids, T: int, top_k: int, X, route_w, Y,
-            stream=None):
+            stream=None, route_on_input: bool = False):
     _check(lib().qmm_moe_ffn(ctypes.c_void_p(hg), ctypes.c_void_p(hu), ctypes.c_void_p(hd),
-                             n_experts, _ptr(ids), T, top_k, _ptr(X), _ptr(route_w), _ptr(Y),
-                             _stream(stream)))
+                             n_experts, _ptr(ids), T, top_k, _ptr(X), _ptr(route_w),
+                             int(route_on_input), _ptr(Y), _stream(stream)))
 
 
 def gemm(h: int, X_bf16, M: int, Y, stream=None):

@@ -5,7 +5,9 @@
 // Engine That Matches Llama.cpp", "Where the wins came from": the weights are
 // decoded inline in the dot product, never expanded into a buffer), for the
 // K-quants and IQ4_NL that "Frink Inference: the Rust alternative to
-// llama.cpp" names ("What is supported", "Where llama.cpp is still ahead").
+// llama.cpp" names ("Where Frink is already better than llama.cpp": the
+// K-quants written byte-identically; "Where llama.cpp is still ahead":
+// IQ4_NL).
 //
 // GEMV: one warp per output row; lane l decodes the row's 32-weight groups
 // l, l+32, ... in registers and multiplies each by the M activation rows

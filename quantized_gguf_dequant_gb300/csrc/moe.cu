@@ -6,7 +6,11 @@
 // sends each token through the top_k experts its router picked and sums their
 // outputs with the router's weights.  Per token t and slot s with expert
 // e = ids[t, s]:  g = Wg_e x_t, u = Wu_e x_t, h = silu(g) * u,
-// y_t = sum_s r[t, s] * Wd_e h.
+// y_t = sum_s r[t, s] * Wd_e h.  Llama 4 applies r to the expert's input
+// instead ("Architecture coverage: 100 models with evidence": the expert
+// weight applied to the input of the expert): g = Wg_e (r x_t),
+// u = Wu_e (r x_t), y_t = sum_s Wd_e h -- the expert step scales each
+// slot's activations by r as it loads them, the combine adds without r.
 //
 // Steps, one kernel each:
 //  1. bucket   -- one CTA sorts the T*top_k slots by expert id (stable, so
@@ -161,6 +165,7 @@ struct MoeParams {
     int NB;                    // super-blocks per row
     int top_k;
     int x_per_slot;
+    const float *xscale;       // per-slot input scale [S] (routing on the input), or null
     int nslot;
     // fuse = 1 (nmat = 2, gate and up): tiles are taken in (gate, up) pairs
     // of the same rows, staged in shared memory (room for maxpairs pairs per
@@ -293,6 +298,11 @@ __global__ void __launch_bounds__(512, 1) moe_expert_kernel(const __grid_constan
                     const float *xr = P.x + xrow * P.ldx + int64_t(sb) * 256 + 64 * cc + 4 * tt;
                     v = __ldg(reinterpret_cast<const float4 *>(xr));
                     w = __ldg(reinterpret_cast<const float4 *>(xr + 32));
+                    if (P.xscale) {  // the slot's routing weight on its input
+                        const float r = __ldg(P.xscale + s);
+                        v = make_float4(r * v.x, r * v.y, r * v.z, r * v.w);
+                        w = make_float4(r * w.x, r * w.y, r * w.z, r * w.w);
+                    }
                 }
                 prep_super_block<kNcol>(sb, m, kGroupTokens, v, w, lane, Bs, Bm, inv);
             }
@@ -441,7 +451,8 @@ __global__ void swiglu_kernel(const float *__restrict__ g, const float *__restri
 }
 
 // y[t][n] = sum_s r[t][s] * ys[t*top_k + s][n], s ascending; dropped slots
-// (ids outside [0, E)) contribute nothing.
+// (ids outside [0, E)) contribute nothing.  r == nullptr: the plain sum (the
+// routing weight was applied to the experts' inputs).
 __global__ void moe_combine_kernel(const float *__restrict__ ys, const float *__restrict__ r,
                                    const int32_t *__restrict__ ids, int E, int T, int top_k,
                                    int64_t Ne, float *__restrict__ y)
@@ -457,7 +468,7 @@ __global__ void moe_combine_kernel(const float *__restrict__ ys, const float *__
             const int64_t slot = t * top_k + s;
             const int e = ids[slot];
             if (e >= 0 && e < E)
-                acc = fmaf(r[slot], ys[slot * Ne + n], acc);
+                acc = r ? fmaf(r[slot], ys[slot * Ne + n], acc) : acc + ys[slot * Ne + n];
         }
         y[i] = acc;
     }
@@ -544,6 +555,7 @@ cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t
     P.NB = int(a.K / 256);
     P.top_k = a.top_k;
     P.x_per_slot = a.x_per_slot;
+    P.xscale = a.xscale;
     P.fuse = a.fuse_swiglu;
     P.maxpairs = a.fuse_swiglu ? a.maxpairs : 0;
     int nw, nslot;

@@ -652,7 +652,8 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
 
 qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, int32_t T,
                         int32_t top_k, const float *X, int32_t x_per_slot,
-                        const float *route_w, float *Y, qmm_stream stream)
+                        const float *route_w, int32_t route_on_input, float *Y,
+                        qmm_stream stream)
 {
     g_err.clear();
     const char *fn = "qmm_moe_gemv";
@@ -667,24 +668,33 @@ qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, i
         return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X ? "X" : "Y");
     if (x_per_slot != 0 && x_per_slot != 1)
         return fail(QMM_ERR_SHAPE, "%s: x_per_slot = %d; it must be 0 or 1", fn, x_per_slot);
+    if (route_on_input != 0 && route_on_input != 1)
+        return fail(QMM_ERR_SHAPE, "%s: route_on_input = %d; it must be 0 or 1", fn,
+                    route_on_input);
+    if (route_on_input && !route_w)
+        return fail(QMM_ERR_NULL, "%s: route_on_input = 1 needs route_w", fn);
     if (!aligned(X, 16))
         return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
     if (!aligned(Y, 4) || (route_w && !aligned(route_w, 4)))
         return fail(QMM_ERR_ALIGN, "%s: %s is not 4-byte aligned", fn, !aligned(Y, 4) ? "Y" : "route_w");
     const int S = T * top_k;
     const int64_t Ne = m->N / n_experts;
+    // Per-slot outputs straight into Y unless the slots are summed with
+    // their routing weights afterwards.
+    const bool combine = route_w && !route_on_input;
     MoeScratch ms;
-    st = moe_scratch(*m, S, n_experts, route_w ? size_t(S) * Ne : 0, 0, fn, ms);
+    st = moe_scratch(*m, S, n_experts, combine ? size_t(S) * Ne : 0, 0, fn, ms);
     if (st != QMM_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = qmm::launch_moe_bucket(expert_ids, S, n_experts, ms.ix, route_w ? nullptr : Y,
+    cudaError_t e = qmm::launch_moe_bucket(expert_ids, S, n_experts, ms.ix, combine ? nullptr : Y,
                                            Ne, Ne, m->status, s);
     if (e == cudaSuccess) {
         qmm::MoeExpertArgs a;
         memset(&a, 0, sizeof(a));
         a.tmap[0] = m->tmap;
-        a.y[0] = route_w ? ms.ys : Y;
+        a.y[0] = combine ? ms.ys : Y;
+        a.xscale = route_on_input ? route_w : nullptr;
         a.nmat = 1;
         a.Ne = Ne;
         a.K = m->K;
@@ -696,7 +706,7 @@ qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, i
         a.status = m->status;
         e = qmm::launch_moe_expert(a, m->sm_count, s);
     }
-    if (e == cudaSuccess && route_w)
+    if (e == cudaSuccess && combine)
         e = qmm::launch_moe_combine(ms.ys, route_w, expert_ids, n_experts, T, top_k, Ne, Y,
                                     m->sm_count, s);
     if (e != cudaSuccess)
@@ -730,7 +740,8 @@ qmm_status qmm_swiglu(const float *g, const float *u, float *hh, int64_t n, qmm_
 
 qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
                        const int32_t *expert_ids, int32_t T, int32_t top_k, const float *X,
-                       const float *route_w, float *Y, qmm_stream stream)
+                       const float *route_w, int32_t route_on_input, float *Y,
+                       qmm_stream stream)
 {
     g_err.clear();
     const char *fn = "qmm_moe_ffn";
@@ -761,6 +772,9 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
                     (long long)md->N, (long long)md->K, n_experts);
     if (!X || !Y || !route_w)
         return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !X ? "X" : (!Y ? "Y" : "route_w"));
+    if (route_on_input != 0 && route_on_input != 1)
+        return fail(QMM_ERR_SHAPE, "%s: route_on_input = %d; it must be 0 or 1", fn,
+                    route_on_input);
     if (!aligned(X, 16))
         return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
     if (!aligned(Y, 4) || !aligned(route_w, 4))
@@ -800,6 +814,7 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
         a.x = X;
         a.ldx = d_model;
         a.x_per_slot = 0;
+        a.xscale = route_on_input ? route_w : nullptr;
         a.fuse_swiglu = fuse ? 1 : 0;
         a.maxpairs = maxpairs;
         e = qmm::launch_moe_expert(a, sms, s);
@@ -807,6 +822,7 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     if (e == cudaSuccess && !fuse)
         e = qmm::launch_swiglu(ms.g, ms.u, ms.h, int64_t(S) * d_ff, sms, s);
     a.fuse_swiglu = 0;
+    a.xscale = nullptr;
     if (e == cudaSuccess) {  // down, one input row per slot
         a.tmap[0] = md->tmap;
         a.tmap[1] = nullptr;
@@ -821,8 +837,8 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
         e = qmm::launch_moe_expert(a, sms, s);
     }
     if (e == cudaSuccess)
-        e = qmm::launch_moe_combine(ms.ys, route_w, expert_ids, n_experts, T, top_k, d_model, Y,
-                                    sms, s);
+        e = qmm::launch_moe_combine(ms.ys, route_on_input ? nullptr : route_w, expert_ids,
+                                    n_experts, T, top_k, d_model, Y, sms, s);
     if (e != cudaSuccess)
         return cuda_fail(e, fn);
     mg->last_stream = s;

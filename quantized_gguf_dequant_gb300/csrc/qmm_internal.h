@@ -270,6 +270,7 @@ struct MoeExpertArgs {
     int64_t ldx;
     int top_k;
     int x_per_slot;
+    const float *xscale;  // per-slot input scale [T*top_k] (routing on the input), or null
     int fuse_swiglu;      // nmat == 2: y[0] = silu(gate) * up, y[1] unused
     int maxpairs;         // (fused) shared-memory room: (gate, up) tile pairs per CTA
     MoeIndex ix;

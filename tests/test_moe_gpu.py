@@ -8,6 +8,8 @@ bound carries the gate/up bounds through SwiGLU into the down projection
 (first order; |silu'| <= 1.1)."""
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -300,3 +302,92 @@ def test_moe_ffn_refusals():
     assert ei.value.status in (q.ERR_NULL, q.ERR_SHAPE)
     for h in (hg, hu, hd_wrong):
         h.close()
+
+
+# ------------------------------------------------------------------ routing on the input (Llama 4)
+
+def _ffn_bound_input(wg, wu, wd, E, d_model, d_ff, ids, r, X):
+    """As _ffn_bound, for the routing weight applied to the expert input:
+    the gate/up bounds are those of the scaled inputs r x, and the slots are
+    summed without r."""
+    g, cg = oracle.moe_gemv(q.Q4_K, wg, E, d_ff, d_model, ids, X, False, r, nthreads=NTHREADS,
+                            route_on_input=True)
+    u, cu = oracle.moe_gemv(q.Q4_K, wu, E, d_ff, d_model, ids, X, False, r, nthreads=NTHREADS,
+                            route_on_input=True)
+    h = oracle.swiglu(g, u)
+    sg = oracle.swiglu(g, np.ones_like(g))
+    a = np.abs(h) + 1.1 * np.abs(u) * cg + np.abs(sg) * cu
+    _, c = oracle.moe_gemv(q.Q4_K, wd, E, d_model, d_ff, ids, a.astype(np.float32), True,
+                           np.ones_like(r), nthreads=NTHREADS)
+    y = oracle.moe_ffn(q.Q4_K, wg, wu, wd, E, d_model, d_ff, ids, X, r, nthreads=NTHREADS,
+                       route_on_input=True)
+    return y, c * 1.0001
+
+
+@pytest.mark.parametrize("E,Ne,K,T,top_k,x_per_slot", [
+    (8, 48, 512, 5, 3, False),
+    (4, 40, 256, 16, 2, True),
+    (16, 64, 1024, 1, 1, False),   # Llama 4 routes each token to one expert
+])
+def test_moe_gemv_route_on_input(E, Ne, K, T, top_k, x_per_slot):
+    """Per-slot outputs of the experts on their routing-weighted inputs."""
+    w, m = _stacked(E, Ne, K, seed=300 + E)
+    ids, r = _ids_uniform(T, E, top_k, seed=301 + T)
+    r = (r * np.float32(3.0) - np.float32(1.0)).astype(np.float32)  # signs and |r| > 1 too
+    X = synth.activations(T * top_k if x_per_slot else T, K, seed=302)
+    y_ref, c = oracle.moe_gemv(q.Q4_K, w, E, Ne, K, ids, X, x_per_slot, r, nthreads=NTHREADS,
+                               route_on_input=True)
+    Y = torch.full((T * top_k, Ne), float("nan"), dtype=torch.float32, device="cuda")
+    q.moe_gemv(m.h, E, to_dev(ids), T, top_k, to_dev(X), x_per_slot, to_dev(r), Y,
+               route_on_input=True)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(Y.cpu().numpy(), y_ref, c, TOL_FP32, "route on input")
+    assert m.status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("E,d_model,d_ff,T,top_k", [
+    (4, 512, 256, 3, 2),
+    (16, 1024, 512, 8, 1),
+])
+def test_moe_ffn_route_on_input(monkeypatch, fused, E, d_model, d_ff, T, top_k):
+    """The Llama 4 expert FFN: r scales the expert input, the slots are summed
+    without it; checked against the oracle's input form, and shown to differ
+    from the output form by more than the bound."""
+    if not fused:
+        monkeypatch.setenv("QMM_MOE_NOFUSE", "1")
+    wg, wu, wd, ids, r, X = _ffn_case(E, d_model, d_ff, T, top_k, seed=40 + E)
+    r = (r * np.float32(4.0)).astype(np.float32)  # far from 1, so the forms separate
+    y_ref, c = _ffn_bound_input(wg, wu, wd, E, d_model, d_ff, ids, r, X)
+    hs = [q.Matrix(q.Q4_K, E * d_ff, d_model, to_dev(wg)),
+          q.Matrix(q.Q4_K, E * d_ff, d_model, to_dev(wu)),
+          q.Matrix(q.Q4_K, E * d_model, d_ff, to_dev(wd))]
+    Y = torch.full((T, d_model), float("nan"), dtype=torch.float32, device="cuda")
+    q.moe_ffn(hs[0].h, hs[1].h, hs[2].h, E, to_dev(ids), T, top_k, to_dev(X), to_dev(r), Y,
+              route_on_input=True)
+    torch.cuda.synchronize()
+    y = Y.cpu().numpy()
+    assert_close_to_oracle(y, y_ref, c, TOL_FP32, "ffn route on input")
+    y_out = oracle.moe_ffn(q.Q4_K, wg, wu, wd, E, d_model, d_ff, ids, X, r, nthreads=NTHREADS)
+    assert np.max(np.abs(y_out - y_ref) - 1e-4 * c) > 0  # the other order is outside the bound
+    assert hs[0].status() == 0
+    for h in hs:
+        h.close()
+
+
+def test_moe_route_on_input_refusals():
+    E, Ne, K = 4, 32, 256
+    w, m = _stacked(E, Ne, K, seed=5)
+    ids, r = _ids_uniform(2, E, 2, seed=6)
+    X = synth.activations(2, K, seed=7)
+    Y = torch.zeros((4, Ne), dtype=torch.float32, device="cuda")
+    with pytest.raises(q.QmmError) as ei:
+        q.moe_gemv(m.h, E, to_dev(ids), 2, 2, to_dev(X), False, None, Y, route_on_input=True)
+    assert ei.value.status == q.ERR_NULL
+    ids_d, X_d, r_d = to_dev(ids), to_dev(X), to_dev(r)
+    rc = q.lib().qmm_moe_gemv(ctypes.c_void_p(m.h), E, ctypes.c_void_p(ids_d.data_ptr()), 2, 2,
+                              ctypes.c_void_p(X_d.data_ptr()), 0, ctypes.c_void_p(r_d.data_ptr()),
+                              2, ctypes.c_void_p(Y.data_ptr()), None)
+    assert rc == q.ERR_SHAPE and "route_on_input" in q.last_error()
+    m.close()
