@@ -78,6 +78,9 @@ def lib():
         L.or_bf16_to_double.argtypes = [ctypes.c_uint16]
         L.or_bf16_to_double.restype = ctypes.c_double
         L.or_swiglu.argtypes = [vp, vp, i64, vp]
+        L.or_quantize_q8_k.argtypes = [vp, i64, vp]
+        L.or_dequant_q8_k.argtypes = [vp, i64, vp]
+        L.or_gemv_q8k.argtypes = [i32, vp, i64, i64, vp, vp, vp, i32]
         L.or_max_threads.restype = i32
         _lib = L
     return _lib
@@ -323,3 +326,36 @@ def moe_ffn(fmt: int, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray,
         for j, sl in enumerate(slots):
             y[sl // top_k] += r[sl // top_k, sl % top_k] * o[j]
     return y
+
+
+# ---------------------------------------------------------------- Q8_K activations
+
+Q8_K_BLOCK = 292  # bytes per 256 activations: d (f32), q[256] (int8), bsums[16] (int16)
+
+
+def quantize_q8_k(x: np.ndarray) -> np.ndarray:
+    """GGUF Q8_K blocks of the fp32 vector x (len % 256 == 0), as uint8."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    out = np.empty(x.size // 256 * Q8_K_BLOCK, np.uint8)
+    _check(lib().or_quantize_q8_k(_p(x), x.size, _p(out)), "quantize_q8_k")
+    return out
+
+
+def dequant_q8_k(xq: np.ndarray, K: int) -> np.ndarray:
+    """The fp64 activations the Q8_K blocks stand for (d * q)."""
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    assert xq.size >= K // 256 * Q8_K_BLOCK
+    out = np.empty(K, np.float64)
+    _check(lib().or_dequant_q8_k(_p(xq), K, _p(out)), "dequant_q8_k")
+    return out
+
+
+def gemv_q8k(fmt: int, w: np.ndarray, N: int, K: int, xq: np.ndarray, nthreads: int = 1):
+    """(Y, C): the integer-dot GEMV against Q8_K activations, as the exact
+    weights times the exact dequantized activations in fp64."""
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    Y = np.empty(N, np.float64)
+    C = np.empty(N, np.float64)
+    _check(lib().or_gemv_q8k(fmt, _p(w), N, K, _p(xq), _p(Y), _p(C), nthreads), "gemv_q8k")
+    return Y, C

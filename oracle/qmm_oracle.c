@@ -30,8 +30,8 @@
  *       w = d*q.
  *   The further formats of the next step ("Frink Inference: the Rust
  *   alternative to llama.cpp", sections "Where llama.cpp is still ahead" --
- *   IQ4_NL -- and "What is supported" -- the other K-quants), also GGUF
- *   block formats:
+ *   IQ4_NL -- and "Where Frink is already better than llama.cpp" -- the
+ *   other K-quants, written byte-identically), also GGUF block formats:
  *     Q5_K super-block, 176 bytes, 256 weights: d, dmin (binary16), the
  *       twelve scale/min bytes of Q4_K, qh[32] (fifth bits), qs[128] (low
  *       four bits, in the Q4_K nibble order).  Weight i: chunk c = i/64,
@@ -449,4 +449,135 @@ int or_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* ---------------------------------------------------------------------- */
+/* Q8_K activations (the integer-dot variant)                              */
+/* ---------------------------------------------------------------------- */
+
+/* "Frink Inference: the Rust alternative to llama.cpp", section "Where
+ * llama.cpp is still ahead": llama.cpp quantizes the activations to Q8_K
+ * before a K-quant dot product, which is why its K-quant logits drift from
+ * an f32 engine's.  The pages name the format only; the layout and the
+ * quantizer here are GGUF's Q8_K (reading: llama.cpp's reference row
+ * quantizer):
+ *   block of 256 activations, 292 bytes:
+ *     [0..3]     d, binary32
+ *     [4..259]   q[256], int8
+ *     [260..291] bsums[16], int16: bsums[g] = sum of q[16g .. 16g+15]
+ *   max = the signed value of the first element with the largest |x| (an
+ *   element replaces the running choice only when strictly larger);
+ *   max == 0: d = 0 and every q = 0.  Otherwise, in binary32 arithmetic,
+ *   iscale = -127 / max, q_j = min(127, round-half-even(iscale * x_j)),
+ *   d = 1 / iscale.  The value a code stands for is d * q_j.
+ * The divisions and the product decide integer codes, so they are taken in
+ * binary32 exactly as written (one rounding each), not in fp64. */
+int or_quantize_q8_k(const float *x, int64_t K, uint8_t *out)
+{
+    if (!x || !out || K <= 0 || K % 256)
+        return -1;
+    for (int64_t b = 0; b < K / 256; ++b) {
+        const float *xb = x + b * 256;
+        uint8_t *ob = out + b * 292;
+        float amax = 0.f, max = 0.f;
+        for (int j = 0; j < 256; ++j) {
+            float ax = fabsf(xb[j]);
+            if (ax > amax) {
+                amax = ax;
+                max = xb[j];
+            }
+        }
+        int8_t q[256];
+        float d;
+        if (amax == 0.f) {
+            d = 0.f;
+            memset(q, 0, sizeof(q));
+        } else {
+            volatile float iscale = -127.f / max;
+            for (int j = 0; j < 256; ++j) {
+                volatile float t = iscale * xb[j];
+                long v = lrintf(t); /* the default rounding mode: half to even */
+                q[j] = (int8_t)(v > 127 ? 127 : v);
+            }
+            d = 1.f / iscale;
+        }
+        memcpy(ob, &d, 4);
+        memcpy(ob + 4, q, 256);
+        for (int g = 0; g < 16; ++g) {
+            int s = 0;
+            for (int j = 0; j < 16; ++j)
+                s += q[16 * g + j];
+            int16_t s16 = (int16_t)s;
+            memcpy(ob + 260 + 2 * g, &s16, 2);
+        }
+    }
+    return 0;
+}
+
+/* The activations Q8_K blocks stand for: x[k] = d_b * q_k (exact in fp64). */
+int or_dequant_q8_k(const uint8_t *xq, int64_t K, double *x)
+{
+    if (!xq || !x || K <= 0 || K % 256)
+        return -1;
+    for (int64_t b = 0; b < K / 256; ++b) {
+        float d;
+        memcpy(&d, xq + b * 292, 4);
+        const int8_t *q = (const int8_t *)(xq + b * 292 + 4);
+        for (int j = 0; j < 256; ++j)
+            x[b * 256 + j] = (double)d * (double)q[j];
+    }
+    return 0;
+}
+
+/* The integer-dot GEMV against Q8_K activations:
+ *   Y[i] = sum_k w[i][k] * xhat[k],  xhat = the values the Q8_K blocks stand for,
+ *   C[i] = sum_k |w[i][k] * xhat[k]|                           (C may be NULL).
+ * llama.cpp's integer kernel adds q_w * q_x in int32 per sub-block and
+ * applies the block scales afterwards; that only regroups this sum (every
+ * integer partial is exact), so the definition is the decode-then-dot of the
+ * exact weights with the exact dequantized activations, in fp64. */
+int or_gemv_q8k(int fmt, const uint8_t *w, int64_t N, int64_t K, const uint8_t *xq,
+                double *Y, double *C, int nthreads)
+{
+    int64_t rb = or_row_bytes(fmt, K);
+    if (!w || !xq || !Y || rb < 0 || N <= 0 || K % 256)
+        return -1;
+    double *xh = (double *)malloc((size_t)K * sizeof(double));
+    if (!xh)
+        return -3;
+    or_dequant_q8_k(xq, K, xh);
+    int bad = 0;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *wr = (double *)malloc((size_t)K * sizeof(double));
+        if (!wr) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            bad = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+            for (int64_t i = 0; i < N; ++i) {
+                dequant_row(fmt, w, K, rb, i, wr);
+                double s = 0.0, a = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double p = wr[k] * xh[k];
+                    s += p;
+                    a += fabs(p);
+                }
+                Y[i] = s;
+                if (C)
+                    C[i] = a;
+            }
+            free(wr);
+        }
+    }
+    free(xh);
+    return bad ? -3 : 0;
 }

@@ -495,3 +495,131 @@ def test_moe_route_on_input_unit_weights_and_linearity():
     assert np.all(Ci >= np.abs(Si) * (1 - 1e-12))
     with pytest.raises(ValueError):
         oracle.moe_gemv(Q4_K, wg, E, F, D, ids, X, False, None, route_on_input=True)
+
+
+# ------------------------------------------------------------- Q8_K activations
+
+def _q8k_fields(blk: bytes):
+    d = struct.unpack("<f", blk[0:4])[0]
+    q = list(struct.unpack("<256b", blk[4:260]))
+    bsums = list(struct.unpack("<16h", blk[260:292]))
+    return d, q, bsums
+
+
+def test_q8_k_hand_block():
+    """One block worked by hand: the largest |x| is -1.0 (index 5), so
+    iscale = -127 / -1 = 127 exactly; 0.5 -> 63.5 -> 64 (half to even),
+    -0.25 -> -31.75 -> -32, 0.75 -> 95.25 -> 95; d = 1/127 in binary32."""
+    x = np.zeros(256, np.float32)
+    x[5], x[6], x[7], x[20], x[255] = -1.0, 0.5, -0.25, 0.75, 1.0 / 127.0
+    d, q, bs = _q8k_fields(oracle.quantize_q8_k(x).tobytes())
+    assert d == float(np.float32(1.0) / np.float32(127.0))
+    expect = {5: -127, 6: 64, 7: -32, 20: 95, 255: 1}
+    for j in range(256):
+        assert q[j] == expect.get(j, 0), j
+    assert bs[0] == -127 + 64 - 32 and bs[1] == 95 and bs[15] == 1
+    assert all(b == 0 for g, b in enumerate(bs) if g not in (0, 1, 15))
+
+
+def test_q8_k_ties_to_even_and_first_max():
+    # max = -63.5 -> iscale = 2 exactly: 0.25 -> 0.5 -> 0, 0.75 -> 1.5 -> 2,
+    # 1.25 -> 2.5 -> 2, -1.25 -> -2.5 -> -2
+    x = np.zeros(256, np.float32)
+    x[0], x[1], x[2], x[3], x[4] = -63.5, 0.25, 0.75, 1.25, -1.25
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(x).tobytes())
+    assert d == 0.5 and q[:5] == [-127, 0, 2, 2, -2]
+    # equal |x| of both signs: the first one is the block's max
+    y = np.zeros(256, np.float32)
+    y[3], y[10] = -4.0, 4.0
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(y).tobytes())
+    assert d > 0 and q[3] == -127 and q[10] == 127
+    y[3], y[10] = 4.0, -4.0
+    d, q, _ = _q8k_fields(oracle.quantize_q8_k(y).tobytes())
+    assert d < 0 and q[3] == -127 and q[10] == 127
+
+
+def test_q8_k_zero_block_and_bound():
+    x = synth.activations(1, 1024, seed=81)[0].copy()
+    x[256:512] = 0.0
+    xq = oracle.quantize_q8_k(x)
+    assert not xq[292:584].any()  # d = 0, q = 0, bsums = 0
+    xh = oracle.dequant_q8_k(xq, 1024)
+    for b in range(4):
+        d, q, bs = _q8k_fields(xq[292 * b:292 * (b + 1)].tobytes())
+        assert all(bs[g] == sum(q[16 * g:16 * g + 16]) for g in range(16))
+        blk = x[256 * b:256 * (b + 1)].astype(np.float64)
+        if d != 0.0:
+            assert q[int(np.argmax(np.abs(blk)))] == -127
+        assert np.all(np.abs(blk - xh[256 * b:256 * (b + 1)]) <= abs(d) * (0.5 + 2.0 ** -20))
+
+
+def test_gemv_q8k_exact_when_x_is_on_the_grid():
+    """x of integers in [-127, 127] with 127 the first largest element of
+    every block: iscale = -1, q = -x, d = -1, so the dequantized activations
+    are x itself and the integer-dot GEMV equals the f32 GEMV exactly."""
+    K, N = 1024, 9
+    rng = np.random.default_rng(82)
+    x = rng.integers(-126, 127, K).astype(np.float32)
+    x[0::256] = 127.0
+    xq = oracle.quantize_q8_k(x)
+    assert np.array_equal(oracle.dequant_q8_k(xq, K), x.astype(np.float64))
+    w = synth.q4k_matrix(N, K, seed=83)
+    y8, c8 = oracle.gemv_q8k(Q4_K, w, N, K, xq)
+    y, c = oracle.gemv(Q4_K, w, N, K, x)
+    assert np.array_equal(y8, y) and np.array_equal(c8, c)
+
+
+def test_gemv_q8k_integer_regrouping_and_naive():
+    """The llama.cpp grouping of the same sum -- per sub-block an integer dot
+    of nibbles and codes scaled by sc, minus m times the block's code sums
+    (bsums), then d_w * d_x -- computed here in Python integers from the raw
+    bytes, equals the oracle; so does a naive loop over the naive block
+    decoder."""
+    K, N = 512, 3
+    w = synth.q4k_matrix(N, K, seed=84)
+    x = synth.activations(1, K, seed=85)[0]
+    xq = oracle.quantize_q8_k(x)
+    y8, c8 = oracle.gemv_q8k(Q4_K, w, N, K, xq)
+    rb = K // 256 * 144
+    wf = np.ascontiguousarray(w).reshape(-1)
+    for n in range(N):
+        tot = 0.0
+        naive = 0.0
+        for b in range(K // 256):
+            blk = bytes(wf[n * rb + 144 * b:n * rb + 144 * (b + 1)])
+            dx, qx, bs = _q8k_fields(xq[292 * b:292 * (b + 1)].tobytes())
+            d = struct.unpack("<e", blk[0:2])[0]
+            dmin = struct.unpack("<e", blk[2:4])[0]
+            sumi = summ = 0
+            for j in range(8):
+                sc, m = oracle.q4k_scale_min(blk[4:16], j)
+                c, hi = divmod(j, 2)
+                dot = 0
+                for l in range(32):
+                    byte = blk[16 + 32 * c + l]
+                    qw = (byte >> 4) if hi else (byte & 15)
+                    dot += qw * qx[32 * j + l]
+                sumi += sc * dot
+                summ += m * (bs[2 * j] + bs[2 * j + 1])
+            tot += float(d) * dx * sumi - float(dmin) * dx * summ
+            wv = _naive_q4k_block(blk)
+            naive += sum(wv[i] * dx * qx[i] for i in range(256))
+        assert math.isclose(tot, y8[n], rel_tol=1e-12, abs_tol=1e-12 * c8[n])
+        assert math.isclose(naive, y8[n], rel_tol=1e-12, abs_tol=1e-12 * c8[n])
+
+
+def test_gemv_q8k_drift_within_stated_bound():
+    """|y_q8k - y_f32| <= sum over blocks of (sum |w| over the block) * |d|/2:
+    each activation moves by at most half a quantization step."""
+    K, N = 2048, 16
+    w = synth.q4k_matrix(N, K, seed=86)
+    x = synth.activations(1, K, seed=87)[0]
+    xq = oracle.quantize_q8_k(x)
+    y8, _ = oracle.gemv_q8k(Q4_K, w, N, K, xq)
+    y, _ = oracle.gemv(Q4_K, w, N, K, x)
+    W = np.abs(oracle.dequant_rows(Q4_K, w, N, K)).reshape(N, K // 256, 256).sum(axis=2)
+    dq = np.array([abs(struct.unpack("<f", xq[292 * b:292 * b + 4].tobytes())[0])
+                   for b in range(K // 256)])
+    bound = W @ (dq * (0.5 + 2.0 ** -20))
+    assert np.all(np.abs(y8 - y) <= bound)
+    assert np.any(np.abs(y8 - y) > 1e-3 * bound)  # the drift is real, not zero
