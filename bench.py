@@ -254,6 +254,32 @@ class Model:
             else:
                 q.gemv(md.h, xv[3], yv[6])
 
+    def q8k_step(self, which="all"):
+        """The decode step on the integer-dot variant: each distinct input
+        quantized to Q8_K once (qmm_quantize_q8_k), then qmm_gemv_q8k_group
+        (q/k/v, gate/up) and qmm_gemv_q8k (o, down).  which: 'all', 'short'
+        (the K=4096 launches with their quantizations) or 'long' (down)."""
+        import torch
+        q = self.q
+        if getattr(self, "xq", None) is None:
+            sizes = [4096, 4096, 4096, 14336]
+            self.xq = [[torch.empty(k // 256 * q.Q8_K_BLOCK, dtype=torch.uint8,
+                                    device=self.x_all.device) for k in sizes]
+                       for _ in self.layers]
+        for L, (mats, xv, yv) in enumerate(self.layers):
+            mq, mk, mv, mo, mg, mu, md = mats
+            xq = self.xq[L]
+            if which in ("all", "short"):
+                q.quantize_q8_k(xv[0], 4096, xq[0])
+                q.gemv_q8k_group([mq.h, mk.h, mv.h], xq[0], yv[0:3])
+                q.quantize_q8_k(xv[1], 4096, xq[1])
+                q.gemv_q8k(mo.h, xq[1], yv[3])
+                q.quantize_q8_k(xv[2], 4096, xq[2])
+                q.gemv_q8k_group([mg.h, mu.h], xq[2], yv[4:6])
+            if which in ("all", "long"):
+                q.quantize_q8_k(xv[3], 14336, xq[3])
+                q.gemv_q8k(md.h, xq[3], yv[6])
+
     def ffn_step(self, fused=True):
         """The dense SwiGLU FFN of every layer (gate, up, down): qmm_ffn_decode,
         or the grouped gate/up GEMV, qmm_swiglu and the down GEMV as separate

@@ -253,6 +253,48 @@ QMM_API qmm_status qmm_dequantize_bf16(qmm_t h, int64_t row0, int64_t nrows,
 QMM_API qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
                                     const float *x, float *y, qmm_stream stream);
 
+/* ---- The integer-dot variant (opt-in): Q8_K activations ----------------
+ * "Frink Inference: the Rust alternative to llama.cpp", section "Where
+ * llama.cpp is still ahead": llama.cpp quantizes the activations to Q8_K
+ * before a K-quant dot product, and its K-quant logits drift slightly from
+ * an engine that keeps f32 activations.  These calls are that path; the f32
+ * calls above stay the reference behaviour.
+ *
+ * Q8_K (GGUF; the pages name it only): 256 activations per 292-byte block,
+ * [binary32 d][256 x int8 q][16 x int16 bsums], bsums[g] = q[16g] + ... +
+ * q[16g+15].  max = the signed value of the first element of largest
+ * magnitude in the block; iscale = -127 / max; q = min(127,
+ * round-half-even(iscale * x)); d = 1 / iscale; all three steps in binary32
+ * (an all-zero block gives d = 0 and q = 0).  The block stands for d * q.
+ *
+ * Drift against the f32 path: every activation moves by at most |d|/2 (half
+ * a code step of its block), so |y_q8k - y_f32| <= sum over blocks b of
+ * (sum of |w| over block b) * |d_b| / 2, plus fp32 rounding. */
+
+/* Quantize K fp32 activations (K a positive multiple of 256) to K/256 Q8_K
+ * blocks at xq (K/256 * 292 bytes, device).  x 16-byte aligned, xq 4-byte
+ * aligned; both device pointers owned by the caller.  One launch; bitwise
+ * equal to the definition above.  Errors: QMM_ERR_NULL, QMM_ERR_SHAPE,
+ * QMM_ERR_ALIGN, QMM_ERR_CUDA; nothing is launched on an argument error. */
+QMM_API qmm_status qmm_quantize_q8_k(const float *x, int64_t K, void *xq, qmm_stream stream);
+
+/* y[n] = sum over super-blocks of d_w d_x * (integer dot of the 4-bit codes
+ * and the Q8_K codes, per sub-block times its 6-bit scale) - dmin d_x * (sum
+ * over sub-blocks of the 6-bit min times the sub-block's Q8_K code sum):
+ * exactly (up to fp32 rounding of the per-super-block scaling and the sum)
+ * sum_k w[n][k] * d q_k.  h: a Q4_K matrix (other formats:
+ * QMM_ERR_UNSUPPORTED); xq: K/256 Q8_K blocks as written by
+ * qmm_quantize_q8_k (device, 4-byte aligned); y: N fp32 (device, 4-byte
+ * aligned).  Each row is reduced inside one warp in a fixed order: bitwise
+ * repeatable.  No scratch, no allocation. */
+QMM_API qmm_status qmm_gemv_q8k(qmm_t h, const void *xq, float *y, qmm_stream stream);
+
+/* qmm_gemv_q8k for n <= 8 Q4_K matrices of one K sharing xq (the q/k/v or
+ * gate/up projections of a layer) in one launch; hs and ys are host arrays
+ * of n entries, ys[i] receives matrix i's outputs. */
+QMM_API qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq,
+                                      float *const *ys, qmm_stream stream);
+
 /* Read and clear the handle's device status word (synchronises the handle's
  * last stream first).  QMM_OK when no device-side fault was recorded. */
 QMM_API qmm_status qmm_get_status(qmm_t h);

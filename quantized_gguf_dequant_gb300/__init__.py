@@ -35,6 +35,7 @@ ENTRY_POINTS = (
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
     "qmm_gemv_noalloc", "qmm_gemm_group", "qmm_launch_count", "qmm_ffn_decode",
+    "qmm_quantize_q8_k", "qmm_gemv_q8k", "qmm_gemv_q8k_group",
 )
 
 
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
             "qmm_gemv_noalloc": [i32, i64, i64, vp, vp, vp, vp],
             "qmm_gemm_group": [ctypes.POINTER(vp), i32, vp, i64, ctypes.POINTER(vp), vp],
             "qmm_ffn_decode": [vp, vp, vp, vp, vp, vp, vp],
+            "qmm_quantize_q8_k": [vp, i64, vp, vp],
+            "qmm_gemv_q8k": [vp, vp, vp, vp],
+            "qmm_gemv_q8k_group": [ctypes.POINTER(vp), i32, vp, ctypes.POINTER(vp), vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -171,6 +175,26 @@ def moe_ffn(hg: int, hu: int, hd: int, n_experts: int, ids, T: int, top_k: int, 
     _check(lib().qmm_moe_ffn(ctypes.c_void_p(hg), ctypes.c_void_p(hu), ctypes.c_void_p(hd),
                              n_experts, _ptr(ids), T, top_k, _ptr(X), _ptr(route_w),
                              int(route_on_input), _ptr(Y), _stream(stream)))
+
+
+Q8_K_BLOCK = 292  # bytes per 256 activations in the Q8_K encoding
+
+
+def quantize_q8_k(x, K: int, xq, stream=None):
+    """qmm_quantize_q8_k: K fp32 activations -> K/256 Q8_K blocks in xq."""
+    _check(lib().qmm_quantize_q8_k(_ptr(x), K, _ptr(xq), _stream(stream)))
+
+
+def gemv_q8k(h: int, xq, y, stream=None):
+    """qmm_gemv_q8k: the integer-dot GEMV of a Q4_K matrix with Q8_K activations."""
+    _check(lib().qmm_gemv_q8k(ctypes.c_void_p(h), _ptr(xq), _ptr(y), _stream(stream)))
+
+
+def gemv_q8k_group(hs, xq, ys, stream=None):
+    n = len(hs)
+    harr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(h) for h in hs])
+    yarr = (ctypes.c_void_p * n)(*[_ptr(y) for y in ys])
+    _check(lib().qmm_gemv_q8k_group(harr, n, _ptr(xq), yarr, _stream(stream)))
 
 
 def gemm(h: int, X_bf16, M: int, Y, stream=None):

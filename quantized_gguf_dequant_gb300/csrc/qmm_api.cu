@@ -1095,4 +1095,80 @@ qmm_status qmm_get_status(qmm_t h)
     return QMM_OK;
 }
 
+qmm_status qmm_quantize_q8_k(const float *x, int64_t K, void *xq, qmm_stream stream)
+{
+    g_err.clear();
+    const char *fn = "qmm_quantize_q8_k";
+    if (!x || !xq)
+        return fail(QMM_ERR_NULL, "%s: %s is NULL", fn, !x ? "x" : "xq");
+    if (K < 256 || K % 256)
+        return fail(QMM_ERR_SHAPE, "%s: K = %lld; a positive multiple of 256 is required", fn,
+                    (long long)K);
+    if (K / 256 > (int64_t(1) << 30))
+        return fail(QMM_ERR_SHAPE, "%s: K = %lld is too large", fn, (long long)K);
+    if (!aligned(x, 16) || !aligned(xq, 4))
+        return fail(QMM_ERR_ALIGN, "%s: x must be 16-byte and xq 4-byte aligned", fn);
+    cudaError_t e = qmm::launch_quantize_q8k(x, K, static_cast<uint8_t *>(xq),
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    return QMM_OK;
+}
+
+qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float *const *ys,
+                              qmm_stream stream)
+{
+    g_err.clear();
+    const char *fn = "qmm_gemv_q8k_group";
+    if (!hs || !ys)
+        return fail(QMM_ERR_NULL, "%s: the %s array is NULL", fn, !hs ? "handle" : "output");
+    if (n < 1 || n > qmm::kMaxGroup)
+        return fail(QMM_ERR_SHAPE, "%s: n = %d; between 1 and %d matrices are supported", fn,
+                    int(n), qmm::kMaxGroup);
+    qmm::Q8kArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int i = 0; i < n; ++i) {
+        qmm_status st = check_handle(hs[i], fn);
+        if (st != QMM_OK)
+            return st;
+        const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
+        if (mi.fmt != QMM_Q4_K)
+            return fail(QMM_ERR_UNSUPPORTED,
+                        "%s: matrix %d has format %d; the integer-dot path takes Q4_K", fn, i,
+                        mi.fmt);
+        if (mi.K != reinterpret_cast<const Matrix *>(hs[0])->K)
+            return fail(QMM_ERR_SHAPE, "%s: matrix %d has K %lld, matrix 0 K %lld", fn, i,
+                        (long long)mi.K, (long long)reinterpret_cast<const Matrix *>(hs[0])->K);
+        if (!ys[i])
+            return fail(QMM_ERR_NULL, "%s: output %d is NULL", fn, i);
+        if (!aligned(ys[i], 4))
+            return fail(QMM_ERR_ALIGN, "%s: output %d is not 4-byte aligned", fn, i);
+        a.w[i] = mi.w;
+        a.y[i] = ys[i];
+        a.N[i] = mi.N;
+    }
+    if (!xq)
+        return fail(QMM_ERR_NULL, "%s: xq is NULL", fn);
+    if (!aligned(xq, 4))
+        return fail(QMM_ERR_ALIGN, "%s: xq is not 4-byte aligned", fn);
+    const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    if (qmm::q8k_smem(m0.K) > size_t(kMaxSmem))
+        return fail(QMM_ERR_SHAPE, "%s: K = %lld; its Q8_K activations (%zu bytes) exceed shared "
+                                   "memory", fn, (long long)m0.K, qmm::q8k_smem(m0.K));
+    a.nmat = n;
+    a.K = m0.K;
+    a.xq = static_cast<const uint8_t *>(xq);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = qmm::launch_gemv_q8k(a, m0.sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+    return QMM_OK;
+}
+
+qmm_status qmm_gemv_q8k(qmm_t h, const void *xq, float *y, qmm_stream stream)
+{
+    return qmm_gemv_q8k_group(&h, 1, xq, &y, stream);
+}
+
 } // extern "C"

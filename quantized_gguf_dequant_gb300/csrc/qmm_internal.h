@@ -288,6 +288,19 @@ cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, i
 cudaError_t launch_moe_combine(const float *ys, const float *r, const int32_t *ids, int E, int T,
                                int top_k, int64_t Ne, float *y, int sm_count, cudaStream_t s);
 
+// --------------------------------------------------------------- Q8_K integer-dot path
+struct Q8kArgs {
+    const uint8_t *w[kMaxGroup];  // Q4_K matrices sharing K
+    float *y[kMaxGroup];
+    int64_t N[kMaxGroup];
+    int nmat;
+    int64_t K;
+    const uint8_t *xq;            // Q8_K blocks of the activations (K/256 x 292 bytes)
+};
+size_t q8k_smem(int64_t K);
+cudaError_t launch_quantize_q8k(const float *x, int64_t K, uint8_t *out, cudaStream_t s);
+cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s);
+
 // --------------------------------------------------------------- no-allocation entry
 // Layout of qmm_gemv_noalloc's static scratch: [status word, padded to 256 B]
 // [tickets][split-K partial sums], 1 MiB in total.
