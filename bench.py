@@ -663,6 +663,21 @@ def run_ours(args, world, rank, local):
             "launches_per_step": launches_of(lambda: q4.step(False)),
             "frac_of_peak": step_bytes / (ms_u * 1e-3) / 1e9 / pk["hbm_gbs"]}
     if args.extras:
+        # The integer-dot variant on the same 32-layer step: every distinct
+        # input quantized to Q8_K once, then the integer GEMVs.
+        st_q = time_graph_stats(lambda: q4.q8k_step("all"), max(20, args.steps // 4), args.warmup,
+                                world)
+        ms_q = st_q["median_ms"]
+        extras["q4k_decode_q8k_integer"] = {
+            "value": step_bytes / (ms_q * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_q,
+            "min_ms": st_q["min_ms"], "reps": st_q["reps"],
+            "launches_per_step": launches_of(lambda: q4.q8k_step("all")),
+            "frac_of_peak": step_bytes / (ms_q * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "f32_over_q8k_time": ms / ms_q,
+            "note": "opt-in Q8_K activations + dp4a integer dot (qmm_quantize_q8_k, "
+                    "qmm_gemv_q8k[_group]); bytes counted as for the f32 step (weights once, "
+                    "f32 inputs once, outputs); drift vs f32 bounded by sum |w| |d|/2 per block"}
+    if args.extras:
         bm = BatchedModel(q4)
         sweep = {}
         for M in (1, 2, 4, 8, 16):

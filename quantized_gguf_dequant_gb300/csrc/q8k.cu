@@ -33,6 +33,7 @@
 // (from bsums) and d.
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 
 #include "qmm_device.cuh"
@@ -195,8 +196,47 @@ __device__ __forceinline__ float super_block_dot(const uint4 (&v)[9], const uint
 __global__ void __launch_bounds__(32 * kWarps) gemv_q8k_kernel(const __grid_constant__ Q8kParams P)
 {
     extern __shared__ __align__(16) uint8_t sx[];
-    pdl_wait();  // the Q8_K activations come from the quantize kernel
     pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = 1 << P.lshift;              // lanes per row
+    const int sub = lane >> P.lshift, li = lane & (L - 1);
+    const int64_t R = 32 >> P.lshift;         // rows per group
+    const int64_t nw = int64_t(gridDim.x) * kWarps;
+    const int spg = (P.NB + L - 1) / L;       // steps per group: lane li takes super-block li + L*step
+
+    // The warp walks (group, step) in order; the weights of the next
+    // position are loaded while the current one is computed.  The first
+    // loads go out before the wait for the previous kernel: the weights do
+    // not depend on it, the activations do.
+    auto row_of = [&](int64_t g, int &mi, int64_t &lr) -> bool {
+        const int64_t row = g * R + sub;
+        if (row >= P.N)
+            return false;
+        mi = 0;
+        while (row >= P.row_end[mi])
+            ++mi;
+        lr = row - (mi ? P.row_end[mi - 1] : 0);
+        return true;
+    };
+    auto load = [&](int64_t g, int st, uint4 (&v)[9]) {
+        int mi;
+        int64_t lr;
+        const int sb = li + L * st;
+        if (g < P.n_groups && sb < P.NB && row_of(g, mi, lr)) {
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(P.w[mi] + lr * P.row_bytes + int64_t(sb) * 144);
+#pragma unroll
+            for (int i = 0; i < 9; ++i)
+                v[i] = ldg_stream(src + i);
+        }
+    };
+
+    int64_t g = int64_t(blockIdx.x) * kWarps + warp;
+    int st = 0;
+    uint4 va[9], vb[9];
+    load(g, st, va);
+
+    pdl_wait();  // the Q8_K activations come from the quantize kernel
     // Stage the activations: codes (4-byte words), sub-block code sums, d.
     for (int i = threadIdx.x; i < P.NB * 64; i += blockDim.x) {
         const int b = i >> 6, j = i & 63;
@@ -213,34 +253,38 @@ __global__ void __launch_bounds__(32 * kWarps) gemv_q8k_kernel(const __grid_cons
             __ldg(reinterpret_cast<const float *>(P.xq + int64_t(b) * kQ8kBlock));
     __syncthreads();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = 1 << P.lshift;              // lanes per row
-    const int sub = lane >> P.lshift, li = lane & (L - 1);
-    const int64_t R = 32 >> P.lshift;         // rows per group
-    const int64_t nw = int64_t(gridDim.x) * kWarps;
-    for (int64_t g = int64_t(blockIdx.x) * kWarps + warp; g < P.n_groups; g += nw) {
-        const int64_t row = g * R + sub;
-        float acc = 0.f;
-        int mi = 0;
-        int64_t lr = row;
-        if (row < P.N) {
-            while (row >= P.row_end[mi])
-                ++mi;
-            lr = row - (mi ? P.row_end[mi - 1] : 0);
-            const uint8_t *wrow = P.w[mi] + lr * P.row_bytes;
-            for (int sb = li; sb < P.NB; sb += L) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(wrow + int64_t(sb) * 144);
-                uint4 v[9];
-#pragma unroll
-                for (int i = 0; i < 9; ++i)
-                    v[i] = ldg_stream(src + i);
-                acc += super_block_dot(v, sx + sb * kRec);
-            }
+    float acc = 0.f;
+    // One position: prefetch the next into `nxt`, add the current (`cur`),
+    // and at a group's last step reduce the row and store it.
+    auto step = [&](uint4 (&cur)[9], uint4 (&nxt)[9]) {
+        int64_t g2 = g;
+        int st2 = st + 1;
+        if (st2 == spg) {
+            st2 = 0;
+            g2 += nw;
         }
-        for (int o = L >> 1; o > 0; o >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (li == 0 && row < P.N)
-            P.y[mi][lr] = acc;
+        load(g2, st2, nxt);
+        const int sb = li + L * st;
+        int mi = 0;
+        int64_t lr = 0;
+        const bool have = row_of(g, mi, lr);
+        if (have && sb < P.NB)
+            acc += super_block_dot(cur, sx + sb * kRec);
+        if (st == spg - 1) {
+            for (int o = L >> 1; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (li == 0 && have)
+                P.y[mi][lr] = acc;
+            acc = 0.f;
+        }
+        g = g2;
+        st = st2;
+    };
+    while (g < P.n_groups) {
+        step(va, vb);
+        if (g >= P.n_groups)
+            break;
+        step(vb, va);
     }
 }
 
@@ -294,6 +338,8 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     for (int l = 0; l <= 5; ++l)
         if ((1 << l) == P.NB)
             lshift = l;
+    if (const char *e = getenv("QMM_Q8K_LSHIFT"))  // tuning override: log2(lanes per row)
+        lshift = std::min(5, std::max(0, atoi(e)));
     P.lshift = lshift;
     const int64_t R = 32 >> lshift;
     P.n_groups = (tot + R - 1) / R;
@@ -303,7 +349,10 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     if (e != cudaSuccess)
         return e;
     const int64_t want = (P.n_groups + kWarps - 1) / kWarps;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sm_count) * 4));
+    int64_t cap = int64_t(sm_count) * 2;
+    if (const char *e = getenv("QMM_Q8K_CTAS"))  // tuning override: grid cap
+        cap = std::max<int64_t>(1, atoll(e));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, cap));
     return launch_pdl(gemv_q8k_kernel, dim3(unsigned(grid)), dim3(32 * kWarps), smem, s, P);
 }
 
