@@ -41,7 +41,10 @@
  *   QMM_IQ4_NL 18 bytes / 32 weights: [fp16 d][16 bytes: weight l < 16 is the
  *             low nibble of byte l, weight 16+l its high nibble]; w = d*T[q]
  *             with GGUF's 16-entry IQ4_NL code book T.
- *   Every format needs K % 256 == 0 here.
+ *   K-quants need K % 256 == 0; Q8_0 and IQ4_NL take any K % 32 == 0 (rows
+ *   that are not whole 256-weight groups are only 2-byte aligned and go
+ *   through the per-group kernels: decode GEMV, batched GEMV, groups, block
+ *   decode, and for Q8_0 the no-allocation GEMV; the other calls refuse them).
  *   A matrix of N rows and K columns is N rows back to back, each row K/256
  *   (K-quants) or K/32 (Q8_0, IQ4_NL) blocks.  An expert-stacked tensor is n_experts such
  *   matrices back to back: row r of expert e is row e*N_e + r.
@@ -102,8 +105,8 @@ typedef void *qmm_stream; /* cudaStream_t */
 
 /* Describe a quantized matrix of N rows x K columns at w_dev (borrowed, not
  * copied).  Requires: fmt one of Q4_K, Q8_0, Q5_K, Q6_K, IQ4_NL; N >= 1;
- * K % 256 == 0 (every format in this version, so every row starts 16-byte
- * aligned); w_dev 16-byte aligned.  Allocates the handle's workspace and
+ * K % 256 == 0 for the K-quants, K % 32 == 0 for Q8_0 and IQ4_NL;
+ * K <= 2^20; w_dev 16-byte aligned.  Allocates the handle's workspace and
  * status word on the current device.  On success *out is a new handle. */
 QMM_API qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
                       qmm_t *out);

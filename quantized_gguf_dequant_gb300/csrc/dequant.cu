@@ -74,7 +74,7 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ w, int64_t K, int64_t
 cudaError_t launch_dequant(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,
                            uint16_t *out_bf16, cudaStream_t s)
 {
-    if (is_extra_format(m.fmt))
+    if (uses_fmt_kernels(m))
         return launch_dequant_fmt(m, row0, nrows, out_f32, out_bf16, s);
     const int64_t total = nrows * (m.K / 32);
     const int threads = 256;

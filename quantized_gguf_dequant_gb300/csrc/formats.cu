@@ -132,12 +132,18 @@ bool is_extra_format(int f)
     return f == fmt::kQ5K || f == fmt::kQ6K || f == fmt::kIQ4NL;
 }
 
+bool uses_fmt_kernels(const Matrix &m)
+{
+    return is_extra_format(m.fmt) || (m.fmt == fmt::kQ80 && m.K % 256 != 0);
+}
+
 cudaError_t launch_gemv_fmt(const Matrix &m, const float *X, int M, int64_t ldx, float *Y,
                             int64_t ldy, cudaStream_t s)
 {
     switch (m.fmt) {
     case fmt::kQ5K: return launch_gemv_fmt_t<fmt::kQ5K>(m, X, M, ldx, Y, ldy, s);
     case fmt::kQ6K: return launch_gemv_fmt_t<fmt::kQ6K>(m, X, M, ldx, Y, ldy, s);
+    case fmt::kQ80: return launch_gemv_fmt_t<fmt::kQ80>(m, X, M, ldx, Y, ldy, s);
     default: return launch_gemv_fmt_t<fmt::kIQ4NL>(m, X, M, ldx, Y, ldy, s);
     }
 }
@@ -149,6 +155,7 @@ cudaError_t launch_dequant_fmt(const Matrix &m, int64_t row0, int64_t nrows, flo
     switch (m.fmt) {
     case fmt::kQ5K: return launch_dequant_fmt_t<fmt::kQ5K>(m, row0, nrows, out_f32, ob, s);
     case fmt::kQ6K: return launch_dequant_fmt_t<fmt::kQ6K>(m, row0, nrows, out_f32, ob, s);
+    case fmt::kQ80: return launch_dequant_fmt_t<fmt::kQ80>(m, row0, nrows, out_f32, ob, s);
     default: return launch_dequant_fmt_t<fmt::kIQ4NL>(m, row0, nrows, out_f32, ob, s);
     }
 }

@@ -19,8 +19,11 @@
 //   IQ4_NL, 18 bytes / 32 weights: [fp16 d][16 bytes]; weight l < 16 is the
 //     low nibble of byte l, weight 16+l the high nibble; w = d*book[code],
 //     exact (11 + 8 bits).
+//   Q8_0, 34 bytes / 32 weights: [fp16 d][32 x int8]; w = d*q, exact.  Taken
+//     here only for rows whose K is a multiple of 32 but not of 256 (the
+//     other Q8_0 kernels take rows in whole 256-weight groups).
 // Rows are whole blocks back to back; blocks are only 2-byte aligned (Q6_K,
-// IQ4_NL), so the decoders read bytes.
+// IQ4_NL, Q8_0), so the decoders read bytes.
 #pragma once
 
 #include <cstdint>
@@ -32,12 +35,13 @@
 namespace qmm {
 namespace fmt {
 
-constexpr int kQ5K = 13, kQ6K = 14, kIQ4NL = 20;
+constexpr int kQ80 = 8, kQ5K = 13, kQ6K = 14, kIQ4NL = 20;
 
 template <int F> struct Block;
 template <> struct Block<kQ5K> { static constexpr int bytes = 176, weights = 256; };
 template <> struct Block<kQ6K> { static constexpr int bytes = 210, weights = 256; };
 template <> struct Block<kIQ4NL> { static constexpr int bytes = 18, weights = 32; };
+template <> struct Block<kQ80> { static constexpr int bytes = 34, weights = 32; };
 
 // The IQ4_NL code book: the value of each 4-bit code before the block scale
 // (GGUF IQ4_NL format definition).
@@ -90,6 +94,12 @@ __device__ __forceinline__ void decode_group(const uint8_t *row, int64_t g, floa
             const int q = ((ql[l] >> lshift) & 15) | (((qh[l] >> (2 * t)) & 3) << 4);
             v[l] = (l < 16 ? s0 : s1) * float(q - 32);
         }
+    } else if constexpr (F == kQ80) {
+        const uint8_t *blk = row + g * 34;
+        const float d = half_bytes(blk);
+#pragma unroll
+        for (int l = 0; l < 32; ++l)
+            v[l] = d * float(int8_t(blk[2 + l]));
     } else {
         const uint8_t *blk = row + g * 18;
         const float d = half_bytes(blk);

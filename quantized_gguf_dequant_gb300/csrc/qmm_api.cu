@@ -215,7 +215,7 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
-    if (qmm::is_extra_format(m0.fmt)) {
+    if (qmm::uses_fmt_kernels(m0)) {
         for (int i = 0; i < n; ++i) {
             const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
             cudaError_t e = qmm::launch_gemv_fmt(mi, x, 1, mi.K, ys[i], mi.N, s);
@@ -400,10 +400,11 @@ qmm_status noalloc_check(int fmt, int64_t N, int64_t K, const void *w, const flo
     if (N < 1)
         return fail(QMM_ERR_SHAPE, "qmm_gemv_noalloc: N = %lld rows; at least one row is needed",
                     (long long)N);
-    if (K < 256 || K % 256 != 0 || K > (int64_t(1) << 20))
+    const int64_t kb = fmt == QMM_Q8_0 ? 32 : 256;
+    if (K < kb || K % kb != 0 || K > (int64_t(1) << 20))
         return fail(QMM_ERR_SHAPE,
-                    "qmm_gemv_noalloc: K = %lld is not a multiple of 256 in [256, 1048576]",
-                    (long long)K);
+                    "qmm_gemv_noalloc: K = %lld is not a multiple of %lld in [%lld, 1048576]",
+                    (long long)K, (long long)kb, (long long)kb);
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_noalloc: the weights and x must be 16-byte aligned "
                                    "and y 4-byte aligned");
@@ -435,13 +436,13 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
     if (N < 1)
         return fail(QMM_ERR_SHAPE, "qmm_create: N = %lld rows; at least one row is needed",
                     (long long)N);
-    if (K < 256 || K % 256 != 0)
+    const bool block32 = fmt == QMM_Q8_0 || fmt == QMM_IQ4_NL;
+    if (block32 ? (K < 32 || K % 32 != 0) : (K < 256 || K % 256 != 0))
         return fail(QMM_ERR_SHAPE,
-                    (fmt == QMM_Q8_0 || fmt == QMM_IQ4_NL)
-                        ? "qmm_create: K = %lld is not a positive multiple of 256 (rows of "
-                          "32-weight blocks are taken in whole 256-weight groups here)"
-                        : "qmm_create: K = %lld is not a positive multiple of 256 (a K-quant "
-                          "super-block holds 256 weights)",
+                    block32 ? "qmm_create: K = %lld is not a positive multiple of 32 (a block "
+                              "holds 32 weights)"
+                            : "qmm_create: K = %lld is not a positive multiple of 256 (a K-quant "
+                              "super-block holds 256 weights)",
                     (long long)K);
     if (K > (int64_t(1) << 20))
         return fail(QMM_ERR_SHAPE, "qmm_create: K = %lld exceeds the supported maximum 1048576",
@@ -614,7 +615,7 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     if (!aligned(Y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (qmm::is_extra_format(m.fmt)) {
+    if (qmm::uses_fmt_kernels(m)) {
         cudaError_t e = qmm::launch_gemv_fmt(m, X, int(M), ldx, Y, ldy, s);
         if (e != cudaSuccess)
             return cuda_fail(e, "qmm_gemv_batched");

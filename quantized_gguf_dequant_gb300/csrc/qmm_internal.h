@@ -68,6 +68,9 @@ inline int64_t row_bytes_of(int fmt, int64_t K)
 // for 1..16 activation rows (X rows ldx apart, Y rows ldy apart) and block
 // decode to fp32 or bf16 (exactly one of out_f32 / out_bf16).
 bool is_extra_format(int fmt);
+// Matrices that take the per-group kernels of formats.cu: the further formats,
+// and Q8_0 rows whose K is a multiple of 32 but not of 256.
+bool uses_fmt_kernels(const Matrix &m);
 cudaError_t launch_gemv_fmt(const Matrix &m, const float *X, int M, int64_t ldx, float *Y,
                             int64_t ldy, cudaStream_t s);
 cudaError_t launch_dequant_fmt(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,

@@ -43,6 +43,22 @@ qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_
     if (e != cudaSuccess)
         return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: cudaGetDevice failed: %s",
                                  cudaGetErrorString(e));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fmt == QMM_Q8_0 && K % 256 != 0) {
+        // Rows of whole 32-weight blocks that are not whole 256-weight groups:
+        // the per-group kernel, one warp per row, no scratch at all.
+        qmm::Matrix m;
+        m.fmt = fmt;
+        m.N = N;
+        m.K = K;
+        m.row_bytes = qmm::row_bytes_of(fmt, K);
+        m.w = static_cast<const uint8_t *>(w_dev);
+        e = qmm::launch_gemv_fmt(m, x, 1, K, y, N, s);
+        if (e != cudaSuccess)
+            return qmm::noalloc_fail(QMM_ERR_CUDA, "qmm_gemv_noalloc: launch failed: %s",
+                                     cudaGetErrorString(e));
+        return QMM_OK;
+    }
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
@@ -62,7 +78,6 @@ qmm_status qmm_gemv_noalloc(qmm_format fmt, int64_t N, int64_t K, const void *w_
                                  "qmm_gemv_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
                                  cudaGetErrorString(e));
     unsigned char *b = static_cast<unsigned char *>(base);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The tickets must start at zero.  A completed call leaves them zero, but
     // a call that timed out may not, so clear them (and the status word) on
     // the stream first -- a memset, not an allocation.

@@ -111,10 +111,55 @@ def test_q4k_only_calls_refuse():
     m.close()
 
 
+@pytest.mark.parametrize("fmt", [q.Q8_0, q.IQ4_NL])
+@pytest.mark.parametrize("N,K", [(37, 32), (300, 4128), (77, 96), (5, 14368)])
+def test_block32_formats_with_k_not_a_multiple_of_256(fmt, N, K):
+    """32-weight-block formats take any K that fills whole blocks: rows are
+    then only 2-byte aligned, and the per-group kernels read them bytewise.
+    GEMV, batched GEMV, a group of two, decode and bf16 decode."""
+    w, m = _matrix(fmt, N, K, seed=N + K + fmt)
+    X = synth.activations(3, K, seed=K + 2)
+    yr, c = oracle.gemv(fmt, w, N, K, X, nthreads=NT)
+    y = m.gemv(to_dev(X[0])).cpu().numpy()
+    assert_close_to_oracle(y, yr[0], c[0], TOL_FP32, f"gemv fmt={fmt} K={K}")
+    Y = torch.full((3, N), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_batched(m.h, to_dev(X), 3, K, Y, N)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(Y.cpu().numpy(), yr, c, TOL_FP32, f"batched fmt={fmt} K={K}")
+    w2, m2 = _matrix(fmt, 11, K, seed=N + K + fmt + 1)
+    y1 = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    y2 = torch.full((11,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_group([m.h, m2.h], to_dev(X[1]), [y1, y2])
+    torch.cuda.synchronize()
+    assert_close_to_oracle(y1.cpu().numpy(), yr[1], c[1], TOL_FP32, "group 0")
+    yr2, c2 = oracle.gemv(fmt, w2, 11, K, X[1], nthreads=NT)
+    assert_close_to_oracle(y2.cpu().numpy(), yr2, c2, TOL_FP32, "group 1")
+    ref = oracle.dequant_rows(fmt, w, N, K).astype(np.float32)
+    got = m.dequantize().cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    assert m.status() == 0
+    m.close()
+    m2.close()
+
+
+def test_q8_0_noalloc_with_k_not_a_multiple_of_256():
+    N, K = 300, 4128
+    w = synth.matrix(q.Q8_0, N, K, seed=17)
+    x = synth.activations(1, K, seed=18)[0]
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_noalloc(q.Q8_0, N, K, to_dev(w), to_dev(x), y)
+    torch.cuda.synchronize()
+    yr, c = oracle.gemv(q.Q8_0, w, N, K, x, nthreads=NT)
+    assert_close_to_oracle(y.cpu().numpy(), yr, c, TOL_FP32, "noalloc Q8_0 K=4128")
+
+
 def test_create_refusals():
     w = torch.zeros(1000, dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QmmError) as ei:
         q.Matrix(q.Q6_K, 1, 100, w)  # K not a multiple of 256
+    assert ei.value.status == q.ERR_SHAPE
+    with pytest.raises(q.QmmError) as ei:
+        q.Matrix(q.Q8_0, 1, 100, w)  # K not a multiple of 32
     assert ei.value.status == q.ERR_SHAPE
     with pytest.raises(q.QmmError) as ei:
         q.Matrix(15, 1, 256, w)  # Q8_K: not a weight format here
