@@ -841,8 +841,9 @@ def run_ours(args, world, rank, local):
                 pass
         extras["extra_formats_decode"] = dict(
             fx, unit="GB/s",
-            note="Llama-3.1-8B decode step, 4 layers, the weights in each further format; the "
-                 "first, plain GEMV of these formats (one warp per row)")
+            note="Llama-3.1-8B decode step, 4 layers, the weights in each further format, "
+                 "through the SIMT formats GEMV (a warp owns rows, a lane one 256-weight unit, "
+                 "activations in shared memory)")
 
     # Every launch of the step is the one-row decode kernel, so its average
     # launch is the step's: algorithmic bytes per launch = step bytes / launches,

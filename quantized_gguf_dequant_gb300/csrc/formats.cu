@@ -12,8 +12,10 @@
 // GEMV: one warp per output row; lane l decodes the row's 32-weight groups
 // l, l+32, ... in registers and multiplies each by the M activation rows
 // (M <= 16), accumulating in fp32; the lanes are then added by a fixed
-// shuffle tree, so results are bitwise repeatable.  A first, plain design:
-// correctness and the format coverage come first, the bandwidth later.
+// shuffle tree, so results are bitwise repeatable.  A plain design that reads
+// bytes: it takes what the fast kernel of formats_fast.cu does not (Q8_0 and
+// IQ4_NL rows whose K is not a multiple of 256, activations that do not fit
+// shared memory) and is kept as the simple second implementation.
 #include "formats.cuh"
 #include "qmm_device.cuh"
 #include "qmm_internal.h"

@@ -215,6 +215,16 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    if (qmm::fmt_fast_rows(m0, 1) > 0) {
+        const Matrix *ms[qmm::kMaxGroup];
+        for (int i = 0; i < n; ++i)
+            ms[i] = reinterpret_cast<const Matrix *>(hs[i]);
+        cudaError_t e = qmm::launch_gemv_fmt_fast(ms, n, x, m0.K, 1, ys, 0, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, fn);
+        reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+        return QMM_OK;
+    }
     if (qmm::uses_fmt_kernels(m0)) {
         for (int i = 0; i < n; ++i) {
             const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
@@ -615,6 +625,14 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     if (!aligned(Y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (qmm::fmt_fast_rows(m, int(M)) > 0) {
+        const Matrix *mp = &m;
+        cudaError_t e = qmm::launch_gemv_fmt_fast(&mp, 1, X, ldx, int(M), &Y, ldy, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "qmm_gemv_batched");
+        reinterpret_cast<Matrix *>(h)->last_stream = s;
+        return QMM_OK;
+    }
     if (qmm::uses_fmt_kernels(m)) {
         cudaError_t e = qmm::launch_gemv_fmt(m, X, int(M), ldx, Y, ldy, s);
         if (e != cudaSuccess)

@@ -71,6 +71,17 @@ bool is_extra_format(int fmt);
 // Matrices that take the per-group kernels of formats.cu: the further formats,
 // and Q8_0 rows whose K is a multiple of 32 but not of 256.
 bool uses_fmt_kernels(const Matrix &m);
+// Decode GEMV of Q5_K / Q6_K / IQ4_NL (K % 256 == 0) at memory speed
+// (formats_fast.cu).
+// Rows of activations per pass of the fast kernel for M rows (4, 2 or 1), or
+// 0 when it does not take the matrix (format, K, shared memory).
+int fmt_fast_rows(const Matrix &m, int M);
+size_t fmt_fast_smem(int fmt, int64_t K, int MR);
+// n matrices (n > 1 only with M == 1) sharing the M activation rows (ldx
+// apart); matrix i's outputs at ys[i], rows ldy apart.  Every output row is
+// bitwise the same as from a one-row call.
+cudaError_t launch_gemv_fmt_fast(const Matrix *const *ms, int n, const float *x, int64_t ldx,
+                                 int M, float *const *ys, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemv_fmt(const Matrix &m, const float *X, int M, int64_t ldx, float *Y,
                             int64_t ldy, cudaStream_t s);
 cudaError_t launch_dequant_fmt(const Matrix &m, int64_t row0, int64_t nrows, float *out_f32,

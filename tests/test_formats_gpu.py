@@ -41,9 +41,15 @@ def test_dequant_bit_exact(fmt):
     m.close()
 
 
+@pytest.mark.parametrize("path", ["fast", "plain"])
 @pytest.mark.parametrize("fmt", FORMATS)
-@pytest.mark.parametrize("N,K", [(1, 256), (9, 512), (300, 2048), (4096, 4096)])
-def test_gemv(fmt, N, K):
+@pytest.mark.parametrize("N,K", [(1, 256), (9, 512), (300, 2048), (4096, 4096), (33, 768),
+                                 (77, 14336), (5, 8192)])
+def test_gemv(monkeypatch, path, fmt, N, K):
+    """The one-row GEMV: the fast kernel (16-byte or 4-byte loads straight to
+    registers; 1, 2, 3, 16, 32 and 56 units per row) and the plain one."""
+    if path == "plain":
+        monkeypatch.setenv("QMM_FMT_PATH", "plain")
     w, m = _matrix(fmt, N, K, seed=N + K + fmt)
     x = synth.activations(1, K, seed=K + 1)[0]
     y = m.gemv(to_dev(x)).cpu().numpy()
@@ -164,3 +170,25 @@ def test_create_refusals():
     with pytest.raises(q.QmmError) as ei:
         q.Matrix(15, 1, 256, w)  # Q8_K: not a weight format here
     assert ei.value.status == q.ERR_FORMAT
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_gemv_group_fast(fmt):
+    """q/k/v-like group of three matrices sharing x in one fast launch, and
+    the result bitwise equal on a second call."""
+    K = 2048
+    Ns = [512, 128, 128]
+    ws, ms = zip(*[_matrix(fmt, N, K, seed=50 + i + fmt) for i, N in enumerate(Ns)])
+    x = synth.activations(1, K, seed=60)[0]
+    outs = []
+    for _ in range(2):
+        ys = [torch.full((N,), float("nan"), dtype=torch.float32, device="cuda") for N in Ns]
+        q.gemv_group([m.h for m in ms], to_dev(x), ys)
+        torch.cuda.synchronize()
+        outs.append([y.cpu().numpy() for y in ys])
+    for i, (N, w) in enumerate(zip(Ns, ws)):
+        yr, c = oracle.gemv(fmt, w, N, K, x, nthreads=NT)
+        assert_close_to_oracle(outs[0][i], yr, c, TOL_FP32, f"group {i}")
+        assert np.array_equal(outs[0][i].view(np.uint32), outs[1][i].view(np.uint32))
+    for m in ms:
+        m.close()
