@@ -73,6 +73,7 @@ def lib():
         L.or_dequant_rows.argtypes = [i32, vp, i64, i64, i64, i64, vp]
         L.or_gemv.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp, vp, i32]
         L.or_gemm_bf16.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, vp, i32]
+        L.or_gemm_bf16_fmt.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp, vp, i32]
         L.or_bf16_from_float.argtypes = [ctypes.c_float]
         L.or_bf16_from_float.restype = ctypes.c_uint16
         L.or_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -192,11 +193,11 @@ def gemv(fmt: int, w: np.ndarray, N: int, K: int, X: np.ndarray,
 
 
 def gemm_bf16(w: np.ndarray, N: int, K: int, Xbf16: np.ndarray,
-              rows=None, nthreads: int = 1):
+              rows=None, nthreads: int = 1, fmt: int = Q4_K):
     """Prefill product with bf16 weights bf16(RN_fp32(w)) and bf16 X.
 
     Xbf16 holds bfloat16 bit patterns (uint16) [M, K].  Returns (Y, C), each
-    [M, nrows]; C is taken with the exact weights.
+    [M, nrows]; C is taken with the exact weights.  w is in format fmt.
     """
     w = np.ascontiguousarray(w, dtype=np.uint8)
     X = np.ascontiguousarray(np.atleast_2d(Xbf16), dtype=np.uint16)
@@ -210,9 +211,9 @@ def gemm_bf16(w: np.ndarray, N: int, K: int, Xbf16: np.ndarray,
         nrows = rows_a.size
     Y = np.empty((M, nrows), np.float64)
     C = np.empty((M, nrows), np.float64)
-    _check(lib().or_gemm_bf16(_p(w), N, K, _p(X), M, K,
-                              None if rows_a is None else _p(rows_a), nrows,
-                              _p(Y), _p(C), int(nthreads)), "gemm_bf16")
+    _check(lib().or_gemm_bf16_fmt(fmt, _p(w), N, K, _p(X), M, K,
+                                  None if rows_a is None else _p(rows_a), nrows,
+                                  _p(Y), _p(C), int(nthreads)), "gemm_bf16")
     return Y, C
 
 

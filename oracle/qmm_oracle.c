@@ -370,17 +370,18 @@ double or_bf16_to_double(uint16_t b)
     return (double)f;
 }
 
-/* The prefill product with bf16 operands.  Each weight is taken as
- * bf16(RN_fp32(w)): the exact value rounded to fp32, then to bf16.  X is M
+/* The prefill product with bf16 operands, for any weight format.  Each
+ * weight is taken as bf16(RN_fp32(w)): the exact value rounded to fp32, then
+ * to bf16.  X is M
  * rows of K bfloat16 patterns (leading dimension ldx).  Then
  *   Y[m*nrows + i] = sum_k w_bf16[rows[i]][k] * x_bf16[m][k]   (fp64)
  *   C[m*nrows + i] = sum_k |w[rows[i]][k] * x_bf16[m][k]|  (exact w)  */
-int or_gemm_bf16(const uint8_t *w, int64_t N, int64_t K,
-                 const uint16_t *X, int64_t M, int64_t ldx,
-                 const int64_t *rows, int64_t nrows,
-                 double *Y, double *C, int nthreads)
+int or_gemm_bf16_fmt(int fmt, const uint8_t *w, int64_t N, int64_t K,
+                     const uint16_t *X, int64_t M, int64_t ldx,
+                     const int64_t *rows, int64_t nrows,
+                     double *Y, double *C, int nthreads)
 {
-    int64_t rb = or_row_bytes(OR_Q4_K, K);
+    int64_t rb = or_row_bytes(fmt, K);
     if (!w || !X || !Y || rb < 0 || N <= 0 || M <= 0 || ldx < K || nrows < 0)
         return -1;
     for (int64_t i = 0; i < nrows; ++i) {
@@ -408,7 +409,7 @@ int or_gemm_bf16(const uint8_t *w, int64_t N, int64_t K,
 #endif
             for (int64_t i = 0; i < nrows; ++i) {
                 int64_t r = rows ? rows[i] : i;
-                dequant_row(OR_Q4_K, w, K, rb, r, wr);
+                dequant_row(fmt, w, K, rb, r, wr);
                 for (int64_t k = 0; k < K; ++k)
                     wb[k] = or_bf16_to_double(or_bf16_from_float((float)wr[k]));
                 for (int64_t m = 0; m < M; ++m) {
@@ -428,6 +429,15 @@ int or_gemm_bf16(const uint8_t *w, int64_t N, int64_t K,
         }
     }
     return bad ? -3 : 0;
+}
+
+/* The Q4_K prefill product (or_gemm_bf16_fmt for Q4_K). */
+int or_gemm_bf16(const uint8_t *w, int64_t N, int64_t K,
+                 const uint16_t *X, int64_t M, int64_t ldx,
+                 const int64_t *rows, int64_t nrows,
+                 double *Y, double *C, int nthreads)
+{
+    return or_gemm_bf16_fmt(OR_Q4_K, w, N, K, X, M, ldx, rows, nrows, Y, C, nthreads);
 }
 
 /* SwiGLU between the gate and up projections of an expert FFN:

@@ -326,6 +326,37 @@ def test_gemm_bf16_identity_and_rounding():
     assert np.allclose(Y, xd @ Wb.T, rtol=1e-13, atol=1e-13)
 
 
+def test_gemm_bf16_q8_0_identity_and_hand_values():
+    """Q8_0 weights d*q are exact in fp32 (11 x 8 bits); the prefill takes
+    them rounded to bf16: 0.1 (fp16 0x2e66) * 127 = 12.6968994140625 rounds
+    to 12.6875 in bf16, 0.1 * -3 = -0.2999267578125 to -0.30078125."""
+    import torch
+    N, K = 3, 256
+    rows = []
+    for n in range(N):
+        blocks = []
+        for b in range(K // 32):
+            q = np.zeros(32, np.int8)
+            q[(5 * b + n) % 32] = 127
+            q[(5 * b + n + 1) % 32] = -3
+            blocks.append(struct.pack("<H", 0x2E66) + q.tobytes())
+        rows.append(b"".join(blocks))
+    w = np.frombuffer(b"".join(rows), np.uint8).copy()
+    k0 = 5 * 0 + 0  # row 0, block 0: q[0] = 127, q[1] = -3
+    X = np.zeros((2, K), np.uint16)
+    X[0, k0] = 0x3F80
+    X[1, k0 + 1] = 0x3F80
+    Y, C = oracle.gemm_bf16(w, N, K, X, fmt=Q8_0)
+    assert Y[0, 0] == 12.6875 and Y[1, 0] == -0.30078125
+    assert C[0, 0] == 0.0999755859375 * 127
+    W = oracle.dequant_rows(Q8_0, w, N, K)
+    Wb = torch.from_numpy(W.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    Xr = synth.activations_bf16(3, K, seed=53)
+    Y, _ = oracle.gemm_bf16(w, N, K, Xr, fmt=Q8_0)
+    xd = torch.from_numpy(Xr.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.allclose(Y, xd @ Wb.T, rtol=1e-13, atol=1e-13)
+
+
 # ------------------------------------------------------------------ SwiGLU / experts
 
 def test_swiglu_closed_forms():
