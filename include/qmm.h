@@ -204,18 +204,19 @@ QMM_API qmm_status qmm_ffn_decode(qmm_t hg, qmm_t hu, qmm_t hd, const float *x, 
 /* Prefill GEMM on the tensor cores -- prompt processing, the one phase
  * where the pages' CUDA engine trails most ("Frink Inference: the Rust
  * alternative to llama.cpp", "Where llama.cpp is still ahead": prefill 25x
- * to 43x slower on CUDA; a tensor-core GEMM as the newer work).  Q4_K only
- * in this version:
+ * to 43x slower on CUDA; a tensor-core GEMM as the newer work).  Q4_K, and
+ * Q8_0 with K % 256 == 0 (other formats: QMM_ERR_UNSUPPORTED):
  * Y[m*N + n] = sum_k bf16(w[n][k]) * X[m*K + k], fp32 accumulation, where
  * bf16(w) rounds the exact weight to fp32 and then to bf16 (nearest even).
  * X: [M, K] bfloat16 bit patterns, 16-byte aligned; Y: [M, N] fp32.
- * M >= 1. */
+ * 1 <= M <= 2^24.  Results are bitwise repeatable (a split of K is added in
+ * slice order). */
 QMM_API qmm_status qmm_gemm(qmm_t h, const uint16_t *X_bf16, int64_t M, float *Y,
                     qmm_stream stream);
 
 /* qmm_gemm for n matrices that share X (the q/k/v or gate/up projections of
- * a layer's prefill) in one launch: Ys[i] is [M, N_i].  All n handles are
- * Q4_K with the same K, n <= 4; hs and Ys are host arrays of n entries.  The
+ * a layer's prefill) in one launch: Ys[i] is [M, N_i].  All n handles have
+ * the same format (Q4_K, or Q8_0 as above) and K, n <= 4; hs and Ys are host arrays of n entries.  The
  * split-K scratch of hs[0] is used. */
 QMM_API qmm_status qmm_gemm_group(const qmm_t *hs, int32_t n, const uint16_t *X_bf16, int64_t M,
                                   float *const *Ys, qmm_stream stream);

@@ -1,4 +1,4 @@
-// gemm_tc.cu -- Q4_K prefill GEMM on the 5th-generation tensor cores
+// gemm_tc.cu -- Q4_K and Q8_0 prefill GEMM on the 5th-generation tensor cores
 // (tcgen05.mma with the accumulators in tensor memory), dequantising the
 // weights into shared memory on the way.
 //
@@ -65,14 +65,22 @@ constexpr int kMaxKSplit = 16;
 // Token tiles of 256 (two MMAs of M = 128 per K step into both 256-column
 // TMEM accumulators) or of 128 (one MMA, one accumulator) for problems whose
 // 256-token tiles would not fill the SMs.  Three stages either way.
-template <int TOK>
+// Weight bytes staged per 64-weight K step and 256 rows: Q4_K the chunk's 32
+// nibble bytes (its 16-byte header separately, once per super-block); Q8_0
+// the chunk's two 34-byte blocks, fetched as the 80-byte window that starts
+// at the 16-byte boundary at or below them (a TMA box must start there).
+constexpr int kQ80Window = 80;
+template <int FMT> constexpr int kRawBytes = FMT == QMM_Q4_K ? kNibBytes : kRows * kQ80Window;
+
+template <int TOK, int FMT>
 struct TileCfg {
     static constexpr int kTok = TOK;
     static constexpr int kHalves = TOK / 128;           // MMAs of M = 128 per K step
-    static constexpr int kStages = 3;
+    // Q8_0's larger windows leave room for two 256-token stages only
+    static constexpr int kStages = (FMT == QMM_Q8_0 && TOK == 256) ? 2 : 3;
     static constexpr int kABytes = TOK * 128;
     static constexpr uint32_t kTmemCols = uint32_t(kHalves) * 256;
-    static constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kNibBytes;
+    static constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kRawBytes<FMT>;
     static constexpr size_t kSmemBytes =
         1024 /* alignment slack */ + size_t(kStages) * kStageBytes + size_t(kHdrSlots) * kHdrBytes + 256;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
@@ -87,7 +95,7 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kRows
 struct GemmParams {
     CUtensorMap tm_x;                   // X [M][K] bf16, box 64 x 256, 128-byte swizzle
     CUtensorMap tm_hdr[kGemmMaxGroup];  // weight bytes [N_i][row_bytes] u8, box 16 x 256
-    CUtensorMap tm_nib[kGemmMaxGroup];  // weight bytes, box 32 x 256
+    CUtensorMap tm_nib[kGemmMaxGroup];  // weight bytes, box 32 x 256 (Q8_0: 80 x 256)
     float *y[kGemmMaxGroup];            // [M][N_i]
     int n_rows[kGemmMaxGroup];          // N_i
     int rt_end[kGemmMaxGroup];          // cumulative 256-row tiles
@@ -237,10 +245,26 @@ __device__ __forceinline__ void dequant4(uint32_t v, float as, float b, uint32_t
     p1 = cvt_bf16x2(f1.x, f1.y);
 }
 
-template <int TOK>
+// Four Q8_0 weights (int8 bytes of v) as two bf16 pairs of RN(d*q); d*q is
+// exact in fp32.
+__device__ __forceinline__ void dequant4_q8(uint32_t v, float d, uint32_t &p0, uint32_t &p1)
+{
+    const float2 off = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
+    const float2 D = make_float2(d, d);
+    const uint32_t u = v ^ 0x80808080u;  // q + 128 in each byte
+    float2 f0 = make_float2(byte_magic(u, 0), byte_magic(u, 1));
+    float2 f1 = make_float2(byte_magic(u, 2), byte_magic(u, 3));
+    f0 = __fmul2_rn(__fadd2_rn(f0, off), D);
+    f1 = __fmul2_rn(__fadd2_rn(f1, off), D);
+    p0 = cvt_bf16x2(f0.x, f0.y);
+    p1 = cvt_bf16x2(f1.x, f1.y);
+}
+
+template <int TOK, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_constant__ GemmParams P)
 {
-    using C = TileCfg<TOK>;
+    using C = TileCfg<TOK, FMT>;
+    constexpr int kRaw = kRawBytes<FMT>;
     constexpr int kTok = C::kTok, kStages = C::kStages, kABytes = C::kABytes;
     constexpr uint32_t kTmemCols = C::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
@@ -248,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
     uint8_t *sA = base;                                  // [kStages][TOK x 128 B]
     uint8_t *sB = sA + kStages * kABytes;                // [kStages][32 KB]
-    uint8_t *sNib = sB + kStages * kBBytes;              // [kStages][8 KB]
-    uint8_t *sHdr = sNib + kStages * kNibBytes;          // [kHdrSlots][4 KB]
+    uint8_t *sNib = sB + kStages * kBBytes;              // [kStages][kRaw]
+    uint8_t *sHdr = sNib + kStages * kRaw;               // [kHdrSlots][4 KB]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sHdr + kHdrSlots * kHdrBytes);
     uint64_t *full = bars;                  // A + nibbles landed      (tx)
     uint64_t *bready = full + kStages;      // B written               (8 dequant warps)
@@ -324,6 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 for (int ks = 4 * sb0; ks < 4 * (sb0 + sb_u); ++ks, ++it) {
                     const int s = it % kStages, u = it / kStages;
                     const int sb = ks >> 2, c = ks & 3;
+                    if constexpr (FMT == QMM_Q8_0) {
+                        // the chunk's blocks sit at 272 sb + 68 c of the row
+                        if (u >= 1 &&
+                            !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
+                            break;
+                        mbar_arrive_expect_tx(&full[s], kABytes + kRaw);
+                        tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
+                        tma_2d(sNib + s * kRaw, &P.tm_nib[mi], 272 * sb + ((68 * c) & ~15), row0,
+                               &full[s]);
+                        continue;
+                    }
                     if (c == 0) {
                         const int h = hit % kHdrSlots, hu = hit / kHdrSlots;
                         if (hu >= 1 &&
@@ -335,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     }
                     if (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
                         break;
-                    mbar_arrive_expect_tx(&full[s], kABytes + kNibBytes);
+                    mbar_arrive_expect_tx(&full[s], kABytes + kRaw);
                     tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
-                    tma_2d(sNib + s * kNibBytes, &P.tm_nib[mi], sb * 144 + 16 + 32 * c, row0, &full[s]);
+                    tma_2d(sNib + s * kRaw, &P.tm_nib[mi], sb * 144 + 16 + 32 * c, row0, &full[s]);
                 }
                 if (abort_flag)
                     break;
@@ -448,7 +483,52 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         const uint32_t swz = uint32_t(r & 7);
         int it = 0, hit = 0;
         bool ok = true;
-        for (int un = blockIdx.x; un < P.units && ok; un += gridDim.x) {
+        if constexpr (FMT == QMM_Q8_0) {
+            for (int un = blockIdx.x; un < P.units && ok; un += gridDim.x) {
+                int t_, ksl_, sb0, sb_u;
+                unit_of(un, t_, ksl_, sb0, sb_u);
+                for (int ks = 4 * sb0; ks < 4 * (sb0 + sb_u); ++ks, ++it) {
+                    const int s = it % kStages, u = it / kStages;
+                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
+                        (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+                        ok = false;
+                        break;
+                    }
+                    // this row's two blocks: [d0][32 q][d1][32 q] from byte
+                    // (68 c) mod 16 of its window -- 17 aligned words
+                    const uint32_t *wd = reinterpret_cast<const uint32_t *>(
+                        sNib + s * kRaw + r * kQ80Window + ((68 * (ks & 3)) & 15));
+                    uint32_t W[17];
+#pragma unroll
+                    for (int i = 0; i < 17; ++i)
+                        W[i] = wd[i];
+                    const float d0 = __half2float(__ushort_as_half((unsigned short)(W[0] & 0xffffu)));
+                    const float d1 = __half2float(__ushort_as_half((unsigned short)(W[8] >> 16)));
+                    uint8_t *brow = sB + s * kBBytes + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {  // 16-byte chunk j: weights 8j .. 8j+7
+                        uint32_t v0, v1;
+                        if (j < 4) {  // block 0: codes at bytes 2..33 (2-byte offset)
+                            v0 = __byte_perm(W[2 * j], W[2 * j + 1], 0x5432u);
+                            v1 = __byte_perm(W[2 * j + 1], W[2 * j + 2], 0x5432u);
+                        } else {      // block 1: codes at bytes 36..67 (aligned)
+                            v0 = W[9 + 2 * (j - 4)];
+                            v1 = W[10 + 2 * (j - 4)];
+                        }
+                        uint32_t p[4];
+                        dequant4_q8(v0, j < 4 ? d0 : d1, p[0], p[1]);
+                        dequant4_q8(v1, j < 4 ? d0 : d1, p[2], p[3]);
+                        *reinterpret_cast<uint4 *>(brow + ((uint32_t(j) ^ swz) << 4)) =
+                            make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                    fence_proxy_async_smem();  // the MMA reads B through the async proxy
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bready[s]);
+                }
+            }
+        }
+        for (int un = blockIdx.x; un < P.units && ok && FMT == QMM_Q4_K; un += gridDim.x) {
             int t_, ksl_, sb0, sb_u;
             unit_of(un, t_, ksl_, sb0, sb_u);
             for (int sb = sb0; sb < sb0 + sb_u && ok; ++sb, ++hit) {
@@ -469,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    const uint8_t *nib = sNib + s * kNibBytes + r * 32;
+                    const uint8_t *nib = sNib + s * kRaw + r * 32;
                     const uint4 n0 = *reinterpret_cast<const uint4 *>(nib);
                     const uint4 n1 = *reinterpret_cast<const uint4 *>(nib + 16);
                     uint32_t sc_lo, m_lo, sc_hi, m_hi;
@@ -579,9 +659,11 @@ __global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
 
 } // namespace
 
-size_t gemm_q4k_smem(int tok)
+size_t gemm_q4k_smem(int tok, int fmt)
 {
-    return tok == 128 ? TileCfg<128>::kSmemBytes : TileCfg<256>::kSmemBytes;
+    if (fmt == QMM_Q8_0)
+        return tok == 128 ? TileCfg<128, QMM_Q8_0>::kSmemBytes : TileCfg<256, QMM_Q8_0>::kSmemBytes;
+    return tok == 128 ? TileCfg<128, QMM_Q4_K>::kSmemBytes : TileCfg<256, QMM_Q4_K>::kSmemBytes;
 }
 
 int gemm_q4k_tiles(int64_t M, int64_t N, int tok)
@@ -672,8 +754,11 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     P.units = P.full_units + (P.tiles - P.full_units) * P.ksplit;
     P.vec_store = vec ? 1 : 0;
     P.status = a.status;
-    auto kern = a.tok == 128 ? gemm_q4k_kernel<128> : gemm_q4k_kernel<256>;
-    const size_t smem = gemm_q4k_smem(a.tok);
+    auto kern = a.fmt == QMM_Q8_0 ? (a.tok == 128 ? gemm_q4k_kernel<128, QMM_Q8_0>
+                                                   : gemm_q4k_kernel<256, QMM_Q8_0>)
+                                  : (a.tok == 128 ? gemm_q4k_kernel<128, QMM_Q4_K>
+                                                   : gemm_q4k_kernel<256, QMM_Q4_K>);
+    const size_t smem = gemm_q4k_smem(a.tok, a.fmt);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess)
         return e;

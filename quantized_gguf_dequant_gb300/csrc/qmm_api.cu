@@ -493,6 +493,18 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
             return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor maps for the prefill GEMM "
                                       "could not be encoded");
         }
+        m->has_gemm_maps = true;
+    } else if (fmt == QMM_Q8_0 && K % 256 == 0) {
+        // prefill GEMM: 80-byte windows over the rows (two 34-byte blocks
+        // from the 16-byte boundary at or below them), 256 rows
+        if (qmm::encode_tmap_2d(m->tmap_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_dev,
+                                uint64_t(m->row_bytes), uint64_t(N), uint64_t(m->row_bytes), 80u,
+                                256u, CU_TENSOR_MAP_SWIZZLE_NONE) != 0) {
+            delete m;
+            return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor map for the prefill GEMM "
+                                      "could not be encoded");
+        }
+        m->has_gemm_maps = true;
     }
     void *p = nullptr;
     const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256;
@@ -932,7 +944,7 @@ qmm_status qmm_ffn_decode(qmm_t hg, qmm_t hu, qmm_t hd, const float *x, float *h
     return do_gemv(&hd, 1, h, yd, s, fn);
 }
 
-// The prefill GEMM for n Q4_K matrices sharing X (n <= 4).
+// The prefill GEMM for n Q4_K or n Q8_0 matrices sharing X (n <= 4).
 static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, int64_t M,
                               float *const *Ys, qmm_stream stream, const char *fn)
 {
@@ -941,10 +953,14 @@ static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, in
         if (st != QMM_OK)
             return st;
         const Matrix *mi = reinterpret_cast<const Matrix *>(hs[i]);
-        if (mi->fmt != QMM_Q4_K)
+        if ((mi->fmt != QMM_Q4_K && mi->fmt != QMM_Q8_0) || !mi->has_gemm_maps)
             return fail(QMM_ERR_UNSUPPORTED,
-                        "%s: the prefill GEMM is implemented for Q4_K weights only (matrix %d is "
-                        "format %d)", fn, i, mi->fmt);
+                        "%s: the prefill GEMM takes Q4_K, and Q8_0 rows of whole 256-weight "
+                        "groups (matrix %d is format %d, K %lld)", fn, i, mi->fmt,
+                        (long long)mi->K);
+        if (mi->fmt != reinterpret_cast<const Matrix *>(hs[0])->fmt)
+            return fail(QMM_ERR_SHAPE, "%s: matrix %d has format %d, matrix 0 format %d", fn, i,
+                        mi->fmt, reinterpret_cast<const Matrix *>(hs[0])->fmt);
         if (mi->K != reinterpret_cast<const Matrix *>(hs[0])->K)
             return fail(QMM_ERR_SHAPE, "%s: matrix %d has K = %lld, matrix 0 K = %lld", fn, i,
                         (long long)mi->K, (long long)reinterpret_cast<const Matrix *>(hs[0])->K);
@@ -966,6 +982,7 @@ static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, in
         return fail(QMM_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
     qmm::GemmArgs a;
     memset(&a, 0, sizeof(a));
+    a.fmt = m->fmt;
     int64_t Ntot = 0;
     int tiles256 = 0, tiles128 = 0;
     for (int i = 0; i < n; ++i) {

@@ -39,7 +39,8 @@ struct Matrix {
     // prefill GEMM: tensor maps over the weight bytes (u8) with boxes of the
     // 16-byte super-block header and of one 32-byte nibble chunk, 256 rows
     alignas(64) unsigned char tmap_hdr[128];
-    alignas(64) unsigned char tmap_nib[128];
+    alignas(64) unsigned char tmap_nib[128];  // Q8_0: 80-byte windows, 256 rows
+    bool has_gemm_maps = false;
     // batched GEMV scratch: the K-slice partial sums (grown on demand)
     void *tcb_ws = nullptr;
     size_t tcb_ws_bytes = 0;
@@ -236,6 +237,7 @@ int make_q4k_column_map(void *out128, const void *w, int64_t N, int64_t row_byte
 // --------------------------------------------------------------- prefill GEMM
 constexpr int kGemmMaxGroup = 4;
 struct GemmArgs {
+    int fmt;                             // QMM_Q4_K or QMM_Q8_0
     const void *tmap_x;                  // X [M][K] bf16: box 64 x tok, 128-byte swizzle
     const void *tmap_hdr[kGemmMaxGroup]; // Matrix::tmap_hdr of each matrix
     const void *tmap_nib[kGemmMaxGroup]; // Matrix::tmap_nib
@@ -249,7 +251,7 @@ struct GemmArgs {
     int64_t M, K;
     unsigned *status;
 };
-size_t gemm_q4k_smem(int tok);
+size_t gemm_q4k_smem(int tok, int fmt);
 int gemm_q4k_tiles(int64_t M, int64_t N, int tok);
 struct GemmSplit {
     int full;    // whole tiles (the first ones)

@@ -36,7 +36,7 @@ int main(int argc, char **argv)
             for (int tok : {128, 256})
                 printf("{\"kind\": \"gemm_tiles\", \"M\": %lld, \"N\": %lld, \"tok\": %d, "
                        "\"tiles\": %d, \"smem\": %zu}\n",
-                       M, N, tok, qmm::gemm_q4k_tiles(M, N, tok), qmm::gemm_q4k_smem(tok));
+                       M, N, tok, qmm::gemm_q4k_tiles(M, N, tok), qmm::gemm_q4k_smem(tok, QMM_Q4_K));
     for (long long K : Ks)
         for (int M = 1; M <= 4; ++M)
             printf("{\"kind\": \"tc_smem\", \"K\": %lld, \"M\": %d, \"smem_16x2\": %zu, "

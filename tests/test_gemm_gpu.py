@@ -38,12 +38,13 @@ def _run(m, Xb, M):
     return Y.cpu().numpy()
 
 
-def _check(M, N, K, seed, rows=None):
-    w = synth.q4k_matrix(N, K, seed)
+def _check(M, N, K, seed, rows=None, fmt=None):
+    fmt = q.Q4_K if fmt is None else fmt
+    w = synth.matrix(fmt, N, K, seed)
     Xb = synth.activations_bf16(M, K, seed + 1)
-    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    m = q.Matrix(fmt, N, K, to_dev(w))
     y = _run(m, Xb, M)
-    y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS)
+    y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS, fmt=fmt)
     got = y if rows is None else y[:, rows]
     assert_close_to_oracle(got, y_ref, c, TOL_BF16, f"gemm M={M} N={N} K={K}")
     assert_close_to_oracle(got, y_ref, c, TIGHT, f"gemm (tight) M={M} N={N} K={K}")
@@ -52,16 +53,18 @@ def _check(M, N, K, seed, rows=None):
     return y
 
 
-def test_gemm_identity_is_bf16_weights():
+@pytest.mark.parametrize("fmt", [12, 8])  # Q4_K, Q8_0
+def test_gemm_identity_is_bf16_weights(fmt):
     """X = I (K x K): Y[m][n] = bf16(w[n][m]) exactly (one nonzero product per
-    output), for every position of every super-block, chunk and nibble."""
+    output), for every position of every super-block, chunk and nibble (Q8_0:
+    every block and code of every 80-byte window offset)."""
     N, K = 300, 512
-    w = synth.q4k_matrix(N, K, 7)
+    w = synth.matrix(fmt, N, K, 7)
     eye = np.eye(K, dtype=np.float32)
     Xb = _bf16_bits_of(eye)
-    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    m = q.Matrix(fmt, N, K, to_dev(w))
     y = _run(m, Xb, K)
-    ref = oracle.dequant_rows(q.Q4_K, w, N, K).astype(np.float32)
+    ref = oracle.dequant_rows(fmt, w, N, K).astype(np.float32)
     want = _bf16_bits_of(ref).T  # [K, N]
     got = _bf16_bits_of(y)       # y holds bf16 values exactly; compare as bits
     assert np.array_equal(y, y.astype(np.float32))
@@ -85,10 +88,35 @@ def test_gemm_small(monkeypatch, tok, M, N, K):
     _check(M, N, K, seed=M + N + K)
 
 
+@pytest.mark.parametrize("fmt", [12, 8])
 @pytest.mark.parametrize("tok", [128, 256])
-def test_gemm_identity_both_tiles(monkeypatch, tok):
+def test_gemm_identity_both_tiles(monkeypatch, tok, fmt):
     monkeypatch.setenv("QMM_GEMM_TOK", str(tok))
-    test_gemm_identity_is_bf16_weights()
+    test_gemm_identity_is_bf16_weights(fmt)
+
+
+@pytest.mark.parametrize("tok", [None, 128, 256])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (130, 513, 768), (257, 1024, 2048),
+                                   (129, 257, 4096)])
+def test_gemm_q8_0_small(monkeypatch, tok, M, N, K):
+    """Q8_0 weights (two 34-byte blocks per 64-weight step, staged as 80-byte
+    windows) on small and ragged shapes."""
+    if tok:
+        monkeypatch.setenv("QMM_GEMM_TOK", str(tok))
+    _check(M, N, K, seed=M + N + K + 8, fmt=q.Q8_0)
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (4096, 14336)])
+def test_gemm_q8_0_llama_shapes_m512(N, K):
+    rng = np.random.default_rng(N + K + 8)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(N - 8, N), rng.choice(N, 48, False)]))
+    _check(512, N, K, seed=N * 5 + K, rows=rows, fmt=q.Q8_0)
+
+
+@pytest.mark.parametrize("ksplit", [2, 4])
+def test_gemm_q8_0_split_k(monkeypatch, ksplit):
+    monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
+    _check(200, 512, 2048, seed=31, fmt=q.Q8_0)
 
 
 @pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)])
@@ -132,13 +160,19 @@ def test_gemm_deterministic_and_graph():
 
 def test_gemm_refusals():
     N, K = 64, 256
-    w8 = synth.q8_0_matrix(N, K, 1)
-    m8 = q.Matrix(q.Q8_0, N, K, to_dev(w8))
+    w6 = synth.matrix(q.Q6_K, N, K, 1)
+    m6 = q.Matrix(q.Q6_K, N, K, to_dev(w6))
     X = torch.zeros((4, K), dtype=torch.int16, device="cuda")
     Y = torch.zeros((4, N), dtype=torch.float32, device="cuda")
     with pytest.raises(q.QmmError) as ei:
-        m8.gemm(X, Y)
+        m6.gemm(X, Y)
     assert ei.value.status == q.ERR_UNSUPPORTED and "Q4_K" in ei.value.message
+    m6.close()
+    w8 = synth.matrix(q.Q8_0, N, 96, 1)  # rows not whole 256-weight groups
+    m8 = q.Matrix(q.Q8_0, N, 96, to_dev(w8))
+    with pytest.raises(q.QmmError) as ei:
+        m8.gemm(torch.zeros((4, 96), dtype=torch.int16, device="cuda"), Y)
+    assert ei.value.status == q.ERR_UNSUPPORTED
     m8.close()
     w = synth.q4k_matrix(N, K, 2)
     m = q.Matrix(q.Q4_K, N, K, to_dev(w))
