@@ -652,6 +652,8 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
         reinterpret_cast<Matrix *>(h)->last_stream = s;
         return QMM_OK;
     }
+    if (M == 1)  // one row: the decode GEMV itself
+        return do_gemv(&h, 1, X, &Y, s, "qmm_gemv_batched");
     const char *bpath = getenv("QMM_BATCHED_PATH");
     const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
     if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes) {
