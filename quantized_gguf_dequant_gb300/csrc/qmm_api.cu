@@ -160,6 +160,82 @@ qmm_status do_gemv_tcb(qmm_t h, const float *X, int64_t ldx, int M, float *Y, in
     return QMM_OK;
 }
 
+// The batched decode on tcgen05 (gemv_tc5.cu) for 2..16 rows of one Q4_K
+// matrix: prepared activations, slice partials and tickets live in the
+// handle's tc5 buffer (grown on demand: a synchronising allocation, so warm
+// up before capturing a graph).
+qmm_status do_gemv_tc5(qmm_t h, const float *X, int64_t ldx, int M, float *Y, int64_t ldy,
+                       cudaStream_t s, const char *fn)
+{
+    Matrix &mm = *reinterpret_cast<Matrix *>(h);
+    if (!mm.has_gemm_maps || mm.fmt != QMM_Q4_K || M < 2 || M > 16)
+        return QMM_ERR_UNSUPPORTED;
+    const qmm::Tc5Plan p = qmm::plan_tc5(mm.N, mm.K, M, mm.sm_count);
+    const size_t prep = (p.prep_bytes + 255) & ~size_t(255);
+    const size_t wsb = (p.ws_floats * 4 + 255) & ~size_t(255);
+    const size_t need = prep + wsb + p.tickets * 4;
+    if (need > mm.tc5_bytes) {
+        cudaError_t e = cudaSuccess;
+        if (mm.tc5_buf) {
+            e = cudaDeviceSynchronize();
+            if (e == cudaSuccess)
+                e = cudaFree(mm.tc5_buf);
+            mm.tc5_buf = nullptr;
+            mm.tc5_bytes = 0;
+            mm.tc5_nc = 0;
+            if (e != cudaSuccess)
+                return cuda_fail(e, fn);
+        }
+        void *ptr = nullptr;
+        e = cudaMalloc(&ptr, need);
+        if (e == cudaSuccess)
+            e = cudaMemset(ptr, 0, need);  // the tickets start at zero
+        if (e != cudaSuccess) {
+            if (ptr)
+                cudaFree(ptr);
+            return fail(QMM_ERR_NOMEM, "%s: could not allocate %zu bytes of batched-decode scratch "
+                        "(%s)", fn, need, cudaGetErrorString(e));
+        }
+        mm.tc5_buf = ptr;
+        mm.tc5_bytes = need;
+    }
+    uint8_t *buf = static_cast<uint8_t *>(mm.tc5_buf);
+    // The tickets sit at the end of the buffer, where every plan of this
+    // handle finds them (zero between launches).
+    unsigned *tickets = reinterpret_cast<unsigned *>(buf + mm.tc5_bytes) - p.tickets;
+    if (reinterpret_cast<uint8_t *>(tickets) < buf + prep + wsb)
+        return fail(QMM_ERR_NOMEM, "%s: batched-decode scratch too small", fn);
+    if (mm.tc5_nc != p.nc) {
+        if (qmm::encode_tmap_2d(mm.tc5_tmap_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, buf,
+                                uint64_t(mm.K), uint64_t(p.nc), uint64_t(mm.K) * 2, 64u,
+                                uint32_t(p.nc), CU_TENSOR_MAP_SWIZZLE_128B) != 0)
+            return fail(QMM_ERR_CUDA, "%s: the tensor map of the prepared activations could not "
+                                      "be encoded", fn);
+        mm.tc5_nc = p.nc;
+    }
+    qmm::Tc5Args a;
+    memset(&a, 0, sizeof(a));
+    a.tmap_hdr = mm.tmap_hdr;
+    a.tmap_nib = mm.tmap_nib;
+    a.tmap_b = mm.tc5_tmap_b;
+    a.prep = buf;
+    a.ws = p.S > 1 ? reinterpret_cast<float *>(buf + prep) : nullptr;
+    a.tickets = tickets;
+    a.X = X;
+    a.ldx = ldx;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.N = mm.N;
+    a.K = mm.K;
+    a.T = M;
+    a.status = mm.status;
+    cudaError_t e = qmm::launch_gemv_tc5(p, a, mm.sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    mm.last_stream = s;
+    return QMM_OK;
+}
+
 // The one-row Q4_K decode kernel (gemv_m1.cu) for n matrices sharing x.
 // QMM_ERR_UNSUPPORTED (nothing launched) when no plan fits its shared memory
 // or the handle's workspace.  QMM_M1_S fixes the number of K slices.
@@ -561,6 +637,8 @@ qmm_status qmm_destroy(qmm_t h)
         cudaFree(m->gemm_ws);
     if (m->tcb_ws)
         cudaFree(m->tcb_ws);
+    if (m->tc5_buf)
+        cudaFree(m->tc5_buf);
     if (prev >= 0)
         cudaSetDevice(prev);
     delete m;
@@ -657,8 +735,13 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     const char *bpath = getenv("QMM_BATCHED_PATH");
     const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
     if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes) {
-        // All rows in one pass over the weights (measured faster than passes
-        // of the decode kernel for every Llama shape from two rows on).
+        // All rows in one pass over the weights: on tcgen05 (the default), or
+        // the mma.sync kernel (QMM_BATCHED_PATH=tcb).
+        if (!(bpath && strcmp(bpath, "tcb") == 0)) {
+            st = do_gemv_tc5(h, X, ldx, int(M), Y, ldy, s, "qmm_gemv_batched");
+            if (st != QMM_ERR_UNSUPPORTED)
+                return st;
+        }
         st = do_gemv_tcb(h, X, ldx, int(M), Y, ldy, s, "qmm_gemv_batched");
         if (st != QMM_ERR_UNSUPPORTED)
             return st;

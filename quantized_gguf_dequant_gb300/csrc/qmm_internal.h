@@ -44,6 +44,12 @@ struct Matrix {
     // batched GEMV scratch: the K-slice partial sums (grown on demand)
     void *tcb_ws = nullptr;
     size_t tcb_ws_bytes = 0;
+    // tcgen05 batched decode: prepared activations, slice partials, tickets
+    // (grown on demand), and the tensor map over the prepared activations
+    void *tc5_buf = nullptr;
+    size_t tc5_bytes = 0;
+    alignas(64) unsigned char tc5_tmap_b[128];
+    int tc5_nc = 0;
     // prefill split-K scratch: the partial products (grown on demand)
     void *gemm_ws = nullptr;
     size_t gemm_ws_bytes = 0;
@@ -303,6 +309,35 @@ cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, i
                           cudaStream_t s);
 cudaError_t launch_moe_combine(const float *ys, const float *r, const int32_t *ids, int E, int T,
                                int top_k, int64_t Ne, float *y, int sm_count, cudaStream_t s);
+
+// --------------------------------------------------------------- batched decode on tcgen05
+// gemv_tc5.cu: Q4_K, 2..16 activation rows, 256-row tiles x K slices.
+struct Tc5Plan {
+    int nc = 0;             // B columns: 16 (T <= 8) or 32 (T <= 16)
+    int tiles = 0;          // 256-row tiles
+    int S = 1, sbs = 0;     // K slices, super-blocks per slice
+    int items = 0;          // tiles * S
+    size_t smem = 0;
+    size_t ws_floats = 0;   // slice partials [S][tiles][256][16] (S > 1)
+    size_t tickets = 0;     // [tiles][8]
+    size_t prep_bytes = 0;  // prepared activations: [nc][K] f16, scales, sub-block sums
+};
+Tc5Plan plan_tc5(int64_t N, int64_t K, int T, int sm_count);
+struct Tc5Args {
+    const void *tmap_hdr, *tmap_nib;  // Matrix::tmap_hdr / tmap_nib
+    const void *tmap_b;               // the prepared activations: [nc][K] f16, box 64 x nc, SW128
+    void *prep;                       // plan.prep_bytes
+    float *ws;                        // plan.ws_floats
+    unsigned *tickets;                // plan.tickets, zeroed once
+    const float *X;
+    int64_t ldx;
+    float *Y;
+    int64_t ldy;
+    int64_t N, K;
+    int T;
+    unsigned *status;
+};
+cudaError_t launch_gemv_tc5(const Tc5Plan &p, const Tc5Args &a, int sm_count, cudaStream_t s);
 
 // --------------------------------------------------------------- Q8_K integer-dot path
 struct Q8kArgs {

@@ -304,10 +304,68 @@ def test_gemv_batched_one_pass(M, N, K):
     m.close()
 
 
+@pytest.mark.parametrize("M", [2, 3, 8, 9, 16])
+@pytest.mark.parametrize("N,K", [(300, 768), (257, 2048), (1024, 4096), (4096, 14336)])
+def test_gemv_batched_tc5(M, N, K):
+    """The tcgen05 batched decode (256-row tiles, K slices chosen by the
+    planner, 16 or 32 B columns) against the oracle; large shapes on
+    sampled rows."""
+    w, m = _matrix(q.Q4_K, N, K, seed=M * 7 + N + K)
+    X = synth.activations(M, K, seed=M + 3 * N)
+    Y = m.gemv_batched(to_dev(X)).cpu().numpy()
+    rng = np.random.default_rng(M + N)
+    rows = None if N <= 1024 else np.unique(np.concatenate(
+        [np.arange(16), np.arange(N - 16, N), rng.choice(N, 96, False)]))
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, rows=rows, nthreads=oracle.max_threads())
+    got = Y if rows is None else Y[:, rows]
+    assert_close_to_oracle(got, Yr, C, TOL_FP32, f"tc5 M={M} N={N} K={K}")
+    assert m.status() == 0
+    m.close()
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 14])
+@pytest.mark.parametrize("M", [9, 16])
+def test_gemv_batched_tc5_forced_slices(monkeypatch, S, M):
+    """K slices whose partial sums the last slice of each (tile, warp) adds
+    in slice order: within bounds, bitwise repeatable, tickets left at zero
+    (a second call gives the same bits)."""
+    monkeypatch.setenv("QMM_TC5_S", str(S))
+    N, K = 515, 256 * 14
+    w, m = _matrix(q.Q4_K, N, K, seed=S + M)
+    X = synth.activations(M, K, seed=S + 1)
+    Y1 = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Y2 = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, nthreads=oracle.max_threads())
+    assert_close_to_oracle(Y1, Yr, C, TOL_FP32, f"tc5 S={S} M={M}")
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    m.close()
+
+
+def test_gemv_batched_tc5_edge_activations():
+    """Rows of very different magnitudes (the per-token, per-super-block
+    power-of-two scale), an all-zero row and a row with one nonzero value."""
+    N, K, M = 384, 1024, 6
+    w, m = _matrix(q.Q4_K, N, K, seed=44)
+    X = synth.activations(M, K, seed=45)
+    X[0] *= np.float32(1e30)
+    X[1] *= np.float32(1e-30)
+    X[2] = 0.0
+    X[3] = 0.0
+    X[3, 517] = 3.0
+    X[4, :256] *= np.float32(1e20)  # one super-block far larger than the rest
+    Y = m.gemv_batched(to_dev(X)).cpu().numpy()
+    Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, nthreads=oracle.max_threads())
+    assert_close_to_oracle(Y, Yr, C, TOL_FP32, "tc5 edge activations")
+    assert np.all(Y[2] == 0.0)
+    m.close()
+
+
 @pytest.mark.parametrize("S", [2, 3, 7])
 def test_gemv_batched_forced_k_slices(monkeypatch, S):
-    """K split into S slices whose partial sums a reduction kernel adds in
-    slice order: within bounds and bitwise repeatable."""
+    """The mma.sync batched kernel (QMM_BATCHED_PATH=tcb): K split into S
+    slices whose partial sums a reduction kernel adds in slice order: within
+    bounds and bitwise repeatable."""
+    monkeypatch.setenv("QMM_BATCHED_PATH", "tcb")
     monkeypatch.setenv("QMM_TCB_S", str(S))
     N, K, M = 515, 256 * 14, 9
     w, m = _matrix(q.Q4_K, N, K, seed=S)
