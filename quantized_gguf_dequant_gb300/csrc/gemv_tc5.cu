@@ -62,6 +62,12 @@ constexpr int kR = 256;               // weight rows per tile (two MMAs of M = 1
 constexpr int kABytes = kR * 128;     // fp16 A of one 64-wide step
 constexpr int kNib = kR * 32;         // nibble bytes of one step
 constexpr int kHdr = kR * 16;         // headers of one super-block
+constexpr int kScl = 16 * 4;          // the super-block's 2^-e per token
+constexpr int kXs = 128 * 4;          // its eight sub-block sums of x per token
+// one header-ring slot; a multiple of 128 bytes, since a tensor copy's
+// shared-memory destination must be 128-byte aligned
+constexpr int kSlot = (kHdr + kScl + kXs + 127) / 128 * 128;
+static_assert(kSlot % 128 == 0 && kHdr % 16 == 0 && kScl % 16 == 0, "slot alignment");
 constexpr int kHdrSlots = 3;
 constexpr int kStages = 4;
 constexpr int kThreads = 576;
@@ -72,7 +78,7 @@ struct Cfg {
     static constexpr int kBBytes = NC * 128;  // NC rows x 64 k of fp16
     static constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kNib;
     static constexpr uint32_t kTmemCols = 4 * NC;  // 2 buffers x 2 halves x NC
-    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + size_t(kHdrSlots) * kHdr + 256;
+    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + size_t(kHdrSlots) * kSlot + 256;
     // kind::f16: D f32 (bit 4), A and B f16 (0), both K-major, N/8 at 17, M/16 at 24
     static constexpr uint32_t kIdesc =
         (1u << 4) | (uint32_t(NC >> 3) << 17) | (uint32_t(128 >> 4) << 24);
@@ -93,6 +99,17 @@ struct T5Params {
     int N, T, NB, S, sbs, tiles, items;
     unsigned *status;
 };
+
+// One-dimensional bulk copy global -> shared (16-byte aligned, a multiple of
+// 16 bytes), completing on bar.
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 
 __device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c)
 {
@@ -120,11 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
     auto sB = [&](int s) { return sA(s) + kABytes; };
     auto sNib = [&](int s) { return sB(s) + C::kBBytes; };
     uint8_t *sHdr = base + size_t(kStages) * C::kStageBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sHdr + kHdrSlots * kHdr);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sHdr + kHdrSlots * kSlot);
     uint64_t *full = bars;                  // nibbles + B landed        (tx)
     uint64_t *aready = full + kStages;      // A written                 (8 A warps)
     uint64_t *empty = aready + kStages;     // the step's MMAs done      (commit)
-    uint64_t *hfull = empty + kStages;      // headers landed            (tx)
+    uint64_t *hfull = empty + kStages;      // headers + scales + sums landed (tx)
     uint64_t *hempty = hfull + kHdrSlots;   // headers read              (8 A + 8 epilogue warps)
     uint64_t *accfull = hempty + kHdrSlots; // [2] super-block sums done (commit)
     uint64_t *accempty = accfull + 2;       // [2] sums read             (8 epilogue warps)
@@ -188,8 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&hfull[h], kHdr);
-                    tma_2d(sHdr + h * kHdr, &P.tm_hdr, sb * 144, row0, &hfull[h]);
+                    uint8_t *slot = sHdr + h * kSlot;
+                    mbar_arrive_expect_tx(&hfull[h], kHdr + kScl + kXs);
+                    tma_2d(slot, &P.tm_hdr, sb * 144, row0, &hfull[h]);
+                    bulk_copy(slot + kHdr, P.scl + size_t(sb) * 16, kScl, &hfull[h]);
+                    bulk_copy(slot + kHdr + kScl, P.xs + size_t(sb) * 128, kXs, &hfull[h]);
                     ++hit;
                     for (int c = 0; c < 4; ++c, ++st) {
                         const int s = st % kStages, u = st / kStages;
@@ -282,16 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
                 if constexpr (NC == 32)
                     tmem_ld16(taddr + 16, *reinterpret_cast<uint32_t(*)[16]>(D + 16));
                 tmem_ld_wait();
-                const uint4 hd = *reinterpret_cast<const uint4 *>(sHdr + h * kHdr + r * 16);
+                const uint8_t *slot = sHdr + h * kSlot;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(slot + r * 16);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0)
                     mbar_arrive(&accempty[b]);  // this buffer may take the next sums
-                    mbar_arrive(&hempty[h]);
-                }
                 const float2 dd = half2_bits_to_float2(hd.x);  // (d, dmin)
-                const float *scl = P.scl + size_t(sb) * 16;
-                const float *xs = P.xs + size_t(sb) * 128;
+                const float *scl = reinterpret_cast<const float *>(slot + kHdr);
+                const float *xs = reinterpret_cast<const float *>(slot + kHdr + kScl);
                 // min term: sum_j m_j * (sum of x over sub-block j), tokens in pairs
                 float2 mn[8];
 #pragma unroll
@@ -305,14 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
                     const float4 *xj = reinterpret_cast<const float4 *>(xs + 16 * j);
 #pragma unroll
                     for (int q = 0; q < NC / 8; ++q) {  // tokens 4q .. 4q+3
-                        const float4 v = __ldg(xj + q);
+                        const float4 v = xj[q];
                         mn[2 * q] = __ffma2_rn(mj, make_float2(v.x, v.y), mn[2 * q]);
                         mn[2 * q + 1] = __ffma2_rn(mj, make_float2(v.z, v.w), mn[2 * q + 1]);
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < NC / 8; ++q) {
-                    const float4 s4 = __ldg(reinterpret_cast<const float4 *>(scl) + q);
+                    const float4 s4 = reinterpret_cast<const float4 *>(scl)[q];
                     const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -323,6 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
                         acc[t] = fmaf(-dd.y, mn_t, acc[t]);
                     }
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&hempty[h]);  // the slot's scales and sums are read
             }
             if (!ok)
                 break;
@@ -397,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc5_kernel(const __grid_cons
                     ok = false;
                     break;
                 }
-                const uint4 hd = *reinterpret_cast<const uint4 *>(sHdr + h * kHdr + r * 16);
+                const uint4 hd = *reinterpret_cast<const uint4 *>(sHdr + h * kSlot + r * 16);
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&hempty[h]);

@@ -735,9 +735,10 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     const char *bpath = getenv("QMM_BATCHED_PATH");
     const bool force_passes = bpath && strcmp(bpath, "passes") == 0;
     if (m.fmt == QMM_Q4_K && M >= 2 && !force_passes) {
-        // All rows in one pass over the weights: on tcgen05 (the default), or
-        // the mma.sync kernel (QMM_BATCHED_PATH=tcb).
-        if (!(bpath && strcmp(bpath, "tcb") == 0)) {
+        // All rows in one pass over the weights: the mma.sync kernel (the
+        // default: measured faster at every Llama shape and M = 4..16), or
+        // the tcgen05 kernel (QMM_BATCHED_PATH=tc5).
+        if (bpath && strcmp(bpath, "tc5") == 0) {
             st = do_gemv_tc5(h, X, ldx, int(M), Y, ldy, s, "qmm_gemv_batched");
             if (st != QMM_ERR_UNSUPPORTED)
                 return st;

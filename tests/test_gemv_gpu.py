@@ -306,10 +306,11 @@ def test_gemv_batched_one_pass(M, N, K):
 
 @pytest.mark.parametrize("M", [2, 3, 8, 9, 16])
 @pytest.mark.parametrize("N,K", [(300, 768), (257, 2048), (1024, 4096), (4096, 14336)])
-def test_gemv_batched_tc5(M, N, K):
-    """The tcgen05 batched decode (256-row tiles, K slices chosen by the
-    planner, 16 or 32 B columns) against the oracle; large shapes on
-    sampled rows."""
+def test_gemv_batched_tc5(monkeypatch, M, N, K):
+    """The tcgen05 batched decode (QMM_BATCHED_PATH=tc5: 256-row tiles, K
+    slices chosen by the planner, 16 or 32 B columns) against the oracle;
+    large shapes on sampled rows."""
+    monkeypatch.setenv("QMM_BATCHED_PATH", "tc5")
     w, m = _matrix(q.Q4_K, N, K, seed=M * 7 + N + K)
     X = synth.activations(M, K, seed=M + 3 * N)
     Y = m.gemv_batched(to_dev(X)).cpu().numpy()
@@ -329,6 +330,7 @@ def test_gemv_batched_tc5_forced_slices(monkeypatch, S, M):
     """K slices whose partial sums the last slice of each (tile, warp) adds
     in slice order: within bounds, bitwise repeatable, tickets left at zero
     (a second call gives the same bits)."""
+    monkeypatch.setenv("QMM_BATCHED_PATH", "tc5")
     monkeypatch.setenv("QMM_TC5_S", str(S))
     N, K = 515, 256 * 14
     w, m = _matrix(q.Q4_K, N, K, seed=S + M)
@@ -341,9 +343,12 @@ def test_gemv_batched_tc5_forced_slices(monkeypatch, S, M):
     m.close()
 
 
-def test_gemv_batched_tc5_edge_activations():
+@pytest.mark.parametrize("path", ["tc5", "tcb"])
+def test_gemv_batched_edge_activations(monkeypatch, path):
     """Rows of very different magnitudes (the per-token, per-super-block
-    power-of-two scale), an all-zero row and a row with one nonzero value."""
+    power-of-two scale), an all-zero row and a row with one nonzero value,
+    on both batched kernels."""
+    monkeypatch.setenv("QMM_BATCHED_PATH", path)
     N, K, M = 384, 1024, 6
     w, m = _matrix(q.Q4_K, N, K, seed=44)
     X = synth.activations(M, K, seed=45)
@@ -355,7 +360,7 @@ def test_gemv_batched_tc5_edge_activations():
     X[4, :256] *= np.float32(1e20)  # one super-block far larger than the rest
     Y = m.gemv_batched(to_dev(X)).cpu().numpy()
     Yr, C = oracle.gemv(q.Q4_K, w, N, K, X, nthreads=oracle.max_threads())
-    assert_close_to_oracle(Y, Yr, C, TOL_FP32, "tc5 edge activations")
+    assert_close_to_oracle(Y, Yr, C, TOL_FP32, f"{path} edge activations")
     assert np.all(Y[2] == 0.0)
     m.close()
 
