@@ -1,6 +1,5 @@
-// m1_device.cuh -- device building blocks of the one-row Q4_K decode
-// kernels (gemv_m1.cu: one GEMV per launch; gemv_chain.cu: a chain of GEMVs
-// in one launch): shared-memory and TMA helpers, the super-block header
+// m1_device.cuh -- device building blocks of the one-row Q4_K decode kernel
+// (gemv_m1.cu): shared-memory and TMA helpers, the super-block header
 // decode, the activation layout, and the arithmetic of one unit (16 rows x
 // 256 weights) described at the top of gemv_m1.cu.
 #pragma once
@@ -218,41 +217,6 @@ __device__ __forceinline__ float unit_rows(uint4 h0, uint4 h1, uint4 qa0, uint4 
         } else {
             mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
             mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
-        }
-    }
-    const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
-                                                          make_float2(dlo[1], dlo[3])),
-                                  __fadd2_rn(make_float2(dhi[0], dhi[2]), make_float2(dhi[1], dhi[3])),
-                                  X0, X1, iv);
-    const bool odd = c & 1;
-    float keep = odd ? tot.y : tot.x;
-    keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
-    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-    return keep;
-}
-
-// unit_rows with the B fragments read from shared memory at the point of
-// use (bx: this lane's entry for k-step 0 of the super-block, entries of
-// consecutive k-steps 8 uint4 apart; act: whether this lane's B entries are
-// non-zero) -- for kernels that cannot keep 32 registers of fragments live.
-__device__ __forceinline__ float unit_rows_sb(uint4 h0, uint4 h1, uint4 qa0, uint4 qa1, uint4 qb0,
-                                              uint4 qb1, uint32_t bx, bool act, const ScaleSel &L,
-                                              int c, float2 X0, float2 X1, float2 iv)
-{
-    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
-    const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
-    const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
-    float dlo[4], dhi[4];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const uint4 b = act ? lds128(bx + uint32_t(t) * 128u) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
-        if (t == 0) {
-            mma16816_zero(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, b.x, b.y);
-            mma16816_zero(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, b.z, b.w);
-        } else {
-            mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, b.x, b.y);
-            mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, b.z, b.w);
         }
     }
     const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
