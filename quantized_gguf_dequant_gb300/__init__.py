@@ -121,8 +121,15 @@ def _ptr(t) -> ctypes.c_void_p:
 
 def _stream(stream=None) -> ctypes.c_void_p:
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        # the current stream's handle without building a Stream object
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return ctypes.c_void_p(raw(torch.cuda.current_device()))
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
 
 
 # --------------------------------------------------------------------- raw ABI

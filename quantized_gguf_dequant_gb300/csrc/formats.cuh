@@ -35,7 +35,7 @@
 namespace qmm {
 namespace fmt {
 
-constexpr int kQ80 = 8, kQ5K = 13, kQ6K = 14, kIQ4NL = 20;
+constexpr int kQ80 = 8, kQ4K = 12, kQ5K = 13, kQ6K = 14, kIQ4NL = 20;
 
 template <int F> struct Block;
 template <> struct Block<kQ5K> { static constexpr int bytes = 176, weights = 256; };

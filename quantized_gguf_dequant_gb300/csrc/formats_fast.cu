@@ -64,6 +64,7 @@ struct FmtParams {
 };
 
 template <int F> struct Unit;
+template <> struct Unit<fmt::kQ4K> { static constexpr int bytes = 144, words = 36; };
 template <> struct Unit<fmt::kQ5K> { static constexpr int bytes = 176, words = 44; };
 template <> struct Unit<fmt::kQ6K> { static constexpr int bytes = 210, words = 54; };
 template <> struct Unit<fmt::kIQ4NL> { static constexpr int bytes = 144, words = 36; };
@@ -176,7 +177,9 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&u)[Unit<F>::words], co
                                          int64_t xst, const float *xsum, int64_t sst,
                                          float (&acc)[MR])
 {
-    if constexpr (F == fmt::kQ5K) {
+    if constexpr (F == fmt::kQ5K || F == fmt::kQ4K) {
+        // Q4_K is Q5_K without the fifth bits: its nibbles start at word 4
+        constexpr int kQs = F == fmt::kQ5K ? 12 : 4;
         const float d = half_lo(u[0]), dmin = half_lo(u[0] >> 16);
         const uint32_t a = u[1], b = u[2], c = u[3];
         const uint32_t scA = a & 0x3f3f3f3fu, mA = b & 0x3f3f3f3fu;
@@ -192,9 +195,10 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&u)[Unit<F>::words], co
                 sv[r] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                const uint32_t qs = u[12 + 8 * (j >> 1) + m], qh = u[4 + m];
-                const uint32_t q = ((j & 1 ? qs >> 4 : qs) & 0x0f0f0f0fu) |
-                                   (((qh >> j) & 0x01010101u) << 4);
+                const uint32_t qs = u[kQs + 8 * (j >> 1) + m];
+                uint32_t q = (j & 1 ? qs >> 4 : qs) & 0x0f0f0f0fu;
+                if constexpr (F == fmt::kQ5K)
+                    q |= ((u[4 + m] >> j) & 0x01010101u) << 4;
 #pragma unroll
                 for (int r = 0; r < MR; ++r)
                     fma4_half(q, lds_f4(xs + r * xst + 32 * j + 4 * m), sv[r]);
@@ -411,13 +415,12 @@ __global__ void __launch_bounds__(32 * kWarpsF) gemv_fmt_fast_kernel(const __gri
 template <int F, int MR>
 cudaError_t launch_fast_t(const FmtParams &P, size_t smem, int sm_count, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(gemv_fmt_fast_kernel<F, MR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    const void *fn = reinterpret_cast<const void *>(gemv_fmt_fast_kernel<F, MR>);
+    cudaError_t e = func_smem(fn, smem);
     if (e != cudaSuccess)
         return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemv_fmt_fast_kernel<F, MR>,
-                                                      32 * kWarpsF, smem);
+    e = func_occupancy(fn, 32 * kWarpsF, smem, &per_sm);
     if (e != cudaSuccess)
         return e;
     const int64_t want = (P.n_groups + kWarpsF - 1) / kWarpsF;
@@ -450,16 +453,20 @@ cudaError_t launch_fast_f(const FmtParams &P, int MR, size_t smem, int sm_count,
 
 size_t fmt_fast_smem(int fmt, int64_t K, int MR)
 {
-    const size_t sums = fmt == fmt::kQ5K ? size_t(K / 32) : fmt == fmt::kQ6K ? size_t(K / 16) : 0;
+    const size_t sums = (fmt == fmt::kQ5K || fmt == fmt::kQ4K) ? size_t(K / 32)
+                        : fmt == fmt::kQ6K                       ? size_t(K / 16)
+                                                                 : 0;
     return size_t(MR) * (size_t(K / 256) * kUnitStride + sums) * 4;
 }
 
 int fmt_fast_rows(const Matrix &m, int M)
 {
-    if (!(m.fmt == fmt::kQ5K || m.fmt == fmt::kQ6K || m.fmt == fmt::kIQ4NL) || m.K % 256 != 0)
+    if (!(m.fmt == fmt::kQ5K || m.fmt == fmt::kQ6K || m.fmt == fmt::kIQ4NL ||
+          m.fmt == fmt::kQ4K) ||
+        m.K % 256 != 0)
         return 0;
     const char *e = getenv("QMM_FMT_PATH");
-    if (e && strcmp(e, "plain") == 0)
+    if (e && strcmp(e, "plain") == 0 && m.fmt != fmt::kQ4K)
         return 0;
     // rows per pass: 4, 2 or 1 -- the most that M has and shared memory holds
     for (int mr : {4, 2, 1})
@@ -509,6 +516,7 @@ cudaError_t launch_gemv_fmt_fast(const Matrix *const *ms, int n, const float *x,
             P.y[i] = ys[i] + int64_t(r0) * ldy;
         cudaError_t e;
         switch (m0.fmt) {
+        case fmt::kQ4K: e = launch_fast_f<fmt::kQ4K>(P, MR, smem, m0.sm_count, s); break;
         case fmt::kQ5K: e = launch_fast_f<fmt::kQ5K>(P, MR, smem, m0.sm_count, s); break;
         case fmt::kQ6K: e = launch_fast_f<fmt::kQ6K>(P, MR, smem, m0.sm_count, s); break;
         default: e = launch_fast_f<fmt::kIQ4NL>(P, MR, smem, m0.sm_count, s); break;

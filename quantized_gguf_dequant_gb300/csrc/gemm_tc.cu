@@ -663,7 +663,7 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
                                   : (a.tok == 128 ? gemm_q4k_kernel<128, QMM_Q4_K>
                                                    : gemm_q4k_kernel<256, QMM_Q4_K>);
     const size_t smem = gemm_q4k_smem(a.tok, a.fmt);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     int grid = sm_count < P.units ? sm_count : P.units;

@@ -597,8 +597,7 @@ cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
     const int minb = e_lb ? atoi(e_lb) : 1;
     KernelFn kern = (a.fmt == QMM_Q4_K) ? pick<QMM_Q4_K>(w, p.rpg, minb)
                                         : pick<QMM_Q8_0>(w, p.rpg, minb);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(p.smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

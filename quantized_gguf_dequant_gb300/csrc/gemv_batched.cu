@@ -434,7 +434,7 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s)
     P.S = p.S;
     P.nslot = tcb_slots();
     TcbKernel kern = pick_tcb(p.nt, a.M == 1);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -584,14 +584,9 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.cap = p.cap;
     P.nslot = p.nslot;
     P.slot_bytes = p.slot_bytes;
-    cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(p.smem));
-    if (e != cudaSuccess)
-        return e;
-    // All shared memory, so that two half-SM CTAs (this launch and the next)
-    // fit side by side.
-    e = cudaFuncSetAttribute(gemv_m1_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             int(cudaSharedmemCarveoutMaxShared));
+    // All shared memory preferred, so that two half-SM CTAs (this launch
+    // and the next) fit side by side.
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(gemv_m1_kernel), p.smem, true);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -492,7 +492,7 @@ cudaError_t launch_gemv_tc(const TcArgs &a, int sm_count, cudaStream_t s)
         P.res_tiles = int(2 * ((tiles / 2 + ctas - 1) / ctas));
     const size_t smem = gemv_tc_smem(a.K, a.M, nslot, nw, P.res_tiles);
     TcKernel kern = pick_tc(2 * a.M);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

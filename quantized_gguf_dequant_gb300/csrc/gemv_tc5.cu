@@ -620,7 +620,7 @@ cudaError_t launch_gemv_tc5(const Tc5Plan &p, const Tc5Args &a, int sm_count, cu
     P.items = p.items;
     P.status = a.status;
     auto kern = p.nc == 16 ? gemv_tc5_kernel<16> : gemv_tc5_kernel<32>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
+    e = func_smem(reinterpret_cast<const void *>(kern), p.smem);
     if (e != cudaSuccess)
         return e;
     cfg.gridDim = dim3(unsigned(std::min(p.items, sm_count)));

@@ -498,8 +498,7 @@ cudaError_t launch_moe_bucket(const int32_t *ids, int S, int E, const MoeIndex &
                               int64_t n0, int64_t ld0, unsigned *status, cudaStream_t s)
 {
     const size_t smem = moe_bucket_smem(S, E);
-    cudaError_t e = cudaFuncSetAttribute(moe_bucket_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(moe_bucket_kernel), smem);
     if (e != cudaSuccess)
         return e;
     return launch_ex(moe_bucket_kernel, dim3(1), dim3(1024), smem, s, ids, S, E, ix.groups,
@@ -562,8 +561,7 @@ cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t
     moe_expert_shape(a.K, nw, nslot);
     P.nslot = nslot;
     const size_t smem = moe_expert_smem(a.K, nw, nslot, P.maxpairs);
-    cudaError_t e = cudaFuncSetAttribute(moe_expert_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(moe_expert_kernel), smem);
     if (e != cudaSuccess)
         return e;
     // The number of groups is known only on the device: one CTA per SM, each

@@ -344,8 +344,7 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     const int64_t R = 32 >> lshift;
     P.n_groups = (tot + R - 1) / R;
     const size_t smem = q8k_smem(a.K);
-    cudaError_t e = cudaFuncSetAttribute(gemv_q8k_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(gemv_q8k_kernel), smem);
     if (e != cudaSuccess)
         return e;
     const int64_t want = (P.n_groups + kWarps - 1) / kWarps;

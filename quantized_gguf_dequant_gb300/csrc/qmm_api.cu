@@ -10,6 +10,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <unordered_map>
+#include <mutex>
 #include <string>
 
 #include <cuda.h>
@@ -287,11 +289,34 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     return QMM_OK;
 }
 
+// Weight bytes up to which a Q4_K GEMV (one row, a matrix or a group) takes
+// the SIMT kernel instead of the decode kernel: below about 4 MiB the decode
+// kernel's fixed set-up (152 CTAs, the TMA ring, the producer) costs more
+// than the bytes (measured: 1024 x 4096 in 8.9 us against 11.0 us; at 4096
+// x 4096 the decode kernel wins, 10.9 against 13.0 us).
+// QMM_Q4K_SMALL_BYTES overrides.
+int64_t q4k_small_bytes()
+{
+    const char *e = getenv("QMM_Q4K_SMALL_BYTES");
+    return e ? int64_t(atoll(e)) : int64_t(4) << 20;
+}
+
 qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
                    const char *fn)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
-    if (qmm::fmt_fast_rows(m0, 1) > 0) {
+    // Q4_K takes the SIMT kernel of formats_fast.cu only when asked
+    // (QMM_Q4K_PATH=fmt) or when the group's weights are small enough that
+    // the decode kernel's fixed set-up dominates (QMM_Q4K_SMALL_BYTES).
+    bool simt_ok = m0.fmt != QMM_Q4_K;
+    if (m0.fmt == QMM_Q4_K) {
+        const char *qp = getenv("QMM_Q4K_PATH");
+        int64_t bytes = 0;
+        for (int i = 0; i < n; ++i)
+            bytes += reinterpret_cast<const Matrix *>(hs[i])->N * m0.row_bytes;
+        simt_ok = (qp && strcmp(qp, "fmt") == 0) || (!qp && bytes <= q4k_small_bytes());
+    }
+    if (simt_ok && qmm::fmt_fast_rows(m0, 1) > 0) {
         const Matrix *ms[qmm::kMaxGroup];
         for (int i = 0; i < n; ++i)
             ms[i] = reinterpret_cast<const Matrix *>(hs[i]);
@@ -457,6 +482,71 @@ namespace qmm {
 
 namespace {
 std::atomic<int64_t> g_launches{0};
+}
+
+namespace {
+// Function attributes already set, per (device, function): the shared-
+// memory limit (threads = smem = 0 in the key), and resident blocks per SM
+// (per threads and shared memory).
+struct FuncKey {
+    int dev;
+    const void *func;
+    int threads;
+    size_t smem;
+    bool operator==(const FuncKey &o) const
+    {
+        return dev == o.dev && func == o.func && threads == o.threads && smem == o.smem;
+    }
+};
+struct FuncKeyHash {
+    size_t operator()(const FuncKey &k) const
+    {
+        return std::hash<const void *>()(k.func) ^ (size_t(k.dev) << 48) ^ (size_t(k.threads) << 32) ^
+               k.smem;
+    }
+};
+std::mutex g_func_mu;
+std::unordered_map<FuncKey, size_t, FuncKeyHash> g_func_smem;
+std::unordered_map<FuncKey, int, FuncKeyHash> g_func_occ;
+} // namespace
+
+cudaError_t func_smem(const void *func, size_t bytes, bool max_carveout)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const FuncKey key{dev, func, 0, 0};
+    std::lock_guard<std::mutex> lock(g_func_mu);
+    auto it = g_func_smem.find(key);
+    if (it != g_func_smem.end() && it->second >= bytes)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess)
+        g_func_smem[key] = bytes;
+    return e;
+}
+
+cudaError_t func_occupancy(const void *func, int threads, size_t smem, int *per_sm)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const FuncKey key{dev, func, threads, smem};
+    std::lock_guard<std::mutex> lock(g_func_mu);
+    auto it = g_func_occ.find(key);
+    if (it != g_func_occ.end()) {
+        *per_sm = it->second;
+        return cudaSuccess;
+    }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, func, threads, smem);
+    if (e == cudaSuccess)
+        g_func_occ[key] = *per_sm;
+    return e;
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -715,7 +805,7 @@ qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t ldx, flo
     if (!aligned(Y, 4))
         return fail(QMM_ERR_ALIGN, "qmm_gemv_batched: Y is not 4-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (qmm::fmt_fast_rows(m, int(M)) > 0) {
+    if (m.fmt != QMM_Q4_K && qmm::fmt_fast_rows(m, int(M)) > 0) {
         const Matrix *mp = &m;
         cudaError_t e = qmm::launch_gemv_fmt_fast(&mp, 1, X, ldx, int(M), &Y, ldy, s);
         if (e != cudaSuccess)

@@ -104,6 +104,16 @@ inline cudaError_t counted(cudaError_t e)
     return e;
 }
 
+// A kernel's dynamic shared-memory limit raised to at least `bytes` on the
+// current device (and, with max_carveout, the whole unified L1/shared array
+// preferred for shared memory).  Function attributes persist, so the runtime
+// is called only when the recorded limit is lower: setting them on every
+// launch cost microseconds of host time per call.
+cudaError_t func_smem(const void *func, size_t bytes, bool max_carveout = false);
+// Resident blocks per SM of `func` at `threads` and `smem`, remembered per
+// (device, function, threads, shared memory).
+cudaError_t func_occupancy(const void *func, int threads, size_t smem, int *per_sm);
+
 // Programmatic dependent launch on every kernel unless QMM_PDL=0.
 inline bool pdl_enabled()
 {

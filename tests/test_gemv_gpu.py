@@ -446,3 +446,25 @@ def test_gemv_chain_in_cuda_graph_matches_eager():
     assert_close_to_oracle(ys[4].cpu().numpy(), np.ravel(y_ref), np.ravel(c), TOL_FP32, "chain long K")
     for m in mats:
         m.close()
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (37, 2048), (1024, 1024), (300, 4096), (77, 14336),
+                                 (5, 8192), (33, 768)])
+def test_gemv_q4k_simt_small_shape_path(monkeypatch, N, K):
+    """The SIMT decode kernel for Q4_K (the small-shape path; forced here with
+    QMM_Q4K_PATH=fmt): one matrix and a group, against the oracle."""
+    monkeypatch.setenv("QMM_Q4K_PATH", "fmt")
+    w, m = _matrix(q.Q4_K, N, K, seed=N + 2 * K)
+    x = synth.activations(1, K, seed=N + 1)[0]
+    y = m.gemv(to_dev(x)).cpu().numpy()
+    yr, c = oracle.gemv(q.Q4_K, w, N, K, x, nthreads=oracle.max_threads())
+    assert_close_to_oracle(y, yr, c, TOL_FP32, f"q4k simt N={N} K={K}")
+    w2, m2 = _matrix(q.Q4_K, 19, K, seed=N + 3)
+    ys = [torch.full((N,), float("nan"), device="cuda"), torch.full((19,), float("nan"), device="cuda")]
+    q.gemv_group([m.h, m2.h], to_dev(x), ys)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(ys[0].cpu().numpy(), yr, c, TOL_FP32, "group 0")
+    yr2, c2 = oracle.gemv(q.Q4_K, w2, 19, K, x, nthreads=oracle.max_threads())
+    assert_close_to_oracle(ys[1].cpu().numpy(), yr2, c2, TOL_FP32, "group 1")
+    m.close()
+    m2.close()
