@@ -74,10 +74,15 @@ def _check_gemv(fmt, N, K, seed, rows=None, x=None):
     return m, w, x, y
 
 
+@pytest.mark.parametrize("small", ["default", "0"])
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 256), (33, 512), (1023, 1024), (1024, 1024),
                                  (257, 2048), (100, 4096), (300, 3072), (5, 14336)])
-def test_gemv_small(fmt, N, K):
+def test_gemv_small(monkeypatch, small, fmt, N, K):
+    """Small shapes on the default route (Q4_K below 4 MiB: the SIMT kernel)
+    and with the decode kernel forced (QMM_Q4K_SMALL_BYTES=0)."""
+    if small != "default":
+        monkeypatch.setenv("QMM_Q4K_SMALL_BYTES", small)
     m, *_ = _check_gemv(fmt, N, K, seed=N + K)
     m.close()
 
@@ -212,6 +217,7 @@ def test_gemv_m1_forced_k_slices(S, monkeypatch):
     super-blocks, slices added by the last CTA; twice, so the row-group
     tickets must have been reset."""
     monkeypatch.setenv("QMM_M1_S", S)
+    monkeypatch.setenv("QMM_Q4K_SMALL_BYTES", "0")  # the decode kernel even for small shapes
     for N, K in ((37, 2048), (300, 4096), (1000, 1024), (77, 14336), (1, 256), (40, 768),
                  (4096, 3584)):
         for rep in range(2):
@@ -224,6 +230,7 @@ def test_gemv_m1_ragged_group(S, monkeypatch):
     """A group of matrices with ragged row counts sharing x: slots that
     straddle two matrices, rows past a matrix end never written."""
     monkeypatch.setenv("QMM_M1_S", S)
+    monkeypatch.setenv("QMM_Q4K_SMALL_BYTES", "0")
     K = 2048
     shapes = [17, 1, 250, 33]
     mats, ws = [], []
