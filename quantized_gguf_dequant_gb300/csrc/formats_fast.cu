@@ -167,6 +167,17 @@ __device__ __forceinline__ void fma4_half(uint32_t q, float4 xv, float2 &s)
     s = __ffma2_rn(make_float2(half_plus(q, 2), half_plus(q, 3)), make_float2(xv.z, xv.w), s);
 }
 
+// s += b_k * x_k for the four bytes of q (0..255, exact through 2^23 + b),
+// four activations: every product exact, as the decode kernel's.
+__device__ __forceinline__ void fma4_exact(uint32_t q, float4 xv, float2 &s)
+{
+    const float2 m = make_float2(-8388608.f, -8388608.f);
+    const float2 a = __fadd2_rn(make_float2(byte_f(q, 0, 0.f), byte_f(q, 1, 0.f)), m);
+    const float2 b = __fadd2_rn(make_float2(byte_f(q, 2, 0.f), byte_f(q, 3, 0.f)), m);
+    s = __ffma2_rn(a, make_float2(xv.x, xv.y), s);
+    s = __ffma2_rn(b, make_float2(xv.z, xv.w), s);
+}
+
 // acc[r] += sum_k w_k x_r,k over one unit, for MR activation rows; xs = the
 // unit's 256 activations of row 0 in shared memory (row r at xs + r * xst),
 // xsum = their group sums (Q5_K: 8 of 32, Q6_K: 16 of 16; row r at
@@ -200,16 +211,30 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&u)[Unit<F>::words], co
                 if constexpr (F == fmt::kQ5K)
                     q |= ((u[4 + m] >> j) & 0x01010101u) << 4;
 #pragma unroll
-                for (int r = 0; r < MR; ++r)
-                    fma4_half(q, lds_f4(xs + r * xst + 32 * j + 4 * m), sv[r]);
+                for (int r = 0; r < MR; ++r) {
+                    if constexpr (F == fmt::kQ4K)
+                        fma4_exact(q, lds_f4(xs + r * xst + 32 * j + 4 * m), sv[r]);
+                    else
+                        fma4_half(q, lds_f4(xs + r * xst + 32 * j + 4 * m), sv[r]);
+                }
             }
-            // a sum q x - b sum x with sum q x = 256 S - 128 sum x
             const float as = d * float(sc), bm = dmin * float(mn);
-            const float a256 = 256.f * as, c0 = -fmaf(128.f, as, bm);
+            if constexpr (F == fmt::kQ4K) {
+                // a sum q x - b sum x, the products exact: a one-hot x gives
+                // RN(a q - b), the exact weight rounded once
 #pragma unroll
-            for (int r = 0; r < MR; ++r) {
-                acc[r] = fmaf(a256, sv[r].x + sv[r].y, acc[r]);
-                acc[r] = fmaf(c0, xsum[r * sst + j], acc[r]);
+                for (int r = 0; r < MR; ++r) {
+                    acc[r] = fmaf(as, sv[r].x + sv[r].y, acc[r]);
+                    acc[r] = fmaf(-bm, xsum[r * sst + j], acc[r]);
+                }
+            } else {
+                // a sum q x - b sum x with sum q x = 256 S - 128 sum x
+                const float a256 = 256.f * as, c0 = -fmaf(128.f, as, bm);
+#pragma unroll
+                for (int r = 0; r < MR; ++r) {
+                    acc[r] = fmaf(a256, sv[r].x + sv[r].y, acc[r]);
+                    acc[r] = fmaf(c0, xsum[r * sst + j], acc[r]);
+                }
             }
         }
     } else if constexpr (F == fmt::kQ6K) {

@@ -290,15 +290,15 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
 }
 
 // Weight bytes up to which a Q4_K GEMV (one row, a matrix or a group) takes
-// the SIMT kernel instead of the decode kernel: below about 4 MiB the decode
-// kernel's fixed set-up (152 CTAs, the TMA ring, the producer) costs more
-// than the bytes (measured: 1024 x 4096 in 8.9 us against 11.0 us; at 4096
-// x 4096 the decode kernel wins, 10.9 against 13.0 us).
-// QMM_Q4K_SMALL_BYTES overrides.
+// the SIMT kernel instead of the decode kernel (QMM_Q4K_SMALL_BYTES; 0 by
+// default).  Measured on the 1024 x 1024 matrix: the same 8.8 us for one
+// call with L2 flushed, and in a CUDA graph of 512 distinct copies the
+// decode kernel is faster (2.7 against 3.0 us per launch); eager calls of
+// 1024 x 4096 favour the SIMT kernel (8.9 against 11.0 us).
 int64_t q4k_small_bytes()
 {
     const char *e = getenv("QMM_Q4K_SMALL_BYTES");
-    return e ? int64_t(atoll(e)) : int64_t(4) << 20;
+    return e ? int64_t(atoll(e)) : int64_t(0);
 }
 
 qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,

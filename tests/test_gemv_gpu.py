@@ -74,13 +74,13 @@ def _check_gemv(fmt, N, K, seed, rows=None, x=None):
     return m, w, x, y
 
 
-@pytest.mark.parametrize("small", ["default", "0"])
+@pytest.mark.parametrize("small", ["default", "4194304"])
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 256), (33, 512), (1023, 1024), (1024, 1024),
                                  (257, 2048), (100, 4096), (300, 3072), (5, 14336)])
 def test_gemv_small(monkeypatch, small, fmt, N, K):
-    """Small shapes on the default route (Q4_K below 4 MiB: the SIMT kernel)
-    and with the decode kernel forced (QMM_Q4K_SMALL_BYTES=0)."""
+    """Small shapes on the default route and with Q4_K matrices up to 4 MiB
+    sent to the SIMT kernel (QMM_Q4K_SMALL_BYTES)."""
     if small != "default":
         monkeypatch.setenv("QMM_Q4K_SMALL_BYTES", small)
     m, *_ = _check_gemv(fmt, N, K, seed=N + K)
