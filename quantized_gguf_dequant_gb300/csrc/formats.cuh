@@ -49,6 +49,18 @@ static __constant__ float kIq4nlBook[16] = {-127.f, -104.f, -83.f, -65.f, -49.f,
                                             -22.f,  -10.f,  1.f,   13.f,  25.f,  38.f,
                                             53.f,   69.f,   89.f,  113.f};
 
+// The same book as int8 bytes, four codes to a word (codes 0-3 in word 0,
+// ...), for the kernels that look codes up with byte permutes.
+constexpr int kIq4nlBookInt[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
+                                   1,    13,   25,  38,  53,  69,  89,  113};
+__host__ __device__ constexpr uint32_t iq4nl_book_word(int i)
+{
+    return uint32_t(kIq4nlBookInt[i] & 0xff) | (uint32_t(kIq4nlBookInt[i + 1] & 0xff) << 8) |
+           (uint32_t(kIq4nlBookInt[i + 2] & 0xff) << 16) | (uint32_t(kIq4nlBookInt[i + 3] & 0xff) << 24);
+}
+static_assert(iq4nl_book_word(0) == 0xbfad9881u && iq4nl_book_word(12) == 0x71594535u,
+              "IQ4_NL book packing");
+
 __device__ __forceinline__ float half_bytes(const uint8_t *p)
 {
     return __half2float(__ushort_as_half(uint16_t(p[0] | (p[1] << 8))));

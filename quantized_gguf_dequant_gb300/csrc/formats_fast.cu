@@ -121,17 +121,6 @@ __device__ __forceinline__ void load_unit(const uint8_t *a, uint32_t (&u)[Unit<F
     }
 }
 
-// The IQ4_NL code book (GGUF IQ4_NL format definition), the values of the
-// 4-bit codes before the block scale, and four of them packed as int8 bytes.
-__device__ constexpr int kBook[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
-                           1,    13,   25,  38,  53,  69,  89,  113};
-__host__ __device__ constexpr uint32_t book_word(int i)
-{
-    return uint32_t(kBook[i] & 0xff) | (uint32_t(kBook[i + 1] & 0xff) << 8) |
-           (uint32_t(kBook[i + 2] & 0xff) << 16) | (uint32_t(kBook[i + 3] & 0xff) << 24);
-}
-static_assert(book_word(0) == 0xbfad9881u && book_word(12) == 0x71594535u, "book packing");
-
 // prmt.b32 in its default mode, selector bit 3 included: a selector nibble
 // 8 + i fills the output byte with the sign bit of source byte i (the
 // __byte_perm intrinsic is specified on the low three bits only).
@@ -276,8 +265,8 @@ __device__ __forceinline__ void unit_dot(const uint32_t (&u)[Unit<F>::words], co
         }
     } else {
         // the code book as int8 bytes: codes 0-7 in (T0, T1), 8-15 in (T2, T3)
-        constexpr uint32_t T0 = book_word(0), T1 = book_word(4), T2 = book_word(8),
-                           T3 = book_word(12);
+        constexpr uint32_t T0 = fmt::iq4nl_book_word(0), T1 = fmt::iq4nl_book_word(4),
+                           T2 = fmt::iq4nl_book_word(8), T3 = fmt::iq4nl_book_word(12);
         constexpr float kBias = 8388608.f + 128.f;  // 2^23 + 128: the int8 offset undone
         const float2 nb = make_float2(-kBias, -kBias);
 #pragma unroll

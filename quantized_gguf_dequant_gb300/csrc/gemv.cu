@@ -36,6 +36,7 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "formats.cuh"
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 
@@ -265,6 +266,196 @@ __device__ __forceinline__ float q8_row(const Q8State &st, const uint8_t *row)
     return fmaf(d.x, S.x, d.y * S.y);
 }
 
+// ----------------------------------------------------------------- further formats
+// Q5_K, Q6_K and IQ4_NL on the same staging and teams.  A thread's 64-weight
+// chunk pairs weight l of its first half with weight l of its second half
+// (xp[l] = (x_l, x_{32+l})), so that each packed FMA covers both.  Codes of
+// up to 7 bits become the float 0.5 + b/256 with one byte permute (bytes
+// [0, 0, b, 0x3f]); the group sums of x (prepared once) take the 0.5 back
+// out, so no per-weight subtraction is needed.  IQ4_NL's signed book values
+// go through 2^23 + 128 + v exactly.
+
+__device__ __forceinline__ float half_plus(uint32_t v, int k)
+{
+    return __uint_as_float(__byte_perm(v, 0x3f000000u, 0x7054u | (unsigned(k) << 8)));
+}
+
+__device__ __forceinline__ uint32_t prmt_raw(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+struct FxState {
+    float2 xp[32];  // (x_l, x_{32+l}) of the chunk
+    float X[4];     // sums of x: Q5_K halves (X[0], X[1]); Q6_K the four groups of 16
+    int off;        // byte offset of the chunk's unit (Q5_K, Q6_K) or blocks (IQ4_NL) in a row
+    int c4;         // chunk within its super-block (K-quants)
+};
+
+template <int FMT>
+__device__ __forceinline__ void fx_prologue(FxState &st, const float *x, int64_t gchunk,
+                                            int local_chunk, bool idle)
+{
+    float a[32], b[32];
+    if (idle) {
+#pragma unroll
+        for (int l = 0; l < 32; ++l)
+            a[l] = b[l] = 0.f;
+    } else {
+        load_chunk_x(x + gchunk * 64, a, b);
+    }
+#pragma unroll
+    for (int l = 0; l < 32; ++l)
+        st.xp[l] = make_float2(a[l], b[l]);
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        s[0] += a[l];
+        s[1] += a[16 + l];
+        s[2] += b[l];
+        s[3] += b[16 + l];
+    }
+    if (FMT == QMM_Q5_K) {
+        st.X[0] = s[0] + s[1];
+        st.X[1] = s[2] + s[3];
+        st.X[2] = st.X[3] = 0.f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st.X[i] = s[i];
+    }
+    st.c4 = int(gchunk & 3);
+    if (FMT == QMM_Q5_K)
+        st.off = idle ? 0 : (local_chunk >> 2) * 176;
+    else if (FMT == QMM_Q6_K)
+        st.off = idle ? 0 : (local_chunk >> 2) * 210;
+    else
+        st.off = idle ? 0 : local_chunk * 36;
+}
+
+// Q5_K: header, fifth bits and the chunk's nibbles, all 16-byte aligned.
+__device__ __forceinline__ float q5_row(const FxState &st, const uint8_t *row)
+{
+    const uint8_t *u = row + st.off;
+    const U4 h = lds128(u);
+    const U4 h0 = lds128(u + 16), h1 = lds128(u + 32);
+    const U4 q0 = lds128(u + 48 + 32 * st.c4), q1 = lds128(u + 64 + 32 * st.c4);
+    const uint32_t qh[8] = {h0.a, h0.b, h0.c, h0.d, h1.a, h1.b, h1.c, h1.d};
+    const uint32_t qs[8] = {q0.a, q0.b, q0.c, q0.d, q1.a, q1.b, q1.c, q1.d};
+    const int j0 = 2 * st.c4;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t hl = qh[t] >> j0;
+        const uint32_t lo = (qs[t] & 0x0f0f0f0fu) | ((hl << 4) & 0x10101010u);
+        const uint32_t hi = ((qs[t] >> 4) & 0x0f0f0f0fu) | ((hl << 3) & 0x10101010u);
+        float2 &acc = (t & 1) ? acc1 : acc0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            acc = __ffma2_rn(make_float2(half_plus(lo, k), half_plus(hi, k)), st.xp[4 * t + k], acc);
+    }
+    const float2 S = __fadd2_rn(acc0, acc1);
+    uint32_t sc0, m0, sc1, m1;
+    {
+        // the (sc, m) pairs of sub-blocks 2c4 and 2c4+1 (Q4_K packing)
+        const int j1 = j0 + 1;
+        auto sm = [&](int j, uint32_t &sc, uint32_t &m) {
+            if (j < 4) {
+                sc = (h.b >> (8 * j)) & 63u;
+                m = (h.c >> (8 * j)) & 63u;
+            } else {
+                const int i = j - 4;
+                const uint32_t bb = (h.d >> (8 * i)) & 0xffu;
+                sc = (bb & 0x0fu) | (((h.b >> (8 * i + 6)) & 3u) << 4);
+                m = (bb >> 4) | (((h.c >> (8 * i + 6)) & 3u) << 4);
+            }
+        };
+        sm(j0, sc0, m0);
+        sm(j1, sc1, m1);
+    }
+    const float2 dd = half2_bits_to_float2(h.a);  // (d, dmin)
+    const float a0 = dd.x * float(sc0), a1 = dd.x * float(sc1);
+    // a sum q x - b sum x, sum q x = 256 S - 128 X
+    const float t = fmaf(256.f * a0, S.x, 256.f * a1 * S.y);
+    const float c0 = fmaf(128.f, a0, dd.y * float(m0)), c1 = fmaf(128.f, a1, dd.y * float(m1));
+    return t - fmaf(c0, st.X[0], c1 * st.X[1]);
+}
+
+// Q6_K: the unit is only 2-byte aligned; words are read from its start
+// rounded down to 4 bytes and realigned with one byte permute each.
+__device__ __forceinline__ float q6_row(const FxState &st, const uint8_t *row)
+{
+    const uintptr_t ua = reinterpret_cast<uintptr_t>(row + st.off);
+    const uint32_t *wb = reinterpret_cast<const uint32_t *>(ua & ~uintptr_t(3));
+    const unsigned sel = (ua & 2) ? 0x5432u : 0x3210u;
+    auto U = [&](int k) { return __byte_perm(wb[k], wb[k + 1], sel); };
+    const int n = st.c4 >> 1, odd = st.c4 & 1;
+    const int t0 = 2 * odd;  // quarters t0 (weights 0..31) and t0 + 1 (32..63)
+    float2 g01 = make_float2(0.f, 0.f), g23 = make_float2(0.f, 0.f);  // (group 0, 2), (1, 3)
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t qla = U(16 * n + m), qlb = U(16 * n + 8 + m), qh = U(32 + 8 * n + m);
+        const uint32_t la = odd ? (qla >> 4) : qla, lb = odd ? (qlb >> 4) : qlb;
+        const uint32_t qa = (la & 0x0f0f0f0fu) | (((qh >> (2 * t0)) & 0x03030303u) << 4);
+        const uint32_t qb = (lb & 0x0f0f0f0fu) | (((qh >> (2 * t0 + 2)) & 0x03030303u) << 4);
+        float2 &acc = (m < 4) ? g01 : g23;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            acc = __ffma2_rn(make_float2(half_plus(qa, k), half_plus(qb, k)), st.xp[4 * m + k], acc);
+    }
+    const uint32_t scw = U(48 + st.c4);  // the chunk's four int8 scales
+    const uint32_t dw = (sel == 0x5432u) ? (wb[52] >> 16) : wb[52];
+    const float d = __half2float(__ushort_as_half((unsigned short)(dw & 0xffffu)));
+    // group g (16 weights): scale byte g; sum (q - 32) x = 256 S - 160 X
+    const float s0 = d * float(int8_t(scw & 0xffu)), s1 = d * float(int8_t((scw >> 8) & 0xffu));
+    const float s2 = d * float(int8_t((scw >> 16) & 0xffu)), s3 = d * float(int8_t(scw >> 24));
+    float r = 256.f * (s0 * g01.x + s1 * g23.x + s2 * g01.y + s3 * g23.y);
+    r -= 160.f * (s0 * st.X[0] + s1 * st.X[1] + s2 * st.X[2] + s3 * st.X[3]);
+    return r;
+}
+
+// IQ4_NL: the chunk's two 18-byte blocks (4-byte aligned as a pair).
+__device__ __forceinline__ float iq4_row(const FxState &st, const uint8_t *row)
+{
+    // the code book as int8 bytes: codes 0-7, 8-15
+    constexpr uint32_t T0 = fmt::iq4nl_book_word(0), T1 = fmt::iq4nl_book_word(4),
+                       T2 = fmt::iq4nl_book_word(8), T3 = fmt::iq4nl_book_word(12);
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(row + st.off);
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i)
+        w[i] = p[i];
+    const float2 d = half2_bits_to_float2(__byte_perm(w[0], w[4], 0x7610));  // (d_A, d_B)
+    const float2 off = make_float2(-8388736.f, -8388736.f);                  // -(2^23 + 128)
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    // look four codes up: (book[c0], book[c1], book[c2], book[c3]) + 128 per byte
+    auto look = [&](uint32_t codes) {  // codes: one 4-bit code per byte, in bits 0-3
+        const uint32_t sel = codes & 0x0007u | (codes >> 4 & 0x0070u) | (codes >> 8 & 0x0700u) |
+                             (codes >> 12 & 0x7000u);
+        const uint32_t mask = prmt_raw(codes << 4, 0u, 0xba98u);  // 0xff where the code >= 8
+        return ((__byte_perm(T0, T1, sel) & ~mask) | (__byte_perm(T2, T3, sel) & mask)) ^ 0x80808080u;
+    };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t ca = __byte_perm(w[i], w[i + 1], 0x5432u);  // block A code bytes 4i..4i+3
+        const uint32_t cb = w[5 + i];                              // block B
+        const uint32_t la = look(ca & 0x0f0f0f0fu), ha = look((ca >> 4) & 0x0f0f0f0fu);
+        const uint32_t lb = look(cb & 0x0f0f0f0fu), hb = look((cb >> 4) & 0x0f0f0f0fu);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            // weight 4i+k (low nibble) and 16+4i+k (high nibble) of each block
+            const float2 vl = __fadd2_rn(make_float2(byte_magic(la, k), byte_magic(lb, k)), off);
+            const float2 vh = __fadd2_rn(make_float2(byte_magic(ha, k), byte_magic(hb, k)), off);
+            acc0 = __ffma2_rn(vl, st.xp[4 * i + k], acc0);
+            acc1 = __ffma2_rn(vh, st.xp[16 + 4 * i + k], acc1);
+        }
+    }
+    const float2 S = __fadd2_rn(acc0, acc1);
+    return fmaf(d.x, S.x, d.y * S.y);
+}
+
 // ----------------------------------------------------------------- reduction
 // Sum RPG values over groups of W lanes (W a power of two <= 32, RPG <= W)
 // with a reduce-scatter: afterwards every lane holds the full sum of one of
@@ -387,10 +578,13 @@ __global__ void __launch_bounds__(kMaxConsumers, MINB) gemv_kernel(const __grid_
     pdl_wait();  // x, y and the workspace belong to the previous kernel until here
     Q4State s4;
     Q8State s8;
-    if (FMT == QMM_Q4_K)
+    FxState sx;
+    if constexpr (FMT == QMM_Q4_K)
         q4_prologue(s4, a.x, gchunk, c, idle);
-    else
+    else if constexpr (FMT == QMM_Q8_0)
         q8_prologue(s8, a.x, gchunk, c, idle);
+    else
+        fx_prologue<FMT>(sx, a.x, gchunk, c, idle);
 
     bool failed = false;
     for (int s = 0; s < nst; ++s) {
@@ -407,7 +601,16 @@ __global__ void __launch_bounds__(kMaxConsumers, MINB) gemv_kernel(const __grid_
             // Rows past the end of the range hold stale bytes; their sums are
             // computed and never stored.
             const uint8_t *row = stage + size_t(g + rg * j) * SB;
-            part[j] = (FMT == QMM_Q4_K) ? q4_row(s4, row) : q8_row(s8, row);
+            if constexpr (FMT == QMM_Q4_K)
+                part[j] = q4_row(s4, row);
+            else if constexpr (FMT == QMM_Q8_0)
+                part[j] = q8_row(s8, row);
+            else if constexpr (FMT == QMM_Q5_K)
+                part[j] = q5_row(sx, row);
+            else if constexpr (FMT == QMM_Q6_K)
+                part[j] = q6_row(sx, row);
+            else
+                part[j] = iq4_row(sx, row);
         }
         int j;
         const float v = reduce_rows<W, RPG>(part, lane, j);
@@ -546,7 +749,13 @@ GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit
     if (p.rg < 1)
         p.rg = 1;
     p.threads = p.rg * team;
-    p.slice_bytes = (fmt == QMM_Q4_K) ? int64_t(p.kchunks / 4) * 144 : int64_t(p.kchunks) * 68;
+    // bytes of one row's K-slice: whole 256-weight groups of the format
+    const int64_t group_bytes = fmt == QMM_Q4_K   ? 144
+                                : fmt == QMM_Q5_K ? 176
+                                : fmt == QMM_Q6_K ? 210
+                                : fmt == QMM_IQ4_NL ? 144
+                                                    : 272;
+    p.slice_bytes = int64_t(p.kchunks / 4) * group_bytes;
     // Q8_0 rows are twice as long in bytes: a sweep of stage sizes and ring
     // depths on the Llama-3.1-8B Q8_0 step put two stages of four rows per
     // team (stage target >= 72 KB) first, 26 % ahead of the Q4_K setting.
@@ -575,6 +784,15 @@ GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit
     return p;
 }
 
+bool gemv_plan_takes(int fmt, const GemvPlan &p, int64_t row_bytes)
+{
+    if (fmt == QMM_Q4_K || fmt == QMM_Q8_0)
+        return true;
+    // The further formats: 32-lane teams only, and bulk copies need rows and
+    // K-slices of whole 16-byte multiples (Q6_K: 2048 weights at a time).
+    return p.threads / p.rg >= 32 && p.slice_bytes % 16 == 0 && row_bytes % 16 == 0;
+}
+
 size_t gemv_workspace_floats(const GemvPlan &p, int64_t N)
 {
     return p.ksplit > 1 ? size_t(p.ksplit) * size_t(N) : 0;
@@ -595,8 +813,14 @@ cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s)
     const int w = P.team < 32 ? P.team : 32;
     const char *e_lb = getenv("QMM_GEMV_MINB");
     const int minb = e_lb ? atoi(e_lb) : 1;
-    KernelFn kern = (a.fmt == QMM_Q4_K) ? pick<QMM_Q4_K>(w, p.rpg, minb)
-                                        : pick<QMM_Q8_0>(w, p.rpg, minb);
+    KernelFn kern;
+    switch (a.fmt) {
+    case QMM_Q4_K: kern = pick<QMM_Q4_K>(w, p.rpg, minb); break;
+    case QMM_Q8_0: kern = pick<QMM_Q8_0>(w, p.rpg, minb); break;
+    case QMM_Q5_K: kern = pick_rpg<QMM_Q5_K, 32, 1>(p.rpg); break;
+    case QMM_Q6_K: kern = pick_rpg<QMM_Q6_K, 32, 1>(p.rpg); break;
+    default: kern = pick_rpg<QMM_IQ4_NL, 32, 1>(p.rpg); break;
+    }
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem);
     if (e != cudaSuccess)
         return e;

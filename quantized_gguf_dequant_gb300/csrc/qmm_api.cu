@@ -289,6 +289,40 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     return QMM_OK;
 }
 
+// The staged fp32 GEMV (gemv.cu) for n matrices sharing x, with a given
+// plan (its K-slice partials in handle 0's workspace).
+qmm_status do_gemv_staged(const qmm_t *hs, int n, const float *x, float *const *ys,
+                          const qmm::GemvPlan &p, cudaStream_t s, const char *fn)
+{
+    const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    qmm::GemvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.fmt = m0.fmt;
+    a.nmat = n;
+    a.K = m0.K;
+    a.row_bytes = m0.row_bytes;
+    a.x = x;
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
+        a.w[i] = mi.w;
+        a.y[i] = ys[i];
+        total += mi.N;
+        a.row_end[i] = total;
+    }
+    for (int i = n; i < qmm::kMaxGroup; ++i)
+        a.row_end[i] = total;
+    a.N = total;
+    a.status = m0.status;
+    a.ws = m0.ws;
+    a.tickets = m0.tickets;
+    cudaError_t e = qmm::launch_gemv(p, a, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, fn);
+    reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
+    return QMM_OK;
+}
+
 // Weight bytes up to which a Q4_K GEMV (one row, a matrix or a group) takes
 // the SIMT kernel instead of the decode kernel (QMM_Q4K_SMALL_BYTES; 0 by
 // default).  Measured on the 1024 x 1024 matrix: the same 8.8 us for one
@@ -315,6 +349,23 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
         for (int i = 0; i < n; ++i)
             bytes += reinterpret_cast<const Matrix *>(hs[i])->N * m0.row_bytes;
         simt_ok = (qp && strcmp(qp, "fmt") == 0) || (!qp && bytes <= q4k_small_bytes());
+    }
+    // Q6_K takes the staged fp32 kernel where its 32-lane teams and 16-byte
+    // bulk copies fit (measured on the Llama-3.1-8B shapes: 0.358 against
+    // 0.406 ms for 4 layers on the SIMT kernel); Q5_K and IQ4_NL measured
+    // faster on the SIMT kernel (0.266 / 0.287 against 0.334 / 0.364 ms).
+    // QMM_FMT_PATH = staged, fast or plain picks the route for all three.
+    const char *fp = getenv("QMM_FMT_PATH");
+    const bool staged_pref = fp ? strcmp(fp, "staged") == 0 : m0.fmt == QMM_Q6_K;
+    if (qmm::is_extra_format(m0.fmt) && m0.K % 256 == 0 && staged_pref) {
+        int64_t total = 0;
+        for (int i = 0; i < n; ++i)
+            total += reinterpret_cast<const Matrix *>(hs[i])->N;
+        qmm::GemvPlan p = qmm::plan_gemv(m0.fmt, total, m0.K, m0.sm_count, env_int("QMM_SPLITK"));
+        if (qmm::gemv_plan_takes(m0.fmt, p, m0.row_bytes) &&
+            qmm::gemv_workspace_floats(p, total) <= m0.ws_floats &&
+            size_t(p.row_slices) <= m0.n_tickets)
+            return do_gemv_staged(hs, n, x, ys, p, s, fn);
     }
     if (simt_ok && qmm::fmt_fast_rows(m0, 1) > 0) {
         const Matrix *ms[qmm::kMaxGroup];
@@ -352,25 +403,9 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
         if (st != QMM_ERR_UNSUPPORTED)
             return st;
     }
-    qmm::GemvArgs a;
-    memset(&a, 0, sizeof(a));
-    a.fmt = m0.fmt;
-    a.nmat = n;
-    a.K = m0.K;
-    a.row_bytes = m0.row_bytes;
-    a.x = x;
     int64_t total = 0;
-    for (int i = 0; i < n; ++i) {
-        const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
-        a.w[i] = mi.w;
-        a.y[i] = ys[i];
-        total += mi.N;
-        a.row_end[i] = total;
-    }
-    for (int i = n; i < qmm::kMaxGroup; ++i)
-        a.row_end[i] = total;
-    a.N = total;
-    a.status = m0.status;
+    for (int i = 0; i < n; ++i)
+        total += reinterpret_cast<const Matrix *>(hs[i])->N;
     qmm::GemvPlan p = qmm::plan_gemv(m0.fmt, total, m0.K, m0.sm_count, env_int("QMM_SPLITK"));
     if (p.ksplit > 1 && (qmm::gemv_workspace_floats(p, total) > m0.ws_floats ||
                          size_t(p.row_slices) > m0.n_tickets)) {
@@ -381,13 +416,7 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
                         fn, (long long)total);
         p = p1;
     }
-    a.ws = m0.ws;
-    a.tickets = m0.tickets;
-    cudaError_t e = qmm::launch_gemv(p, a, s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, fn);
-    reinterpret_cast<Matrix *>(hs[0])->last_stream = s;
-    return QMM_OK;
+    return do_gemv_staged(hs, n, x, ys, p, s, fn);
 }
 
 // ------------------------------------------------------------------ experts

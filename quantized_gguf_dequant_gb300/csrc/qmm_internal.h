@@ -158,6 +158,9 @@ struct GemvArgs {
 // Plan for N total rows of K columns; `force_ksplit` > 0 overrides split-K.
 GemvPlan plan_gemv(int fmt, int64_t N, int64_t K, int sm_count, int force_ksplit);
 size_t gemv_workspace_floats(const GemvPlan &p, int64_t N);
+// Whether launch_gemv takes this plan for the format (Q5_K / Q6_K / IQ4_NL
+// need 32-lane teams and 16-byte row and slice sizes).
+bool gemv_plan_takes(int fmt, const GemvPlan &p, int64_t row_bytes);
 cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
 
 // --------------------------------------------------------------- tensor-core Q4_K GEMV

@@ -5,6 +5,8 @@ batched GEMV within 1e-4 of sum|w x|, the dense FFN through its grouped
 route, and the refusals of the calls that take Q4_K only."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 
@@ -41,15 +43,17 @@ def test_dequant_bit_exact(fmt):
     m.close()
 
 
-@pytest.mark.parametrize("path", ["fast", "plain"])
+@pytest.mark.parametrize("path", ["default", "staged", "fast", "plain"])
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("N,K", [(1, 256), (9, 512), (300, 2048), (4096, 4096), (33, 768),
-                                 (77, 14336), (5, 8192)])
+                                 (77, 14336), (5, 8192), (1000, 6144)])
 def test_gemv(monkeypatch, path, fmt, N, K):
-    """The one-row GEMV: the fast kernel (16-byte or 4-byte loads straight to
-    registers; 1, 2, 3, 16, 32 and 56 units per row) and the plain one."""
-    if path == "plain":
-        monkeypatch.setenv("QMM_FMT_PATH", "plain")
+    """The one-row GEMV on every route: the staged fp32 kernel (where its
+    32-lane teams fit, K-sliced for long rows; the SIMT kernel elsewhere),
+    the SIMT kernel (1, 2, 3, 16, 24, 32 and 56 units per row), the plain
+    one, and the default choice among them."""
+    if path != "default":
+        monkeypatch.setenv("QMM_FMT_PATH", path)
     w, m = _matrix(fmt, N, K, seed=N + K + fmt)
     x = synth.activations(1, K, seed=K + 1)[0]
     y = m.gemv(to_dev(x)).cpu().numpy()
@@ -68,11 +72,16 @@ def test_gemv_batched(fmt, M):
     Y = m.gemv_batched(to_dev(X)).cpu().numpy()
     Yr, C = oracle.gemv(fmt, w, N, K, X, nthreads=NT)
     assert_close_to_oracle(Y, Yr, C, TOL_FP32, f"fmt={fmt} M={M}")
-    # the same bits as one row at a time, and as a repeated call
-    y0 = m.gemv(to_dev(X[0])).cpu().numpy()
-    assert np.array_equal(Y[0].view(np.uint32), y0.view(np.uint32))
+    # a repeated call gives the same bits; so does one row at a time on the
+    # same (SIMT) kernel
     Y2 = m.gemv_batched(to_dev(X)).cpu().numpy()
     assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+    os.environ["QMM_FMT_PATH"] = "fast"
+    try:
+        y0 = m.gemv(to_dev(X[0])).cpu().numpy()
+    finally:
+        del os.environ["QMM_FMT_PATH"]
+    assert np.array_equal(Y[0].view(np.uint32), y0.view(np.uint32))
     m.close()
 
 
