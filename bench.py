@@ -348,7 +348,7 @@ class MoeModel:
     32 tokens routed top-8 by a seeded softmax; one step runs every layer's
     whole expert FFN (bucket, gate+up, SwiGLU, down, combine)."""
 
-    def __init__(self, layers=16, T=32, device="cuda"):
+    def __init__(self, layers=16, T=32, device="cuda", fmt=synth.Q4_K):
         import torch
         import quantized_gguf_dequant_gb300 as q
         self.q = q
@@ -356,12 +356,13 @@ class MoeModel:
         self.E, self.T, self.k, self.dm, self.dff = E, T, k, dm, dff
         self.layers = []
         self.active_bytes = 0
-        per_expert = 3 * dff * synth.row_bytes(synth.Q4_K, dm)  # gate, up, down (same size)
+        # gate, up (dff rows of dm) and down (dm rows of dff)
+        per_expert = 2 * dff * synth.row_bytes(fmt, dm) + dm * synth.row_bytes(fmt, dff)
         for L in range(layers):
             hs = []
             for j, (N, K) in enumerate(((E * dff, dm), (E * dff, dm), (E * dm, dff))):
-                w = synth.q4k_matrix(N, K, synth.layer_seed(SEED + 100, L, j))
-                hs.append(q.Matrix(synth.Q4_K, N, K, torch.from_numpy(w).to(device)))
+                w = synth.matrix(fmt, N, K, synth.layer_seed(SEED + 100, L, j))
+                hs.append(q.Matrix(fmt, N, K, torch.from_numpy(w).to(device)))
             ids, r = synth.router(T, E, k, synth.layer_seed(SEED + 200, L, 0))
             X = synth.activations(T, dm, synth.layer_seed(SEED + 300, L, 0))
             self.active_bytes += len(np.unique(ids)) * per_expert
@@ -731,6 +732,21 @@ def run_ours(args, world, rank, local):
             "note": "qmm_moe_ffn per layer (bucket, gate+up, SwiGLU, down, combine); bytes = "
                     "the Q4_K gate/up/down bytes of every expert some token picked, plus X, Y, "
                     "ids and routing weights; 16 layers = 3.6 GB of experts > L2"}
+        mo.close()
+        del mo
+        torch.cuda.empty_cache()
+        mo = MoeModel(fmt=synth.Q8_0)
+        st_m = time_graph_stats(mo.step, max(20, args.steps // 4), args.warmup, world)
+        ms_m = st_m["median_ms"]
+        bm_ = mo.bytes_per_step()
+        extras["olmoe_moe_ffn_q8_0"] = {
+            "value": bm_ / (ms_m * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_m,
+            "min_ms": st_m["min_ms"], "reps": st_m["reps"],
+            "bytes_per_step": bm_, "layers": len(mo.layers), "tokens": mo.T,
+            "frac_of_peak": bm_ / (ms_m * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "us_per_layer": ms_m * 1e3 / len(mo.layers), "launches_per_step": launches_of(mo.step),
+            "note": "the same OLMoE expert FFN with Q8_0 experts (moe_q8_kernel for gate+up "
+                    "with SwiGLU, and for down); 16 layers = 6.8 GB of experts"}
         mo.close()
         del mo
         torch.cuda.empty_cache()

@@ -152,11 +152,15 @@ QMM_API qmm_status qmm_gemv_batched(qmm_t h, const float *X, int64_t M, int64_t 
  * order).  route_on_input == 1 (route_w required; the Llama 4 form, where
  * the routing weight multiplies the expert's input -- "Architecture
  * coverage: 100 models with evidence"): Y is [T*top_k, N_e],
- * Y[t*top_k+s] = W_{ids[t,s]} (route_w[t,s] * x), the product r*x rounded to
- * fp32 as the activations are loaded, no sum over slots.  Each
+ * Y[t*top_k+s] = W_{ids[t,s]} (route_w[t,s] * x), no sum over slots (Q4_K:
+ * the product r*x rounded to fp32 as the activations are loaded; Q8_0: r
+ * times the slot's fp32 dot product, the same value up to rounding).  Each
  * expert's rows are read once per call for all of its slots.  An id outside
  * [0, n_experts) leaves that slot's contribution 0 and sets QMM_ERR_EXPERT in
- * the status word.  1 <= T*top_k <= 4096, top_k <= 16. */
+ * the status word.  1 <= T*top_k <= 4096, top_k <= 16.  Formats: Q4_K, and
+ * Q8_0 with K a multiple of 256 (Q8_0: "Frink Inference: the Rust
+ * alternative to llama.cpp", "Where llama.cpp is still ahead"); anything
+ * else is refused with QMM_ERR_UNSUPPORTED. */
 QMM_API qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids,
                         int32_t T, int32_t top_k, const float *X,
                         int32_t x_per_slot, const float *route_w, int32_t route_on_input,
@@ -176,8 +180,9 @@ QMM_API qmm_status qmm_swiglu(const float *g, const float *u, float *h, int64_t 
  * "Architecture coverage: 100 models with evidence": the expert weight
  * applied to the input of the expert), h = silu(Wg (r x)) * (Wu (r x)),
  * y_t = sum_s Wd h; SwiGLU makes the two differ.  Uses hg's workspace for
- * the [T*top_k, d_ff] intermediate.  Same limits and id checking as
- * qmm_moe_gemv. */
+ * the [T*top_k, d_ff] intermediate.  Same limits, formats and id checking as
+ * qmm_moe_gemv; gate and up must share a format (they run in one launch;
+ * QMM_ERR_FORMAT otherwise), down may be the other one. */
 QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
                        const int32_t *expert_ids, int32_t T, int32_t top_k,
                        const float *X, const float *route_w, int32_t route_on_input,

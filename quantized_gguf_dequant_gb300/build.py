@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqmm.so")
-SOURCES = ["qmm_api.cu", "dequant.cu", "gemv.cu", "gemv_tc.cu", "qmm_noalloc.cu", "moe.cu", "gemm_tc.cu", "tmap.cu", "gemv_batched.cu", "formats.cu", "gemv_m1.cu", "q8k.cu", "formats_fast.cu", "gemv_tc5.cu"]
+SOURCES = ["qmm_api.cu", "dequant.cu", "gemv.cu", "gemv_tc.cu", "qmm_noalloc.cu", "moe.cu", "gemm_tc.cu", "tmap.cu", "gemv_batched.cu", "formats.cu", "gemv_m1.cu", "q8k.cu", "formats_fast.cu", "gemv_tc5.cu", "moe_q8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -425,10 +425,11 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
 qmm_status moe_check(const Matrix &m, int n_experts, const int32_t *ids, int T, int top_k,
                      const char *fn)
 {
-    if (m.fmt != QMM_Q4_K)
+    if (m.fmt != QMM_Q4_K && !(m.fmt == QMM_Q8_0 && m.has_moe_map))
         return fail(QMM_ERR_UNSUPPORTED,
-                    "%s: the expert GEMV is implemented for Q4_K weights only (this handle is "
-                    "format %d)", fn, m.fmt);
+                    "%s: the expert GEMV is implemented for Q4_K weights and for Q8_0 weights "
+                    "with K a multiple of 256 (this handle is format %d, K = %lld)", fn, m.fmt,
+                    (long long)m.K);
     if (!ids)
         return fail(QMM_ERR_NULL, "%s: expert_ids is NULL", fn);
     if (n_experts < 1 || n_experts > qmm::kMoeMaxExperts)
@@ -447,7 +448,7 @@ qmm_status moe_check(const Matrix &m, int n_experts, const int32_t *ids, int T, 
         return fail(QMM_ERR_ALIGN, "%s: expert_ids is not 4-byte aligned", fn);
     int nw, nslot;
     qmm::moe_expert_shape(m.K, nw, nslot);
-    if (qmm::moe_expert_smem(m.K, nw, nslot, 0) > kMaxSmem)
+    if (m.fmt == QMM_Q4_K && qmm::moe_expert_smem(m.K, nw, nslot, 0) > kMaxSmem)
         return fail(QMM_ERR_SHAPE, "%s: K = %lld is too long for the expert kernel's shared "
                     "memory (%zu bytes needed)", fn, (long long)m.K,
                     qmm::moe_expert_smem(m.K, nw, nslot, 0));
@@ -700,6 +701,12 @@ qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev, q
                                       "could not be encoded");
         }
         m->has_gemm_maps = true;
+        if (qmm::encode_moe_q8_map(m->tmap_moe, w_dev, N, m->row_bytes) != 0) {
+            delete m;
+            return fail(QMM_ERR_CUDA, "qmm_create: the TMA tensor map for the expert GEMV "
+                                      "could not be encoded");
+        }
+        m->has_moe_map = true;
     }
     void *p = nullptr;
     const size_t bytes = m->ws_floats * 4 + m->n_tickets * 4 + 256;
@@ -928,7 +935,7 @@ qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, i
     if (e == cudaSuccess) {
         qmm::MoeExpertArgs a;
         memset(&a, 0, sizeof(a));
-        a.tmap[0] = m->tmap;
+        a.tmap[0] = m->fmt == QMM_Q8_0 ? m->tmap_moe : m->tmap;
         a.y[0] = combine ? ms.ys : Y;
         a.xscale = route_on_input ? route_w : nullptr;
         a.nmat = 1;
@@ -940,7 +947,8 @@ qmm_status qmm_moe_gemv(qmm_t h, int32_t n_experts, const int32_t *expert_ids, i
         a.x_per_slot = x_per_slot;
         a.ix = ms.ix;
         a.status = m->status;
-        e = qmm::launch_moe_expert(a, m->sm_count, s);
+        e = m->fmt == QMM_Q8_0 ? qmm::launch_moe_q8(a, m->sm_count, s)
+                               : qmm::launch_moe_expert(a, m->sm_count, s);
     }
     if (e == cudaSuccess && combine)
         e = qmm::launch_moe_combine(ms.ys, route_w, expert_ids, n_experts, T, top_k, Ne, Y,
@@ -999,6 +1007,9 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     if (st != QMM_OK)
         return st;
     const int64_t d_ff = mg->N / n_experts, d_model = mg->K;
+    if (mu->fmt != mg->fmt)
+        return fail(QMM_ERR_FORMAT, "%s: gate (format %d) and up (format %d) must share a format "
+                    "(they run in one launch)", fn, mg->fmt, mu->fmt);
     if (mu->N != mg->N || mu->K != mg->K || md->K != d_ff || md->N != int64_t(n_experts) * d_model)
         return fail(QMM_ERR_SHAPE,
                     "%s: shapes disagree: gate %lld x %lld, up %lld x %lld, down %lld x %lld; "
@@ -1037,11 +1048,12 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
     const int64_t tpm = (d_ff + 15) / 16;
     const int maxpairs =
         int((int64_t(qmm::moe_max_groups(S, n_experts)) * tpm + sms - 1) / sms) + 1;
+    const bool q8 = mg->fmt == QMM_Q8_0;
     const bool fuse = !getenv("QMM_MOE_NOFUSE") &&
-                      qmm::moe_expert_smem(d_model, nw, nslot, maxpairs) <= kMaxSmem;
+                      (q8 || qmm::moe_expert_smem(d_model, nw, nslot, maxpairs) <= kMaxSmem);
     if (e == cudaSuccess) {
-        a.tmap[0] = mg->tmap;
-        a.tmap[1] = mu->tmap;
+        a.tmap[0] = q8 ? mg->tmap_moe : mg->tmap;
+        a.tmap[1] = q8 ? mu->tmap_moe : mu->tmap;
         a.y[0] = fuse ? ms.h : ms.g;
         a.y[1] = fuse ? nullptr : ms.u;
         a.nmat = 2;
@@ -1053,14 +1065,14 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
         a.xscale = route_on_input ? route_w : nullptr;
         a.fuse_swiglu = fuse ? 1 : 0;
         a.maxpairs = maxpairs;
-        e = qmm::launch_moe_expert(a, sms, s);
+        e = q8 ? qmm::launch_moe_q8(a, sms, s) : qmm::launch_moe_expert(a, sms, s);
     }
     if (e == cudaSuccess && !fuse)
         e = qmm::launch_swiglu(ms.g, ms.u, ms.h, int64_t(S) * d_ff, sms, s);
     a.fuse_swiglu = 0;
     a.xscale = nullptr;
     if (e == cudaSuccess) {  // down, one input row per slot
-        a.tmap[0] = md->tmap;
+        a.tmap[0] = md->fmt == QMM_Q8_0 ? md->tmap_moe : md->tmap;
         a.tmap[1] = nullptr;
         a.y[0] = ms.ys;
         a.y[1] = nullptr;
@@ -1070,7 +1082,7 @@ qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
         a.x = ms.h;
         a.ldx = d_ff;
         a.x_per_slot = 1;
-        e = qmm::launch_moe_expert(a, sms, s);
+        e = md->fmt == QMM_Q8_0 ? qmm::launch_moe_q8(a, sms, s) : qmm::launch_moe_expert(a, sms, s);
     }
     if (e == cudaSuccess)
         e = qmm::launch_moe_combine(ms.ys, route_on_input ? nullptr : route_w, expert_ids,

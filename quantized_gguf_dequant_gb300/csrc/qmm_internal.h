@@ -41,6 +41,9 @@ struct Matrix {
     alignas(64) unsigned char tmap_hdr[128];
     alignas(64) unsigned char tmap_nib[128];  // Q8_0: 80-byte windows, 256 rows
     bool has_gemm_maps = false;
+    // Q8_0 expert GEMV: the rows as u32 words, boxes of one 272-byte slice x 32 rows
+    alignas(64) unsigned char tmap_moe[128];
+    bool has_moe_map = false;
     // batched GEMV scratch: the K-slice partial sums (grown on demand)
     void *tcb_ws = nullptr;
     size_t tcb_ws_bytes = 0;
@@ -318,6 +321,13 @@ cudaError_t launch_moe_bucket(const int32_t *ids, int S, int E, const MoeIndex &
 void moe_expert_shape(int64_t K, int &nw, int &nslot);
 size_t moe_expert_smem(int64_t K, int nw, int nslot, int maxpairs);
 cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t s);
+// moe_q8.cu: the expert GEMV for Q8_0 weights (K % 256 == 0), on the same
+// bucketing and arguments (tmap: the maps of encode_moe_q8_map; maxpairs
+// unused; SwiGLU fusion always fits).
+size_t moe_q8_smem(int nstage);
+int moe_q8_stages();
+int encode_moe_q8_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
+cudaError_t launch_moe_q8(const MoeExpertArgs &a, int sm_count, cudaStream_t s);
 cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, int sm_count,
                           cudaStream_t s);
 cudaError_t launch_moe_combine(const float *ys, const float *r, const int32_t *ids, int E, int T,
