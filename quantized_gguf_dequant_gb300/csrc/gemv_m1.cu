@@ -111,8 +111,13 @@ __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, i
     return row < P.rows[m];
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const __grid_constant__ M1Params P)
 {
+    // super-block bytes, one unit's bytes (16 rows), offset of the nibbles
+    constexpr int SB = FMT == QMM_Q5_K ? 176 : 144;
+    constexpr int UB = kTileRows * SB;
+    constexpr int QOFF = FMT == QMM_Q5_K ? 48 : 16;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
     const int lane = threadIdx.x & 31;
@@ -181,12 +186,12 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 const bool mine = lane < TS && tile < P.T;
                 const int nvalid = __popc(__ballot_sync(0xffffffffu, mine));
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * WS) * kTileBytes);
+                    mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * WS) * UB);
                 __syncwarp();
                 if (mine) {
                     const int m = mat_of_tile(P, tile);
                     const int lt = tile - (m == 0 ? 0 : P.tile_end[m - 1]);
-                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * kTileBytes,
+                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
                                 &P.tmap[m], lt * kTileRows, sb0 + p * WS, &full[slot], pol);
                 }
             } else if (lane == 0) {
@@ -307,8 +312,9 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         load_b(0);
         const int slot_bytes = P.slot_bytes;
         // This lane's bytes of its unit in slot 0: header of row g (and of
-        // row g+8 at +8*144), its 32-byte nibble chunk at +16+32c.
-        const uint32_t ubase = smem_u32(ring) + uint32_t(warp * kTileBytes + g * 144);
+        // row g+8 at +8*SB), its 32-byte nibble chunk at +QOFF+32c (Q5_K: the
+        // 32 fifth-bit bytes at +16).
+        const uint32_t ubase = smem_u32(ring) + uint32_t(warp * UB + g * SB);
         // Column wsb of the partial sums; lanes c = 0 and 1 own rows g and
         // g+8 of tile wt of the item.
         const uint32_t pbase =
@@ -331,11 +337,18 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             const int p = *(volatile int *)&s_pass[slot];
             const uint32_t a0 = ubase + soff;
             const uint4 h0 = lds128(a0);
-            const uint4 h1 = lds128(a0 + 8 * 144);
-            const uint4 qa0 = lds128(a0 + 16 + 32 * c);
-            const uint4 qa1 = lds128(a0 + 32 + 32 * c);
-            const uint4 qb0 = lds128(a0 + 8 * 144 + 16 + 32 * c);
-            const uint4 qb1 = lds128(a0 + 8 * 144 + 32 + 32 * c);
+            const uint4 h1 = lds128(a0 + 8 * SB);
+            const uint4 qa0 = lds128(a0 + QOFF + 32 * c);
+            const uint4 qa1 = lds128(a0 + QOFF + 16 + 32 * c);
+            const uint4 qb0 = lds128(a0 + 8 * SB + QOFF + 32 * c);
+            const uint4 qb1 = lds128(a0 + 8 * SB + QOFF + 16 + 32 * c);
+            uint4 ha0, ha1, hb0, hb1;
+            if constexpr (FMT == QMM_Q5_K) {
+                ha0 = lds128(a0 + 16);
+                ha1 = lds128(a0 + 32);
+                hb0 = lds128(a0 + 8 * SB + 16);
+                hb1 = lds128(a0 + 8 * SB + 32);
+            }
             mbar_arrive(&empty[slot]);  // the unit is in registers: release the slot
             soff += uint32_t(slot_bytes);
             if (++slot == NS) {
@@ -352,7 +365,12 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 items[kc] = it;
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
-            float keep = unit_rows(h0, h1, qa0, qa1, qb0, qb1, B, L, c, X0, X1, iv);
+            float keep;
+            if constexpr (FMT == QMM_Q5_K)
+                keep = unit_rows5(h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1, B, L, c, X0, X1,
+                                  iv);
+            else
+                keep = unit_rows(h0, h1, qa0, qa1, qb0, qb1, B, L, c, X0, X1, iv);
             const uint32_t pa = pbase + uint32_t(kc * itile * 4);
             if (p > 0)
                 keep = lds_f32_if(pa, writer) + keep;  // passes added in order
@@ -429,10 +447,10 @@ int env_m1_slices()
 
 } // namespace
 
-size_t m1_smem(int KS, int WS, int TS, int cap, int nslot)
+size_t m1_smem(int KS, int WS, int TS, int cap, int nslot, int sb_bytes)
 {
     const int W = WS * TS;
-    return size_t(nslot) * (size_t(W) * kTileBytes + 16) + size_t(KS) * 1024 + size_t(KS) * 32 +
+    return size_t(nslot) * (size_t(W) * kTileRows * sb_bytes + 16) + size_t(KS) * 1024 + size_t(KS) * 32 +
            size_t((KS + 3) & ~3) * 4 + size_t(WS) * cap * TS * kTileRows * 4 + size_t(cap) * 8 + 8;
 }
 
@@ -442,7 +460,7 @@ int env_m1_warps()
     return (e && atoi(e) == 8) ? 8 : kM1MaxWarps;
 }
 
-M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int sb_bytes)
 {
     M1Plan p;
     if (maxw <= 0)
@@ -529,7 +547,7 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
     p.cap = 2 * avg + 2;
     auto slots = [&](int cap) {
         int ns = 0;
-        while (ns < 16 && m1_smem(p.KS, p.WS, p.TS, cap, ns + 1) <= budget)
+        while (ns < 16 && m1_smem(p.KS, p.WS, p.TS, cap, ns + 1, sb_bytes) <= budget)
             ++ns;
         return ns;
     };
@@ -545,8 +563,8 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw)
     p.F = avg * p.NP <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
     if (p.F < 1)
         p.F = 1;
-    p.slot_bytes = p.W * kTileBytes;
-    p.smem = m1_smem(p.KS, p.WS, p.TS, p.cap, ns);
+    p.slot_bytes = p.W * kTileRows * sb_bytes;
+    p.smem = m1_smem(p.KS, p.WS, p.TS, p.cap, ns, sb_bytes);
     p.ws_floats = S > 1 ? size_t(S) * size_t(T) * kTileRows : 0;
     p.tickets = size_t(2 * S) + (S > 1 ? size_t(p.n_items) : 0);
     return p;
@@ -586,7 +604,8 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.slot_bytes = p.slot_bytes;
     // All shared memory preferred, so that two half-SM CTAs (this launch
     // and the next) fit side by side.
-    cudaError_t e = func_smem(reinterpret_cast<const void *>(gemv_m1_kernel), p.smem, true);
+    const auto kern = a.fmt == QMM_Q5_K ? gemv_m1_kernel<QMM_Q5_K> : gemv_m1_kernel<QMM_Q4_K>;
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem, true);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -599,7 +618,7 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return counted(cudaLaunchKernelEx(&cfg, gemv_m1_kernel, P));
+    return counted(cudaLaunchKernelEx(&cfg, kern, P));
 }
 
 } // namespace qmm

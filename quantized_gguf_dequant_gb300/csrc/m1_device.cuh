@@ -1,4 +1,4 @@
-// m1_device.cuh -- device building blocks of the one-row Q4_K decode kernel
+// m1_device.cuh -- device building blocks of the one-row Q4_K / Q5_K decode kernel
 // (gemv_m1.cu): shared-memory and TMA helpers, the super-block header
 // decode, the activation layout, and the arithmetic of one unit (16 rows x
 // 256 weights) described at the top of gemv_m1.cu.
@@ -217,6 +217,52 @@ __device__ __forceinline__ float unit_rows(uint4 h0, uint4 h1, uint4 qa0, uint4 
         } else {
             mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
             mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
+        }
+    }
+    const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
+                                                          make_float2(dlo[1], dlo[3])),
+                                  __fadd2_rn(make_float2(dhi[0], dhi[2]), make_float2(dhi[1], dhi[3])),
+                                  X0, X1, iv);
+    const bool odd = c & 1;
+    float keep = odd ? tot.y : tot.x;
+    keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    return keep;
+}
+
+// unit_rows for Q5_K: the same operands with each code's fifth bit (qh
+// bytes l of the super-block's 32: bit 2c for the low nibble of chunk byte
+// 32c + l, bit 2c+1 for the high one) put above its nibble -- bit 4 of the
+// low-nibble half (value q * 2^-24, q < 32) and bit 8 of the high-nibble
+// half (value 16 q * 2^-24): still exact fp16 subnormals.  ha / hb: the 32
+// qh bytes of rows g and g+8.
+__device__ __forceinline__ float unit_rows5(uint4 h0, uint4 h1, uint4 qa0, uint4 qa1, uint4 qb0,
+                                            uint4 qb1, uint4 ha0, uint4 ha1, uint4 hb0, uint4 hb1,
+                                            const uint4 (&B)[8], const ScaleSel &L, int c,
+                                            float2 X0, float2 X1, float2 iv)
+{
+    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
+    const uint32_t blo = 0x00100010u, bhi = 0x01000100u;
+    const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+    const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+    const uint32_t va[8] = {ha0.x, ha0.y, ha0.z, ha0.w, ha1.x, ha1.y, ha1.z, ha1.w};
+    const uint32_t vb[8] = {hb0.x, hb0.y, hb0.z, hb0.w, hb1.x, hb1.y, hb1.z, hb1.w};
+    const int sh = 2 * c;
+    float dlo[4], dhi[4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
+        const uint32_t pa = va[t] >> sh, pb = vb[t] >> sh, qa = pa >> 8, qb = pb >> 8;
+        const uint32_t a0 = (xa & mlo) | ((pa << 4) & blo), a1 = (xb & mlo) | ((pb << 4) & blo);
+        const uint32_t a2 = (ya & mlo) | ((qa << 4) & blo), a3 = (yb & mlo) | ((qb << 4) & blo);
+        const uint32_t b0 = (xa & mhi) | ((pa << 7) & bhi), b1 = (xb & mhi) | ((pb << 7) & bhi);
+        const uint32_t b2 = (ya & mhi) | ((qa << 7) & bhi), b3 = (yb & mhi) | ((qb << 7) & bhi);
+        if (t == 0) {
+            mma16816_zero(dlo, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816_zero(dhi, b0, b1, b2, b3, B[t].z, B[t].w);
+        } else {
+            mma16816(dlo, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816(dhi, b0, b1, b2, b3, B[t].z, B[t].w);
         }
     }
     const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),

@@ -238,7 +238,7 @@ qmm_status do_gemv_tc5(qmm_t h, const float *X, int64_t ldx, int M, float *Y, in
     return QMM_OK;
 }
 
-// The one-row Q4_K decode kernel (gemv_m1.cu) for n matrices sharing x.
+// The one-row Q4_K / Q5_K decode kernel (gemv_m1.cu) for n matrices sharing x.
 // QMM_ERR_UNSUPPORTED (nothing launched) when no plan fits its shared memory
 // or the handle's workspace.  QMM_M1_S fixes the number of K slices.
 qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
@@ -250,7 +250,7 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     int64_t T = 0;
     for (int i = 0; i < n; ++i) {
         const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
-        if (!mi.has_tmap)
+        if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K) || mi.K % 256 != 0)
             return QMM_ERR_UNSUPPORTED;
         a.rows[i] = mi.N;
         a.y[i] = ys[i];
@@ -259,11 +259,12 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     if (T * 16 > (int64_t(1) << 30))
         return QMM_ERR_UNSUPPORTED;
     const int64_t NB = m0.K / 256;
-    qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0);
+    const int sbb = m0.fmt == QMM_Q5_K ? 176 : 144;
+    qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0, 0, sbb);
     // Fewer K slices when the handle's workspace or tickets are too small.
     for (int S = p.S; S >= 1 && (p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets); --S)
         if (NB % S == 0)
-            p = qmm::plan_m1(T, NB, m0.sm_count, S);
+            p = qmm::plan_m1(T, NB, m0.sm_count, S, 0, sbb);
     if (p.nslot < 2 || p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets)
         return QMM_ERR_UNSUPPORTED;
     // Each matrix's column view with boxes of this plan's pass width (kept
@@ -271,12 +272,13 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     for (int i = 0; i < n; ++i) {
         Matrix &mi = *reinterpret_cast<Matrix *>(hs[i]);
         if (mi.tmap3_ks != p.WS) {
-            if (qmm::make_q4k_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.WS) != 0)
+            if (qmm::make_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.WS, sbb) != 0)
                 return QMM_ERR_UNSUPPORTED;
             mi.tmap3_ks = p.WS;
         }
         a.tmap[i] = mi.tmap3;
     }
+    a.fmt = m0.fmt;
     a.nmat = n;
     a.x = x;
     a.ws = m0.ws;
@@ -356,6 +358,13 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
     // faster on the SIMT kernel (0.266 / 0.287 against 0.334 / 0.364 ms).
     // QMM_FMT_PATH = staged, fast or plain picks the route for all three.
     const char *fp = getenv("QMM_FMT_PATH");
+    // Q5_K: the tensor-core decode kernel of Q4_K with the fifth bits added
+    // to the operands (QMM_FMT_PATH=staged, fast or plain keeps it off).
+    if (m0.fmt == QMM_Q5_K && !fp) {
+        qmm_status st = do_gemv_m1(hs, n, x, ys, s, fn);
+        if (st != QMM_ERR_UNSUPPORTED)
+            return st;
+    }
     const bool staged_pref = fp ? strcmp(fp, "staged") == 0 : m0.fmt == QMM_Q6_K;
     if (qmm::is_extra_format(m0.fmt) && m0.K % 256 == 0 && staged_pref) {
         int64_t total = 0;

@@ -206,6 +206,7 @@ struct M1Plan {
     size_t tickets = 0;          // counters: 2 per slice, plus one per item when S > 1
 };
 struct M1Args {
+    int fmt;                      // QMM_Q4_K or QMM_Q5_K
     const void *tmap[kMaxGroup];  // Matrix::tmap3 of each matrix (boxes of WS super-blocks)
     int64_t rows[kMaxGroup];
     float *y[kMaxGroup];
@@ -219,8 +220,10 @@ struct M1Args {
 // fixes the number of K slices (it must divide NB).
 // maxw: 8 or 16 consumer warps at most (0: QMM_M1_WARPS, default 16).
 // nslot == 0: no plan fits.
-M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw = 0);
-size_t m1_smem(int KS, int WS, int TS, int cap, int nslot);
+// sb_bytes: 144 (Q4_K) or 176 (Q5_K).
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw = 0,
+               int sb_bytes = 144);
+size_t m1_smem(int KS, int WS, int TS, int cap, int nslot, int sb_bytes = 144);
 cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s);
 
 // --------------------------------------------------------------- batched tensor-core Q4_K GEMV
@@ -254,7 +257,10 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle);
 // The 3-D column view of a Q4_K matrix (tmap.cu) with boxes of one 16-row
 // tile x ks super-blocks; 0 on success.
-int make_q4k_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks);
+// 3-D column view (super-block bytes as u64 words, row, super-block) with
+// boxes of 16 rows x ks super-blocks; sb_bytes 144 (Q4_K) or 176 (Q5_K).
+int make_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks,
+                    int sb_bytes);
 
 // --------------------------------------------------------------- prefill GEMM
 constexpr int kGemmMaxGroup = 4;

@@ -43,19 +43,22 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
     return r == CUDA_SUCCESS ? 0 : -2;
 }
 
-// A Q4_K matrix of N rows seen as a 3-D tensor of uint64 words: (18 words =
-// one 144-byte super-block, N rows, NB super-blocks), strides row_bytes and
-// 144 bytes.  A box (18, 16, ks) is then one 16-row tile of ks consecutive
-// super-blocks, landing in shared memory as ks units of 16 rows x 144 bytes
-// (super-block major), every row 144 bytes after the previous one.
-int make_q4k_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks)
+// A Q4_K (Q5_K) matrix of N rows seen as a 3-D tensor of uint64 words: (18
+// (22) words = one 144 (176)-byte super-block, N rows, NB super-blocks),
+// strides row_bytes and the super-block size.  A box (words, 16, ks) is then
+// one 16-row tile of ks consecutive super-blocks, landing in shared memory as
+// ks units of 16 rows (super-block major), every row one super-block after
+// the previous one.
+int make_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks,
+                    int sb_bytes)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
     if (!encode)
         return -1;
-    const cuuint64_t dims[3] = {18u, cuuint64_t(N), cuuint64_t(row_bytes / 144)};
-    const cuuint64_t strides[2] = {cuuint64_t(row_bytes), 144u};
-    const cuuint32_t box[3] = {18u, 16u, cuuint32_t(ks)};
+    const cuuint32_t words = cuuint32_t(sb_bytes / 8);
+    const cuuint64_t dims[3] = {words, cuuint64_t(N), cuuint64_t(row_bytes / sb_bytes)};
+    const cuuint64_t strides[2] = {cuuint64_t(row_bytes), cuuint64_t(sb_bytes)};
+    const cuuint32_t box[3] = {words, 16u, cuuint32_t(ks)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = encode(reinterpret_cast<CUtensorMap *>(out128), CU_TENSOR_MAP_DATA_TYPE_UINT64, 3,
                         const_cast<void *>(w), dims, strides, box, estr,

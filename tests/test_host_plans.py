@@ -34,8 +34,11 @@ def plans(tmp_path_factory):
     def objects():
         if not os.path.isdir(qbuild.BUILD):
             return []
+        # the objects of the current sources only (a stale object of a
+        # removed source would not link)
+        names = {os.path.splitext(src)[0] + ".o" for src in qbuild.SOURCES}
         return sorted(os.path.join(qbuild.BUILD, f) for f in os.listdir(qbuild.BUILD)
-                      if f.endswith(".o"))
+                      if f in names)
 
     objs = objects()
     if len(objs) < len(qbuild.SOURCES):  # the library exists but its objects were removed
