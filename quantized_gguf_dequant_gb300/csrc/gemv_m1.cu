@@ -114,10 +114,13 @@ __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, i
 template <int FMT>
 __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const __grid_constant__ M1Params P)
 {
-    // super-block bytes, one unit's bytes (16 rows), offset of the nibbles
-    constexpr int SB = FMT == QMM_Q5_K ? 176 : 144;
+    // super-block bytes, one unit's bytes (16 rows), offset of the nibbles,
+    // activation sums per super-block (Q6_K: one per 16-weight group)
+    constexpr bool Q6 = FMT == QMM_Q6_K;
+    constexpr int SB = FMT == QMM_Q5_K ? 176 : (Q6 ? 210 : 144);
     constexpr int UB = kTileRows * SB;
     constexpr int QOFF = FMT == QMM_Q5_K ? 48 : 16;
+    constexpr int XN = Q6 ? 16 : 8;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
     const int lane = threadIdx.x & 31;
@@ -126,13 +129,13 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     const int sb0 = sl * KS;
     const int itile = TS * kTileRows;  // rows of one item
 
-    // Shared memory: ring [NS][slot_bytes] | Bx [KS][8][4][2] uint4 | Xs [KS][8]
+    // Shared memory: ring [NS][slot_bytes] | Bx [KS][8][4][2] uint4 | Xs [KS][XN]
     // | inv [KS] | part [WS][cap*TS*16] | items [cap] | flags [cap] | full[NS],
     // empty[NS]
     uint8_t *ring = smem;
     uint4 *Bx = reinterpret_cast<uint4 *>(smem + size_t(NS) * P.slot_bytes);
     float *Xs = reinterpret_cast<float *>(Bx + size_t(KS) * 64);
-    float *inv = Xs + size_t(KS) * 8;
+    float *inv = Xs + size_t(KS) * XN;
     float *part = inv + ((KS + 3) & ~3);
     const int pcol = P.cap * itile;  // floats per column of partial sums
     int *items = reinterpret_cast<int *>(part + size_t(WS) * pcol);
@@ -191,8 +194,13 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 if (mine) {
                     const int m = mat_of_tile(P, tile);
                     const int lt = tile - (m == 0 ? 0 : P.tile_end[m - 1]);
-                    tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
-                                &P.tmap[m], lt * kTileRows, sb0 + p * WS, &full[slot], pol);
+                    if constexpr (Q6)  // 16 rows x 8 super-blocks (1680 bytes), row-major
+                        tma_load_2d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
+                                    &P.tmap[m], ((sb0 + p * WS) / 8) * 210, lt * kTileRows,
+                                    &full[slot], pol);
+                    else
+                        tma_load_3d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
+                                    &P.tmap[m], lt * kTileRows, sb0 + p * WS, &full[slot], pol);
                 }
             } else if (lane == 0) {
                 mbar_arrive(&full[slot]);  // completes the phase with no bytes
@@ -270,7 +278,11 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             // This slice of x -> B entries; super-blocks j = warp, warp + W, ...,
             // the loads of up to four in flight together.
             const int cc = lane >> 3, tt = lane & 7;
-            const float *xb = P.x + int64_t(sb0) * 256 + 64 * cc + 4 * tt;
+            // v: the weights of chunk cc's low nibbles, w (xb + wo): of its
+            // high nibbles
+            const float *xb = P.x + int64_t(sb0) * 256 +
+                              (Q6 ? 128 * (cc >> 1) + 32 * (cc & 1) : 64 * cc) + 4 * tt;
+            constexpr int wo = Q6 ? 64 : 32;
             for (int j0 = warp; j0 < KS; j0 += 4 * W) {
                 float4 v[4], w[4];
 #pragma unroll
@@ -278,14 +290,14 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                     const int j = j0 + i * W;
                     if (j < KS) {
                         v[i] = __ldg(reinterpret_cast<const float4 *>(xb + int64_t(j) * 256));
-                        w[i] = __ldg(reinterpret_cast<const float4 *>(xb + int64_t(j) * 256 + 32));
+                        w[i] = __ldg(reinterpret_cast<const float4 *>(xb + int64_t(j) * 256 + wo));
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int j = j0 + i * W;
                     if (j < KS)
-                        prep_sb(v[i], w[i], lane, Bx + size_t(j) * 64, Xs + j * 8, inv + j);
+                        prep_sb<Q6>(v[i], w[i], lane, Bx + size_t(j) * 64, Xs + j * XN, inv + j);
                 }
             }
         }
@@ -300,13 +312,20 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         // super-block of pass p (reloaded per pass when there are several).
         uint4 B[8];
         float2 X0, X1, iv;
+        float4 X6;  // Q6_K: the sums of the lane column's four 16-weight groups
+        const int g6 = 8 * (c >> 1) + 2 * (c & 1);
         auto load_b = [&](int p) {
             const int j = p * WS + wsb;
 #pragma unroll
             for (int t = 0; t < 8; ++t)
                 B[t] = act ? Bx[size_t(j) * 64 + (t * 4 + c) * 2 + term] : make_uint4(0u, 0u, 0u, 0u);
-            X0 = make_float2(Xs[j * 8 + 2 * c], Xs[j * 8 + 2 * c]);
-            X1 = make_float2(Xs[j * 8 + 2 * c + 1], Xs[j * 8 + 2 * c + 1]);
+            if constexpr (Q6) {
+                X6 = make_float4(Xs[j * XN + g6], Xs[j * XN + g6 + 1], Xs[j * XN + g6 + 4],
+                                 Xs[j * XN + g6 + 5]);
+            } else {
+                X0 = make_float2(Xs[j * XN + 2 * c], Xs[j * XN + 2 * c]);
+                X1 = make_float2(Xs[j * XN + 2 * c + 1], Xs[j * XN + 2 * c + 1]);
+            }
             iv = make_float2(inv[j], inv[j]);
         };
         load_b(0);
@@ -314,7 +333,9 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         // This lane's bytes of its unit in slot 0: header of row g (and of
         // row g+8 at +8*SB), its 32-byte nibble chunk at +QOFF+32c (Q5_K: the
         // 32 fifth-bit bytes at +16).
-        const uint32_t ubase = smem_u32(ring) + uint32_t(warp * UB + g * SB);
+        // Q6_K: a tile's box is 16 rows of WS (= 8) super-blocks, row-major.
+        const uint32_t ubase =
+            smem_u32(ring) + uint32_t(Q6 ? wt * WS * UB + g * WS * SB + wsb * SB : warp * UB + g * SB);
         // Column wsb of the partial sums; lanes c = 0 and 1 own rows g and
         // g+8 of tile wt of the item.
         const uint32_t pbase =
@@ -336,13 +357,26 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 break;
             const int p = *(volatile int *)&s_pass[slot];
             const uint32_t a0 = ubase + soff;
-            const uint4 h0 = lds128(a0);
-            const uint4 h1 = lds128(a0 + 8 * SB);
-            const uint4 qa0 = lds128(a0 + QOFF + 32 * c);
-            const uint4 qa1 = lds128(a0 + QOFF + 16 + 32 * c);
-            const uint4 qb0 = lds128(a0 + 8 * SB + QOFF + 32 * c);
-            const uint4 qb1 = lds128(a0 + 8 * SB + QOFF + 16 + 32 * c);
-            uint4 ha0, ha1, hb0, hb1;
+            uint32_t q6a[8], q6ha[8], q6b[8], q6hb[8], s6a = 0, s6b = 0, d6 = 0;
+            if constexpr (Q6) {
+                const uint32_t a1 = a0 + 8 * WS * SB;  // row g + 8
+                const int n = c >> 1, s2 = 2 * (c & 1);
+                q6_load(a0, c, q6a, q6ha);
+                q6_load(a1, c, q6b, q6hb);
+                s6a = lds_u16(a0 + 192 + 8 * n + s2) | (lds_u16(a0 + 196 + 8 * n + s2) << 16);
+                s6b = lds_u16(a1 + 192 + 8 * n + s2) | (lds_u16(a1 + 196 + 8 * n + s2) << 16);
+                d6 = lds_u16(a0 + 208) | (lds_u16(a1 + 208) << 16);
+            }
+            // (Q4_K / Q5_K units are 16-byte aligned; Q6_K's were read above)
+            uint4 h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1;
+            if constexpr (!Q6) {
+                h0 = lds128(a0);
+                h1 = lds128(a0 + 8 * SB);
+                qa0 = lds128(a0 + QOFF + 32 * c);
+                qa1 = lds128(a0 + QOFF + 16 + 32 * c);
+                qb0 = lds128(a0 + 8 * SB + QOFF + 32 * c);
+                qb1 = lds128(a0 + 8 * SB + QOFF + 16 + 32 * c);
+            }
             if constexpr (FMT == QMM_Q5_K) {
                 ha0 = lds128(a0 + 16);
                 ha1 = lds128(a0 + 32);
@@ -366,7 +400,9 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
             float keep;
-            if constexpr (FMT == QMM_Q5_K)
+            if constexpr (Q6)
+                keep = unit_rows6(q6a, q6ha, q6b, q6hb, s6a, s6b, d6, B, c, X6, iv);
+            else if constexpr (FMT == QMM_Q5_K)
                 keep = unit_rows5(h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1, B, L, c, X0, X1,
                                   iv);
             else
@@ -450,7 +486,8 @@ int env_m1_slices()
 size_t m1_smem(int KS, int WS, int TS, int cap, int nslot, int sb_bytes)
 {
     const int W = WS * TS;
-    return size_t(nslot) * (size_t(W) * kTileRows * sb_bytes + 16) + size_t(KS) * 1024 + size_t(KS) * 32 +
+    const size_t xn = sb_bytes == 210 ? 16 : 8;  // activation sums per super-block
+    return size_t(nslot) * (size_t(W) * kTileRows * sb_bytes + 16) + size_t(KS) * 1024 + size_t(KS) * xn * 4 +
            size_t((KS + 3) & ~3) * 4 + size_t(WS) * cap * TS * kTileRows * 4 + size_t(cap) * 8 + 8;
 }
 
@@ -477,11 +514,14 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
     const int forced = force_S > 0 ? force_S : env_m1_slices();
     // (WS, TS) for a slice of ks super-blocks: the most consumer warps that
     // still leave every SM an item, then the widest pass.
+    // Q6_K (210-byte super-blocks): a TMA box spans 8 super-blocks (1680
+    // bytes, the first whole multiple of 16 bytes), so passes are 8 wide.
+    const bool q6 = sb_bytes == 210;
     auto shape = [&](int ks, int s_, int &ws_best, int &ts_best) {
         double best = -1.0;
         const int per = sm_count / s_ >= 1 ? sm_count / s_ : 1;
         for (int ws = (ks < maxw ? ks : maxw); ws >= 1; --ws) {
-            if (ks % ws)
+            if (ks % ws || (q6 && ws != 8))
                 continue;
             for (int ts = 1; ts <= 8 && ws * ts <= maxw; ts *= 2) {
                 const int64_t items = (T + ts - 1) / ts;
@@ -520,7 +560,7 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
             S = int(cand);
     }
     for (int64_t cand = 1; S == 0 && cand <= NB && cand <= sm_count; ++cand)
-        if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3)
+        if (NB % cand == 0 && size_t(NB / cand) * 1056 <= budget / 3 && (!q6 || (NB / cand) % 8 == 0))
             S = int(cand);
     if (S == 0)
         return p;  // nslot == 0: not supported
@@ -528,7 +568,8 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
     p.S = S;
     p.KS = int(NB / S);
     // Pass width WS (a divisor of KS, at most maxw) and tiles per item TS.
-    shape(p.KS, S, p.WS, p.TS);
+    if (shape(p.KS, S, p.WS, p.TS) < 0)
+        return M1Plan();  // no pass width fits (Q6_K: KS not a multiple of 8)
     const int per_slice = sm_count / S >= 1 ? sm_count / S : 1;
     p.NP = p.KS / p.WS;
     p.W = p.WS * p.TS;
@@ -604,7 +645,9 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.slot_bytes = p.slot_bytes;
     // All shared memory preferred, so that two half-SM CTAs (this launch
     // and the next) fit side by side.
-    const auto kern = a.fmt == QMM_Q5_K ? gemv_m1_kernel<QMM_Q5_K> : gemv_m1_kernel<QMM_Q4_K>;
+    const auto kern = a.fmt == QMM_Q5_K   ? gemv_m1_kernel<QMM_Q5_K>
+                      : a.fmt == QMM_Q6_K ? gemv_m1_kernel<QMM_Q6_K>
+                                          : gemv_m1_kernel<QMM_Q4_K>;
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem, true);
     if (e != cudaSuccess)
         return e;

@@ -139,6 +139,7 @@ __device__ __forceinline__ float2 pair_total(uint4 h0, uint4 h1, const ScaleSel 
 // sub-block sums and 2^-s.  Lane (cc, tt) = (lane >> 3, lane & 7) holds
 // x[64cc + 4tt .. +3] (v, sub-block 2cc) and x[64cc + 32 + 4tt .. +3] (w,
 // sub-block 2cc+1).
+template <bool G16 = false>
 __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx, float *xsum,
                                         float *inv)
 {
@@ -178,17 +179,32 @@ __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx,
                                            pack(hi[4], hi[6]), pack(hi[5], hi[7]));
     bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[2]), pack(lo[1], lo[3]),
                                            pack(lo[4], lo[6]), pack(lo[5], lo[7]));
-    // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
     float sl = (v.x + v.y) + (v.z + v.w);
     float sh = (w.x + w.y) + (w.z + w.w);
+    if constexpr (!G16) {
+        // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        sl += __shfl_xor_sync(0xffffffffu, sl, o);
-        sh += __shfl_xor_sync(0xffffffffu, sh, o);
-    }
-    if (tt == 0) {
-        xsum[2 * cc] = sl;
-        xsum[2 * cc + 1] = sh;
+        for (int o = 1; o < 8; o <<= 1) {
+            sl += __shfl_xor_sync(0xffffffffu, sl, o);
+            sh += __shfl_xor_sync(0xffffffffu, sh, o);
+        }
+        if (tt == 0) {
+            xsum[2 * cc] = sl;
+            xsum[2 * cc + 1] = sh;
+        }
+    } else {
+        // Sums of the 16-weight groups (Q6_K's scale groups): lanes tt < 4
+        // and tt >= 4 hold the two halves of v and of w; fixed order.
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+            sl += __shfl_xor_sync(0xffffffffu, sl, o);
+            sh += __shfl_xor_sync(0xffffffffu, sh, o);
+        }
+        if ((tt & 3) == 0) {
+            const int g0 = 8 * (cc >> 1) + 2 * (cc & 1) + (tt >> 2);
+            xsum[g0] = sl;
+            xsum[g0 + 4] = sh;
+        }
     }
     if (lane == 0)
         *inv = scale_pow2(1.f, -s);
@@ -269,6 +285,126 @@ __device__ __forceinline__ float unit_rows5(uint4 h0, uint4 h1, uint4 qa0, uint4
                                                           make_float2(dlo[1], dlo[3])),
                                   __fadd2_rn(make_float2(dhi[0], dhi[2]), make_float2(dhi[1], dhi[3])),
                                   X0, X1, iv);
+    const bool odd = c & 1;
+    float keep = odd ? tot.y : tot.x;
+    keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    return keep;
+}
+
+// ---------------------------------------------------------------- Q6_K
+// A Q6_K super-block (210 bytes: 128 bytes of low nibbles, 64 of 2-bit high
+// parts, 16 int8 scales, fp16 d) is read like Q4_K's: lane column c takes
+// low-nibble byte chunk c (ql bytes 32c .. 32c+31), whose low nibbles are
+// weights 128n + 32s + l and high nibbles weights 128n + 64 + 32s + l
+// (n = c >> 1, s = c & 1, l < 32), and the high parts of those weights from
+// qh bytes 32n + l (bits 2s..2s+1 for the low nibble, 2s+4..2s+5 for the
+// high one).  The six-bit code q enters the MMA as an fp16 subnormal like a
+// Q4_K nibble (q * 2^-24 from the low nibble, 16 q * 2^-24 from the high
+// one), and the MMAs of k-steps 0-3 and 4-7 (l < 16, l >= 16) accumulate
+// apart: each of the lane's four accumulators is one 16-weight scale group.
+// Super-blocks sit 210 bytes apart, so a unit starts m = 0, 2, .., 14 bytes
+// past a 16-byte boundary (the same m for every unit a warp reads): each
+// 32-byte field comes in as three 16-byte loads from the boundary below and
+// is realigned by W4 = m / 4 words and a two-byte permute when m % 4 = 2.
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
+{
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+// Words 0..7 of the 32 bytes starting W4 words (+2 bytes with sel 0x5432)
+// after the 16-byte-aligned address ab.
+template <int W4>
+__device__ __forceinline__ void q6_field(uint32_t ab, unsigned sel, uint32_t (&out)[8])
+{
+    const uint4 u0 = lds128(ab), u1 = lds128(ab + 16), u2 = lds128(ab + 32);
+    const uint32_t w[12] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, u2.x, u2.y, u2.z, u2.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        out[k] = __byte_perm(w[W4 + k], w[W4 + k + 1], sel);
+}
+
+// The lane's low-nibble chunk and high parts of the super-block at smem
+// address a (a % 16 == m, W4 = m / 4).
+template <int W4>
+__device__ __forceinline__ void q6_fields(uint32_t a, int c, unsigned sel, uint32_t (&ql)[8],
+                                          uint32_t (&qh)[8])
+{
+    const uint32_t ab = a & ~15u;
+    q6_field<W4>(ab + 32 * c, sel, ql);
+    q6_field<W4>(ab + 128 + 32 * (c >> 1), sel, qh);
+}
+
+__device__ __forceinline__ void q6_load(uint32_t a, int c, uint32_t (&ql)[8], uint32_t (&qh)[8])
+{
+    const unsigned sel = (a & 2u) ? 0x5432u : 0x3210u;
+    switch ((a >> 2) & 3u) {
+    case 0: q6_fields<0>(a, c, sel, ql, qh); break;
+    case 1: q6_fields<1>(a, c, sel, ql, qh); break;
+    case 2: q6_fields<2>(a, c, sel, ql, qh); break;
+    default: q6_fields<3>(a, c, sel, ql, qh); break;
+    }
+}
+
+// One Q6_K unit for one lane: rows g (qa, ha; scale bytes sa = (group
+// 8n+2s, 8n+2s+1, 8n+4+2s, 8n+5+2s) as a word; d0) and g+8 (qb, hb, sb, d1);
+// X: the four groups' activation sums (the same for both rows).
+__device__ __forceinline__ float unit_rows6(const uint32_t (&qa)[8], const uint32_t (&ha)[8],
+                                            const uint32_t (&qb)[8], const uint32_t (&hb)[8],
+                                            uint32_t sa, uint32_t sb, uint32_t dd,
+                                            const uint4 (&B)[8], int c, float4 X, float2 iv)
+{
+    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
+    const uint32_t blo = 0x00300030u, bhi = 0x03000300u;
+    const int sh = 2 * (c & 1);
+    float la[4], lb[4], ua[4], ub[4];  // low / high nibbles, groups l < 16 (a) and l >= 16 (b)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t xa = qa[t], xb = qb[t], ya = xa >> 8, yb = xb >> 8;
+        const uint32_t pa = ha[t] >> sh, pb = hb[t] >> sh;  // bits 0-1: low nibble's high part
+        const uint32_t ra = pa >> 4, rb = pb >> 4;          // bits 0-1: high nibble's
+        const uint32_t a0 = (xa & mlo) | ((pa << 4) & blo), a1 = (xb & mlo) | ((pb << 4) & blo);
+        const uint32_t a2 = (ya & mlo) | ((pa >> 4) & blo), a3 = (yb & mlo) | ((pb >> 4) & blo);
+        const uint32_t b0 = (xa & mhi) | ((ra << 8) & bhi), b1 = (xb & mhi) | ((rb << 8) & bhi);
+        const uint32_t b2 = (ya & mhi) | (ra & bhi), b3 = (yb & mhi) | (rb & bhi);
+        float(&dl)[4] = t < 4 ? la : lb;
+        float(&dh)[4] = t < 4 ? ua : ub;
+        if ((t & 3) == 0) {
+            mma16816_zero(dl, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816_zero(dh, b0, b1, b2, b3, B[t].z, B[t].w);
+        } else {
+            mma16816(dl, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816(dh, b0, b1, b2, b3, B[t].z, B[t].w);
+        }
+    }
+    // (row g, row g+8) sums of the hi and lo columns of each group
+    const float2 Dla = __fadd2_rn(make_float2(la[0], la[2]), make_float2(la[1], la[3]));
+    const float2 Dlb = __fadd2_rn(make_float2(lb[0], lb[2]), make_float2(lb[1], lb[3]));
+    const float2 Dua = __fadd2_rn(make_float2(ua[0], ua[2]), make_float2(ua[1], ua[3]));
+    const float2 Dub = __fadd2_rn(make_float2(ub[0], ub[2]), make_float2(ub[1], ub[3]));
+    // int8 scales -> floats: (2^23 + 128 + sc) - (2^23 + 128)
+    const uint32_t qa8 = sa ^ 0x80808080u, qb8 = sb ^ 0x80808080u;
+    const float2 off = make_float2(-8388736.f, -8388736.f);
+    const float2 s0 = __fadd2_rn(make_float2(byte_magic(qa8, 0), byte_magic(qb8, 0)), off);
+    const float2 s1 = __fadd2_rn(make_float2(byte_magic(qa8, 1), byte_magic(qb8, 1)), off);
+    const float2 s2 = __fadd2_rn(make_float2(byte_magic(qa8, 2), byte_magic(qb8, 2)), off);
+    const float2 s3 = __fadd2_rn(make_float2(byte_magic(qa8, 3), byte_magic(qb8, 3)), off);
+    // sum (q - 32) x per group = D * 2^24 (low) or D * 2^20 (high), times
+    // 2^-s for the activation scale, minus 32 X
+    const float2 lo = __ffma2_rn(s0, Dla, __fmul2_rn(s1, Dlb));
+    const float2 hi = __ffma2_rn(s2, Dua, __fmul2_rn(s3, Dub));
+    const float2 q = __ffma2_rn(lo, make_float2(16777216.f, 16777216.f),
+                                __fmul2_rn(hi, make_float2(1048576.f, 1048576.f)));
+    const float2 mn = __ffma2_rn(s0, make_float2(X.x, X.x),
+                                 __ffma2_rn(s1, make_float2(X.y, X.y),
+                                            __ffma2_rn(s2, make_float2(X.z, X.z),
+                                                       __fmul2_rn(s3, make_float2(X.w, X.w)))));
+    const float2 d = half2_bits_to_float2(dd);  // (d of row g, d of row g+8)
+    const float2 tot = __ffma2_rn(__fmul2_rn(d, iv), q,
+                                  __fmul2_rn(make_float2(-32.f * d.x, -32.f * d.y), mn));
     const bool odd = c & 1;
     float keep = odd ? tot.y : tot.x;
     keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);

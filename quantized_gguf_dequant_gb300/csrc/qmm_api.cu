@@ -250,7 +250,10 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     int64_t T = 0;
     for (int i = 0; i < n; ++i) {
         const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
-        if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K) || mi.K % 256 != 0)
+        if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K && mi.fmt != QMM_Q6_K) || mi.K % 256 != 0)
+            return QMM_ERR_UNSUPPORTED;
+        // Q6_K: TMA boxes of 8 super-blocks (1680 bytes) need K % 2048 == 0
+        if (mi.fmt == QMM_Q6_K && mi.K % 2048 != 0)
             return QMM_ERR_UNSUPPORTED;
         a.rows[i] = mi.N;
         a.y[i] = ys[i];
@@ -259,7 +262,7 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     if (T * 16 > (int64_t(1) << 30))
         return QMM_ERR_UNSUPPORTED;
     const int64_t NB = m0.K / 256;
-    const int sbb = m0.fmt == QMM_Q5_K ? 176 : 144;
+    const int sbb = m0.fmt == QMM_Q5_K ? 176 : (m0.fmt == QMM_Q6_K ? 210 : 144);
     qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0, 0, sbb);
     // Fewer K slices when the handle's workspace or tickets are too small.
     for (int S = p.S; S >= 1 && (p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets); --S)
@@ -272,7 +275,15 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     for (int i = 0; i < n; ++i) {
         Matrix &mi = *reinterpret_cast<Matrix *>(hs[i]);
         if (mi.tmap3_ks != p.WS) {
-            if (qmm::make_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.WS, sbb) != 0)
+            // Q6_K: a 2-D view of the rows as u64 words, boxes of 8
+            // super-blocks (210 words) x 16 rows
+            const int r = mi.fmt == QMM_Q6_K
+                              ? qmm::encode_tmap_2d(mi.tmap3, CU_TENSOR_MAP_DATA_TYPE_UINT64, mi.w,
+                                                    uint64_t(mi.row_bytes / 8), uint64_t(mi.N),
+                                                    uint64_t(mi.row_bytes), 210u, 16u,
+                                                    CU_TENSOR_MAP_SWIZZLE_NONE)
+                              : qmm::make_column_map(mi.tmap3, mi.w, mi.N, mi.row_bytes, p.WS, sbb);
+            if (r != 0)
                 return QMM_ERR_UNSUPPORTED;
             mi.tmap3_ks = p.WS;
         }
@@ -358,9 +369,10 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
     // faster on the SIMT kernel (0.266 / 0.287 against 0.334 / 0.364 ms).
     // QMM_FMT_PATH = staged, fast or plain picks the route for all three.
     const char *fp = getenv("QMM_FMT_PATH");
-    // Q5_K: the tensor-core decode kernel of Q4_K with the fifth bits added
-    // to the operands (QMM_FMT_PATH=staged, fast or plain keeps it off).
-    if (m0.fmt == QMM_Q5_K && !fp) {
+    // Q5_K and Q6_K: the tensor-core decode kernel of Q4_K with the high
+    // bits added to the operands (QMM_FMT_PATH=staged, fast or plain keeps
+    // it off).
+    if ((m0.fmt == QMM_Q5_K || m0.fmt == QMM_Q6_K) && !fp) {
         qmm_status st = do_gemv_m1(hs, n, x, ys, s, fn);
         if (st != QMM_ERR_UNSUPPORTED)
             return st;
