@@ -57,6 +57,7 @@
 
 #include <cuda.h>
 
+#include "formats.cuh"
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
 #include "m1_device.cuh"
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     // super-block bytes, one unit's bytes (16 rows), offset of the nibbles,
     // activation sums per super-block (Q6_K: one per 16-weight group)
     constexpr bool Q6 = FMT == QMM_Q6_K;
+    constexpr bool IQ = FMT == QMM_IQ4_NL;
     constexpr int SB = FMT == QMM_Q5_K ? 176 : (Q6 ? 210 : 144);
     constexpr int UB = kTileRows * SB;
     constexpr int QOFF = FMT == QMM_Q5_K ? 48 : 16;
@@ -280,9 +282,14 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             const int cc = lane >> 3, tt = lane & 7;
             // v: the weights of chunk cc's low nibbles, w (xb + wo): of its
             // high nibbles
+            // (IQ4_NL: k-step tt of lane column cc reads code bytes
+            // 4(tt & 3) .. +3 of block 2cc + tt / 4: low-nibble weights there,
+            // high-nibble ones 16 further)
             const float *xb = P.x + int64_t(sb0) * 256 +
-                              (Q6 ? 128 * (cc >> 1) + 32 * (cc & 1) : 64 * cc) + 4 * tt;
-            constexpr int wo = Q6 ? 64 : 32;
+                              (Q6   ? 128 * (cc >> 1) + 32 * (cc & 1) + 4 * tt
+                               : IQ ? 64 * cc + 32 * (tt >> 2) + 4 * (tt & 3)
+                                    : 64 * cc + 4 * tt);
+            constexpr int wo = Q6 ? 64 : (IQ ? 16 : 32);
             for (int j0 = warp; j0 < KS; j0 += 4 * W) {
                 float4 v[4], w[4];
 #pragma unroll
@@ -297,7 +304,8 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 for (int i = 0; i < 4; ++i) {
                     const int j = j0 + i * W;
                     if (j < KS)
-                        prep_sb<Q6>(v[i], w[i], lane, Bx + size_t(j) * 64, Xs + j * XN, inv + j);
+                        prep_sb<Q6 ? 1 : (IQ ? 2 : 0)>(v[i], w[i], lane, Bx + size_t(j) * 64,
+                                                        Xs + j * XN, inv + j);
                 }
             }
         }
@@ -308,6 +316,11 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         const bool act = (g >> 1) == c;
         const int term = g & 1;
         const ScaleSel L = scale_sel(c);
+        // IQ4_NL: the code book as u = book + 128 bytes
+        const Iq4Book book = {fmt::iq4nl_book_word(0) ^ 0x80808080u,
+                              fmt::iq4nl_book_word(4) ^ 0x80808080u,
+                              fmt::iq4nl_book_word(8) ^ 0x80808080u,
+                              fmt::iq4nl_book_word(12) ^ 0x80808080u};
         // B fragments, sub-block sums and inverse scale of this warp's
         // super-block of pass p (reloaded per pass when there are several).
         uint4 B[8];
@@ -322,6 +335,8 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if constexpr (Q6) {
                 X6 = make_float4(Xs[j * XN + g6], Xs[j * XN + g6 + 1], Xs[j * XN + g6 + 4],
                                  Xs[j * XN + g6 + 5]);
+            } else if constexpr (IQ) {
+                X0 = make_float2(Xs[j * XN + 2 * c], Xs[j * XN + 2 * c + 1]);  // blocks 2c, 2c+1
             } else {
                 X0 = make_float2(Xs[j * XN + 2 * c], Xs[j * XN + 2 * c]);
                 X1 = make_float2(Xs[j * XN + 2 * c + 1], Xs[j * XN + 2 * c + 1]);
@@ -368,8 +383,16 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 d6 = lds_u16(a0 + 208) | (lds_u16(a1 + 208) << 16);
             }
             // (Q4_K / Q5_K units are 16-byte aligned; Q6_K's were read above)
+            uint32_t iwa[9], iwb[9];
+            if constexpr (IQ) {
+#pragma unroll
+                for (int q = 0; q < 9; ++q) {
+                    iwa[q] = lds32(a0 + 36 * c + 4 * q);
+                    iwb[q] = lds32(a0 + 8 * SB + 36 * c + 4 * q);
+                }
+            }
             uint4 h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1;
-            if constexpr (!Q6) {
+            if constexpr (!Q6 && !IQ) {
                 h0 = lds128(a0);
                 h1 = lds128(a0 + 8 * SB);
                 qa0 = lds128(a0 + QOFF + 32 * c);
@@ -400,7 +423,9 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
             float keep;
-            if constexpr (Q6)
+            if constexpr (IQ)
+                keep = unit_rows_iq4(iwa, iwb, book, B, c, X0, iv);
+            else if constexpr (Q6)
                 keep = unit_rows6(q6a, q6ha, q6b, q6hb, s6a, s6b, d6, B, c, X6, iv);
             else if constexpr (FMT == QMM_Q5_K)
                 keep = unit_rows5(h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1, B, L, c, X0, X1,
@@ -645,9 +670,10 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.slot_bytes = p.slot_bytes;
     // All shared memory preferred, so that two half-SM CTAs (this launch
     // and the next) fit side by side.
-    const auto kern = a.fmt == QMM_Q5_K   ? gemv_m1_kernel<QMM_Q5_K>
-                      : a.fmt == QMM_Q6_K ? gemv_m1_kernel<QMM_Q6_K>
-                                          : gemv_m1_kernel<QMM_Q4_K>;
+    const auto kern = a.fmt == QMM_Q5_K     ? gemv_m1_kernel<QMM_Q5_K>
+                      : a.fmt == QMM_Q6_K   ? gemv_m1_kernel<QMM_Q6_K>
+                      : a.fmt == QMM_IQ4_NL ? gemv_m1_kernel<QMM_IQ4_NL>
+                                            : gemv_m1_kernel<QMM_Q4_K>;
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem, true);
     if (e != cudaSuccess)
         return e;

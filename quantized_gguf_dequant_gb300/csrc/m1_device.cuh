@@ -139,7 +139,12 @@ __device__ __forceinline__ float2 pair_total(uint4 h0, uint4 h1, const ScaleSel 
 // sub-block sums and 2^-s.  Lane (cc, tt) = (lane >> 3, lane & 7) holds
 // x[64cc + 4tt .. +3] (v, sub-block 2cc) and x[64cc + 32 + 4tt .. +3] (w,
 // sub-block 2cc+1).
-template <bool G16 = false>
+// MODE 0: Q4_K / Q5_K (above).  MODE 1: Q6_K -- sums of the 16-weight
+// groups instead (v's and w's halves).  MODE 2: IQ4_NL -- the k-slots of a
+// lane column take adjacent weights ((v.x, v.y) in (2c, 2c+1), (v.z, v.w) in
+// (2c+8, 2c+9); w likewise for the high-nibble MMA) and the sums are of the
+// 32-weight blocks (v and w of lanes tt & ~3 .. tt | 3).
+template <int MODE = 0>
 __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx, float *xsum,
                                         float *inv)
 {
@@ -174,14 +179,30 @@ __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx,
     auto pack = [](__half a, __half b) {
         return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
     };
-    // k-step tt: elements (4tt, 4tt+2) in k-slots (2c, 2c+1), (4tt+1, 4tt+3) in (2c+8, 2c+9).
-    bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[2]), pack(hi[1], hi[3]),
-                                           pack(hi[4], hi[6]), pack(hi[5], hi[7]));
-    bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[2]), pack(lo[1], lo[3]),
-                                           pack(lo[4], lo[6]), pack(lo[5], lo[7]));
+    if constexpr (MODE == 2) {
+        // k-step tt: elements (0, 1) in k-slots (2c, 2c+1), (2, 3) in (2c+8, 2c+9).
+        bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[1]), pack(hi[2], hi[3]),
+                                               pack(hi[4], hi[5]), pack(hi[6], hi[7]));
+        bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[1]), pack(lo[2], lo[3]),
+                                               pack(lo[4], lo[5]), pack(lo[6], lo[7]));
+    } else {
+        // k-step tt: elements (4tt, 4tt+2) in k-slots (2c, 2c+1), (4tt+1, 4tt+3) in (2c+8, 2c+9).
+        bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[2]), pack(hi[1], hi[3]),
+                                               pack(hi[4], hi[6]), pack(hi[5], hi[7]));
+        bx[(tt * 4 + cc) * 2 + 1] = make_uint4(pack(lo[0], lo[2]), pack(lo[1], lo[3]),
+                                               pack(lo[4], lo[6]), pack(lo[5], lo[7]));
+    }
     float sl = (v.x + v.y) + (v.z + v.w);
     float sh = (w.x + w.y) + (w.z + w.w);
-    if constexpr (!G16) {
+    if constexpr (MODE == 2) {
+        // Block sums (blocks 2cc and 2cc+1), fixed order.
+        float sb = sl + sh;
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1)
+            sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        if ((tt & 3) == 0)
+            xsum[2 * cc + (tt >> 2)] = sb;
+    } else if constexpr (MODE == 0) {
         // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
@@ -405,6 +426,95 @@ __device__ __forceinline__ float unit_rows6(const uint32_t (&qa)[8], const uint3
     const float2 d = half2_bits_to_float2(dd);  // (d of row g, d of row g+8)
     const float2 tot = __ffma2_rn(__fmul2_rn(d, iv), q,
                                   __fmul2_rn(make_float2(-32.f * d.x, -32.f * d.y), mn));
+    const bool odd = c & 1;
+    float keep = odd ? tot.y : tot.x;
+    keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    return keep;
+}
+
+// ---------------------------------------------------------------- IQ4_NL
+// Eight 18-byte blocks (fp16 d, 16 code bytes: byte j holds the codes of
+// weights j (low nibble) and j+16 (high)) make a 144-byte unit like Q4_K's.
+// Lane column c takes blocks 2c (k-steps 0-3) and 2c+1 (4-7); k-step t reads
+// code bytes j..j+3 (j = 4(t & 3)) of its block.  Each code is looked up as
+// u = book + 128 (1 .. 241, an exact fp16 subnormal u * 2^-24): the low 16
+// bits of a code word hold four codes in nibble order (low j, high j, low
+// j+1, high j+1) and serve as the byte-permute selector directly (bit 3
+// cleared; a sign-replicating permute of the word and the word shifted by 4
+// gives the 0xFF mask of the codes >= 8 that picks the second table half).
+// Per block: sum book x = sum u x - 128 X.
+struct Iq4Book {
+    uint32_t t0, t1, t2, t3;  // u of codes 0-3, 4-7, 8-11, 12-15
+};
+
+__device__ __forceinline__ uint32_t prmt_m(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// u of the four codes in the low 16 bits of q (selector nibbles) -> bytes
+// (u0, u1, u2, u3) in that order; m: the word's codes >= 8 mask source.
+__device__ __forceinline__ uint32_t iq4_look(const Iq4Book &bk, uint32_t sel, uint32_t mask)
+{
+    const uint32_t lo = __byte_perm(bk.t0, bk.t1, sel), hi = __byte_perm(bk.t2, bk.t3, sel);
+    return (lo & ~mask) | (hi & mask);
+}
+
+// One IQ4_NL unit for one lane: wa / wb the nine words at byte 36c of rows g
+// and g+8 (block 2c: d in the low half of word 0, codes from byte 2; block
+// 2c+1: d in the high half of word 4, codes in words 5-8); X: the sums of
+// blocks 2c and 2c+1.
+__device__ __forceinline__ float unit_rows_iq4(const uint32_t (&wa)[9], const uint32_t (&wb)[9],
+                                               const Iq4Book &bk, const uint4 (&B)[8], int c,
+                                               float2 X, float2 iv)
+{
+    float la[4], lb[4], ua[4], ub[4];  // low / high codes of block 2c (a) and 2c+1 (b)
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t qa = t < 4 ? __byte_perm(wa[t], wa[t + 1], 0x5432u) : wa[t + 1];
+        const uint32_t qb = t < 4 ? __byte_perm(wb[t], wb[t + 1], 0x5432u) : wb[t + 1];
+        // codes of bytes j, j+1 (A) and j+2, j+3 (B) of rows g and g+8
+        const uint32_t qa4 = qa << 4, qb4 = qb << 4;
+        const uint32_t oa0 = iq4_look(bk, qa & 0x7777u, prmt_m(qa4, qa, 0xd9c8u));
+        const uint32_t oa1 = iq4_look(bk, (qa >> 16) & 0x7777u, prmt_m(qa4, qa, 0xfbeau));
+        const uint32_t ob0 = iq4_look(bk, qb & 0x7777u, prmt_m(qb4, qb, 0xd9c8u));
+        const uint32_t ob1 = iq4_look(bk, (qb >> 16) & 0x7777u, prmt_m(qb4, qb, 0xfbeau));
+        // (u_j, u_j+1) and (u_j+2, u_j+3): low codes; the high ones (j+16 ..)
+        const uint32_t a0 = __byte_perm(oa0, 0u, 0x4240u), a1 = __byte_perm(ob0, 0u, 0x4240u);
+        const uint32_t a2 = __byte_perm(oa1, 0u, 0x4240u), a3 = __byte_perm(ob1, 0u, 0x4240u);
+        const uint32_t b0 = __byte_perm(oa0, 0u, 0x4341u), b1 = __byte_perm(ob0, 0u, 0x4341u);
+        const uint32_t b2 = __byte_perm(oa1, 0u, 0x4341u), b3 = __byte_perm(ob1, 0u, 0x4341u);
+        float(&dl)[4] = t < 4 ? la : lb;
+        float(&dh)[4] = t < 4 ? ua : ub;
+        if ((t & 3) == 0) {
+            mma16816_zero(dl, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816_zero(dh, b0, b1, b2, b3, B[t].z, B[t].w);
+        } else {
+            mma16816(dl, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816(dh, b0, b1, b2, b3, B[t].z, B[t].w);
+        }
+    }
+    // (row g, row g+8): sum u x of each block (hi + lo columns, both nibbles)
+    const float2 Sa = __fadd2_rn(__fadd2_rn(make_float2(la[0], la[2]), make_float2(la[1], la[3])),
+                                 __fadd2_rn(make_float2(ua[0], ua[2]), make_float2(ua[1], ua[3])));
+    const float2 Sb = __fadd2_rn(__fadd2_rn(make_float2(lb[0], lb[2]), make_float2(lb[1], lb[3])),
+                                 __fadd2_rn(make_float2(ub[0], ub[2]), make_float2(ub[1], ub[3])));
+    const float2 da = half2_bits_to_float2(__byte_perm(wa[0], wb[0], 0x5410u));  // d of block 2c
+    const float2 db = half2_bits_to_float2(__byte_perm(wa[4], wb[4], 0x7632u));  // d of block 2c+1
+    const float2 k24 = make_float2(16777216.f, 16777216.f);
+    const float2 ta = __ffma2_rn(__fmul2_rn(Sa, iv), k24, make_float2(-128.f * X.x, -128.f * X.x));
+    const float2 tb = __ffma2_rn(__fmul2_rn(Sb, iv), k24, make_float2(-128.f * X.y, -128.f * X.y));
+    const float2 tot = __ffma2_rn(da, ta, __fmul2_rn(db, tb));
     const bool odd = c & 1;
     float keep = odd ? tot.y : tot.x;
     keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);

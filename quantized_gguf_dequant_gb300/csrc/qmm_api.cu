@@ -250,7 +250,8 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     int64_t T = 0;
     for (int i = 0; i < n; ++i) {
         const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
-        if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K && mi.fmt != QMM_Q6_K) || mi.K % 256 != 0)
+        if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K && mi.fmt != QMM_Q6_K &&
+             mi.fmt != QMM_IQ4_NL) || mi.K % 256 != 0)
             return QMM_ERR_UNSUPPORTED;
         // Q6_K: TMA boxes of 8 super-blocks (1680 bytes) need K % 2048 == 0
         if (mi.fmt == QMM_Q6_K && mi.K % 2048 != 0)
@@ -369,10 +370,10 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
     // faster on the SIMT kernel (0.266 / 0.287 against 0.334 / 0.364 ms).
     // QMM_FMT_PATH = staged, fast or plain picks the route for all three.
     const char *fp = getenv("QMM_FMT_PATH");
-    // Q5_K and Q6_K: the tensor-core decode kernel of Q4_K with the high
-    // bits added to the operands (QMM_FMT_PATH=staged, fast or plain keeps
-    // it off).
-    if ((m0.fmt == QMM_Q5_K || m0.fmt == QMM_Q6_K) && !fp) {
+    // Q5_K, Q6_K and IQ4_NL: the tensor-core decode kernel of Q4_K with the
+    // high bits added to the operands (IQ4_NL: the looked-up codes)
+    // (QMM_FMT_PATH=staged, fast or plain keeps it off).
+    if ((m0.fmt == QMM_Q5_K || m0.fmt == QMM_Q6_K || m0.fmt == QMM_IQ4_NL) && !fp) {
         qmm_status st = do_gemv_m1(hs, n, x, ys, s, fn);
         if (st != QMM_ERR_UNSUPPORTED)
             return st;
