@@ -857,9 +857,9 @@ def run_ours(args, world, rank, local):
                 pass
         extras["extra_formats_decode"] = dict(
             fx, unit="GB/s",
-            note="Llama-3.1-8B decode step, 4 layers, the weights in each further format, "
-                 "through the SIMT formats GEMV (a warp owns rows, a lane one 256-weight unit, "
-                 "activations in shared memory)")
+            note="Llama-3.1-8B decode step, 4 layers (graph, PDL), the weights in each further "
+                 "format, through the library's default route: the tensor-core decode kernel "
+                 "(gemv_m1_kernel<Q5_K / Q6_K / IQ4_NL>, codes as exact fp16 subnormals)")
 
     # Every launch of the step is the one-row decode kernel, so its average
     # launch is the step's: algorithmic bytes per launch = step bytes / launches,
