@@ -7,13 +7,17 @@
 // W_e x_slot, with gate and up optionally in one launch and SwiGLU applied
 // there.
 //
-// Arithmetic, fp32 on the CUDA cores: a Q8_0 block is d (fp16) and 32 int8
-// codes q; q becomes the float 2^23 + 128 + q with one byte permute (the
-// code's byte, sign bit flipped, under the exponent byte 0x4B) and one
-// packed subtraction, both exact; products accumulate per block in packed
-// FFMA2 over (weight i, weight i+1) pairs, and the block sum is scaled by d
-// once.  With the routing weight on the input (Llama 4) the slot's sum is
-// multiplied by r afterwards: the same value as W (r x) up to rounding.
+// Arithmetic, on the tensor cores (mma.sync m16n8k16, fp16 operands, fp32
+// accumulation): a Q8_0 block is d (fp16) and 32 int8 codes q.  Each code
+// enters the MMA as u = q + 128 (one XOR flips the sign bits; one byte
+// permute puts two codes into the low bytes of an fp16 pair, u * 2^-24, an
+// exact subnormal).  The B columns are the group's four tokens, each as two
+// fp16 terms (hi + lo) of its activations scaled by a power of two per block
+// and token, so every product is exact and one MMA per 16 weights serves all
+// four tokens.  Per block and token: sum q x = sum u x - 128 X (X the
+// block's activation sum), times d, added in fp32.  With the routing weight
+// on the input (Llama 4) the slot's sum is multiplied by r afterwards: the
+// same value as W (r x) up to rounding.
 //
 // Work.  An item is (group, row tile): 64 rows of one matrix, or 32 rows of
 // gate and the same 32 rows of up.  An item's rows stream through shared
@@ -22,13 +26,13 @@
 // lanes of a quarter warp reading neighbouring rows hit disjoint banks) and
 // the group's activations for the slice (one 1 KB bulk copy per token).  A
 // producer warp fills a ring of stages; eight consumer warps take, in every
-// stage, Q8_0 block w of the slice for warp w (weights 32w .. 32w+31) and
-// rows l and l+32 for lane l, so a lane keeps its sums over the whole K in
-// registers and the activations of a half block (16 weights x the group's
-// tokens) serve both of its rows.  At the end of an item the eight warps'
-// sums meet in shared memory and are added in warp order (bitwise
-// repeatable), then stored (with silu(gate) * up when fused).  CTA b takes
-// items b, b + G, b + 2G, ... of the (group, tile) sequence.
+// stage, Q8_0 block w of the slice for warp w (weights 32w .. 32w+31, two
+// MMA k-steps) over all 64 rows (four 16-row MMA tiles), preparing the
+// block's B fragments once; lane (g, c) keeps, over the whole K, the sums of
+// rows g and g+8 of each tile for token c.  At the end of an item the eight
+// warps' sums meet in shared memory and are added in warp order (bitwise
+// repeatable), then stored (with silu(gate) * up when fused).  CTA b takes items b, b + G,
+// b + 2G, ... of the (group, tile) sequence.
 #include <cstring>
 
 #include <cuda.h>
@@ -36,6 +40,7 @@
 
 #include "qmm_device.cuh"
 #include "qmm_internal.h"
+#include "tc_common.cuh"
 
 namespace qmm {
 
@@ -94,114 +99,110 @@ __device__ __forceinline__ void tma_box(void *dst, const CUtensorMap *map, int x
         : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_u32(p)));
-    return v;
-}
-
-__device__ __forceinline__ float4 lds128f(const void *p)
-{
-    const uint4 v = lds128(p);
-    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                       __uint_as_float(v.w));
-}
-
 __device__ __forceinline__ void consumers_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"r"(32 * kQ8eWarps) : "memory");
 }
 
-// Words k = 0..3 of the 16 bytes starting I words (+ 2 bytes when sel is
-// 0x5432) into the 32 bytes a ++ b.
-template <int I>
-__device__ __forceinline__ void pick4(const uint32_t (&a)[8], unsigned sel, uint32_t (&q)[4])
+__device__ __forceinline__ uint32_t lds32(const void *p)
 {
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        q[k] = __byte_perm(a[I + k], a[I + k + 1], sel);
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+    return v;
 }
 
-// One row's half block: 16 codes (four words) against the half block's
-// activations xv[t][0..15]; returns d * sum per token.
-template <int NT>
-__device__ __forceinline__ void half_block(const uint32_t (&q)[4], const float (&xv)[kGroupTokens][16],
-                                           float d, float (&out)[kGroupTokens])
+__device__ __forceinline__ uint32_t lds_u16(const void *p)
 {
-    const float2 off = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
-    float2 acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-        acc[t] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t u = q[k] ^ 0x80808080u;  // int8 -> 128 + q as a byte
-        const float2 w01 = __fadd2_rn(make_float2(byte_magic(u, 0), byte_magic(u, 1)), off);
-        const float2 w23 = __fadd2_rn(make_float2(byte_magic(u, 2), byte_magic(u, 3)), off);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            acc[t] = __ffma2_rn(w01, make_float2(xv[t][4 * k], xv[t][4 * k + 1]), acc[t]);
-            acc[t] = __ffma2_rn(w23, make_float2(xv[t][4 * k + 2], xv[t][4 * k + 3]), acc[t]);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-        out[t] = d * (acc[t].x + acc[t].y);
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
+    return v;
 }
 
-// One stage for one consumer lane: block w of the slice, rows l and l + 32.
-template <int NT>
-__device__ __forceinline__ void stage_dot(const uint8_t *st, int w, int lane,
-                                          float (&run)[2][kGroupTokens])
+__device__ __forceinline__ uint32_t pack_half2(__half a, __half b)
 {
+    return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
+}
+
+// One stage for one consumer lane (g, c) of warp w: block w of the slice over
+// the stage's four 16-row tiles.  k-step h (0, 1) covers codes 16h .. 16h+15
+// of the block; lane column c supplies codes 16h + 4c .. +3: (4c, 4c+1) in
+// k-slots (2c, 2c+1), (4c+2, 4c+3) in (2c+8, 2c+9).  B column n is token n/2,
+// term n%2 (hi, lo).  run[t][r]: row 16t + g + 8r, token c.
+__device__ __forceinline__ void stage_mma(const uint8_t *st, int w, int lane, int cnt,
+                                          float (&run)[4][2])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const int tk = g >> 1, term = g & 1;  // the B column this lane supplies
     const float *xs = reinterpret_cast<const float *>(st + kQ8eWBytes);  // [4][256]
-    const int blk = 34 * w;
-    float d[2];
+    // ---- B: the block's activations of token tk, scaled by 2^s (s per block
+    // and token: the largest |x| below 2^15), split into hi + lo halves
+    float4 v[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const uint8_t *row = st + (lane + 32 * r) * kQ8eSliceBytes;
-        const uint32_t dw = *reinterpret_cast<const uint32_t *>(row + (blk & ~3));
-        d[r] = __half2float(__ushort_as_half((unsigned short)((blk & 2) ? (dw >> 16) : (dw & 0xffffu))));
-    }
+    for (int h = 0; h < 2; ++h)
+        v[h] = tk < cnt ? *reinterpret_cast<const float4 *>(xs + tk * 256 + 32 * w + 16 * h + 4 * c)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t mb = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        mb = max(mb, max(max(__float_as_uint(v[h].x) & 0x7fffffffu, __float_as_uint(v[h].y) & 0x7fffffffu),
+                         max(__float_as_uint(v[h].z) & 0x7fffffffu, __float_as_uint(v[h].w) & 0x7fffffffu)));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const int s = mb ? 14 - (int(mb >> 23) - 127) : 0;
+    float xsum = (v[0].x + v[0].y) + (v[0].z + v[0].w) + ((v[1].x + v[1].y) + (v[1].z + v[1].w));
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+    uint32_t b[2][2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        // the half block's activations (the same address in every lane)
-        float xv[kGroupTokens][16];
+        const float e[4] = {scale_pow2(v[h].x, s), scale_pow2(v[h].y, s), scale_pow2(v[h].z, s),
+                            scale_pow2(v[h].w, s)};
+        __half q[4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = lds128f(xs + t * 256 + 32 * w + 16 * h + 4 * k);
-                xv[t][4 * k] = v.x;
-                xv[t][4 * k + 1] = v.y;
-                xv[t][4 * k + 2] = v.z;
-                xv[t][4 * k + 3] = v.w;
-            }
-        // codes 16h .. 16h+15 of the block start at byte o of the row slice
-        const int o = blk + 2 + 16 * h;
-        const int a16 = o & ~15;
-        const unsigned sel = (o & 2) ? 0x5432u : 0x3210u;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const uint8_t *row = st + (lane + 32 * r) * kQ8eSliceBytes;
-            const uint4 A = lds128(row + a16), B = lds128(row + a16 + 16);
-            const uint32_t a[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
-            uint32_t q[4];
-            switch ((o >> 2) & 3) {
-            case 0: pick4<0>(a, sel, q); break;
-            case 1: pick4<1>(a, sel, q); break;
-            case 2: pick4<2>(a, sel, q); break;
-            default: pick4<3>(a, sel, q); break;
-            }
-            float s[kGroupTokens];
-            half_block<NT>(q, xv, d[r], s);
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-                run[r][t] += s[t];
+        for (int i = 0; i < 4; ++i) {
+            const __half hi = __float2half_rn(e[i]);
+            q[i] = term ? __float2half_rn(e[i] - __half2float(hi)) : hi;
         }
+        b[h][0] = pack_half2(q[0], q[1]);
+        b[h][1] = pack_half2(q[2], q[3]);
+    }
+    // the D side is token c: its scale and block sum from lane (2c, 0)
+    const int sc_ = __shfl_sync(0xffffffffu, s, 8 * c);
+    const float off = -128.f * __shfl_sync(0xffffffffu, xsum, 8 * c);
+    // ---- A: four codes of rows g and g+8 of each tile per k-step
+    const int blk = 34 * w;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint8_t *r0 = st + (16 * t + g) * kQ8eSliceBytes;
+        const uint8_t *r1 = r0 + 8 * kQ8eSliceBytes;
+        float d[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int o = blk + 2 + 16 * h + 4 * c;  // 4-byte aligned when w is odd
+            uint32_t wa, wb;
+            if (w & 1) {
+                wa = lds32(r0 + o);
+                wb = lds32(r1 + o);
+            } else {
+                wa = __byte_perm(lds32(r0 + o - 2), lds32(r0 + o + 2), 0x5432u);
+                wb = __byte_perm(lds32(r1 + o - 2), lds32(r1 + o + 2), 0x5432u);
+            }
+            wa ^= 0x80808080u;  // u = q + 128
+            wb ^= 0x80808080u;
+            const uint32_t a0 = __byte_perm(wa, 0u, 0x4140u), a1 = __byte_perm(wb, 0u, 0x4140u);
+            const uint32_t a2 = __byte_perm(wa, 0u, 0x4342u), a3 = __byte_perm(wb, 0u, 0x4342u);
+            if (h == 0)
+                tc::mma16816_zero(d, a0, a1, a2, a3, b[h][0], b[h][1]);
+            else
+                tc::mma16816(d, a0, a1, a2, a3, b[h][0], b[h][1]);
+        }
+        const float d0 = __half2float(__ushort_as_half((unsigned short)lds_u16(r0 + blk)));
+        const float d1 = __half2float(__ushort_as_half((unsigned short)lds_u16(r1 + blk)));
+        // sum u x = (hi + lo columns) * 2^24 * 2^-s (two exact power-of-two steps)
+        const float u0 = scale_pow2((d[0] + d[1]) * 16777216.f, -sc_);
+        const float u1 = scale_pow2((d[2] + d[3]) * 16777216.f, -sc_);
+        run[t][0] = fmaf(d0, u0 + off, run[t][0]);
+        run[t][1] = fmaf(d1, u1 + off, run[t][1]);
     }
 }
 
@@ -312,20 +313,18 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
     int64_t k = 0;
     int ib = 0;  // item parity: which half of red[]
     const int i = int(threadIdx.x);  // 0 .. 255
-    // the (row, token) this thread stores at the end of an item
+    // the (row, token) this thread stores at the end of an item (if any)
     const int t_mine = P.nmat == 2 ? (i < kQ8eBoxRows * kGroupTokens ? i / kQ8eBoxRows : -1)
-                                   : i / kQ8eRows;
+                                   : (i < kQ8eRows * kGroupTokens ? i / kQ8eRows : -1);
     const int r_mine = P.nmat == 2 ? (i & (kQ8eBoxRows - 1)) : (i & (kQ8eRows - 1));
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x, ib ^= 1) {
         const int tt = int(it % P.tpm);
         int cnt = 0, s_mine = -1;
         float sc_mine = 1.f;
-        float run[2][kGroupTokens];
+        float run[4][2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int t = 0; t < kGroupTokens; ++t)
-                run[r][t] = 0.f;
+        for (int t = 0; t < 4; ++t)
+            run[t][0] = run[t][1] = 0.f;
         for (int j = 0; j < P.NB; ++j, ++k) {
             const int slot = int(k % NS);
             if (*reinterpret_cast<volatile int *>(&s_fail))
@@ -345,10 +344,7 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
                 if (P.xscale && s_mine >= 0)
                     sc_mine = __ldg(P.xscale + s_mine);  // used at the end of the item
             }
-            if (cnt <= 2)
-                stage_dot<2>(st, warp, lane, run);
-            else
-                stage_dot<kGroupTokens>(st, warp, lane, run);
+            stage_mma(st, warp, lane, cnt, run);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[slot]);
@@ -356,9 +352,10 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
         // the warps' sums of this item, then their sum in warp order
         float *rb = red + ib * kQ8eRedFloats;
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-            *reinterpret_cast<float4 *>(rb + (warp * kQ8eRows + lane + 32 * r) * 4) =
-                make_float4(run[r][0], run[r][1], run[r][2], run[r][3]);
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                rb[(warp * kQ8eRows + 16 * t + (lane >> 2) + 8 * r) * 4 + (lane & 3)] = run[t][r];
         consumers_sync();
         if (*reinterpret_cast<volatile int *>(&s_fail))
             break;

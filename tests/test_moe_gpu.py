@@ -173,6 +173,27 @@ def test_moe_gemv_bad_ids(fmt, routed):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_moe_gemv_edge_activations(fmt):
+    """Token rows of very different magnitudes (the per-block power-of-two
+    scale of the activations), an all-zero row and a one-hot row."""
+    E, Ne, K, T, top_k = 4, 64, 512, 6, 2
+    w, m = _stacked(E, Ne, K, seed=61, fmt=fmt)
+    ids = np.array([[0, 1], [0, 2], [1, 3], [0, 3], [2, 1], [3, 0]], np.int32)
+    X = synth.activations(T, K, seed=62)
+    X[0] *= np.float32(1e30)
+    X[1] *= np.float32(1e-30)
+    X[2] = 0.0
+    X[3] = 0.0
+    X[3, 300] = 2.5
+    X[4, :32] *= np.float32(1e20)  # one block far larger than the rest
+    y_ref, c = oracle.moe_gemv(fmt, w, E, Ne, K, ids, X, False, nthreads=NTHREADS)
+    y = _run_moe(m, E, ids, X, False)
+    assert_close_to_oracle(y, y_ref, c, TOL_FP32, f"moe edge activations fmt={fmt}")
+    assert np.all(y[4:6] == 0.0)  # token 2's slots
+    m.close()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_moe_gemv_deterministic(fmt):
     E, Ne, K, T, top_k = 64, 128, 1024, 32, 8
     w, m = _stacked(E, Ne, K, seed=31, fmt=fmt)
