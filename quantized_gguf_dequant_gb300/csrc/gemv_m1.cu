@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     // activation sums per super-block (Q6_K: one per 16-weight group)
     constexpr bool Q6 = FMT == QMM_Q6_K;
     constexpr bool IQ = FMT == QMM_IQ4_NL;
-    constexpr int SB = FMT == QMM_Q5_K ? 176 : (Q6 ? 210 : 144);
+    constexpr bool Q8 = FMT == QMM_Q8_0;
+    constexpr int SB = FMT == QMM_Q5_K ? 176 : (Q6 ? 210 : (Q8 ? 272 : 144));
     constexpr int UB = kTileRows * SB;
     constexpr int QOFF = FMT == QMM_Q5_K ? 48 : 16;
     constexpr int XN = Q6 ? 16 : 8;
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 for (int i = 0; i < 4; ++i) {
                     const int j = j0 + i * W;
                     if (j < KS)
-                        prep_sb<Q6 ? 1 : (IQ ? 2 : 0)>(v[i], w[i], lane, Bx + size_t(j) * 64,
+                        prep_sb<Q6 ? 1 : (IQ ? 2 : (Q8 ? 3 : 0))>(v[i], w[i], lane, Bx + size_t(j) * 64,
                                                         Xs + j * XN, inv + j);
                 }
             }
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if constexpr (Q6) {
                 X6 = make_float4(Xs[j * XN + g6], Xs[j * XN + g6 + 1], Xs[j * XN + g6 + 4],
                                  Xs[j * XN + g6 + 5]);
-            } else if constexpr (IQ) {
+            } else if constexpr (IQ || Q8) {
                 X0 = make_float2(Xs[j * XN + 2 * c], Xs[j * XN + 2 * c + 1]);  // blocks 2c, 2c+1
             } else {
                 X0 = make_float2(Xs[j * XN + 2 * c], Xs[j * XN + 2 * c]);
@@ -383,6 +384,14 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 d6 = lds_u16(a0 + 208) | (lds_u16(a1 + 208) << 16);
             }
             // (Q4_K / Q5_K units are 16-byte aligned; Q6_K's were read above)
+            uint32_t q8a[17], q8b[17];
+            if constexpr (Q8) {
+#pragma unroll
+                for (int q = 0; q < 17; ++q) {
+                    q8a[q] = lds32(a0 + 68 * c + 4 * q);
+                    q8b[q] = lds32(a0 + 8 * SB + 68 * c + 4 * q);
+                }
+            }
             uint32_t iwa[9], iwb[9];
             if constexpr (IQ) {
 #pragma unroll
@@ -392,7 +401,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 }
             }
             uint4 h0, h1, qa0, qa1, qb0, qb1, ha0, ha1, hb0, hb1;
-            if constexpr (!Q6 && !IQ) {
+            if constexpr (!Q6 && !IQ && !Q8) {
                 h0 = lds128(a0);
                 h1 = lds128(a0 + 8 * SB);
                 qa0 = lds128(a0 + QOFF + 32 * c);
@@ -423,7 +432,9 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if (it * TS + wt >= P.T)
                 continue;  // past the last tile (a ragged final item)
             float keep;
-            if constexpr (IQ)
+            if constexpr (Q8)
+                keep = unit_rows_q8(q8a, q8b, B, c, X0, iv);
+            else if constexpr (IQ)
                 keep = unit_rows_iq4(iwa, iwb, book, B, c, X0, iv);
             else if constexpr (Q6)
                 keep = unit_rows6(q6a, q6ha, q6b, q6hb, s6a, s6b, d6, B, c, X6, iv);
@@ -673,6 +684,7 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     const auto kern = a.fmt == QMM_Q5_K     ? gemv_m1_kernel<QMM_Q5_K>
                       : a.fmt == QMM_Q6_K   ? gemv_m1_kernel<QMM_Q6_K>
                       : a.fmt == QMM_IQ4_NL ? gemv_m1_kernel<QMM_IQ4_NL>
+                      : a.fmt == QMM_Q8_0   ? gemv_m1_kernel<QMM_Q8_0>
                                             : gemv_m1_kernel<QMM_Q4_K>;
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem, true);
     if (e != cudaSuccess)

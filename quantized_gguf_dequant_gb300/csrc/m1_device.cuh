@@ -143,7 +143,8 @@ __device__ __forceinline__ float2 pair_total(uint4 h0, uint4 h1, const ScaleSel 
 // groups instead (v's and w's halves).  MODE 2: IQ4_NL -- the k-slots of a
 // lane column take adjacent weights ((v.x, v.y) in (2c, 2c+1), (v.z, v.w) in
 // (2c+8, 2c+9); w likewise for the high-nibble MMA) and the sums are of the
-// 32-weight blocks (v and w of lanes tt & ~3 .. tt | 3).
+// 32-weight blocks (v and w of lanes tt & ~3 .. tt | 3).  MODE 3: Q8_0 --
+// MODE 2's adjacent k-slots with MODE 0's sums (v: block 2cc, w: 2cc+1).
 template <int MODE = 0>
 __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx, float *xsum,
                                         float *inv)
@@ -179,7 +180,7 @@ __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx,
     auto pack = [](__half a, __half b) {
         return uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
     };
-    if constexpr (MODE == 2) {
+    if constexpr (MODE >= 2) {
         // k-step tt: elements (0, 1) in k-slots (2c, 2c+1), (2, 3) in (2c+8, 2c+9).
         bx[(tt * 4 + cc) * 2 + 0] = make_uint4(pack(hi[0], hi[1]), pack(hi[2], hi[3]),
                                                pack(hi[4], hi[5]), pack(hi[6], hi[7]));
@@ -202,7 +203,7 @@ __device__ __forceinline__ void prep_sb(float4 v, float4 w, int lane, uint4 *bx,
             sb += __shfl_xor_sync(0xffffffffu, sb, o);
         if ((tt & 3) == 0)
             xsum[2 * cc + (tt >> 2)] = sb;
-    } else if constexpr (MODE == 0) {
+    } else if constexpr (MODE == 0 || MODE == 3) {
         // Sub-block sums (sub-blocks 2cc and 2cc+1), fixed order over tt.
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
@@ -511,6 +512,55 @@ __device__ __forceinline__ float unit_rows_iq4(const uint32_t (&wa)[9], const ui
                                  __fadd2_rn(make_float2(ub[0], ub[2]), make_float2(ub[1], ub[3])));
     const float2 da = half2_bits_to_float2(__byte_perm(wa[0], wb[0], 0x5410u));  // d of block 2c
     const float2 db = half2_bits_to_float2(__byte_perm(wa[4], wb[4], 0x7632u));  // d of block 2c+1
+    const float2 k24 = make_float2(16777216.f, 16777216.f);
+    const float2 ta = __ffma2_rn(__fmul2_rn(Sa, iv), k24, make_float2(-128.f * X.x, -128.f * X.x));
+    const float2 tb = __ffma2_rn(__fmul2_rn(Sb, iv), k24, make_float2(-128.f * X.y, -128.f * X.y));
+    const float2 tot = __ffma2_rn(da, ta, __fmul2_rn(db, tb));
+    const bool odd = c & 1;
+    float keep = odd ? tot.y : tot.x;
+    keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
+    keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+    return keep;
+}
+
+// ---------------------------------------------------------------- Q8_0
+// Eight 34-byte blocks (fp16 d, 32 int8 codes) make a 272-byte unit of 256
+// weights.  Lane column c takes blocks 2c (the "low" MMA of each k-step) and
+// 2c+1 (the "high" one); k-step t reads codes 4t .. 4t+3 of each.  A code
+// enters as u = q + 128 (one XOR flips the sign bits), two codes per fp16
+// pair (u * 2^-24, exact subnormals).  Per block: sum q x = sum u x - 128 X.
+
+// One Q8_0 unit for one lane: wa / wb the seventeen words at byte 68c of
+// rows g and g+8 (block 2c: d in the low half of word 0, codes from byte 2;
+// block 2c+1: d in the high half of word 8, codes in words 9-16); X: the
+// sums of blocks 2c and 2c+1.
+__device__ __forceinline__ float unit_rows_q8(const uint32_t (&wa)[17], const uint32_t (&wb)[17],
+                                              const uint4 (&B)[8], int c, float2 X, float2 iv)
+{
+    float da4[4], db4[4];  // blocks 2c and 2c+1
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t pa = __byte_perm(wa[t], wa[t + 1], 0x5432u) ^ 0x80808080u;  // block 2c
+        const uint32_t pb = __byte_perm(wb[t], wb[t + 1], 0x5432u) ^ 0x80808080u;
+        const uint32_t qa = wa[9 + t] ^ 0x80808080u;  // block 2c+1
+        const uint32_t qb = wb[9 + t] ^ 0x80808080u;
+        const uint32_t a0 = __byte_perm(pa, 0u, 0x4140u), a1 = __byte_perm(pb, 0u, 0x4140u);
+        const uint32_t a2 = __byte_perm(pa, 0u, 0x4342u), a3 = __byte_perm(pb, 0u, 0x4342u);
+        const uint32_t b0 = __byte_perm(qa, 0u, 0x4140u), b1 = __byte_perm(qb, 0u, 0x4140u);
+        const uint32_t b2 = __byte_perm(qa, 0u, 0x4342u), b3 = __byte_perm(qb, 0u, 0x4342u);
+        if (t == 0) {
+            mma16816_zero(da4, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816_zero(db4, b0, b1, b2, b3, B[t].z, B[t].w);
+        } else {
+            mma16816(da4, a0, a1, a2, a3, B[t].x, B[t].y);
+            mma16816(db4, b0, b1, b2, b3, B[t].z, B[t].w);
+        }
+    }
+    // (row g, row g+8): sum u x of each block (hi + lo columns)
+    const float2 Sa = __fadd2_rn(make_float2(da4[0], da4[2]), make_float2(da4[1], da4[3]));
+    const float2 Sb = __fadd2_rn(make_float2(db4[0], db4[2]), make_float2(db4[1], db4[3]));
+    const float2 da = half2_bits_to_float2(__byte_perm(wa[0], wb[0], 0x5410u));  // d of block 2c
+    const float2 db = half2_bits_to_float2(__byte_perm(wa[8], wb[8], 0x7632u));  // d of block 2c+1
     const float2 k24 = make_float2(16777216.f, 16777216.f);
     const float2 ta = __ffma2_rn(__fmul2_rn(Sa, iv), k24, make_float2(-128.f * X.x, -128.f * X.x));
     const float2 tb = __ffma2_rn(__fmul2_rn(Sb, iv), k24, make_float2(-128.f * X.y, -128.f * X.y));

@@ -251,7 +251,7 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     for (int i = 0; i < n; ++i) {
         const Matrix &mi = *reinterpret_cast<const Matrix *>(hs[i]);
         if ((mi.fmt != QMM_Q4_K && mi.fmt != QMM_Q5_K && mi.fmt != QMM_Q6_K &&
-             mi.fmt != QMM_IQ4_NL) || mi.K % 256 != 0)
+             mi.fmt != QMM_IQ4_NL && mi.fmt != QMM_Q8_0) || mi.K % 256 != 0)
             return QMM_ERR_UNSUPPORTED;
         // Q6_K: TMA boxes of 8 super-blocks (1680 bytes) need K % 2048 == 0
         if (mi.fmt == QMM_Q6_K && mi.K % 2048 != 0)
@@ -263,7 +263,11 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     if (T * 16 > (int64_t(1) << 30))
         return QMM_ERR_UNSUPPORTED;
     const int64_t NB = m0.K / 256;
-    const int sbb = m0.fmt == QMM_Q5_K ? 176 : (m0.fmt == QMM_Q6_K ? 210 : 144);
+    // bytes of 256 weights: Q4_K / IQ4_NL 144, Q5_K 176, Q6_K 210, Q8_0 272
+    const int sbb = m0.fmt == QMM_Q5_K   ? 176
+                    : m0.fmt == QMM_Q6_K ? 210
+                    : m0.fmt == QMM_Q8_0 ? 272
+                                         : 144;
     qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0, 0, sbb);
     // Fewer K slices when the handle's workspace or tickets are too small.
     for (int S = p.S; S >= 1 && (p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets); --S)
@@ -370,10 +374,11 @@ qmm_status do_gemv(const qmm_t *hs, int n, const float *x, float *const *ys, cud
     // faster on the SIMT kernel (0.266 / 0.287 against 0.334 / 0.364 ms).
     // QMM_FMT_PATH = staged, fast or plain picks the route for all three.
     const char *fp = getenv("QMM_FMT_PATH");
-    // Q5_K, Q6_K and IQ4_NL: the tensor-core decode kernel of Q4_K with the
-    // high bits added to the operands (IQ4_NL: the looked-up codes)
-    // (QMM_FMT_PATH=staged, fast or plain keeps it off).
-    if ((m0.fmt == QMM_Q5_K || m0.fmt == QMM_Q6_K || m0.fmt == QMM_IQ4_NL) && !fp) {
+    // Q5_K, Q6_K, IQ4_NL and Q8_0: the tensor-core decode kernel of Q4_K with
+    // the high bits added to the operands (IQ4_NL: the looked-up codes; Q8_0:
+    // the bytes themselves) (QMM_FMT_PATH=staged, fast or plain keeps it off).
+    if ((m0.fmt == QMM_Q5_K || m0.fmt == QMM_Q6_K || m0.fmt == QMM_IQ4_NL ||
+         (m0.fmt == QMM_Q8_0 && m0.K % 256 == 0)) && !fp) {
         qmm_status st = do_gemv_m1(hs, n, x, ys, s, fn);
         if (st != QMM_ERR_UNSUPPORTED)
             return st;

@@ -390,6 +390,33 @@ def test_gemv_batched_forced_k_slices(monkeypatch, S):
     m.close()
 
 
+@pytest.mark.parametrize("path", ["default", "staged"])
+@pytest.mark.parametrize("N,K", [(1, 256), (33, 768), (300, 2048), (1000, 4096), (77, 14336),
+                                 (4096, 14336)])
+def test_q8_0_routes(monkeypatch, path, N, K):
+    """Q8_0 on the tensor-core decode kernel (the default where K is a
+    multiple of 256) and on the staged fp32 kernel (QMM_FMT_PATH=staged),
+    sampled rows at the largest shape; grouped launch of two matrices too."""
+    if path != "default":
+        monkeypatch.setenv("QMM_FMT_PATH", path)
+    rng = np.random.default_rng(N + K)
+    rows = None if N <= 1000 else np.unique(np.concatenate(
+        [np.arange(16), np.arange(N - 16, N), rng.choice(N, 64, False)]))
+    m, w, x, y = _check_gemv(q.Q8_0, N, K, seed=N * 3 + K, rows=rows)
+    w2, m2 = _matrix(q.Q8_0, 40, K, seed=N + 1)
+    y1 = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    y2 = torch.full((40,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_group([m.h, m2.h], to_dev(x), [y1, y2])
+    torch.cuda.synchronize()
+    yr1, c1 = oracle.gemv(q.Q8_0, w, N, K, x, rows=rows, nthreads=oracle.max_threads())
+    y1h = y1.cpu().numpy()
+    assert_close_to_oracle(y1h if rows is None else y1h[rows], yr1, c1, TOL_FP32, "group 0")
+    yr2, c2 = oracle.gemv(q.Q8_0, w2, 40, K, x, nthreads=oracle.max_threads())
+    assert_close_to_oracle(y2.cpu().numpy(), yr2, c2, TOL_FP32, "group 1")
+    m.close()
+    m2.close()
+
+
 def test_launch_count_counts_kernels():
     """qmm_launch_count advances by the kernels each call launches."""
     w, m = _matrix(q.Q4_K, 512, 1024, seed=5)
