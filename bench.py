@@ -710,8 +710,9 @@ def run_ours(args, world, rank, local):
         extras["q4k_dense_ffn_decode"] = {
             "unit": "GB/s", "bytes_per_step": fb, **ffn,
             "note": "the Llama-3.1-8B SwiGLU FFN of every layer for one token: qmm_ffn_decode "
-                    "(gate and up in one launch with SwiGLU in its epilogue, then down) against "
-                    "the grouped gate/up GEMV, qmm_swiglu and the down GEMV as separate calls"}
+                    "(gate and up in one decode-kernel launch, their tiles interleaved, SwiGLU "
+                    "in its output phase, then down) against the grouped gate/up GEMV, "
+                    "qmm_swiglu and the down GEMV as separate calls"}
     q4.close()
     del q4
     torch.cuda.empty_cache()

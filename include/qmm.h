@@ -191,12 +191,14 @@ QMM_API qmm_status qmm_moe_ffn(qmm_t hg, qmm_t hu, qmm_t hd, int32_t n_experts,
 /* A dense SwiGLU FFN for one token (decode):  h = silu(Wg x) * (Wu x),
  * y = Wd h.  hg, hu: d_ff x d_model (same format), hd: d_model x d_ff.
  * x: d_model fp32, h: d_ff fp32 (the intermediate, also returned), y: d_model
- * fp32 (device; x and h 16-byte aligned, y 4-byte aligned).  For Q4_K gate/up
- * whose activations fit the decode kernel, gate and up run in one launch with
- * SwiGLU applied in its epilogue (the gate and up products never reach
- * memory); otherwise gate and up run as one grouped GEMV, the up product going
- * to scratch held by the up handle (allocated on the first such call; make
- * that call before capturing a CUDA graph), and SwiGLU runs as its own kernel.
+ * fp32 (device; x and h 16-byte aligned, y 4-byte aligned).  Where the decode
+ * kernel takes the shape (every format with K a multiple of 256; Q6_K 2048),
+ * gate and up run in one launch with SwiGLU applied in its output phase (the
+ * gate and up products never reach memory); otherwise (Q4_K) the earlier
+ * tensor-core kernel's pair mode does the same, or gate and up run as one
+ * grouped GEMV, the up product going to scratch held by the up handle
+ * (allocated on the first such call; make that call before capturing a CUDA
+ * graph), and SwiGLU runs as its own kernel.
  * Errors: QMM_ERR_SHAPE for mismatched shapes or formats, QMM_ERR_NULL,
  * QMM_ERR_ALIGN, QMM_ERR_NOMEM (scratch), QMM_ERR_CUDA; nothing is launched
  * on an argument error.

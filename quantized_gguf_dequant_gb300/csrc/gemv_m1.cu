@@ -91,10 +91,18 @@ struct M1Params {
     int F;                        // fixed items per CTA
     int cap;                      // items a CTA may take
     int nslot, slot_bytes;
+    // SwiGLU (nmat == 2, gate and up of equal rows): tiles interleaved
+    // (gate tile t at 2t, up tile t at 2t+1; items of an even number of
+    // tiles), y[0] receives silu(gate) * up
+    int fuse;
 };
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 __device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
 {
+    if (P.fuse)
+        return t & 1;
     int m = 0;
 #pragma unroll
     for (int i = 0; i < kMaxGroup - 1; ++i)
@@ -108,11 +116,11 @@ __device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
 __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, int &m, int &row)
 {
     m = mat_of_tile(P, tile);
-    row = (tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
+    row = (P.fuse ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
     return row < P.rows[m];
 }
 
-template <int FMT>
+template <int FMT, int UPW>
 __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const __grid_constant__ M1Params P)
 {
     // super-block bytes, one unit's bytes (16 rows), offset of the nibbles,
@@ -128,6 +136,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
     const int lane = threadIdx.x & 31;
     const int W = P.W, NS = P.nslot, KS = P.KS, TS = P.TS, WS = P.WS, NP = P.NP;
+    // UPW: units per consumer warp and slot (WS * TS = W * UPW)
     const int b1 = int(blockIdx.x) / P.S, sl = int(blockIdx.x) - b1 * P.S;
     const int sb0 = sl * KS;
     const int itile = TS * kTileRows;  // rows of one item
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 __syncwarp();
                 if (mine) {
                     const int m = mat_of_tile(P, tile);
-                    const int lt = tile - (m == 0 ? 0 : P.tile_end[m - 1]);
+                    const int lt = P.fuse ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1]);
                     if constexpr (Q6)  // 16 rows x 8 super-blocks (1680 bytes), row-major
                         tma_load_2d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
                                     &P.tmap[m], ((sb0 + p * WS) / 8) * 210, lt * kTileRows,
@@ -372,7 +381,14 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
             if (it < 0)
                 break;
             const int p = *(volatile int *)&s_pass[slot];
-            const uint32_t a0 = ubase + soff;
+            int kc = 0;
+            // Units w, w + W, ... of the slot (UPW of them; the same
+            // super-block, tiles wt, wt + W/WS, ...), one after the other; the
+            // slot is released once the last one is in registers.
+#pragma unroll
+            for (int u = 0; u < UPW; ++u) {
+            const int tl = wt + u * (W / WS);  // tile of the item
+            const uint32_t a0 = ubase + soff + uint32_t(u * W * UB);
             uint32_t q6a[8], q6ha[8], q6b[8], q6hb[8], s6a = 0, s6b = 0, d6 = 0;
             if constexpr (Q6) {
                 const uint32_t a1 = a0 + 8 * WS * SB;  // row g + 8
@@ -415,21 +431,25 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 hb0 = lds128(a0 + 8 * SB + 16);
                 hb1 = lds128(a0 + 8 * SB + 32);
             }
-            mbar_arrive(&empty[slot]);  // the unit is in registers: release the slot
-            soff += uint32_t(slot_bytes);
-            if (++slot == NS) {
-                slot = 0;
-                soff = 0;
-                par ^= 1u;
+            if (u == UPW - 1) {
+                mbar_arrive(&empty[slot]);  // the units are in registers: release the slot
+                soff += uint32_t(slot_bytes);
+                if (++slot == NS) {
+                    slot = 0;
+                    soff = 0;
+                    par ^= 1u;
+                }
             }
-            if (NP > 1)
-                load_b(p);
-            const int kc = k;
-            if (p == NP - 1)
-                ++k;
-            if (p == 0 && warp == 0 && lane == 0)
-                items[kc] = it;
-            if (it * TS + wt >= P.T)
+            if (u == 0) {
+                if (NP > 1)
+                    load_b(p);
+                kc = k;
+                if (p == NP - 1)
+                    ++k;
+                if (p == 0 && warp == 0 && lane == 0)
+                    items[kc] = it;
+            }
+            if (it * TS + tl >= P.T)
                 continue;  // past the last tile (a ragged final item)
             float keep;
             if constexpr (Q8)
@@ -443,26 +463,34 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                                   iv);
             else
                 keep = unit_rows(h0, h1, qa0, qa1, qb0, qb1, B, L, c, X0, X1, iv);
-            const uint32_t pa = pbase + uint32_t(kc * itile * 4);
+            const uint32_t pa = pbase + uint32_t((kc * itile + u * (W / WS) * kTileRows) * 4);
             if (p > 0)
                 keep = lds_f32_if(pa, writer) + keep;  // passes added in order
             sts_f32_if(pa, keep, writer);
+            }
         }
         named_sync(1, W * 32);
 
         // ---- output: add the columns in column order, then (S > 1) the slices
         const int nrow = k * itile;
+        // fused: row i of a gate tile pairs with row i + 16 (its up tile)
+        auto store = [&](int tile, int r, float sg, float su) {
+            int m, row;
+            if (locate_row(P, tile, r, m, row))
+                P.y[m][row] = P.fuse ? silu(sg) * su : sg;
+        };
         if (P.S == 1) {
             for (int i = threadIdx.x; i < nrow; i += W * 32) {
                 const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
-                if (tile >= P.T)
+                if (tile >= P.T || (P.fuse && (tile & 1)))
                     continue;
-                float s = 0.f;
+                float s = 0.f, su = 0.f;
                 for (int w = 0; w < WS; ++w)
                     s += part[size_t(w) * pcol + i];
-                int m, row;
-                if (locate_row(P, tile, i % kTileRows, m, row))
-                    P.y[m][row] = s;
+                if (P.fuse)
+                    for (int w = 0; w < WS; ++w)
+                        su += part[size_t(w) * pcol + i + kTileRows];
+                store(tile, i % kTileRows, s, su);
             }
         } else {
             const size_t sst = size_t(P.T) * kTileRows;
@@ -486,14 +514,16 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 if (!flags[i / itile])
                     continue;
                 const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
-                if (tile >= P.T)
+                if (tile >= P.T || (P.fuse && (tile & 1)))
                     continue;
-                float s = 0.f;
+                float s = 0.f, su = 0.f;
                 for (int q = 0; q < P.S; ++q)
                     s += __ldcg(P.ws + size_t(q) * sst + size_t(tile) * kTileRows + i % kTileRows);
-                int m, row;
-                if (locate_row(P, tile, i % kTileRows, m, row))
-                    P.y[m][row] = s;
+                if (P.fuse)
+                    for (int q = 0; q < P.S; ++q)
+                        su += __ldcg(P.ws + size_t(q) * sst + size_t(tile + 1) * kTileRows +
+                                     i % kTileRows);
+                store(tile, i % kTileRows, s, su);
             }
             named_sync(1, W * 32);
             for (int i = threadIdx.x; i < k; i += W * 32)
@@ -533,7 +563,8 @@ int env_m1_warps()
     return (e && atoi(e) == 8) ? 8 : kM1MaxWarps;
 }
 
-M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int sb_bytes)
+M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int sb_bytes,
+               int min_ts, int upw)
 {
     M1Plan p;
     if (maxw <= 0)
@@ -559,10 +590,10 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
         for (int ws = (ks < maxw ? ks : maxw); ws >= 1; --ws) {
             if (ks % ws || (q6 && ws != 8))
                 continue;
-            for (int ts = 1; ts <= 8 && ws * ts <= maxw; ts *= 2) {
+            for (int ts = min_ts > upw ? min_ts : upw; ts <= 8 && ws * ts <= maxw * upw; ts *= 2) {
                 const int64_t items = (T + ts - 1) / ts;
                 const double use = items >= per ? 1.0 : double(items) / per;
-                const double score = ws * ts * use;
+                const double score = ws * ts / upw * use;
                 if (score > best + 1e-9) {
                     best = score;
                     ws_best = ws;
@@ -608,7 +639,8 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
         return M1Plan();  // no pass width fits (Q6_K: KS not a multiple of 8)
     const int per_slice = sm_count / S >= 1 ? sm_count / S : 1;
     p.NP = p.KS / p.WS;
-    p.W = p.WS * p.TS;
+    p.upw = upw;
+    p.W = p.WS * p.TS / upw;
     p.n_items = int((T + p.TS - 1) / p.TS);
     // One CTA per SM and slice; for very tall matrices more (several waves),
     // so that a CTA's share stays within kM1MaxShare items.
@@ -640,7 +672,7 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
     p.F = avg * p.NP <= ns ? avg : (3 * p.n_items) / (4 * p.G1);
     if (p.F < 1)
         p.F = 1;
-    p.slot_bytes = p.W * kTileRows * sb_bytes;
+    p.slot_bytes = p.WS * p.TS * kTileRows * sb_bytes;  // units of the slot
     p.smem = m1_smem(p.KS, p.WS, p.TS, p.cap, ns, sb_bytes);
     p.ws_floats = S > 1 ? size_t(S) * size_t(T) * kTileRows : 0;
     p.tickets = size_t(2 * S) + (S > 1 ? size_t(p.n_items) : 0);
@@ -679,13 +711,17 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.cap = p.cap;
     P.nslot = p.nslot;
     P.slot_bytes = p.slot_bytes;
+    P.fuse = a.fuse_swiglu;
+    if (P.fuse && (a.nmat != 2 || a.rows[0] != a.rows[1] || p.TS % 2 != 0))
+        return cudaErrorInvalidValue;
     // All shared memory preferred, so that two half-SM CTAs (this launch
     // and the next) fit side by side.
-    const auto kern = a.fmt == QMM_Q5_K     ? gemv_m1_kernel<QMM_Q5_K>
-                      : a.fmt == QMM_Q6_K   ? gemv_m1_kernel<QMM_Q6_K>
-                      : a.fmt == QMM_IQ4_NL ? gemv_m1_kernel<QMM_IQ4_NL>
-                      : a.fmt == QMM_Q8_0   ? gemv_m1_kernel<QMM_Q8_0>
-                                            : gemv_m1_kernel<QMM_Q4_K>;
+    const bool two = p.upw == 2;
+    const auto kern = a.fmt == QMM_Q5_K     ? (two ? gemv_m1_kernel<QMM_Q5_K, 2> : gemv_m1_kernel<QMM_Q5_K, 1>)
+                      : a.fmt == QMM_Q6_K   ? (two ? gemv_m1_kernel<QMM_Q6_K, 2> : gemv_m1_kernel<QMM_Q6_K, 1>)
+                      : a.fmt == QMM_IQ4_NL ? (two ? gemv_m1_kernel<QMM_IQ4_NL, 2> : gemv_m1_kernel<QMM_IQ4_NL, 1>)
+                      : a.fmt == QMM_Q8_0   ? (two ? gemv_m1_kernel<QMM_Q8_0, 2> : gemv_m1_kernel<QMM_Q8_0, 1>)
+                                            : (two ? gemv_m1_kernel<QMM_Q4_K, 2> : gemv_m1_kernel<QMM_Q4_K, 1>);
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), p.smem, true);
     if (e != cudaSuccess)
         return e;

@@ -242,9 +242,17 @@ qmm_status do_gemv_tc5(qmm_t h, const float *X, int64_t ldx, int M, float *Y, in
 // QMM_ERR_UNSUPPORTED (nothing launched) when no plan fits its shared memory
 // or the handle's workspace.  QMM_M1_S fixes the number of K slices.
 qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, cudaStream_t s,
-                      const char *fn)
+                      const char *fn, bool fuse = false)
 {
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
+    // fuse (gate, up): ys[0] = silu(gate x) * (up x), the pair's tiles interleaved
+    if (fuse && (n != 2 || reinterpret_cast<const Matrix *>(hs[1])->N != m0.N))
+        return QMM_ERR_UNSUPPORTED;
+    const int min_ts = fuse ? 2 : 1;
+    // units per warp and slot: 2 for the fused pairs (a warp takes a gate
+    // tile's unit and its up tile's), else 1 (QMM_M1_UPW=2 to try 2)
+    const char *eu = getenv("QMM_M1_UPW");
+    const int upw = fuse ? 2 : ((eu && atoi(eu) == 2) ? 2 : 1);
     qmm::M1Args a;
     memset(&a, 0, sizeof(a));
     int64_t T = 0;
@@ -268,11 +276,11 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
                     : m0.fmt == QMM_Q6_K ? 210
                     : m0.fmt == QMM_Q8_0 ? 272
                                          : 144;
-    qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0, 0, sbb);
+    qmm::M1Plan p = qmm::plan_m1(T, NB, m0.sm_count, 0, 0, sbb, min_ts, upw);
     // Fewer K slices when the handle's workspace or tickets are too small.
     for (int S = p.S; S >= 1 && (p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets); --S)
         if (NB % S == 0)
-            p = qmm::plan_m1(T, NB, m0.sm_count, S, 0, sbb);
+            p = qmm::plan_m1(T, NB, m0.sm_count, S, 0, sbb, min_ts, upw);
     if (p.nslot < 2 || p.ws_floats > m0.ws_floats || p.tickets > m0.n_tickets)
         return QMM_ERR_UNSUPPORTED;
     // Each matrix's column view with boxes of this plan's pass width (kept
@@ -297,6 +305,7 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
     a.fmt = m0.fmt;
     a.nmat = n;
     a.x = x;
+    a.fuse_swiglu = fuse ? 1 : 0;
     a.ws = m0.ws;
     a.tickets = m0.tickets;
     a.status = m0.status;
@@ -1148,8 +1157,21 @@ qmm_status qmm_ffn_decode(qmm_t hg, qmm_t hu, qmm_t hd, const float *x, float *h
         return fail(QMM_ERR_ALIGN, "%s: y is not 4-byte aligned", fn);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const qmm_t gu[2] = {hg, hu};
-    if (mg.fmt == QMM_Q4_K && tc_fits(mg, 1) &&
-        !(getenv("QMM_FFN_NOFUSE") && getenv("QMM_FFN_NOFUSE")[0] == '1')) {
+    const bool nofuse = getenv("QMM_FFN_NOFUSE") && getenv("QMM_FFN_NOFUSE")[0] == '1';
+    // Gate and up on the decode kernel with SwiGLU in its output phase (the
+    // pair's tiles interleaved), where it takes the shape; QMM_FFN_PATH=tc
+    // keeps the earlier tensor-core kernel's pair mode.
+    const char *fpath = getenv("QMM_FFN_PATH");
+    st = QMM_ERR_UNSUPPORTED;
+    if (!nofuse && !(fpath && strcmp(fpath, "tc") == 0)) {
+        float *ys2[2] = {h, nullptr};
+        st = do_gemv_m1(gu, 2, x, ys2, s, fn, true);
+        if (st != QMM_OK && st != QMM_ERR_UNSUPPORTED)
+            return st;
+    }
+    if (st == QMM_OK) {
+        // h written by the fused launch
+    } else if (mg.fmt == QMM_Q4_K && tc_fits(mg, 1) && !nofuse) {
         // Gate and up in one tensor-core launch, SwiGLU in its epilogue.
         qmm::TcArgs a;
         memset(&a, 0, sizeof(a));

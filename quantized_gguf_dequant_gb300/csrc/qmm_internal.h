@@ -195,7 +195,8 @@ struct M1Plan {
     int maxw = 0;                // consumer warps at most: 8 (half an SM) or 16
     int S = 0, KS = 0;           // K slices, super-blocks per slice
     int WS = 0, NP = 0;          // super-blocks per pass, passes per item (KS = WS * NP)
-    int TS = 0, W = 0;           // tiles per item, consumer warps (WS * TS)
+    int TS = 0, W = 0;           // tiles per item, consumer warps (WS * TS / upw)
+    int upw = 1;                 // units per consumer warp and slot
     int G1 = 0;                  // CTAs per slice (grid = G1 * S)
     int n_items = 0;             // items per slice
     int F = 0;                   // fixed items per CTA (fetched before the PDL wait)
@@ -215,14 +216,17 @@ struct M1Args {
     float *ws;
     unsigned *tickets;
     unsigned *status;
+    int fuse_swiglu;              // nmat == 2 (gate, up of equal rows): y[0] = silu(gate) * up
 };
 // T: 16-row tiles over all matrices; NB: super-blocks per row; force_S > 0
 // fixes the number of K slices (it must divide NB).
 // maxw: 8 or 16 consumer warps at most (0: QMM_M1_WARPS, default 16).
 // nslot == 0: no plan fits.
 // sb_bytes: 144 (Q4_K) or 176 (Q5_K).
+// min_ts: the least tiles per item (2 for the fused gate/up pairs); upw:
+// units per consumer warp and ring slot (1, or 2: W = WS * TS / 2).
 M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw = 0,
-               int sb_bytes = 144);
+               int sb_bytes = 144, int min_ts = 1, int upw = 1);
 size_t m1_smem(int KS, int WS, int TS, int cap, int nslot, int sb_bytes = 144);
 cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s);
 

@@ -54,19 +54,28 @@ def _handles(fmt, wg, wu, wd, d_model, d_ff):
             q.Matrix(fmt, d_model, d_ff, to_dev(wd))]
 
 
-@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("fused", ["decode", "tc", "no"])
 @pytest.mark.parametrize("fmt,d_model,d_ff", [
     (q.Q4_K, 256, 256),
     (q.Q4_K, 512, 768),
     (q.Q4_K, 1024, 2816),     # more (gate, up) tile pairs than CTAs
     (q.Q4_K, 2048, 5632),
     (q.Q4_K, 4096, 14336),    # Llama-3.1-8B
-    (q.Q4_K, 40960, 256),     # activations too long for the fused kernel: grouped route
-    (q.Q8_0, 512, 768),       # Q8_0: grouped route
+    (q.Q4_K, 40960, 256),     # long activations: K sliced (decode kernel) / grouped route
+    (q.Q8_0, 512, 768),
+    (q.Q8_0, 4096, 14336),
+    (q.Q5_K, 2048, 5632),
+    (q.Q6_K, 2048, 6144),
+    (q.IQ4_NL, 1024, 2816),
 ])
 def test_ffn_decode(monkeypatch, fused, fmt, d_model, d_ff):
-    if not fused:
+    """SwiGLU fused into the decode kernel's output phase ('decode': gate and
+    up tiles interleaved in one launch), into the earlier tensor-core
+    kernel's pair mode ('tc', Q4_K), or as its own kernel ('no')."""
+    if fused == "no":
         monkeypatch.setenv("QMM_FFN_NOFUSE", "1")
+    elif fused == "tc":
+        monkeypatch.setenv("QMM_FFN_PATH", "tc")
     wg, wu, wd, x = _case(fmt, d_model, d_ff, seed=d_model + d_ff + fmt)
     h_ref, ch, y_ref, cy = _reference(fmt, wg, wu, wd, x, d_model, d_ff)
     hs = _handles(fmt, wg, wu, wd, d_model, d_ff)
