@@ -91,17 +91,16 @@ struct M1Params {
     int F;                        // fixed items per CTA
     int cap;                      // items a CTA may take
     int nslot, slot_bytes;
-    // SwiGLU (nmat == 2, gate and up of equal rows): tiles interleaved
-    // (gate tile t at 2t, up tile t at 2t+1; items of an even number of
-    // tiles), y[0] receives silu(gate) * up
-    int fuse;
 };
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
+// FUSE: the (gate, up) pair with its tiles interleaved (gate tile t at 2t,
+// up tile t at 2t+1).
+template <bool FUSE>
 __device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
 {
-    if (P.fuse)
+    if (FUSE)
         return t & 1;
     int m = 0;
 #pragma unroll
@@ -113,10 +112,11 @@ __device__ __forceinline__ int mat_of_tile(const M1Params &P, int t)
 
 // Global row (tile*16 + r) -> (matrix, row of the matrix); false if the tile
 // is the ragged end of a matrix and the row does not exist.
+template <bool FUSE>
 __device__ __forceinline__ bool locate_row(const M1Params &P, int tile, int r, int &m, int &row)
 {
-    m = mat_of_tile(P, tile);
-    row = (P.fuse ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
+    m = mat_of_tile<FUSE>(P, tile);
+    row = (FUSE ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1])) * kTileRows + r;
     return row < P.rows[m];
 }
 
@@ -136,7 +136,10 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
     const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);  // warp-uniform
     const int lane = threadIdx.x & 31;
     const int W = P.W, NS = P.nslot, KS = P.KS, TS = P.TS, WS = P.WS, NP = P.NP;
-    // UPW: units per consumer warp and slot (WS * TS = W * UPW)
+    // UPW: units per consumer warp and slot (WS * TS = W * UPW); two only for
+    // the fused (gate, up) pair: the gate unit and the up unit of the same
+    // rows and super-block, y[0] receiving silu(gate) * up
+    constexpr bool FUSE = UPW == 2;
     const int b1 = int(blockIdx.x) / P.S, sl = int(blockIdx.x) - b1 * P.S;
     const int sb0 = sl * KS;
     const int itile = TS * kTileRows;  // rows of one item
@@ -204,8 +207,8 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                     mbar_arrive_expect_tx(&full[slot], unsigned(nvalid * WS) * UB);
                 __syncwarp();
                 if (mine) {
-                    const int m = mat_of_tile(P, tile);
-                    const int lt = P.fuse ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1]);
+                    const int m = mat_of_tile<FUSE>(P, tile);
+                    const int lt = FUSE ? tile >> 1 : tile - (m == 0 ? 0 : P.tile_end[m - 1]);
                     if constexpr (Q6)  // 16 rows x 8 super-blocks (1680 bytes), row-major
                         tma_load_2d(ring + size_t(slot) * P.slot_bytes + size_t(lane) * WS * UB,
                                     &P.tmap[m], ((sb0 + p * WS) / 8) * 210, lt * kTileRows,
@@ -476,18 +479,18 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
         // fused: row i of a gate tile pairs with row i + 16 (its up tile)
         auto store = [&](int tile, int r, float sg, float su) {
             int m, row;
-            if (locate_row(P, tile, r, m, row))
-                P.y[m][row] = P.fuse ? silu(sg) * su : sg;
+            if (locate_row<FUSE>(P, tile, r, m, row))
+                P.y[m][row] = FUSE ? silu(sg) * su : sg;
         };
         if (P.S == 1) {
             for (int i = threadIdx.x; i < nrow; i += W * 32) {
                 const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
-                if (tile >= P.T || (P.fuse && (tile & 1)))
+                if (tile >= P.T || (FUSE && (tile & 1)))
                     continue;
                 float s = 0.f, su = 0.f;
                 for (int w = 0; w < WS; ++w)
                     s += part[size_t(w) * pcol + i];
-                if (P.fuse)
+                if (FUSE)
                     for (int w = 0; w < WS; ++w)
                         su += part[size_t(w) * pcol + i + kTileRows];
                 store(tile, i % kTileRows, s, su);
@@ -514,12 +517,12 @@ __global__ void __launch_bounds__(32 * (kM1MaxWarps + 1)) gemv_m1_kernel(const _
                 if (!flags[i / itile])
                     continue;
                 const int tile = items[i / itile] * TS + (i % itile) / kTileRows;
-                if (tile >= P.T || (P.fuse && (tile & 1)))
+                if (tile >= P.T || (FUSE && (tile & 1)))
                     continue;
                 float s = 0.f, su = 0.f;
                 for (int q = 0; q < P.S; ++q)
                     s += __ldcg(P.ws + size_t(q) * sst + size_t(tile) * kTileRows + i % kTileRows);
-                if (P.fuse)
+                if (FUSE)
                     for (int q = 0; q < P.S; ++q)
                         su += __ldcg(P.ws + size_t(q) * sst + size_t(tile + 1) * kTileRows +
                                      i % kTileRows);
@@ -711,8 +714,9 @@ cudaError_t launch_gemv_m1(const M1Args &a, const M1Plan &p, cudaStream_t s)
     P.cap = p.cap;
     P.nslot = p.nslot;
     P.slot_bytes = p.slot_bytes;
-    P.fuse = a.fuse_swiglu;
-    if (P.fuse && (a.nmat != 2 || a.rows[0] != a.rows[1] || p.TS % 2 != 0))
+    // the fused pair runs the two-unit kernel, everything else the one-unit one
+    if ((a.fuse_swiglu != 0) != (p.upw == 2) ||
+        (a.fuse_swiglu && (a.nmat != 2 || a.rows[0] != a.rows[1] || p.TS % 2 != 0)))
         return cudaErrorInvalidValue;
     // All shared memory preferred, so that two half-SM CTAs (this launch
     // and the next) fit side by side.

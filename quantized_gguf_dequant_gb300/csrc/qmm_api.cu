@@ -250,9 +250,8 @@ qmm_status do_gemv_m1(const qmm_t *hs, int n, const float *x, float *const *ys, 
         return QMM_ERR_UNSUPPORTED;
     const int min_ts = fuse ? 2 : 1;
     // units per warp and slot: 2 for the fused pairs (a warp takes a gate
-    // tile's unit and its up tile's), else 1 (QMM_M1_UPW=2 to try 2)
-    const char *eu = getenv("QMM_M1_UPW");
-    const int upw = fuse ? 2 : ((eu && atoi(eu) == 2) ? 2 : 1);
+    // tile's unit and its up tile's), else 1
+    const int upw = fuse ? 2 : 1;
     qmm::M1Args a;
     memset(&a, 0, sizeof(a));
     int64_t T = 0;
