@@ -245,22 +245,26 @@ __device__ __forceinline__ float unit_rows(uint4 h0, uint4 h1, uint4 qa0, uint4 
     const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u;
     const uint32_t wa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
     const uint32_t wb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
-    float dlo[4], dhi[4];
+    // four accumulation chains (k-steps even / odd) for the MMA latency
+    float dlo[2][4], dhi[2][4];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
         const uint32_t xa = wa[t], xb = wb[t], ya = wa[t] >> 8, yb = wb[t] >> 8;
-        if (t == 0) {
-            mma16816_zero(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
-            mma16816_zero(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
+        float(&l)[4] = dlo[t & 1];
+        float(&h)[4] = dhi[t & 1];
+        if (t < 2) {
+            mma16816_zero(l, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
+            mma16816_zero(h, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
         } else {
-            mma16816(dlo, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
-            mma16816(dhi, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
+            mma16816(l, xa & mlo, xb & mlo, ya & mlo, yb & mlo, B[t].x, B[t].y);
+            mma16816(h, xa & mhi, xb & mhi, ya & mhi, yb & mhi, B[t].z, B[t].w);
         }
     }
-    const float2 tot = pair_total(h0, h1, L, __fadd2_rn(make_float2(dlo[0], dlo[2]),
-                                                          make_float2(dlo[1], dlo[3])),
-                                  __fadd2_rn(make_float2(dhi[0], dhi[2]), make_float2(dhi[1], dhi[3])),
-                                  X0, X1, iv);
+    const float2 lo = __fadd2_rn(__fadd2_rn(make_float2(dlo[0][0], dlo[0][2]), make_float2(dlo[0][1], dlo[0][3])),
+                                 __fadd2_rn(make_float2(dlo[1][0], dlo[1][2]), make_float2(dlo[1][1], dlo[1][3])));
+    const float2 hi = __fadd2_rn(__fadd2_rn(make_float2(dhi[0][0], dhi[0][2]), make_float2(dhi[0][1], dhi[0][3])),
+                                 __fadd2_rn(make_float2(dhi[1][0], dhi[1][2]), make_float2(dhi[1][1], dhi[1][3])));
+    const float2 tot = pair_total(h0, h1, L, lo, hi, X0, X1, iv);
     const bool odd = c & 1;
     float keep = odd ? tot.y : tot.x;
     keep += __shfl_xor_sync(0xffffffffu, odd ? tot.x : tot.y, 1);
