@@ -657,9 +657,12 @@ M1Plan plan_m1(int64_t T, int64_t NB, int sm_count, int force_S, int maxw, int s
     // for twice a CTA's average share of items; if fewer than three slots
     // fit, the item room shrinks (never below one item over the average).
     p.cap = 2 * avg + 2;
+    // QMM_M1_NSLOT caps the ring (a tuning knob)
+    const char *en = getenv("QMM_M1_NSLOT");
+    const int ns_max = (en && atoi(en) >= 2 && atoi(en) <= 16) ? atoi(en) : 16;
     auto slots = [&](int cap) {
         int ns = 0;
-        while (ns < 16 && m1_smem(p.KS, p.WS, p.TS, cap, ns + 1, sb_bytes) <= budget)
+        while (ns < ns_max && m1_smem(p.KS, p.WS, p.TS, cap, ns + 1, sb_bytes) <= budget)
             ++ns;
         return ns;
     };
