@@ -21,18 +21,19 @@
 //
 // Work.  An item is (group, row tile): 64 rows of one matrix, or 32 rows of
 // gate and the same 32 rows of up.  An item's rows stream through shared
-// memory one K-slice of 256 weights at a time: a stage holds the rows'
-// 272-byte slices (two TMA boxes of 32 rows; rows 272 bytes apart, so the
-// lanes of a quarter warp reading neighbouring rows hit disjoint banks) and
-// the group's activations for the slice (one 1 KB bulk copy per token).  A
+// memory two K-slices of 256 weights at a time (one where a row has an odd
+// number of slices): a stage holds the rows' 544-byte pieces (two TMA boxes
+// of 32 rows over a u64 view of the rows) and the group's activations for
+// those slices (one bulk copy per token).  Longer row pieces per stage
+// measured faster than one slice (185 against 270 us per OLMoE layer).  A
 // producer warp fills a ring of stages; eight consumer warps take, in every
-// stage, Q8_0 block w of the slice for warp w (weights 32w .. 32w+31, two
-// MMA k-steps) over all 64 rows (four 16-row MMA tiles), preparing the
-// block's B fragments once; lane (g, c) keeps, over the whole K, the sums of
-// rows g and g+8 of each tile for token c.  At the end of an item the eight
-// warps' sums meet in shared memory and are added in warp order (bitwise
-// repeatable), then stored (with silu(gate) * up when fused).  CTA b takes items b, b + G,
-// b + 2G, ... of the (group, tile) sequence.
+// slice of a stage, Q8_0 block w for warp w (weights 32w .. 32w+31, two MMA
+// k-steps) over all 64 rows (four 16-row MMA tiles), preparing the block's
+// B fragments once; lane (g, c) keeps, over the whole K, the sums of rows g
+// and g+8 of each tile for token c.  At the end of an item the eight warps'
+// sums meet in shared memory and are added in warp order (bitwise
+// repeatable), then stored (with silu(gate) * up when fused).  CTA b takes
+// items b, b + G, b + 2G, ... of the (group, tile) sequence.
 #include <cstring>
 
 #include <cuda.h>
@@ -50,18 +51,25 @@ constexpr int kQ8eWarps = 8;                   // consumer warps (one per block 
 constexpr int kQ8eThreads = 32 * (kQ8eWarps + 1);
 constexpr int kQ8eRows = 64;                   // rows per item (stage)
 constexpr int kQ8eBoxRows = 32;                // rows per TMA box
-constexpr int kQ8eSliceBytes = 272;            // 8 blocks of 34 bytes = 256 weights
-constexpr int kQ8eWBytes = kQ8eRows * kQ8eSliceBytes;        // 17408
-constexpr int kQ8eXBytes = kGroupTokens * 256 * 4;           // 4096
-constexpr int kQ8eHdrBytes = 128;                            // item header (first stage)
-constexpr int kQ8eStageBytes = kQ8eWBytes + kQ8eXBytes + kQ8eHdrBytes;  // 21632
+constexpr int kQ8eHdrBytes = 128;              // item header (first stage)
 constexpr int kQ8eRedFloats = kQ8eWarps * kQ8eRows * 4;      // one item's per-warp sums
 
+// A stage holds SPS K-slices of 256 weights (SPS = 2 where the row has an
+// even number of slices: 544-byte row pieces, half as many stages per item).
+template <int SPS>
+struct Q8eShape {
+    static constexpr int kSlice = 272 * SPS;                   // bytes of a row in a stage
+    static constexpr int kW = kQ8eRows * kSlice;               // weight bytes of a stage
+    static constexpr int kX = kGroupTokens * 256 * SPS * 4;    // activations of a stage
+    static constexpr int kStage = kW + kX + kQ8eHdrBytes;
+    static constexpr int kStages = SPS == 1 ? 8 : 4;
+    static_assert(kStage % 128 == 0, "stages start on 128-byte boundaries");
+};
+
 static_assert(kGroupTokens == 4, "the consumer keeps four token sums per row");
-static_assert(kQ8eStageBytes % 128 == 0, "stages start on 128-byte boundaries");
 
 struct MoeQ8Params {
-    CUtensorMap tmap[2];    // u32 view of the stacked experts' rows, box (68, 32)
+    CUtensorMap tmap[2];    // u64 view of the stacked experts' rows, box (34 * SPS, 32)
     float *y[2];
     const float *x;
     int64_t ldx;
@@ -128,18 +136,23 @@ __device__ __forceinline__ uint32_t pack_half2(__half a, __half b)
 // of the block; lane column c supplies codes 16h + 4c .. +3: (4c, 4c+1) in
 // k-slots (2c, 2c+1), (4c+2, 4c+3) in (2c+8, 2c+9).  B column n is token n/2,
 // term n%2 (hi, lo).  run[t][r]: row 16t + g + 8r, token c.
-__device__ __forceinline__ void stage_mma(const uint8_t *st, int w, int lane, int cnt,
+template <int SPS>
+__device__ __forceinline__ void stage_mma(const uint8_t *st, int sl, int w, int lane, int cnt,
                                           float (&run)[4][2])
 {
+    using S = Q8eShape<SPS>;
     const int g = lane >> 2, c = lane & 3;
     const int tk = g >> 1, term = g & 1;  // the B column this lane supplies
-    const float *xs = reinterpret_cast<const float *>(st + kQ8eWBytes);  // [4][256]
+    // slice sl of the stage: activations [4][256 * SPS] from + sl * 256, rows
+    // S::kSlice bytes apart from + sl * 272
+    const float *xs = reinterpret_cast<const float *>(st + S::kW) + sl * 256;
+    const int xst = 256 * SPS;
     // ---- B: the block's activations of token tk, scaled by 2^s (s per block
     // and token: the largest |x| below 2^15), split into hi + lo halves
     float4 v[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-        v[h] = tk < cnt ? *reinterpret_cast<const float4 *>(xs + tk * 256 + 32 * w + 16 * h + 4 * c)
+        v[h] = tk < cnt ? *reinterpret_cast<const float4 *>(xs + tk * xst + 32 * w + 16 * h + 4 * c)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
     uint32_t mb = 0;
 #pragma unroll
@@ -173,8 +186,8 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int w, int lane, in
     const int blk = 34 * w;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        const uint8_t *r0 = st + (16 * t + g) * kQ8eSliceBytes;
-        const uint8_t *r1 = r0 + 8 * kQ8eSliceBytes;
+        const uint8_t *r0 = st + (16 * t + g) * S::kSlice + sl * 272;
+        const uint8_t *r1 = r0 + 8 * S::kSlice;
         float d[4];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -206,12 +219,15 @@ __device__ __forceinline__ void stage_mma(const uint8_t *st, int w, int lane, in
     }
 }
 
+template <int SPS>
 __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_constant__ MoeQ8Params P)
 {
+    using S = Q8eShape<SPS>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int NS = P.nstage;
+    const int NJ = P.NB / SPS;  // stages per item
     uint8_t *stages = smem;
-    float *red = reinterpret_cast<float *>(smem + size_t(NS) * kQ8eStageBytes);  // [2][8][64][4]
+    float *red = reinterpret_cast<float *>(smem + size_t(NS) * S::kStage);  // [2][8][64][4]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + 2 * kQ8eRedFloats);
     uint64_t *empty = full + NS;
     __shared__ int s_fail;
@@ -258,7 +274,7 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
                 const int tt = int(it % P.tpm);
                 const int4 grp = gA;
                 const int y0 = grp.x * P.Ne + tt * rows_per_mat;
-                for (int j = 0; j < P.NB; ++j, ++k) {
+                for (int j = 0; j < NJ; ++j, ++k) {
                     const int slot = int(k % NS);
                     if (k >= NS &&
                         !mbar_wait_bounded(&empty[slot], unsigned((k / NS - 1) & 1))) {
@@ -267,30 +283,30 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
                         failed = true;
                         break;
                     }
-                    uint8_t *st = stages + size_t(slot) * kQ8eStageBytes;
+                    uint8_t *st = stages + size_t(slot) * S::kStage;
                     if (j == 0) {  // the item's token count and slots
-                        int *hdr = reinterpret_cast<int *>(st + kQ8eWBytes + kQ8eXBytes);
+                        int *hdr = reinterpret_cast<int *>(st + S::kW + S::kX);
                         hdr[0] = grp.z;
 #pragma unroll
                         for (int m = 0; m < kGroupTokens; ++m)
                             hdr[1 + m] = sA[m];
                     }
-                    mbar_arrive_expect_tx(&full[slot], unsigned(kQ8eWBytes + grp.z * 1024));
+                    mbar_arrive_expect_tx(&full[slot], unsigned(S::kW + grp.z * 1024 * SPS));
+                    const int xw = j * 34 * SPS;  // u64 words into the row
                     if (P.nmat == 2) {
-                        tma_box(st, &P.tmap[0], j * 68, y0, &full[slot], pw);
-                        tma_box(st + kQ8eBoxRows * kQ8eSliceBytes, &P.tmap[1], j * 68, y0,
-                                &full[slot], pw);
+                        tma_box(st, &P.tmap[0], xw, y0, &full[slot], pw);
+                        tma_box(st + kQ8eBoxRows * S::kSlice, &P.tmap[1], xw, y0, &full[slot], pw);
                     } else {
-                        tma_box(st, &P.tmap[0], j * 68, y0, &full[slot], pw);
-                        tma_box(st + kQ8eBoxRows * kQ8eSliceBytes, &P.tmap[0], j * 68,
-                                y0 + kQ8eBoxRows, &full[slot], pw);
+                        tma_box(st, &P.tmap[0], xw, y0, &full[slot], pw);
+                        tma_box(st + kQ8eBoxRows * S::kSlice, &P.tmap[0], xw, y0 + kQ8eBoxRows,
+                                &full[slot], pw);
                     }
 #pragma unroll
                     for (int m = 0; m < kGroupTokens; ++m)
                         if (m < grp.z) {
                             const int64_t xrow = P.x_per_slot ? sA[m] : sA[m] / P.top_k;
-                            bulk_g2s(st + kQ8eWBytes + m * 1024, P.x + xrow * P.ldx + j * 256,
-                                     1024u, &full[slot], px);
+                            bulk_g2s(st + S::kW + m * 1024 * SPS, P.x + xrow * P.ldx + j * 256 * SPS,
+                                     1024u * SPS, &full[slot], px);
                         }
                 }
                 gA = gB;
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
 #pragma unroll
         for (int t = 0; t < 4; ++t)
             run[t][0] = run[t][1] = 0.f;
-        for (int j = 0; j < P.NB; ++j, ++k) {
+        for (int j = 0; j < NJ; ++j, ++k) {
             const int slot = int(k % NS);
             if (*reinterpret_cast<volatile int *>(&s_fail))
                 break;
@@ -336,15 +352,17 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
                 }
                 break;
             }
-            const uint8_t *st = stages + size_t(slot) * kQ8eStageBytes;
+            const uint8_t *st = stages + size_t(slot) * S::kStage;
             if (j == 0) {
-                const int *hdr = reinterpret_cast<const int *>(st + kQ8eWBytes + kQ8eXBytes);
+                const int *hdr = reinterpret_cast<const int *>(st + S::kW + S::kX);
                 cnt = hdr[0];
                 s_mine = (t_mine >= 0 && t_mine < cnt) ? hdr[1 + t_mine] : -1;
                 if (P.xscale && s_mine >= 0)
                     sc_mine = __ldg(P.xscale + s_mine);  // used at the end of the item
             }
-            stage_mma(st, warp, lane, cnt, run);
+#pragma unroll
+            for (int sl = 0; sl < SPS; ++sl)
+                stage_mma<SPS>(st, sl, warp, lane, cnt, run);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[slot]);
@@ -388,19 +406,25 @@ __global__ void __launch_bounds__(kQ8eThreads, 1) moe_q8_kernel(const __grid_con
 
 } // namespace
 
-size_t moe_q8_smem(int nstage)
-{
-    return size_t(nstage) * kQ8eStageBytes + size_t(2) * kQ8eRedFloats * sizeof(float) +
-           size_t(2) * nstage * sizeof(uint64_t);
-}
+// Slices per stage for rows of NB 256-weight slices.
+// (Four slices per stage measured slower: two stages in flight and 4-way
+// bank conflicts at a 1088-byte row stride.)
+int moe_q8_sps(int64_t NB) { return NB % 2 == 0 ? 2 : 1; }
 
-int moe_q8_stages() { return 8; }
+size_t moe_q8_smem(int sps)
+{
+    const size_t stage = sps == 2 ? size_t(Q8eShape<2>::kStage) : size_t(Q8eShape<1>::kStage);
+    const int ns = sps == 2 ? Q8eShape<2>::kStages : Q8eShape<1>::kStages;
+    return size_t(ns) * stage + size_t(2) * kQ8eRedFloats * sizeof(float) +
+           size_t(2) * ns * sizeof(uint64_t);
+}
 
 int encode_moe_q8_map(void *out128, const void *w, int64_t N, int64_t row_bytes)
 {
-    return encode_tmap_2d(out128, CU_TENSOR_MAP_DATA_TYPE_UINT32, w, uint64_t(row_bytes / 4),
-                          uint64_t(N), uint64_t(row_bytes), 68u, uint32_t(kQ8eBoxRows),
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int sps = moe_q8_sps(row_bytes / 272);
+    return encode_tmap_2d(out128, CU_TENSOR_MAP_DATA_TYPE_UINT64, w, uint64_t(row_bytes / 8),
+                          uint64_t(N), uint64_t(row_bytes), uint32_t(34 * sps),
+                          uint32_t(kQ8eBoxRows), CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 cudaError_t launch_moe_q8(const MoeExpertArgs &a, int sm_count, cudaStream_t s)
@@ -426,9 +450,11 @@ cudaError_t launch_moe_q8(const MoeExpertArgs &a, int sm_count, cudaStream_t s)
     P.tpm = int((a.Ne + rows - 1) / rows);
     P.top_k = a.top_k;
     P.x_per_slot = a.x_per_slot;
-    P.nstage = moe_q8_stages();
-    const size_t smem = moe_q8_smem(P.nstage);
-    cudaError_t e = func_smem(reinterpret_cast<const void *>(moe_q8_kernel), smem);
+    const int sps = moe_q8_sps(P.NB);
+    P.nstage = sps == 2 ? Q8eShape<2>::kStages : Q8eShape<1>::kStages;
+    const size_t smem = moe_q8_smem(sps);
+    const auto kern = sps == 2 ? moe_q8_kernel<2> : moe_q8_kernel<1>;
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -441,7 +467,7 @@ cudaError_t launch_moe_q8(const MoeExpertArgs &a, int sm_count, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return counted(cudaLaunchKernelEx(&cfg, moe_q8_kernel, P));
+    return counted(cudaLaunchKernelEx(&cfg, kern, P));
 }
 
 } // namespace qmm

@@ -334,8 +334,8 @@ cudaError_t launch_moe_expert(const MoeExpertArgs &a, int sm_count, cudaStream_t
 // moe_q8.cu: the expert GEMV for Q8_0 weights (K % 256 == 0), on the same
 // bucketing and arguments (tmap: the maps of encode_moe_q8_map; maxpairs
 // unused; SwiGLU fusion always fits).
-size_t moe_q8_smem(int nstage);
-int moe_q8_stages();
+int moe_q8_sps(int64_t NB);     // K-slices per stage (1 or 2)
+size_t moe_q8_smem(int sps);
 int encode_moe_q8_map(void *out128, const void *w, int64_t N, int64_t row_bytes);
 cudaError_t launch_moe_q8(const MoeExpertArgs &a, int sm_count, cudaStream_t s);
 cudaError_t launch_swiglu(const float *g, const float *u, float *h, int64_t n, int sm_count,
