@@ -254,13 +254,25 @@ class Model:
             else:
                 q.gemv(md.h, xv[3], yv[6])
 
-    def q8k_step(self, which="all"):
+    def q8k_step(self, which="all", fused=False):
         """The decode step on the integer-dot variant: each distinct input
         quantized to Q8_K once (qmm_quantize_q8_k), then qmm_gemv_q8k_group
-        (q/k/v, gate/up) and qmm_gemv_q8k (o, down).  which: 'all', 'short'
-        (the K=4096 launches with their quantizations) or 'long' (down)."""
+        (q/k/v, gate/up) and qmm_gemv_q8k (o, down); fused: the quantization
+        inside each GEMV launch (qmm_gemv_q8k_fused[_group]).  which: 'all',
+        'short' (the K=4096 launches with their quantizations) or 'long'
+        (down)."""
         import torch
         q = self.q
+        if fused:
+            for mats, xv, yv in self.layers:
+                mq, mk, mv, mo, mg, mu, md = mats
+                if which in ("all", "short"):
+                    q.gemv_q8k_fused_group([mq.h, mk.h, mv.h], xv[0], yv[0:3])
+                    q.gemv_q8k_fused(mo.h, xv[1], yv[3])
+                    q.gemv_q8k_fused_group([mg.h, mu.h], xv[2], yv[4:6])
+                if which in ("all", "long"):
+                    q.gemv_q8k_fused(md.h, xv[3], yv[6])
+            return
         if getattr(self, "xq", None) is None:
             sizes = [4096, 4096, 4096, 14336]
             self.xq = [[torch.empty(k // 256 * q.Q8_K_BLOCK, dtype=torch.uint8,
@@ -678,6 +690,17 @@ def run_ours(args, world, rank, local):
             "note": "opt-in Q8_K activations + dp4a integer dot (qmm_quantize_q8_k, "
                     "qmm_gemv_q8k[_group]); bytes counted as for the f32 step (weights once, "
                     "f32 inputs once, outputs); drift vs f32 bounded by sum |w| |d|/2 per block"}
+        st_f = time_graph_stats(lambda: q4.q8k_step("all", fused=True), max(20, args.steps // 4),
+                                args.warmup, world)
+        ms_f = st_f["median_ms"]
+        extras["q4k_decode_q8k_integer_fused"] = {
+            "value": step_bytes / (ms_f * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_f,
+            "min_ms": st_f["min_ms"], "reps": st_f["reps"],
+            "launches_per_step": launches_of(lambda: q4.q8k_step("all", fused=True)),
+            "frac_of_peak": step_bytes / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "f32_over_q8k_time": ms / ms_f,
+            "note": "the same integer-dot step with the Q8_K quantization inside each GEMV "
+                    "launch (qmm_gemv_q8k_fused[_group]; bitwise equal results)"}
     if args.extras:
         bm = BatchedModel(q4)
         sweep = {}

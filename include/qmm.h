@@ -306,6 +306,17 @@ QMM_API qmm_status qmm_gemv_q8k(qmm_t h, const void *xq, float *y, qmm_stream st
 QMM_API qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq,
                                       float *const *ys, qmm_stream stream);
 
+/* qmm_gemv_q8k and qmm_gemv_q8k_group on f32 activations x (K values,
+ * device, 16-byte aligned): the launch quantizes x to Q8_K itself (every CTA
+ * the blocks it reads, in shared memory; the same bytes as
+ * qmm_quantize_q8_k) and runs the same integer-dot GEMV, so the results are
+ * bitwise those of qmm_quantize_q8_k followed by qmm_gemv_q8k[_group], in one
+ * launch instead of two and without the xq buffer.  Errors as for those
+ * calls; x NULL: QMM_ERR_NULL. */
+QMM_API qmm_status qmm_gemv_q8k_fused(qmm_t h, const float *x, float *y, qmm_stream stream);
+QMM_API qmm_status qmm_gemv_q8k_fused_group(const qmm_t *hs, int32_t n, const float *x,
+                                            float *const *ys, qmm_stream stream);
+
 /* Read and clear the handle's device status word (synchronises the handle's
  * last stream first).  QMM_OK when no device-side fault was recorded. */
 QMM_API qmm_status qmm_get_status(qmm_t h);

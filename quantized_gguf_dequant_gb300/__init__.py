@@ -35,7 +35,8 @@ ENTRY_POINTS = (
     "qmm_moe_gemv", "qmm_swiglu", "qmm_moe_ffn", "qmm_gemm", "qmm_dequantize",
     "qmm_dequantize_bf16", "qmm_get_status", "qmm_last_error", "qmm_version",
     "qmm_gemv_noalloc", "qmm_gemm_group", "qmm_launch_count", "qmm_ffn_decode",
-    "qmm_quantize_q8_k", "qmm_gemv_q8k", "qmm_gemv_q8k_group",
+    "qmm_quantize_q8_k", "qmm_gemv_q8k", "qmm_gemv_q8k_group", "qmm_gemv_q8k_fused",
+    "qmm_gemv_q8k_fused_group",
 )
 
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
             "qmm_quantize_q8_k": [vp, i64, vp, vp],
             "qmm_gemv_q8k": [vp, vp, vp, vp],
             "qmm_gemv_q8k_group": [ctypes.POINTER(vp), i32, vp, ctypes.POINTER(vp), vp],
+            "qmm_gemv_q8k_fused": [vp, vp, vp, vp],
+            "qmm_gemv_q8k_fused_group": [ctypes.POINTER(vp), i32, vp, ctypes.POINTER(vp), vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -202,6 +205,19 @@ def gemv_q8k_group(hs, xq, ys, stream=None):
     harr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(h) for h in hs])
     yarr = (ctypes.c_void_p * n)(*[_ptr(y) for y in ys])
     _check(lib().qmm_gemv_q8k_group(harr, n, _ptr(xq), yarr, _stream(stream)))
+
+
+def gemv_q8k_fused(h: int, x, y, stream=None):
+    """qmm_gemv_q8k_fused: the integer-dot GEMV on f32 activations, quantized
+    to Q8_K inside the launch."""
+    _check(lib().qmm_gemv_q8k_fused(ctypes.c_void_p(h), _ptr(x), _ptr(y), _stream(stream)))
+
+
+def gemv_q8k_fused_group(hs, x, ys, stream=None):
+    n = len(hs)
+    harr = (ctypes.c_void_p * n)(*[ctypes.c_void_p(h) for h in hs])
+    yarr = (ctypes.c_void_p * n)(*[_ptr(y) for y in ys])
+    _check(lib().qmm_gemv_q8k_fused_group(harr, n, _ptr(x), yarr, _stream(stream)))
 
 
 def gemm(h: int, X_bf16, M: int, Y, stream=None):

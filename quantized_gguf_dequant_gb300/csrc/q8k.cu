@@ -134,6 +134,7 @@ struct Q8kParams {
     int NB;             // super-blocks per row
     int64_t row_bytes;
     const uint8_t *xq;  // Q8_K blocks of the activations
+    const float *x;     // or the f32 activations, quantized in the kernel
     int lshift;         // log2(lanes per row)
     int64_t n_groups;   // row groups (32 >> lshift rows each)
 };
@@ -193,6 +194,72 @@ __device__ __forceinline__ float super_block_dot(const uint4 (&v)[9], const uint
     return (dm.x * dx) * float(sumi) - (dm.y * dx) * float(summ);
 }
 
+// Q8_K quantization of activation block b (256 values at xb) by one warp:
+// the record's codes, sub-block code sums and d, exactly as
+// quantize_q8k_kernel writes the block (the same steps and rounding).
+__device__ __forceinline__ void quantize_record(const float *xb, int lane, uint8_t *rec)
+{
+    const float4 v0 = __ldg(reinterpret_cast<const float4 *>(xb) + lane);
+    const float4 v1 = __ldg(reinterpret_cast<const float4 *>(xb + 128) + lane);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float amax = 0.f, mx = 0.f;
+    int mi = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float ax = fabsf(v[k]);
+        if (ax > amax) {
+            amax = ax;
+            mx = v[k];
+            mi = (k < 4 ? 0 : 128) + 4 * lane + (k & 3);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oa = __shfl_xor_sync(0xffffffffu, amax, o);
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+        if (oa > amax || (oa == amax && oi < mi)) {
+            amax = oa;
+            mx = om;
+            mi = oi;
+        }
+    }
+    int q[8];
+    float d = 0.f;
+    if (amax == 0.f) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            q[k] = 0;
+    } else {
+        const float iscale = __fdiv_rn(-127.f, mx);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            q[k] = min(127, __float2int_rn(__fmul_rn(iscale, v[k])));
+        d = __fdiv_rn(1.f, iscale);
+    }
+    reinterpret_cast<uint32_t *>(rec)[lane] =
+        (uint32_t(q[0]) & 0xffu) | ((uint32_t(q[1]) & 0xffu) << 8) |
+        ((uint32_t(q[2]) & 0xffu) << 16) | (uint32_t(q[3]) << 24);
+    reinterpret_cast<uint32_t *>(rec + 128)[lane] =
+        (uint32_t(q[4]) & 0xffu) | ((uint32_t(q[5]) & 0xffu) << 8) |
+        ((uint32_t(q[6]) & 0xffu) << 16) | (uint32_t(q[7]) << 24);
+    // sub-block j (32 codes): lanes 8j'..8j'+7 of the first (j = j') or
+    // second (j = 4 + j') half
+    int s0 = q[0] + q[1] + q[2] + q[3], s1 = q[4] + q[5] + q[6] + q[7];
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+    if ((lane & 7) == 0) {
+        reinterpret_cast<int *>(rec + 256)[lane >> 3] = s0;
+        reinterpret_cast<int *>(rec + 256)[4 + (lane >> 3)] = s1;
+    }
+    if (lane == 0)
+        *reinterpret_cast<float *>(rec + 288) = d;
+}
+
+template <bool FROMX>
 __global__ void __launch_bounds__(32 * kWarps) gemv_q8k_kernel(const __grid_constant__ Q8kParams P)
 {
     extern __shared__ __align__(16) uint8_t sx[];
@@ -236,7 +303,12 @@ __global__ void __launch_bounds__(32 * kWarps) gemv_q8k_kernel(const __grid_cons
     uint4 va[9], vb[9];
     load(g, st, va);
 
-    pdl_wait();  // the Q8_K activations come from the quantize kernel
+    pdl_wait();  // the activations come from the previous kernel
+    if constexpr (FROMX) {
+        // Quantize the activations here, one Q8_K block per warp in turn.
+        for (int b = warp; b < P.NB; b += kWarps)
+            quantize_record(P.x + int64_t(b) * 256, lane, sx + b * kRec);
+    } else {
     // Stage the activations: codes (4-byte words), sub-block code sums, d.
     for (int i = threadIdx.x; i < P.NB * 64; i += blockDim.x) {
         const int b = i >> 6, j = i & 63;
@@ -251,6 +323,7 @@ __global__ void __launch_bounds__(32 * kWarps) gemv_q8k_kernel(const __grid_cons
     for (int b = threadIdx.x; b < P.NB; b += blockDim.x)
         *reinterpret_cast<float *>(sx + b * kRec + 288) =
             __ldg(reinterpret_cast<const float *>(P.xq + int64_t(b) * kQ8kBlock));
+    }
     __syncthreads();
 
     float acc = 0.f;
@@ -333,6 +406,7 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     P.NB = int(a.K / 256);
     P.row_bytes = (a.K / 256) * 144;
     P.xq = a.xq;
+    P.x = a.x;
     // lanes per row: NB when it divides 32 (several rows per warp), else 32
     int lshift = 5;
     for (int l = 0; l <= 5; ++l)
@@ -344,7 +418,8 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     const int64_t R = 32 >> lshift;
     P.n_groups = (tot + R - 1) / R;
     const size_t smem = q8k_smem(a.K);
-    cudaError_t e = func_smem(reinterpret_cast<const void *>(gemv_q8k_kernel), smem);
+    const auto kern = a.x ? gemv_q8k_kernel<true> : gemv_q8k_kernel<false>;
+    cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;
     const int64_t want = (P.n_groups + kWarps - 1) / kWarps;
@@ -352,7 +427,7 @@ cudaError_t launch_gemv_q8k(const Q8kArgs &a, int sm_count, cudaStream_t s)
     if (const char *e = getenv("QMM_Q8K_CTAS"))  // tuning override: grid cap
         cap = std::max<int64_t>(1, atoll(e));
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, cap));
-    return launch_pdl(gemv_q8k_kernel, dim3(unsigned(grid)), dim3(32 * kWarps), smem, s, P);
+    return launch_pdl(kern, dim3(unsigned(grid)), dim3(32 * kWarps), smem, s, P);
 }
 
 } // namespace qmm

@@ -1416,11 +1416,15 @@ qmm_status qmm_quantize_q8_k(const float *x, int64_t K, void *xq, qmm_stream str
     return QMM_OK;
 }
 
-qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float *const *ys,
-                              qmm_stream stream)
+} // extern "C"
+
+namespace {
+
+// The integer-dot GEMV for n matrices: on Q8_K blocks xq, or (x non-null)
+// on f32 activations quantized inside the launch.
+qmm_status q8k_group_common(const qmm_t *hs, int32_t n, const void *xq, const float *x,
+                            float *const *ys, qmm_stream stream, const char *fn)
 {
-    g_err.clear();
-    const char *fn = "qmm_gemv_q8k_group";
     if (!hs || !ys)
         return fail(QMM_ERR_NULL, "%s: the %s array is NULL", fn, !hs ? "handle" : "output");
     if (n < 1 || n > qmm::kMaxGroup)
@@ -1448,10 +1452,15 @@ qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float 
         a.y[i] = ys[i];
         a.N[i] = mi.N;
     }
-    if (!xq)
-        return fail(QMM_ERR_NULL, "%s: xq is NULL", fn);
-    if (!aligned(xq, 4))
-        return fail(QMM_ERR_ALIGN, "%s: xq is not 4-byte aligned", fn);
+    if (x) {
+        if (!aligned(x, 16))
+            return fail(QMM_ERR_ALIGN, "%s: x is not 16-byte aligned", fn);
+    } else {
+        if (!xq)
+            return fail(QMM_ERR_NULL, "%s: xq is NULL", fn);
+        if (!aligned(xq, 4))
+            return fail(QMM_ERR_ALIGN, "%s: xq is not 4-byte aligned", fn);
+    }
     const Matrix &m0 = *reinterpret_cast<const Matrix *>(hs[0]);
     if (qmm::q8k_smem(m0.K) > size_t(kMaxSmem))
         return fail(QMM_ERR_SHAPE, "%s: K = %lld; its Q8_K activations (%zu bytes) exceed shared "
@@ -1459,6 +1468,7 @@ qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float 
     a.nmat = n;
     a.K = m0.K;
     a.xq = static_cast<const uint8_t *>(xq);
+    a.x = x;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = qmm::launch_gemv_q8k(a, m0.sm_count, s);
     if (e != cudaSuccess)
@@ -1467,9 +1477,37 @@ qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float 
     return QMM_OK;
 }
 
+} // namespace
+
+extern "C" {
+
+qmm_status qmm_gemv_q8k_group(const qmm_t *hs, int32_t n, const void *xq, float *const *ys,
+                              qmm_stream stream)
+{
+    g_err.clear();
+    return q8k_group_common(hs, n, xq, nullptr, ys, stream, "qmm_gemv_q8k_group");
+}
+
 qmm_status qmm_gemv_q8k(qmm_t h, const void *xq, float *y, qmm_stream stream)
 {
     return qmm_gemv_q8k_group(&h, 1, xq, &y, stream);
+}
+
+qmm_status qmm_gemv_q8k_fused_group(const qmm_t *hs, int32_t n, const float *x,
+                                    float *const *ys, qmm_stream stream)
+{
+    g_err.clear();
+    if (!x)
+        return fail(QMM_ERR_NULL, "qmm_gemv_q8k_fused_group: x is NULL");
+    return q8k_group_common(hs, n, nullptr, x, ys, stream, "qmm_gemv_q8k_fused_group");
+}
+
+qmm_status qmm_gemv_q8k_fused(qmm_t h, const float *x, float *y, qmm_stream stream)
+{
+    g_err.clear();
+    if (!x)
+        return fail(QMM_ERR_NULL, "qmm_gemv_q8k_fused: x is NULL");
+    return q8k_group_common(&h, 1, nullptr, x, &y, stream, "qmm_gemv_q8k_fused");
 }
 
 } // extern "C"

@@ -380,6 +380,7 @@ struct Q8kArgs {
     int nmat;
     int64_t K;
     const uint8_t *xq;            // Q8_K blocks of the activations (K/256 x 292 bytes)
+    const float *x;               // or (non-null) the f32 activations, quantized in the GEMV
 };
 size_t q8k_smem(int64_t K);
 cudaError_t launch_quantize_q8k(const float *x, int64_t K, uint8_t *out, cudaStream_t s);

@@ -110,6 +110,11 @@ def test_gemv_q8k_matches_oracle(N, K):
     q.gemv_q8k(m.h, _quantize_dev(x), y2)
     torch.cuda.synchronize()
     assert np.array_equal(got.view(np.int32), y2.cpu().numpy().view(np.int32))
+    # quantized inside the GEMV launch: the same bits
+    y3 = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_q8k_fused(m.h, to_dev(x), y3)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.view(np.int32), y3.cpu().numpy().view(np.int32))
     m.close()
 
 
@@ -145,12 +150,39 @@ def test_gemv_q8k_group():
     ms = [q.Matrix(q.Q4_K, N, K, to_dev(w)) for N, w in zip(shapes, ws)]
     ys = [torch.full((N,), float("nan"), dtype=torch.float32, device="cuda") for N in shapes]
     q.gemv_q8k_group([m.h for m in ms], _quantize_dev(x), ys)
+    yf = [torch.full((N,), float("nan"), dtype=torch.float32, device="cuda") for N in shapes]
+    q.gemv_q8k_fused_group([m.h for m in ms], to_dev(x), yf)
     torch.cuda.synchronize()
-    for N, w, y in zip(shapes, ws, ys):
+    for N, w, y, y2 in zip(shapes, ws, ys, yf):
         y_ref, c = oracle.gemv_q8k(q.Q4_K, w, N, K, xq, nthreads=NTHREADS)
         assert_close_to_oracle(y.cpu().numpy(), y_ref, c, TOL_Q8K, f"group N={N}")
+        assert np.array_equal(y.cpu().numpy().view(np.int32), y2.cpu().numpy().view(np.int32))
     for m in ms:
         m.close()
+
+
+@pytest.mark.parametrize("K", [256, 4096, 14336])
+def test_gemv_q8k_fused_special_blocks(K):
+    """The in-launch quantization on blocks with a zero block, ties of the
+    largest magnitude and extreme scales: the same bits as the separate
+    quantization."""
+    N = 40
+    w = synth.q4k_matrix(N, K, seed=K + 7)
+    x = synth.activations(1, K, seed=K + 8)[0]
+    x[:256] = 0.0                      # a zero block
+    if K > 256:
+        x[256:512] = np.float32(1e-30) * x[256:512]
+        amax = np.abs(x[256:512]).max()
+        x[300], x[301] = -amax, amax  # ties in magnitude: the first one sets the sign
+    x[-256:] *= np.float32(1e30)
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    y1 = torch.empty(N, dtype=torch.float32, device="cuda")
+    y2 = torch.empty(N, dtype=torch.float32, device="cuda")
+    q.gemv_q8k(m.h, _quantize_dev(x), y1)
+    q.gemv_q8k_fused(m.h, to_dev(x), y2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y1.cpu().numpy().view(np.int32), y2.cpu().numpy().view(np.int32))
+    m.close()
 
 
 def test_q8k_in_cuda_graph():
