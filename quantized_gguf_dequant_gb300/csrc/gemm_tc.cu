@@ -29,6 +29,18 @@
 // accumulate into two 256-column TMEM accumulators (all 512 columns).
 // Tiles are spread over a persistent grid.
 //
+// Three rings of their own depth.  A stage's X is needed from its copy to
+// its MMAs, its raw weight bytes from their copy until the dequant warps
+// have written the stage's B, its bf16 B from the dequantisation to the
+// MMAs.  One ring of (X, raw, B) stages would hold every buffer for the copy
+// latency plus the dequantisation plus the MMAs, and three such stages are
+// all that shared memory takes; separate rings hold each buffer only for its
+// own part (X: copy + MMAs; raw: copy + dequantisation; B: dequantisation +
+// MMAs), so the X ring can be deeper, the raw bytes run ahead of the X
+// copies and the dequantisation overlaps the MMAs of the previous stage.  The producer
+// feeds the X and raw rings as two independent streams (polling both
+// rings' free slots), so neither waits behind the other.
+//
 // Warp roles (576 threads):
 //   warp 0        TMA producer (one lane)
 //   warp 1        TMEM allocation and MMA issue (one lane)
@@ -60,6 +72,8 @@ constexpr int kBBytes = kRows * 128;  // 32768
 constexpr int kNibBytes = kRows * 32; // 8192
 constexpr int kHdrBytes = kRows * 16; // 4096
 constexpr int kHdrSlots = 2;
+constexpr int kEpiStage = 32 * 32 * 4;               // one 32-token x 32-column fp32 chunk
+constexpr size_t kEpiStageBytes = 8 * kEpiStage;     // one per epilogue warp
 constexpr int kThreads = 576;
 constexpr int kEpiWarp0 = 2;
 constexpr int kDequantWarp0 = 10;
@@ -67,7 +81,7 @@ constexpr int kMaxKSplit = 16;
 
 // Token tiles of 256 (two MMAs of M = 128 per K step into both 256-column
 // TMEM accumulators) or of 128 (one MMA, one accumulator) for problems whose
-// 256-token tiles would not fill the SMs.  Three stages either way.
+// 256-token tiles would not fill the SMs.
 // Weight bytes staged per 64-weight K step and 256 rows: Q4_K the chunk's 32
 // nibble bytes (its 16-byte header separately, once per super-block); Q8_0
 // the chunk's two 34-byte blocks, fetched as the 80-byte window that starts
@@ -75,18 +89,21 @@ constexpr int kMaxKSplit = 16;
 constexpr int kQ80Window = 80;
 template <int FMT> constexpr int kRawBytes = FMT == QMM_Q4_K ? kNibBytes : kRows * kQ80Window;
 
-template <int TOK, int FMT>
+// Ring depths: NX stages of X, NB of bf16 B, NR of raw weight bytes.
+template <int TOK, int FMT, int NX, int NB, int NR>
 struct TileCfg {
     static constexpr int kTok = TOK;
     static constexpr int kHalves = TOK / 128;           // MMAs of M = 128 per K step
-    // Q8_0's larger windows leave room for two 256-token stages only
-    static constexpr int kStages = (FMT == QMM_Q8_0 && TOK == 256) ? 2 : 3;
     static constexpr int kABytes = TOK * 128;
+    static constexpr int kRaw = kRawBytes<FMT>;
+    static constexpr int kHdr = FMT == QMM_Q4_K ? kHdrSlots : 0;
     static constexpr uint32_t kTmemCols = uint32_t(kHalves) * 256;
-    static constexpr size_t kStageBytes = size_t(kABytes) + kBBytes + kRawBytes<FMT>;
-    static constexpr size_t kSmemBytes =
-        1024 /* alignment slack */ + size_t(kStages) * kStageBytes + size_t(kHdrSlots) * kHdrBytes + 256;
+    static constexpr int kBars = 2 * NX + 2 * NB + 2 * NR + 2 * kHdrSlots + 3;
+    static constexpr size_t kSmemBytes = 1024 /* alignment slack */ + size_t(NX) * kABytes +
+                                         size_t(NB) * kBBytes + size_t(NR) * kRaw +
+                                         size_t(kHdr) * kHdrBytes + kEpiStageBytes + size_t(kBars) * 8;
     static_assert(kSmemBytes <= 232448, "shared memory per block");
+    static_assert(NR <= 8, "two header slots: the raw stream runs at most NR stages ahead");
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulate, A and B
@@ -99,6 +116,8 @@ struct GemmParams {
     CUtensorMap tm_x;                   // X [M][K] bf16, box 64 x 256, 128-byte swizzle
     CUtensorMap tm_hdr[kGemmMaxGroup];  // weight bytes [N_i][row_bytes] u8, box 16 x 256
     CUtensorMap tm_nib[kGemmMaxGroup];  // weight bytes, box 32 x 256 (Q8_0: 80 x 256)
+    CUtensorMap tm_y[kGemmMaxGroup];    // Y_i [M][N_i] fp32, box 32 x 32, 128-byte swizzle
+    CUtensorMap tm_ws;                  // partials [ksplit][M][Ntot] fp32, box 32 x 32 x 1
     float *y[kGemmMaxGroup];            // [M][N_i]
     int n_rows[kGemmMaxGroup];          // N_i
     int rt_end[kGemmMaxGroup];          // cumulative 256-row tiles
@@ -112,6 +131,7 @@ struct GemmParams {
     int full_units;      // tiles [0, full_units) run whole, one unit each
     int units;           // full_units + (tiles - full_units) * ksplit
     int vec_store;       // Y rows 16-byte aligned: store float4
+    int tma_store;       // tm_y (and tm_ws when split) are valid: bulk-store whole chunks
     unsigned *status;
 };
 
@@ -164,27 +184,31 @@ __device__ __forceinline__ void dequant4_q8(uint32_t v, float d, uint32_t &p0, u
     p1 = cvt_bf16x2(f1.x, f1.y);
 }
 
-template <int TOK, int FMT>
+template <int TOK, int FMT, int NX, int NB, int NR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_constant__ GemmParams P)
 {
-    using C = TileCfg<TOK, FMT>;
-    constexpr int kRaw = kRawBytes<FMT>;
-    constexpr int kTok = C::kTok, kStages = C::kStages, kABytes = C::kABytes;
+    using C = TileCfg<TOK, FMT, NX, NB, NR>;
+    constexpr int kRaw = C::kRaw, kHS = kHdrSlots;
+    constexpr int kTok = C::kTok, kABytes = C::kABytes;
     constexpr uint32_t kTmemCols = C::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = (smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - smem_u32(smem_raw));
-    uint8_t *sA = base;                                  // [kStages][TOK x 128 B]
-    uint8_t *sB = sA + kStages * kABytes;                // [kStages][32 KB]
-    uint8_t *sNib = sB + kStages * kBBytes;              // [kStages][kRaw]
-    uint8_t *sHdr = sNib + kStages * kRaw;               // [kHdrSlots][4 KB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sHdr + kHdrSlots * kHdrBytes);
-    uint64_t *full = bars;                  // A + nibbles landed      (tx)
-    uint64_t *bready = full + kStages;      // B written               (8 dequant warps)
-    uint64_t *empty = bready + kStages;     // MMAs of the slot done   (commit)
-    uint64_t *hfull = empty + kStages;      // headers landed          (tx)
-    uint64_t *hempty = hfull + kHdrSlots;   // headers consumed        (8 dequant warps)
-    uint64_t *accfull = hempty + kHdrSlots; // accumulators complete   (commit)
+    uint8_t *sA = base;                                  // [NX][TOK x 128 B]
+    uint8_t *sB = sA + NX * kABytes;                     // [NB][32 KB]
+    uint8_t *sRaw = sB + NB * kBBytes;                   // [NR][kRaw]
+    uint8_t *sHdr = sRaw + NR * kRaw;                    // [kHdr][4 KB]
+    uint8_t *sEpi = sHdr + C::kHdr * kHdrBytes;          // [8 epilogue warps][4 KB], 1024-aligned
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sEpi + kEpiStageBytes);
+    uint64_t *xfull = bars;                 // X landed                (tx)
+    uint64_t *xempty = xfull + NX;          // MMAs of the X slot done (commit)
+    uint64_t *bready = xempty + NX;         // B written               (8 dequant warps)
+    uint64_t *bempty = bready + NB;         // MMAs of the B slot done (commit)
+    uint64_t *rfull = bempty + NB;          // raw bytes landed        (tx)
+    uint64_t *rempty = rfull + NR;          // raw bytes used          (8 dequant warps)
+    uint64_t *hfull = rempty + NR;          // headers landed          (tx)
+    uint64_t *hempty = hfull + kHS;         // headers used            (8 dequant warps)
+    uint64_t *accfull = hempty + kHS;       // accumulators complete   (commit)
     uint64_t *accempty = accfull + 1;       // accumulators drained    (8 epilogue warps)
     uint64_t *drain = accempty + 1;         // final MMA drain         (commit)
     __shared__ uint32_t tmem_base_sh;
@@ -210,12 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&bready[s], 8);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < NX; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], 1);
         }
-        for (int h = 0; h < kHdrSlots; ++h) {
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&bready[s], 8);
+            mbar_init(&bempty[s], 1);
+        }
+        for (int s = 0; s < NR; ++s) {
+            mbar_init(&rfull[s], 1);
+            mbar_init(&rempty[s], 8);
+        }
+        for (int h = 0; h < kHS; ++h) {
             mbar_init(&hfull[h], 1);
             mbar_init(&hempty[h], 8);
         }
@@ -242,51 +273,84 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int it = 0, hit = 0;  // stages and super-blocks issued
-            for (int un = blockIdx.x; un < P.units && !abort_flag; un += gridDim.x) {
+            // Two cursors over this CTA's stages (units blockIdx.x, +grid, ...,
+            // each a run of 64-wide K steps): the X stream and the raw stream.
+            struct Cursor {
+                int un, ks, ks_end, tok0, mi, row0;
+            };
+            auto seek = [&](Cursor &c, int un) {
+                c.un = un;
+                if (un >= P.units)
+                    return;
                 int t, kslice, sb0, sb_u;
                 unit_of(un, t, kslice, sb0, sb_u);
-                int mi, row0;
-                matrix_row_tile(P, t / P.tok_tiles, mi, row0);
-                const int tok0 = (t % P.tok_tiles) * kTok;
-                for (int ks = 4 * sb0; ks < 4 * (sb0 + sb_u); ++ks, ++it) {
-                    const int s = it % kStages, u = it / kStages;
-                    const int sb = ks >> 2, c = ks & 3;
-                    if constexpr (FMT == QMM_Q8_0) {
-                        // the chunk's blocks sit at 272 sb + 68 c of the row
-                        if (u >= 1 &&
-                            !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
-                            break;
-                        mbar_arrive_expect_tx(&full[s], kABytes + kRaw);
-                        tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
-                        tma_2d(sNib + s * kRaw, &P.tm_nib[mi], 272 * sb + ((68 * c) & ~15), row0,
-                               &full[s]);
-                        continue;
-                    }
-                    if (c == 0) {
-                        const int h = hit % kHdrSlots, hu = hit / kHdrSlots;
-                        if (hu >= 1 &&
-                            !wait_phase(&hempty[h], unsigned(hu - 1) & 1u, &abort_flag, P.status))
-                            break;
-                        mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
-                        tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr[mi], sb * 144, row0, &hfull[h]);
-                        ++hit;
-                    }
-                    if (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))
-                        break;
-                    mbar_arrive_expect_tx(&full[s], kABytes + kRaw);
-                    tma_2d(sA + s * kABytes, &P.tm_x, ks * 64, tok0, &full[s]);
-                    tma_2d(sNib + s * kRaw, &P.tm_nib[mi], sb * 144 + 16 + 32 * c, row0, &full[s]);
+                matrix_row_tile(P, t / P.tok_tiles, c.mi, c.row0);
+                c.tok0 = (t % P.tok_tiles) * kTok;
+                c.ks = 4 * sb0;
+                c.ks_end = 4 * (sb0 + sb_u);
+            };
+            auto step = [&](Cursor &c) {
+                if (++c.ks == c.ks_end)
+                    seek(c, c.un + int(gridDim.x));
+            };
+            Cursor cx, cr;
+            seek(cx, blockIdx.x);
+            seek(cr, blockIdx.x);
+            int ix = 0, ir = 0, hit = 0;  // stages / super-blocks issued per stream
+            long long idle0 = clock64();
+            while (!abort_flag && (cx.un < P.units || cr.un < P.units)) {
+                bool moved = false;
+                // X of stage ix into slot ix % NX, once the MMAs of its previous
+                // stage there are done.
+                if (cx.un < P.units &&
+                    (ix < NX || mbar_test_wait(&xempty[ix % NX], unsigned(ix / NX - 1) & 1u))) {
+                    const int s = ix % NX;
+                    mbar_arrive_expect_tx(&xfull[s], kABytes);
+                    tma_2d(sA + s * kABytes, &P.tm_x, cx.ks * 64, cx.tok0, &xfull[s]);
+                    ++ix;
+                    step(cx);
+                    moved = true;
                 }
-                if (abort_flag)
-                    break;
+                // Raw bytes of stage ir (and, at a super-block's first chunk,
+                // its headers), once the dequant warps hold the previous ones.
+                if (cr.un < P.units) {
+                    const int s = ir % NR, sb = cr.ks >> 2, c = cr.ks & 3;
+                    const bool with_hdr = FMT == QMM_Q4_K && c == 0;
+                    const int h = hit % kHS;
+                    if ((ir < NR || mbar_test_wait(&rempty[s], unsigned(ir / NR - 1) & 1u)) &&
+                        (!with_hdr || hit < kHS ||
+                         mbar_test_wait(&hempty[h], unsigned(hit / kHS - 1) & 1u))) {
+                        if (with_hdr) {
+                            mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
+                            tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr[cr.mi], sb * 144, cr.row0, &hfull[h]);
+                            ++hit;
+                        }
+                        // Q8_0: the chunk's blocks sit at 272 sb + 68 c of the row
+                        const int xoff = FMT == QMM_Q8_0 ? 272 * sb + ((68 * c) & ~15) : sb * 144 + 16 + 32 * c;
+                        mbar_arrive_expect_tx(&rfull[s], kRaw);
+                        tma_2d(sRaw + s * kRaw, &P.tm_nib[cr.mi], xoff, cr.row0, &rfull[s]);
+                        ++ir;
+                        step(cr);
+                        moved = true;
+                    }
+                }
+                if (moved) {
+                    idle0 = clock64();
+                } else if (clock64() - idle0 > kWaitBudgetCycles) {
+                    atomicOr(P.status, kStatusTimeoutBit);
+                    abort_flag = 1;
+                } else {
+                    __nanosleep(32);
+                }
             }
             // Copies still in flight must land before the CTA exits: wait for
             // the last phase of every slot that was used (bounded).
-            for (int s = 0; s < kStages && s < it; ++s)
-                mbar_wait_bounded(&full[s], unsigned((it - 1 - s) / kStages) & 1u, 200000000ll);
-            for (int h = 0; h < kHdrSlots && h < hit; ++h)
-                mbar_wait_bounded(&hfull[h], unsigned((hit - 1 - h) / kHdrSlots) & 1u, 200000000ll);
+            for (int s = 0; s < NX && s < ix; ++s)
+                mbar_wait_bounded(&xfull[s], unsigned((ix - 1 - s) / NX) & 1u, 200000000ll);
+            for (int s = 0; s < NR && s < ir; ++s)
+                mbar_wait_bounded(&rfull[s], unsigned((ir - 1 - s) / NR) & 1u, 200000000ll);
+            for (int h = 0; h < kHS && h < hit; ++h)
+                mbar_wait_bounded(&hfull[h], unsigned((hit - 1 - h) / kHS) & 1u, 200000000ll);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
@@ -300,14 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 int t_, ksl_, sb0_, sb_u;
                 unit_of(un, t_, ksl_, sb0_, sb_u);
                 for (int ks = 0; ks < 4 * sb_u; ++ks, ++it) {
-                    const int s = it % kStages, u = it / kStages;
-                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
-                        !wait_phase(&bready[s], unsigned(u) & 1u, &abort_flag, P.status)) {
+                    const int sx = it % NX, sbf = it % NB;
+                    if (!wait_phase(&xfull[sx], unsigned(it / NX) & 1u, &abort_flag, P.status) ||
+                        !wait_phase(&bready[sbf], unsigned(it / NB) & 1u, &abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
+                    const uint32_t a0 = smem_u32(sA + sx * kABytes), b0 = smem_u32(sB + sbf * kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t bd = sw128_desc(b0 + 32 * kk);
@@ -317,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                             mma_bf16(tmem + uint32_t(h * kRows), sw128_desc(a0 + h * 16384 + 32 * kk),
                                      bd, acc);
                     }
-                    mma_commit(&empty[s]);
+                    mma_commit(&xempty[sx]);
+                    mma_commit(&bempty[sbf]);
                 }
                 if (!ok)
                     break;
@@ -329,11 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         }
     } else if (warp < kDequantWarp0) {
         // ---------------------------------------------------------- epilogue
+        // A warp's 32 tokens x 32 columns per chunk: TMEM -> registers -> its
+        // staging buffer (row = token, 128-byte swizzle) -> one bulk tensor
+        // store into Y (or the partials).  The accumulators are free once the
+        // last chunk is in registers; the stores complete in the background.
+        // Chunks a store cannot take (Y not 16-byte aligned, a partial
+        // 32-column piece) are written by the threads themselves.
         const int quarter = warp & 3;
         const int eh = (warp - kEpiWarp0) >> 2;  // 256-token tiles: token half; 128: column half
         const int tok_in_tile = (C::kHalves == 2 ? eh * 128 : 0) + quarter * 32 + lane;
         constexpr int kCols = C::kHalves == 2 ? kRows : kRows / 2;  // columns this warp drains
         const int col0 = C::kHalves == 2 ? 0 : eh * (kRows / 2);
+        uint8_t *stage = sEpi + (warp - kEpiWarp0) * kEpiStage;
+        uint8_t *srow = stage + lane * 128;
+        const uint32_t sw = uint32_t(lane & 7);
+        bool pending = false;  // lane 0 has a bulk store that may still read the buffer
         int lt = 0;
         for (int un = blockIdx.x; un < P.units; un += gridDim.x, ++lt) {
             if (!wait_phase(accfull, unsigned(lt) & 1u, &abort_flag, P.status))
@@ -343,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             unit_of(un, t, kslice, sb0_, sb_u_);
             const bool split = un >= P.full_units && P.ksplit > 1;
             const int tok = (t % P.tok_tiles) * kTok + tok_in_tile;
+            const int tok_w = tok - lane;  // the warp's first token
             int mi, row0;
             matrix_row_tile(P, t / P.tok_tiles, mi, row0);
             const int Nm = P.n_rows[mi];
@@ -360,7 +436,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 tmem_ld16(taddr + uint32_t(ch * 32 + 16), *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                 tmem_ld_wait();
                 const int n0 = row0 + col0 + ch * 32;
-                if (tok < P.M) {
+                if (P.tma_store && n0 + 32 <= Nm) {
+                    if (tok_w >= P.M)
+                        continue;
+                    if (pending && lane == 0)
+                        bulk_wait_read();  // the previous chunk has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(srow + ((uint32_t(j) ^ sw) << 4)) =
+                            make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    fence_proxy_async_smem();  // the bulk store reads the buffer through the async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (split)
+                            tma_store_3d(&P.tm_ws, stage, P.col_off[mi] + n0, tok_w, kslice);
+                        else
+                            tma_store_2d(&P.tm_y[mi], stage, n0, tok_w);
+                        bulk_commit();
+                        pending = true;
+                    }
+                } else if (tok < P.M) {
                     if (P.vec_store && n0 + 32 <= Nm) {
                         float4 *dst = reinterpret_cast<float4 *>(yrow + n0);
 #pragma unroll
@@ -381,8 +477,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             if (lane == 0)
                 mbar_arrive(accempty);  // the accumulators are free for the next unit
         }
+        if (pending && lane == 0)
+            bulk_wait_all();  // the stores are complete before the CTA exits
     } else {
         // ---------------------------------------------------------- dequantisation
+        // Per stage: load the raw bytes, wait for the B slot (the MMAs of its
+        // previous stage), write the bf16 weights, then free the B slot's
+        // contents to the MMA and the raw slot to the producer.  The raw slot
+        // is freed only after the stores that use its bytes, so the order of
+        // the reads and the release rests on a data dependency, not on how
+        // the loads are scheduled.
         const int r = (warp - kDequantWarp0) * 32 + lane;  // weight row within the tile
         const uint32_t swz = uint32_t(r & 7);
         int it = 0, hit = 0;
@@ -392,23 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 int t_, ksl_, sb0, sb_u;
                 unit_of(un, t_, ksl_, sb0, sb_u);
                 for (int ks = 4 * sb0; ks < 4 * (sb0 + sb_u); ++ks, ++it) {
-                    const int s = it % kStages, u = it / kStages;
-                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
-                        (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+                    const int s = it % NR, sbf = it % NB;
+                    if (!wait_phase(&rfull[s], unsigned(it / NR) & 1u, &abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
                     // this row's two blocks: [d0][32 q][d1][32 q] from byte
                     // (68 c) mod 16 of its window -- 17 aligned words
                     const uint32_t *wd = reinterpret_cast<const uint32_t *>(
-                        sNib + s * kRaw + r * kQ80Window + ((68 * (ks & 3)) & 15));
+                        sRaw + s * kRaw + r * kQ80Window + ((68 * (ks & 3)) & 15));
                     uint32_t W[17];
 #pragma unroll
                     for (int i = 0; i < 17; ++i)
                         W[i] = wd[i];
+                    if (it >= NB &&
+                        !wait_phase(&bempty[sbf], unsigned(it / NB - 1) & 1u, &abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();  // the slot's MMA reads (async proxy) before these writes
                     const float d0 = __half2float(__ushort_as_half((unsigned short)(W[0] & 0xffffu)));
                     const float d1 = __half2float(__ushort_as_half((unsigned short)(W[8] >> 16)));
-                    uint8_t *brow = sB + s * kBBytes + r * 128;
+                    uint8_t *brow = sB + sbf * kBBytes + r * 128;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {  // 16-byte chunk j: weights 8j .. 8j+7
                         uint32_t v0, v1;
@@ -427,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     }
                     fence_proxy_async_smem();  // the MMA reads B through the async proxy
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&bready[s]);
+                    if (lane == 0) {
+                        mbar_arrive(&bready[sbf]);
+                        mbar_arrive(&rempty[s]);  // B was computed from them: the raw bytes are free
+                    }
                 }
             }
         }
@@ -436,33 +547,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             int t_, ksl_, sb0, sb_u;
             unit_of(un, t_, ksl_, sb0, sb_u);
             for (int sb = sb0; sb < sb0 + sb_u && ok; ++sb, ++hit) {
-                const int h = hit % kHdrSlots;
-                if (!wait_phase(&hfull[h], unsigned(hit / kHdrSlots) & 1u, &abort_flag, P.status)) {
+                const int h = hit % kHS;
+                if (!wait_phase(&hfull[h], unsigned(hit / kHS) & 1u, &abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
                 const uint4 hd = *reinterpret_cast<const uint4 *>(sHdr + h * kHdrBytes + r * 16);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&hempty[h]);  // the header now lives in registers
                 const float2 dd = half2_bits_to_float2(hd.x);
                 for (int c = 0; c < 4; ++c, ++it) {
-                    const int s = it % kStages, u = it / kStages;
-                    if (!wait_phase(&full[s], unsigned(u) & 1u, &abort_flag, P.status) ||
-                        (u >= 1 && !wait_phase(&empty[s], unsigned(u - 1) & 1u, &abort_flag, P.status))) {
+                    const int s = it % NR, sbf = it % NB;
+                    if (!wait_phase(&rfull[s], unsigned(it / NR) & 1u, &abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
-                    const uint8_t *nib = sNib + s * kRaw + r * 32;
+                    const uint8_t *nib = sRaw + s * kRaw + r * 32;
                     const uint4 n0 = *reinterpret_cast<const uint4 *>(nib);
                     const uint4 n1 = *reinterpret_cast<const uint4 *>(nib + 16);
+                    if (it >= NB &&
+                        !wait_phase(&bempty[sbf], unsigned(it / NB - 1) & 1u, &abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();  // the slot's MMA reads (async proxy) before these writes
                     uint32_t sc_lo, m_lo, sc_hi, m_hi;
                     scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
                     scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
                     const float a_lo = dd.x * float(sc_lo), b_lo = dd.y * float(m_lo);
                     const float a_hi16 = dd.x * float(sc_hi) * 0.0625f, b_hi = dd.y * float(m_hi);
                     const uint32_t w[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-                    uint8_t *brow = sB + s * kBBytes + r * 128;
+                    uint8_t *brow = sB + sbf * kBBytes + r * 128;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {  // chunks j (low nibbles) and j + 4 (high)
                         uint32_t p[4], q[4];
@@ -477,8 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                     }
                     fence_proxy_async_smem();  // the MMA reads B through the async proxy
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&bready[s]);
+                    if (lane == 0) {
+                        mbar_arrive(&bready[sbf]);
+                        // B was computed from the raw bytes (and, by the last
+                        // chunk, from every header word): both slots are free
+                        mbar_arrive(&rempty[s]);
+                        if (c == 3)
+                            mbar_arrive(&hempty[h]);
+                    }
                 }
             }
         }
@@ -561,13 +680,43 @@ __global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
     }
 }
 
+// The kernel instance and its shared memory for a token tile and format.
+// Ring depths (NX, NB, NR) fill the 227 KB of shared memory beside the
+// epilogue's 32 KB of staging; QMM_GEMM_RINGS selects one of the
+// alternatives kept for Q4_K (1 or 2) in place of the default (0).
+using GemmKernel = decltype(&gemm_q4k_kernel<256, QMM_Q4_K, 3, 2, 3>);
+struct GemmInstance {
+    GemmKernel fn;
+    size_t smem;
+};
+
+template <int TOK, int FMT, int NX, int NB, int NR>
+GemmInstance instance()
+{
+    return {gemm_q4k_kernel<TOK, FMT, NX, NB, NR>, TileCfg<TOK, FMT, NX, NB, NR>::kSmemBytes};
+}
+
+GemmInstance pick_gemm(int tok, int fmt)
+{
+    int v = 0;
+    if (const char *e = getenv("QMM_GEMM_RINGS"))
+        v = atoi(e);
+    if (fmt == QMM_Q8_0)
+        return tok == 128 ? instance<128, QMM_Q8_0, 4, 2, 3>() : instance<256, QMM_Q8_0, 2, 2, 3>();
+    if (tok == 128)
+        return v == 1   ? instance<128, QMM_Q4_K, 5, 2, 4>()
+               : v == 2 ? instance<128, QMM_Q4_K, 6, 2, 3>()
+                        : instance<128, QMM_Q4_K, 4, 3, 3>();
+    return v == 1   ? instance<256, QMM_Q4_K, 2, 3, 3>()
+           : v == 2 ? instance<256, QMM_Q4_K, 2, 2, 6>()
+                    : instance<256, QMM_Q4_K, 3, 2, 3>();
+}
+
 } // namespace
 
 size_t gemm_q4k_smem(int tok, int fmt)
 {
-    if (fmt == QMM_Q8_0)
-        return tok == 128 ? TileCfg<128, QMM_Q8_0>::kSmemBytes : TileCfg<256, QMM_Q8_0>::kSmemBytes;
-    return tok == 128 ? TileCfg<128, QMM_Q4_K>::kSmemBytes : TileCfg<256, QMM_Q4_K>::kSmemBytes;
+    return pick_gemm(tok, fmt).smem;
 }
 
 int gemm_q4k_tiles(int64_t M, int64_t N, int tok)
@@ -658,11 +807,22 @@ cudaError_t launch_gemm_q4k(const GemmArgs &a, int sm_count, cudaStream_t s)
     P.units = P.full_units + (P.tiles - P.full_units) * P.ksplit;
     P.vec_store = vec ? 1 : 0;
     P.status = a.status;
-    auto kern = a.fmt == QMM_Q8_0 ? (a.tok == 128 ? gemm_q4k_kernel<128, QMM_Q8_0>
-                                                   : gemm_q4k_kernel<256, QMM_Q8_0>)
-                                  : (a.tok == 128 ? gemm_q4k_kernel<128, QMM_Q4_K>
-                                                   : gemm_q4k_kernel<256, QMM_Q4_K>);
-    const size_t smem = gemm_q4k_smem(a.tok, a.fmt);
+    // Bulk-store epilogue: every Y_i (and the partials) as a tensor of fp32
+    // rows, 32 x 32 boxes with the 128-byte swizzle of the staging buffers.
+    bool tma = vec && getenv("QMM_GEMM_THREAD_STORES") == nullptr;
+    for (int i = 0; i < a.nmat && tma; ++i)
+        tma = encode_tmap_2d(&P.tm_y[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.y[i], uint64_t(a.N[i]),
+                             uint64_t(a.M), uint64_t(a.N[i]) * 4, 32u, 32u,
+                             CU_TENSOR_MAP_SWIZZLE_128B) == 0;
+    if (tma && a.ksplit > 1)
+        tma = encode_tmap_3d(&P.tm_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.ws, uint64_t(P.Ntot),
+                             uint64_t(a.M), uint64_t(a.ksplit), uint64_t(P.Ntot) * 4,
+                             uint64_t(a.M) * uint64_t(P.Ntot) * 4, 32u, 32u, 1u,
+                             CU_TENSOR_MAP_SWIZZLE_128B) == 0;
+    P.tma_store = tma ? 1 : 0;
+    const GemmInstance gi = pick_gemm(a.tok, a.fmt);
+    const auto kern = gi.fn;
+    const size_t smem = gi.smem;
     cudaError_t e = func_smem(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess)
         return e;

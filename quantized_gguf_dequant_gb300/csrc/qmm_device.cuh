@@ -63,6 +63,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     return ok != 0;
 }
 
+// Non-blocking probe: has phase `parity` of the mbarrier completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait with a suspend-time hint: the thread may sleep (up to the hint,
 // in ns) until the phase completes instead of spinning.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned parity)

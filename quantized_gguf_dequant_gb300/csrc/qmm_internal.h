@@ -259,8 +259,10 @@ cudaError_t launch_gemv_tcb(const TcbArgs &a, const TcbPlan &p, cudaStream_t s);
 // CUtensorMapSwizzle); 0 on success.
 int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uint64_t dim1,
                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, int swizzle);
-// The 3-D column view of a Q4_K matrix (tmap.cu) with boxes of one 16-row
-// tile x ks super-blocks; 0 on success.
+// The same for a 3-D tensor (dims innermost first, strides of dims 1 and 2).
+int encode_tmap_3d(void *out128, int dtype, const void *base, uint64_t dim0, uint64_t dim1,
+                   uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                   uint32_t box1, uint32_t box2, int swizzle);
 // 3-D column view (super-block bytes as u64 words, row, super-block) with
 // boxes of 16 rows x ks super-blocks; sb_bytes 144 (Q4_K) or 176 (Q5_K).
 int make_column_map(void *out128, const void *w, int64_t N, int64_t row_bytes, int ks,

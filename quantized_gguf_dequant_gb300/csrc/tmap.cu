@@ -43,6 +43,24 @@ int encode_tmap_2d(void *out128, int dtype, const void *base, uint64_t dim0, uin
     return r == CUDA_SUCCESS ? 0 : -2;
 }
 
+int encode_tmap_3d(void *out128, int dtype, const void *base, uint64_t dim0, uint64_t dim1,
+                   uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0,
+                   uint32_t box1, uint32_t box2, int swizzle)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+    if (!encode)
+        return -1;
+    const cuuint64_t dims[3] = {cuuint64_t(dim0), cuuint64_t(dim1), cuuint64_t(dim2)};
+    const cuuint64_t strides[2] = {cuuint64_t(stride1_bytes), cuuint64_t(stride2_bytes)};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = encode(reinterpret_cast<CUtensorMap *>(out128), CUtensorMapDataType(dtype), 3,
+                        const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CUtensorMapSwizzle(swizzle),
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -2;
+}
+
 // A Q4_K (Q5_K) matrix of N rows seen as a 3-D tensor of uint64 words: (18
 // (22) words = one 144 (176)-byte super-block, N rows, NB super-blocks),
 // strides row_bytes and the super-block size.  A box (words, 16, ks) is then

@@ -262,3 +262,26 @@ def test_gemm_tail_wave_split():
     y_ref, c = oracle.gemm_bf16(w, N, K, Xb, rows=rows, nthreads=NTHREADS)
     assert_close_to_oracle(Y1[:, rows], y_ref, c, TIGHT, "tail split")
     m.close()
+
+
+@pytest.mark.parametrize("fmt", [12, 8])
+@pytest.mark.parametrize("ksplit", [None, 4])
+@pytest.mark.parametrize("M,N", [(300, 1024), (512, 300)])
+def test_gemm_bulk_store_epilogue_matches_thread_stores(monkeypatch, fmt, ksplit, M, N):
+    """The epilogue's bulk tensor stores (32 x 32 chunks through shared
+    memory; ragged token tiles clipped by the tensor map, a ragged 32-column
+    piece left to the threads) write the same bits as per-thread stores,
+    into Y and, with K split, into the partials."""
+    if ksplit:
+        monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
+    K = 2048
+    w = synth.matrix(fmt, N, K, M + N + fmt)
+    Xb = synth.activations_bf16(M, K, 7)
+    m = q.Matrix(fmt, N, K, to_dev(w))
+    y_bulk = _run(m, Xb, M)
+    monkeypatch.setenv("QMM_GEMM_THREAD_STORES", "1")
+    y_thr = _run(m, Xb, M)
+    assert np.all(np.isfinite(y_bulk))
+    assert np.array_equal(y_bulk.view(np.uint32), y_thr.view(np.uint32))
+    assert m.status() == 0
+    m.close()
