@@ -1262,12 +1262,11 @@ static qmm_status gemm_common(const qmm_t *hs, int n, const uint16_t *X_bf16, in
     }
     a.nmat = n;
     // 256-token tiles reuse each dequantised weight twice as often as 128-token
-    // tiles.  Measured on the Llama shapes, 128-token tiles win only when the
-    // 256-token tiles are few (at most 64) and K is short (<= 4096: the q/k/v
-    // group and o at 512 tokens); elsewhere 256 is as fast or faster (the
-    // K-split of the tail wave recovers the parallelism).  QMM_GEMM_TOK
-    // forces either.
-    a.tok = (tiles256 <= 64 && m->K <= 4096) ? 128 : 256;
+    // tiles; measured on the Llama shapes at 512 and 2048 tokens they are as
+    // fast or faster for every matrix (the K split of the tail wave recovers
+    // the parallelism of few tiles).  At most 128 tokens take 128-token tiles
+    // (a 256-token tile would be half padding).  QMM_GEMM_TOK forces either.
+    a.tok = M <= 128 ? 128 : 256;
     if (const char *e = getenv("QMM_GEMM_TOK"))
         if (atoi(e) == 128 || atoi(e) == 256)
             a.tok = atoi(e);
