@@ -461,16 +461,43 @@ def small_matrix_extra(pk):
         torch.cuda.synchronize()
         if i >= 3:
             lat.append(e0.elapsed_time(e1) * 1e3)
+    # The same harness around a one-element add (the floor of any kernel launch
+    # between two events after the flush)
+    one = torch.zeros(1, device="cuda")
+    floor = []
+    for i in range(24):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one.add_(1.0)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            floor.append(e0.elapsed_time(e1) * 1e3)
+    # In a graph: (flush + call) x 20 minus flush x 20, per call -- the call's
+    # added time with L2 flushed, without the events' own resolution; the same
+    # for a 590 KB device copy.
+    src = torch.empty(wbytes // 4, dtype=torch.float32, device="cuda")
+    dst = torch.empty_like(src)
+    t_fl, _ = time_graph(lambda: [flush.fill_(1.0) for _ in range(20)], 3, 3, 1)
+    t_gv, _ = time_graph(lambda: [(flush.fill_(1.0), q.gemv(mats[0].h, x, ys[0])) for _ in range(20)], 3, 3, 1)
+    t_cp, _ = time_graph(lambda: [(flush.fill_(1.0), dst.copy_(src)) for _ in range(20)], 3, 3, 1)
     ms, _ = time_graph(lambda: [q.gemv(m.h, x, ys[i]) for i, m in enumerate(mats)], 5, 3, 1)
     tput = copies * (wbytes + 4 * K + 4 * N) / (ms * 1e-3) / 1e9
     for m in mats:
         m.close()
     del flush
     return {"latency_us_median": statistics.median(lat), "latency_us_min": min(lat),
+            "one_element_kernel_latency_us_median": statistics.median(floor),
+            "graph_added_us_per_call": (t_gv - t_fl) * 1e3 / 20,
+            "graph_added_us_per_590kb_copy": (t_cp - t_fl) * 1e3 / 20,
             "rotating_gbs": tput, "rotating_frac_of_peak": tput / pk["hbm_gbs"],
             "note": "qmm_gemv on a 1024 x 1024 Q4_K matrix (589,824 B): latency of one call with "
-                    "L2 flushed (CUDA events around the call), and 512 distinct copies in one CUDA "
-                    "graph (weights > L2)"}
+                    "L2 flushed (CUDA events around the call; the same harness around a one-element "
+                    "add kernel gives its floor), the time one call adds to a graph of flushes, "
+                    "beside a 590 KB device copy, and 512 distinct copies in one CUDA graph "
+                    "(weights > L2)"}
 
 
 def launches_of(fn):
