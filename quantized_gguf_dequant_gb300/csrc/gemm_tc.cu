@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sb_n = P.K / 256;
     // Unit un: a whole tile (un < full_units) or K slice `kslice` of one of
-    // the tail tiles; sb_u super-blocks from sb0 each.
+    // the tail tiles: super-blocks [kslice * n / ks, (kslice + 1) * n / ks)
+    // of the n = K / 256 (slices differ by at most one super-block).
     auto unit_of = [&](int un, int &t, int &kslice, int &sb0, int &sb_u) {
         if (un < P.full_units) {
             t = un;
@@ -228,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             const int v = un - P.full_units;
             t = P.full_units + v / P.ksplit;
             kslice = v - (v / P.ksplit) * P.ksplit;
-            sb_u = sb_n / P.ksplit;
-            sb0 = kslice * sb_u;
+            sb0 = kslice * sb_n / P.ksplit;
+            sb_u = (kslice + 1) * sb_n / P.ksplit - sb0;
         }
     };
 
@@ -728,10 +729,11 @@ int gemm_q4k_tiles(int64_t M, int64_t N, int tok)
 // 3.7 us per super-block of a 256 x 256 tile and runs its units one after the
 // other (one CTA per SM).  Whole tiles fill full waves; the tiles of the last,
 // partial wave (all tiles when there are fewer than the SMs) are split in K
-// into `ksplit` slices (a divisor of K/256, at most 16), which costs writing
-// and re-reading their fp32 partials at about 5 TB/s.  The count with the
-// least estimated time wins (1 = no split).  QMM_GEMM_KSPLIT forces a value
-// (if it divides K/256); then every tile is split.
+// into `ksplit` slices (at most 16 and at most K/256; the super-blocks are
+// shared out as evenly as they go, so the longest slice takes the ceiling),
+// which costs writing and re-reading their fp32 partials at about 5 TB/s.
+// The count with the least estimated time wins (1 = no split).
+// QMM_GEMM_KSPLIT forces a value (at most K/256); then every tile is split.
 GemmSplit gemm_q4k_split(int tiles, int tok, int64_t K, int sm_count)
 {
     const int sb = int(K / 256);
@@ -740,7 +742,7 @@ GemmSplit gemm_q4k_split(int tiles, int tok, int64_t K, int sm_count)
     g.ksplit = 1;
     if (const char *e = getenv("QMM_GEMM_KSPLIT")) {
         const int f = atoi(e);
-        if (f >= 1 && f <= kMaxKSplit && sb % f == 0) {
+        if (f >= 1 && f <= kMaxKSplit && f <= sb) {
             g.ksplit = f;
             g.full = f > 1 ? 0 : tiles;
             return g;
@@ -753,10 +755,8 @@ GemmSplit gemm_q4k_split(int tiles, int tok, int64_t K, int sm_count)
     const double us_per_sb = 3.7, partial_bytes_per_us = 5.0e6, tile_bytes = double(tok) * kRows * 4;
     double best_t = 1e30;
     for (int ks = 1; ks <= kMaxKSplit && ks <= sb; ++ks) {
-        if (sb % ks != 0)
-            continue;
         const double waves = double((int64_t(tail) * ks + sm_count - 1) / sm_count);
-        double t = waves * (sb / ks) * us_per_sb;
+        double t = waves * ((sb + ks - 1) / ks) * us_per_sb;
         if (ks > 1)
             t += double(ks) * tail * tile_bytes * 2.0 / partial_bytes_per_us;
         if (t < best_t - 1e-9) {

@@ -113,7 +113,7 @@ def test_gemm_q8_0_llama_shapes_m512(N, K):
     _check(512, N, K, seed=N * 5 + K, rows=rows, fmt=q.Q8_0)
 
 
-@pytest.mark.parametrize("ksplit", [2, 4])
+@pytest.mark.parametrize("ksplit", [2, 3, 4])
 def test_gemm_q8_0_split_k(monkeypatch, ksplit):
     monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
     _check(200, 512, 2048, seed=31, fmt=q.Q8_0)
@@ -188,10 +188,12 @@ def test_gemm_refusals():
     m.close()
 
 
-@pytest.mark.parametrize("ksplit", [2, 4, 8])
+@pytest.mark.parametrize("ksplit", [2, 3, 4, 5, 7, 8])
 def test_gemm_split_k_forced(monkeypatch, ksplit):
     """K split over several CTAs, the partial products added in slice order by
-    a reduction kernel: within bounds, and repeatable bit for bit."""
+    a reduction kernel: within bounds, and repeatable bit for bit.  K = 2048
+    has 8 super-blocks, so 3, 5 and 7 slices are uneven (super-blocks
+    [k * 8 / ks, (k + 1) * 8 / ks) each)."""
     monkeypatch.setenv("QMM_GEMM_KSPLIT", str(ksplit))
     M, N, K = 300, 513, 2048
     y = _check(M, N, K, seed=ksplit)
@@ -265,7 +267,7 @@ def test_gemm_tail_wave_split():
 
 
 @pytest.mark.parametrize("fmt", [12, 8])
-@pytest.mark.parametrize("ksplit", [None, 4])
+@pytest.mark.parametrize("ksplit", [None, 3, 4])
 @pytest.mark.parametrize("M,N", [(300, 1024), (512, 300)])
 def test_gemm_bulk_store_epilogue_matches_thread_stores(monkeypatch, fmt, ksplit, M, N):
     """The epilogue's bulk tensor stores (32 x 32 chunks through shared

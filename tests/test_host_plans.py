@@ -89,7 +89,7 @@ def test_batched_plan_of_the_down_projection(plans):
 def test_prefill_split(plans):
     for g in plans["gemm_split"]:
         tiles, K, full, ks = g["tiles"], g["K"], g["full"], g["ksplit"]
-        assert 1 <= ks <= 16 and (K // 256) % ks == 0, g
+        assert 1 <= ks <= 16 and ks <= K // 256, g
         if tiles % SMS == 0:
             assert ks == 1 and full == tiles, g  # whole waves: nothing to split
         if ks > 1:
