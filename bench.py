@@ -963,6 +963,21 @@ def run_only(args, world, local):
         q8.close()
         return {"workload": f"Llama-3.1-8B Q8_0 decode, {args.layers} layers", "ms_per_step": ms,
                 "gbs": b8 * args.layers / (ms * 1e-3) / 1e9}
+    if args.only == "tall":
+        # The decode kernel's steady streaming rate: one Q4_K GEMV on a
+        # 131072 x 4096 matrix (302 MB), where a launch's fixed cost is a few
+        # percent of its time.
+        import quantized_gguf_dequant_gb300 as q
+        N, K = 131072, 4096
+        w = torch.from_numpy(synth.q4k_matrix(N, K, SEED + 900)).cuda()
+        m = q.Matrix(synth.Q4_K, N, K, w)
+        x = torch.from_numpy(synth.activations(1, K, SEED + 901)[0]).cuda()
+        y = torch.empty(N, dtype=torch.float32, device="cuda")
+        ms, _ = timer(lambda: q.gemv(m.h, x, y), args.steps, args.warmup, world)
+        nbytes = N * synth.row_bytes(synth.Q4_K, K) + 4 * K + 4 * N
+        m.close()
+        return {"workload": "Q4_K GEMV 131072 x 4096 (302 MB), one launch", "ms_per_step": ms,
+                "gbs": nbytes / (ms * 1e-3) / 1e9}
     if args.only == "ffn":
         q4 = Model(synth.Q4_K, layers=args.layers)
         out = {"workload": f"Llama-3.1-8B dense FFN decode, {args.layers} layers"}
@@ -1062,9 +1077,10 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="launch directly instead of replaying a CUDA graph (profiling)")
-    ap.add_argument("--only", choices=["prefill", "moe", "batched", "q8", "ffn"], default=None,
+    ap.add_argument("--only", choices=["prefill", "moe", "batched", "q8", "ffn", "tall"], default=None,
                     help="time just one secondary workload (profiling): the prefill GEMMs at "
-                         "--prefill-m tokens, or the OLMoE expert FFN")
+                         "--prefill-m tokens, the OLMoE expert FFN, ..., or one decode GEMV on a "
+                         "131072 x 4096 Q4_K matrix (the decode kernel's steady streaming rate)")
     ap.add_argument("--prefill-m", type=int, default=2048)
     args = ap.parse_args()
     if args.warmup < 3:
