@@ -234,6 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         }
     };
 
+    // The descriptors of the first copies and stores, fetched while the
+    // previous kernel drains.
+    if (threadIdx.x == 32 * kEpiWarp0)
+        prefetch_tmap(&P.tm_x);
+    if (threadIdx.x >= 32 * kEpiWarp0 + 1 && threadIdx.x < 32 * kEpiWarp0 + 1 + P.nmat) {
+        const int i = int(threadIdx.x) - 32 * kEpiWarp0 - 1;
+        prefetch_tmap(&P.tm_nib[i]);
+        if (FMT == QMM_Q4_K)
+            prefetch_tmap(&P.tm_hdr[i]);
+        if (P.tma_store)
+            prefetch_tmap(&P.tm_y[i]);
+    }
+    if (threadIdx.x == 32 * kEpiWarp0 + 8 && P.tma_store && P.ksplit > 1)
+        prefetch_tmap(&P.tm_ws);
     if (threadIdx.x == 0) {
         for (int s = 0; s < NX; ++s) {
             mbar_init(&xfull[s], 1);

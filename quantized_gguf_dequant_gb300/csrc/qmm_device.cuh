@@ -111,6 +111,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity
 }
 
 // ----------------------------------------------------------------- bulk copy
+// Fetch a TMA descriptor (a kernel parameter's generic address) into the
+// descriptor cache ahead of its first copy, e.g. while the previous kernel in
+// the stream drains.
+__device__ __forceinline__ void prefetch_tmap(const void *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // One-dimensional bulk copy global -> shared through the TMA engine,
 // completing `bytes` transactions on `bar`.  dst, src 16-byte aligned, bytes a
 // multiple of 16.  The L2 policy marks the (read-once) weight stream
