@@ -127,7 +127,7 @@ struct GemmParams {
     float *ws;           // split-K partials [ksplit][M][Ntot] (ksplit > 1)
     int M, K;
     int tok_tiles, tiles;
-    int ksplit;          // K slices of each tail tile (divides K / 256)
+    int ksplit;          // K slices of each tail tile (at most K / 256)
     int full_units;      // tiles [0, full_units) run whole, one unit each
     int units;           // full_units + (tiles - full_units) * ksplit
     int vec_store;       // Y rows 16-byte aligned: store float4
