@@ -1,11 +1,15 @@
 """Seeded random shapes through every compute entry point, against the oracle.
 
-Each case draws N, K (any multiple of 256), batch sizes, expert counts and
-top-k from a fixed seed, so odd row counts (not multiples of 16 or 256), odd
-super-block counts and odd batch sizes all occur; each result must meet the
-path's bound (1e-4 of sum|w x| for the fp32 paths, 1e-3 for the bf16 prefill
-against the oracle's bf16 product)."""
+Each case draws the weight format, N, K (any multiple of 256), batch sizes,
+expert counts and top-k from a fixed seed, so odd row counts (not multiples
+of 16 or 256), odd super-block counts and odd batch sizes all occur; each
+result must meet the path's bound (1e-4 of sum|w x| for the fp32 paths, 1e-3
+for the bf16 prefill against the oracle's bf16 product).  QMM_FUZZ_SEED
+shifts every seed and QMM_FUZZ_CASES sets the number of cases, for longer
+runs than the default 12 cases of seed 0."""
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import pytest
@@ -20,23 +24,24 @@ torch = pytest.importorskip("torch")
 q = pytest.importorskip("quantized_gguf_dequant_gb300")
 
 NT = max(1, oracle.max_threads())
-CASES = 12
+CASES = int(os.environ.get("QMM_FUZZ_CASES", "12"))
+SHIFT = 100000 * int(os.environ.get("QMM_FUZZ_SEED", "0"))
 
 
 def _rng(case, salt):
-    return np.random.default_rng(1000 * salt + case)
+    return np.random.default_rng(SHIFT + 1000 * salt + case)
 
 
 @pytest.mark.parametrize("case", range(CASES))
 def test_fuzz_gemv_and_batched(case):
     r = _rng(case, 1)
-    fmt = q.Q4_K if case % 3 else q.Q8_0
+    fmt = [q.Q4_K, q.Q8_0, q.Q4_K, q.Q5_K, q.Q6_K, q.IQ4_NL][int(r.integers(0, 6))]
     N = int(r.integers(1, 700))
     K = 256 * int(r.integers(1, 24))
     M = int(r.integers(1, 17))
-    w = synth.matrix(fmt, N, K, 50 + case)
+    w = synth.matrix(fmt, N, K, SHIFT + 50 + case)
     m = q.Matrix(fmt, N, K, to_dev(w))
-    X = synth.activations(M, K, 60 + case)
+    X = synth.activations(M, K, SHIFT + 60 + case)
     Y = m.gemv_batched(to_dev(X)).cpu().numpy()
     y1 = m.gemv(to_dev(X[0])).cpu().numpy()
     Yr, C = oracle.gemv(fmt, w, N, K, X, nthreads=NT)
@@ -49,17 +54,18 @@ def test_fuzz_gemv_and_batched(case):
 @pytest.mark.parametrize("case", range(CASES))
 def test_fuzz_gemm(case):
     r = _rng(case, 2)
+    fmt = q.Q8_0 if r.integers(0, 3) == 0 else q.Q4_K
     N = int(r.integers(1, 900))
     K = 256 * int(r.integers(1, 12))
     M = int(r.integers(1, 600))
-    w = synth.q4k_matrix(N, K, 70 + case)
-    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
-    Xb = synth.activations_bf16(M, K, 80 + case)
+    w = synth.matrix(fmt, N, K, SHIFT + 70 + case)
+    m = q.Matrix(fmt, N, K, to_dev(w))
+    Xb = synth.activations_bf16(M, K, SHIFT + 80 + case)
     Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     m.gemm(to_dev(Xb.view(np.int16)), Y)
     torch.cuda.synchronize()
-    Yr, C = oracle.gemm_bf16(w, N, K, Xb, nthreads=NT)
-    assert_close_to_oracle(Y.cpu().numpy(), Yr, C, 1e-3, f"gemm N={N} K={K} M={M}")
+    Yr, C = oracle.gemm_bf16(w, N, K, Xb, nthreads=NT, fmt=fmt)
+    assert_close_to_oracle(Y.cpu().numpy(), Yr, C, 1e-3, f"gemm fmt={fmt} N={N} K={K} M={M}")
     assert m.status() == 0
     m.close()
 
@@ -67,6 +73,7 @@ def test_fuzz_gemm(case):
 @pytest.mark.parametrize("case", range(CASES))
 def test_fuzz_moe(case):
     r = _rng(case, 3)
+    fmt = q.Q8_0 if r.integers(0, 3) == 0 else q.Q4_K
     E = int(r.integers(1, 24))
     Ne = int(r.integers(1, 200))
     K = 256 * int(r.integers(1, 6))
@@ -74,16 +81,16 @@ def test_fuzz_moe(case):
     top_k = int(r.integers(1, min(E, 8) + 1))
     xps = bool(case % 2)
     routed = case % 3 != 0
-    w = synth.q4k_matrix(E * Ne, K, 90 + case)
-    m = q.Matrix(q.Q4_K, E * Ne, K, to_dev(w))
-    ids, rw = synth.router(T, E, top_k, 91 + case)
-    X = synth.activations(T * top_k if xps else T, K, 92 + case)
+    w = synth.matrix(fmt, E * Ne, K, SHIFT + 90 + case)
+    m = q.Matrix(fmt, E * Ne, K, to_dev(w))
+    ids, rw = synth.router(T, E, top_k, SHIFT + 91 + case)
+    X = synth.activations(T * top_k if xps else T, K, SHIFT + 92 + case)
     rows = T if routed else T * top_k
     Y = torch.full((rows, Ne), float("nan"), dtype=torch.float32, device="cuda")
     q.moe_gemv(m.h, E, to_dev(ids), T, top_k, to_dev(X), xps, to_dev(rw) if routed else None, Y)
     torch.cuda.synchronize()
-    Yr, C = oracle.moe_gemv(q.Q4_K, w, E, Ne, K, ids, X, xps, rw if routed else None, nthreads=NT)
+    Yr, C = oracle.moe_gemv(fmt, w, E, Ne, K, ids, X, xps, rw if routed else None, nthreads=NT)
     assert_close_to_oracle(Y.cpu().numpy(), Yr, C, TOL_FP32,
-                           f"moe E={E} Ne={Ne} K={K} T={T} k={top_k} xps={xps} routed={routed}")
+                           f"moe fmt={fmt} E={E} Ne={Ne} K={K} T={T} k={top_k} xps={xps} routed={routed}")
     assert m.status() == 0
     m.close()
