@@ -94,3 +94,59 @@ def test_fuzz_moe(case):
                            f"moe fmt={fmt} E={E} Ne={Ne} K={K} T={T} k={top_k} xps={xps} routed={routed}")
     assert m.status() == 0
     m.close()
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_ffn_decode(case):
+    """qmm_ffn_decode on random widths and formats (the decode kernel's fused
+    gate/up pairs, or the grouped route where they do not fit), against the
+    oracle composition with the GEMV bound carried through SwiGLU."""
+    r = _rng(case, 4)
+    fmt = [q.Q4_K, q.Q8_0, q.Q5_K, q.Q6_K, q.IQ4_NL][int(r.integers(0, 5))]
+    d_model = 256 * int(r.integers(1, 20))
+    d_ff = 256 * int(r.integers(1, 30))
+    wg = synth.matrix(fmt, d_ff, d_model, SHIFT + 110 + case)
+    wu = synth.matrix(fmt, d_ff, d_model, SHIFT + 111 + case)
+    wd = synth.matrix(fmt, d_model, d_ff, SHIFT + 112 + case)
+    x = synth.activations(1, d_model, SHIFT + 113 + case)[0]
+    hs = [q.Matrix(fmt, d_ff, d_model, to_dev(wg)), q.Matrix(fmt, d_ff, d_model, to_dev(wu)),
+          q.Matrix(fmt, d_model, d_ff, to_dev(wd))]
+    h = torch.full((d_ff,), float("nan"), dtype=torch.float32, device="cuda")
+    y = torch.full((d_model,), float("nan"), dtype=torch.float32, device="cuda")
+    q.ffn_decode(hs[0].h, hs[1].h, hs[2].h, to_dev(x), h, y)
+    torch.cuda.synchronize()
+    g, cg = oracle.gemv(fmt, wg, d_ff, d_model, x[None], nthreads=NT)
+    u, cu = oracle.gemv(fmt, wu, d_ff, d_model, x[None], nthreads=NT)
+    h_ref = oracle.swiglu(g[0], u[0])
+    sg = oracle.swiglu(g[0], np.ones_like(g[0]))
+    a = np.abs(h_ref) + 1.1 * np.abs(u[0]) * cg[0] + np.abs(sg) * cu[0]
+    what = f"ffn fmt={fmt} d_model={d_model} d_ff={d_ff}"
+    assert_close_to_oracle(h.cpu().numpy(), h_ref, a * 1.0001, TOL_FP32, what + " h")
+    y_ref, _ = oracle.gemv(fmt, wd, d_model, d_ff, h_ref.astype(np.float32)[None], nthreads=NT)
+    _, cd = oracle.gemv(fmt, wd, d_model, d_ff, a.astype(np.float32)[None], nthreads=NT)
+    assert_close_to_oracle(y.cpu().numpy(), y_ref[0], cd[0] * 1.0001, TOL_FP32, what + " y")
+    for m in hs:
+        assert m.status() == 0
+        m.close()
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_gemv_group(case):
+    """qmm_gemv_group: one to four matrices of random, ragged row counts that
+    share x, in one format, each against the oracle."""
+    r = _rng(case, 5)
+    fmt = [q.Q4_K, q.Q8_0, q.Q5_K, q.Q6_K, q.IQ4_NL][int(r.integers(0, 5))]
+    K = 256 * int(r.integers(1, 40))
+    Ns = [int(r.integers(1, 1500)) for _ in range(int(r.integers(1, 5)))]
+    ws = [synth.matrix(fmt, N, K, SHIFT + 120 + 10 * case + i) for i, N in enumerate(Ns)]
+    ms = [q.Matrix(fmt, N, K, to_dev(w)) for N, w in zip(Ns, ws)]
+    x = synth.activations(1, K, SHIFT + 121 + case)[0]
+    ys = [torch.full((N,), float("nan"), dtype=torch.float32, device="cuda") for N in Ns]
+    q.gemv_group([m.h for m in ms], to_dev(x), ys)
+    torch.cuda.synchronize()
+    for i, (N, w, y) in enumerate(zip(Ns, ws, ys)):
+        yr, c = oracle.gemv(fmt, w, N, K, x, nthreads=NT)
+        assert_close_to_oracle(y.cpu().numpy(), yr, c, TOL_FP32, f"group {i} fmt={fmt} N={Ns} K={K}")
+    for m in ms:
+        assert m.status() == 0
+        m.close()
