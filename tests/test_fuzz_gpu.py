@@ -150,3 +150,33 @@ def test_fuzz_gemv_group(case):
     for m in ms:
         assert m.status() == 0
         m.close()
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_gemv_q8k(case):
+    """The opt-in integer-dot GEMV on random shapes: the quantizer's bytes
+    equal the oracle's, the GEMV is within 1e-5 of sum|w xhat| of the
+    oracle's integer-dot GEMV, and the variant that quantizes inside the
+    launch gives the same bits."""
+    r = _rng(case, 6)
+    N = int(r.integers(1, 3000))
+    K = 256 * int(r.integers(1, 60))
+    w = synth.q4k_matrix(N, K, SHIFT + 130 + case)
+    x = synth.activations(1, K, SHIFT + 131 + case)[0]
+    xq_ref = oracle.quantize_q8_k(x)
+    xq = torch.full((K // 256 * q.Q8_K_BLOCK,), 0xAB, dtype=torch.uint8, device="cuda")
+    q.quantize_q8_k(to_dev(x), K, xq)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), np.asarray(xq_ref, dtype=np.uint8))
+    m = q.Matrix(q.Q4_K, N, K, to_dev(w))
+    y = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_q8k(m.h, xq, y)
+    yf = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    q.gemv_q8k_fused(m.h, to_dev(x), yf)
+    torch.cuda.synchronize()
+    y_ref, c = oracle.gemv_q8k(q.Q4_K, w, N, K, xq_ref, nthreads=NT)
+    got = y.cpu().numpy()
+    assert_close_to_oracle(got, y_ref, c, 1e-5, f"q8k N={N} K={K}")
+    assert np.array_equal(got.view(np.int32), yf.cpu().numpy().view(np.int32))
+    assert m.status() == 0
+    m.close()
