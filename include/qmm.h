@@ -107,7 +107,12 @@ typedef void *qmm_stream; /* cudaStream_t */
  * copied).  Requires: fmt one of Q4_K, Q8_0, Q5_K, Q6_K, IQ4_NL; N >= 1;
  * K % 256 == 0 for the K-quants, K % 32 == 0 for Q8_0 and IQ4_NL;
  * K <= 2^20; w_dev 16-byte aligned.  Allocates the handle's workspace and
- * status word on the current device.  On success *out is a new handle. */
+ * status word on the current device.  On success *out is a new handle.
+ * The bytes at w_dev must be fully written before the first call on the
+ * handle is enqueued and stay unchanged while calls on it may run: the
+ * kernels start fetching weights while earlier work in the stream is still
+ * finishing (programmatic dependent launch), so a kernel that writes them
+ * must have completed first (synchronise after loading the weights). */
 QMM_API qmm_status qmm_create(qmm_format fmt, int64_t N, int64_t K, const void *w_dev,
                       qmm_t *out);
 

@@ -283,8 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    pdl_wait();  // X belongs to earlier kernels until here, Y too
-
+    // X, Y and the split-K scratch belong to earlier kernels until their
+    // dependency wait: the producer waits before its first X copy and the
+    // epilogue before its first store.  The weights are the handle's, fixed
+    // before any call, so their ring fills (and the dequant warps start)
+    // while the previous kernel drains; the MMA and dequant warps touch only
+    // shared and tensor memory.
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
@@ -312,6 +316,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
             seek(cx, blockIdx.x);
             seek(cr, blockIdx.x);
             int ix = 0, ir = 0, hit = 0;  // stages / super-blocks issued per stream
+            // Is the raw slot of stage ir (and, at a super-block's first
+            // chunk, a header slot) free?
+            auto raw_free = [&]() {
+                const int s = ir % NR, c = cr.ks & 3;
+                const bool with_hdr = FMT == QMM_Q4_K && c == 0;
+                const int h = hit % kHS;
+                return (ir < NR || mbar_test_wait(&rempty[s], unsigned(ir / NR - 1) & 1u)) &&
+                       (!with_hdr || hit < kHS ||
+                        mbar_test_wait(&hempty[h], unsigned(hit / kHS - 1) & 1u));
+            };
+            auto issue_raw = [&]() {
+                const int s = ir % NR, sb = cr.ks >> 2, c = cr.ks & 3;
+                if (FMT == QMM_Q4_K && c == 0) {
+                    const int h = hit % kHS;
+                    mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
+                    tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr[cr.mi], sb * 144, cr.row0, &hfull[h]);
+                    ++hit;
+                }
+                // Q8_0: the chunk's blocks sit at 272 sb + 68 c of the row
+                const int xoff = FMT == QMM_Q8_0 ? 272 * sb + ((68 * c) & ~15) : sb * 144 + 16 + 32 * c;
+                mbar_arrive_expect_tx(&rfull[s], kRaw);
+                tma_2d(sRaw + s * kRaw, &P.tm_nib[cr.mi], xoff, cr.row0, &rfull[s]);
+                ++ir;
+                step(cr);
+            };
+            // The weights first: the raw ring's free slots before the wait.
+            while (cr.un < P.units && ir < NR && raw_free())
+                issue_raw();
+            pdl_wait();
             long long idle0 = clock64();
             while (!abort_flag && (cx.un < P.units || cr.un < P.units)) {
                 bool moved = false;
@@ -328,27 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
                 }
                 // Raw bytes of stage ir (and, at a super-block's first chunk,
                 // its headers), once the dequant warps hold the previous ones.
-                if (cr.un < P.units) {
-                    const int s = ir % NR, sb = cr.ks >> 2, c = cr.ks & 3;
-                    const bool with_hdr = FMT == QMM_Q4_K && c == 0;
-                    const int h = hit % kHS;
-                    if ((ir < NR || mbar_test_wait(&rempty[s], unsigned(ir / NR - 1) & 1u)) &&
-                        (!with_hdr || hit < kHS ||
-                         mbar_test_wait(&hempty[h], unsigned(hit / kHS - 1) & 1u))) {
-                        if (with_hdr) {
-                            mbar_arrive_expect_tx(&hfull[h], kHdrBytes);
-                            tma_2d(sHdr + h * kHdrBytes, &P.tm_hdr[cr.mi], sb * 144, cr.row0, &hfull[h]);
-                            ++hit;
-                        }
-                        // Q8_0: the chunk's blocks sit at 272 sb + 68 c of the row
-                        const int xoff = FMT == QMM_Q8_0 ? 272 * sb + ((68 * c) & ~15) : sb * 144 + 16 + 32 * c;
-                        mbar_arrive_expect_tx(&rfull[s], kRaw);
-                        tma_2d(sRaw + s * kRaw, &P.tm_nib[cr.mi], xoff, cr.row0, &rfull[s]);
-                        ++ir;
-                        step(cr);
-                        moved = true;
-                    }
-                }
+                if (cr.un < P.units && raw_free())
+                    issue_raw(), moved = true;
                 if (moved) {
                     idle0 = clock64();
                 } else if (clock64() - idle0 > kWaitBudgetCycles) {
@@ -415,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_q4k_kernel(const __grid_cons
         // last chunk is in registers; the stores complete in the background.
         // Chunks a store cannot take (Y not 16-byte aligned, a partial
         // 32-column piece) are written by the threads themselves.
+        pdl_wait();  // Y and the partials belong to earlier kernels until here
         const int quarter = warp & 3;
         const int eh = (warp - kEpiWarp0) >> 2;  // 256-token tiles: token half; 128: column half
         const int tok_in_tile = (C::kHalves == 2 ? eh * 128 : 0) + quarter * 32 + lane;
