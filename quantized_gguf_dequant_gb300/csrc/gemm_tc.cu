@@ -684,20 +684,17 @@ __global__ void splitk_reduce_kernel(const __grid_constant__ ReduceParams R)
         const int64_t e = int64_t(tok) * R.Ntot + R.col_off[mi] + row;
         float *dst = R.y[mi] + int64_t(tok) * R.n_rows[mi] + row;
         if (R.vec && row + 4 <= R.n_rows[mi]) {
-            float4 v[kMaxKSplit];
-#pragma unroll
-            for (int k = 0; k < kMaxKSplit; ++k)
-                if (k < R.ks)
-                    v[k] = __ldcs(reinterpret_cast<const float4 *>(R.ws + k * plane + e));
-            float4 acc = v[0];
-#pragma unroll
-            for (int k = 1; k < kMaxKSplit; ++k)
-                if (k < R.ks) {
-                    acc.x += v[k].x;
-                    acc.y += v[k].y;
-                    acc.z += v[k].z;
-                    acc.w += v[k].w;
-                }
+            // slice order; the running sum keeps the registers (and so the
+            // occupancy that hides the loads' latency) low
+            float4 acc = __ldcs(reinterpret_cast<const float4 *>(R.ws + e));
+#pragma unroll 4
+            for (int k = 1; k < R.ks; ++k) {
+                const float4 v = __ldcs(reinterpret_cast<const float4 *>(R.ws + k * plane + e));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
             *reinterpret_cast<float4 *>(dst) = acc;
         } else {
             for (int c = 0; c < 4 && row + c < R.n_rows[mi]; ++c) {
